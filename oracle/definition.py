@@ -1,0 +1,68 @@
+"""Definition form of kernelised attention, fp64 numpy (test infrastructure only).
+
+Written from "Transformers are RNNs" (Chinese translation, "線性變換器"):
+
+* sec. 3.1 eq. (3): V'_i = sum_j sim(Q_i, K_j) V_j / sum_j sim(Q_i, K_j);
+* sec. 3.2 eq. (4): sim(q, k) = phi(q)^T phi(k), phi applied row-wise;
+* sec. 3.2.1 eq. (7): phi(x) = elu(x) + 1 (alpha = 1);
+* sec. 3.3 eq. (8): the causal form sums over j <= i only.
+
+This is the O(N^2) quadratic form the linear method avoids.  The matrix of
+similarities is formed explicitly with one matmul; there is no regrouping.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+def phi_np(x: np.ndarray) -> np.ndarray:
+    """elu(x) + 1 in fp64: x + 1 for x > 0, exp(x) for x <= 0."""
+    x = np.asarray(x, dtype=np.float64)
+    return np.where(x > 0.0, x + 1.0, np.exp(np.minimum(x, 0.0)))
+
+
+def _as64(a) -> np.ndarray:
+    if hasattr(a, "detach"):
+        a = a.detach().to("cpu").float().numpy()
+    return np.asarray(a, dtype=np.float64)
+
+
+def definition_noncausal(q, k, v) -> np.ndarray:
+    """eq. (3)/(4) over all j.  q, k: [..., N, D]; v: [..., N, M]."""
+    q, k, v = _as64(q), _as64(k), _as64(v)
+    w = phi_np(q) @ np.swapaxes(phi_np(k), -1, -2)          # sim(Q_i, K_j), [..., N, N]
+    return (w @ v) / w.sum(axis=-1, keepdims=True)
+
+
+def definition_causal(q, k, v) -> np.ndarray:
+    """eq. (8) with the similarity of eq. (4): sums over j <= i."""
+    q, k, v = _as64(q), _as64(k), _as64(v)
+    N = q.shape[-2]
+    w = phi_np(q) @ np.swapaxes(phi_np(k), -1, -2)
+    w = w * np.tril(np.ones((N, N)))                           # keep j <= i
+    return (w @ v) / w.sum(axis=-1, keepdims=True)
+
+
+def definition_rows(q, k, v, rows, causal: bool, prefix_state=None) -> np.ndarray:
+    """eq. (3)/(8) for selected query rows only, for long sequences.
+
+    q, k: [N, D], v: [N, M] of ONE head; rows: 1-D int array of query indices.
+    Row i costs O(i * D) (causal) so sampled rows of a 64k sequence are cheap.
+    ``prefix_state`` = (S0, z0) adds the contribution of tokens before this
+    sequence (the state carried in): V'_i = (phi(q)^T S0 + sum ...) / (phi(q)^T z0 + sum ...).
+    """
+    q, k, v = _as64(q), _as64(k), _as64(v)
+    rows = np.asarray(rows, dtype=np.int64)
+    fq = phi_np(q[rows])                                        # [R, D]
+    out = np.empty((rows.size, v.shape[-1]), np.float64)
+    for r, i in enumerate(rows):
+        hi = i + 1 if causal else q.shape[0]
+        w = phi_np(k[:hi]) @ fq[r]                               # [hi]
+        num = w @ v[:hi]
+        den = w.sum()
+        if prefix_state is not None:
+            S0, z0 = prefix_state
+            num = num + fq[r] @ np.asarray(S0, np.float64)
+            den = den + fq[r] @ np.asarray(z0, np.float64)
+        out[r] = num / den
+    return out
