@@ -1,0 +1,522 @@
+"""Benchmark of the kernelised linear attention library on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0).  A step is one causal forward (phi feature map,
+intra-chunk masked products, inter-chunk state read-out, state carry, final
+state written out) over the training-shaped workload B=16, H=8, N=3072,
+D=M=64, bf16 inputs N(0,1)/sqrt(64), chunk 64: `value` is tokens/s (B*N per
+step) with inputs resident in HBM, L2 flushed between timed steps.  The same
+line carries the other legs of the metric as separate objects: decode
+steps/s with the state's HBM GB/s (B=256, H=16, D=M=64 after a 1024-token
+prefill), the non-causal forward (B=8, H=8, N=4096) and the long causal
+forward (B=1, H=16, N=65536, D=M=128).
+
+--impl reference times the fp64 CPU oracle (the only reference there is) on
+a bounded sample of the same workload.  Under torchrun each rank runs the
+same per-GPU workload on its own GPU (independent heads: weak scaling, no
+collective in the data path); timings are reduced with MAX over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+MAIN = "causal_b16h8n3072d64"
+METRIC = "causal linear-attn fwd tokens/s & % tensor roofline; decode steps/s & HBM GB/s"
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+
+def _env_int(name, default):
+    try:
+        return int(os.environ.get(name, default))
+    except ValueError:
+        return default
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "bf16_tflops_sustained": float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS,
+                "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during a region."""
+
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "20"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._reader = threading.Thread(target=self._read, daemon=True)
+            self._reader.start()
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, begin: bool):
+        if begin:
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = [l for (t, l) in self.lines if self.t0 is None or (self.t0 - 0.05 <= t <= (self.t1 or t) + 0.05)]
+        if not rows:
+            rows = [l for (_, l) in self.lines]
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in rows:
+            parts = [p.strip() for p in l.split(",")]
+            if len(parts) < 10:
+                continue
+            try:
+                sm.append(float(parts[2]))
+                smax.append(float(parts[3]))
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[6:10]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- helpers
+
+def _kernel_source_hash():
+    import glob
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "weight_recurrence_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _traffic(kernel_key):
+    """ncu DRAM bytes per launch recorded in profiles/traffic.json, if taken on this source."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            t = json.load(f)
+        e = t.get(kernel_key)
+        if e and e.get("source_sha") == _kernel_source_hash():
+            return e.get("dram_bytes_per_launch")
+    except (OSError, ValueError):
+        pass
+    return None
+
+
+class Flusher:
+    """Writes a buffer twice the size of L2 between timed steps."""
+
+    def __init__(self, torch, device):
+        l2 = getattr(torch.cuda.get_device_properties(device), "L2_cache_size", 128 << 20) or (128 << 20)
+        self.buf = torch.empty(2 * l2 // 4, dtype=torch.float32, device=device)
+
+    def __call__(self):
+        self.buf.fill_(1.0)
+
+
+def _timed_steps(torch, fn, steps, warmup, flush, stream):
+    """Per-step CUDA-event times (ms) on `stream`, L2 flushed before each step."""
+    for _ in range(warmup):
+        flush()
+        fn()
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in evs:
+        flush()
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def _alg_bytes_fwd(w):
+    """Algorithmic bytes of one forward: read Q, K, V once, write O once."""
+    el = 2 if str(w.dtype).endswith("bfloat16") else 4
+    return w.B * w.H * w.N * (2 * w.D + 2 * w.M) * el
+
+
+def _alg_flops_fwd(w):
+    """4*D*M flops per head-token: state update (2DM) + read-out (2DM)."""
+    return 4.0 * w.D * w.M * w.B * w.H * w.N
+
+
+def _exec_flops_causal(w, chunk):
+    """Flops the chunked kernel executes: intra-chunk 2C(D+M) + inter 2DM + update 2DM per head-token."""
+    return (2.0 * chunk * (w.D + w.M) + 4.0 * w.D * w.M) * w.B * w.H * w.N
+
+
+# -------------------------------------------------------------- our arm
+
+def run_ours(args, rank, world, dist):
+    import torch
+
+    from weight_recurrence_gb300 import build as labuild
+    from weight_recurrence_gb300 import inputs, la
+
+    labuild.build()
+    local = _env_int("LOCAL_RANK", 0)
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream(dev)
+    pk = peaks()
+    flush = Flusher(torch, dev)
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+
+    def max_over_ranks(x):
+        if dist is None:
+            return x
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    # ---------------------------------------------------- main: causal cfg
+    w = inputs.WORKLOADS[MAIN]
+    q, k, v = [t.to(dev) for t in inputs.workload_inputs(w)]
+    S = torch.zeros(w.B, w.H, w.D, w.M, device=dev)
+    z = torch.zeros(w.B, w.H, w.D, device=dev)
+    out = torch.empty(w.B, w.H, w.N, w.M, dtype=w.dtype, device=dev)
+
+    # Each step continues from the state the previous one left (S, z in/out),
+    # exactly as consecutive segments of one long sequence would.
+    def step():
+        la.la_forward_causal(q, k, v, out=out, chunk=w.chunk, S=S, z=z, stream=stream)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    for _ in range(args.warmup):
+        flush()
+        step()
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    l0 = la.la_launch_count()
+    sampler.mark(True)
+    t_wall0 = time.perf_counter()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for a, b in evs:
+        flush()
+        a.record(stream)
+        step()
+        b.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.perf_counter()
+    sampler.mark(False)
+    barrier()
+    torch.cuda.synchronize()
+    launches = la.la_launch_count() - l0
+    times = [a.elapsed_time(b) for a, b in evs]
+    assert la.la_get_last_error() == la.LA_OK
+    ms_local = sum(times) / len(times)
+    ms = max_over_ranks(ms_local)
+    clocks = sampler.stop()
+    tokens_per_step = w.B * w.N
+    value = world * tokens_per_step / (ms / 1e3)
+    launches_per_call = launches / max(1, args.steps)
+    bytes_step = _alg_bytes_fwd(w)
+    achieved_gbs = bytes_step / (ms / 1e3) / 1e9
+    chunk_exec = w.chunk if w.chunk else 128
+    roofline = {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved_gbs / pk["hbm_gbs"], 4), "traffic": _traffic("causal_" + MAIN),
+                "peak_source": pk["source"], "alg_bytes_per_launch": bytes_step,
+                "launches_per_step": launches_per_call}
+    tensor = {"alg_tflops": round(_alg_flops_fwd(w) / (ms / 1e3) / 1e12, 2),
+              "exec_tflops": round(_exec_flops_causal(w, chunk_exec) / (ms / 1e3) / 1e12, 2),
+              "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+              "frac_alg": round(_alg_flops_fwd(w) / (ms / 1e3) / 1e12 / pk["bf16_tflops"], 4),
+              "frac_exec": round(_exec_flops_causal(w, chunk_exec) / (ms / 1e3) / 1e12 / pk["bf16_tflops"], 4),
+              "note": "at D=M=64 the causal forward is HBM-bound (32 flop/B algorithmic vs ~287 flop/B "
+                      "machine balance); the HBM fraction is the governing roofline"}
+
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1)/sqrt(D) bf16; no dataset)",
+        "config": {"workload": MAIN, "B": w.B, "H": w.H, "N": w.N, "D": w.D, "M": w.M,
+                   "chunk": w.chunk, "global_batch": w.B * world, "seq_len": w.N,
+                   "parallelism": "dp%d (independent heads per rank)" % world,
+                   "l2": "flushed between timed steps (2x L2 write)"},
+        "roofline": roofline, "tensor": tensor, "clocks": clocks, "gpu_launches": launches,
+        "wall_s_timed_region": round(t_wall1 - t_wall0, 4),
+    }
+
+    # ---------------------------------------------- e2e: host buffers
+    if not args.no_e2e:
+        qh = q.cpu().pin_memory()
+        kh = k.cpu().pin_memory()
+        vh = v.cpu().pin_memory()
+        oh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+        qd, kd, vd = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+
+        def e2e_step():
+            qd.copy_(qh, non_blocking=True)
+            kd.copy_(kh, non_blocking=True)
+            vd.copy_(vh, non_blocking=True)
+            la.la_forward_causal(qd, kd, vd, out=out, chunk=w.chunk, S=S, z=z, stream=stream)
+            oh.copy_(out, non_blocking=True)
+
+        n_e2e = max(3, min(args.steps, 20))
+        et = _timed_steps(torch, e2e_step, n_e2e, 2, flush, stream)
+        e_ms = max_over_ranks(sum(et) / len(et))
+        nb = q.numel() * q.element_size()
+        result["e2e"] = {"value": round(world * tokens_per_step / (e_ms / 1e3), 1), "unit": "tokens/s",
+                         "h2d_bytes_per_step": 3 * nb, "d2h_bytes_per_step": out.numel() * out.element_size(),
+                         "ms_per_step": round(e_ms, 4), "steps": n_e2e,
+                         "path": "pinned host -> device copies, la_forward_causal, device -> pinned host"}
+    del q, k, v, out
+
+    # ------------------------------------------------- secondary legs
+    if not args.main_only:
+        result["legs"] = {}
+        result["legs"]["noncausal"] = _leg_fwd(torch, la, inputs, "noncausal_b8h8n4096d64", dev, stream,
+                                               flush, pk, 30, max_over_ranks, world)
+        result["legs"]["long_causal"] = _leg_fwd(torch, la, inputs, "causal_b1h16n65536d128", dev, stream,
+                                                 flush, pk, 5, max_over_ranks, world)
+        result["legs"]["decode"] = _leg_decode(torch, la, inputs, dev, stream, flush, pk, args,
+                                               max_over_ranks, world)
+
+    # ------------------------------------------------- CPU baseline (rank 0)
+    if rank == 0 and not args.no_cpu:
+        result["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_seconds)
+    return result
+
+
+def _leg_fwd(torch, la, inputs, name, dev, stream, flush, pk, steps, max_over_ranks, world):
+    w = inputs.WORKLOADS[name]
+    q, k, v = [t.to(dev) for t in inputs.workload_inputs(w)]
+    out = torch.empty(w.B, w.H, w.N, w.M, dtype=w.dtype, device=dev)
+    if w.op == "causal":
+        fn = lambda: la.la_forward_causal(q, k, v, out=out, chunk=w.chunk, stream=stream)  # noqa: E731
+    else:
+        fn = lambda: la.la_forward_noncausal(q, k, v, out=out, stream=stream)  # noqa: E731
+    l0 = la.la_launch_count()
+    t = _timed_steps(torch, fn, steps, 3, flush, stream)
+    launches = (la.la_launch_count() - l0) // (steps + 3)
+    ms = max_over_ranks(sum(t) / len(t))
+    gbs = _alg_bytes_fwd(w) / (ms / 1e3) / 1e9
+    leg = {"workload": name, "op": w.op, "value": round(world * w.B * w.N / (ms / 1e3), 1), "unit": "tokens/s",
+           "ms_per_step": round(ms, 5), "steps": steps, "launches_per_step": launches,
+           "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                        "frac": round(gbs / pk["hbm_gbs"], 4), "traffic": _traffic(w.op + "_" + name)},
+           "alg_tflops": round(_alg_flops_fwd(w) / (ms / 1e3) / 1e12, 2)}
+    del q, k, v, out
+    torch.cuda.empty_cache()
+    return leg
+
+
+def _leg_decode(torch, la, inputs, dev, stream, flush, pk, args, max_over_ranks, world):
+    w = inputs.WORKLOADS["decode_b256h16d64"]
+    B, H, D, M = w.B, w.H, w.D, w.M
+    # prefill the state with 1024 random tokens through the causal forward
+    qp, kp, vp = [t.to(dev) for t in inputs.qkv(B, H, w.N, D, M, w.dtype, w.scale, seed=w.seed)]
+    S = torch.zeros(B, H, D, M, device=dev)
+    z = torch.zeros(B, H, D, device=dev)
+    la.la_forward_causal(qp, kp, vp, S=S, z=z, want_out=False, stream=stream)
+    del qp, kp, vp
+    steps = w.steps
+    qs, ks, vs = inputs.decode_tokens(steps, B, H, D, M, w.dtype, seed=w.seed + 1000, device=dev)
+    y = torch.empty(B, H, M, dtype=w.dtype, device=dev)
+    n_flush = min(args.decode_steps, steps)
+    t_idx = [0]
+
+    def one():
+        i = t_idx[0] % steps
+        la.la_decode_step(qs[i], ks[i], vs[i], S, z, y=y, stream=stream)
+        t_idx[0] += 1
+
+    times = _timed_steps(torch, one, n_flush, 3, flush, stream)
+    ms = max_over_ranks(sum(times) / len(times))
+    bytes_step = B * H * (2 * D * M * 4 + 2 * D * 4 + (2 * D + 2 * M) * 2)
+    gbs = bytes_step / (ms / 1e3) / 1e9
+    leg = {"workload": "decode_b256h16d64", "value": round(world / (ms / 1e3), 1), "unit": "steps/s",
+           "ms_per_step": round(ms, 5), "steps": n_flush, "prefill_tokens": w.N,
+           "hbm_gbs": round(gbs, 1),
+           "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                        "frac": round(gbs / pk["hbm_gbs"], 4), "traffic": _traffic("decode_decode_b256h16d64"),
+                        "alg_bytes_per_launch": bytes_step},
+           "l2": "flushed before every timed step (state read from HBM)"}
+    # all 4096 sequential steps captured in a CUDA graph, no flush: the 65 MiB state stays in L2
+    if not args.no_graph:
+        try:
+            g = torch.cuda.CUDAGraph()
+            s2 = torch.cuda.Stream(dev)
+            s2.wait_stream(stream)
+            with torch.cuda.stream(s2):
+                la.la_decode_step(qs[0], ks[0], vs[0], S, z, y=y, stream=s2)
+                torch.cuda.synchronize()
+                with torch.cuda.graph(g, stream=s2):
+                    for i in range(steps):
+                        la.la_decode_step(qs[i], ks[i], vs[i], S, z, y=y, stream=s2)
+            stream.wait_stream(s2)
+            g.replay()
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            torch.cuda.synchronize()
+            gms = max_over_ranks(a.elapsed_time(b))
+            leg["graph_4096"] = {"steps_per_s": round(world * steps / (gms / 1e3), 1),
+                                 "ms_total": round(gms, 3), "effective_gbs": round(bytes_step * steps / (gms / 1e3) / 1e9, 1),
+                                 "l2": "not flushed: the state is L2-resident between steps; not an HBM figure"}
+            del g
+        except Exception as e:  # report, do not hide
+            leg["graph_4096"] = {"error": repr(e)}
+    del qs, ks, vs, S, z, y
+    torch.cuda.empty_cache()
+    return leg
+
+
+# ------------------------------------------------------------ CPU oracle
+
+def cpu_baseline(w, budget_s=4.0):
+    """The fp64 recurrence oracle on the host cores, on a bounded sample of heads."""
+    import oracle
+    from weight_recurrence_gb300 import inputs
+
+    oracle.build()
+    nthreads = oracle.max_threads()
+    heads = max(1, min(w.B * w.H, 2 * nthreads))
+    q, k, v = inputs.workload_inputs(w)
+    qs = q.reshape(-1, w.N, w.D)[:heads].contiguous()
+    ks = k.reshape(-1, w.N, w.D)[:heads].contiguous()
+    vs = v.reshape(-1, w.N, w.M)[:heads].contiguous()
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        oracle.causal(qs, ks, vs, nthreads=nthreads)
+        reps += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    dt = (time.perf_counter() - t0) / reps
+    head_tokens_per_s = heads * w.N / dt
+    return {"value": round(head_tokens_per_s / w.H, 1), "unit": "tokens/s", "cores": nthreads, "kind": "oracle",
+            "sample": "%d of %d heads x N=%d (fp64 recurrence, eqs. 10-12), %d reps; tokens/s = head-tokens/s / H"
+                      % (heads, w.B * w.H, w.N, reps)}
+
+
+def run_reference(args, rank, world):
+    """The reference arm: the fp64 oracle on host cores, one bounded sample per step."""
+    import oracle
+    from weight_recurrence_gb300 import inputs
+
+    oracle.build()
+    w = inputs.WORKLOADS[MAIN]
+    nthreads = oracle.max_threads()
+    heads = max(1, min(w.B * w.H, nthreads))
+    q, k, v = inputs.workload_inputs(w)
+    qs = q.reshape(-1, w.N, w.D)[:heads].contiguous()
+    ks = k.reshape(-1, w.N, w.D)[:heads].contiguous()
+    vs = v.reshape(-1, w.N, w.M)[:heads].contiguous()
+    for _ in range(args.warmup):
+        oracle.causal(qs, ks, vs, nthreads=nthreads)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.causal(qs, ks, vs, nthreads=nthreads)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = heads * w.N / dt / w.H
+    sample = "%d of %d heads x N=%d per step (fp64 recurrence oracle); tokens/s = head-tokens/s / H" % (
+        heads, w.B * w.H, w.N)
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded N(0,1)/sqrt(D) bf16 widened to f64)",
+            "config": {"workload": MAIN, "B": w.B, "H": w.H, "N": w.N, "D": w.D, "M": w.M, "chunk": w.chunk},
+            "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": nthreads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--decode-steps", type=int, default=256, help="flushed decode steps to time")
+    ap.add_argument("--cpu-seconds", type=float, default=4.0)
+    ap.add_argument("--main-only", action="store_true", help="skip the non-causal, long and decode legs")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--no-graph", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+
+    world = _env_int("WORLD_SIZE", 1)
+    rank = _env_int("RANK", 0)
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return 0
+
+    dist = None
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(_env_int("LOCAL_RANK", 0))
+        tdist.init_process_group("nccl")
+        dist = tdist
+    res = run_ours(args, rank, world, dist)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

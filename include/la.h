@@ -1,0 +1,154 @@
+/*
+ * la.h - C ABI of a GB300 (sm_103a) library for kernelised linear attention
+ * with the feature map phi(x) = elu(x) + 1.
+ *
+ * Method: "Transformers are RNNs: Fast Autoregressive Transformers with Linear
+ * Attention" (Katharopoulos et al.), read in its Chinese translation (page
+ * title "線性變換器").  Per head, with Q, K in R^{N x D} and V in R^{N x M}
+ * (sec. 3.1 and 3.2.1 notation; rows are positions):
+ *
+ *   phi(x)       = x + 1 (x > 0), exp(x) (x <= 0)            sec. 3.2.1 eq. (7)
+ *   non-causal   V'_i = phi(Q_i)^T (sum_j phi(K_j) V_j^T)
+ *                       / phi(Q_i)^T (sum_j phi(K_j))          sec. 3.2 eq. (5)
+ *   causal       the same sums over j <= i:                   sec. 3.3 eq. (9)
+ *                S_i = S_{i-1} + phi(K_i) V_i^T,  Z_i = Z_{i-1} + phi(K_i),
+ *                V'_i = phi(Q_i)^T S_i / phi(Q_i)^T Z_i        eqs. (10)-(12)
+ *   decode       one step of eqs. (18)-(20): update s, z, then read out
+ *                (the layer's f_l and residual are not part of this library).
+ *
+ * There is no epsilon in any denominator and no 1/sqrt(D) inside phi: phi > 0,
+ * so every denominator is a sum of positive terms.
+ *
+ * Conventions for every entry point
+ * ---------------------------------
+ * Layout:    contiguous row-major.  Q, K: [B, H, N, D]; V, out: [B, H, N, M];
+ *            state S: [B, H, D, M] fp32 (S[d][m] = sum phi(K)_d V_m);
+ *            z: [B, H, D] fp32.  Decode q, k: [B, H, D]; v, y: [B, H, M].
+ * Types:     Q, K, V and out share one dtype (LA_DTYPE_F32 or LA_DTYPE_BF16);
+ *            all arithmetic is fp32 (bf16 operands on tensor cores accumulate
+ *            in fp32); the state is always fp32; bf16 results are rounded to
+ *            nearest-even once.
+ * Sizes:     D, M in {16, 32, 64, 128}; B, H, N >= 0.  An empty problem
+ *            (B*H*N == 0) is valid and launches nothing.
+ * Pointers:  device pointers (or pointers the GPU can dereference), 16-byte
+ *            aligned.  The caller owns every buffer, the workspace and the
+ *            stream; the library allocates no device memory and keeps no
+ *            state besides cached device properties and a per-device error
+ *            word.  Inputs are read-only; out must not alias an input.
+ * Stream:    a cudaStream_t (NULL = legacy default stream).  Work is enqueued
+ *            asynchronously; the call returns once it is enqueued.
+ * Errors:    argument checks happen on the host before any launch and return
+ *            LA_ERR_INVALID_ARG (bad pointer, alignment, negative size,
+ *            workspace too small) or LA_ERR_UNSUPPORTED (D or M outside the
+ *            supported set).  A failed launch returns LA_ERR_CUDA.  A kernel
+ *            that gives up waiting (every wait in the library is bounded)
+ *            records LA_ERR_TIMEOUT in the device error word, which
+ *            la_get_last_error() reports.
+ */
+#ifndef LA_H
+#define LA_H
+
+#include <stddef.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *la_stream_t;
+
+typedef enum {
+    LA_OK = 0,
+    LA_ERR_INVALID_ARG = 1,
+    LA_ERR_UNSUPPORTED = 2,
+    LA_ERR_CUDA = 3,
+    LA_ERR_TIMEOUT = 4
+} la_status;
+
+typedef enum { LA_DTYPE_F32 = 0, LA_DTYPE_BF16 = 1 } la_dtype;
+
+typedef enum { LA_OP_NONCAUSAL = 0, LA_OP_CAUSAL = 1, LA_OP_DECODE = 2 } la_op;
+
+typedef struct {
+    int B, H, N, D, M;
+    la_dtype dtype;
+} la_shape;
+
+/*
+ * Bytes of device workspace the call `op` needs for shape `s` and chunk
+ * length `chunk` (0 = default).  0 means the call needs none and accepts a
+ * NULL workspace.  Returns (size_t)-1 for an invalid shape.
+ */
+size_t la_workspace_bytes(la_op op, la_shape s, int chunk);
+
+/*
+ * Non-causal attention, sec. 3.2 eq. (5): the summaries sum_j phi(K_j) V_j^T
+ * (D x M) and sum_j phi(K_j) (D) are reduced once per head over all N keys in
+ * fp32, then every query row reads them out.
+ *   q, k: [B,H,N,D]; v: [B,H,N,M]; out: [B,H,N,M] (same dtype as q).
+ *   workspace: la_workspace_bytes(LA_OP_NONCAUSAL, s, 0) bytes, device memory.
+ */
+la_status la_forward_noncausal(const void *q, const void *k, const void *v, void *out,
+                               la_shape s, void *workspace, size_t ws_bytes,
+                               la_stream_t stream);
+
+/*
+ * Causal attention, sec. 3.3 eqs. (9)-(12), computed chunk by chunk: within a
+ * chunk of `chunk` rows the masked products phi(Q) phi(K)^T (j <= i, the
+ * diagonal kept) multiply V; the rows see earlier chunks through the carried
+ * fp32 state (S, z).  This regrouping of the sums of eq. (9) is exact in real
+ * arithmetic; results for different chunk lengths differ only by rounding.
+ *   out: [B,H,N,M] or NULL (state only, e.g. to prefill a decoder).
+ *   chunk: 0 (library default) or 64 or 128; the fp32 SIMT path ignores it.
+ *   S: [B,H,D,M] fp32, z: [B,H,D] fp32: both NULL (start from s_0 = 0, z_0 = 0,
+ *      eqs. (16)-(17)) or both non-NULL: the call starts from the state they
+ *      hold and overwrites them with the state after the last token.  Exactly
+ *      one NULL is LA_ERR_INVALID_ARG.
+ *   workspace: la_workspace_bytes(LA_OP_CAUSAL, s, chunk) bytes.
+ */
+la_status la_forward_causal(const void *q, const void *k, const void *v, void *out,
+                            la_shape s, int chunk, float *S, float *z,
+                            void *workspace, size_t ws_bytes, la_stream_t stream);
+
+/*
+ * One recurrent step, sec. 3.4 eqs. (18)-(20), for B*H independent heads:
+ *   S <- S + phi(k) v^T,  z <- z + phi(k),  y = phi(q)^T S / phi(q)^T z
+ * (state updated first, then read out).  s.N is ignored.
+ *   q, k: [B,H,D]; v, y: [B,H,M] (dtype s.dtype); S, z fp32 updated in place.
+ */
+la_status la_decode_step(const void *q, const void *k, const void *v, void *y,
+                         float *S, float *z, la_shape s, la_stream_t stream);
+
+/*
+ * Synchronises `stream`, then returns and clears the current device's error
+ * word (LA_ERR_TIMEOUT if a kernel gave up a bounded wait since the last call)
+ * or LA_ERR_CUDA if the stream itself reports an error.
+ */
+la_status la_get_last_error(la_stream_t stream);
+
+/* Static English name of a status code. */
+const char *la_status_string(la_status st);
+
+/* Library version as major * 10000 + minor * 100 + patch. */
+int la_version(void);
+
+/*
+ * Number of kernels this process has launched through the library so far
+ * (all devices).  Benchmarks read it before and after a timed region.
+ */
+unsigned long long la_launch_count(void);
+
+/*
+ * Test hook (no counterpart in the method): when `enable` is non-zero, the
+ * next causal tensor-core launches on this process wait on a flag that nothing
+ * ever sets, with a wait limit of about `limit_us` microseconds, before they
+ * touch any data; they then record LA_ERR_TIMEOUT, release their tensor memory
+ * and return.  Exercises the bounded-wait error path without hanging a GPU.
+ */
+void la_debug_inject_timeout(int enable, int limit_us);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LA_H */

@@ -1,0 +1,108 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+The library must load on a machine without a GPU, export every entry point
+that include/la.h declares, and reject bad arguments on the host before any
+CUDA call (the header promises checks happen before any launch).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+from weight_recurrence_gb300 import build as labuild
+from weight_recurrence_gb300 import la
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "la.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    labuild.build()
+    return la.lib()
+
+
+def _declared():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(la_[a-z_]+)\s*\(", src)))
+
+
+def test_header_declares_expected_calls():
+    assert set(_declared()) == set(la.EXPORTED)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_status_strings(lib):
+    for st in range(5):
+        assert la.status_string(st)
+    assert la.status_string(la.LA_ERR_TIMEOUT) != la.status_string(la.LA_OK)
+    assert la.la_version() >= 10000
+
+
+def _shape(B=1, H=1, N=8, D=16, M=16, dt=la.LA_DTYPE_F32):
+    return la.la_shape(B, H, N, D, M, dt)
+
+
+FAKE = ctypes.c_void_p(0x10000)          # aligned, never dereferenced: checks fail first
+MISALIGNED = ctypes.c_void_p(0x10008)
+
+
+def test_workspace_query(lib):
+    assert la.la_workspace_bytes(la.LA_OP_DECODE, _shape()) == 0
+    assert la.la_workspace_bytes(la.LA_OP_CAUSAL, _shape()) >= 0
+    assert la.la_workspace_bytes(la.LA_OP_NONCAUSAL, _shape(N=4096, D=64, M=64)) > 0
+    with pytest.raises(la.LAError):
+        la.la_workspace_bytes(la.LA_OP_CAUSAL, _shape(D=48))
+    with pytest.raises(la.LAError):
+        la.la_workspace_bytes(la.LA_OP_CAUSAL, _shape(), chunk=96)
+
+
+@pytest.mark.parametrize("D,M", [(8, 16), (16, 24), (256, 64), (64, 0)])
+def test_unsupported_dims(lib, D, M):
+    st = lib.la_forward_causal(FAKE, FAKE, FAKE, FAKE, _shape(D=D, M=M), 0, None, None, None, 0, None)
+    assert st == la.LA_ERR_UNSUPPORTED
+    st = lib.la_decode_step(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, _shape(D=D, M=M), None)
+    assert st == la.LA_ERR_UNSUPPORTED
+
+
+def test_invalid_arguments(lib):
+    sh = _shape()
+    # negative sizes / unknown dtype
+    assert lib.la_forward_causal(FAKE, FAKE, FAKE, FAKE, _shape(N=-1), 0, None, None, None, 0, None) \
+        == la.LA_ERR_INVALID_ARG
+    assert lib.la_forward_noncausal(FAKE, FAKE, FAKE, FAKE, _shape(B=-2), None, 0, None) \
+        == la.LA_ERR_INVALID_ARG
+    assert lib.la_forward_causal(FAKE, FAKE, FAKE, FAKE, _shape(dt=7), 0, None, None, None, 0, None) \
+        == la.LA_ERR_INVALID_ARG
+    # null and misaligned pointers
+    assert lib.la_forward_causal(None, FAKE, FAKE, FAKE, sh, 0, None, None, None, 0, None) \
+        == la.LA_ERR_INVALID_ARG
+    assert lib.la_forward_causal(FAKE, MISALIGNED, FAKE, FAKE, sh, 0, None, None, None, 0, None) \
+        == la.LA_ERR_INVALID_ARG
+    assert lib.la_decode_step(FAKE, FAKE, FAKE, FAKE, None, FAKE, sh, None) == la.LA_ERR_INVALID_ARG
+    # exactly one of S, z given
+    assert lib.la_forward_causal(FAKE, FAKE, FAKE, FAKE, sh, 0, FAKE, None, None, 0, None) \
+        == la.LA_ERR_INVALID_ARG
+    # unsupported chunk length
+    assert lib.la_forward_causal(FAKE, FAKE, FAKE, FAKE, sh, 96, None, None, None, 0, None) \
+        == la.LA_ERR_UNSUPPORTED
+    # workspace too small for the non-causal reduction
+    big = _shape(N=4096, D=64, M=64)
+    assert lib.la_forward_noncausal(FAKE, FAKE, FAKE, ctypes.c_void_p(0x20000), big, FAKE, 16, None) \
+        == la.LA_ERR_INVALID_ARG
+    # output aliasing an input
+    assert lib.la_forward_causal(FAKE, ctypes.c_void_p(0x20000), ctypes.c_void_p(0x30000), FAKE, sh, 0,
+                                 None, None, None, 0, None) == la.LA_ERR_INVALID_ARG
+
+
+def test_empty_problems_are_noops(lib):
+    # nothing to compute -> OK without touching the (fake) buffers or any device
+    assert lib.la_forward_causal(None, None, None, None, _shape(N=0), 0, None, None, None, 0, None) == la.LA_OK
+    assert lib.la_forward_noncausal(None, None, None, None, _shape(B=0), None, 0, None) == la.LA_OK
+    assert lib.la_decode_step(None, None, None, None, None, None, _shape(H=0), None) == la.LA_OK

@@ -1,0 +1,191 @@
+// la_api.cu - the extern "C" entry points of liblinattn.so: host-side argument
+// checks, dispatch to the kernels, and the per-device error word.
+#include <atomic>
+#include <mutex>
+
+#include "la_common.cuh"
+#include "la_internal.h"
+
+// One error word per device (each device holds its own copy of a __device__
+// variable).  Kernels receive its address; la_get_last_error() reads and clears it.
+__device__ int g_la_error_word = 0;
+
+namespace la {
+
+volatile int g_inject_timeout = 0;
+volatile int g_inject_limit_us = 1000;
+
+static std::atomic<unsigned long long> g_launches{0};
+void count_launches(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+DeviceInfo g_dev[kMaxDevices];
+bool g_dev_ready[kMaxDevices];
+std::mutex g_dev_mu;
+
+bool dim_ok(int x) { return x == 16 || x == 32 || x == 64 || x == 128; }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Shape checks common to every call.  Negative sizes and unknown dtypes are
+// invalid arguments; D, M outside {16, 32, 64, 128} are unsupported.
+la_status check_shape(const la_shape &s, bool uses_n) {
+    if (s.B < 0 || s.H < 0 || (uses_n && s.N < 0)) return LA_ERR_INVALID_ARG;
+    if (s.dtype != LA_DTYPE_F32 && s.dtype != LA_DTYPE_BF16) return LA_ERR_INVALID_ARG;
+    if (!dim_ok(s.D) || !dim_ok(s.M)) return LA_ERR_UNSUPPORTED;
+    return LA_OK;
+}
+
+la_status check_ptr(const void *p, bool needed) {
+    if (!needed) return LA_OK;
+    if (p == nullptr || !aligned16(p)) return LA_ERR_INVALID_ARG;
+    return LA_OK;
+}
+
+bool chunk_ok(int chunk) { return chunk == 0 || chunk == 64 || chunk == 128; }
+
+la_status from_cuda(cudaError_t e) { return e == cudaSuccess ? LA_OK : LA_ERR_CUDA; }
+
+}  // namespace
+
+const DeviceInfo *device_info() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    if (!g_dev_ready[dev]) {
+        DeviceInfo d;
+        if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+                cudaSuccess)
+            return nullptr;
+        void *addr = nullptr;
+        if (cudaGetSymbolAddress(&addr, g_la_error_word) != cudaSuccess) return nullptr;
+        d.err_word = static_cast<int *>(addr);
+        g_dev[dev] = d;
+        g_dev_ready[dev] = true;
+    }
+    return &g_dev[dev];
+}
+
+}  // namespace la
+
+using namespace la;
+
+extern "C" {
+
+int la_version(void) { return 10000; }
+
+unsigned long long la_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+const char *la_status_string(la_status st) {
+    switch (st) {
+        case LA_OK: return "ok";
+        case LA_ERR_INVALID_ARG: return "invalid argument";
+        case LA_ERR_UNSUPPORTED: return "unsupported shape or dtype";
+        case LA_ERR_CUDA: return "CUDA error";
+        case LA_ERR_TIMEOUT: return "a kernel gave up a bounded wait";
+    }
+    return "unknown status";
+}
+
+void la_debug_inject_timeout(int enable, int limit_us) {
+    g_inject_limit_us = limit_us > 0 ? limit_us : 1;
+    g_inject_timeout = enable ? 1 : 0;
+}
+
+size_t la_workspace_bytes(la_op op, la_shape s, int chunk) {
+    if (check_shape(s, op != LA_OP_DECODE) != LA_OK) return (size_t)-1;
+    switch (op) {
+        case LA_OP_NONCAUSAL:
+            if (tc_noncausal_supported(s)) return tc_noncausal_ws_bytes(s);
+            return simt_noncausal_ws_bytes(s);
+        case LA_OP_CAUSAL:
+            if (!chunk_ok(chunk)) return (size_t)-1;
+            if (tc_causal_supported(s, chunk)) return tc_causal_ws_bytes(s, chunk);
+            return 0;
+        case LA_OP_DECODE: return 0;
+    }
+    return (size_t)-1;
+}
+
+la_status la_forward_noncausal(const void *q, const void *k, const void *v, void *out, la_shape s,
+                               void *workspace, size_t ws_bytes, la_stream_t stream) {
+    la_status st = check_shape(s, true);
+    if (st != LA_OK) return st;
+    const long long BH = (long long)s.B * s.H;
+    const bool work = BH > 0 && s.N > 0;
+    if ((st = check_ptr(q, work)) || (st = check_ptr(k, work)) || (st = check_ptr(v, work)) ||
+        (st = check_ptr(out, work)))
+        return st;
+    if (!work) return LA_OK;
+    const size_t need = la_workspace_bytes(LA_OP_NONCAUSAL, s, 0);
+    if (ws_bytes < need || (need > 0 && check_ptr(workspace, true) != LA_OK)) return LA_ERR_INVALID_ARG;
+    if (out == q || out == k || out == v) return LA_ERR_INVALID_ARG;
+    const DeviceInfo *dev = device_info();
+    if (!dev) return LA_ERR_CUDA;
+    Problem p{q, k, v, out, nullptr, nullptr, BH, s.N, s.D, s.M, s.dtype, 0, workspace, ws_bytes,
+              (cudaStream_t)stream};
+    if (tc_noncausal_supported(s)) return from_cuda(tc_noncausal(p, *dev));
+    return from_cuda(simt_noncausal(p, *dev));
+}
+
+la_status la_forward_causal(const void *q, const void *k, const void *v, void *out, la_shape s,
+                            int chunk, float *S, float *z, void *workspace, size_t ws_bytes,
+                            la_stream_t stream) {
+    la_status st = check_shape(s, true);
+    if (st != LA_OK) return st;
+    if (!chunk_ok(chunk)) return LA_ERR_UNSUPPORTED;
+    if ((S == nullptr) != (z == nullptr)) return LA_ERR_INVALID_ARG;
+    const long long BH = (long long)s.B * s.H;
+    const bool work = BH > 0 && s.N > 0;
+    if ((st = check_ptr(S, S != nullptr && BH > 0)) || (st = check_ptr(z, z != nullptr && BH > 0)))
+        return st;
+    if ((st = check_ptr(q, work)) || (st = check_ptr(k, work)) || (st = check_ptr(v, work)) ||
+        (st = check_ptr(out, work && out != nullptr)))
+        return st;
+    if (!work) return LA_OK;   // an empty sequence leaves the state as it is
+    if (out != nullptr && (out == q || out == k || out == v)) return LA_ERR_INVALID_ARG;
+    const size_t need = la_workspace_bytes(LA_OP_CAUSAL, s, chunk);
+    if (ws_bytes < need || (need > 0 && check_ptr(workspace, true) != LA_OK)) return LA_ERR_INVALID_ARG;
+    const DeviceInfo *dev = device_info();
+    if (!dev) return LA_ERR_CUDA;
+    Problem p{q, k, v, out, S, z, BH, s.N, s.D, s.M, s.dtype, chunk, workspace, ws_bytes,
+              (cudaStream_t)stream};
+    if (tc_causal_supported(s, chunk)) return from_cuda(tc_causal(p, *dev));
+    return from_cuda(simt_causal(p, *dev));
+}
+
+la_status la_decode_step(const void *q, const void *k, const void *v, void *y, float *S, float *z,
+                         la_shape s, la_stream_t stream) {
+    la_status st = check_shape(s, false);
+    if (st != LA_OK) return st;
+    const long long BH = (long long)s.B * s.H;
+    const bool work = BH > 0;
+    if ((st = check_ptr(q, work)) || (st = check_ptr(k, work)) || (st = check_ptr(v, work)) ||
+        (st = check_ptr(y, work)) || (st = check_ptr(S, work)) || (st = check_ptr(z, work)))
+        return st;
+    if (!work) return LA_OK;
+    if (BH > 0x7fffffffLL) return LA_ERR_UNSUPPORTED;
+    const DeviceInfo *dev = device_info();
+    if (!dev) return LA_ERR_CUDA;
+    Problem p{q, k, v, y, S, z, BH, 1, s.D, s.M, s.dtype, 0, nullptr, 0, (cudaStream_t)stream};
+    return from_cuda(decode_step(p, *dev));
+}
+
+la_status la_get_last_error(la_stream_t stream) {
+    if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return LA_ERR_CUDA;
+    if (cudaGetLastError() != cudaSuccess) return LA_ERR_CUDA;
+    int word = 0;
+    if (cudaMemcpyFromSymbol(&word, g_la_error_word, sizeof(int)) != cudaSuccess) return LA_ERR_CUDA;
+    if (word != 0) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbol(g_la_error_word, &zero, sizeof(int)) != cudaSuccess) return LA_ERR_CUDA;
+    }
+    return (la_status)word;
+}
+
+}  // extern "C"

@@ -1,0 +1,46 @@
+// la_common.cuh - device helpers shared by the kernels of liblinattn.so.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace la {
+
+// Error codes a kernel may record in the device error word (values of la_status).
+constexpr int kErrTimeout = 4;
+
+// phi(x) = elu(x) + 1 with alpha = 1 ("Transformers are RNNs", sec. 3.2.1,
+// eq. (7)): x + 1 for x > 0, exp(x) otherwise.  Accurate exp for the SIMT path.
+__device__ __forceinline__ float phi_accurate(float x) { return x > 0.f ? x + 1.f : expf(x); }
+
+// Same map with the exponential taken on the MUFU unit as 2^(x * log2 e):
+// ex2.approx.ftz.f32 has a relative error of about 2^-22, far below the bf16
+// rounding that follows on the tensor-core path.
+__device__ __forceinline__ float phi_fast(float x) {
+    float t = fminf(x, 0.f) * 1.4426950408889634f;
+    float e;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(t));
+    return x > 0.f ? x + 1.f : e;
+}
+
+template <typename T> __device__ __forceinline__ float to_f32(T x);
+template <> __device__ __forceinline__ float to_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float x);
+template <> __device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+// Records `code` in the error word unless an earlier error is already there.
+__device__ __forceinline__ void record_error(int *err, int code) {
+    if (err) atomicCAS(err, 0, code);
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+}  // namespace la

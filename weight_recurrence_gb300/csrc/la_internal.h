@@ -1,0 +1,59 @@
+// la_internal.h - host-side declarations shared by the translation units of
+// liblinattn.so (argument checking lives in la_api.cu, kernels elsewhere).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/la.h"
+
+namespace la {
+
+// Cached per-device facts.
+struct DeviceInfo {
+    int sm_count = 0;
+    int cc_major = 0, cc_minor = 0;
+    int max_smem_optin = 0;
+    int *err_word = nullptr;   // device address of this device's error word
+};
+
+// Returns nullptr if the current device cannot be queried.
+const DeviceInfo *device_info();
+
+// Problem description shared by the launchers (all sizes already validated).
+struct Problem {
+    const void *q, *k, *v;
+    void *out;                 // may be null (causal: state only)
+    float *S, *z;              // causal carry / decode state, may be null (causal)
+    long long BH;              // B * H
+    int N, D, M;
+    la_dtype dtype;
+    int chunk;
+    void *ws;
+    size_t ws_bytes;
+    cudaStream_t stream;
+};
+
+// ---- SIMT kernels (la_simt.cu): any D, M in {16,32,64,128}, fp32 or bf16.
+size_t simt_noncausal_ws_bytes(const la_shape &s);
+cudaError_t simt_noncausal(const Problem &p, const DeviceInfo &dev);
+cudaError_t simt_causal(const Problem &p, const DeviceInfo &dev);
+cudaError_t decode_step(const Problem &p, const DeviceInfo &dev);
+
+// ---- tensor-core (tcgen05) kernels (la_tc.cu): bf16, D, M in {64, 128}.
+bool tc_causal_supported(const la_shape &s, int chunk);
+size_t tc_causal_ws_bytes(const la_shape &s, int chunk);
+cudaError_t tc_causal(const Problem &p, const DeviceInfo &dev);
+bool tc_noncausal_supported(const la_shape &s);
+size_t tc_noncausal_ws_bytes(const la_shape &s);
+cudaError_t tc_noncausal(const Problem &p, const DeviceInfo &dev);
+
+// Counts kernel launches made through the library (la_api.cu).
+void count_launches(int n);
+
+// Test hook state (la_api.cu).
+extern volatile int g_inject_timeout;
+extern volatile int g_inject_limit_us;
+
+}  // namespace la

@@ -54,12 +54,16 @@ WORKLOADS = {
 }
 
 
-def qkv(B, H, N, D, M, dtype=torch.bfloat16, scale=1.0, seed=0):
-    """Q, K [B,H,N,D] and V [B,H,N,M] on the CPU, drawn Q then K then V."""
-    g = torch.Generator().manual_seed(int(seed))
+def qkv(B, H, N, D, M, dtype=torch.bfloat16, scale=1.0, seed=0, device="cpu"):
+    """Q, K [B,H,N,D] and V [B,H,N,M], drawn Q then K then V.
+
+    On the CPU (the default, used by every parity test) the values are the
+    CPU generator's; ``device="cuda..."`` draws with that device's generator
+    instead (a different, equally seeded stream, used only for timing)."""
+    g = torch.Generator(device=device).manual_seed(int(seed))
     out = []
     for shape in ((B, H, N, D), (B, H, N, D), (B, H, N, M)):
-        x = torch.randn(shape, generator=g, dtype=torch.float32)
+        x = torch.randn(shape, generator=g, dtype=torch.float32, device=device)
         if scale != 1.0:
             x = x * scale
         out.append(x.to(dtype).contiguous())
@@ -77,12 +81,13 @@ def state(B, H, D, M, seed=0, scale=1.0):
     return S.contiguous(), z.contiguous()
 
 
-def decode_tokens(steps, B, H, D, M, dtype=torch.bfloat16, seed=0, scale=1.0):
-    """Per-step decode inputs as one block [steps, 3, B, H, max(D, M)] split into
-    q [steps,B,H,D], k [steps,B,H,D], v [steps,B,H,M] views (drawn q, k, v per step)."""
-    g = torch.Generator().manual_seed(int(seed))
+def decode_tokens(steps, B, H, D, M, dtype=torch.bfloat16, seed=0, scale=1.0, device="cpu"):
+    """Per-step decode inputs drawn as one block [steps, 3, B, H, max(D, M)] and
+    split into q [steps,B,H,D], k [steps,B,H,D], v [steps,B,H,M] (q, k, v per step).
+    ``device`` as in :func:`qkv`."""
+    g = torch.Generator(device=device).manual_seed(int(seed))
     W = max(D, M)
-    x = torch.randn((steps, 3, B, H, W), generator=g, dtype=torch.float32)
+    x = torch.randn((steps, 3, B, H, W), generator=g, dtype=torch.float32, device=device)
     if scale != 1.0:
         x = x * scale
     x = x.to(dtype)

@@ -1,0 +1,192 @@
+"""ctypes binding of liblinattn.so (argument marshalling only).
+
+Every function here has the name of the C entry point it calls (see
+``include/la.h``) and takes torch tensors for the device buffers; torch
+provides device memory and the current CUDA stream, nothing else.  All work
+runs in the library's kernels.  If the library is missing the first call
+raises: there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "lib", "liblinattn.so")
+
+LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_CUDA, LA_ERR_TIMEOUT = range(5)
+LA_DTYPE_F32, LA_DTYPE_BF16 = 0, 1
+LA_OP_NONCAUSAL, LA_OP_CAUSAL, LA_OP_DECODE = 0, 1, 2
+
+EXPORTED = ("la_workspace_bytes", "la_forward_noncausal", "la_forward_causal", "la_decode_step",
+            "la_get_last_error", "la_status_string", "la_version", "la_launch_count",
+            "la_debug_inject_timeout")
+
+
+class LAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__("%s: %s (status %d)" % (where, status_string(status), status))
+
+
+class la_shape(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int), ("H", ctypes.c_int), ("N", ctypes.c_int),
+                ("D", ctypes.c_int), ("M", ctypes.c_int), ("dtype", ctypes.c_int)]
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("liblinattn.so is not built (%s); run "
+                               "`python -m weight_recurrence_gb300.build`" % LIB_PATH)
+        L = ctypes.CDLL(LIB_PATH)
+        vp, sz, i = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+        L.la_workspace_bytes.restype = sz
+        L.la_workspace_bytes.argtypes = [i, la_shape, i]
+        L.la_forward_noncausal.restype = i
+        L.la_forward_noncausal.argtypes = [vp, vp, vp, vp, la_shape, vp, sz, vp]
+        L.la_forward_causal.restype = i
+        L.la_forward_causal.argtypes = [vp, vp, vp, vp, la_shape, i, vp, vp, vp, sz, vp]
+        L.la_decode_step.restype = i
+        L.la_decode_step.argtypes = [vp, vp, vp, vp, vp, vp, la_shape, vp]
+        L.la_get_last_error.restype = i
+        L.la_get_last_error.argtypes = [vp]
+        L.la_status_string.restype = ctypes.c_char_p
+        L.la_status_string.argtypes = [i]
+        L.la_version.restype = i
+        L.la_launch_count.restype = ctypes.c_ulonglong
+        L.la_debug_inject_timeout.restype = None
+        L.la_debug_inject_timeout.argtypes = [i, i]
+        _lib = L
+    return _lib
+
+
+def status_string(st: int) -> str:
+    return lib().la_status_string(int(st)).decode()
+
+
+def _dtype_code(t: torch.dtype) -> int:
+    if t == torch.float32:
+        return LA_DTYPE_F32
+    if t == torch.bfloat16:
+        return LA_DTYPE_BF16
+    raise TypeError("unsupported dtype %s (float32 or bfloat16)" % t)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream, device):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(st: int, where: str):
+    if st != LA_OK:
+        raise LAError(st, where)
+
+
+def _contig(*ts):
+    for t in ts:
+        if t is not None and not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+
+
+def shape_of(q: torch.Tensor, v: torch.Tensor) -> la_shape:
+    B, H, N, D = q.shape
+    return la_shape(B, H, N, D, v.shape[-1], _dtype_code(q.dtype))
+
+
+def la_workspace_bytes(op: int, shape: la_shape, chunk: int = 0) -> int:
+    n = lib().la_workspace_bytes(int(op), shape, int(chunk))
+    if n == ctypes.c_size_t(-1).value:
+        raise LAError(LA_ERR_INVALID_ARG, "la_workspace_bytes")
+    return int(n)
+
+
+_ws_cache = {}
+
+
+def _workspace(nbytes: int, device) -> torch.Tensor | None:
+    if nbytes == 0:
+        return None
+    key = (torch.device(device).index, torch.cuda.current_stream(device).cuda_stream)
+    buf = _ws_cache.get(key)
+    if buf is None or buf.numel() < nbytes:
+        buf = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
+        _ws_cache[key] = buf
+    return buf
+
+
+def la_forward_noncausal(q, k, v, out=None, stream=None):
+    """V' = phi(Q)(phi(K)^T V) / phi(Q) sum phi(K) for q, k [B,H,N,D], v [B,H,N,M]."""
+    _contig(q, k, v)
+    s = shape_of(q, v)
+    if out is None:
+        out = torch.empty(q.shape[:-1] + (v.shape[-1],), dtype=q.dtype, device=q.device)
+    _contig(out)
+    need = la_workspace_bytes(LA_OP_NONCAUSAL, s, 0)
+    ws = _workspace(need, q.device)
+    st = lib().la_forward_noncausal(_ptr(q), _ptr(k), _ptr(v), _ptr(out), s, _ptr(ws), need,
+                                    _stream(stream, q.device))
+    _check(st, "la_forward_noncausal")
+    return out
+
+
+def la_forward_causal(q, k, v, out=None, chunk=0, S=None, z=None, want_out=True, stream=None):
+    """Causal form (sums over j <= i).  S [B,H,D,M] / z [B,H,D] fp32, if given,
+    hold the carried-in state and receive the state after the last token."""
+    _contig(q, k, v, S, z)
+    s = shape_of(q, v)
+    if out is None and want_out:
+        out = torch.empty(q.shape[:-1] + (v.shape[-1],), dtype=q.dtype, device=q.device)
+    _contig(out)
+    need = la_workspace_bytes(LA_OP_CAUSAL, s, chunk)
+    ws = _workspace(need, q.device)
+    st = lib().la_forward_causal(_ptr(q), _ptr(k), _ptr(v), _ptr(out), s, int(chunk), _ptr(S), _ptr(z),
+                                 _ptr(ws), need, _stream(stream, q.device))
+    _check(st, "la_forward_causal")
+    return out
+
+
+def la_decode_step(q, k, v, S, z, y=None, stream=None):
+    """One recurrent step for q, k [B,H,D], v [B,H,M]; S, z fp32 updated in place."""
+    _contig(q, k, v, S, z)
+    B, H, D = q.shape
+    M = v.shape[-1]
+    if y is None:
+        y = torch.empty((B, H, M), dtype=q.dtype, device=q.device)
+    _contig(y)
+    s = la_shape(B, H, 1, D, M, _dtype_code(q.dtype))
+    st = lib().la_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(y), _ptr(S), _ptr(z), s,
+                              _stream(stream, q.device))
+    _check(st, "la_decode_step")
+    return y
+
+
+def la_get_last_error(stream=None, device=None) -> int:
+    """Synchronises the stream and returns (and clears) the device error word."""
+    dev = device if device is not None else torch.cuda.current_device()
+    return int(lib().la_get_last_error(_stream(stream, dev)))
+
+
+def la_debug_inject_timeout(enable: bool, limit_us: int = 1000):
+    lib().la_debug_inject_timeout(1 if enable else 0, int(limit_us))
+
+
+def la_version() -> int:
+    return int(lib().la_version())
+
+
+def la_launch_count() -> int:
+    """Kernels launched through the library by this process so far."""
+    return int(lib().la_launch_count())
