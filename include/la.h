@@ -120,6 +120,31 @@ la_status la_decode_step(const void *q, const void *k, const void *v, void *y,
                          float *S, float *z, la_shape s, la_stream_t stream);
 
 /*
+ * Non-causal attention that allocates nothing, for callers that cannot
+ * allocate device memory: code that only receives pointers from a host
+ * framework owning the device memory pool, or a loop that must not call the
+ * allocator once it is running (cudaMalloc and cudaFree synchronise the
+ * device).  No counterpart in the paper: it computes exactly what
+ * la_forward_noncausal computes (the same kernels), but its fp32 partial sums
+ * live in an 8 MiB array compiled into this library (a file-scope __device__
+ * array, held by every GPU that loads the library until the process exits)
+ * instead of a caller workspace.
+ *   Limit: B*H*(D*M + D)*4 bytes must not exceed 8 MiB (for D = M = 64,
+ *   B*H <= 504; for D = M = 128, B*H <= 127); larger problems return
+ *   LA_ERR_UNSUPPORTED before any launch.
+ *   The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make that first call
+ *   before any stream capture.
+ *   Every call shares the one array: calls that overlap on the GPU (on two
+ *   streams, or from two threads) race and corrupt each other's results.  The
+ *   array keeps the last call's contents; nothing in it needs to start at
+ *   zero (each call overwrites every partial sum it reads).
+ * Arguments, layout and errors as la_forward_noncausal.
+ */
+la_status la_forward_noncausal_noalloc(const void *q, const void *k, const void *v, void *out,
+                                       la_shape s, la_stream_t stream);
+
+/*
  * Synchronises `stream`, then returns and clears the current device's error
  * word (LA_ERR_TIMEOUT if a kernel gave up a bounded wait since the last call)
  * or LA_ERR_CUDA if the stream itself reports an error.

@@ -40,6 +40,8 @@ size_t simt_noncausal_ws_bytes(const la_shape &s);
 cudaError_t simt_noncausal(const Problem &p, const DeviceInfo &dev);
 cudaError_t simt_causal(const Problem &p, const DeviceInfo &dev);
 cudaError_t decode_step(const Problem &p, const DeviceInfo &dev);
+// Same two kernels as simt_noncausal with at most max_splits partial sums in p.ws.
+cudaError_t simt_noncausal_capped(const Problem &p, const DeviceInfo &dev, int max_splits);
 
 // ---- tensor-core (tcgen05) kernels (la_tc.cu): bf16, D, M in {64, 128}.
 bool tc_causal_supported(const la_shape &s, int chunk);

@@ -356,7 +356,37 @@ cudaError_t simt_causal_t(const Problem &p) {
     return cudaGetLastError();
 }
 
+template <typename T>
+cudaError_t simt_noncausal_capped_t(const Problem &p, const DeviceInfo &dev, int max_splits) {
+    const int nsplit = std::max(1, std::min(nc_nsplit(p.BH, p.N, dev.sm_count), max_splits));
+    const int L = (p.N + nsplit - 1) / nsplit;
+    const int ldq = p.D + 1;
+    size_t sm1 = sizeof(float) * ((size_t)p.D * p.M + p.D + kCs * ldq + (size_t)kCs * p.M);
+    size_t sm2 = sizeof(float) * ((size_t)p.D * p.M + p.D + kCs * ldq + kCs);
+    cudaError_t e = cudaFuncSetAttribute(nc_reduce_simt_kernel<T>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(nc_readout_simt_kernel<T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)sm2);
+    if (e != cudaSuccess) return e;
+    nc_reduce_simt_kernel<T><<<dim3((unsigned)p.BH, nsplit), kThreads, sm1, p.stream>>>(
+        (const T *)p.k, (const T *)p.v, (float *)p.ws, p.N, p.D, p.M, nsplit, L);
+    count_launches(1);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const int R = 256;
+    const int nrb = (p.N + R - 1) / R;
+    nc_readout_simt_kernel<T><<<dim3((unsigned)p.BH, nrb), kThreads, sm2, p.stream>>>(
+        (const T *)p.q, (const float *)p.ws, (T *)p.out, p.N, p.D, p.M, nsplit, R);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
 }  // namespace
+
+cudaError_t simt_noncausal_capped(const Problem &p, const DeviceInfo &dev, int max_splits) {
+    return p.dtype == LA_DTYPE_F32 ? simt_noncausal_capped_t<float>(p, dev, max_splits)
+                                   : simt_noncausal_capped_t<__nv_bfloat16>(p, dev, max_splits);
+}
 
 size_t simt_noncausal_ws_bytes(const la_shape &s) {
     // Sized for the largest split count any device could pick (16 splits max).

@@ -22,7 +22,7 @@ LA_OP_NONCAUSAL, LA_OP_CAUSAL, LA_OP_DECODE = 0, 1, 2
 
 EXPORTED = ("la_workspace_bytes", "la_forward_noncausal", "la_forward_causal", "la_decode_step",
             "la_get_last_error", "la_status_string", "la_version", "la_launch_count",
-            "la_debug_inject_timeout")
+            "la_debug_inject_timeout", "la_forward_noncausal_noalloc")
 
 
 class LAError(RuntimeError):
@@ -62,6 +62,8 @@ def lib() -> ctypes.CDLL:
         L.la_status_string.argtypes = [i]
         L.la_version.restype = i
         L.la_launch_count.restype = ctypes.c_ulonglong
+        L.la_forward_noncausal_noalloc.restype = i
+        L.la_forward_noncausal_noalloc.argtypes = [vp, vp, vp, vp, la_shape, vp]
         L.la_debug_inject_timeout.restype = None
         L.la_debug_inject_timeout.argtypes = [i, i]
         _lib = L
@@ -139,6 +141,20 @@ def la_forward_noncausal(q, k, v, out=None, stream=None):
     st = lib().la_forward_noncausal(_ptr(q), _ptr(k), _ptr(v), _ptr(out), s, _ptr(ws), need,
                                     _stream(stream, q.device))
     _check(st, "la_forward_noncausal")
+    return out
+
+
+def la_forward_noncausal_noalloc(q, k, v, out=None, stream=None):
+    """As la_forward_noncausal, but the library uses its own fixed 8 MiB device
+    scratch array instead of a workspace (for callers that cannot allocate;
+    overlapping calls race on that array)."""
+    _contig(q, k, v)
+    s = shape_of(q, v)
+    if out is None:
+        out = torch.empty(q.shape[:-1] + (v.shape[-1],), dtype=q.dtype, device=q.device)
+    _contig(out)
+    st = lib().la_forward_noncausal_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(out), s, _stream(stream, q.device))
+    _check(st, "la_forward_noncausal_noalloc")
     return out
 
 
