@@ -54,6 +54,10 @@ CAUSAL_CASES = [
     (2, 2, 127, 64, 64, torch.bfloat16, 1.0, 0),
     (1, 3, 200, 16, 32, torch.bfloat16, 1.0, 0),
     (1, 1, 1, 64, 64, torch.bfloat16, 1.0, 0),
+    # long sequences with few heads: split into segments (two-pass state carry)
+    (1, 2, 5000, 64, 64, torch.bfloat16, 0.125, 0),
+    (1, 1, 9000, 128, 128, torch.bfloat16, 1.0 / math.sqrt(128), 0),
+    (1, 1, 4100, 64, 128, torch.bfloat16, 0.125, 0),
 ]
 
 
@@ -74,9 +78,11 @@ def test_causal_vs_oracle(B, H, N, D, M, dtype, scale, chunk):
         assert row_rel_err(out, definition_causal(q, k, v)) <= tol
 
 
-@pytest.mark.parametrize("dtype,D,M", [(torch.float32, 32, 64), (torch.bfloat16, 64, 64), (torch.bfloat16, 128, 128)])
-def test_causal_state_carry_in_and_out(dtype, D, M):
-    B, H, N = 2, 2, 333
+@pytest.mark.parametrize("dtype,D,M,N", [(torch.float32, 32, 64, 333), (torch.bfloat16, 64, 64, 333),
+                                         (torch.bfloat16, 128, 128, 333), (torch.bfloat16, 64, 64, 6000),
+                                         (torch.bfloat16, 128, 64, 3500)])
+def test_causal_state_carry_in_and_out(dtype, D, M, N):
+    B, H = 1, 2
     q, k, v = inputs.qkv(B, H, N, D, M, dtype, 1.0 / math.sqrt(D), seed=77)
     S0, z0 = inputs.state(B, H, D, M, seed=78)
     ref, Sref, zref = oracle.causal(q, k, v, S0=S0.double().numpy(), z0=z0.double().numpy())

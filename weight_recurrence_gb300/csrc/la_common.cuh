@@ -14,15 +14,6 @@ constexpr int kErrTimeout = 4;
 // eq. (7)): x + 1 for x > 0, exp(x) otherwise.  Accurate exp for the SIMT path.
 __device__ __forceinline__ float phi_accurate(float x) { return x > 0.f ? x + 1.f : expf(x); }
 
-// Same map with the exponential taken on the MUFU unit as 2^(x * log2 e):
-// ex2.approx.ftz.f32 has a relative error of about 2^-22, far below the bf16
-// rounding that follows on the tensor-core path.
-__device__ __forceinline__ float phi_fast(float x) {
-    float t = fminf(x, 0.f) * 1.4426950408889634f;
-    float e;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(t));
-    return x > 0.f ? x + 1.f : e;
-}
 
 template <typename T> __device__ __forceinline__ float to_f32(T x);
 template <> __device__ __forceinline__ float to_f32<float>(float x) { return x; }

@@ -11,22 +11,31 @@
 //   out_i  = num_i / den_i                               (eq. (12))
 //   S_prev += phi(K_c)^T V_c,  z_prev += phi(K_c)^T 1   (eqs. (10), (11))
 // Exact in real arithmetic: the j <= i sum of eq. (9) is split at the chunk
-// start into the in-chunk part and the carried prefix state.
+// start into the in-chunk part and the carried prefix state.  The non-causal
+// form (sec. 3.2 eq. (5)) is the same two summaries taken over all keys
+// (state_reduce_kernel) followed by the read-out phi(Q) S / phi(Q) z
+// (readout_kernel).
 //
-// Roles per CTA (one CTA = one head segment, 192 threads):
-//   warp 0     TMA producer: Q, K, V chunk tiles into a ring of NS stages,
-//              128-byte swizzled (the tcgen05 canonical K-major layout);
-//   warp 1     MMA issuer (one thread): all tcgen05.mma, completion through
-//              tcgen05.commit on mbarriers;
-//   warps 2-5  "working group", one thread per TMEM lane / chunk row: applies
-//              phi in place in shared memory, masks P and writes it back to
-//              TMEM as bf16 (the A operand of A V), snapshots the fp32 state to
-//              a bf16 shared-memory copy (the B operand of phi(Q) S_prev),
-//              divides and stores the output rows.
+// Roles of the causal CTA (480 threads):
+//   warp 0      TMA producer: chunk tiles into a ring of NS stages, 128-byte
+//               swizzled (the tcgen05 canonical K-major layout);
+//   warp 1      MMA issuer (one thread): P, A V and phi(Q) S_prev, completion
+//               through tcgen05.commit on mbarriers;
+//   warp 2      state-MMA issuer (one thread): S += phi(K)^T V, the serial
+//               chain from chunk to chunk, never queued behind other MMAs;
+//   warps 3-6   P group, one thread per TMEM lane: masks P and writes it back to
+//               TMEM as bf16 (the A operand of A V), and forms phi(Q_i).z_prev;
+//   warps 7-10  O group: snapshots the fp32 TMEM state into a bf16 shared-memory
+//               copy (the B operand of phi(Q) S_prev), divides the output rows,
+//               stages them in the stage's dead Q/K tiles and stores them by TMA;
+//   warps 11-14 feature-map group: applies phi in place to the Q and K tiles as
+//               they land, running ahead of the MMAs by up to NS chunks.
+// The reduction and read-out kernels use warps 0-9 the same way with one
+// epilogue group (320 threads).
 // The state S (D x M) and z (D) stay in TMEM in fp32 for the whole segment.
-// Long sequences are cut into segments; the state entering segment g is the
-// carried-in state plus the fp32 sums of segments < g, which
-// state_reduce_kernel computes beforehand (two passes, no inter-CTA waits).
+// Long sequences with few heads are cut into segments; the state entering
+// segment g is the carried-in state plus the fp32 sums of segments < g,
+// computed beforehand by state_reduce_kernel (two passes, no inter-CTA waits).
 // Every mbarrier wait is bounded; a CTA that gives up records LA_ERR_TIMEOUT,
 // lets its copies and MMAs drain, frees its TMEM and returns.
 #include <algorithm>
@@ -36,83 +45,34 @@
 #include "tc_host.h"
 #include "tc_ptx.cuh"
 
+// Optional timeline of CTA 0 for performance work: compiled only with
+// -DLA_TRACE (never in the library build); read with la_trace_read().
+#ifdef LA_TRACE
+__device__ unsigned long long g_la_trace[5][64][8];
+extern "C" int la_trace_read(unsigned long long *dst) {
+    return (int)cudaMemcpyFromSymbol(dst, g_la_trace, sizeof(g_la_trace));
+}
+#define LA_TRACE_AT(role, it, ev)                                                     \
+    do {                                                                              \
+        if (blockIdx.x == 0 && (it) < 64) g_la_trace[role][it][ev] = (unsigned long long)clock64(); \
+    } while (0)
+#else
+#define LA_TRACE_AT(role, it, ev) ((void)0)
+#endif
+
 namespace la {
 namespace {
 
 using namespace tc;
 
 constexpr int kC = 128;                          // chunk rows (MMA M)
-constexpr int kWg = 128;                         // working-group threads
-constexpr int kThreads = 64 + kWg;
+constexpr int kGrp = 128;                        // threads of one warpgroup
+constexpr int kThreads = 64 + 2 * kGrp;          // producer, MMA, epilogue group, phi group
 constexpr uint64_t kWaitNs = 2000000000ull;      // 2 s per wait
 constexpr uint32_t kSmemMax = 232448;            // 227 KB opt-in per CTA
-constexpr int kOnesBytes = 2048;                 // 16 K-rows x 64 bf16 ones
+constexpr int kOnesBytes = 1024;                 // one 8-row swizzle atom of a ones operand
 
-template <int D, int M>
-struct Cfg {
-    static constexpr int TILE_QK = kC * D * 2;
-    static constexpr int TILE_V = kC * M * 2;
-    static constexpr int STAGE = 2 * TILE_QK + TILE_V;
-    static constexpr int SNAP = D * M * 2;
-    static constexpr int NPB = (M == 64) ? 2 : 1;      // P buffers in TMEM
-    static constexpr bool O_IN_P = (M == 64);          // O shares the P buffer's upper 64 columns
-    static constexpr int NBARS_FIXED = 4 + 4 * 2;      // snap, s_full, never, drain, 4 per-buffer x2
-    static constexpr int FIXED = SNAP + kOnesBytes + D * 4 + 8 * (NBARS_FIXED + 3 * 8) + 16;
-    static constexpr int NS_FIT = (int)((kSmemMax - FIXED) / STAGE);
-    static constexpr int NS = NS_FIT > 4 ? 4 : NS_FIT;
-    static_assert(NS >= 2, "pipeline needs two stages");
-    // shared-memory map (from a 1024-byte aligned base)
-    static constexpr int OFF_SNAP = NS * STAGE;
-    static constexpr int OFF_ONES = OFF_SNAP + SNAP;
-    static constexpr int OFF_Z = OFF_ONES + kOnesBytes;
-    static constexpr int OFF_BAR = OFF_Z + D * 4;
-    static constexpr int NBARS = 3 * NS + 4 * NPB + 4;
-    static constexpr int OFF_TSLOT = OFF_BAR + 8 * NBARS;
-    static constexpr int SMEM = OFF_TSLOT + 16;
-    static_assert(SMEM <= (int)kSmemMax, "shared memory budget");
-    // TMEM columns
-    static constexpr uint32_t TMEM_COLS = 512;
-    static constexpr uint32_t COL_S = 256;
-    static constexpr uint32_t COL_Z = 256 + M;
-    static __device__ __forceinline__ uint32_t col_p(int b) { return O_IN_P ? 128u * b : 0u; }
-    static __device__ __forceinline__ uint32_t col_o(int b) { return O_IN_P ? 128u * b + 64u : 128u; }
-};
-
-struct CausalArgs {
-    void *out;               // [BH, N, M] bf16 or null
-    float *S;                // [BH, D, M] in/out or null
-    float *z;                // [BH, D] in/out or null
-    const float *seg_ws;     // [BH, nseg, D*M + D] segment sums (segments < nseg-1) or null
-    int N;
-    int nseg;                // segments per head
-    int cps;                 // chunks per segment
-    int *err;
-    uint64_t inject_ns;      // test hook: wait this long on a flag nobody sets
-};
-
-struct Bars {
-    uint64_t *full, *empty, *phi;          // [NS]
-    uint64_t *p_full, *a_ready, *o_full, *o_free;  // [NPB]
-    uint64_t *snap, *s_full, *never, *drain;
-};
-
-template <typename C>
-__device__ __forceinline__ Bars carve_bars(uint8_t *sm) {
-    uint64_t *b = reinterpret_cast<uint64_t *>(sm + C::OFF_BAR);
-    Bars r;
-    r.full = b;
-    r.empty = b + C::NS;
-    r.phi = b + 2 * C::NS;
-    r.p_full = b + 3 * C::NS;
-    r.a_ready = r.p_full + C::NPB;
-    r.o_full = r.a_ready + C::NPB;
-    r.o_free = r.o_full + C::NPB;
-    r.snap = r.o_free + C::NPB;
-    r.s_full = r.snap + 1;
-    r.never = r.s_full + 1;
-    r.drain = r.never + 1;
-    return r;
-}
+// ---------------------------------------------------------------- helpers
 
 __device__ __forceinline__ uint64_t now_ns() { return globaltimer_ns(); }
 
@@ -123,49 +83,79 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatil
     return mbar_wait_bounded(bar, parity, now_ns() + kWaitNs, abort);
 }
 
+// Warp-uniform variant: the whole warp proceeds only if every lane's wait succeeded.
+__device__ __forceinline__ bool wait_bar_warp(uint64_t *bar, uint32_t parity, volatile int *abort) {
+    return __all_sync(0xffffffffu, wait_bar(bar, parity, abort));
+}
+
 __device__ __forceinline__ void set_abort(volatile int *abort, int *err) {
     *abort = 1;
     record_error(err, kErrTimeout);
 }
 
-// phi in place on one 16-byte chunk (8 bf16) of a swizzled tile; zero = write zeros.
-__device__ __forceinline__ void phi_chunk(uint8_t *p, bool zero) {
-    uint4 v = *reinterpret_cast<uint4 *>(p);
-    uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const float lo = phi_fast(bf16lo(w[i])), hi = phi_fast(bf16hi(w[i]));
-        w[i] = zero ? 0u : pack_bf16x2(lo, hi);
-    }
-    *reinterpret_cast<uint4 *>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+// Named barrier for the 128 threads of the epilogue group.
+__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// phi(x) = elu(x) + 1 on two bf16 values, written as max(x, 0) + min(e^x, 1):
+// for x > 0 that is x + 1 and for x <= 0 it is e^x.  e^x = 2^(x log2 e) is taken
+// in fp32 on the MUFU unit and rounded once to bf16; the max, min and add run
+// on packed bf16 pairs.  Each result is rounded exactly once (x + 1, or e^x),
+// so it equals the fp32 evaluation rounded to bf16.  NaN propagates.
+__device__ __forceinline__ uint32_t phi_bf16x2(uint32_t w) {
+    float el, eh;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(el) : "f"(bf16lo(w) * 1.4426950408889634f));
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(eh) : "f"(bf16hi(w) * 1.4426950408889634f));
+    const uint32_t e = pack_bf16x2(el, eh);
+    uint32_t m, n, r;
+    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(m) : "r"(w), "r"(0u));
+    asm("min.NaN.bf16x2 %0, %1, %2;" : "=r"(n) : "r"(e), "r"(0x3F803F80u));
+    asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(m), "r"(n));
+    return r;
 }
 
-// Applies phi to the C x DD tile at `tile` (sub-tiles of 64 columns, each
-// C rows x 128 bytes).  Rows >= zero_from are written as zeros.
+// Applies phi in place to a C x DD tile (sub-tiles of 64 columns, each C rows
+// x 128 bytes); rows >= zero_from are written as zeros.  Each thread handles
+// four 16-byte chunks at a time (loads, then 16 independent phi pairs, then
+// stores) so that enough exponentials are in flight.
 template <int DD>
 __device__ __forceinline__ void phi_tile(uint8_t *tile, int t, int zero_from) {
     constexpr int CHUNKS = kC * DD * 2 / 16;
-#pragma unroll 4
-    for (int u = t; u < CHUNKS; u += kWg) {
-        const uint32_t off = (uint32_t)u * 16u;
-        const int row = (int)((off % (kC * 128u)) >> 7);
-        phi_chunk(tile + off, row >= zero_from);
+    static_assert(CHUNKS % (4 * kGrp) == 0, "whole rounds of four chunks per thread");
+#pragma unroll 1
+    for (int u0 = t; u0 < CHUNKS; u0 += 4 * kGrp) {
+        uint4 v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = *reinterpret_cast<const uint4 *>(tile + (u0 + i * kGrp) * 16);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            v[i].x = phi_bf16x2(v[i].x);
+            v[i].y = phi_bf16x2(v[i].y);
+            v[i].z = phi_bf16x2(v[i].z);
+            v[i].w = phi_bf16x2(v[i].w);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t off = (uint32_t)(u0 + i * kGrp) * 16u;
+            const int row = (int)((off % (kC * 128u)) >> 7);
+            *reinterpret_cast<uint4 *>(tile + off) = row >= zero_from ? make_uint4(0u, 0u, 0u, 0u) : v[i];
+        }
     }
 }
 
-// Writes row r of a D x M fp32 state (values in v, M entries) as bf16 into the
+// Writes columns [c0, c0+32) of row r of a D x M fp32 state as bf16 into the
 // MN-major swizzled snapshot [D rows x M cols] (sub-tiles of 64 columns).
-template <int D, int M>
-__device__ __forceinline__ void store_snap_row(uint8_t *snap, int r, const float *v) {
+template <int D>
+__device__ __forceinline__ void store_snap32(uint8_t *snap, int r, int c0, const float *v) {
 #pragma unroll
-    for (int c8 = 0; c8 < M / 8; ++c8) {
-        const int c = c8 * 8;
+    for (int c8 = 0; c8 < 4; ++c8) {
+        const int c = c0 + c8 * 8;
         uint8_t *dst = snap + (c / 64) * D * 128 + sw128_offset(r, c % 64);
+        const float *x = v + c8 * 8;
         uint4 w;
-        w.x = pack_bf16x2(v[c + 0], v[c + 1]);
-        w.y = pack_bf16x2(v[c + 2], v[c + 3]);
-        w.z = pack_bf16x2(v[c + 4], v[c + 5]);
-        w.w = pack_bf16x2(v[c + 6], v[c + 7]);
+        w.x = pack_bf16x2(x[0], x[1]);
+        w.y = pack_bf16x2(x[2], x[3]);
+        w.z = pack_bf16x2(x[4], x[5]);
+        w.w = pack_bf16x2(x[6], x[7]);
         *reinterpret_cast<uint4 *>(dst) = w;
     }
 }
@@ -192,51 +182,734 @@ __device__ __forceinline__ float q_dot_z(const uint8_t *qt, int r, const float *
     return acc;
 }
 
-__device__ __forceinline__ void wg_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// Loads 32 consecutive fp32 TMEM columns of this thread's lane.
+__device__ __forceinline__ void tmem_ld32f(uint32_t taddr, float (&v)[32]) {
+    uint32_t a[16], b[16];
+    tmem_ld16(taddr, a);
+    tmem_ld16(taddr + 16, b);
+    tmem_wait_ld();
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        v[j] = __uint_as_float(a[j]);
+        v[16 + j] = __uint_as_float(b[j]);
+    }
+}
 
-// ----------------------------------------------------------------------------
-// Causal chunked kernel.
+__device__ __forceinline__ void tmem_st32f(uint32_t taddr, const float (&v)[32]) {
+    uint32_t a[16], b[16];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        a[j] = __float_as_uint(v[j]);
+        b[j] = __float_as_uint(v[16 + j]);
+    }
+    tmem_st16(taddr, a);
+    tmem_st16(taddr + 16, b);
+}
+
+// Stores 32 outputs (scaled by inv) of one row as bf16.
+__device__ __forceinline__ void store_out32(__nv_bfloat16 *dst, const float (&v)[32], float inv) {
+    uint4 *d = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+    for (int c = 0; c < 32; c += 8) {
+        uint4 w;
+        w.x = pack_bf16x2(v[c] * inv, v[c + 1] * inv);
+        w.y = pack_bf16x2(v[c + 2] * inv, v[c + 3] * inv);
+        w.z = pack_bf16x2(v[c + 4] * inv, v[c + 5] * inv);
+        w.w = pack_bf16x2(v[c + 6] * inv, v[c + 7] * inv);
+        d[c / 8] = w;
+    }
+}
+
+// A (TMEM) x B (shared memory) MMA, kind::f16.
+__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                           uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Descriptors of the operand tiles (all 128-byte swizzled, 1024-byte aligned).
+// A descriptor's start-address field counts 16-byte units in its low bits, so
+// a K-step is a constant added to a base descriptor built once per chunk: the
+// single thread issuing MMAs must not spend its time on descriptor arithmetic.
+// K-major tile with rows of up to 128 elements stored as 64-element sub-tiles
+// of kC rows: K-step ks (16 elements) starts 32 bytes further, or in the next
+// sub-tile after 4 steps.
+__device__ __forceinline__ uint64_t kmajor_base(uint32_t tile) { return smem_desc(tile, 16, 1024); }
+__host__ __device__ constexpr uint64_t kmajor_step(int ks, int rows = kC) {
+    return (uint64_t)((ks / 4) * rows * 128 / 16 + (ks % 4) * 2);
+}
+// MN-major: K-step ks covers rows 16ks..16ks+15, 2048 bytes further.
+__host__ __device__ constexpr uint64_t mnmajor_step(int ks) { return (uint64_t)(ks * 128); }
+// B operand of 16 K-rows made of one 8-row atom read twice (K-group stride 0):
+// valid because every row of the ones operand is the same.
+__device__ __forceinline__ uint64_t ones_desc(uint32_t tile) { return smem_desc(tile, 1024, 0); }
+
+// ------------------------------------------------------------ causal kernel
+
+// Warps of the causal CTA: 0 producer, 1 MMA issuer, 2 state-MMA issuer,
+// 3-6 P group, 7-10 O group, 11-14 feature-map group.
+constexpr int kWarpP = 3, kWarpO = 7, kWarpPhi = 11;
+constexpr int kThreadsCausal = 32 * (kWarpPhi + 4);
+
 template <int D, int M>
-__global__ void __launch_bounds__(kThreads, 1)
+struct Cfg {
+    static constexpr int TILE_QK = kC * D * 2;
+    static constexpr int TILE_V = kC * M * 2;
+    static constexpr int STAGE = 2 * TILE_QK + TILE_V;
+    static constexpr int SNAP = D * M * 2;
+    static_assert(kC * M * 2 <= 2 * TILE_QK, "the output tile can be staged in the stage's Q and K tiles");
+    // M = 64: O shares its P buffer; V is read as [V | ones] (N = 80) so that
+    // the state update also yields z and A V also yields the row sums; and the
+    // snapshot is read as [S | z] (N = 80) so that phi(Q) S_prev also yields
+    // phi(Q).z_prev.  The ones operand is a [C x 64] MN-major tile with ones in
+    // column 0; z of snapshot b is stored as two bf16 parts (hi, lo) in its
+    // columns 16(b+1)+1 and 16(b+1)+2, read as an N-atom that starts 32(b+1)
+    // bytes into the tile (the 128-byte swizzle acts on address bits, so a
+    // 16-column window of a swizzled tile is itself a valid atom).
+    static constexpr bool O_IN_P = (M == 64);
+    static constexpr bool ZMMA = O_IN_P;
+    static constexpr int NPB = O_IN_P ? 3 : 1;         // P buffers in TMEM
+    static constexpr int NDZ = ZMMA ? 1 : 2;           // phi(Q).z_prev hand-over slots (TMEM)
+    static constexpr int ONES = O_IN_P ? kC * 128 : kOnesBytes;
+    static constexpr int ZS_BYTES = ZMMA ? 0 : 2 * D * 4;
+    static constexpr int NBARS_MAX = 3 * 4 + 4 * 3 + 2 + 5;
+    static constexpr int FIXED1 = SNAP + ONES + ZS_BYTES + 8 * NBARS_MAX + 16;
+    // two state snapshots when two stages still fit beside them
+    static constexpr bool DB = (kSmemMax - FIXED1 - SNAP) / STAGE >= 2;
+    static constexpr int NSB = DB ? 2 : 1;
+    static constexpr int FIXED = FIXED1 + (NSB - 1) * SNAP;
+    static constexpr int NS_FIT = (int)((kSmemMax - FIXED) / STAGE);
+    static constexpr int NS = NS_FIT > 4 ? 4 : NS_FIT;
+    static_assert(NS >= 2, "pipeline needs two stages");
+    static constexpr int NBARS = 3 * NS + 4 * NPB + NDZ + 5;
+    // Output tiles are staged for the TMA store in buffers of their own when
+    // room is left after the stages (then a stage is released as soon as its
+    // MMAs are done), else in the stage's dead Q/K tiles (then the stage waits
+    // for the store to read them).
+    static constexpr int OUT_TILE = kC * M * 2;
+    static constexpr int BASE = NS * STAGE + NSB * SNAP + ONES + ZS_BYTES + 8 * NBARS + 16;
+    static constexpr int NOB = !ZMMA ? 0 : (BASE + 2 * OUT_TILE <= (int)kSmemMax ? 2 : (BASE + OUT_TILE <= (int)kSmemMax ? 1 : 0));
+    static constexpr int OFF_SNAP = NS * STAGE;
+    static constexpr int OFF_ONES = OFF_SNAP + NSB * SNAP;
+    static constexpr int OFF_Z = OFF_ONES + ONES;           // z snapshots [2][D] fp32 (without ZMMA)
+    static constexpr int OFF_OUT = OFF_Z + ZS_BYTES;
+    static constexpr int OFF_BAR = OFF_OUT + NOB * OUT_TILE;
+    static constexpr int OFF_TSLOT = OFF_BAR + 8 * NBARS;
+    static constexpr int SMEM = OFF_TSLOT + 16;
+    static_assert(SMEM <= (int)kSmemMax, "shared memory budget");
+    // TMEM columns.  M = 64: three 144-column buffers, each holding P
+    // (128 fp32 columns), then A (bf16, columns 0-63) and O (columns 64-143:
+    // 64 numerator columns, then row sum, phi(Q).z_hi, phi(Q).z_lo); S and z
+    // in 432-511.  M = 128: P, a separate A, O, S, z, a 16-column row-sum
+    // block and two 16-column slots handing phi(Q).z_prev from the P group to
+    // the O group.
+    static constexpr uint32_t TMEM_COLS = 512;
+    static constexpr uint32_t COL_S = O_IN_P ? 432 : 320;
+    static constexpr uint32_t COL_Z = COL_S + M;
+    static __device__ __forceinline__ uint32_t col_p(int b) { return O_IN_P ? 144u * b : 0u; }
+    static __device__ __forceinline__ uint32_t col_a(int b) { return O_IN_P ? 144u * b : 128u; }
+    static __device__ __forceinline__ uint32_t col_o(int b) { return O_IN_P ? 144u * b + 64u : 192u; }
+    static __device__ __forceinline__ uint32_t col_den(int b) { return O_IN_P ? 144u * b + 128u : 464u; }
+    static __device__ __forceinline__ uint32_t col_dz(int j) { return 480u + 16u * (j & 1); }
+    static_assert(O_IN_P ? (COL_Z + 16 <= TMEM_COLS) : (COL_Z + 16 <= 464), "TMEM budget");
+};
+
+struct CausalArgs {
+    bool has_out;            // store the output rows (through tm_o)
+    float *S;                // [BH, D, M] in/out or null
+    float *z;                // [BH, D] in/out or null
+    const float *seg_ws;     // nseg > 1: [BH, nseg, D*M + D]; slots < nseg-1 hold segment sums,
+                             // slot nseg-1 the state carried in
+    int N;
+    int nseg;                // segments per head
+    int cps;                 // chunks per segment
+    int *err;
+    uint64_t inject_ns;      // test hook: wait this long on a flag nobody sets
+};
+
+// Named barrier of the O group's 128 threads.
+__device__ __forceinline__ void o_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
+
+template <int D, int M>
+__global__ void __launch_bounds__(kThreadsCausal, 1)
 causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                 const __grid_constant__ CUtensorMap tm_v, const CausalArgs args)
+                 const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                 const CausalArgs args)
 {
     using C = Cfg<D, M>;
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     volatile int *abort = reinterpret_cast<volatile int *>(smem + C::OFF_TSLOT + 4);
 
-    const int item = blockIdx.x;
-    const int bh = item / args.nseg, seg = item % args.nseg;
+    const int bh = blockIdx.x / args.nseg, seg = blockIdx.x % args.nseg;
     const int nch_total = (args.N + kC - 1) / kC;
     const int c_begin = seg * args.cps;
-    const int c_end = min(nch_total, c_begin + args.cps);
-    const int n = max(0, c_end - c_begin);
+    const int n = max(0, min(nch_total, c_begin + args.cps) - c_begin);
 
-    Bars bars = carve_bars<C>(smem);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
+    uint64_t *full = bar, *empty = bar + C::NS, *phi_done = bar + 2 * C::NS;
+    uint64_t *p_full = bar + 3 * C::NS, *a_ready = p_full + C::NPB, *o_full = a_ready + C::NPB,
+             *o_free = o_full + C::NPB, *dz_ready = o_free + C::NPB;
+    // snapshot of the state entering chunk j: barrier j & 1, phase j >> 1 (two
+    // barriers, so that no waiter can fall two phases behind one barrier)
+    uint64_t *snap_bar = dz_ready + C::NDZ, *s_full = snap_bar + 2, *never = s_full + 1, *drain = never + 1;
+    auto snap_wait = [&](int j) { return wait_bar(&snap_bar[j & 1], (j >> 1) & 1, abort); };
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + C::OFF_TSLOT);
-    uint8_t *snap = smem + C::OFF_SNAP;
+    uint8_t *snap0 = smem + C::OFF_SNAP;
     uint8_t *ones = smem + C::OFF_ONES;
-    float *zs = reinterpret_cast<float *>(smem + C::OFF_Z);
+    float *zs0 = reinterpret_cast<float *>(smem + C::OFF_Z);
+    auto snap_buf = [&](int j) { return snap0 + (C::DB ? (j & 1) : 0) * C::SNAP; };
+    // column of the ones tile holding z_hi of snapshot j (z_lo in the next one)
+    auto zcol = [&](int j) { return 16 * (1 + (C::DB ? (j & 1) : 0)) + 1; };
+    auto zs_buf = [&](int j) { return zs0 + (j & 1) * D; };
 
     if (tid == 0) {
-        *abort = (smem_u32(smem) & 1023u) ? 1 : 0;   // layout needs a 1024-byte aligned base
+        *abort = (smem_u32(smem) & 1023u) ? 1 : 0;   // the swizzled layouts need a 1024-byte aligned base
         if (*abort) record_error(args.err, kErrTimeout);
         for (int s = 0; s < C::NS; ++s) {
-            mbar_init(&bars.full[s], 1);
-            mbar_init(&bars.empty[s], 1);
-            mbar_init(&bars.phi[s], kWg);
+            mbar_init(&full[s], 1);
+            // released by both MMA issuers (own output buffers) or by the O group after the store
+            mbar_init(&empty[s], C::NOB ? 2 : 1);
+            mbar_init(&phi_done[s], kGrp);
         }
         for (int b = 0; b < C::NPB; ++b) {
-            mbar_init(&bars.p_full[b], 1);
-            mbar_init(&bars.a_ready[b], kWg);
-            mbar_init(&bars.o_full[b], 1);
-            mbar_init(&bars.o_free[b], kWg);
+            mbar_init(&p_full[b], 1);
+            mbar_init(&a_ready[b], kGrp);
+            mbar_init(&o_full[b], 1);
+            mbar_init(&o_free[b], kGrp);
         }
-        mbar_init(bars.snap, kWg);
-        mbar_init(bars.s_full, 1);
-        mbar_init(bars.never, 1);
-        mbar_init(bars.drain, 1);
+        for (int b = 0; b < C::NDZ; ++b) mbar_init(&dz_ready[b], kGrp);
+        mbar_init(&snap_bar[0], kGrp);
+        mbar_init(&snap_bar[1], kGrp);
+        mbar_init(s_full, 1);
+        mbar_init(never, 1);
+        mbar_init(drain, 2);
+        fence_mbar_init();
+    }
+    // ones operand, MN-major, ones in column 0 and zeros elsewhere: [C K-rows x 64]
+    // when it is read as the second N-atom of [V | ones], else one 8-row atom
+    for (int i = tid; i < C::ONES / 4; i += kThreadsCausal) reinterpret_cast<uint32_t *>(ones)[i] = 0u;
+    __syncthreads();
+    for (int k = tid; k < C::ONES / 128; k += kThreadsCausal)
+        *reinterpret_cast<uint16_t *>(ones + sw128_offset(k, 0)) = 0x3F80u;
+    if (warp == 0) {
+        tmem_alloc(tslot, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+
+    // Test hook: wait on a barrier that nothing arrives on, then give up.
+    if (args.inject_ns && tid == 0) {
+        if (!mbar_wait_bounded(never, 0, now_ns() + args.inject_ns, nullptr)) set_abort(abort, args.err);
+    }
+    __syncthreads();
+
+    constexpr uint32_t ID_16 = idesc_bf16(128, 16, 1, 1);
+    const uint32_t ones_a = smem_u32(ones);
+    const uint64_t ones_d = ones_desc(ones_a);
+    // V read MN-major; with M = 64 its second N-atom is the ones tile
+    auto v_base = [&](uint32_t va) { return smem_desc(va, C::O_IN_P ? ones_a - va : (uint32_t)(kC * 128), 1024); };
+
+    if (warp == 0) {
+        // ------------------------------------------------------ producer
+        if (lane == 0 && !*abort) {
+            prefetch_tmap(&tm_q);
+            prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_v);
+            int issued = 0;
+            for (int it = 0; it < n; ++it) {
+                const int s = it % C::NS, k = it / C::NS;
+                if (it >= C::NS && !wait_bar(&empty[s], (k - 1) & 1, abort)) break;
+                uint8_t *st = smem + s * C::STAGE;
+                const int t0 = (c_begin + it) * kC;
+                LA_TRACE_AT(0, it, 0);
+                mbar_arrive_expect_tx(&full[s], C::STAGE);
+#pragma unroll
+                for (int j = 0; j < D / 64; ++j) tma_load_3d(st + j * kC * 128, &tm_q, &full[s], j * 64, t0, bh);
+#pragma unroll
+                for (int j = 0; j < D / 64; ++j)
+                    tma_load_3d(st + C::TILE_QK + j * kC * 128, &tm_k, &full[s], j * 64, t0, bh);
+#pragma unroll
+                for (int j = 0; j < M / 64; ++j)
+                    tma_load_3d(st + 2 * C::TILE_QK + j * kC * 128, &tm_v, &full[s], j * 64, t0, bh);
+                ++issued;
+            }
+            if (*abort) {   // let the copies in flight land before the CTA exits
+                for (int it = max(0, issued - C::NS); it < issued; ++it)
+                    mbar_wait_bounded(&full[it % C::NS], (it / C::NS) & 1, now_ns() + kWaitNs, nullptr);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------ MMA issuer
+        // P = phi(Q) phi(K)^T, O = A V (+ row sums) and O += phi(Q) S_prev
+        if (lane == 0 && !*abort) {
+            constexpr int NV = C::O_IN_P ? M + 16 : M;      // N of the MMAs that read V
+            constexpr uint32_t ID_P = idesc_bf16(128, kC, 0, 0);
+            constexpr uint32_t ID_O = idesc_bf16(128, M, 0, 1);
+            constexpr uint32_t ID_AV = idesc_bf16(128, NV, 0, 1);
+            constexpr uint32_t ID_D = idesc_bf16(128, 16, 0, 1);
+            // P = phi(Q) phi(K)^T for chunk j into its P buffer
+            auto issue_p = [&](int j) {
+                const int s = j % C::NS, pb = j % C::NPB;
+                tc_fence_after();
+                const uint32_t st = smem_u32(smem + s * C::STAGE);
+                const uint64_t dq = kmajor_base(st), dk = kmajor_base(st + C::TILE_QK);
+                const uint32_t dp = tmem + C::col_p(pb);
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks)
+                    mma_f16_ss(dp, dq + kmajor_step(ks), dk + kmajor_step(ks), ID_P, ks > 0);
+                mma_commit(&p_full[pb]);
+                LA_TRACE_AT(1, j, 2);
+            };
+            // O (+)= phi(Q) [S_prev | z]: the z atom is the 16-column window of the ones
+            // tile holding snapshot j's z
+            auto issue_inter = [&](uint32_t qa, uint32_t sa, uint32_t zatom, uint32_t ocol, bool acc) {
+                constexpr uint32_t ID_I = C::ZMMA ? idesc_bf16(128, M + 16, 0, 1) : ID_O;
+                const uint64_t dq = kmajor_base(qa);
+                const uint64_t ds = smem_desc(sa, C::ZMMA ? zatom - sa : (uint32_t)(D * 128), 1024);
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks)
+                    mma_f16_ss(tmem + ocol, dq + kmajor_step(ks), ds + mnmajor_step(ks), ID_I, acc || ks > 0);
+            };
+            // numerator, row sums and phi(Q) S_prev for chunk j
+            auto issue_av = [&](int j) {
+                const int s = j % C::NS, pb = j % C::NPB;
+                const uint32_t st = smem_u32(smem + s * C::STAGE);
+                const uint32_t qa = st, va = st + 2 * C::TILE_QK;
+                const uint32_t sa = smem_u32(snap_buf(j));
+                const uint32_t za = ones_a + 2 * (zcol(j) - 1);
+                tc_fence_after();
+                const uint64_t dv = v_base(va);
+                if (C::O_IN_P) {
+                    // O = A [V | 1] (numerator and row sums), then O += phi(Q) S_prev
+#pragma unroll
+                    for (int ks = 0; ks < kC / 16; ++ks)
+                        mma_f16_ts(tmem + C::col_o(pb), tmem + C::col_a(pb) + ks * 8, dv + mnmajor_step(ks), ID_AV,
+                                   ks > 0);
+                    issue_inter(qa, sa, za, C::col_o(pb), true);
+                } else {
+                    issue_inter(qa, sa, za, C::col_o(0), false);
+                    // O += A V and row sums A 1  (A = masked P as bf16 in TMEM, K = C)
+#pragma unroll
+                    for (int ks = 0; ks < kC / 16; ++ks) {
+                        const uint32_t at = tmem + C::col_a(0) + ks * 8;
+                        mma_f16_ts(tmem + C::col_o(0), at, dv + mnmajor_step(ks), ID_O, 1);
+                        mma_f16_ts(tmem + C::col_den(0), at, ones_d, ID_D, ks > 0);
+                    }
+                }
+                mma_commit(&o_full[pb]);
+                if (C::NOB) mma_commit(&empty[s]);
+                LA_TRACE_AT(1, j, 5);
+            };
+            // Issues, in whatever order their inputs become ready, P(jp) (needs phi of
+            // chunk jp and a free P buffer) and the output MMAs of chunk ja (need A(ja)
+            // and the snapshot of the state before chunk ja); the output MMAs go first.
+            // Every barrier tested here can be at most one phase ahead of its test.
+            int jp = 0, ja = 0;
+            uint64_t deadline = now_ns() + kWaitNs;
+            uint32_t idle = 0;
+            while (ja < n) {
+                bool progress = false;
+                if (ja < jp) {
+                    const int pb = ja % C::NPB, kb = ja / C::NPB;
+                    bool rdy = mbar_test(&a_ready[pb], kb & 1) && mbar_test(&snap_bar[ja & 1], (ja >> 1) & 1);
+                    if (!C::O_IN_P && ja > 0) rdy = rdy && mbar_test(&o_free[0], (ja - 1) & 1);
+                    if (rdy) {
+                        issue_av(ja++);
+                        progress = true;
+                    }
+                }
+                if (!progress && jp < n) {
+                    const int s = jp % C::NS, pb = jp % C::NPB, kb = jp / C::NPB;
+                    bool rdy = mbar_test(&phi_done[s], (jp / C::NS) & 1);
+                    if (C::O_IN_P) {
+                        if (kb > 0) rdy = rdy && mbar_test(&o_free[pb], (kb - 1) & 1);
+                    } else if (jp > 0) {
+                        rdy = rdy && mbar_test(&a_ready[0], (jp - 1) & 1);   // P(jp-1) has been read
+                    }
+                    if (rdy) {
+                        issue_p(jp++);
+                        progress = true;
+                    }
+                }
+                if (progress) {
+                    idle = 0;
+                } else if ((++idle & 63u) == 0) {
+                    if (*abort) break;
+                    if (idle == 64) deadline = now_ns() + kWaitNs;
+                    else if (now_ns() > deadline) { set_abort(abort, args.err); break; }
+                }
+            }
+        }
+        if (lane == 0) mma_commit(drain);   // arrives once this thread's MMAs (if any) are done
+    } else if (warp == 2) {
+        // ------------------------------------------------------ state-MMA issuer
+        // S += phi(K)^T V and z += phi(K)^T 1, one chunk after the other, as soon
+        // as the previous state has been snapshotted (A = phi(K) read MN-major,
+        // 128 rows; accumulator rows >= D are never read)
+        if (lane == 0 && !*abort) {
+            constexpr int NV = C::O_IN_P ? M + 16 : M;
+            constexpr uint32_t ID_S = idesc_bf16(128, NV, 1, 1);
+            for (int it = 0; it < n; ++it) {
+                const int s = it % C::NS;
+                if (!wait_bar(&phi_done[s], (it / C::NS) & 1, abort)) break;
+                LA_TRACE_AT(4, it, 6);
+                if (!snap_wait(it)) break;   // S(it-1) has been read out
+                LA_TRACE_AT(4, it, 7);
+                tc_fence_after();
+                const uint32_t st = smem_u32(smem + s * C::STAGE);
+                const uint64_t dk = smem_desc(st + C::TILE_QK, kC * 128, 1024), dv = v_base(st + 2 * C::TILE_QK);
+#pragma unroll
+                for (int ks = 0; ks < kC / 16; ++ks) {
+                    mma_f16_ss(tmem + C::COL_S, dk + mnmajor_step(ks), dv + mnmajor_step(ks), ID_S, 1);
+                    if (!C::O_IN_P) mma_f16_ss(tmem + C::COL_Z, dk + mnmajor_step(ks), ones_d, ID_16, 1);
+                }
+                mma_commit(s_full);
+                if (C::NOB) mma_commit(&empty[s]);
+            }
+        }
+        if (lane == 0) mma_commit(drain);
+    } else if (warp < kWarpO) {
+        // ------------------------------------------------------ P group
+        // masks P(it), rounds it to bf16 into TMEM (the A operand), and
+        // computes phi(Q_r).z_prev for the O group
+        const int q4 = warp & 3;                 // TMEM lane quarter this warp may access
+        const int r = 32 * q4 + lane;            // chunk row owned by this thread
+        const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
+        for (int it = 0; it < n; ++it) {
+            const int s = it % C::NS, pb = it % C::NPB, kb = it / C::NPB;
+            if (tid == 32 * kWarpP) LA_TRACE_AT(2, it, 3);
+            bool ok = wait_bar_warp(&p_full[pb], kb & 1, abort);
+            if (!C::O_IN_P && it > 0) ok = ok && wait_bar_warp(&o_full[0], (it - 1) & 1, abort);
+            if (tid == 32 * kWarpP) LA_TRACE_AT(2, it, 4);
+            if (ok) {
+                tc_fence_after();
+#pragma unroll 1
+                for (int c0 = 0; c0 < kC; c0 += 32) {
+                    uint32_t a[16];
+                    if (c0 > 32 * q4) {          // above the diagonal for every row of this warp
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) a[j] = 0u;
+                    } else {
+                        float x[32];
+                        tmem_ld32f(tmem + lane_off + C::col_p(pb) + c0, x);
+                        if (c0 == 32 * q4) {     // the diagonal block: keep j <= r
+#pragma unroll
+                            for (int j = 0; j < 16; ++j)
+                                a[j] = pack_bf16x2(c0 + 2 * j <= r ? x[2 * j] : 0.f,
+                                                   c0 + 2 * j + 1 <= r ? x[2 * j + 1] : 0.f);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j) a[j] = pack_bf16x2(x[2 * j], x[2 * j + 1]);
+                        }
+                    }
+                    tmem_st16(tmem + lane_off + C::col_a(pb) + c0 / 2, a);
+                }
+                tmem_wait_st();
+            }
+            tc_fence_before();
+            mbar_arrive(&a_ready[pb]);
+            if (tid == 32 * kWarpP) LA_TRACE_AT(2, it, 5);
+            if (!C::ZMMA) {
+                // phi(Q_r) . z_prev into TMEM for the O group (the stage is released only
+                // after the O group is done with the chunk)
+                if (__all_sync(0xffffffffu, snap_wait(it))) {
+                    uint32_t w[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) w[j] = 0u;
+                    w[0] = __float_as_uint(q_dot_z<D>(smem + s * C::STAGE, r, zs_buf(it)));
+                    tmem_st16(tmem + lane_off + C::col_dz(it), w);
+                    tmem_wait_st();
+                }
+                tc_fence_before();
+                mbar_arrive(&dz_ready[it % C::NDZ]);
+            }
+        }
+    } else if (warp < kWarpPhi) {
+        // ------------------------------------------------------ O group
+        // state snapshots (the B operand of phi(Q) S_prev) and the output rows
+        const int q4 = warp & 3;
+        const int r = 32 * q4 + lane;
+        const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
+        const bool srow = r < D;                 // owns a state row
+        const bool swarp = 32 * q4 < D;          // warp-uniform
+        const bool leader = tid == 32 * kWarpO;
+        float *S_h = args.S ? args.S + (size_t)bh * D * M : nullptr;
+        float *z_h = args.z ? args.z + (size_t)bh * D : nullptr;
+
+        // state entering the segment: carried-in state plus earlier segments' sums
+        if (swarp) {
+            const float *ws_h = args.seg_ws ? args.seg_ws + (size_t)bh * args.nseg * (D * M + D) : nullptr;
+            float zr = 0.f;
+            if (srow) {
+                if (ws_h) {
+                    zr = ws_h[(size_t)(args.nseg - 1) * (D * M + D) + D * M + r];
+                    for (int g = 0; g < seg; ++g) zr += ws_h[(size_t)g * (D * M + D) + D * M + r];
+                } else if (z_h) {
+                    zr = z_h[r];
+                }
+                if (C::ZMMA) {
+                    const __nv_bfloat16 hi = __float2bfloat16_rn(zr);
+                    const __nv_bfloat16 lo = __float2bfloat16_rn(zr - __bfloat162float(hi));
+                    *reinterpret_cast<__nv_bfloat16 *>(ones + sw128_offset(r, zcol(0))) = hi;
+                    *reinterpret_cast<__nv_bfloat16 *>(ones + sw128_offset(r, zcol(0) + 1)) = lo;
+                } else {
+                    zs_buf(0)[r] = zr;
+                }
+            }
+#pragma unroll 1
+            for (int c0 = 0; c0 < M; c0 += 32) {
+                float v[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = 0.f;
+                if (srow) {
+                    auto add = [&](const float *src) {
+#pragma unroll
+                        for (int j = 0; j < 32; j += 4) {
+                            const float4 x = *reinterpret_cast<const float4 *>(src + r * M + c0 + j);
+                            v[j] += x.x; v[j + 1] += x.y; v[j + 2] += x.z; v[j + 3] += x.w;
+                        }
+                    };
+                    if (ws_h) {
+                        add(ws_h + (size_t)(args.nseg - 1) * (D * M + D));
+                        for (int g = 0; g < seg; ++g) add(ws_h + (size_t)g * (D * M + D));
+                    } else if (S_h) {
+                        add(S_h);
+                    }
+                    store_snap32<D>(snap_buf(0), r, c0, v);
+                }
+                tmem_st32f(tmem + lane_off + C::COL_S + c0, v);
+            }
+            uint32_t w[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) w[j] = 0u;
+            w[0] = __float_as_uint(zr);
+            tmem_st16(tmem + lane_off + C::COL_Z, w);
+            tmem_wait_st();
+        }
+        tc_fence_before();
+        fence_proxy_async();
+        mbar_arrive(&snap_bar[0]);
+        if (leader && args.has_out) prefetch_tmap(&tm_o);
+
+        for (int it = 0; it < n; ++it) {
+            const int s = it % C::NS, pb = it % C::NPB, kb = it / C::NPB;
+            // ---- snapshot of the state after chunk it, for chunk it+1
+            if (tid == 32 * kWarpO + 32 * (4 - kWarpO % 4) % 128) LA_TRACE_AT(4, it, 0);
+            bool ok = wait_bar_warp(s_full, it & 1, abort);
+            if (!C::DB) ok = ok && wait_bar_warp(&o_full[pb], kb & 1, abort);   // single snapshot: read by O(it)
+            if (tid == 32 * kWarpO + 32 * (4 - kWarpO % 4) % 128) LA_TRACE_AT(4, it, 1);
+            if (it + 1 < n) {
+                if (ok && swarp) {
+                    tc_fence_after();
+                    uint8_t *sb = snap_buf(it + 1);
+#pragma unroll 1
+                    for (int c0 = 0; c0 < M; c0 += 32) {
+                        float v[32];
+                        tmem_ld32f(tmem + lane_off + C::COL_S + c0, v);
+                        if (srow) store_snap32<D>(sb, r, c0, v);
+                    }
+                    uint32_t zv[16];
+                    tmem_ld16(tmem + lane_off + C::COL_Z, zv);
+                    tmem_wait_ld();
+                    if (srow) {
+                        const float zr = __uint_as_float(zv[0]);
+                        if (C::ZMMA) {
+                            const __nv_bfloat16 hi = __float2bfloat16_rn(zr);
+                            const __nv_bfloat16 lo = __float2bfloat16_rn(zr - __bfloat162float(hi));
+                            *reinterpret_cast<__nv_bfloat16 *>(ones + sw128_offset(r, zcol(it + 1))) = hi;
+                            *reinterpret_cast<__nv_bfloat16 *>(ones + sw128_offset(r, zcol(it + 1) + 1)) = lo;
+                        } else {
+                            zs_buf(it + 1)[r] = zr;
+                        }
+                    }
+                }
+                tc_fence_before();
+                fence_proxy_async();
+                mbar_arrive(&snap_bar[(it + 1) & 1]);
+            }
+            if (tid == 32 * kWarpO + 32 * (4 - kWarpO % 4) % 128) LA_TRACE_AT(4, it, 2);
+            // ---- output rows of chunk it: num / (row sum + phi(Q).z_prev), staged as
+            // a swizzled tile in the (now dead) Q and K tiles of the stage, stored by TMA
+            const int t0 = (c_begin + it) * kC;
+            ok = wait_bar_warp(&o_full[pb], kb & 1, abort);
+            if (!C::ZMMA) ok = ok && wait_bar_warp(&dz_ready[it % C::NDZ], (it / C::NDZ) & 1, abort);
+            if (tid == 32 * kWarpO + 32 * (4 - kWarpO % 4) % 128) LA_TRACE_AT(4, it, 3);
+            uint8_t *stage_out = C::NOB ? smem + C::OFF_OUT + (it % (C::NOB ? C::NOB : 1)) * C::OUT_TILE
+                                        : smem + s * C::STAGE;
+            if (C::NOB) o_sync();   // the store that last read this buffer has finished reading it
+            if (ok) {
+                tc_fence_after();
+                uint32_t dv[16];
+                tmem_ld16(tmem + lane_off + C::col_den(pb), dv);
+                float den;
+                if (C::ZMMA) {   // row sum + phi(Q).z_hi + phi(Q).z_lo
+                    tmem_wait_ld();
+                    den = __uint_as_float(dv[0]) + (__uint_as_float(dv[1]) + __uint_as_float(dv[2]));
+                } else {
+                    uint32_t zv[16];
+                    tmem_ld16(tmem + lane_off + C::col_dz(it), zv);
+                    tmem_wait_ld();
+                    den = __uint_as_float(dv[0]) + __uint_as_float(zv[0]);
+                }
+                const float inv = 1.f / den;
+#pragma unroll 1
+                for (int c0 = 0; c0 < M; c0 += 32) {
+                    float o[32];
+                    tmem_ld32f(tmem + lane_off + C::col_o(pb) + c0, o);
+                    if (args.has_out) {
+#pragma unroll
+                        for (int c8 = 0; c8 < 4; ++c8) {
+                            const int c = c0 + 8 * c8;
+                            uint4 w;
+                            w.x = pack_bf16x2(o[8 * c8] * inv, o[8 * c8 + 1] * inv);
+                            w.y = pack_bf16x2(o[8 * c8 + 2] * inv, o[8 * c8 + 3] * inv);
+                            w.z = pack_bf16x2(o[8 * c8 + 4] * inv, o[8 * c8 + 5] * inv);
+                            w.w = pack_bf16x2(o[8 * c8 + 6] * inv, o[8 * c8 + 7] * inv);
+                            *reinterpret_cast<uint4 *>(stage_out + (c / 64) * kC * 128 + sw128_offset(r, c % 64)) = w;
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&o_free[pb]);
+            if (!C::NOB && it == n - 1) ok = ok && wait_bar_warp(s_full, it & 1, abort);   // last update read K, V
+            fence_proxy_async();
+            o_sync();
+            if (leader) {
+                if (ok && args.has_out) {
+#pragma unroll
+                    for (int j = 0; j < M / 64; ++j) tma_store_3d(&tm_o, stage_out + j * kC * 128, j * 64, t0, bh);
+                    tma_store_commit();
+                }
+                if (C::NOB == 2) {
+                    tma_store_wait_read1();   // the other buffer is free for the next chunk
+                } else {
+                    tma_store_wait_read0();
+                    if (!C::NOB) mbar_arrive(&empty[s]);
+                }
+            }
+            if (tid == 32 * kWarpO + 32 * (4 - kWarpO % 4) % 128) LA_TRACE_AT(4, it, 4);
+        }
+        if (leader && args.has_out) tma_store_wait_all0();
+        // ---- state after the last token (last segment only)
+        if (S_h && seg == args.nseg - 1 && n > 0) {
+            const bool ok = wait_bar_warp(s_full, (n - 1) & 1, abort);
+            if (ok && swarp) {
+                tc_fence_after();
+#pragma unroll 1
+                for (int c0 = 0; c0 < M; c0 += 32) {
+                    float v[32];
+                    tmem_ld32f(tmem + lane_off + C::COL_S + c0, v);
+                    if (srow)
+#pragma unroll
+                        for (int j = 0; j < 32; j += 4)
+                            *reinterpret_cast<float4 *>(S_h + r * M + c0 + j) =
+                                make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+                }
+                uint32_t zv[16];
+                tmem_ld16(tmem + lane_off + C::COL_Z, zv);
+                tmem_wait_ld();
+                if (srow) z_h[r] = __uint_as_float(zv[0]);
+            }
+        }
+    } else {
+        // ------------------------------------------------------ feature-map group
+        const int t = tid - 32 * kWarpPhi;
+        for (int it = 0; it < n; ++it) {
+            const int s = it % C::NS;
+            if (t == 0) LA_TRACE_AT(3, it, 0);
+            if (wait_bar(&full[s], (it / C::NS) & 1, abort)) {
+                if (t == 0) LA_TRACE_AT(3, it, 1);
+                uint8_t *st = smem + s * C::STAGE;
+                phi_tile<D>(st, t, kC);
+                phi_tile<D>(st + C::TILE_QK, t, min(kC, args.N - (c_begin + it) * kC));
+                if (t == 0) LA_TRACE_AT(3, it, 2);
+            }
+            fence_proxy_async();
+            mbar_arrive(&phi_done[s]);
+        }
+    }
+    // no MMA may still be running when the CTA frees its TMEM
+    if (tid == 0) mbar_wait_bounded(drain, 0, now_ns() + kWaitNs, nullptr);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+// ------------------------------------------------- state reduction kernel
+// For each (head, split): S = sum_j phi(K_j) V_j^T and z = sum_j phi(K_j)
+// over the split's chunks, in fp32, into ws[bh][split] = (S row-major, z).
+// The CTA of split 0 can also copy a carried-in state (or zeros) into slot
+// init_slot, so that the causal kernel's segments read their starting state
+// from the workspace only.
+
+template <int D, int M>
+struct RCfg {
+    static constexpr int TILE_K = kC * D * 2;
+    static constexpr int TILE_V = kC * M * 2;
+    static constexpr int STAGE = TILE_K + TILE_V;
+    static constexpr int NS_FIT = (int)((kSmemMax - 4096) / STAGE);
+    static constexpr int NS = NS_FIT > 4 ? 4 : NS_FIT;
+    static constexpr int OFF_ONES = NS * STAGE;
+    static constexpr int OFF_BAR = OFF_ONES + kOnesBytes;
+    static constexpr int NBARS = 3 * NS + 2;
+    static constexpr int OFF_TSLOT = OFF_BAR + 8 * NBARS;
+    static constexpr int SMEM = OFF_TSLOT + 16;
+    static constexpr uint32_t TMEM_COLS = 256;
+    static constexpr uint32_t COL_S = 0, COL_Z = M;
+};
+
+struct ReduceArgs {
+    float *ws;               // [BH, nslot, D*M + D]
+    const float *S_init;     // [BH, D, M] or null
+    const float *z_init;     // [BH, D] or null
+    int N;
+    int nslot;               // slots per head in ws
+    int nred;                // splits reduced per head (CTAs per head)
+    int cps;                 // chunks per split
+    int init_slot;           // -1: none
+    int *err;
+};
+
+template <int D, int M>
+__global__ void __launch_bounds__(kThreads, 1)
+state_reduce_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                    const ReduceArgs args)
+{
+    using C = RCfg<D, M>;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    volatile int *abort = reinterpret_cast<volatile int *>(smem + C::OFF_TSLOT + 4);
+    const int bh = blockIdx.x / args.nred, sp = blockIdx.x % args.nred;
+    const int nch_total = (args.N + kC - 1) / kC;
+    const int c_begin = sp * args.cps;
+    const int n = max(0, min(nch_total, c_begin + args.cps) - c_begin);
+
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
+    uint64_t *full = bar, *empty = bar + C::NS, *phi_done = bar + 2 * C::NS;
+    uint64_t *done = bar + 3 * C::NS, *init = done + 1;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + C::OFF_TSLOT);
+    uint8_t *ones = smem + C::OFF_ONES;
+
+    if (tid == 0) {
+        *abort = (smem_u32(smem) & 1023u) ? 1 : 0;
+        if (*abort) record_error(args.err, kErrTimeout);
+        for (int s = 0; s < C::NS; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+            mbar_init(&phi_done[s], kGrp);
+        }
+        mbar_init(done, 1);
+        mbar_init(init, kGrp);
         fence_mbar_init();
     }
     for (int i = tid; i < kOnesBytes / 4; i += kThreads) reinterpret_cast<uint32_t *>(ones)[i] = 0x3F803F80u;
@@ -250,320 +923,299 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     tc_fence_after();
     const uint32_t tmem = *tslot;
 
-    // Test hook: wait on a barrier that nothing arrives on, then give up.
-    if (args.inject_ns && tid == 0) {
-        if (!mbar_wait_bounded(bars.never, 0, now_ns() + args.inject_ns, nullptr)) set_abort(abort, args.err);
-    }
-    __syncthreads();
-
     if (warp == 0) {
-        // ------------------------------------------------------ producer
         if (lane == 0 && !*abort) {
-            prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
             int issued = 0;
             for (int it = 0; it < n; ++it) {
                 const int s = it % C::NS, k = it / C::NS;
-                if (it >= C::NS && !wait_bar(&bars.empty[s], (k - 1) & 1, abort)) break;
+                if (it >= C::NS && !wait_bar(&empty[s], (k - 1) & 1, abort)) break;
                 uint8_t *st = smem + s * C::STAGE;
                 const int t0 = (c_begin + it) * kC;
-                mbar_arrive_expect_tx(&bars.full[s], C::STAGE);
+                mbar_arrive_expect_tx(&full[s], C::STAGE);
 #pragma unroll
-                for (int j = 0; j < D / 64; ++j) tma_load_3d(st + j * kC * 128, &tm_q, &bars.full[s], j * 64, t0, bh);
-#pragma unroll
-                for (int j = 0; j < D / 64; ++j)
-                    tma_load_3d(st + C::TILE_QK + j * kC * 128, &tm_k, &bars.full[s], j * 64, t0, bh);
+                for (int j = 0; j < D / 64; ++j) tma_load_3d(st + j * kC * 128, &tm_k, &full[s], j * 64, t0, bh);
 #pragma unroll
                 for (int j = 0; j < M / 64; ++j)
-                    tma_load_3d(st + 2 * C::TILE_QK + j * kC * 128, &tm_v, &bars.full[s], j * 64, t0, bh);
+                    tma_load_3d(st + C::TILE_K + j * kC * 128, &tm_v, &full[s], j * 64, t0, bh);
                 ++issued;
             }
-            if (*abort) {
-                // let the copies in flight land before the CTA exits
-                const int first = max(0, issued - C::NS);
-                for (int it = first; it < issued; ++it)
-                    mbar_wait_bounded(&bars.full[it % C::NS], (it / C::NS) & 1, now_ns() + kWaitNs, nullptr);
-            }
+            if (*abort)
+                for (int it = max(0, issued - C::NS); it < issued; ++it)
+                    mbar_wait_bounded(&full[it % C::NS], (it / C::NS) & 1, now_ns() + kWaitNs, nullptr);
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------ MMA issuer
         if (lane == 0 && !*abort) {
-            constexpr uint32_t ID_P = idesc_bf16(128, kC, 0, 0);
-            constexpr uint32_t ID_O = idesc_bf16(128, M, 0, 1);
             constexpr uint32_t ID_S = idesc_bf16(128, M, 1, 1);
             constexpr uint32_t ID_Z = idesc_bf16(128, 16, 1, 1);
             const uint32_t ones_a = smem_u32(ones);
-            for (int it = 0; it < n; ++it) {
-                const int s = it % C::NS, k = it / C::NS;
-                const int pb = it % C::NPB, kb = it / C::NPB;
-                const uint32_t st = smem_u32(smem + s * C::STAGE);
-                const uint32_t qa = st, ka = st + C::TILE_QK, va = st + 2 * C::TILE_QK;
-                if (!wait_bar(&bars.phi[s], k & 1, abort)) break;
-                if (kb > 0) {
-                    // P buffer pb is free once the chunk that used it last has been read out
-                    if (C::O_IN_P) {
-                        if (!wait_bar(&bars.o_free[pb], (kb - 1) & 1, abort)) break;
-                    } else {
-                        if (!wait_bar(&bars.o_full[pb], (kb - 1) & 1, abort)) break;
-                    }
-                }
+            bool ok = wait_bar(init, 0, abort);   // accumulators zeroed
+            for (int it = 0; ok && it < n; ++it) {
+                const int s = it % C::NS;
+                if (!(ok = wait_bar(&phi_done[s], (it / C::NS) & 1, abort))) break;
                 tc_fence_after();
-                // P = phi(Q) phi(K)^T  (K-major A and B, K = D)
-#pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t off = (ks / 4) * kC * 128 + (ks % 4) * 32;
-                    mma_f16_ss(tmem + C::col_p(pb), smem_desc(qa + off, 16, 1024), smem_desc(ka + off, 16, 1024),
-                               ID_P, ks > 0);
-                }
-                mma_commit(&bars.p_full[pb]);
-                // snapshot of the state before this chunk is in shared memory
-                if (!wait_bar(bars.snap, it & 1, abort)) break;
-                if (C::O_IN_P) {
-                    if (!wait_bar(&bars.a_ready[pb], kb & 1, abort)) break;
-                } else if (it > 0) {
-                    if (!wait_bar(&bars.o_free[0], (it - 1) & 1, abort)) break;
-                }
-                tc_fence_after();
-                // O = phi(Q) S_prev   (A = phi(Q) K-major, B = S snapshot MN-major, K = D)
-                const uint32_t sa = smem_u32(snap);
-#pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    const uint32_t aoff = (ks / 4) * kC * 128 + (ks % 4) * 32;
-                    mma_f16_ss(tmem + C::col_o(pb), smem_desc(qa + aoff, 16, 1024),
-                               smem_desc(sa + ks * 2048, D * 128, 1024), ID_O, ks > 0);
-                }
-                // S += phi(K)^T V and z += phi(K)^T 1  (A = phi(K) read MN-major; M = 128 rows,
-                // rows >= D of the accumulator are never read)
+                const uint32_t ka = smem_u32(smem + s * C::STAGE), va = ka + C::TILE_K;
+                const uint64_t dk = smem_desc(ka, kC * 128, 1024), dv = smem_desc(va, kC * 128, 1024);
+                const uint64_t dones = ones_desc(ones_a);
 #pragma unroll
                 for (int ks = 0; ks < kC / 16; ++ks) {
-                    const uint64_t adesc = smem_desc(ka + ks * 2048, kC * 128, 1024);
-                    mma_f16_ss(tmem + C::COL_S, adesc, smem_desc(va + ks * 2048, kC * 128, 1024), ID_S, 1);
-                    mma_f16_ss(tmem + C::COL_Z, adesc, smem_desc(ones_a, 1024, 1024), ID_Z, 1);
+                    mma_f16_ss(tmem + C::COL_S, dk + mnmajor_step(ks), dv + mnmajor_step(ks), ID_S, 1);
+                    mma_f16_ss(tmem + C::COL_Z, dk + mnmajor_step(ks), dones, ID_Z, 1);
                 }
-                mma_commit(bars.s_full);
-                if (!C::O_IN_P && !wait_bar(&bars.a_ready[pb], kb & 1, abort)) break;
-                tc_fence_after();
-                // O += A V  (A = masked P as bf16 in TMEM, B = V MN-major, K = C)
-#pragma unroll
-                for (int ks = 0; ks < kC / 16; ++ks) {
-                    const uint64_t bdesc = smem_desc(va + ks * 2048, kC * 128, 1024);
-                    const uint32_t a_t = tmem + C::col_p(pb) + ks * 8;
-                    asm volatile(
-                        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-                        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(tmem + C::col_o(pb)),
-                        "r"(a_t), "l"(bdesc), "r"(ID_O), "r"(1)
-                        : "memory");
-                }
-                mma_commit(&bars.o_full[pb]);
-                mma_commit(&bars.empty[s]);
+                mma_commit(&empty[s]);
             }
-            // no MMA may still be running when the CTA frees its TMEM
-            mma_commit(bars.drain);
-            mbar_wait_bounded(bars.drain, 0, now_ns() + kWaitNs, nullptr);
+            mma_commit(done);
+            mbar_wait_bounded(done, 0, now_ns() + kWaitNs, nullptr);
         }
-    } else {
-        // ------------------------------------------------------ working group
-        const int t = tid - 64;
-        const int q4 = warp & 3;                 // TMEM lane quarter this warp may access
-        const int r = 32 * q4 + lane;            // chunk row / state row owned by this thread
+    } else if (warp < 6) {
+        const int q4 = warp & 3;
+        const int r = 32 * q4 + lane;
         const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
-        const bool srow = r < D;                 // owns a state row
-        const bool swarp = 32 * q4 < D;          // warp-uniform
-        const float *ws_h = args.seg_ws ? args.seg_ws + (size_t)bh * args.nseg * (D * M + D) : nullptr;
-        float *S_h = args.S ? args.S + (size_t)bh * D * M : nullptr;
-        float *z_h = args.z ? args.z + (size_t)bh * D : nullptr;
-        __nv_bfloat16 *out_h = args.out ? reinterpret_cast<__nv_bfloat16 *>(args.out) + (size_t)bh * args.N * M
-                                        : nullptr;
-
-        // initial state: carried-in state plus the sums of earlier segments
+        const bool swarp = 32 * q4 < D;
         if (swarp) {
-            float v[M];
-            float zr = 0.f;
+            float zero[32];
 #pragma unroll
-            for (int c = 0; c < M; ++c) v[c] = 0.f;
-            if (srow) {
-                if (S_h) {
-#pragma unroll
-                    for (int c = 0; c < M; c += 4) {
-                        const float4 x = *reinterpret_cast<const float4 *>(S_h + r * M + c);
-                        v[c] = x.x; v[c + 1] = x.y; v[c + 2] = x.z; v[c + 3] = x.w;
-                    }
-                    zr = z_h[r];
-                }
-                for (int g = 0; g < seg; ++g) {
-                    const float *src = ws_h + (size_t)g * (D * M + D);
-#pragma unroll
-                    for (int c = 0; c < M; c += 4) {
-                        const float4 x = *reinterpret_cast<const float4 *>(src + r * M + c);
-                        v[c] += x.x; v[c + 1] += x.y; v[c + 2] += x.z; v[c + 3] += x.w;
-                    }
-                    zr += src[D * M + r];
-                }
-                store_snap_row<D, M>(snap, r, v);
-                zs[r] = zr;
-            }
-#pragma unroll
-            for (int c0 = 0; c0 < M; c0 += 16) {
-                uint32_t w[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) w[j] = __float_as_uint(v[c0 + j]);
-                tmem_st16(tmem + lane_off + C::COL_S + c0, w);
-            }
-            uint32_t w[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) w[j] = 0u;
-            w[0] = __float_as_uint(zr);
-            tmem_st16(tmem + lane_off + C::COL_Z, w);
+            for (int j = 0; j < 32; ++j) zero[j] = 0.f;
+            for (int c0 = 0; c0 < M + 16; c0 += 32) tmem_st32f(tmem + lane_off + c0, zero);
             tmem_wait_st();
         }
         tc_fence_before();
-        fence_proxy_async();
-        mbar_arrive(bars.snap);
-
-        float den = 0.f;
-        // phi of the first chunk
-        if (n > 0) {
-            if (wait_bar(&bars.full[0], 0, abort)) {
-                uint8_t *st = smem;
-                const int valid = min(kC, args.N - c_begin * kC);
-                phi_tile<D>(st, t, kC);
-                phi_tile<D>(st + C::TILE_QK, t, valid);
-            }
-            fence_proxy_async();
-            mbar_arrive(&bars.phi[0]);
+        mbar_arrive(init);
+        float *dst = args.ws + ((size_t)bh * args.nslot + sp) * (D * M + D);
+        if (args.init_slot >= 0 && sp == 0 && r < D) {
+            float *di = args.ws + ((size_t)bh * args.nslot + args.init_slot) * (D * M + D);
+            const float *Si = args.S_init ? args.S_init + (size_t)bh * D * M : nullptr;
+            for (int c = 0; c < M; c += 4)
+                *reinterpret_cast<float4 *>(di + r * M + c) =
+                    Si ? *reinterpret_cast<const float4 *>(Si + r * M + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+            di[D * M + r] = args.z_init ? args.z_init[(size_t)bh * D + r] : 0.f;
         }
+        const bool ok = wait_bar_warp(done, 0, abort);
+        if (ok && swarp) {
+            tc_fence_after();
+#pragma unroll 1
+            for (int c0 = 0; c0 < M; c0 += 32) {
+                float v[32];
+                tmem_ld32f(tmem + lane_off + C::COL_S + c0, v);
+                if (r < D)
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4)
+                        *reinterpret_cast<float4 *>(dst + r * M + c0 + j) =
+                            make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+            }
+            uint32_t zv[16];
+            tmem_ld16(tmem + lane_off + C::COL_Z, zv);
+            tmem_wait_ld();
+            if (r < D) dst[D * M + r] = __uint_as_float(zv[0]);
+        }
+    } else {
+        const int t = tid - 64 - kGrp;
         for (int it = 0; it < n; ++it) {
             const int s = it % C::NS;
-            const int pb = it % C::NPB, kb = it / C::NPB;
-            const int t0 = (c_begin + it) * kC;
-            const int valid = min(kC, args.N - t0);
-            uint8_t *st = smem + s * C::STAGE;
-            // ---- P: mask j > r, row sums of the bf16-rounded values, back to TMEM as bf16
-            bool ok = wait_bar(&bars.p_full[pb], kb & 1, abort);
-            ok = __all_sync(0xffffffffu, ok);
-            if (ok) {
-                tc_fence_after();
-                float rs = 0.f;
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    uint32_t pv[64];
-#pragma unroll
-                    for (int j = 0; j < 4; ++j)
-                        tmem_ld16(tmem + lane_off + C::col_p(pb) + h * 64 + j * 16,
-                                  *reinterpret_cast<uint32_t(*)[16]>(&pv[j * 16]));
-                    tmem_wait_ld();
-                    uint32_t a[32];
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int c = h * 64 + 2 * j;
-                        const float x0 = (c <= r) ? __uint_as_float(pv[2 * j]) : 0.f;
-                        const float x1 = (c + 1 <= r) ? __uint_as_float(pv[2 * j + 1]) : 0.f;
-                        a[j] = pack_bf16x2(x0, x1);
-                        rs += bf16lo(a[j]) + bf16hi(a[j]);
-                    }
-                    tmem_st16(tmem + lane_off + C::col_p(pb) + h * 32, *reinterpret_cast<uint32_t(*)[16]>(&a[0]));
-                    tmem_st16(tmem + lane_off + C::col_p(pb) + h * 32 + 16,
-                              *reinterpret_cast<uint32_t(*)[16]>(&a[16]));
-                }
-                tmem_wait_st();
-                den = rs + q_dot_z<D>(st, r, zs);
-            }
-            tc_fence_before();
-            mbar_arrive(&bars.a_ready[pb]);
-            if (it + 1 < n) {
-                // ---- phi of the next chunk (lets the next P = phi(Q) phi(K)^T start early)
-                const int s1 = (it + 1) % C::NS, k1 = (it + 1) / C::NS;
-                if (wait_bar(&bars.full[s1], k1 & 1, abort)) {
-                    uint8_t *st1 = smem + s1 * C::STAGE;
-                    const int valid1 = min(kC, args.N - t0 - kC);
-                    phi_tile<D>(st1, t, kC);
-                    phi_tile<D>(st1 + C::TILE_QK, t, valid1);
-                }
-                fence_proxy_async();
-                mbar_arrive(&bars.phi[s1]);
-            }
-            wg_sync();   // every thread is done reading z_prev before it is replaced
-            if (it + 1 < n) {
-                // ---- snapshot of the state after this chunk, for the next chunk
-                bool ok2 = wait_bar(bars.s_full, it & 1, abort);
-                ok2 = __all_sync(0xffffffffu, ok2);
-                if (ok2 && swarp) {
-                    tc_fence_after();
-                    uint32_t sv[M];
-#pragma unroll
-                    for (int c0 = 0; c0 < M; c0 += 16)
-                        tmem_ld16(tmem + lane_off + C::COL_S + c0, *reinterpret_cast<uint32_t(*)[16]>(&sv[c0]));
-                    uint32_t zv[16];
-                    tmem_ld16(tmem + lane_off + C::COL_Z, zv);
-                    tmem_wait_ld();
-                    if (srow) {
-                        store_snap_row<D, M>(snap, r, reinterpret_cast<const float *>(sv));
-                        zs[r] = __uint_as_float(zv[0]);
-                    }
-                }
-                tc_fence_before();
-                fence_proxy_async();
-                mbar_arrive(bars.snap);
-            }
-            // ---- output rows
-            bool ok3 = wait_bar(&bars.o_full[pb], kb & 1, abort);
-            ok3 = __all_sync(0xffffffffu, ok3);
-            if (ok3) {
-                tc_fence_after();
-                uint32_t ov[M];
-#pragma unroll
-                for (int c0 = 0; c0 < M; c0 += 16)
-                    tmem_ld16(tmem + lane_off + C::col_o(pb) + c0, *reinterpret_cast<uint32_t(*)[16]>(&ov[c0]));
-                tmem_wait_ld();
-                tc_fence_before();
-                mbar_arrive(&bars.o_free[pb]);
-                if (out_h && r < valid) {
-                    const float inv = 1.f / den;
-                    uint4 *dst = reinterpret_cast<uint4 *>(out_h + (size_t)(t0 + r) * M);
-#pragma unroll
-                    for (int c = 0; c < M; c += 8) {
-                        uint4 w;
-                        w.x = pack_bf16x2(__uint_as_float(ov[c]) * inv, __uint_as_float(ov[c + 1]) * inv);
-                        w.y = pack_bf16x2(__uint_as_float(ov[c + 2]) * inv, __uint_as_float(ov[c + 3]) * inv);
-                        w.z = pack_bf16x2(__uint_as_float(ov[c + 4]) * inv, __uint_as_float(ov[c + 5]) * inv);
-                        w.w = pack_bf16x2(__uint_as_float(ov[c + 6]) * inv, __uint_as_float(ov[c + 7]) * inv);
-                        dst[c / 8] = w;
-                    }
-                }
-            } else {
-                tc_fence_before();
-                mbar_arrive(&bars.o_free[pb]);
-            }
-        }
-        // ---- final state of the sequence (last segment only)
-        if (S_h && seg == args.nseg - 1 && n > 0) {
-            bool ok4 = wait_bar(bars.s_full, (n - 1) & 1, abort);
-            ok4 = __all_sync(0xffffffffu, ok4);
-            if (ok4 && swarp) {
-                tc_fence_after();
-                uint32_t sv[M];
-#pragma unroll
-                for (int c0 = 0; c0 < M; c0 += 16)
-                    tmem_ld16(tmem + lane_off + C::COL_S + c0, *reinterpret_cast<uint32_t(*)[16]>(&sv[c0]));
-                uint32_t zv[16];
-                tmem_ld16(tmem + lane_off + C::COL_Z, zv);
-                tmem_wait_ld();
-                if (srow) {
-#pragma unroll
-                    for (int c = 0; c < M; c += 4)
-                        *reinterpret_cast<float4 *>(S_h + r * M + c) =
-                            make_float4(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1]),
-                                        __uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3]));
-                    z_h[r] = __uint_as_float(zv[0]);
-                }
-            }
+            if (wait_bar(&full[s], (it / C::NS) & 1, abort))
+                phi_tile<D>(smem + s * C::STAGE, t, min(kC, args.N - (c_begin + it) * kC));
+            fence_proxy_async();
+            mbar_arrive(&phi_done[s]);
         }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     if (warp == 0) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+// ------------------------------------------------------- read-out kernel
+// Non-causal read-out: S = sum of the splits' partial sums, then for every
+// query row V'_i = phi(Q_i)^T S / phi(Q_i)^T z (sec. 3.2 eq. (5)).
+
+template <int D, int M>
+struct OCfg {
+    static constexpr int TILE_Q = kC * D * 2;
+    static constexpr int SNAP = D * M * 2;
+    static constexpr int NS_FIT = (int)((kSmemMax - SNAP - D * 4 - 512) / TILE_Q);
+    static constexpr int NS = NS_FIT > 4 ? 4 : NS_FIT;
+    static constexpr int OFF_SNAP = NS * TILE_Q;
+    static constexpr int OFF_Z = OFF_SNAP + SNAP;
+    static constexpr int OFF_BAR = OFF_Z + D * 4;
+    static constexpr int NBARS = 3 * NS + 4 + 2;
+    static constexpr int OFF_TSLOT = OFF_BAR + 8 * NBARS;
+    static constexpr int SMEM = OFF_TSLOT + 16;
+    static constexpr uint32_t TMEM_COLS = 256;
+    static __device__ __forceinline__ uint32_t col_o(int b) { return (uint32_t)(b * M); }
+};
+
+struct ReadoutArgs {
+    void *out;               // [BH, N, M] bf16
+    const float *ws;         // [BH, nsplit, D*M + D]
+    int N;
+    int nsplit;
+    int nrb;                 // CTAs per head
+    int cpr;                 // chunks per CTA
+    int *err;
+};
+
+template <int D, int M>
+__global__ void __launch_bounds__(kThreads, 1)
+readout_kernel(const __grid_constant__ CUtensorMap tm_q, const ReadoutArgs args)
+{
+    using C = OCfg<D, M>;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    volatile int *abort = reinterpret_cast<volatile int *>(smem + C::OFF_TSLOT + 4);
+    const int bh = blockIdx.x / args.nrb, rb = blockIdx.x % args.nrb;
+    const int nch_total = (args.N + kC - 1) / kC;
+    const int c_begin = rb * args.cpr;
+    const int n = max(0, min(nch_total, c_begin + args.cpr) - c_begin);
+
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
+    uint64_t *full = bar, *empty = bar + C::NS, *phi_done = bar + 2 * C::NS;
+    uint64_t *o_full = bar + 3 * C::NS, *o_free = o_full + 2, *snap_bar = o_free + 2, *drain = snap_bar + 1;
+    uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + C::OFF_TSLOT);
+    uint8_t *snap = smem + C::OFF_SNAP;
+    float *zs = reinterpret_cast<float *>(smem + C::OFF_Z);
+
+    if (tid == 0) {
+        *abort = (smem_u32(smem) & 1023u) ? 1 : 0;
+        if (*abort) record_error(args.err, kErrTimeout);
+        for (int s = 0; s < C::NS; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kGrp);   // released by the epilogue after its last read of phi(Q)
+            mbar_init(&phi_done[s], kGrp);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&o_full[b], 1);
+            mbar_init(&o_free[b], kGrp);
+        }
+        mbar_init(snap_bar, kGrp);
+        mbar_init(drain, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(tslot, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+
+    if (warp == 0) {
+        if (lane == 0 && !*abort) {
+            prefetch_tmap(&tm_q);
+            int issued = 0;
+            for (int it = 0; it < n; ++it) {
+                const int s = it % C::NS, k = it / C::NS;
+                if (it >= C::NS && !wait_bar(&empty[s], (k - 1) & 1, abort)) break;
+                uint8_t *st = smem + s * C::TILE_Q;
+                mbar_arrive_expect_tx(&full[s], C::TILE_Q);
+#pragma unroll
+                for (int j = 0; j < D / 64; ++j)
+                    tma_load_3d(st + j * kC * 128, &tm_q, &full[s], j * 64, (c_begin + it) * kC, bh);
+                ++issued;
+            }
+            if (*abort)
+                for (int it = max(0, issued - C::NS); it < issued; ++it)
+                    mbar_wait_bounded(&full[it % C::NS], (it / C::NS) & 1, now_ns() + kWaitNs, nullptr);
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && !*abort) {
+            constexpr uint32_t ID_O = idesc_bf16(128, M, 0, 1);
+            const uint32_t snap_a = smem_u32(snap);
+            bool ok = wait_bar(snap_bar, 0, abort);
+            for (int it = 0; ok && it < n; ++it) {
+                const int s = it % C::NS, ob = it & 1;
+                if (!(ok = wait_bar(&phi_done[s], (it / C::NS) & 1, abort))) break;
+                if (it >= 2 && !(ok = wait_bar(&o_free[ob], ((it >> 1) - 1) & 1, abort))) break;
+                tc_fence_after();
+                const uint64_t dq = kmajor_base(smem_u32(smem + s * C::TILE_Q));
+                const uint64_t ds = smem_desc(snap_a, D * 128, 1024);
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks)
+                    mma_f16_ss(tmem + C::col_o(ob), dq + kmajor_step(ks), ds + mnmajor_step(ks), ID_O, ks > 0);
+                mma_commit(&o_full[ob]);
+            }
+            mma_commit(drain);
+            mbar_wait_bounded(drain, 0, now_ns() + kWaitNs, nullptr);
+        }
+    } else if (warp < 6) {
+        const int q4 = warp & 3;
+        const int r = 32 * q4 + lane;
+        const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
+        if (r < D) {
+            const float *src = args.ws + (size_t)bh * args.nsplit * (D * M + D);
+            float zr = 0.f;
+            for (int g = 0; g < args.nsplit; ++g) zr += src[(size_t)g * (D * M + D) + D * M + r];
+            zs[r] = zr;
+#pragma unroll 1
+            for (int c0 = 0; c0 < M; c0 += 32) {
+                float v[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = 0.f;
+                for (int g = 0; g < args.nsplit; ++g) {
+                    const float *p = src + (size_t)g * (D * M + D) + r * M + c0;
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4) {
+                        const float4 x = *reinterpret_cast<const float4 *>(p + j);
+                        v[j] += x.x; v[j + 1] += x.y; v[j + 2] += x.z; v[j + 3] += x.w;
+                    }
+                }
+                store_snap32<D>(snap, r, c0, v);
+            }
+        }
+        fence_proxy_async();
+        mbar_arrive(snap_bar);
+        epi_sync();   // z in shared memory is complete
+        __nv_bfloat16 *out_h = reinterpret_cast<__nv_bfloat16 *>(args.out) + (size_t)bh * args.N * M;
+        for (int it = 0; it < n; ++it) {
+            const int s = it % C::NS, ob = it & 1;
+            const int t0 = (c_begin + it) * kC;
+            const int valid = min(kC, args.N - t0);
+            const bool ok = wait_bar_warp(&o_full[ob], (it >> 1) & 1, abort);
+            if (ok) {
+                tc_fence_after();
+                const float inv = 1.f / q_dot_z<D>(smem + s * C::TILE_Q, r, zs);
+#pragma unroll 1
+                for (int c0 = 0; c0 < M; c0 += 32) {
+                    float o[32];
+                    tmem_ld32f(tmem + lane_off + C::col_o(ob) + c0, o);
+                    if (r < valid) store_out32(out_h + (size_t)(t0 + r) * M + c0, o, inv);
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&o_free[ob]);
+            mbar_arrive(&empty[s]);
+        }
+    } else {
+        const int t = tid - 64 - kGrp;
+        for (int it = 0; it < n; ++it) {
+            const int s = it % C::NS;
+            if (wait_bar(&full[s], (it / C::NS) & 1, abort)) phi_tile<D>(smem + s * C::TILE_Q, t, kC);
+            fence_proxy_async();
+            mbar_arrive(&phi_done[s]);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+// ---------------------------------------------------------------- launchers
+
+template <typename K>
+cudaError_t set_smem(K kernel, int bytes) {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+}
+
+// Segments per head for the causal kernel: enough CTAs to cover the SMs
+// (one CTA per SM), at least 8 chunks per segment.
+int causal_nseg(long long BH, int N, int sm_count) {
+    const long long nch = (N + kC - 1) / kC;
+    if (BH >= (long long)sm_count * 3 / 4) return 1;
+    long long nseg = std::max(1LL, (long long)sm_count / BH);
+    nseg = std::min(nseg, std::max(1LL, nch / 8));
+    return (int)nseg;
 }
 
 template <int D, int M>
@@ -573,31 +1225,91 @@ cudaError_t launch_causal(const Problem &p, const DeviceInfo &dev) {
     if (!make_tmap_bf16_3d(&tq, p.q, D, p.N, p.BH, 64, kC) || !make_tmap_bf16_3d(&tk, p.k, D, p.N, p.BH, 64, kC) ||
         !make_tmap_bf16_3d(&tv, p.v, M, p.N, p.BH, 64, kC))
         return cudaErrorInvalidValue;
+    const int nch = (p.N + kC - 1) / kC;
+    int nseg = causal_nseg(p.BH, p.N, dev.sm_count);
+    const int cps = (nch + nseg - 1) / nseg;
+    nseg = (nch + cps - 1) / cps;
+    cudaError_t e;
+    if (nseg > 1) {
+        if (p.ws_bytes < (size_t)p.BH * nseg * (D * M + D) * sizeof(float)) return cudaErrorInvalidValue;
+        ReduceArgs r{(float *)p.ws, p.S, p.z, p.N, nseg, nseg - 1, cps, nseg - 1, dev.err_word};
+        if ((e = set_smem(state_reduce_kernel<D, M>, RCfg<D, M>::SMEM)) != cudaSuccess) return e;
+        state_reduce_kernel<D, M><<<(unsigned)(p.BH * (nseg - 1)), kThreads, RCfg<D, M>::SMEM, p.stream>>>(tk, tv, r);
+        count_launches(1);
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    }
+    CUtensorMap to;
+    if (p.out && !make_tmap_bf16_3d(&to, p.out, M, p.N, p.BH, 64, kC)) return cudaErrorInvalidValue;
+    if (!p.out) to = tq;   // never used
     CausalArgs a;
-    a.out = p.out;
+    a.has_out = p.out != nullptr;
     a.S = p.S;
     a.z = p.z;
-    a.seg_ws = nullptr;
+    a.seg_ws = nseg > 1 ? (const float *)p.ws : nullptr;
     a.N = p.N;
-    a.nseg = 1;
-    a.cps = (p.N + kC - 1) / kC;
+    a.nseg = nseg;
+    a.cps = cps;
     a.err = dev.err_word;
     a.inject_ns = g_inject_timeout ? (uint64_t)g_inject_limit_us * 1000ull : 0ull;
-    cudaError_t e = cudaFuncSetAttribute(causal_tc_kernel<D, M>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    causal_tc_kernel<D, M><<<(unsigned)(p.BH * a.nseg), kThreads, C::SMEM, p.stream>>>(tq, tk, tv, a);
+    if ((e = set_smem(causal_tc_kernel<D, M>, C::SMEM)) != cudaSuccess) return e;
+    causal_tc_kernel<D, M><<<(unsigned)(p.BH * nseg), kThreadsCausal, C::SMEM, p.stream>>>(tq, tk, tv, to, a);
     count_launches(1);
     return cudaGetLastError();
 }
 
-}  // namespace
-
-bool tc_causal_supported(const la_shape &s, int chunk) {
-    return s.dtype == LA_DTYPE_BF16 && (s.D == 64 || s.D == 128) && (s.M == 64 || s.M == 128) &&
-           (chunk == 0 || chunk == 128);
+// Splits of the non-causal reduction and row blocks of the read-out, each
+// sized so that the grid covers the SMs once.
+void nc_grid(long long BH, int N, int sm_count, int &nsplit, int &cps, int &nrb, int &cpr) {
+    const int nch = (N + kC - 1) / kC;
+    const int want = (int)std::max(1LL, (long long)sm_count / std::max(1LL, BH));
+    nsplit = std::max(1, std::min(want, nch));
+    cps = (nch + nsplit - 1) / nsplit;
+    nsplit = (nch + cps - 1) / cps;
+    nrb = std::max(1, std::min(want, nch));
+    cpr = (nch + nrb - 1) / nrb;
+    nrb = (nch + cpr - 1) / cpr;
 }
 
-size_t tc_causal_ws_bytes(const la_shape &, int) { return 0; }
+template <int D, int M>
+cudaError_t launch_noncausal(const Problem &p, const DeviceInfo &dev) {
+    CUtensorMap tq, tk, tv;
+    if (!make_tmap_bf16_3d(&tq, p.q, D, p.N, p.BH, 64, kC) || !make_tmap_bf16_3d(&tk, p.k, D, p.N, p.BH, 64, kC) ||
+        !make_tmap_bf16_3d(&tv, p.v, M, p.N, p.BH, 64, kC))
+        return cudaErrorInvalidValue;
+    int nsplit, cps, nrb, cpr;
+    nc_grid(p.BH, p.N, dev.sm_count, nsplit, cps, nrb, cpr);
+    if (p.ws_bytes < (size_t)p.BH * nsplit * (D * M + D) * sizeof(float)) return cudaErrorInvalidValue;
+    cudaError_t e;
+    ReduceArgs r{(float *)p.ws, nullptr, nullptr, p.N, nsplit, nsplit, cps, -1, dev.err_word};
+    if ((e = set_smem(state_reduce_kernel<D, M>, RCfg<D, M>::SMEM)) != cudaSuccess) return e;
+    state_reduce_kernel<D, M><<<(unsigned)(p.BH * nsplit), kThreads, RCfg<D, M>::SMEM, p.stream>>>(tk, tv, r);
+    count_launches(1);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    ReadoutArgs o{p.out, (const float *)p.ws, p.N, nsplit, nrb, cpr, dev.err_word};
+    if ((e = set_smem(readout_kernel<D, M>, OCfg<D, M>::SMEM)) != cudaSuccess) return e;
+    readout_kernel<D, M><<<(unsigned)(p.BH * nrb), kThreads, OCfg<D, M>::SMEM, p.stream>>>(tq, o);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+bool tc_dims(const la_shape &s) {
+    return s.dtype == LA_DTYPE_BF16 && (s.D == 64 || s.D == 128) && (s.M == 64 || s.M == 128);
+}
+
+}  // namespace
+
+bool tc_causal_supported(const la_shape &s, int chunk) { return tc_dims(s) && (chunk == 0 || chunk == 128); }
+
+size_t tc_causal_ws_bytes(const la_shape &s, int) {
+    // Sized for the most segments any device picks (one CTA per SM, up to
+    // 192 SMs assumed; never more than one segment per 8 chunks).
+    const long long BH = (long long)s.B * s.H;
+    if (BH <= 0 || s.N <= 0) return 0;
+    const long long nch = (s.N + kC - 1) / kC;
+    const long long nseg = std::min(std::max(1LL, 192LL / BH), std::max(1LL, nch / 8));
+    if (nseg <= 1) return 0;
+    return (size_t)BH * nseg * ((size_t)s.D * s.M + s.D) * sizeof(float);
+}
 
 cudaError_t tc_causal(const Problem &p, const DeviceInfo &dev) {
     if (p.D == 64 && p.M == 64) return launch_causal<64, 64>(p, dev);
@@ -607,8 +1319,22 @@ cudaError_t tc_causal(const Problem &p, const DeviceInfo &dev) {
     return cudaErrorInvalidValue;
 }
 
-bool tc_noncausal_supported(const la_shape &) { return false; }
-size_t tc_noncausal_ws_bytes(const la_shape &) { return 0; }
-cudaError_t tc_noncausal(const Problem &, const DeviceInfo &) { return cudaErrorNotSupported; }
+bool tc_noncausal_supported(const la_shape &s) { return tc_dims(s); }
+
+size_t tc_noncausal_ws_bytes(const la_shape &s) {
+    const long long BH = (long long)s.B * s.H;
+    if (BH <= 0 || s.N <= 0) return 0;
+    const long long nch = (s.N + kC - 1) / kC;
+    const long long nsplit = std::min(std::max(1LL, 192LL / BH), nch);
+    return (size_t)BH * nsplit * ((size_t)s.D * s.M + s.D) * sizeof(float);
+}
+
+cudaError_t tc_noncausal(const Problem &p, const DeviceInfo &dev) {
+    if (p.D == 64 && p.M == 64) return launch_noncausal<64, 64>(p, dev);
+    if (p.D == 64 && p.M == 128) return launch_noncausal<64, 128>(p, dev);
+    if (p.D == 128 && p.M == 64) return launch_noncausal<128, 64>(p, dev);
+    if (p.D == 128 && p.M == 128) return launch_noncausal<128, 128>(p, dev);
+    return cudaErrorInvalidValue;
+}
 
 }  // namespace la
