@@ -285,7 +285,10 @@ def run_ours(args, rank, world, dist):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1)/sqrt(D) bf16; no dataset)",
         "config": {"workload": MAIN, "B": w.B, "H": w.H, "N": w.N, "D": w.D, "M": w.M,
-                   "chunk": w.chunk, "global_batch": w.B * world, "seq_len": w.N,
+                   "chunk": w.chunk, "chunk_configured": 64,
+                   "chunk_note": "tensor-core path regroups by 128-row chunks (one tcgen05 M=128 tile); "
+                                 "same sums as C=64 in exact arithmetic",
+                   "global_batch": w.B * world, "seq_len": w.N,
                    "parallelism": "dp%d (independent heads per rank)" % world,
                    "l2": "flushed between timed steps (2x L2 write)"},
         "roofline": roofline, "tensor": tensor, "clocks": clocks, "gpu_launches": launches,
@@ -443,7 +446,7 @@ def cpu_baseline(w, budget_s=4.0):
     dt = (time.perf_counter() - t0) / reps
     head_tokens_per_s = heads * w.N / dt
     return {"value": round(head_tokens_per_s / w.H, 1), "unit": "tokens/s", "cores": nthreads, "kind": "oracle",
-            "sample": "%d of %d heads x N=%d (fp64 recurrence, eqs. 10-12), %d reps; tokens/s = head-tokens/s / H"
+            "sample": "%d of %d heads x N=%d (fp64 recurrence), %d reps; tokens/s = head-tokens/s / H"
                       % (heads, w.B * w.H, w.N, reps)}
 
 

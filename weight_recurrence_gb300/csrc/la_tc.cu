@@ -39,6 +39,9 @@
 // Every mbarrier wait is bounded; a CTA that gives up records LA_ERR_TIMEOUT,
 // lets its copies and MMAs drain, frees its TMEM and returns.
 #include <algorithm>
+#include <mutex>
+#include <utility>
+#include <vector>
 
 #include "la_common.cuh"
 #include "la_internal.h"
@@ -204,20 +207,6 @@ __device__ __forceinline__ void tmem_st32f(uint32_t taddr, const float (&v)[32])
     }
     tmem_st16(taddr, a);
     tmem_st16(taddr + 16, b);
-}
-
-// Stores 32 outputs (scaled by inv) of one row as bf16.
-__device__ __forceinline__ void store_out32(__nv_bfloat16 *dst, const float (&v)[32], float inv) {
-    uint4 *d = reinterpret_cast<uint4 *>(dst);
-#pragma unroll
-    for (int c = 0; c < 32; c += 8) {
-        uint4 w;
-        w.x = pack_bf16x2(v[c] * inv, v[c + 1] * inv);
-        w.y = pack_bf16x2(v[c + 2] * inv, v[c + 3] * inv);
-        w.z = pack_bf16x2(v[c + 4] * inv, v[c + 5] * inv);
-        w.w = pack_bf16x2(v[c + 6] * inv, v[c + 7] * inv);
-        d[c / 8] = w;
-    }
 }
 
 // A (TMEM) x B (shared memory) MMA, kind::f16.
@@ -850,17 +839,20 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 // over the split's chunks, in fp32, into ws[bh][split] = (S row-major, z).
 // The CTA of split 0 can also copy a carried-in state (or zeros) into slot
 // init_slot, so that the causal kernel's segments read their starting state
-// from the workspace only.
+// from the workspace only.  Two CTAs share an SM.
 
 template <int D, int M>
 struct RCfg {
     static constexpr int TILE_K = kC * D * 2;
     static constexpr int TILE_V = kC * M * 2;
     static constexpr int STAGE = TILE_K + TILE_V;
-    static constexpr int NS_FIT = (int)((kSmemMax - 4096) / STAGE);
-    static constexpr int NS = NS_FIT > 4 ? 4 : NS_FIT;
+    static constexpr bool VONES = (M == 64);           // V read as [V | ones], z in column M
+    static constexpr int ONES = VONES ? kC * 128 : kOnesBytes;
+    static constexpr int BUDGET = (int)kSmemMax / 2 - 1024;   // two CTAs per SM
+    static constexpr int NS_FIT = (BUDGET - ONES - 256) / STAGE;
+    static constexpr int NS = NS_FIT > 4 ? 4 : (NS_FIT < 2 ? 2 : NS_FIT);
     static constexpr int OFF_ONES = NS * STAGE;
-    static constexpr int OFF_BAR = OFF_ONES + kOnesBytes;
+    static constexpr int OFF_BAR = OFF_ONES + ONES;
     static constexpr int NBARS = 3 * NS + 2;
     static constexpr int OFF_TSLOT = OFF_BAR + 8 * NBARS;
     static constexpr int SMEM = OFF_TSLOT + 16;
@@ -881,7 +873,7 @@ struct ReduceArgs {
 };
 
 template <int D, int M>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kThreads, 2)
 state_reduce_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
                     const ReduceArgs args)
 {
@@ -912,7 +904,10 @@ state_reduce_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         mbar_init(init, kGrp);
         fence_mbar_init();
     }
-    for (int i = tid; i < kOnesBytes / 4; i += kThreads) reinterpret_cast<uint32_t *>(ones)[i] = 0x3F803F80u;
+    // ones operand (MN-major, ones in column 0)
+    for (int i = tid; i < C::ONES / 4; i += kThreads) reinterpret_cast<uint32_t *>(ones)[i] = 0u;
+    __syncthreads();
+    for (int k = tid; k < C::ONES / 128; k += kThreads) *reinterpret_cast<uint16_t *>(ones + sw128_offset(k, 0)) = 0x3F80u;
     if (warp == 0) {
         tmem_alloc(tslot, C::TMEM_COLS);
         tmem_relinquish();
@@ -947,7 +942,7 @@ state_reduce_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         }
     } else if (warp == 1) {
         if (lane == 0 && !*abort) {
-            constexpr uint32_t ID_S = idesc_bf16(128, M, 1, 1);
+            constexpr uint32_t ID_S = idesc_bf16(128, C::VONES ? M + 16 : M, 1, 1);
             constexpr uint32_t ID_Z = idesc_bf16(128, 16, 1, 1);
             const uint32_t ones_a = smem_u32(ones);
             bool ok = wait_bar(init, 0, abort);   // accumulators zeroed
@@ -956,12 +951,13 @@ state_reduce_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
                 if (!(ok = wait_bar(&phi_done[s], (it / C::NS) & 1, abort))) break;
                 tc_fence_after();
                 const uint32_t ka = smem_u32(smem + s * C::STAGE), va = ka + C::TILE_K;
-                const uint64_t dk = smem_desc(ka, kC * 128, 1024), dv = smem_desc(va, kC * 128, 1024);
+                const uint64_t dk = smem_desc(ka, kC * 128, 1024);
+                const uint64_t dv = smem_desc(va, C::VONES ? ones_a - va : (uint32_t)(kC * 128), 1024);
                 const uint64_t dones = ones_desc(ones_a);
 #pragma unroll
                 for (int ks = 0; ks < kC / 16; ++ks) {
                     mma_f16_ss(tmem + C::COL_S, dk + mnmajor_step(ks), dv + mnmajor_step(ks), ID_S, 1);
-                    mma_f16_ss(tmem + C::COL_Z, dk + mnmajor_step(ks), dones, ID_Z, 1);
+                    if (!C::VONES) mma_f16_ss(tmem + C::COL_Z, dk + mnmajor_step(ks), dones, ID_Z, 1);
                 }
                 mma_commit(&empty[s]);
             }
@@ -1027,26 +1023,32 @@ state_reduce_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
 
 // ------------------------------------------------------- read-out kernel
 // Non-causal read-out: S = sum of the splits' partial sums, then for every
-// query row V'_i = phi(Q_i)^T S / phi(Q_i)^T z (sec. 3.2 eq. (5)).
+// query row V'_i = phi(Q_i)^T S / phi(Q_i)^T z (sec. 3.2 eq. (5)).  The
+// snapshot is read as [S | z_hi z_lo] so that one MMA yields numerator and
+// denominator; output tiles are staged in the (dead) Q tile of their stage and
+// stored by TMA.  Two CTAs share an SM.
 
 template <int D, int M>
 struct OCfg {
     static constexpr int TILE_Q = kC * D * 2;
-    static constexpr int SNAP = D * M * 2;
-    static constexpr int NS_FIT = (int)((kSmemMax - SNAP - D * 4 - 512) / TILE_Q);
-    static constexpr int NS = NS_FIT > 4 ? 4 : NS_FIT;
-    static constexpr int OFF_SNAP = NS * TILE_Q;
-    static constexpr int OFF_Z = OFF_SNAP + SNAP;
-    static constexpr int OFF_BAR = OFF_Z + D * 4;
+    static constexpr int SNAP = D * M * 2 + D * 128;   // M/64 state atoms then the z atom
+    static_assert(kC * M * 2 <= TILE_Q * 2, "output tile fits in the Q tiles of a stage");
+    static constexpr int STAGE = TILE_Q >= kC * M * 2 ? TILE_Q : kC * M * 2;
+    static constexpr int BUDGET = (int)kSmemMax / 2 - 1024;
+    static constexpr int NS_FIT = (BUDGET - SNAP - 256) / STAGE;
+    static constexpr int NS = NS_FIT > 4 ? 4 : (NS_FIT < 2 ? 2 : NS_FIT);
+    static constexpr int OFF_SNAP = NS * STAGE;
+    static constexpr int OFF_BAR = OFF_SNAP + SNAP;
     static constexpr int NBARS = 3 * NS + 4 + 2;
     static constexpr int OFF_TSLOT = OFF_BAR + 8 * NBARS;
     static constexpr int SMEM = OFF_TSLOT + 16;
+    static constexpr int NO = M + 16;                   // O columns per buffer (numerator, z_hi, z_lo)
+    static constexpr int NOBUF = 2 * NO <= 256 ? 2 : 1; // O buffers within 256 TMEM columns
     static constexpr uint32_t TMEM_COLS = 256;
-    static __device__ __forceinline__ uint32_t col_o(int b) { return (uint32_t)(b * M); }
+    static __device__ __forceinline__ uint32_t col_o(int b) { return (uint32_t)(b * NO); }
 };
 
 struct ReadoutArgs {
-    void *out;               // [BH, N, M] bf16
     const float *ws;         // [BH, nsplit, D*M + D]
     int N;
     int nsplit;
@@ -1056,8 +1058,9 @@ struct ReadoutArgs {
 };
 
 template <int D, int M>
-__global__ void __launch_bounds__(kThreads, 1)
-readout_kernel(const __grid_constant__ CUtensorMap tm_q, const ReadoutArgs args)
+__global__ void __launch_bounds__(kThreads, 2)
+readout_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_o,
+               const ReadoutArgs args)
 {
     using C = OCfg<D, M>;
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -1073,14 +1076,13 @@ readout_kernel(const __grid_constant__ CUtensorMap tm_q, const ReadoutArgs args)
     uint64_t *o_full = bar + 3 * C::NS, *o_free = o_full + 2, *snap_bar = o_free + 2, *drain = snap_bar + 1;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + C::OFF_TSLOT);
     uint8_t *snap = smem + C::OFF_SNAP;
-    float *zs = reinterpret_cast<float *>(smem + C::OFF_Z);
 
     if (tid == 0) {
         *abort = (smem_u32(smem) & 1023u) ? 1 : 0;
         if (*abort) record_error(args.err, kErrTimeout);
         for (int s = 0; s < C::NS; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kGrp);   // released by the epilogue after its last read of phi(Q)
+            mbar_init(&empty[s], 1);      // released by the epilogue after the store read its tile
             mbar_init(&phi_done[s], kGrp);
         }
         for (int b = 0; b < 2; ++b) {
@@ -1107,7 +1109,7 @@ readout_kernel(const __grid_constant__ CUtensorMap tm_q, const ReadoutArgs args)
             for (int it = 0; it < n; ++it) {
                 const int s = it % C::NS, k = it / C::NS;
                 if (it >= C::NS && !wait_bar(&empty[s], (k - 1) & 1, abort)) break;
-                uint8_t *st = smem + s * C::TILE_Q;
+                uint8_t *st = smem + s * C::STAGE;
                 mbar_arrive_expect_tx(&full[s], C::TILE_Q);
 #pragma unroll
                 for (int j = 0; j < D / 64; ++j)
@@ -1120,15 +1122,15 @@ readout_kernel(const __grid_constant__ CUtensorMap tm_q, const ReadoutArgs args)
         }
     } else if (warp == 1) {
         if (lane == 0 && !*abort) {
-            constexpr uint32_t ID_O = idesc_bf16(128, M, 0, 1);
+            constexpr uint32_t ID_O = idesc_bf16(128, C::NO, 0, 1);
             const uint32_t snap_a = smem_u32(snap);
             bool ok = wait_bar(snap_bar, 0, abort);
             for (int it = 0; ok && it < n; ++it) {
-                const int s = it % C::NS, ob = it & 1;
+                const int s = it % C::NS, ob = it % C::NOBUF, kb = it / C::NOBUF;
                 if (!(ok = wait_bar(&phi_done[s], (it / C::NS) & 1, abort))) break;
-                if (it >= 2 && !(ok = wait_bar(&o_free[ob], ((it >> 1) - 1) & 1, abort))) break;
+                if (kb > 0 && !(ok = wait_bar(&o_free[ob], (kb - 1) & 1, abort))) break;
                 tc_fence_after();
-                const uint64_t dq = kmajor_base(smem_u32(smem + s * C::TILE_Q));
+                const uint64_t dq = kmajor_base(smem_u32(smem + s * C::STAGE));
                 const uint64_t ds = smem_desc(snap_a, D * 128, 1024);
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks)
@@ -1142,11 +1144,19 @@ readout_kernel(const __grid_constant__ CUtensorMap tm_q, const ReadoutArgs args)
         const int q4 = warp & 3;
         const int r = 32 * q4 + lane;
         const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
+        const bool leader = tid == 64;
+        // the state: sum of the splits, as bf16 [S | z_hi z_lo] (atoms D*128 bytes apart)
         if (r < D) {
             const float *src = args.ws + (size_t)bh * args.nsplit * (D * M + D);
             float zr = 0.f;
             for (int g = 0; g < args.nsplit; ++g) zr += src[(size_t)g * (D * M + D) + D * M + r];
-            zs[r] = zr;
+            uint8_t *za = snap + (M / 64) * D * 128;
+            for (int c = 0; c < 64; c += 8)
+                *reinterpret_cast<uint4 *>(za + sw128_offset(r, c)) = make_uint4(0u, 0u, 0u, 0u);
+            const __nv_bfloat16 hi = __float2bfloat16_rn(zr);
+            const __nv_bfloat16 lo = __float2bfloat16_rn(zr - __bfloat162float(hi));
+            *reinterpret_cast<__nv_bfloat16 *>(za + sw128_offset(r, 0)) = hi;
+            *reinterpret_cast<__nv_bfloat16 *>(za + sw128_offset(r, 1)) = lo;
 #pragma unroll 1
             for (int c0 = 0; c0 < M; c0 += 32) {
                 float v[32];
@@ -1165,32 +1175,54 @@ readout_kernel(const __grid_constant__ CUtensorMap tm_q, const ReadoutArgs args)
         }
         fence_proxy_async();
         mbar_arrive(snap_bar);
-        epi_sync();   // z in shared memory is complete
-        __nv_bfloat16 *out_h = reinterpret_cast<__nv_bfloat16 *>(args.out) + (size_t)bh * args.N * M;
+        if (leader) prefetch_tmap(&tm_o);
         for (int it = 0; it < n; ++it) {
-            const int s = it % C::NS, ob = it & 1;
+            const int s = it % C::NS, ob = it % C::NOBUF, kb = it / C::NOBUF;
             const int t0 = (c_begin + it) * kC;
-            const int valid = min(kC, args.N - t0);
-            const bool ok = wait_bar_warp(&o_full[ob], (it >> 1) & 1, abort);
+            uint8_t *tile = smem + s * C::STAGE;   // phi(Q) is dead once o_full fires
+            const bool ok = wait_bar_warp(&o_full[ob], kb & 1, abort);
             if (ok) {
                 tc_fence_after();
-                const float inv = 1.f / q_dot_z<D>(smem + s * C::TILE_Q, r, zs);
+                uint32_t dv[16];
+                tmem_ld16(tmem + lane_off + C::col_o(ob) + M, dv);
+                tmem_wait_ld();
+                const float inv = 1.f / (__uint_as_float(dv[0]) + __uint_as_float(dv[1]));
 #pragma unroll 1
                 for (int c0 = 0; c0 < M; c0 += 32) {
                     float o[32];
                     tmem_ld32f(tmem + lane_off + C::col_o(ob) + c0, o);
-                    if (r < valid) store_out32(out_h + (size_t)(t0 + r) * M + c0, o, inv);
+#pragma unroll
+                    for (int c8 = 0; c8 < 4; ++c8) {
+                        const int c = c0 + 8 * c8;
+                        uint4 w;
+                        w.x = pack_bf16x2(o[8 * c8] * inv, o[8 * c8 + 1] * inv);
+                        w.y = pack_bf16x2(o[8 * c8 + 2] * inv, o[8 * c8 + 3] * inv);
+                        w.z = pack_bf16x2(o[8 * c8 + 4] * inv, o[8 * c8 + 5] * inv);
+                        w.w = pack_bf16x2(o[8 * c8 + 6] * inv, o[8 * c8 + 7] * inv);
+                        *reinterpret_cast<uint4 *>(tile + (c / 64) * kC * 128 + sw128_offset(r, c % 64)) = w;
+                    }
                 }
             }
             tc_fence_before();
             mbar_arrive(&o_free[ob]);
-            mbar_arrive(&empty[s]);
+            fence_proxy_async();
+            epi_sync();
+            if (leader) {
+                if (ok) {
+#pragma unroll
+                    for (int j = 0; j < M / 64; ++j) tma_store_3d(&tm_o, tile + j * kC * 128, j * 64, t0, bh);
+                    tma_store_commit();
+                    tma_store_wait_read0();
+                }
+                mbar_arrive(&empty[s]);
+            }
         }
+        if (leader) tma_store_wait_all0();
     } else {
         const int t = tid - 64 - kGrp;
         for (int it = 0; it < n; ++it) {
             const int s = it % C::NS;
-            if (wait_bar(&full[s], (it / C::NS) & 1, abort)) phi_tile<D>(smem + s * C::TILE_Q, t, kC);
+            if (wait_bar(&full[s], (it / C::NS) & 1, abort)) phi_tile<D>(smem + s * C::STAGE, t, kC);
             fence_proxy_async();
             mbar_arrive(&phi_done[s]);
         }
@@ -1203,9 +1235,22 @@ readout_kernel(const __grid_constant__ CUtensorMap tm_q, const ReadoutArgs args)
 
 // ---------------------------------------------------------------- launchers
 
+// Opts a kernel in to `bytes` of dynamic shared memory, once per (kernel,
+// device): the memo is keyed by the kernel's address, since all instances
+// of a kernel template share one function type.
 template <typename K>
 cudaError_t set_smem(K kernel, int bytes) {
-    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    static std::mutex mu;
+    static std::vector<std::pair<const void *, int>> done;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+    const void *key = reinterpret_cast<const void *>(kernel);
+    std::lock_guard<std::mutex> lock(mu);
+    for (const auto &d : done)
+        if (d.first == key && d.second == dev) return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) done.emplace_back(key, dev);
+    return e;
 }
 
 // Segments per head for the causal kernel: enough CTAs to cover the SMs
@@ -1222,8 +1267,8 @@ template <int D, int M>
 cudaError_t launch_causal(const Problem &p, const DeviceInfo &dev) {
     using C = Cfg<D, M>;
     CUtensorMap tq, tk, tv;
-    if (!make_tmap_bf16_3d(&tq, p.q, D, p.N, p.BH, 64, kC) || !make_tmap_bf16_3d(&tk, p.k, D, p.N, p.BH, 64, kC) ||
-        !make_tmap_bf16_3d(&tv, p.v, M, p.N, p.BH, 64, kC))
+    if (!cached_tmap_bf16_3d(&tq, p.q, D, p.N, p.BH, 64, kC) || !cached_tmap_bf16_3d(&tk, p.k, D, p.N, p.BH, 64, kC) ||
+        !cached_tmap_bf16_3d(&tv, p.v, M, p.N, p.BH, 64, kC))
         return cudaErrorInvalidValue;
     const int nch = (p.N + kC - 1) / kC;
     int nseg = causal_nseg(p.BH, p.N, dev.sm_count);
@@ -1239,7 +1284,7 @@ cudaError_t launch_causal(const Problem &p, const DeviceInfo &dev) {
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     CUtensorMap to;
-    if (p.out && !make_tmap_bf16_3d(&to, p.out, M, p.N, p.BH, 64, kC)) return cudaErrorInvalidValue;
+    if (p.out && !cached_tmap_bf16_3d(&to, p.out, M, p.N, p.BH, 64, kC)) return cudaErrorInvalidValue;
     if (!p.out) to = tq;   // never used
     CausalArgs a;
     a.has_out = p.out != nullptr;
@@ -1273,11 +1318,13 @@ void nc_grid(long long BH, int N, int sm_count, int &nsplit, int &cps, int &nrb,
 template <int D, int M>
 cudaError_t launch_noncausal(const Problem &p, const DeviceInfo &dev) {
     CUtensorMap tq, tk, tv;
-    if (!make_tmap_bf16_3d(&tq, p.q, D, p.N, p.BH, 64, kC) || !make_tmap_bf16_3d(&tk, p.k, D, p.N, p.BH, 64, kC) ||
-        !make_tmap_bf16_3d(&tv, p.v, M, p.N, p.BH, 64, kC))
+    if (!cached_tmap_bf16_3d(&tq, p.q, D, p.N, p.BH, 64, kC) || !cached_tmap_bf16_3d(&tk, p.k, D, p.N, p.BH, 64, kC) ||
+        !cached_tmap_bf16_3d(&tv, p.v, M, p.N, p.BH, 64, kC))
         return cudaErrorInvalidValue;
     int nsplit, cps, nrb, cpr;
-    nc_grid(p.BH, p.N, dev.sm_count, nsplit, cps, nrb, cpr);
+    nc_grid(p.BH, p.N, 2 * dev.sm_count, nsplit, cps, nrb, cpr);
+    CUtensorMap to;
+    if (!cached_tmap_bf16_3d(&to, p.out, M, p.N, p.BH, 64, kC)) return cudaErrorInvalidValue;
     if (p.ws_bytes < (size_t)p.BH * nsplit * (D * M + D) * sizeof(float)) return cudaErrorInvalidValue;
     cudaError_t e;
     ReduceArgs r{(float *)p.ws, nullptr, nullptr, p.N, nsplit, nsplit, cps, -1, dev.err_word};
@@ -1285,9 +1332,9 @@ cudaError_t launch_noncausal(const Problem &p, const DeviceInfo &dev) {
     state_reduce_kernel<D, M><<<(unsigned)(p.BH * nsplit), kThreads, RCfg<D, M>::SMEM, p.stream>>>(tk, tv, r);
     count_launches(1);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    ReadoutArgs o{p.out, (const float *)p.ws, p.N, nsplit, nrb, cpr, dev.err_word};
+    ReadoutArgs o{(const float *)p.ws, p.N, nsplit, nrb, cpr, dev.err_word};
     if ((e = set_smem(readout_kernel<D, M>, OCfg<D, M>::SMEM)) != cudaSuccess) return e;
-    readout_kernel<D, M><<<(unsigned)(p.BH * nrb), kThreads, OCfg<D, M>::SMEM, p.stream>>>(tq, o);
+    readout_kernel<D, M><<<(unsigned)(p.BH * nrb), kThreads, OCfg<D, M>::SMEM, p.stream>>>(tq, to, o);
     count_launches(1);
     return cudaGetLastError();
 }
@@ -1325,7 +1372,7 @@ size_t tc_noncausal_ws_bytes(const la_shape &s) {
     const long long BH = (long long)s.B * s.H;
     if (BH <= 0 || s.N <= 0) return 0;
     const long long nch = (s.N + kC - 1) / kC;
-    const long long nsplit = std::min(std::max(1LL, 192LL / BH), nch);
+    const long long nsplit = std::min(std::max(1LL, 2 * 192LL / BH), nch);
     return (size_t)BH * nsplit * ((size_t)s.D * s.M + s.D) * sizeof(float);
 }
 

@@ -45,5 +45,35 @@ inline bool make_tmap_bf16_3d(CUtensorMap *map, const void *base, uint64_t cols,
     return r == CUDA_SUCCESS;
 }
 
+// Same as make_tmap_bf16_3d, served from a small per-thread cache keyed by
+// (base, cols, rows, outer, box): encoding a tensor map costs host time on
+// every call, and a caller usually passes the same buffers again and again.
+inline bool cached_tmap_bf16_3d(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows, uint64_t outer,
+                                uint32_t box_cols, uint32_t box_rows) {
+    struct Entry {
+        const void *base;
+        uint64_t cols, rows, outer;
+        uint32_t box_cols, box_rows;
+        CUtensorMap map;
+        bool used;
+    };
+    constexpr int kEntries = 16;
+    thread_local Entry cache[kEntries];
+    thread_local int next = 0;
+    for (int i = 0; i < kEntries; ++i) {
+        const Entry &e = cache[i];
+        if (e.used && e.base == base && e.cols == cols && e.rows == rows && e.outer == outer &&
+            e.box_cols == box_cols && e.box_rows == box_rows) {
+            *map = e.map;
+            return true;
+        }
+    }
+    if (!make_tmap_bf16_3d(map, base, cols, rows, outer, box_cols, box_rows)) return false;
+    Entry &e = cache[next];
+    next = (next + 1) % kEntries;
+    e = Entry{base, cols, rows, outer, box_cols, box_rows, *map, true};
+    return true;
+}
+
 }  // namespace tc
 }  // namespace la

@@ -86,10 +86,14 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def _stream(stream, device):
+def _stream_ptr(stream, device) -> int:
     if stream is None:
         stream = torch.cuda.current_stream(device)
-    return ctypes.c_void_p(stream.cuda_stream)
+    return stream.cuda_stream
+
+
+def _stream(stream, device):
+    return ctypes.c_void_p(_stream_ptr(stream, device))
 
 
 def _check(st: int, where: str):
@@ -108,20 +112,28 @@ def shape_of(q: torch.Tensor, v: torch.Tensor) -> la_shape:
     return la_shape(B, H, N, D, v.shape[-1], _dtype_code(q.dtype))
 
 
+_SIZE_MAX = ctypes.c_size_t(-1).value
+_ws_bytes_cache = {}
+
+
 def la_workspace_bytes(op: int, shape: la_shape, chunk: int = 0) -> int:
-    n = lib().la_workspace_bytes(int(op), shape, int(chunk))
-    if n == ctypes.c_size_t(-1).value:
-        raise LAError(LA_ERR_INVALID_ARG, "la_workspace_bytes")
-    return int(n)
+    key = (int(op), shape.B, shape.H, shape.N, shape.D, shape.M, shape.dtype, int(chunk))
+    n = _ws_bytes_cache.get(key)
+    if n is None:
+        n = lib().la_workspace_bytes(int(op), shape, int(chunk))
+        if n == _SIZE_MAX:
+            raise LAError(LA_ERR_INVALID_ARG, "la_workspace_bytes")
+        _ws_bytes_cache[key] = n = int(n)
+    return n
 
 
 _ws_cache = {}
 
 
-def _workspace(nbytes: int, device) -> torch.Tensor | None:
+def _workspace(nbytes: int, device, stream_ptr: int) -> torch.Tensor | None:
     if nbytes == 0:
         return None
-    key = (torch.device(device).index, torch.cuda.current_stream(device).cuda_stream)
+    key = (device.index, stream_ptr)
     buf = _ws_cache.get(key)
     if buf is None or buf.numel() < nbytes:
         buf = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=device)
@@ -137,9 +149,9 @@ def la_forward_noncausal(q, k, v, out=None, stream=None):
         out = torch.empty(q.shape[:-1] + (v.shape[-1],), dtype=q.dtype, device=q.device)
     _contig(out)
     need = la_workspace_bytes(LA_OP_NONCAUSAL, s, 0)
-    ws = _workspace(need, q.device)
-    st = lib().la_forward_noncausal(_ptr(q), _ptr(k), _ptr(v), _ptr(out), s, _ptr(ws), need,
-                                    _stream(stream, q.device))
+    sp = _stream_ptr(stream, q.device)
+    ws = _workspace(need, q.device, sp)
+    st = lib().la_forward_noncausal(_ptr(q), _ptr(k), _ptr(v), _ptr(out), s, _ptr(ws), need, ctypes.c_void_p(sp))
     _check(st, "la_forward_noncausal")
     return out
 
@@ -167,9 +179,10 @@ def la_forward_causal(q, k, v, out=None, chunk=0, S=None, z=None, want_out=True,
         out = torch.empty(q.shape[:-1] + (v.shape[-1],), dtype=q.dtype, device=q.device)
     _contig(out)
     need = la_workspace_bytes(LA_OP_CAUSAL, s, chunk)
-    ws = _workspace(need, q.device)
+    sp = _stream_ptr(stream, q.device)
+    ws = _workspace(need, q.device, sp)
     st = lib().la_forward_causal(_ptr(q), _ptr(k), _ptr(v), _ptr(out), s, int(chunk), _ptr(S), _ptr(z),
-                                 _ptr(ws), need, _stream(stream, q.device))
+                                 _ptr(ws), need, ctypes.c_void_p(sp))
     _check(st, "la_forward_causal")
     return out
 
