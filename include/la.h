@@ -3,9 +3,9 @@
  * with the feature map phi(x) = elu(x) + 1.
  *
  * Method: "Transformers are RNNs: Fast Autoregressive Transformers with Linear
- * Attention" (Katharopoulos et al.), read in its Chinese translation (page
- * title "線性變換器").  Per head, with Q, K in R^{N x D} and V in R^{N x M}
- * (sec. 3.1 and 3.2.1 notation; rows are positions):
+ * Attention" (Katharopoulos et al.), read in its Chinese translation.  Per
+ * head, with Q, K in R^{N x D} and V in R^{N x M} (sec. 3.1 and 3.2.1
+ * notation; rows are positions):
  *
  *   phi(x)       = x + 1 (x > 0), exp(x) (x <= 0)            sec. 3.2.1 eq. (7)
  *   non-causal   V'_i = phi(Q_i)^T (sum_j phi(K_j) V_j^T)

@@ -4,8 +4,8 @@ TEST INFRASTRUCTURE ONLY: imported by ``tests/``, ``__graft_entry__.smoke()``
 and the CPU-baseline leg of ``bench.py``, never by the product package.  It
 shares no code with the CUDA library.
 
-Two independent forms, both written from "Transformers are RNNs" (Chinese
-translation, page title "線性變換器"):
+Two independent forms, both written from "Transformers are RNNs" (read in
+its Chinese translation):
 
 * ``recurrence`` (C, ``la_oracle.c``): sec. 3.3 eqs. (10)-(12) and sec. 3.4
   eqs. (16)-(20) walked token by token in fp64 loops; also sec. 3.2 eq. (5)

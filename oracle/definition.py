@@ -1,6 +1,6 @@
 """Definition form of kernelised attention, fp64 numpy (test infrastructure only).
 
-Written from "Transformers are RNNs" (Chinese translation, "線性變換器"):
+Written from "Transformers are RNNs" (read in its Chinese translation):
 
 * sec. 3.1 eq. (3): V'_i = sum_j sim(Q_i, K_j) V_j / sum_j sim(Q_i, K_j);
 * sec. 3.2 eq. (4): sim(q, k) = phi(q)^T phi(k), phi applied row-wise;

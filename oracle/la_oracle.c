@@ -8,8 +8,8 @@
  * library.
  *
  * Source: "Transformers are RNNs: Fast Autoregressive Transformers with
- * Linear Attention" (Katharopoulos et al.), read in its Chinese translation
- * (page title "線性變換器").  Every function below restates one passage of it:
+ * Linear Attention" (Katharopoulos et al.), read in its Chinese translation.
+ * Every function below restates one passage of it:
  *
  *   phi            sec. 3.2.1, eq. (7): phi(x) = elu(x) + 1, elu with alpha = 1
  *                  (Clevert et al.), so phi(x) = x + 1 for x > 0, exp(x) else.

@@ -1,6 +1,6 @@
 """Pins for the fp64 oracle, checked against things other than the oracle itself.
 
-Sources ("Transformers are RNNs", Chinese translation 線性變換器):
+Sources ("Transformers are RNNs", read in its Chinese translation):
   * hand-worked fixtures in tests/golden/hand_examples.json (eqs. (3), (4), (7), (8));
   * the definition form (numpy quadratic form of eqs. (3)/(4)/(8)) vs the C
     recurrence of eqs. (10)-(12)/(16)-(20) - two independent programs;

@@ -1,7 +1,7 @@
 // la_tc.cu - tensor-core (tcgen05 + TMA) kernels of liblinattn.so for bf16
 // inputs with D, M in {64, 128}.
 //
-// Method ("Transformers are RNNs", Chinese translation "線性變換器"):
+// Method ("Transformers are RNNs", read in its Chinese translation):
 // causal attention, sec. 3.3 eqs. (9)-(12), regrouped into chunks of C = 128
 // rows.  For chunk c with rows t0..t0+C-1 of one head:
 //   P      = phi(Q_c) phi(K_c)^T                       (C x C, fp32 in TMEM)
