@@ -200,7 +200,7 @@ def run_ours(args, rank, world, dist):
     import torch
 
     from weight_recurrence_gb300 import build as labuild
-    from weight_recurrence_gb300 import inputs, la
+    from weight_recurrence_gb300 import inputs, la, ranks
 
     labuild.build()
     local = _env_int("LOCAL_RANK", 0)
@@ -215,15 +215,21 @@ def run_ours(args, rank, world, dist):
             dist.barrier()
 
     def max_over_ranks(x):
-        if dist is None:
-            return x
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+        return ranks.reduce_max(x, dist, dev)
+
+    if args.only:
+        # one workload alone, for profiler captures: no clocks, e2e or CPU legs
+        w = inputs.WORKLOADS[args.only]
+        if w.op == "decode":
+            leg = _leg_decode(torch, la, inputs, dev, stream, flush, pk, args, max_over_ranks, world, rank)
+        else:
+            leg = _leg_fwd(torch, la, inputs, args.only, dev, stream, flush, pk, args.steps, max_over_ranks,
+                           world, rank, warmup=args.warmup)
+        return {"only": args.only, "leg": leg, "gpu_launches_total": la.la_launch_count()}
 
     # ---------------------------------------------------- main: causal cfg
     w = inputs.WORKLOADS[MAIN]
-    q, k, v = [t.to(dev) for t in inputs.workload_inputs(w)]
+    q, k, v = [t.to(dev) for t in inputs.workload_inputs(w, rank)]
     S = torch.zeros(w.B, w.H, w.D, w.M, device=dev)
     z = torch.zeros(w.B, w.H, w.D, device=dev)
     out = torch.empty(w.B, w.H, w.N, w.M, dtype=w.dtype, device=dev)
@@ -262,7 +268,7 @@ def run_ours(args, rank, world, dist):
     ms = max_over_ranks(ms_local)
     clocks = sampler.stop()
     tokens_per_step = w.B * w.N
-    value = world * tokens_per_step / (ms / 1e3)
+    value = ranks.whole_job_rate(tokens_per_step, world, ms / 1e3)
     launches_per_call = launches / max(1, args.steps)
     bytes_step = _alg_bytes_fwd(w)
     achieved_gbs = bytes_step / (ms / 1e3) / 1e9
@@ -324,11 +330,11 @@ def run_ours(args, rank, world, dist):
     if not args.main_only:
         result["legs"] = {}
         result["legs"]["noncausal"] = _leg_fwd(torch, la, inputs, "noncausal_b8h8n4096d64", dev, stream,
-                                               flush, pk, 30, max_over_ranks, world)
+                                               flush, pk, 30, max_over_ranks, world, rank)
         result["legs"]["long_causal"] = _leg_fwd(torch, la, inputs, "causal_b1h16n65536d128", dev, stream,
-                                                 flush, pk, 5, max_over_ranks, world)
+                                                 flush, pk, 5, max_over_ranks, world, rank)
         result["legs"]["decode"] = _leg_decode(torch, la, inputs, dev, stream, flush, pk, args,
-                                               max_over_ranks, world)
+                                               max_over_ranks, world, rank)
 
     # ------------------------------------------------- CPU baseline (rank 0)
     if rank == 0 and not args.no_cpu:
@@ -336,17 +342,17 @@ def run_ours(args, rank, world, dist):
     return result
 
 
-def _leg_fwd(torch, la, inputs, name, dev, stream, flush, pk, steps, max_over_ranks, world):
+def _leg_fwd(torch, la, inputs, name, dev, stream, flush, pk, steps, max_over_ranks, world, rank, warmup=3):
     w = inputs.WORKLOADS[name]
-    q, k, v = [t.to(dev) for t in inputs.workload_inputs(w)]
+    q, k, v = [t.to(dev) for t in inputs.workload_inputs(w, rank)]
     out = torch.empty(w.B, w.H, w.N, w.M, dtype=w.dtype, device=dev)
     if w.op == "causal":
         fn = lambda: la.la_forward_causal(q, k, v, out=out, chunk=w.chunk, stream=stream)  # noqa: E731
     else:
         fn = lambda: la.la_forward_noncausal(q, k, v, out=out, stream=stream)  # noqa: E731
     l0 = la.la_launch_count()
-    t = _timed_steps(torch, fn, steps, 3, flush, stream)
-    launches = (la.la_launch_count() - l0) // (steps + 3)
+    t = _timed_steps(torch, fn, steps, warmup, flush, stream)
+    launches = (la.la_launch_count() - l0) // (steps + warmup)
     ms = max_over_ranks(sum(t) / len(t))
     gbs = _alg_bytes_fwd(w) / (ms / 1e3) / 1e9
     leg = {"workload": name, "op": w.op, "value": round(world * w.B * w.N / (ms / 1e3), 1), "unit": "tokens/s",
@@ -359,17 +365,18 @@ def _leg_fwd(torch, la, inputs, name, dev, stream, flush, pk, steps, max_over_ra
     return leg
 
 
-def _leg_decode(torch, la, inputs, dev, stream, flush, pk, args, max_over_ranks, world):
+def _leg_decode(torch, la, inputs, dev, stream, flush, pk, args, max_over_ranks, world, rank):
     w = inputs.WORKLOADS["decode_b256h16d64"]
     B, H, D, M = w.B, w.H, w.D, w.M
     # prefill the state with 1024 random tokens through the causal forward
-    qp, kp, vp = [t.to(dev) for t in inputs.qkv(B, H, w.N, D, M, w.dtype, w.scale, seed=w.seed)]
+    qp, kp, vp = [t.to(dev) for t in inputs.workload_inputs(w, rank)]
     S = torch.zeros(B, H, D, M, device=dev)
     z = torch.zeros(B, H, D, device=dev)
     la.la_forward_causal(qp, kp, vp, S=S, z=z, want_out=False, stream=stream)
     del qp, kp, vp
     steps = w.steps
-    qs, ks, vs = inputs.decode_tokens(steps, B, H, D, M, w.dtype, seed=w.seed + 1000, device=dev)
+    qs, ks, vs = inputs.decode_tokens(steps, B, H, D, M, w.dtype, seed=inputs.rank_seed(w.seed + 1000, rank),
+                                      device=dev)
     y = torch.empty(B, H, M, dtype=w.dtype, device=dev)
     n_flush = min(args.decode_steps, steps)
     t_idx = [0]
@@ -379,7 +386,7 @@ def _leg_decode(torch, la, inputs, dev, stream, flush, pk, args, max_over_ranks,
         la.la_decode_step(qs[i], ks[i], vs[i], S, z, y=y, stream=stream)
         t_idx[0] += 1
 
-    times = _timed_steps(torch, one, n_flush, 3, flush, stream)
+    times = _timed_steps(torch, one, n_flush, args.warmup if args.only else 3, flush, stream)
     ms = max_over_ranks(sum(times) / len(times))
     bytes_step = B * H * (2 * D * M * 4 + 2 * D * 4 + (2 * D + 2 * M) * 2)
     gbs = bytes_step / (ms / 1e3) / 1e9
@@ -494,6 +501,11 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-graph", action="store_true")
+    ap.add_argument("--only", default=None,
+                    choices=["causal_b16h8n3072d64", "noncausal_b8h8n4096d64", "causal_b1h16n65536d128",
+                             "decode_b256h16d64"],
+                    help="time this one workload alone (--steps/--warmup; decode: --decode-steps) and print "
+                         "its leg object; for profiler captures, not a bench line")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
 

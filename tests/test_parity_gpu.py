@@ -305,3 +305,43 @@ def test_full_tiny_f32_vs_definition():
     out = la.la_forward_causal(*_dev(q, k, v))
     torch.cuda.synchronize()
     assert row_rel_err(out, definition_causal(q, k, v)) <= TOL_F32
+
+
+def test_full_decode_b256h16d64():
+    """The full decode workload in the bench's launch configuration: a 1024-token
+    prefill through the causal forward, then 4096 sequential steps over the whole
+    [256, 16] batch.  Sampled heads are replayed by the recurrence oracle; their
+    outputs are compared at steps 0, 1, 2, 1023, every 512th and 4095, and their
+    final state after the last step."""
+    w = inputs.WORKLOADS["decode_b256h16d64"]
+    B, H, D, M, T = w.B, w.H, w.D, w.M, w.steps
+    q, k, v = inputs.workload_inputs(w)
+    rng = np.random.default_rng(w.seed)
+    flat = rng.choice(B * H, size=6, replace=False)
+    bsel, hsel = torch.as_tensor(flat // H), torch.as_tensor(flat % H)
+    S = torch.zeros(B, H, D, M, device=DEV)
+    z = torch.zeros(B, H, D, device=DEV)
+    la.la_forward_causal(*_dev(q, k, v), S=S, z=z, want_out=False)
+    _, Sr, zr = oracle.causal(q[bsel, hsel], k[bsel, hsel], v[bsel, hsel], want_out=False)
+    del q, k, v
+    qs, ks, vs = inputs.decode_tokens(T, B, H, D, M, w.dtype, seed=inputs.rank_seed(w.seed + 1000, 0), device=DEV)
+    check = sorted({0, 1, 2, 1023, T - 1} | set(range(0, T, 512)))
+    y = torch.empty(B, H, M, dtype=w.dtype, device=DEV)
+    seen = {}
+    bd, hd = bsel.to(DEV), hsel.to(DEV)
+    for t in range(T):
+        la.la_decode_step(qs[t], ks[t], vs[t], S, z, y=y)
+        if t in check:
+            seen[t] = y[bd, hd].clone()
+    torch.cuda.synchronize()
+    assert la.la_get_last_error() == la.LA_OK
+    qh, kh, vh = (x[:, bd, hd].cpu() for x in (qs, ks, vs))
+    del qs, ks, vs
+    worst = 0.0
+    for t in range(T):
+        yr = oracle.decode_step(qh[t], kh[t], vh[t], Sr, zr, nthreads=1)
+        if t in seen:
+            worst = max(worst, row_rel_err(seen[t].cpu(), yr))
+    assert worst <= TOL_BF16, worst
+    assert head_rel_err(S[bd, hd].cpu(), Sr, nlead=1) <= TOL_BF16
+    assert head_rel_err(z[bd, hd].cpu(), zr, nlead=1) <= TOL_BF16

@@ -8,7 +8,7 @@ library has not been built.
 """
 import importlib
 
-__all__ = ["la", "inputs"]
+__all__ = ["la", "inputs", "ranks"]
 
 
 def __getattr__(name):

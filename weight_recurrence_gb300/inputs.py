@@ -98,6 +98,15 @@ def decode_tokens(steps, B, H, D, M, dtype=torch.bfloat16, seed=0, scale=1.0, de
     return x[:, 0, :, :, :D].contiguous(), x[:, 1, :, :, :D].contiguous(), x[:, 2, :, :, :M].contiguous()
 
 
-def workload_inputs(w: Workload):
-    """Inputs of a named workload: (q, k, v) on the CPU."""
-    return qkv(w.B, w.H, w.N, w.D, w.M, w.dtype, w.scale, w.seed)
+def rank_seed(seed: int, rank: int) -> int:
+    """Seed of rank ``rank``'s share when several processes each take an
+    independent batch of a workload: rank 0 keeps ``seed``, the others are
+    offset by a prime so that no two ranks draw the same stream."""
+    if rank < 0:
+        raise ValueError("rank must be >= 0")
+    return int(seed) + 7919 * int(rank)
+
+
+def workload_inputs(w: Workload, rank: int = 0):
+    """Inputs of a named workload: (q, k, v) on the CPU, rank ``rank``'s batch."""
+    return qkv(w.B, w.H, w.N, w.D, w.M, w.dtype, w.scale, rank_seed(w.seed, rank))
