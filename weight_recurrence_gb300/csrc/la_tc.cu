@@ -19,15 +19,18 @@
 // Roles of the causal CTA (480 threads):
 //   warp 0      TMA producer: chunk tiles into a ring of NS stages, 128-byte
 //               swizzled (the tcgen05 canonical K-major layout);
-//   warp 1      MMA issuer (one thread): P, A V and phi(Q) S_prev, completion
-//               through tcgen05.commit on mbarriers;
-//   warp 2      state-MMA issuer (one thread): S += phi(K)^T V, the serial
-//               chain from chunk to chunk, never queued behind other MMAs;
+//   warp 1      P issuer (one thread): P = phi(Q) phi(K)^T as soon as the
+//               feature map is applied; at D = M = 64 also the chunk's state
+//               increment phi(K)^T [V | 1] into a fresh TMEM buffer;
+//   warp 2      output issuer (one thread): at other sizes first the state
+//               update S += phi(K)^T V (accumulated in TMEM), then A V and
+//               phi(Q) S_prev; completion through tcgen05.commit on mbarriers;
 //   warps 3-6   P group, one thread per TMEM lane: masks P and writes it back to
 //               TMEM as bf16 (the A operand of A V), and forms phi(Q_i).z_prev;
-//   warps 7-10  O group: snapshots the fp32 TMEM state into a bf16 shared-memory
-//               copy (the B operand of phi(Q) S_prev), divides the output rows,
-//               stages them in the stage's dead Q/K tiles and stores them by TMA;
+//   warps 7-10  O group: keeps the state (in registers at D = M = 64, adding
+//               each increment; else in TMEM), writes the bf16 shared-memory
+//               snapshot that is the B operand of phi(Q) S_prev, divides the
+//               output rows and stores them straight to global memory;
 //   warps 11-14 feature-map group: applies phi in place to the Q and K tiles as
 //               they land, running ahead of the MMAs by up to NS chunks.
 // The reduction and read-out kernels use warps 0-9 the same way with one
@@ -238,10 +241,10 @@ __device__ __forceinline__ uint64_t ones_desc(uint32_t tile) { return smem_desc(
 
 // ------------------------------------------------------------ causal kernel
 
-// Warps of the causal CTA: 0 producer, 1 MMA issuer, 2 state-MMA issuer,
-// 3-6 P group, 7-10 O group, 11-14 feature-map group.
+// Warps of the causal CTA: 0 producer, 1 P issuer, 2 output issuer, 3-6 P
+// group, 7-10 O group, 11-14 feature-map group (phi(Q) and phi(K)), or 11-14
+// phi(Q) and 15-18 phi(K) with two feature-map groups.
 constexpr int kWarpP = 3, kWarpO = 7, kWarpPhi = 11;
-constexpr int kThreadsCausal = 32 * (kWarpPhi + 4);
 
 template <int D, int M>
 struct Cfg {
@@ -249,7 +252,6 @@ struct Cfg {
     static constexpr int TILE_V = kC * M * 2;
     static constexpr int STAGE = 2 * TILE_QK + TILE_V;
     static constexpr int SNAP = D * M * 2;
-    static_assert(kC * M * 2 <= 2 * TILE_QK, "the output tile can be staged in the stage's Q and K tiles");
     // M = 64: O shares its P buffer; V is read as [V | ones] (N = 80) so that
     // the state update also yields z and A V also yields the row sums; and the
     // snapshot is read as [S | z] (N = 80) so that phi(Q) S_prev also yields
@@ -260,11 +262,27 @@ struct Cfg {
     // 16-column window of a swizzled tile is itself a valid atom).
     static constexpr bool O_IN_P = (M == 64);
     static constexpr bool ZMMA = O_IN_P;
-    static constexpr int NPB = O_IN_P ? 3 : 1;         // P buffers in TMEM
+    // D = M = 64: each chunk's state increment dS = phi(K)^T [V | 1] goes to a
+    // fresh TMEM buffer (two of them) and the O group adds it to an fp32 copy
+    // of the state held in its registers, so the state MMAs never wait for a
+    // snapshot.  The increment's A operand repeats its 64 rows (M-atom stride
+    // 0), so accumulator lanes 64-127 hold a second copy and all four warps of
+    // the O group can each take one row and half of its columns.
+    static constexpr bool DS = (D == 64 && M == 64);
+    static constexpr int NPB = DS ? 2 : (O_IN_P ? 3 : 1);   // P buffers in TMEM
+    // D = M = 64: output rows are staged (swizzled) in the stage's dead Q and K
+    // tiles and stored by TMA, the stage being released once the store has
+    // read them; one feature-map group.  Other sizes: each O-group thread
+    // stores its own output row, and two feature-map groups share the tiles
+    // (measured choices: at D = M = 128 the feature map, not the stage ring,
+    // limits the pipeline).
+    static constexpr bool OUT_TMA = DS;
+    static constexpr int NPHI = DS ? 1 : 2;
+    static constexpr int THREADS = 32 * (kWarpPhi + 4 * NPHI);
     static constexpr int NDZ = ZMMA ? 1 : 2;           // phi(Q).z_prev hand-over slots (TMEM)
     static constexpr int ONES = O_IN_P ? kC * 128 : kOnesBytes;
     static constexpr int ZS_BYTES = ZMMA ? 0 : 2 * D * 4;
-    static constexpr int NBARS_MAX = 3 * 4 + 4 * 3 + 2 + 5;
+    static constexpr int NBARS_MAX = 3 * 4 + 4 * 3 + 2 + 5 + 4;
     static constexpr int FIXED1 = SNAP + ONES + ZS_BYTES + 8 * NBARS_MAX + 16;
     // two state snapshots when two stages still fit beside them
     static constexpr bool DB = (kSmemMax - FIXED1 - SNAP) / STAGE >= 2;
@@ -273,23 +291,16 @@ struct Cfg {
     static constexpr int NS_FIT = (int)((kSmemMax - FIXED) / STAGE);
     static constexpr int NS = NS_FIT > 4 ? 4 : NS_FIT;
     static_assert(NS >= 2, "pipeline needs two stages");
-    static constexpr int NBARS = 3 * NS + 4 * NPB + NDZ + 5;
-    // Output tiles are staged for the TMA store in buffers of their own when
-    // room is left after the stages (then a stage is released as soon as its
-    // MMAs are done), else in the stage's dead Q/K tiles (then the stage waits
-    // for the store to read them).
-    static constexpr int OUT_TILE = kC * M * 2;
-    static constexpr int BASE = NS * STAGE + NSB * SNAP + ONES + ZS_BYTES + 8 * NBARS + 16;
-    static constexpr int NOB = !ZMMA ? 0 : (BASE + 2 * OUT_TILE <= (int)kSmemMax ? 2 : (BASE + OUT_TILE <= (int)kSmemMax ? 1 : 0));
+    static constexpr int NBARS = 3 * NS + 4 * NPB + NDZ + 5 + 4;
     static constexpr int OFF_SNAP = NS * STAGE;
     static constexpr int OFF_ONES = OFF_SNAP + NSB * SNAP;
     static constexpr int OFF_Z = OFF_ONES + ONES;           // z snapshots [2][D] fp32 (without ZMMA)
-    static constexpr int OFF_OUT = OFF_Z + ZS_BYTES;
-    static constexpr int OFF_BAR = OFF_OUT + NOB * OUT_TILE;
+    static constexpr int OFF_BAR = OFF_Z + ZS_BYTES;
     static constexpr int OFF_TSLOT = OFF_BAR + 8 * NBARS;
     static constexpr int SMEM = OFF_TSLOT + 16;
     static_assert(SMEM <= (int)kSmemMax, "shared memory budget");
-    // TMEM columns.  M = 64: three 144-column buffers, each holding P
+    // TMEM columns.  D = M = 64: two 144-column P/O buffers (as below) and two
+    // 80-column increment buffers at 288 and 368.  M = 64: three 144-column buffers, each holding P
     // (128 fp32 columns), then A (bf16, columns 0-63) and O (columns 64-143:
     // 64 numerator columns, then row sum, phi(Q).z_hi, phi(Q).z_lo); S and z
     // in 432-511.  M = 128: P, a separate A, O, S, z, a 16-column row-sum
@@ -303,11 +314,12 @@ struct Cfg {
     static __device__ __forceinline__ uint32_t col_o(int b) { return O_IN_P ? 144u * b + 64u : 192u; }
     static __device__ __forceinline__ uint32_t col_den(int b) { return O_IN_P ? 144u * b + 128u : 464u; }
     static __device__ __forceinline__ uint32_t col_dz(int j) { return 480u + 16u * (j & 1); }
+    static __device__ __forceinline__ uint32_t col_ds(int j) { return 288u + 80u * (j & 1); }
     static_assert(O_IN_P ? (COL_Z + 16 <= TMEM_COLS) : (COL_Z + 16 <= 464), "TMEM budget");
 };
 
 struct CausalArgs {
-    bool has_out;            // store the output rows (through tm_o)
+    __nv_bfloat16 *out;      // [BH, N, M] or null (state only)
     float *S;                // [BH, D, M] in/out or null
     float *z;                // [BH, D] in/out or null
     const float *seg_ws;     // nseg > 1: [BH, nseg, D*M + D]; slots < nseg-1 hold segment sums,
@@ -323,7 +335,7 @@ struct CausalArgs {
 __device__ __forceinline__ void o_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
 
 template <int D, int M>
-__global__ void __launch_bounds__(kThreadsCausal, 1)
+__global__ void __launch_bounds__(Cfg<D, M>::THREADS, 1)
 causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                  const CausalArgs args)
@@ -345,6 +357,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     // snapshot of the state entering chunk j: barrier j & 1, phase j >> 1 (two
     // barriers, so that no waiter can fall two phases behind one barrier)
     uint64_t *snap_bar = dz_ready + C::NDZ, *s_full = snap_bar + 2, *never = s_full + 1, *drain = never + 1;
+    uint64_t *ds_full = drain + 1, *ds_free = ds_full + 2;   // increment buffers (DS)
     auto snap_wait = [&](int j) { return wait_bar(&snap_bar[j & 1], (j >> 1) & 1, abort); };
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + C::OFF_TSLOT);
     uint8_t *snap0 = smem + C::OFF_SNAP;
@@ -360,9 +373,11 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         if (*abort) record_error(args.err, kErrTimeout);
         for (int s = 0; s < C::NS; ++s) {
             mbar_init(&full[s], 1);
-            // released by both MMA issuers (own output buffers) or by the O group after the store
-            mbar_init(&empty[s], C::NOB ? 2 : 1);
-            mbar_init(&phi_done[s], kGrp);
+            // released by the output issuer's commit, with DS also by the P
+            // issuer's (state increment), and without ZMMA by the P group once it
+            // has read phi(Q) for phi(Q).z_prev
+            mbar_init(&empty[s], (C::DS ? 2 : 1) + (C::ZMMA ? 0 : kGrp) + (C::OUT_TMA ? 1 : 0));
+            mbar_init(&phi_done[s], C::NPHI * kGrp);
         }
         for (int b = 0; b < C::NPB; ++b) {
             mbar_init(&p_full[b], 1);
@@ -376,13 +391,17 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         mbar_init(s_full, 1);
         mbar_init(never, 1);
         mbar_init(drain, 2);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&ds_full[b], 1);
+            mbar_init(&ds_free[b], kGrp);
+        }
         fence_mbar_init();
     }
     // ones operand, MN-major, ones in column 0 and zeros elsewhere: [C K-rows x 64]
     // when it is read as the second N-atom of [V | ones], else one 8-row atom
-    for (int i = tid; i < C::ONES / 4; i += kThreadsCausal) reinterpret_cast<uint32_t *>(ones)[i] = 0u;
+    for (int i = tid; i < C::ONES / 4; i += C::THREADS) reinterpret_cast<uint32_t *>(ones)[i] = 0u;
     __syncthreads();
-    for (int k = tid; k < C::ONES / 128; k += kThreadsCausal)
+    for (int k = tid; k < C::ONES / 128; k += C::THREADS)
         *reinterpret_cast<uint16_t *>(ones + sw128_offset(k, 0)) = 0x3F80u;
     if (warp == 0) {
         tmem_alloc(tslot, C::TMEM_COLS);
@@ -436,17 +455,24 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             }
         }
     } else if (warp == 1) {
-        // ------------------------------------------------------ MMA issuer
-        // P = phi(Q) phi(K)^T, O = A V (+ row sums) and O += phi(Q) S_prev
+        // ------------------------------------------------------ P issuer
+        // P = phi(Q) phi(K)^T for each chunk into its P buffer, as soon as the
+        // feature map is applied and the buffer is free; with DS also the state
+        // increment dS = phi(K)^T [V | 1] into its buffer
         if (lane == 0 && !*abort) {
-            constexpr int NV = C::O_IN_P ? M + 16 : M;      // N of the MMAs that read V
             constexpr uint32_t ID_P = idesc_bf16(128, kC, 0, 0);
-            constexpr uint32_t ID_O = idesc_bf16(128, M, 0, 1);
-            constexpr uint32_t ID_AV = idesc_bf16(128, NV, 0, 1);
-            constexpr uint32_t ID_D = idesc_bf16(128, 16, 0, 1);
-            // P = phi(Q) phi(K)^T for chunk j into its P buffer
-            auto issue_p = [&](int j) {
-                const int s = j % C::NS, pb = j % C::NPB;
+            constexpr uint32_t ID_DS = idesc_bf16(128, M + 16, 1, 1);
+            for (int j = 0; j < n; ++j) {
+                const int s = j % C::NS, pb = j % C::NPB, kb = j / C::NPB;
+                if (!wait_bar(&phi_done[s], (j / C::NS) & 1, abort)) break;
+                LA_TRACE_AT(1, j, 0);
+                if (C::O_IN_P) {
+                    // O(j - NPB) shares the buffer: it must have been read out
+                    if (kb > 0 && !wait_bar(&o_free[pb], (kb - 1) & 1, abort)) break;
+                } else if (j > 0 && !wait_bar(&a_ready[0], (j - 1) & 1, abort)) {   // P(j-1) has been read
+                    break;
+                }
+                LA_TRACE_AT(1, j, 1);
                 tc_fence_after();
                 const uint32_t st = smem_u32(smem + s * C::STAGE);
                 const uint64_t dq = kmajor_base(st), dk = kmajor_base(st + C::TILE_QK);
@@ -456,35 +482,81 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     mma_f16_ss(dp, dq + kmajor_step(ks), dk + kmajor_step(ks), ID_P, ks > 0);
                 mma_commit(&p_full[pb]);
                 LA_TRACE_AT(1, j, 2);
-            };
-            // O (+)= phi(Q) [S_prev | z]: the z atom is the 16-column window of the ones
-            // tile holding snapshot j's z
-            auto issue_inter = [&](uint32_t qa, uint32_t sa, uint32_t zatom, uint32_t ocol, bool acc) {
-                constexpr uint32_t ID_I = C::ZMMA ? idesc_bf16(128, M + 16, 0, 1) : ID_O;
-                const uint64_t dq = kmajor_base(qa);
-                const uint64_t ds = smem_desc(sa, C::ZMMA ? zatom - sa : (uint32_t)(D * 128), 1024);
+                if (C::DS) {
+                    if (j >= 2 && !wait_bar(&ds_free[j & 1], ((j >> 1) - 1) & 1, abort)) break;
+                    LA_TRACE_AT(1, j, 3);
+                    tc_fence_after();
+                    // A = phi(K)^T read MN-major with M-atom stride 0 (rows 64-127 repeat 0-63)
+                    const uint64_t dk = smem_desc(st + C::TILE_QK, 0, 1024), dv = v_base(st + 2 * C::TILE_QK);
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks)
-                    mma_f16_ss(tmem + ocol, dq + kmajor_step(ks), ds + mnmajor_step(ks), ID_I, acc || ks > 0);
-            };
-            // numerator, row sums and phi(Q) S_prev for chunk j
-            auto issue_av = [&](int j) {
-                const int s = j % C::NS, pb = j % C::NPB;
+                    for (int ks = 0; ks < kC / 16; ++ks)
+                        mma_f16_ss(tmem + C::col_ds(j), dk + mnmajor_step(ks), dv + mnmajor_step(ks), ID_DS, ks > 0);
+                    mma_commit(&ds_full[j & 1]);
+                    mma_commit(&empty[s]);
+                    LA_TRACE_AT(1, j, 4);
+                }
+            }
+        }
+        if (lane == 0) mma_commit(drain);   // arrives once this thread's MMAs (if any) are done
+    } else if (warp == 2) {
+        // ------------------------------------------------------ output issuer
+        // Per chunk, in this order: (without DS) S += phi(K)^T V and z +=
+        // phi(K)^T 1 (the serial chain from chunk to chunk; A = phi(K) read
+        // MN-major, 128 rows, accumulator rows >= D never read), then the output
+        // MMAs O = A [V | 1] + phi(Q) [S_prev | z_prev].  One commit after the
+        // output MMAs covers both, so it releases the stage; s_full after the
+        // state update also guarantees that the output MMAs of the previous
+        // chunk, which read the snapshot buffer the O group overwrites next,
+        // have completed.
+        if (lane == 0 && !*abort) {
+            constexpr int NV = C::O_IN_P ? M + 16 : M;
+            constexpr uint32_t ID_S = idesc_bf16(128, NV, 1, 1);
+            constexpr uint32_t ID_O = idesc_bf16(128, M, 0, 1);
+            constexpr uint32_t ID_AV = idesc_bf16(128, NV, 0, 1);
+            constexpr uint32_t ID_D = idesc_bf16(128, 16, 0, 1);
+            constexpr uint32_t ID_I = C::ZMMA ? idesc_bf16(128, M + 16, 0, 1) : ID_O;
+            for (int it = 0; it < n; ++it) {
+                const int s = it % C::NS, pb = it % C::NPB, kb = it / C::NPB;
+                if (!wait_bar(&phi_done[s], (it / C::NS) & 1, abort)) break;
+                if (!snap_wait(it)) break;   // S(it-1) has been read out
+                LA_TRACE_AT(4, it, 5);
+                tc_fence_after();
                 const uint32_t st = smem_u32(smem + s * C::STAGE);
                 const uint32_t qa = st, va = st + 2 * C::TILE_QK;
-                const uint32_t sa = smem_u32(snap_buf(j));
-                const uint32_t za = ones_a + 2 * (zcol(j) - 1);
-                tc_fence_after();
                 const uint64_t dv = v_base(va);
+                if (!C::DS) {
+                    const uint64_t dk = smem_desc(st + C::TILE_QK, kC * 128, 1024);
+#pragma unroll
+                    for (int ks = 0; ks < kC / 16; ++ks) {
+                        mma_f16_ss(tmem + C::COL_S, dk + mnmajor_step(ks), dv + mnmajor_step(ks), ID_S, 1);
+                        if (!C::O_IN_P) mma_f16_ss(tmem + C::COL_Z, dk + mnmajor_step(ks), ones_d, ID_16, 1);
+                    }
+                    mma_commit(s_full);
+                }
+
+                if (!wait_bar(&a_ready[pb], kb & 1, abort)) break;
+                if (!C::O_IN_P && it > 0 && !wait_bar(&o_free[0], (it - 1) & 1, abort)) break;
+                LA_TRACE_AT(4, it, 6);
+                tc_fence_after();
+                // phi(Q) [S_prev | z]: the z atom is the 16-column window of the ones
+                // tile holding snapshot it's z
+                const uint32_t sa = smem_u32(snap_buf(it));
+                const uint32_t za = ones_a + 2 * (zcol(it) - 1);
+                const uint64_t dq = kmajor_base(qa);
+                const uint64_t ds = smem_desc(sa, C::ZMMA ? za - sa : (uint32_t)(D * 128), 1024);
                 if (C::O_IN_P) {
                     // O = A [V | 1] (numerator and row sums), then O += phi(Q) S_prev
 #pragma unroll
                     for (int ks = 0; ks < kC / 16; ++ks)
                         mma_f16_ts(tmem + C::col_o(pb), tmem + C::col_a(pb) + ks * 8, dv + mnmajor_step(ks), ID_AV,
                                    ks > 0);
-                    issue_inter(qa, sa, za, C::col_o(pb), true);
+#pragma unroll
+                    for (int ks = 0; ks < D / 16; ++ks)
+                        mma_f16_ss(tmem + C::col_o(pb), dq + kmajor_step(ks), ds + mnmajor_step(ks), ID_I, 1);
                 } else {
-                    issue_inter(qa, sa, za, C::col_o(0), false);
+#pragma unroll
+                    for (int ks = 0; ks < D / 16; ++ks)
+                        mma_f16_ss(tmem + C::col_o(0), dq + kmajor_step(ks), ds + mnmajor_step(ks), ID_I, ks > 0);
                     // O += A V and row sums A 1  (A = masked P as bf16 in TMEM, K = C)
 #pragma unroll
                     for (int ks = 0; ks < kC / 16; ++ks) {
@@ -494,74 +566,8 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     }
                 }
                 mma_commit(&o_full[pb]);
-                if (C::NOB) mma_commit(&empty[s]);
-                LA_TRACE_AT(1, j, 5);
-            };
-            // Issues, in whatever order their inputs become ready, P(jp) (needs phi of
-            // chunk jp and a free P buffer) and the output MMAs of chunk ja (need A(ja)
-            // and the snapshot of the state before chunk ja); the output MMAs go first.
-            // Every barrier tested here can be at most one phase ahead of its test.
-            int jp = 0, ja = 0;
-            uint64_t deadline = now_ns() + kWaitNs;
-            uint32_t idle = 0;
-            while (ja < n) {
-                bool progress = false;
-                if (ja < jp) {
-                    const int pb = ja % C::NPB, kb = ja / C::NPB;
-                    bool rdy = mbar_test(&a_ready[pb], kb & 1) && mbar_test(&snap_bar[ja & 1], (ja >> 1) & 1);
-                    if (!C::O_IN_P && ja > 0) rdy = rdy && mbar_test(&o_free[0], (ja - 1) & 1);
-                    if (rdy) {
-                        issue_av(ja++);
-                        progress = true;
-                    }
-                }
-                if (!progress && jp < n) {
-                    const int s = jp % C::NS, pb = jp % C::NPB, kb = jp / C::NPB;
-                    bool rdy = mbar_test(&phi_done[s], (jp / C::NS) & 1);
-                    if (C::O_IN_P) {
-                        if (kb > 0) rdy = rdy && mbar_test(&o_free[pb], (kb - 1) & 1);
-                    } else if (jp > 0) {
-                        rdy = rdy && mbar_test(&a_ready[0], (jp - 1) & 1);   // P(jp-1) has been read
-                    }
-                    if (rdy) {
-                        issue_p(jp++);
-                        progress = true;
-                    }
-                }
-                if (progress) {
-                    idle = 0;
-                } else if ((++idle & 63u) == 0) {
-                    if (*abort) break;
-                    if (idle == 64) deadline = now_ns() + kWaitNs;
-                    else if (now_ns() > deadline) { set_abort(abort, args.err); break; }
-                }
-            }
-        }
-        if (lane == 0) mma_commit(drain);   // arrives once this thread's MMAs (if any) are done
-    } else if (warp == 2) {
-        // ------------------------------------------------------ state-MMA issuer
-        // S += phi(K)^T V and z += phi(K)^T 1, one chunk after the other, as soon
-        // as the previous state has been snapshotted (A = phi(K) read MN-major,
-        // 128 rows; accumulator rows >= D are never read)
-        if (lane == 0 && !*abort) {
-            constexpr int NV = C::O_IN_P ? M + 16 : M;
-            constexpr uint32_t ID_S = idesc_bf16(128, NV, 1, 1);
-            for (int it = 0; it < n; ++it) {
-                const int s = it % C::NS;
-                if (!wait_bar(&phi_done[s], (it / C::NS) & 1, abort)) break;
-                LA_TRACE_AT(4, it, 6);
-                if (!snap_wait(it)) break;   // S(it-1) has been read out
+                mma_commit(&empty[s]);
                 LA_TRACE_AT(4, it, 7);
-                tc_fence_after();
-                const uint32_t st = smem_u32(smem + s * C::STAGE);
-                const uint64_t dk = smem_desc(st + C::TILE_QK, kC * 128, 1024), dv = v_base(st + 2 * C::TILE_QK);
-#pragma unroll
-                for (int ks = 0; ks < kC / 16; ++ks) {
-                    mma_f16_ss(tmem + C::COL_S, dk + mnmajor_step(ks), dv + mnmajor_step(ks), ID_S, 1);
-                    if (!C::O_IN_P) mma_f16_ss(tmem + C::COL_Z, dk + mnmajor_step(ks), ones_d, ID_16, 1);
-                }
-                mma_commit(s_full);
-                if (C::NOB) mma_commit(&empty[s]);
             }
         }
         if (lane == 0) mma_commit(drain);
@@ -576,6 +582,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             const int s = it % C::NS, pb = it % C::NPB, kb = it / C::NPB;
             if (tid == 32 * kWarpP) LA_TRACE_AT(2, it, 3);
             bool ok = wait_bar_warp(&p_full[pb], kb & 1, abort);
+            // without O_IN_P, A(it-1) must have been consumed before it is overwritten
             if (!C::O_IN_P && it > 0) ok = ok && wait_bar_warp(&o_full[0], (it - 1) & 1, abort);
             if (tid == 32 * kWarpP) LA_TRACE_AT(2, it, 4);
             if (ok) {
@@ -607,8 +614,8 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             mbar_arrive(&a_ready[pb]);
             if (tid == 32 * kWarpP) LA_TRACE_AT(2, it, 5);
             if (!C::ZMMA) {
-                // phi(Q_r) . z_prev into TMEM for the O group (the stage is released only
-                // after the O group is done with the chunk)
+                // phi(Q_r) . z_prev into TMEM for the O group; the stage is released
+                // once every thread of this group has read its phi(Q) row
                 if (__all_sync(0xffffffffu, snap_wait(it))) {
                     uint32_t w[16];
 #pragma unroll
@@ -619,6 +626,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 }
                 tc_fence_before();
                 mbar_arrive(&dz_ready[it % C::NDZ]);
+                mbar_arrive(&empty[s]);
             }
         }
     } else if (warp < kWarpPhi) {
@@ -627,113 +635,62 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         const int q4 = warp & 3;
         const int r = 32 * q4 + lane;
         const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
-        const bool srow = r < D;                 // owns a state row
-        const bool swarp = 32 * q4 < D;          // warp-uniform
-        const bool leader = tid == 32 * kWarpO;
         float *S_h = args.S ? args.S + (size_t)bh * D * M : nullptr;
         float *z_h = args.z ? args.z + (size_t)bh * D : nullptr;
-
-        // state entering the segment: carried-in state plus earlier segments' sums
-        if (swarp) {
-            const float *ws_h = args.seg_ws ? args.seg_ws + (size_t)bh * args.nseg * (D * M + D) : nullptr;
+        const float *ws_h = args.seg_ws ? args.seg_ws + (size_t)bh * args.nseg * (D * M + D) : nullptr;
+        const bool tracer = tid == 32 * kWarpO + 32 * ((4 - kWarpO % 4) % 4);
+        // z of a snapshot as two bf16 parts in the ones tile (ZMMA), or fp32
+        auto put_z = [&](int j, int row, float zr) {
+            if (C::ZMMA) {
+                const __nv_bfloat16 hi = __float2bfloat16_rn(zr);
+                const __nv_bfloat16 lo = __float2bfloat16_rn(zr - __bfloat162float(hi));
+                *reinterpret_cast<__nv_bfloat16 *>(ones + sw128_offset(row, zcol(j))) = hi;
+                *reinterpret_cast<__nv_bfloat16 *>(ones + sw128_offset(row, zcol(j) + 1)) = lo;
+            } else {
+                zs_buf(j)[row] = zr;
+            }
+        };
+        // fp32 state entering the segment (row `row`, columns c0..c0+31, and z):
+        // the carried-in state plus the earlier segments' sums
+        auto load_state32 = [&](int row, int c0, float (&v)[32]) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] = 0.f;
+            auto add = [&](const float *src) {
+#pragma unroll
+                for (int j = 0; j < 32; j += 4) {
+                    const float4 x = *reinterpret_cast<const float4 *>(src + row * M + c0 + j);
+                    v[j] += x.x; v[j + 1] += x.y; v[j + 2] += x.z; v[j + 3] += x.w;
+                }
+            };
+            if (ws_h) {
+                add(ws_h + (size_t)(args.nseg - 1) * (D * M + D));
+                for (int g = 0; g < seg; ++g) add(ws_h + (size_t)g * (D * M + D));
+            } else if (S_h) {
+                add(S_h);
+            }
+        };
+        auto load_z = [&](int row) {
             float zr = 0.f;
-            if (srow) {
-                if (ws_h) {
-                    zr = ws_h[(size_t)(args.nseg - 1) * (D * M + D) + D * M + r];
-                    for (int g = 0; g < seg; ++g) zr += ws_h[(size_t)g * (D * M + D) + D * M + r];
-                } else if (z_h) {
-                    zr = z_h[r];
-                }
-                if (C::ZMMA) {
-                    const __nv_bfloat16 hi = __float2bfloat16_rn(zr);
-                    const __nv_bfloat16 lo = __float2bfloat16_rn(zr - __bfloat162float(hi));
-                    *reinterpret_cast<__nv_bfloat16 *>(ones + sw128_offset(r, zcol(0))) = hi;
-                    *reinterpret_cast<__nv_bfloat16 *>(ones + sw128_offset(r, zcol(0) + 1)) = lo;
-                } else {
-                    zs_buf(0)[r] = zr;
-                }
+            if (ws_h) {
+                zr = ws_h[(size_t)(args.nseg - 1) * (D * M + D) + D * M + row];
+                for (int g = 0; g < seg; ++g) zr += ws_h[(size_t)g * (D * M + D) + D * M + row];
+            } else if (z_h) {
+                zr = z_h[row];
             }
-#pragma unroll 1
-            for (int c0 = 0; c0 < M; c0 += 32) {
-                float v[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] = 0.f;
-                if (srow) {
-                    auto add = [&](const float *src) {
-#pragma unroll
-                        for (int j = 0; j < 32; j += 4) {
-                            const float4 x = *reinterpret_cast<const float4 *>(src + r * M + c0 + j);
-                            v[j] += x.x; v[j + 1] += x.y; v[j + 2] += x.z; v[j + 3] += x.w;
-                        }
-                    };
-                    if (ws_h) {
-                        add(ws_h + (size_t)(args.nseg - 1) * (D * M + D));
-                        for (int g = 0; g < seg; ++g) add(ws_h + (size_t)g * (D * M + D));
-                    } else if (S_h) {
-                        add(S_h);
-                    }
-                    store_snap32<D>(snap_buf(0), r, c0, v);
-                }
-                tmem_st32f(tmem + lane_off + C::COL_S + c0, v);
-            }
-            uint32_t w[16];
-#pragma unroll
-            for (int j = 0; j < 16; ++j) w[j] = 0u;
-            w[0] = __float_as_uint(zr);
-            tmem_st16(tmem + lane_off + C::COL_Z, w);
-            tmem_wait_st();
-        }
-        tc_fence_before();
-        fence_proxy_async();
-        mbar_arrive(&snap_bar[0]);
-        if (leader && args.has_out) prefetch_tmap(&tm_o);
-
-        for (int it = 0; it < n; ++it) {
-            const int s = it % C::NS, pb = it % C::NPB, kb = it / C::NPB;
-            // ---- snapshot of the state after chunk it, for chunk it+1
-            if (tid == 32 * kWarpO + 32 * (4 - kWarpO % 4) % 128) LA_TRACE_AT(4, it, 0);
-            bool ok = wait_bar_warp(s_full, it & 1, abort);
-            if (!C::DB) ok = ok && wait_bar_warp(&o_full[pb], kb & 1, abort);   // single snapshot: read by O(it)
-            if (tid == 32 * kWarpO + 32 * (4 - kWarpO % 4) % 128) LA_TRACE_AT(4, it, 1);
-            if (it + 1 < n) {
-                if (ok && swarp) {
-                    tc_fence_after();
-                    uint8_t *sb = snap_buf(it + 1);
-#pragma unroll 1
-                    for (int c0 = 0; c0 < M; c0 += 32) {
-                        float v[32];
-                        tmem_ld32f(tmem + lane_off + C::COL_S + c0, v);
-                        if (srow) store_snap32<D>(sb, r, c0, v);
-                    }
-                    uint32_t zv[16];
-                    tmem_ld16(tmem + lane_off + C::COL_Z, zv);
-                    tmem_wait_ld();
-                    if (srow) {
-                        const float zr = __uint_as_float(zv[0]);
-                        if (C::ZMMA) {
-                            const __nv_bfloat16 hi = __float2bfloat16_rn(zr);
-                            const __nv_bfloat16 lo = __float2bfloat16_rn(zr - __bfloat162float(hi));
-                            *reinterpret_cast<__nv_bfloat16 *>(ones + sw128_offset(r, zcol(it + 1))) = hi;
-                            *reinterpret_cast<__nv_bfloat16 *>(ones + sw128_offset(r, zcol(it + 1) + 1)) = lo;
-                        } else {
-                            zs_buf(it + 1)[r] = zr;
-                        }
-                    }
-                }
-                tc_fence_before();
-                fence_proxy_async();
-                mbar_arrive(&snap_bar[(it + 1) & 1]);
-            }
-            if (tid == 32 * kWarpO + 32 * (4 - kWarpO % 4) % 128) LA_TRACE_AT(4, it, 2);
-            // ---- output rows of chunk it: num / (row sum + phi(Q).z_prev), staged as
-            // a swizzled tile in the (now dead) Q and K tiles of the stage, stored by TMA
-            const int t0 = (c_begin + it) * kC;
-            ok = wait_bar_warp(&o_full[pb], kb & 1, abort);
+            return zr;
+        };
+        // output rows of chunk it: num / (row sum + phi(Q).z_prev), either staged
+        // in the stage and stored by TMA, or each thread storing its own row;
+        // then the P/O buffer is handed back
+        const bool leader = tid == 32 * kWarpO;
+        if (leader && args.out && C::OUT_TMA) prefetch_tmap(&tm_o);
+        auto output_rows = [&](int it) {
+            const int pb = it % C::NPB, kb = it / C::NPB;
+            const int t = (c_begin + it) * kC + r;
+            uint8_t *stage_out = smem + (it % C::NS) * C::STAGE;
+            bool ok = wait_bar_warp(&o_full[pb], kb & 1, abort);
             if (!C::ZMMA) ok = ok && wait_bar_warp(&dz_ready[it % C::NDZ], (it / C::NDZ) & 1, abort);
-            if (tid == 32 * kWarpO + 32 * (4 - kWarpO % 4) % 128) LA_TRACE_AT(4, it, 3);
-            uint8_t *stage_out = C::NOB ? smem + C::OFF_OUT + (it % (C::NOB ? C::NOB : 1)) * C::OUT_TILE
-                                        : smem + s * C::STAGE;
-            if (C::NOB) o_sync();   // the store that last read this buffer has finished reading it
+            if (tracer) LA_TRACE_AT(4, it, 3);
             if (ok) {
                 tc_fence_after();
                 uint32_t dv[16];
@@ -749,11 +706,14 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     den = __uint_as_float(dv[0]) + __uint_as_float(zv[0]);
                 }
                 const float inv = 1.f / den;
+                uint4 *dst = !C::OUT_TMA && args.out && t < args.N
+                                 ? reinterpret_cast<uint4 *>(args.out + ((size_t)bh * args.N + t) * M)
+                                 : nullptr;
 #pragma unroll 1
                 for (int c0 = 0; c0 < M; c0 += 32) {
                     float o[32];
                     tmem_ld32f(tmem + lane_off + C::col_o(pb) + c0, o);
-                    if (args.has_out) {
+                    if (args.out) {
 #pragma unroll
                         for (int c8 = 0; c8 < 4; ++c8) {
                             const int c = c0 + 8 * c8;
@@ -762,65 +722,182 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                             w.y = pack_bf16x2(o[8 * c8 + 2] * inv, o[8 * c8 + 3] * inv);
                             w.z = pack_bf16x2(o[8 * c8 + 4] * inv, o[8 * c8 + 5] * inv);
                             w.w = pack_bf16x2(o[8 * c8 + 6] * inv, o[8 * c8 + 7] * inv);
-                            *reinterpret_cast<uint4 *>(stage_out + (c / 64) * kC * 128 + sw128_offset(r, c % 64)) = w;
+                            if (C::OUT_TMA)
+                                *reinterpret_cast<uint4 *>(stage_out + (c / 64) * kC * 128 + sw128_offset(r, c % 64)) = w;
+                            else if (dst)
+                                dst[c / 8] = w;
                         }
                     }
                 }
             }
             tc_fence_before();
             mbar_arrive(&o_free[pb]);
-            if (!C::NOB && it == n - 1) ok = ok && wait_bar_warp(s_full, it & 1, abort);   // last update read K, V
-            fence_proxy_async();
-            o_sync();
-            if (leader) {
-                if (ok && args.has_out) {
+            if (C::OUT_TMA) {
+                fence_proxy_async();
+                o_sync();
+                if (leader) {
+                    if (ok && args.out) {
 #pragma unroll
-                    for (int j = 0; j < M / 64; ++j) tma_store_3d(&tm_o, stage_out + j * kC * 128, j * 64, t0, bh);
-                    tma_store_commit();
-                }
-                if (C::NOB == 2) {
-                    tma_store_wait_read1();   // the other buffer is free for the next chunk
-                } else {
+                        for (int j = 0; j < M / 64; ++j)
+                            tma_store_3d(&tm_o, stage_out + j * kC * 128, j * 64, (c_begin + it) * kC, bh);
+                        tma_store_commit();
+                    }
                     tma_store_wait_read0();
-                    if (!C::NOB) mbar_arrive(&empty[s]);
+                    mbar_arrive(&empty[it % C::NS]);
                 }
             }
-            if (tid == 32 * kWarpO + 32 * (4 - kWarpO % 4) % 128) LA_TRACE_AT(4, it, 4);
-        }
-        if (leader && args.has_out) tma_store_wait_all0();
-        // ---- state after the last token (last segment only)
-        if (S_h && seg == args.nseg - 1 && n > 0) {
-            const bool ok = wait_bar_warp(s_full, (n - 1) & 1, abort);
-            if (ok && swarp) {
-                tc_fence_after();
+            if (tracer) LA_TRACE_AT(4, it, 4);
+        };
+
+        if (C::DS) {
+            // The state lives here in fp32: thread (q4, lane) owns row d of it,
+            // columns 32h..32h+31 (h = q4 / 2), and z_d when h = 0.  It reads the
+            // same row of each increment from accumulator lane 32 q4 + lane.
+            const int d = 32 * (q4 & 1) + lane, h = q4 >> 1;
+            float sv[32];
+            float zr = 0.f;
+            load_state32(d, 32 * h, sv);
+            if (h == 0) zr = load_z(d);
+            store_snap32<D>(snap_buf(0), d, 32 * h, sv);
+            if (h == 0) put_z(0, d, zr);
+            fence_proxy_async();
+            mbar_arrive(&snap_bar[0]);
+            for (int it = 0; it < n; ++it) {
+                if (tracer) LA_TRACE_AT(4, it, 0);
+                const bool ok = wait_bar_warp(&ds_full[it & 1], (it >> 1) & 1, abort);
+                if (tracer) LA_TRACE_AT(4, it, 1);
+                if (ok) {
+                    tc_fence_after();
+                    float dsv[32];
+                    tmem_ld32f(tmem + lane_off + C::col_ds(it) + 32 * h, dsv);
+                    if (h == 0) {    // warp-uniform: z is column M of the increment
+                        uint32_t zv[16];
+                        tmem_ld16(tmem + lane_off + C::col_ds(it) + M, zv);
+                        tmem_wait_ld();
+                        zr += __uint_as_float(zv[0]);
+                    }
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) sv[j] += dsv[j];
+                }
+                tc_fence_before();
+                mbar_arrive(&ds_free[it & 1]);
+                if (it + 1 < n) {
+                    // the buffer of snapshot it+1 was last read by the output MMAs
+                    // of chunk it-1, which completed before output_rows(it-1) ran
+                    store_snap32<D>(snap_buf(it + 1), d, 32 * h, sv);
+                    if (h == 0) put_z(it + 1, d, zr);
+                    fence_proxy_async();
+                    mbar_arrive(&snap_bar[(it + 1) & 1]);
+                }
+                if (tracer) LA_TRACE_AT(4, it, 2);
+                output_rows(it);
+            }
+            if (leader && C::OUT_TMA && args.out) tma_store_wait_all0();
+            // state after the last token (last segment only)
+            if (S_h && seg == args.nseg - 1 && n > 0 && !*abort) {
+#pragma unroll
+                for (int j = 0; j < 32; j += 4)
+                    *reinterpret_cast<float4 *>(S_h + d * M + 32 * h + j) = make_float4(sv[j], sv[j + 1], sv[j + 2], sv[j + 3]);
+                if (h == 0) z_h[d] = zr;
+            }
+        } else {
+            const bool srow = r < D;                 // owns a state row
+            const bool swarp = 32 * q4 < D;          // warp-uniform
+            // the state entering the segment into TMEM and snapshot 0
+            if (swarp) {
+                float zr = 0.f;
+                if (srow) {
+                    zr = load_z(r);
+                    put_z(0, r, zr);
+                }
 #pragma unroll 1
                 for (int c0 = 0; c0 < M; c0 += 32) {
                     float v[32];
-                    tmem_ld32f(tmem + lane_off + C::COL_S + c0, v);
-                    if (srow)
 #pragma unroll
-                        for (int j = 0; j < 32; j += 4)
-                            *reinterpret_cast<float4 *>(S_h + r * M + c0 + j) =
-                                make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+                    for (int j = 0; j < 32; ++j) v[j] = 0.f;
+                    if (srow) {
+                        load_state32(r, c0, v);
+                        store_snap32<D>(snap_buf(0), r, c0, v);
+                    }
+                    tmem_st32f(tmem + lane_off + C::COL_S + c0, v);
                 }
-                uint32_t zv[16];
-                tmem_ld16(tmem + lane_off + C::COL_Z, zv);
-                tmem_wait_ld();
-                if (srow) z_h[r] = __uint_as_float(zv[0]);
+                uint32_t w[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) w[j] = 0u;
+                w[0] = __float_as_uint(zr);
+                tmem_st16(tmem + lane_off + C::COL_Z, w);
+                tmem_wait_st();
+            }
+            tc_fence_before();
+            fence_proxy_async();
+            mbar_arrive(&snap_bar[0]);
+
+            for (int it = 0; it < n; ++it) {
+                const int pb = it % C::NPB, kb = it / C::NPB;
+                // ---- snapshot of the state after chunk it, for chunk it+1
+                if (tracer) LA_TRACE_AT(4, it, 0);
+                bool ok = wait_bar_warp(s_full, it & 1, abort);
+                if (!C::DB) ok = ok && wait_bar_warp(&o_full[pb], kb & 1, abort);   // single snapshot: read by O(it)
+                if (tracer) LA_TRACE_AT(4, it, 1);
+                if (it + 1 < n) {
+                    if (ok && swarp) {
+                        tc_fence_after();
+                        uint8_t *sb = snap_buf(it + 1);
+#pragma unroll 1
+                        for (int c0 = 0; c0 < M; c0 += 32) {
+                            float v[32];
+                            tmem_ld32f(tmem + lane_off + C::COL_S + c0, v);
+                            if (srow) store_snap32<D>(sb, r, c0, v);
+                        }
+                        uint32_t zv[16];
+                        tmem_ld16(tmem + lane_off + C::COL_Z, zv);
+                        tmem_wait_ld();
+                        if (srow) put_z(it + 1, r, __uint_as_float(zv[0]));
+                    }
+                    tc_fence_before();
+                    fence_proxy_async();
+                    mbar_arrive(&snap_bar[(it + 1) & 1]);
+                }
+                if (tracer) LA_TRACE_AT(4, it, 2);
+                output_rows(it);
+            }
+            if (leader && C::OUT_TMA && args.out) tma_store_wait_all0();
+            // ---- state after the last token (last segment only)
+            if (S_h && seg == args.nseg - 1 && n > 0) {
+                const bool ok = wait_bar_warp(s_full, (n - 1) & 1, abort);
+                if (ok && swarp) {
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int c0 = 0; c0 < M; c0 += 32) {
+                        float v[32];
+                        tmem_ld32f(tmem + lane_off + C::COL_S + c0, v);
+                        if (srow)
+#pragma unroll
+                            for (int j = 0; j < 32; j += 4)
+                                *reinterpret_cast<float4 *>(S_h + r * M + c0 + j) =
+                                    make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+                    }
+                    uint32_t zv[16];
+                    tmem_ld16(tmem + lane_off + C::COL_Z, zv);
+                    tmem_wait_ld();
+                    if (srow) z_h[r] = __uint_as_float(zv[0]);
+                }
             }
         }
     } else {
-        // ------------------------------------------------------ feature-map group
-        const int t = tid - 32 * kWarpPhi;
+        // ------------------------------------------------------ feature-map group(s)
+        // K rows past the sequence end are zeroed: they must add nothing
+        const int grp = (warp - kWarpPhi) / 4;   // 0: Q (and K with one group), 1: K
+        const int t = tid - 32 * (kWarpPhi + 4 * grp);
         for (int it = 0; it < n; ++it) {
             const int s = it % C::NS;
-            if (t == 0) LA_TRACE_AT(3, it, 0);
+            if (t == 0) LA_TRACE_AT(3, it, 3 * grp);
             if (wait_bar(&full[s], (it / C::NS) & 1, abort)) {
-                if (t == 0) LA_TRACE_AT(3, it, 1);
+                if (t == 0) LA_TRACE_AT(3, it, 3 * grp + 1);
                 uint8_t *st = smem + s * C::STAGE;
-                phi_tile<D>(st, t, kC);
-                phi_tile<D>(st + C::TILE_QK, t, min(kC, args.N - (c_begin + it) * kC));
-                if (t == 0) LA_TRACE_AT(3, it, 2);
+                if (grp == 0) phi_tile<D>(st, t, kC);
+                if (grp == C::NPHI - 1) phi_tile<D>(st + C::TILE_QK, t, min(kC, args.N - (c_begin + it) * kC));
+                if (t == 0) LA_TRACE_AT(3, it, 3 * grp + 2);
             }
             fence_proxy_async();
             mbar_arrive(&phi_done[s]);
@@ -1287,7 +1364,7 @@ cudaError_t launch_causal(const Problem &p, const DeviceInfo &dev) {
     if (p.out && !cached_tmap_bf16_3d(&to, p.out, M, p.N, p.BH, 64, kC)) return cudaErrorInvalidValue;
     if (!p.out) to = tq;   // never used
     CausalArgs a;
-    a.has_out = p.out != nullptr;
+    a.out = reinterpret_cast<__nv_bfloat16 *>(p.out);
     a.S = p.S;
     a.z = p.z;
     a.seg_ws = nseg > 1 ? (const float *)p.ws : nullptr;
@@ -1297,7 +1374,7 @@ cudaError_t launch_causal(const Problem &p, const DeviceInfo &dev) {
     a.err = dev.err_word;
     a.inject_ns = g_inject_timeout ? (uint64_t)g_inject_limit_us * 1000ull : 0ull;
     if ((e = set_smem(causal_tc_kernel<D, M>, C::SMEM)) != cudaSuccess) return e;
-    causal_tc_kernel<D, M><<<(unsigned)(p.BH * nseg), kThreadsCausal, C::SMEM, p.stream>>>(tq, tk, tv, to, a);
+    causal_tc_kernel<D, M><<<(unsigned)(p.BH * nseg), C::THREADS, C::SMEM, p.stream>>>(tq, tk, tv, to, a);
     count_launches(1);
     return cudaGetLastError();
 }
