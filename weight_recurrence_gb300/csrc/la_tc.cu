@@ -13,10 +13,10 @@
 // Exact in real arithmetic: the j <= i sum of eq. (9) is split at the chunk
 // start into the in-chunk part and the carried prefix state.  The non-causal
 // form (sec. 3.2 eq. (5)) is the same two summaries taken over all keys
-// (state_reduce_kernel) followed by the read-out phi(Q) S / phi(Q) z
-// (readout_kernel).
+// followed by the read-out phi(Q) S / phi(Q) z (noncausal_tc_kernel, one
+// launch, the CTAs of a head exchanging partial sums within a cluster).
 //
-// Roles of the causal CTA (480 threads):
+// Roles of the causal CTA (480 threads; 608 with two feature-map groups):
 //   warp 0      TMA producer: chunk tiles into a ring of NS stages, 128-byte
 //               swizzled (the tcgen05 canonical K-major layout);
 //   warp 1      P issuer (one thread): P = phi(Q) phi(K)^T as soon as the
@@ -33,7 +33,7 @@
 //               output rows and stores them straight to global memory;
 //   warps 11-14 feature-map group: applies phi in place to the Q and K tiles as
 //               they land, running ahead of the MMAs by up to NS chunks.
-// The reduction and read-out kernels use warps 0-9 the same way with one
+// The segment-sum and non-causal kernels use warps 0-9 the same way with one
 // epilogue group (320 threads).
 // The state S (D x M) and z (D) stay in TMEM in fp32 for the whole segment.
 // Long sequences with few heads are cut into segments; the state entering
@@ -1098,60 +1098,84 @@ state_reduce_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     if (warp == 0) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
-// ------------------------------------------------------- read-out kernel
-// Non-causal read-out: S = sum of the splits' partial sums, then for every
-// query row V'_i = phi(Q_i)^T S / phi(Q_i)^T z (sec. 3.2 eq. (5)).  The
-// snapshot is read as [S | z_hi z_lo] so that one MMA yields numerator and
-// denominator; output tiles are staged in the (dead) Q tile of their stage and
-// stored by TMA.  Two CTAs share an SM.
+// ------------------------------------------------ fused non-causal kernel
+// Non-causal attention, sec. 3.2 eq. (5), in one launch.  The CTAs of one
+// head form a thread-block cluster; CTA g of the cluster owns rows
+// [g * cps * C, (g + 1) * cps * C) of the head.
+//   phase 1: S_g = sum phi(K_j) V_j^T, z_g = sum phi(K_j) over its rows (fp32,
+//            TMEM), written to the workspace slot ws[bh][g];
+//   exchange: cluster barrier (release/acquire), then every CTA sums the
+//            cluster's G slots into a bf16 snapshot [S | z_hi z_lo];
+//   phase 2: for its rows, V'_i = phi(Q_i)^T S / phi(Q_i)^T z by one MMA of
+//            N = M + 16 per 128-row tile, divided, staged in the tile's slot
+//            and stored by TMA.
+// The producer streams the Q tiles of phase 2 into the ring as soon as the
+// K, V tiles of phase 1 release it, so the exchange overlaps their loads and
+// their feature map.  Warps: 0 producer, 1 MMA issuer, 2-5 epilogue group,
+// 6-9 feature-map group.
 
 template <int D, int M>
-struct OCfg {
-    static constexpr int TILE_Q = kC * D * 2;
-    static constexpr int SNAP = D * M * 2 + D * 128;   // M/64 state atoms then the z atom
-    static_assert(kC * M * 2 <= TILE_Q * 2, "output tile fits in the Q tiles of a stage");
-    static constexpr int STAGE = TILE_Q >= kC * M * 2 ? TILE_Q : kC * M * 2;
-    static constexpr int BUDGET = (int)kSmemMax / 2 - 1024;
-    static constexpr int NS_FIT = (BUDGET - SNAP - 256) / STAGE;
-    static constexpr int NS = NS_FIT > 4 ? 4 : (NS_FIT < 2 ? 2 : NS_FIT);
-    static constexpr int OFF_SNAP = NS * STAGE;
-    static constexpr int OFF_BAR = OFF_SNAP + SNAP;
-    static constexpr int NBARS = 3 * NS + 4 + 2;
+struct NCfg {
+    static constexpr int TILE_K = kC * D * 2;
+    static constexpr int TILE_V = kC * M * 2;
+    static constexpr int STAGE = TILE_K + TILE_V;       // also holds a Q tile and its output tile
+    static constexpr bool VONES = (M == 64);            // V read as [V | ones], z in column M
+    static constexpr int ONES = VONES ? kC * 128 : kOnesBytes;
+    static constexpr int SNAP = D * M * 2 + D * 128;    // M/64 state atoms then the z atom
+    // the ones tile is dead once phase 1's MMAs are done: the snapshot may reuse it
+    static constexpr bool SHARE = ONES >= SNAP;
+    static constexpr int CTAS_PER_SM = (D == 64 && M == 64) ? 2 : 1;
+    static constexpr int BUDGET = (int)kSmemMax / CTAS_PER_SM - 1024;
+    static constexpr int FIXED = (SHARE ? ONES : ONES + SNAP) + 256;
+    static constexpr int NS_FIT = (BUDGET - FIXED) / STAGE;
+    static constexpr int NS = NS_FIT > 4 ? 4 : NS_FIT;
+    static_assert(NS >= 2, "pipeline needs two stages");
+    static constexpr int OFF_ONES = NS * STAGE;
+    static constexpr int OFF_SNAP = SHARE ? OFF_ONES : OFF_ONES + ONES;
+    static constexpr int NBARS = 3 * NS + 2 + 2 + 4;
+    static constexpr int OFF_BAR = OFF_SNAP + (SHARE ? ONES : SNAP);
     static constexpr int OFF_TSLOT = OFF_BAR + 8 * NBARS;
     static constexpr int SMEM = OFF_TSLOT + 16;
-    static constexpr int NO = M + 16;                   // O columns per buffer (numerator, z_hi, z_lo)
-    static constexpr int NOBUF = 2 * NO <= 256 ? 2 : 1; // O buffers within 256 TMEM columns
-    static constexpr uint32_t TMEM_COLS = 256;
+    static_assert(SMEM <= BUDGET + 1024, "shared memory budget");
+    // TMEM: the phase-1 accumulator [S | z] at column 0, then (after it has
+    // been read out) the phase-2 output buffers of NO columns each
+    static constexpr uint32_t TMEM_COLS = CTAS_PER_SM == 2 ? 256 : 512;
+    static constexpr uint32_t COL_S = 0, COL_Z = M;
+    static constexpr int NO = M + 16;                   // numerator, z_hi, z_lo
+    static constexpr int NOBUF = 2 * NO <= (int)TMEM_COLS ? 2 : 1;
     static __device__ __forceinline__ uint32_t col_o(int b) { return (uint32_t)(b * NO); }
 };
 
-struct ReadoutArgs {
-    const float *ws;         // [BH, nsplit, D*M + D]
+struct NoncausalArgs {
+    float *ws;               // [BH, G, D*M + D]
     int N;
-    int nsplit;
-    int nrb;                 // CTAs per head
-    int cpr;                 // chunks per CTA
+    int G;                   // CTAs per head (cluster size)
+    int cps;                 // chunks per CTA
     int *err;
 };
 
 template <int D, int M>
-__global__ void __launch_bounds__(kThreads, 2)
-readout_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_o,
-               const ReadoutArgs args)
+__global__ void __launch_bounds__(kThreads, NCfg<D, M>::CTAS_PER_SM)
+noncausal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                    const NoncausalArgs args)
 {
-    using C = OCfg<D, M>;
+    using C = NCfg<D, M>;
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     volatile int *abort = reinterpret_cast<volatile int *>(smem + C::OFF_TSLOT + 4);
-    const int bh = blockIdx.x / args.nrb, rb = blockIdx.x % args.nrb;
+    const int bh = blockIdx.x / args.G, g = blockIdx.x % args.G;
     const int nch_total = (args.N + kC - 1) / kC;
-    const int c_begin = rb * args.cpr;
-    const int n = max(0, min(nch_total, c_begin + args.cpr) - c_begin);
+    const int c_begin = g * args.cps;
+    const int n = max(0, min(nch_total, c_begin + args.cps) - c_begin);
+    const int total = 2 * n;                 // ring slots used: n K/V tiles, then n Q tiles
 
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
     uint64_t *full = bar, *empty = bar + C::NS, *phi_done = bar + 2 * C::NS;
-    uint64_t *o_full = bar + 3 * C::NS, *o_free = o_full + 2, *snap_bar = o_free + 2, *drain = snap_bar + 1;
+    uint64_t *o_full = bar + 3 * C::NS, *o_free = o_full + 2;
+    uint64_t *init = o_free + 2, *red_done = init + 1, *snap_bar = red_done + 1, *drain = snap_bar + 1;
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + C::OFF_TSLOT);
+    uint8_t *ones = smem + C::OFF_ONES;
     uint8_t *snap = smem + C::OFF_SNAP;
 
     if (tid == 0) {
@@ -1159,52 +1183,98 @@ readout_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         if (*abort) record_error(args.err, kErrTimeout);
         for (int s = 0; s < C::NS; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);      // released by the epilogue after the store read its tile
+            mbar_init(&empty[s], 1);   // phase 1: MMA commit; phase 2: epilogue after the store read the tile
             mbar_init(&phi_done[s], kGrp);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&o_full[b], 1);
             mbar_init(&o_free[b], kGrp);
         }
+        mbar_init(init, kGrp);
+        mbar_init(red_done, 1);
         mbar_init(snap_bar, kGrp);
         mbar_init(drain, 1);
         fence_mbar_init();
     }
+    for (int i = tid; i < C::ONES / 4; i += kThreads) reinterpret_cast<uint32_t *>(ones)[i] = 0u;
+    __syncthreads();
+    for (int k = tid; k < C::ONES / 128; k += kThreads) *reinterpret_cast<uint16_t *>(ones + sw128_offset(k, 0)) = 0x3F80u;
     if (warp == 0) {
         tmem_alloc(tslot, C::TMEM_COLS);
         tmem_relinquish();
     }
+    fence_proxy_async();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
+    const bool epi = warp >= 2 && warp < 6;
+    // every thread arrives on the cluster barrier exactly once; the epilogue
+    // group only after its partial sums are in the workspace
+    if (!epi) cluster_arrive_release();
 
     if (warp == 0) {
+        // ------------------------------------------------------ producer
         if (lane == 0 && !*abort) {
             prefetch_tmap(&tm_q);
+            prefetch_tmap(&tm_k);
+            prefetch_tmap(&tm_v);
             int issued = 0;
-            for (int it = 0; it < n; ++it) {
-                const int s = it % C::NS, k = it / C::NS;
-                if (it >= C::NS && !wait_bar(&empty[s], (k - 1) & 1, abort)) break;
+            for (int idx = 0; idx < total; ++idx) {
+                const int s = idx % C::NS, k = idx / C::NS;
+                if (idx >= C::NS && !wait_bar(&empty[s], (k - 1) & 1, abort)) break;
                 uint8_t *st = smem + s * C::STAGE;
-                mbar_arrive_expect_tx(&full[s], C::TILE_Q);
+                if (idx < n) {
+                    const int t0 = (c_begin + idx) * kC;
+                    mbar_arrive_expect_tx(&full[s], C::STAGE);
 #pragma unroll
-                for (int j = 0; j < D / 64; ++j)
-                    tma_load_3d(st + j * kC * 128, &tm_q, &full[s], j * 64, (c_begin + it) * kC, bh);
+                    for (int j = 0; j < D / 64; ++j) tma_load_3d(st + j * kC * 128, &tm_k, &full[s], j * 64, t0, bh);
+#pragma unroll
+                    for (int j = 0; j < M / 64; ++j)
+                        tma_load_3d(st + C::TILE_K + j * kC * 128, &tm_v, &full[s], j * 64, t0, bh);
+                } else {
+                    const int t0 = (c_begin + idx - n) * kC;
+                    mbar_arrive_expect_tx(&full[s], C::TILE_K);
+#pragma unroll
+                    for (int j = 0; j < D / 64; ++j) tma_load_3d(st + j * kC * 128, &tm_q, &full[s], j * 64, t0, bh);
+                }
                 ++issued;
             }
             if (*abort)
-                for (int it = max(0, issued - C::NS); it < issued; ++it)
-                    mbar_wait_bounded(&full[it % C::NS], (it / C::NS) & 1, now_ns() + kWaitNs, nullptr);
+                for (int idx = max(0, issued - C::NS); idx < issued; ++idx)
+                    mbar_wait_bounded(&full[idx % C::NS], (idx / C::NS) & 1, now_ns() + kWaitNs, nullptr);
         }
     } else if (warp == 1) {
+        // ------------------------------------------------------ MMA issuer
         if (lane == 0 && !*abort) {
+            constexpr uint32_t ID_S = idesc_bf16(128, C::VONES ? M + 16 : M, 1, 1);
+            constexpr uint32_t ID_Z = idesc_bf16(128, 16, 1, 1);
             constexpr uint32_t ID_O = idesc_bf16(128, C::NO, 0, 1);
-            const uint32_t snap_a = smem_u32(snap);
-            bool ok = wait_bar(snap_bar, 0, abort);
+            const uint32_t ones_a = smem_u32(ones);
+            bool ok = wait_bar(init, 0, abort);   // accumulator zeroed
+            // phase 1: [S | z] += phi(K)^T [V | 1]
             for (int it = 0; ok && it < n; ++it) {
-                const int s = it % C::NS, ob = it % C::NOBUF, kb = it / C::NOBUF;
+                const int s = it % C::NS;
                 if (!(ok = wait_bar(&phi_done[s], (it / C::NS) & 1, abort))) break;
+                tc_fence_after();
+                const uint32_t ka = smem_u32(smem + s * C::STAGE), va = ka + C::TILE_K;
+                const uint64_t dk = smem_desc(ka, kC * 128, 1024);
+                const uint64_t dv = smem_desc(va, C::VONES ? ones_a - va : (uint32_t)(kC * 128), 1024);
+                const uint64_t dones = ones_desc(ones_a);
+#pragma unroll
+                for (int ks = 0; ks < kC / 16; ++ks) {
+                    mma_f16_ss(tmem + C::COL_S, dk + mnmajor_step(ks), dv + mnmajor_step(ks), ID_S, 1);
+                    if (!C::VONES) mma_f16_ss(tmem + C::COL_Z, dk + mnmajor_step(ks), dones, ID_Z, 1);
+                }
+                mma_commit(&empty[s]);
+            }
+            mma_commit(red_done);
+            // phase 2: O = phi(Q) [S | z_hi z_lo]
+            ok = ok && wait_bar(snap_bar, 0, abort);
+            const uint32_t snap_a = smem_u32(snap);
+            for (int i = 0; ok && i < n; ++i) {
+                const int idx = n + i, s = idx % C::NS, ob = i % C::NOBUF, kb = i / C::NOBUF;
+                if (!(ok = wait_bar(&phi_done[s], (idx / C::NS) & 1, abort))) break;
                 if (kb > 0 && !(ok = wait_bar(&o_free[ob], (kb - 1) & 1, abort))) break;
                 tc_fence_after();
                 const uint64_t dq = kmajor_base(smem_u32(smem + s * C::STAGE));
@@ -1214,48 +1284,115 @@ readout_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
                     mma_f16_ss(tmem + C::col_o(ob), dq + kmajor_step(ks), ds + mnmajor_step(ks), ID_O, ks > 0);
                 mma_commit(&o_full[ob]);
             }
-            mma_commit(drain);
+        }
+        if (lane == 0) {
+            mma_commit(drain);   // arrives once this thread's MMAs (if any) are done
             mbar_wait_bounded(drain, 0, now_ns() + kWaitNs, nullptr);
         }
-    } else if (warp < 6) {
+    } else if (epi) {
+        // ------------------------------------------------------ epilogue group
         const int q4 = warp & 3;
         const int r = 32 * q4 + lane;
         const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
+        const bool swarp = 32 * q4 < D;
         const bool leader = tid == 64;
-        // the state: sum of the splits, as bf16 [S | z_hi z_lo] (atoms D*128 bytes apart)
-        if (r < D) {
-            const float *src = args.ws + (size_t)bh * args.nsplit * (D * M + D);
-            float zr = 0.f;
-            for (int g = 0; g < args.nsplit; ++g) zr += src[(size_t)g * (D * M + D) + D * M + r];
-            uint8_t *za = snap + (M / 64) * D * 128;
-            for (int c = 0; c < 64; c += 8)
-                *reinterpret_cast<uint4 *>(za + sw128_offset(r, c)) = make_uint4(0u, 0u, 0u, 0u);
-            const __nv_bfloat16 hi = __float2bfloat16_rn(zr);
-            const __nv_bfloat16 lo = __float2bfloat16_rn(zr - __bfloat162float(hi));
-            *reinterpret_cast<__nv_bfloat16 *>(za + sw128_offset(r, 0)) = hi;
-            *reinterpret_cast<__nv_bfloat16 *>(za + sw128_offset(r, 1)) = lo;
+        constexpr int W = D * M + D;
+        float *slot = args.ws + ((size_t)bh * args.G + g) * W;
+        if (swarp) {
+            float zero[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) zero[j] = 0.f;
+            for (int c0 = 0; c0 < M + 16; c0 += 32) tmem_st32f(tmem + lane_off + c0, zero);
+            tmem_wait_st();
+        }
+        tc_fence_before();
+        mbar_arrive(init);
+        // this CTA's partial sums into its workspace slot
+        const bool ok1 = wait_bar_warp(red_done, 0, abort);
+        if (ok1 && swarp) {
+            tc_fence_after();
 #pragma unroll 1
             for (int c0 = 0; c0 < M; c0 += 32) {
                 float v[32];
+                tmem_ld32f(tmem + lane_off + C::COL_S + c0, v);
+                if (r < D)
 #pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] = 0.f;
-                for (int g = 0; g < args.nsplit; ++g) {
-                    const float *p = src + (size_t)g * (D * M + D) + r * M + c0;
+                    for (int j = 0; j < 32; j += 4)
+                        *reinterpret_cast<float4 *>(slot + r * M + c0 + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+            }
+            uint32_t zv[16];
+            tmem_ld16(tmem + lane_off + C::COL_Z, zv);
+            tmem_wait_ld();
+            if (r < D) slot[D * M + r] = __uint_as_float(zv[0]);
+        }
+        tc_fence_before();
+        __threadfence();
+        cluster_arrive_release();
+        cluster_wait_acquire();
+        // the head's state: sum of the cluster's slots, as bf16 [S | z_hi z_lo].
+        // All 128 threads take 16-column blocks (consecutive threads, consecutive
+        // blocks of a row) and load up to four slots' blocks before adding, so
+        // that the reads overlap instead of paying one L2 round trip each.
+        if (!*abort) {
+            const float *src = args.ws + (size_t)bh * args.G * W;
+            const int tg = tid - 64;
+            constexpr int BPR = M / 16;                  // 16-column blocks per row
+#pragma unroll 1
+            for (int b = tg; b < D * BPR; b += kGrp) {
+                const int row = b / BPR, c0 = (b % BPR) * 16;
+                float v[16];
 #pragma unroll
-                    for (int j = 0; j < 32; j += 4) {
-                        const float4 x = *reinterpret_cast<const float4 *>(p + j);
-                        v[j] += x.x; v[j + 1] += x.y; v[j + 2] += x.z; v[j + 3] += x.w;
+                for (int j = 0; j < 16; ++j) v[j] = 0.f;
+#pragma unroll 1
+                for (int j0 = 0; j0 < args.G; j0 += 4) {
+                    float4 x[4][4];
+#pragma unroll
+                    for (int a4 = 0; a4 < 4; ++a4) {
+                        const int js = min(j0 + a4, args.G - 1);   // in range; zeroed below if past G
+                        const float4 *p = reinterpret_cast<const float4 *>(src + (size_t)js * W + row * M + c0);
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) x[a4][q] = __ldcg(p + q);   // L2: written by other CTAs
+                        if (j0 + a4 >= args.G)
+#pragma unroll
+                            for (int q = 0; q < 4; ++q) x[a4][q] = make_float4(0.f, 0.f, 0.f, 0.f);
                     }
+#pragma unroll
+                    for (int a4 = 0; a4 < 4; ++a4)
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            v[4 * q] += x[a4][q].x; v[4 * q + 1] += x[a4][q].y;
+                            v[4 * q + 2] += x[a4][q].z; v[4 * q + 3] += x[a4][q].w;
+                        }
                 }
-                store_snap32<D>(snap, r, c0, v);
+#pragma unroll
+                for (int c8 = 0; c8 < 2; ++c8) {
+                    const int c = c0 + 8 * c8;
+                    uint4 w;
+                    w.x = pack_bf16x2(v[8 * c8], v[8 * c8 + 1]);
+                    w.y = pack_bf16x2(v[8 * c8 + 2], v[8 * c8 + 3]);
+                    w.z = pack_bf16x2(v[8 * c8 + 4], v[8 * c8 + 5]);
+                    w.w = pack_bf16x2(v[8 * c8 + 6], v[8 * c8 + 7]);
+                    *reinterpret_cast<uint4 *>(snap + (c / 64) * D * 128 + sw128_offset(row, c % 64)) = w;
+                }
+            }
+            if (r < D) {
+                float zr = 0.f;
+                for (int j = 0; j < args.G; ++j) zr += __ldcg(src + (size_t)j * W + D * M + r);
+                uint8_t *za = snap + (M / 64) * D * 128;
+                for (int c = 0; c < 64; c += 8)
+                    *reinterpret_cast<uint4 *>(za + sw128_offset(r, c)) = make_uint4(0u, 0u, 0u, 0u);
+                const __nv_bfloat16 hi = __float2bfloat16_rn(zr);
+                const __nv_bfloat16 lo = __float2bfloat16_rn(zr - __bfloat162float(hi));
+                *reinterpret_cast<__nv_bfloat16 *>(za + sw128_offset(r, 0)) = hi;
+                *reinterpret_cast<__nv_bfloat16 *>(za + sw128_offset(r, 1)) = lo;
             }
         }
         fence_proxy_async();
         mbar_arrive(snap_bar);
         if (leader) prefetch_tmap(&tm_o);
-        for (int it = 0; it < n; ++it) {
-            const int s = it % C::NS, ob = it % C::NOBUF, kb = it / C::NOBUF;
-            const int t0 = (c_begin + it) * kC;
+        for (int i = 0; i < n; ++i) {
+            const int idx = n + i, s = idx % C::NS, ob = i % C::NOBUF, kb = i / C::NOBUF;
+            const int t0 = (c_begin + i) * kC;
             uint8_t *tile = smem + s * C::STAGE;   // phi(Q) is dead once o_full fires
             const bool ok = wait_bar_warp(&o_full[ob], kb & 1, abort);
             if (ok) {
@@ -1296,14 +1433,21 @@ readout_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__
         }
         if (leader) tma_store_wait_all0();
     } else {
+        // ------------------------------------------------------ feature-map group
+        // phase 1 K tiles (rows past the sequence end zeroed: they must add
+        // nothing), then phase 2 Q tiles
         const int t = tid - 64 - kGrp;
-        for (int it = 0; it < n; ++it) {
-            const int s = it % C::NS;
-            if (wait_bar(&full[s], (it / C::NS) & 1, abort)) phi_tile<D>(smem + s * C::STAGE, t, kC);
+        for (int idx = 0; idx < total; ++idx) {
+            const int s = idx % C::NS;
+            if (wait_bar(&full[s], (idx / C::NS) & 1, abort)) {
+                if (idx < n) phi_tile<D>(smem + s * C::STAGE, t, min(kC, args.N - (c_begin + idx) * kC));
+                else phi_tile<D>(smem + s * C::STAGE, t, kC);
+            }
             fence_proxy_async();
             mbar_arrive(&phi_done[s]);
         }
     }
+    if (!epi) cluster_wait_acquire();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -1379,41 +1523,44 @@ cudaError_t launch_causal(const Problem &p, const DeviceInfo &dev) {
     return cudaGetLastError();
 }
 
-// Splits of the non-causal reduction and row blocks of the read-out, each
-// sized so that the grid covers the SMs once.
-void nc_grid(long long BH, int N, int sm_count, int &nsplit, int &cps, int &nrb, int &cpr) {
+// CTAs per head of the fused non-causal kernel (the cluster size, at most 8)
+// and chunks per CTA, sized so that the grid covers the CTA slots once.
+void nc_grid(long long BH, int N, int slots, int &G, int &cps) {
     const int nch = (N + kC - 1) / kC;
-    const int want = (int)std::max(1LL, (long long)sm_count / std::max(1LL, BH));
-    nsplit = std::max(1, std::min(want, nch));
-    cps = (nch + nsplit - 1) / nsplit;
-    nsplit = (nch + cps - 1) / cps;
-    nrb = std::max(1, std::min(want, nch));
-    cpr = (nch + nrb - 1) / nrb;
-    nrb = (nch + cpr - 1) / cpr;
+    const int want = (int)std::max(1LL, (long long)slots / std::max(1LL, BH));
+    G = std::max(1, std::min(std::min(want, 8), nch));
+    cps = (nch + G - 1) / G;
+    G = (nch + cps - 1) / cps;
 }
 
 template <int D, int M>
 cudaError_t launch_noncausal(const Problem &p, const DeviceInfo &dev) {
-    CUtensorMap tq, tk, tv;
+    using C = NCfg<D, M>;
+    CUtensorMap tq, tk, tv, to;
     if (!cached_tmap_bf16_3d(&tq, p.q, D, p.N, p.BH, 64, kC) || !cached_tmap_bf16_3d(&tk, p.k, D, p.N, p.BH, 64, kC) ||
-        !cached_tmap_bf16_3d(&tv, p.v, M, p.N, p.BH, 64, kC))
+        !cached_tmap_bf16_3d(&tv, p.v, M, p.N, p.BH, 64, kC) || !cached_tmap_bf16_3d(&to, p.out, M, p.N, p.BH, 64, kC))
         return cudaErrorInvalidValue;
-    int nsplit, cps, nrb, cpr;
-    nc_grid(p.BH, p.N, 2 * dev.sm_count, nsplit, cps, nrb, cpr);
-    CUtensorMap to;
-    if (!cached_tmap_bf16_3d(&to, p.out, M, p.N, p.BH, 64, kC)) return cudaErrorInvalidValue;
-    if (p.ws_bytes < (size_t)p.BH * nsplit * (D * M + D) * sizeof(float)) return cudaErrorInvalidValue;
+    int G, cps;
+    nc_grid(p.BH, p.N, C::CTAS_PER_SM * dev.sm_count, G, cps);
+    if (p.ws_bytes < (size_t)p.BH * G * (D * M + D) * sizeof(float)) return cudaErrorInvalidValue;
     cudaError_t e;
-    ReduceArgs r{(float *)p.ws, nullptr, nullptr, p.N, nsplit, nsplit, cps, -1, dev.err_word};
-    if ((e = set_smem(state_reduce_kernel<D, M>, RCfg<D, M>::SMEM)) != cudaSuccess) return e;
-    state_reduce_kernel<D, M><<<(unsigned)(p.BH * nsplit), kThreads, RCfg<D, M>::SMEM, p.stream>>>(tk, tv, r);
+    if ((e = set_smem(noncausal_tc_kernel<D, M>, C::SMEM)) != cudaSuccess) return e;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(p.BH * G));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::SMEM;
+    cfg.stream = p.stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)G;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const NoncausalArgs a{(float *)p.ws, p.N, G, cps, dev.err_word};
+    e = cudaLaunchKernelEx(&cfg, noncausal_tc_kernel<D, M>, tq, tk, tv, to, a);
     count_launches(1);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    ReadoutArgs o{(const float *)p.ws, p.N, nsplit, nrb, cpr, dev.err_word};
-    if ((e = set_smem(readout_kernel<D, M>, OCfg<D, M>::SMEM)) != cudaSuccess) return e;
-    readout_kernel<D, M><<<(unsigned)(p.BH * nrb), kThreads, OCfg<D, M>::SMEM, p.stream>>>(tq, to, o);
-    count_launches(1);
-    return cudaGetLastError();
+    return e;
 }
 
 bool tc_dims(const la_shape &s) {
@@ -1446,11 +1593,12 @@ cudaError_t tc_causal(const Problem &p, const DeviceInfo &dev) {
 bool tc_noncausal_supported(const la_shape &s) { return tc_dims(s); }
 
 size_t tc_noncausal_ws_bytes(const la_shape &s) {
+    // the cluster size nc_grid picks on any device (up to 192 SMs, two CTAs each)
     const long long BH = (long long)s.B * s.H;
     if (BH <= 0 || s.N <= 0) return 0;
     const long long nch = (s.N + kC - 1) / kC;
-    const long long nsplit = std::min(std::max(1LL, 2 * 192LL / BH), nch);
-    return (size_t)BH * nsplit * ((size_t)s.D * s.M + s.D) * sizeof(float);
+    const long long G = std::min(std::min(std::max(1LL, 2 * 192LL / BH), 8LL), nch);
+    return (size_t)BH * G * ((size_t)s.D * s.M + s.D) * sizeof(float);
 }
 
 cudaError_t tc_noncausal(const Problem &p, const DeviceInfo &dev) {

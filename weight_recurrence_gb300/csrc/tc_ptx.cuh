@@ -107,6 +107,14 @@ __device__ __forceinline__ void tma_store_wait_read1() {
 
 __device__ __forceinline__ void tma_store_wait_all0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// Thread-block cluster barrier, split into arrive (release: this thread's
+// earlier writes, global ones included, become visible to the cluster) and
+// wait (acquire).  Every thread of every CTA of the cluster must arrive once
+// per phase; the hardware barrier has no timeout, so callers arrive on every
+// path.
+__device__ __forceinline__ void cluster_arrive_release() { asm volatile("barrier.cluster.arrive.release;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait_acquire() { asm volatile("barrier.cluster.wait.acquire;" ::: "memory"); }
+
 __device__ __forceinline__ void prefetch_tmap(const void *tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
