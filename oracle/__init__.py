@@ -13,9 +13,15 @@ its Chinese translation):
 * ``definition`` (numpy, ``definition.py``): sec. 3.1 eq. (3) with
   sim(q, k) = phi(q)^T phi(k) (sec. 3.2 eq. (4)) and the causal mask of
   sec. 3.3 eq. (8), as a dense quadratic form.
+* ``causal_backward`` / ``noncausal_backward`` (C): gradients by the chain
+  rule through eqs. (10)-(12) (forward sweep for dQ, reverse cumulative sums
+  for dK, dV - the constant-memory scheme sec. 3.3.1 describes, whose own
+  equations (13)-(15) the page does not print).
 
 Parity status: pinned (see tests/test_oracle.py) by the hand-derived fixtures
-under tests/golden/, closed forms, invariants and planted-mistake checks.
+under tests/golden/, closed forms, invariants and planted-mistake checks; the
+backward (tests/test_oracle_backward.py) by central finite differences and by
+autograd of the definition form, closed forms and planted-mistake checks.
 """
 from __future__ import annotations
 
@@ -62,6 +68,12 @@ def _load():
                                           ctypes.c_int, ctypes.c_int]
         lib.lao_decode.restype = ctypes.c_int
         lib.lao_decode.argtypes = [f32p, f32p, f32p, L, L, L, dp, dp, dp, ctypes.c_int]
+        lib.lao_causal_backward_mut.restype = ctypes.c_int
+        lib.lao_causal_backward_mut.argtypes = [f32p, f32p, f32p, f32p, L, L, L, L, dp, dp, dp, dp,
+                                                dp, dp, dp, dp, dp, ctypes.c_int, ctypes.c_int]
+        lib.lao_noncausal_backward_mut.restype = ctypes.c_int
+        lib.lao_noncausal_backward_mut.argtypes = [f32p, f32p, f32p, f32p, L, L, L, L, dp, dp, dp,
+                                                   ctypes.c_int, ctypes.c_int]
         _lib = lib
     return _lib
 
@@ -143,8 +155,63 @@ def decode_step(q, k, v, S, z, nthreads=0):
     return y
 
 
+def _f64_or_none(x, shape):
+    if x is None:
+        return None
+    return np.ascontiguousarray(np.asarray(x.detach().cpu().double().numpy() if hasattr(x, "detach") else x,
+                                           np.float64).reshape(shape))
+
+
+def causal_backward(q, k, v, G, S0=None, z0=None, dSN=None, dzN=None, nthreads=0, mutant=0):
+    """Gradients through the causal form, eqs. (9)-(12), given G = dL/dV'.
+
+    q, k: [..., N, D]; v, G: [..., N, M].  S0/z0: carried-in state (or None);
+    dSN/dzN: gradient reaching the final state (or None).  Returns
+    (dq, dk, dv, dS0, dz0), all fp64; dS0/dz0 are dL/dS_0, dL/dZ_0."""
+    q, k, v, G = _f32(q), _f32(k), _f32(v), _f32(G)
+    lead = q.shape[:-2]
+    N, D = q.shape[-2], q.shape[-1]
+    M = v.shape[-1]
+    BH = int(np.prod(lead)) if lead else 1
+    dq = np.empty(lead + (N, D), np.float64)
+    dk = np.empty(lead + (N, D), np.float64)
+    dv = np.empty(lead + (N, M), np.float64)
+    dS0 = np.empty(lead + (D, M), np.float64)
+    dz0 = np.empty(lead + (D,), np.float64)
+    S0a, z0a = _f64_or_none(S0, lead + (D, M)), _f64_or_none(z0, lead + (D,))
+    dSa, dza = _f64_or_none(dSN, lead + (D, M)), _f64_or_none(dzN, lead + (D,))
+    rc = _load().lao_causal_backward_mut(q.reshape(-1), k.reshape(-1), v.reshape(-1), G.reshape(-1),
+                                         BH, N, D, M, _ptr(S0a), _ptr(z0a), _ptr(dSa), _ptr(dza),
+                                         _ptr(dq), _ptr(dk), _ptr(dv), _ptr(dS0), _ptr(dz0),
+                                         int(nthreads), int(mutant))
+    if rc != 0:
+        raise ValueError("oracle: bad shape")
+    return dq, dk, dv, dS0, dz0
+
+
+def noncausal_backward(q, k, v, G, nthreads=0, mutant=0):
+    """Gradients through the non-causal form, eq. (5), given G = dL/dV'.
+    Returns (dq, dk, dv) in fp64."""
+    q, k, v, G = _f32(q), _f32(k), _f32(v), _f32(G)
+    lead = q.shape[:-2]
+    N, D = q.shape[-2], q.shape[-1]
+    M = v.shape[-1]
+    BH = int(np.prod(lead)) if lead else 1
+    dq = np.empty(lead + (N, D), np.float64)
+    dk = np.empty(lead + (N, D), np.float64)
+    dv = np.empty(lead + (N, M), np.float64)
+    rc = _load().lao_noncausal_backward_mut(q.reshape(-1), k.reshape(-1), v.reshape(-1), G.reshape(-1),
+                                            BH, N, D, M, _ptr(dq), _ptr(dk), _ptr(dv),
+                                            int(nthreads), int(mutant))
+    if rc != 0:
+        raise ValueError("oracle: bad shape")
+    return dq, dk, dv
+
+
 # Planted-mistake identifiers of la_oracle.c (test use only).
 MUTANTS = {
     "relu": 1, "no_z_update": 2, "read_before_update": 3, "transpose_S": 4,
     "phi_sign": 5, "shifted_v": 6, "den_uses_k": 7,
+    # backward
+    "bwd_no_e": 11, "bwd_dphi_is_phi": 12, "bwd_excl_diag": 13, "bwd_dv_uses_q": 14,
 }

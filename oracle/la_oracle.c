@@ -25,6 +25,22 @@
  *   lao_decode     sec. 3.4, eqs. (18)-(20) for one time step; the residual and
  *                  f_l of eq. (20) belong to the surrounding layer and are left
  *                  out (the attention fraction only).
+ *   lao_causal_backward, lao_noncausal_backward
+ *                  gradients of a loss L through eqs. (9)-(12) (resp. eq. (5)),
+ *                  given G_i = dL/dV'_i.  Sec. 3.3.1 states that the gradient of
+ *                  the causal numerator is a cumulative sum computable with
+ *                  constant extra memory, but its equations (13)-(15) and its
+ *                  Algorithm 1 are not printed on the page; the steps below are
+ *                  the chain rule applied to eqs. (10)-(12), in their order:
+ *                    g_i = G_i / den_i,  e_i = -(g_i . num_i) / den_i
+ *                    dphi(Q_i) = S_i g_i + e_i Z_i             (forward sweep)
+ *                    R_i = sum_{j>=i} phi(Q_j) g_j^T, r_i = sum_{j>=i} e_j phi(Q_j)
+ *                    dphi(K_i) = R_i V_i + r_i,  dV_i = R_i^T phi(K_i)   (reverse sweep)
+ *                  and dQ = dphi(Q) * phi'(Q), dK = dphi(K) * phi'(K) with
+ *                  phi'(x) = 1 for x > 0, exp(x) else.  A carried-in state
+ *                  (S_0, Z_0) enters as in the forward; dL/dS_N, dL/dZ_N (the
+ *                  gradient arriving through the final state) start R and r,
+ *                  and R_1, r_1 are dL/dS_0, dL/dZ_0.
  *
  * Readings where the page is silent (each listed in the design notes):
  *   - no epsilon in any denominator (none of eqs. (4), (5), (9), (12) has one);
@@ -55,7 +71,12 @@ enum {
     MUT_TRANSPOSE_S = 4,   /* num_m = sum_d phi(q)_d S[m][d] (S transposed)    */
     MUT_PHI_NEG = 5,       /* phi(x) = exp(-x) for x <= 0 (sign slip)         */
     MUT_NO_DIAG_V = 6,     /* use V_{i-1} in place of V_i in the update       */
-    MUT_DEN_Q_OF_K = 7     /* denominator phi(K_i)^T Z_i instead of phi(Q_i)  */
+    MUT_DEN_Q_OF_K = 7,    /* denominator phi(K_i)^T Z_i instead of phi(Q_i)  */
+    /* backward */
+    MUT_B_NO_E = 11,       /* drop the denominator's term e_i                 */
+    MUT_B_DPHI_IS_PHI = 12,/* chain rule through phi instead of phi'          */
+    MUT_B_EXCL_DIAG = 13,  /* reverse sums over j > i instead of j >= i       */
+    MUT_B_DV_USES_Q = 14   /* dV_i = R_i^T phi(Q_i) instead of phi(K_i)       */
 };
 
 static double phi_m(double x, int mutant)
@@ -250,6 +271,177 @@ int lao_decode(const float *q, const float *k, const float *v,
             for (long d = 0; d < D; ++d) num += lao_phi((double)qh[d]) * Sh[d * M + m];
             y[h * M + m] = num / den;
         }
+    }
+    return 0;
+}
+
+
+/* phi'(x): 1 for x > 0, exp(x) for x <= 0 (elu with alpha = 1, plus one). */
+static double dphi_m(double x, int mutant)
+{
+    if (mutant == MUT_B_DPHI_IS_PHI) return lao_phi(x);
+    return x > 0.0 ? 1.0 : exp(x);
+}
+
+/*
+ * Backward of the causal form.  q, k, G (=dL/dout): [BH, N, D] / [BH, N, M];
+ * v: [BH, N, M].  S0 [BH, D, M], z0 [BH, D]: carried-in state or NULL (zero).
+ * dSN [BH, D, M], dzN [BH, D]: gradient reaching the final state or NULL.
+ * Outputs dq, dk [BH, N, D], dv [BH, N, M] (fp64) and, if non-NULL,
+ * dS0 [BH, D, M], dz0 [BH, D] (fp64).
+ */
+int lao_causal_backward_mut(const float *q, const float *k, const float *v, const float *G,
+                            long BH, long N, long D, long M,
+                            const double *S0, const double *z0, const double *dSN, const double *dzN,
+                            double *dq, double *dk, double *dv, double *dS0, double *dz0,
+                            int nthreads, int mutant)
+{
+    if (BH < 0 || N < 0 || D <= 0 || M <= 0) return 1;
+    set_threads(nthreads);
+    long h;
+#pragma omp parallel for schedule(static)
+    for (h = 0; h < BH; ++h) {
+        double *S = calloc((size_t)(D * M), sizeof(double));
+        double *z = calloc((size_t)D, sizeof(double));
+        double *g = malloc(sizeof(double) * (size_t)(N * M + 1));
+        double *e = malloc(sizeof(double) * (size_t)(N + 1));
+        double *fq = malloc(sizeof(double) * (size_t)D);
+        double *fk = malloc(sizeof(double) * (size_t)D);
+        double *num = malloc(sizeof(double) * (size_t)M);
+        const float *qh = q + h * N * D, *kh = k + h * N * D, *vh = v + h * N * M, *Gh = G + h * N * M;
+        if (S0) memcpy(S, S0 + h * D * M, sizeof(double) * (size_t)(D * M));
+        if (z0) memcpy(z, z0 + h * D, sizeof(double) * (size_t)D);
+        /* forward sweep: eqs. (10)-(12), then g_i, e_i and dphi(Q_i) */
+        for (long i = 0; i < N; ++i) {
+            for (long d = 0; d < D; ++d) {
+                fq[d] = lao_phi((double)qh[i * D + d]);
+                fk[d] = lao_phi((double)kh[i * D + d]);
+            }
+            for (long d = 0; d < D; ++d) {
+                for (long m = 0; m < M; ++m) S[d * M + m] += fk[d] * (double)vh[i * M + m];
+                z[d] += fk[d];
+            }
+            double den = 0.0;
+            for (long d = 0; d < D; ++d) den += fq[d] * z[d];
+            double gn = 0.0;
+            for (long m = 0; m < M; ++m) {
+                double t = 0.0;
+                for (long d = 0; d < D; ++d) t += fq[d] * S[d * M + m];
+                num[m] = t;
+                g[i * M + m] = (double)Gh[i * M + m] / den;
+                gn += g[i * M + m] * t;
+            }
+            e[i] = mutant == MUT_B_NO_E ? 0.0 : -gn / den;
+            for (long d = 0; d < D; ++d) {
+                double t = e[i] * z[d];
+                for (long m = 0; m < M; ++m) t += S[d * M + m] * g[i * M + m];
+                dq[(h * N + i) * D + d] = t * dphi_m((double)qh[i * D + d], mutant);
+            }
+        }
+        /* reverse sweep: R and r accumulate phi(Q_j) g_j^T and e_j phi(Q_j), j >= i */
+        double *R = S, *r = z;   /* reuse the buffers */
+        if (dSN) memcpy(R, dSN + h * D * M, sizeof(double) * (size_t)(D * M));
+        else memset(R, 0, sizeof(double) * (size_t)(D * M));
+        if (dzN) memcpy(r, dzN + h * D, sizeof(double) * (size_t)D);
+        else memset(r, 0, sizeof(double) * (size_t)D);
+        for (long i = N - 1; i >= 0; --i) {
+            for (long d = 0; d < D; ++d) {
+                fq[d] = lao_phi((double)qh[i * D + d]);
+                fk[d] = lao_phi((double)kh[i * D + d]);
+            }
+            if (mutant != MUT_B_EXCL_DIAG)
+                for (long d = 0; d < D; ++d) {
+                    for (long m = 0; m < M; ++m) R[d * M + m] += fq[d] * g[i * M + m];
+                    r[d] += e[i] * fq[d];
+                }
+            for (long d = 0; d < D; ++d) {
+                double t = r[d];
+                for (long m = 0; m < M; ++m) t += R[d * M + m] * (double)vh[i * M + m];
+                dk[(h * N + i) * D + d] = t * dphi_m((double)kh[i * D + d], mutant);
+            }
+            for (long m = 0; m < M; ++m) {
+                double t = 0.0;
+                for (long d = 0; d < D; ++d) t += R[d * M + m] * (mutant == MUT_B_DV_USES_Q ? fq[d] : fk[d]);
+                dv[(h * N + i) * M + m] = t;
+            }
+            if (mutant == MUT_B_EXCL_DIAG)
+                for (long d = 0; d < D; ++d) {
+                    for (long m = 0; m < M; ++m) R[d * M + m] += fq[d] * g[i * M + m];
+                    r[d] += e[i] * fq[d];
+                }
+        }
+        if (dS0) memcpy(dS0 + h * D * M, R, sizeof(double) * (size_t)(D * M));
+        if (dz0) memcpy(dz0 + h * D, r, sizeof(double) * (size_t)D);
+        free(S); free(z); free(g); free(e); free(fq); free(fk); free(num);
+    }
+    return 0;
+}
+
+/*
+ * Backward of the non-causal form, eq. (5): the same steps with every sum
+ * over all N keys: S, z are the full sums; R = sum_j phi(Q_j) g_j^T and
+ * r = sum_j e_j phi(Q_j) over all queries.
+ */
+int lao_noncausal_backward_mut(const float *q, const float *k, const float *v, const float *G,
+                               long BH, long N, long D, long M,
+                               double *dq, double *dk, double *dv, int nthreads, int mutant)
+{
+    if (BH < 0 || N < 0 || D <= 0 || M <= 0) return 1;
+    set_threads(nthreads);
+    long h;
+#pragma omp parallel for schedule(static)
+    for (h = 0; h < BH; ++h) {
+        double *S = calloc((size_t)(D * M), sizeof(double));
+        double *z = calloc((size_t)D, sizeof(double));
+        double *R = calloc((size_t)(D * M), sizeof(double));
+        double *r = calloc((size_t)D, sizeof(double));
+        double *fq = malloc(sizeof(double) * (size_t)D);
+        double *fk = malloc(sizeof(double) * (size_t)D);
+        double *g = malloc(sizeof(double) * (size_t)M);
+        const float *qh = q + h * N * D, *kh = k + h * N * D, *vh = v + h * N * M, *Gh = G + h * N * M;
+        for (long j = 0; j < N; ++j)
+            for (long d = 0; d < D; ++d) {
+                double f = lao_phi((double)kh[j * D + d]);
+                for (long m = 0; m < M; ++m) S[d * M + m] += f * (double)vh[j * M + m];
+                z[d] += f;
+            }
+        for (long i = 0; i < N; ++i) {
+            for (long d = 0; d < D; ++d) fq[d] = lao_phi((double)qh[i * D + d]);
+            double den = 0.0;
+            for (long d = 0; d < D; ++d) den += fq[d] * z[d];
+            double gn = 0.0;
+            for (long m = 0; m < M; ++m) {
+                double t = 0.0;
+                for (long d = 0; d < D; ++d) t += fq[d] * S[d * M + m];
+                g[m] = (double)Gh[i * M + m] / den;
+                gn += g[m] * t;
+            }
+            const double e = mutant == MUT_B_NO_E ? 0.0 : -gn / den;
+            for (long d = 0; d < D; ++d) {
+                double t = e * z[d];
+                for (long m = 0; m < M; ++m) t += S[d * M + m] * g[m];
+                dq[(h * N + i) * D + d] = t * dphi_m((double)qh[i * D + d], mutant);
+                for (long m = 0; m < M; ++m) R[d * M + m] += fq[d] * g[m];
+                r[d] += e * fq[d];
+            }
+        }
+        for (long j = 0; j < N; ++j) {
+            for (long d = 0; d < D; ++d) {
+                fk[d] = lao_phi((double)kh[j * D + d]);
+                fq[d] = lao_phi((double)qh[j * D + d]);
+            }
+            for (long d = 0; d < D; ++d) {
+                double t = r[d];
+                for (long m = 0; m < M; ++m) t += R[d * M + m] * (double)vh[j * M + m];
+                dk[(h * N + j) * D + d] = t * dphi_m((double)kh[j * D + d], mutant);
+            }
+            for (long m = 0; m < M; ++m) {
+                double t = 0.0;
+                for (long d = 0; d < D; ++d) t += R[d * M + m] * (mutant == MUT_B_DV_USES_Q ? fq[d] : fk[d]);
+                dv[(h * N + j) * M + m] = t;
+            }
+        }
+        free(S); free(z); free(R); free(r); free(fq); free(fk); free(g);
     }
     return 0;
 }
