@@ -67,7 +67,13 @@ typedef enum {
 
 typedef enum { LA_DTYPE_F32 = 0, LA_DTYPE_BF16 = 1 } la_dtype;
 
-typedef enum { LA_OP_NONCAUSAL = 0, LA_OP_CAUSAL = 1, LA_OP_DECODE = 2 } la_op;
+typedef enum {
+    LA_OP_NONCAUSAL = 0,
+    LA_OP_CAUSAL = 1,
+    LA_OP_DECODE = 2,
+    LA_OP_NONCAUSAL_BWD = 3,
+    LA_OP_CAUSAL_BWD = 4
+} la_op;
 
 typedef struct {
     int B, H, N, D, M;
@@ -120,12 +126,50 @@ la_status la_decode_step(const void *q, const void *k, const void *v, void *y,
                          float *S, float *z, la_shape s, la_stream_t stream);
 
 /*
+ * Backward of the causal form (the gradient sec. 3.3.1 computes as cumulative
+ * sums in constant extra memory; its eqs. (13)-(15) are not printed on the
+ * page, so this is the chain rule through eqs. (10)-(12)).  Given
+ * dout = dL/dV' it writes dq, dk, dv = dL/dQ, dL/dK, dL/dV:
+ *   g_i = dout_i / den_i,  e_i = -(g_i . num_i) / den_i,
+ *   dphi(Q_i) = S_i g_i + e_i Z_i                       (forward sweep)
+ *   R_i = sum_{j>=i} phi(Q_j) g_j^T,  r_i = sum_{j>=i} e_j phi(Q_j)
+ *   dphi(K_i) = R_i V_i + r_i,  dV_i = R_i^T phi(K_i)    (reverse sweep)
+ * and dQ = dphi(Q) phi'(Q), dK = dphi(K) phi'(K), phi'(x) = 1 (x > 0), e^x.
+ *   q, k, dq, dk: [B,H,N,D]; v, dout, dv: [B,H,N,M], all of dtype s.dtype;
+ *   the gradients may not alias the inputs or each other.
+ *   S0, z0: [B,H,D,M], [B,H,D] fp32, the state the forward started from
+ *      (both NULL: zero); dSN, dzN: gradient reaching the forward's final
+ *      state (both NULL: zero); dS0, dz0: receive dL/dS_0, dL/dZ_0 (both NULL:
+ *      not wanted).  Chaining the backward of consecutive segments through
+ *      dS0 -> dSN reproduces the backward of the whole sequence.
+ *   workspace: la_workspace_bytes(LA_OP_CAUSAL_BWD, s, 0) bytes: g and e of
+ *      every token, B*H*N*(M+1) floats (no per-token state is stored).
+ * Arithmetic fp32 on CUDA cores; errors as la_forward_causal.
+ */
+la_status la_backward_causal(const void *q, const void *k, const void *v, const void *dout,
+                             void *dq, void *dk, void *dv, la_shape s,
+                             const float *S0, const float *z0, const float *dSN, const float *dzN,
+                             float *dS0, float *dz0, void *workspace, size_t ws_bytes,
+                             la_stream_t stream);
+
+/*
+ * Backward of the non-causal form, sec. 3.2 eq. (5): the same steps with the
+ * sums over all N keys (S, Z the full sums, R and r summed over all queries).
+ *   Arguments as la_backward_causal without the state ones;
+ *   workspace: la_workspace_bytes(LA_OP_NONCAUSAL_BWD, s, 0) bytes.
+ */
+la_status la_backward_noncausal(const void *q, const void *k, const void *v, const void *dout,
+                                void *dq, void *dk, void *dv, la_shape s,
+                                void *workspace, size_t ws_bytes, la_stream_t stream);
+
+/*
  * Non-causal attention that allocates nothing, for callers that cannot
  * allocate device memory: code that only receives pointers from a host
  * framework owning the device memory pool, or a loop that must not call the
  * allocator once it is running (cudaMalloc and cudaFree synchronise the
- * device).  No counterpart in the paper: it computes exactly what
- * la_forward_noncausal computes (the same kernels), but its fp32 partial sums
+ * device).  No counterpart in the paper: it computes what
+ * la_forward_noncausal computes (on the CUDA-core kernels, with the number of
+ * key splits capped so that the partial sums fit), but its fp32 partial sums
  * live in an 8 MiB array compiled into this library (a file-scope __device__
  * array, held by every GPU that loads the library until the process exits)
  * instead of a caller workspace.

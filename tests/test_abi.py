@@ -106,3 +106,40 @@ def test_empty_problems_are_noops(lib):
     assert lib.la_forward_causal(None, None, None, None, _shape(N=0), 0, None, None, None, 0, None) == la.LA_OK
     assert lib.la_forward_noncausal(None, None, None, None, _shape(B=0), None, 0, None) == la.LA_OK
     assert lib.la_decode_step(None, None, None, None, None, None, _shape(H=0), None) == la.LA_OK
+
+
+def _addr(i):
+    return ctypes.c_void_p(0x100000 * (i + 1))
+
+
+def test_backward_argument_checks(lib):
+    sh = _shape(N=64, D=16, M=16)
+    q, k, v, g, dq, dk, dv = (_addr(i) for i in range(7))
+    ws_c = la.la_workspace_bytes(la.LA_OP_CAUSAL_BWD, sh)
+    ws_n = la.la_workspace_bytes(la.LA_OP_NONCAUSAL_BWD, sh)
+    assert ws_c == 1 * 1 * 64 * (16 + 1) * 4        # g and e of every token
+    assert ws_n > 0
+    args = (q, k, v, g, dq, dk, dv, sh)
+    # exactly one of each state pair given
+    for pos in range(6):
+        st = [None] * 6
+        st[pos] = FAKE
+        assert lib.la_backward_causal(*args, *st, _addr(9), ws_c, None) == la.LA_ERR_INVALID_ARG
+    # workspace too small / missing
+    assert lib.la_backward_causal(*args, None, None, None, None, None, None, _addr(9), ws_c - 4, None) \
+        == la.LA_ERR_INVALID_ARG
+    assert lib.la_backward_noncausal(*args, None, 0, None) == la.LA_ERR_INVALID_ARG
+    # gradient aliasing an input, or another gradient
+    assert lib.la_backward_causal(q, k, v, g, k, dk, dv, sh, None, None, None, None, None, None, _addr(9), ws_c,
+                                  None) == la.LA_ERR_INVALID_ARG
+    assert lib.la_backward_noncausal(q, k, v, g, dq, dq, dv, sh, _addr(9), ws_n, None) == la.LA_ERR_INVALID_ARG
+    # misaligned input, unsupported width
+    assert lib.la_backward_noncausal(MISALIGNED, k, v, g, dq, dk, dv, sh, _addr(9), ws_n, None) \
+        == la.LA_ERR_INVALID_ARG
+    assert lib.la_backward_causal(*args[:7], _shape(D=48), None, None, None, None, None, None, None, 0, None) \
+        == la.LA_ERR_UNSUPPORTED
+    # empty problems launch nothing
+    assert lib.la_backward_noncausal(None, None, None, None, None, None, None, _shape(N=0), None, 0, None) \
+        == la.LA_OK
+    assert lib.la_backward_causal(None, None, None, None, None, None, None, _shape(B=0), None, None, None, None,
+                                  None, None, None, 0, None) == la.LA_OK

@@ -108,8 +108,85 @@ size_t la_workspace_bytes(la_op op, la_shape s, int chunk) {
             if (tc_causal_supported(s, chunk)) return tc_causal_ws_bytes(s, chunk);
             return 0;
         case LA_OP_DECODE: return 0;
+        case LA_OP_NONCAUSAL_BWD: return noncausal_bwd_ws_bytes(s);
+        case LA_OP_CAUSAL_BWD: return causal_bwd_ws_bytes(s);
     }
     return (size_t)-1;
+}
+
+namespace {
+
+// Checks common to both backward calls; fills the device-side problem.
+la_status check_backward(const void *q, const void *k, const void *v, const void *dout, void *dq, void *dk,
+                         void *dv, const la_shape &s, la_op op, void *workspace, size_t ws_bytes, bool &work) {
+    la_status st = check_shape(s, true);
+    if (st != LA_OK) return st;
+    const long long BH = (long long)s.B * s.H;
+    work = BH > 0 && s.N > 0;
+    if ((st = check_ptr(q, work)) || (st = check_ptr(k, work)) || (st = check_ptr(v, work)) ||
+        (st = check_ptr(dout, work)) || (st = check_ptr(dq, work)) || (st = check_ptr(dk, work)) ||
+        (st = check_ptr(dv, work)))
+        return st;
+    if (!work) return LA_OK;
+    // the gradients must not overlap the inputs or each other
+    const void *ins[4] = {q, k, v, dout};
+    const void *outs[3] = {dq, dk, dv};
+    for (const void *o : outs)
+        for (const void *i : ins)
+            if (o == i) return LA_ERR_INVALID_ARG;
+    if (dq == dk || dq == dv || dk == dv) return LA_ERR_INVALID_ARG;
+    const size_t need = la_workspace_bytes(op, s, 0);
+    if (ws_bytes < need || (need > 0 && check_ptr(workspace, true) != LA_OK)) return LA_ERR_INVALID_ARG;
+    return LA_OK;
+}
+
+}  // namespace
+
+la_status la_backward_noncausal(const void *q, const void *k, const void *v, const void *dout, void *dq,
+                                void *dk, void *dv, la_shape s, void *workspace, size_t ws_bytes,
+                                la_stream_t stream) {
+    bool work = false;
+    la_status st = check_backward(q, k, v, dout, dq, dk, dv, s, LA_OP_NONCAUSAL_BWD, workspace, ws_bytes, work);
+    if (st != LA_OK || !work) return st;
+    const DeviceInfo *dev = device_info();
+    if (!dev) return LA_ERR_CUDA;
+    BwdProblem p{q, k, v, dout, dq, dk, dv, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
+                 (long long)s.B * s.H, s.N, s.D, s.M, s.dtype, workspace, ws_bytes, (cudaStream_t)stream};
+    return from_cuda(noncausal_backward(p, *dev));
+}
+
+la_status la_backward_causal(const void *q, const void *k, const void *v, const void *dout, void *dq,
+                             void *dk, void *dv, la_shape s, const float *S0, const float *z0,
+                             const float *dSN, const float *dzN, float *dS0, float *dz0, void *workspace,
+                             size_t ws_bytes, la_stream_t stream) {
+    if ((S0 == nullptr) != (z0 == nullptr) || (dSN == nullptr) != (dzN == nullptr) ||
+        (dS0 == nullptr) != (dz0 == nullptr))
+        return LA_ERR_INVALID_ARG;
+    bool work = false;
+    la_status st = check_backward(q, k, v, dout, dq, dk, dv, s, LA_OP_CAUSAL_BWD, workspace, ws_bytes, work);
+    if (st != LA_OK) return st;
+    const long long BH = (long long)s.B * s.H;
+    for (const void *p : {(const void *)S0, (const void *)z0, (const void *)dSN, (const void *)dzN,
+                          (const void *)dS0, (const void *)dz0})
+        if ((st = check_ptr(p, p != nullptr && BH > 0)) != LA_OK) return st;
+    if (!work) {
+        // an empty sequence passes the final-state gradient straight through
+        if (dS0 && BH > 0) {
+            const size_t nS = (size_t)BH * s.D * s.M * sizeof(float), nz = (size_t)BH * s.D * sizeof(float);
+            cudaStream_t cs = (cudaStream_t)stream;
+            cudaError_t e = dSN ? cudaMemcpyAsync(dS0, dSN, nS, cudaMemcpyDeviceToDevice, cs)
+                                : cudaMemsetAsync(dS0, 0, nS, cs);
+            if (e == cudaSuccess)
+                e = dzN ? cudaMemcpyAsync(dz0, dzN, nz, cudaMemcpyDeviceToDevice, cs) : cudaMemsetAsync(dz0, 0, nz, cs);
+            return from_cuda(e);
+        }
+        return LA_OK;
+    }
+    const DeviceInfo *dev = device_info();
+    if (!dev) return LA_ERR_CUDA;
+    BwdProblem p{q, k, v, dout, dq, dk, dv, S0, z0, dSN, dzN, dS0, dz0,
+                 BH, s.N, s.D, s.M, s.dtype, workspace, ws_bytes, (cudaStream_t)stream};
+    return from_cuda(causal_backward(p));
 }
 
 la_status la_forward_noncausal(const void *q, const void *k, const void *v, void *out, la_shape s,

@@ -35,6 +35,27 @@ struct Problem {
     cudaStream_t stream;
 };
 
+// Backward-pass problem (sizes already validated).
+struct BwdProblem {
+    const void *q, *k, *v, *dout;
+    void *dq, *dk, *dv;
+    const float *S0, *z0;      // carried-in state of the forward (causal), may be null
+    const float *dSN, *dzN;    // gradient reaching the final state (causal), may be null
+    float *dS0, *dz0;          // gradient of the carried-in state (causal), may be null
+    long long BH;
+    int N, D, M;
+    la_dtype dtype;
+    void *ws;
+    size_t ws_bytes;
+    cudaStream_t stream;
+};
+
+// ---- backward (la_bwd.cu): CUDA cores, any D, M in {16,32,64,128}, fp32 or bf16.
+size_t causal_bwd_ws_bytes(const la_shape &s);
+size_t noncausal_bwd_ws_bytes(const la_shape &s);
+cudaError_t causal_backward(const BwdProblem &p);
+cudaError_t noncausal_backward(const BwdProblem &p, const DeviceInfo &dev);
+
 // ---- SIMT kernels (la_simt.cu): any D, M in {16,32,64,128}, fp32 or bf16.
 size_t simt_noncausal_ws_bytes(const la_shape &s);
 cudaError_t simt_noncausal(const Problem &p, const DeviceInfo &dev);

@@ -18,11 +18,12 @@ LIB_PATH = os.path.join(_PKG, "lib", "liblinattn.so")
 
 LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_CUDA, LA_ERR_TIMEOUT = range(5)
 LA_DTYPE_F32, LA_DTYPE_BF16 = 0, 1
-LA_OP_NONCAUSAL, LA_OP_CAUSAL, LA_OP_DECODE = 0, 1, 2
+LA_OP_NONCAUSAL, LA_OP_CAUSAL, LA_OP_DECODE, LA_OP_NONCAUSAL_BWD, LA_OP_CAUSAL_BWD = 0, 1, 2, 3, 4
 
 EXPORTED = ("la_workspace_bytes", "la_forward_noncausal", "la_forward_causal", "la_decode_step",
             "la_get_last_error", "la_status_string", "la_version", "la_launch_count",
-            "la_debug_inject_timeout", "la_forward_noncausal_noalloc")
+            "la_debug_inject_timeout", "la_forward_noncausal_noalloc", "la_backward_causal",
+            "la_backward_noncausal")
 
 
 class LAError(RuntimeError):
@@ -66,6 +67,10 @@ def lib() -> ctypes.CDLL:
         L.la_forward_noncausal_noalloc.argtypes = [vp, vp, vp, vp, la_shape, vp]
         L.la_debug_inject_timeout.restype = None
         L.la_debug_inject_timeout.argtypes = [i, i]
+        L.la_backward_causal.restype = i
+        L.la_backward_causal.argtypes = [vp, vp, vp, vp, vp, vp, vp, la_shape, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.la_backward_noncausal.restype = i
+        L.la_backward_noncausal.argtypes = [vp, vp, vp, vp, vp, vp, vp, la_shape, vp, sz, vp]
         _lib = L
     return _lib
 
@@ -200,6 +205,44 @@ def la_decode_step(q, k, v, S, z, y=None, stream=None):
                               _stream(stream, q.device))
     _check(st, "la_decode_step")
     return y
+
+
+def la_backward_causal(q, k, v, dout, dq=None, dk=None, dv=None, S0=None, z0=None, dSN=None, dzN=None,
+                       dS0=None, dz0=None, stream=None):
+    """Gradients dq, dk, dv of the causal form given dout = dL/dV'.  S0/z0: the
+    state the forward started from; dSN/dzN: gradient reaching its final
+    state; dS0/dz0 (fp32, written): gradient of the starting state."""
+    _contig(q, k, v, dout, S0, z0, dSN, dzN, dS0, dz0)
+    s = shape_of(q, v)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _contig(dq, dk, dv)
+    need = la_workspace_bytes(LA_OP_CAUSAL_BWD, s, 0)
+    sp = _stream_ptr(stream, q.device)
+    ws = _workspace(need, q.device, sp)
+    st = lib().la_backward_causal(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), s,
+                                  _ptr(S0), _ptr(z0), _ptr(dSN), _ptr(dzN), _ptr(dS0), _ptr(dz0),
+                                  _ptr(ws), need, ctypes.c_void_p(sp))
+    _check(st, "la_backward_causal")
+    return dq, dk, dv
+
+
+def la_backward_noncausal(q, k, v, dout, dq=None, dk=None, dv=None, stream=None):
+    """Gradients dq, dk, dv of the non-causal form given dout = dL/dV'."""
+    _contig(q, k, v, dout)
+    s = shape_of(q, v)
+    dq = torch.empty_like(q) if dq is None else dq
+    dk = torch.empty_like(k) if dk is None else dk
+    dv = torch.empty_like(v) if dv is None else dv
+    _contig(dq, dk, dv)
+    need = la_workspace_bytes(LA_OP_NONCAUSAL_BWD, s, 0)
+    sp = _stream_ptr(stream, q.device)
+    ws = _workspace(need, q.device, sp)
+    st = lib().la_backward_noncausal(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), _ptr(dq), _ptr(dk), _ptr(dv), s,
+                                     _ptr(ws), need, ctypes.c_void_p(sp))
+    _check(st, "la_backward_noncausal")
+    return dq, dk, dv
 
 
 def la_get_last_error(stream=None, device=None) -> int:
