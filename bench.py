@@ -234,6 +234,10 @@ def run_ours(args, rank, world, dist):
 
     if args.only:
         # one workload alone, for profiler captures: no clocks, e2e or CPU legs
+        if args.only.startswith("backward_"):
+            leg = _leg_backward(torch, la, inputs, args.only[len("backward_"):], dev, stream, flush, pk,
+                                args.steps, max_over_ranks, world, rank, warmup=args.warmup)
+            return {"only": args.only, "leg": leg, "gpu_launches_total": la.la_launch_count()}
         w = inputs.WORKLOADS[args.only]
         if w.op == "decode":
             leg = _leg_decode(torch, la, inputs, dev, stream, flush, pk, args, max_over_ranks, world, rank)
@@ -352,6 +356,8 @@ def run_ours(args, rank, world, dist):
                                                  flush, pk, 5, max_over_ranks, world, rank)
         result["legs"]["decode"] = _leg_decode(torch, la, inputs, dev, stream, flush, pk, args,
                                                max_over_ranks, world, rank)
+        result["legs"]["backward"] = _leg_backward(torch, la, inputs, MAIN, dev, stream, flush, pk, 5,
+                                                   max_over_ranks, world, rank)
 
     # ------------------------------------------------- CPU baseline (rank 0)
     if rank == 0 and not args.no_cpu:
@@ -379,6 +385,35 @@ def _leg_fwd(torch, la, inputs, name, dev, stream, flush, pk, steps, max_over_ra
                         "frac": round(gbs / pk["hbm_gbs"], 4), "traffic": _traffic(w.op + "_" + name)},
            "alg_tflops": round(_alg_flops_fwd(w) / (ms / 1e3) / 1e12, 2), "l2": flush.describe(in_bytes)}
     del q, k, v, out
+    torch.cuda.empty_cache()
+    return leg
+
+
+def _leg_backward(torch, la, inputs, name, dev, stream, flush, pk, steps, max_over_ranks, world, rank, warmup=3):
+    """Causal backward (dQ, dK, dV from dL/dV') on a forward workload's shape."""
+    w = inputs.WORKLOADS[name]
+    q, k, v = [t.to(dev) for t in inputs.workload_inputs(w, rank)]
+    g = torch.Generator(device=dev).manual_seed(inputs.rank_seed(w.seed + 2000, rank))
+    G = torch.randn(v.shape, generator=g, device=dev).to(w.dtype)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    fn = lambda: la.la_backward_causal(q, k, v, G, dq=dq, dk=dk, dv=dv, stream=stream)  # noqa: E731
+    in_bytes = 4 * q.numel() * q.element_size()
+    l0 = la.la_launch_count()
+    t = _timed_steps(torch, fn, steps, warmup, flush.for_inputs(in_bytes), stream)
+    launches = (la.la_launch_count() - l0) // (steps + warmup)
+    ms = max_over_ranks(sum(t) / len(t))
+    el = q.element_size()
+    alg = w.B * w.H * w.N * (4 * w.D + 3 * w.M) * el      # read Q, K, V, dO; write dQ, dK, dV
+    gbs = alg / (ms / 1e3) / 1e9
+    leg = {"workload": name, "op": "causal_backward", "value": round(world * w.B * w.N / (ms / 1e3), 1),
+           "unit": "tokens/s", "ms_per_step": round(ms, 5), "steps": steps, "launches_per_step": launches,
+           "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                        "frac": round(gbs / pk["hbm_gbs"], 4), "traffic": _traffic("backward_" + name),
+                        "alg_bytes_per_launch": alg},
+           "l2": flush.describe(in_bytes),
+           "note": "tcgen05 kernels (bf16 D = M = 64): a forward sweep (dQ, keeps g and e) and a reverse "
+                   "sweep (dK, dV), one CTA per head each"}
+    del q, k, v, G, dq, dk, dv
     torch.cuda.empty_cache()
     return leg
 
@@ -521,7 +556,7 @@ def main():
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--only", default=None,
                     choices=["causal_b16h8n3072d64", "noncausal_b8h8n4096d64", "causal_b1h16n65536d128",
-                             "decode_b256h16d64"],
+                             "decode_b256h16d64", "backward_causal_b16h8n3072d64"],
                     help="time this one workload alone (--steps/--warmup; decode: --decode-steps) and print "
                          "its leg object; for profiler captures, not a bench line")
     args = ap.parse_args()

@@ -117,7 +117,8 @@ def test_backward_argument_checks(lib):
     q, k, v, g, dq, dk, dv = (_addr(i) for i in range(7))
     ws_c = la.la_workspace_bytes(la.LA_OP_CAUSAL_BWD, sh)
     ws_n = la.la_workspace_bytes(la.LA_OP_NONCAUSAL_BWD, sh)
-    assert ws_c == 1 * 1 * 64 * (16 + 1) * 4        # g and e of every token
+    # g and e of every token, and two segment sums (one segment at N = 64)
+    assert ws_c == 1 * 1 * 64 * (16 + 1) * 4 + 2 * (16 * 16 + 16) * 4
     assert ws_n > 0
     args = (q, k, v, g, dq, dk, dv, sh)
     # exactly one of each state pair given

@@ -72,6 +72,10 @@ CASES = [
     (1, 2, 515, 128, 128, torch.bfloat16, 1.0 / math.sqrt(128)),
     (1, 2, 300, 64, 128, torch.bfloat16, 0.125),
     (1, 3, 200, 128, 16, torch.bfloat16, 1.0),
+    # tensor-core path (bf16, D = M = 64): ragged, shorter than a chunk, one chunk
+    (1, 2, 77, 64, 64, torch.bfloat16, 0.125),
+    (2, 1, 128, 64, 64, torch.bfloat16, 1.0),
+    (1, 3, 645, 64, 64, torch.bfloat16, 0.5),
 ]
 
 
@@ -95,10 +99,10 @@ def test_noncausal_backward_vs_oracle(B, H, N, D, M, dtype, scale):
     _check_grads(got, ref, dtype, G, "noncausal")
 
 
-@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
-def test_causal_backward_with_state(dtype):
+@pytest.mark.parametrize("dtype,D", [(torch.float32, 32), (torch.bfloat16, 32), (torch.bfloat16, 64)])
+def test_causal_backward_with_state(dtype, D):
     """Carried-in state, gradient through the final state, and dS0/dz0 out."""
-    B, H, N, D, M = 2, 2, 150, 32, 64
+    B, H, N, M = 2, 2, 150, 64
     q, k, v = inputs.qkv(B, H, N, D, M, dtype, 0.25, seed=901)
     G = _dout(B, H, N, M, dtype, 902)
     S0, z0 = inputs.state(B, H, D, M, seed=903, scale=0.05)
@@ -111,15 +115,16 @@ def test_causal_backward_with_state(dtype):
     got = la.la_backward_causal(qd, kd, vd, Gd, S0=S0d, z0=z0d, dSN=dSNd, dzN=dzNd, dS0=dS0, dz0=dz0)
     torch.cuda.synchronize()
     _check_grads(got, (rq, rk, rv), dtype, G, "state")
-    assert head_rel_err(dS0.cpu(), rS) <= 1e-4
-    assert head_rel_err(dz0.cpu(), rz) <= 1e-4
+    assert head_rel_err(dS0.cpu(), rS) <= (1e-4 if D != 64 else 2e-2)
+    assert head_rel_err(dz0.cpu(), rz) <= (1e-4 if D != 64 else 2e-2)
 
 
-def test_causal_backward_split_chains():
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_causal_backward_split_chains(dtype):
     """Backward of two segments joined through dS0 -> dSN equals the whole backward."""
     B, H, N, D, M, split = 1, 2, 333, 64, 64, 130
-    q, k, v = inputs.qkv(B, H, N, D, M, torch.float32, 0.125, seed=910)
-    G = _dout(B, H, N, M, torch.float32, 911)
+    q, k, v = inputs.qkv(B, H, N, D, M, dtype, 0.125, seed=910)
+    G = _dout(B, H, N, M, dtype, 911)
     qd, kd, vd, Gd = _dev(q, k, v, G)
     whole = la.la_backward_causal(qd, kd, vd, Gd)
     S1 = torch.zeros(B, H, D, M, device=DEV)
@@ -134,7 +139,7 @@ def test_causal_backward_split_chains():
     g1 = la.la_backward_causal(*sl1, dSN=dS1, dzN=dz1)
     torch.cuda.synchronize()
     for a, b, w in zip(g1, g2, whole):
-        assert grad_err(torch.cat([a, b], dim=2), w.cpu().numpy(), G) <= 1e-4
+        assert grad_err(torch.cat([a, b], dim=2), w.float().cpu().numpy(), G) <= _tol(dtype)
 
 
 def test_causal_backward_empty_passes_state_gradient_through():

@@ -186,7 +186,8 @@ la_status la_backward_causal(const void *q, const void *k, const void *v, const 
     if (!dev) return LA_ERR_CUDA;
     BwdProblem p{q, k, v, dout, dq, dk, dv, S0, z0, dSN, dzN, dS0, dz0,
                  BH, s.N, s.D, s.M, s.dtype, workspace, ws_bytes, (cudaStream_t)stream};
-    return from_cuda(causal_backward(p));
+    if (tc_backward_supported(s)) return from_cuda(tc_causal_backward(p, *dev));
+    return from_cuda(causal_backward(p, *dev));
 }
 
 la_status la_forward_noncausal(const void *q, const void *k, const void *v, void *out, la_shape s,

@@ -63,29 +63,38 @@ struct BwdSmem {
     }
 };
 
-// Pass 1, forward over the chunks of one head (one CTA per head): recomputes
-// the forward (S, Z from the carried-in state), writes dQ and keeps g, e.
+// Pass 1, forward over the chunks of one segment of a head (one CTA per
+// segment): recomputes the forward from the state entering the segment (the
+// carried-in state plus the earlier segments' sums phi(K)^T V, phi(K) from
+// seg_s), writes dQ and keeps g, e.
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
 bwd_causal_pass1_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
                         const T *__restrict__ G, T *__restrict__ dq, float *__restrict__ g_ws,
                         float *__restrict__ e_ws, const float *__restrict__ S0, const float *__restrict__ z0,
-                        int N, int D, int M)
+                        const float *__restrict__ seg_s, int N, int D, int M, int nseg, int L)
 {
     extern __shared__ float sm[];
     BwdSmem s(sm, D, M);
     const int ldq = s.ldq, lda = s.lda;
-    const long long h = blockIdx.x;
+    const long long h = blockIdx.x / nseg;
+    const int seg = blockIdx.x % nseg;
     const int tid = threadIdx.x;
+    const int W = D * M + D;
+    const int t_begin = seg * L, t_end = min(N, t_begin + L);
     const T *qh = q + h * N * D, *kh = k + h * N * D, *vh = v + h * N * M, *Gh = G + h * N * M;
     T *dqh = dq + h * N * D;
     float *gh = g_ws + h * N * M, *eh = e_ws + h * N;
 
-    for (int i = tid; i < D * M; i += kThreads) s.S[i] = S0 ? S0[h * D * M + i] : 0.f;
-    for (int i = tid; i < D; i += kThreads) s.z[i] = z0 ? z0[h * D + i] : 0.f;
+    const float *segh = seg_s + h * nseg * (long long)W;
+    for (int i = tid; i < W; i += kThreads) {
+        float a = i < D * M ? (S0 ? S0[h * D * M + i] : 0.f) : (z0 ? z0[h * D + (i - D * M)] : 0.f);
+        for (int g = 0; g < seg; ++g) a += segh[g * (long long)W + i];
+        s.S[i] = a;   // S then z (contiguous)
+    }
 
-    for (int t0 = 0; t0 < N; t0 += kCs) {
-        const int rows = min(kCs, N - t0);
+    for (int t0 = t_begin; t0 < t_end; t0 += kCs) {
+        const int rows = min(kCs, t_end - t0);
         __syncthreads();
         for (int idx = tid; idx < kCs * D; idx += kThreads) {
             const int i = idx / D, d = idx - i * D;
@@ -175,31 +184,40 @@ bwd_causal_pass1_kernel(const T *__restrict__ q, const T *__restrict__ k, const 
     }
 }
 
-// Pass 2, backward over the chunks of one head: R, r start from the gradient
-// reaching the final state (or 0) and take in each chunk after its dK, dV.
+// Pass 2, backward over the chunks of one segment of a head: R, r start from
+// the gradient reaching the final state (or 0) plus the later segments' sums
+// phi(Q)^T g, e phi(Q) (seg_r), and take in each chunk after its dK, dV.
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
 bwd_causal_pass2_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
                         const float *__restrict__ g_ws, const float *__restrict__ e_ws, T *__restrict__ dk,
                         T *__restrict__ dv, const float *__restrict__ dSN, const float *__restrict__ dzN,
-                        float *__restrict__ dS0, float *__restrict__ dz0, int N, int D, int M)
+                        float *__restrict__ dS0, float *__restrict__ dz0, const float *__restrict__ seg_r,
+                        int N, int D, int M, int nseg, int L)
 {
     extern __shared__ float sm[];
     BwdSmem s(sm, D, M);
     float *R = s.S, *r = s.z;
     const int ldq = s.ldq, lda = s.lda;
-    const long long h = blockIdx.x;
+    const long long h = blockIdx.x / nseg;
+    const int seg = blockIdx.x % nseg;
     const int tid = threadIdx.x;
+    const int W = D * M + D;
+    const int t_begin = seg * L, t_end = min(N, t_begin + L);
     const T *qh = q + h * N * D, *kh = k + h * N * D, *vh = v + h * N * M;
     T *dkh = dk + h * N * D, *dvh = dv + h * N * M;
     const float *gh = g_ws + h * N * M, *eh = e_ws + h * N;
 
-    for (int i = tid; i < D * M; i += kThreads) R[i] = dSN ? dSN[h * D * M + i] : 0.f;
-    for (int i = tid; i < D; i += kThreads) r[i] = dzN ? dzN[h * D + i] : 0.f;
+    const float *segh = seg_r + h * nseg * (long long)W;
+    for (int i = tid; i < W; i += kThreads) {
+        float a = i < D * M ? (dSN ? dSN[h * D * M + i] : 0.f) : (dzN ? dzN[h * D + (i - D * M)] : 0.f);
+        for (int g = seg + 1; g < nseg; ++g) a += segh[g * (long long)W + i];
+        R[i] = a;     // R then r (contiguous)
+    }
 
-    const int nch = (N + kCs - 1) / kCs;
+    const int nch = (t_end - t_begin + kCs - 1) / kCs;
     for (int c = nch - 1; c >= 0; --c) {
-        const int t0 = c * kCs, rows = min(kCs, N - t0);
+        const int t0 = t_begin + c * kCs, rows = min(kCs, t_end - t0);
         __syncthreads();
         for (int idx = tid; idx < kCs * D; idx += kThreads) {
             const int i = idx / D, d = idx - i * D;
@@ -262,10 +280,59 @@ bwd_causal_pass2_kernel(const T *__restrict__ q, const T *__restrict__ k, const 
         }
     }
     __syncthreads();
-    if (dS0)
+    if (dS0 && seg == 0)
         for (int i = tid; i < D * M; i += kThreads) dS0[h * D * M + i] = R[i];
-    if (dz0)
+    if (dz0 && seg == 0)
         for (int i = tid; i < D; i += kThreads) dz0[h * D + i] = r[i];
+}
+
+// Per (head, segment): sum_i phi(Q_i) g_i^T and sum_i e_i phi(Q_i) over the
+// segment's rows, the part of R, r that pass 2 carries into earlier segments.
+template <typename T>
+__global__ void __launch_bounds__(kThreads)
+bwd_qg_sums_kernel(const T *__restrict__ q, const float *__restrict__ g_ws, const float *__restrict__ e_ws,
+                   float *__restrict__ seg_r, int N, int D, int M, int nseg, int L)
+{
+    extern __shared__ float sm[];
+    const int ldq = D + 1, W = D * M + D;
+    float *acc = sm;                  // [W]
+    float *fq = acc + W;              // [kCs][ldq]
+    float *gg = fq + kCs * ldq;       // [kCs][M]
+    float *ee = gg + kCs * M;         // [kCs]
+    const long long h = blockIdx.x / nseg;
+    const int seg = blockIdx.x % nseg, tid = threadIdx.x;
+    const int t_begin = seg * L, t_end = min(N, t_begin + L);
+    const T *qh = q + h * N * D;
+    const float *gh = g_ws + h * N * M, *eh = e_ws + h * N;
+    for (int i = tid; i < W; i += kThreads) acc[i] = 0.f;
+    for (int t0 = t_begin; t0 < t_end; t0 += kCs) {
+        const int rows = min(kCs, t_end - t0);
+        __syncthreads();
+        for (int idx = tid; idx < kCs * D; idx += kThreads) {
+            const int i = idx / D, d = idx - i * D;
+            fq[i * ldq + d] = i < rows ? phi_accurate(to_f32(qh[(long long)(t0 + i) * D + d])) : 0.f;
+        }
+        for (int idx = tid; idx < kCs * M; idx += kThreads) {
+            const int i = idx / M;
+            gg[idx] = i < rows ? gh[(long long)t0 * M + idx] : 0.f;
+        }
+        for (int i = tid; i < kCs; i += kThreads) ee[i] = i < rows ? eh[t0 + i] : 0.f;
+        __syncthreads();
+        for (int idx = tid; idx < D * M; idx += kThreads) {
+            const int d = idx / M, m = idx - d * M;
+            float a = 0.f;
+            for (int i = 0; i < rows; ++i) a += fq[i * ldq + d] * gg[i * M + m];
+            acc[idx] += a;
+        }
+        for (int d = tid; d < D; d += kThreads) {
+            float a = 0.f;
+            for (int i = 0; i < rows; ++i) a += ee[i] * fq[i * ldq + d];
+            acc[D * M + d] += a;
+        }
+    }
+    __syncthreads();
+    float *dst = seg_r + (h * nseg + seg) * (long long)W;
+    for (int i = tid; i < W; i += kThreads) dst[i] = acc[i];
 }
 
 // ------------------------------------------------------------- non-causal
@@ -478,7 +545,7 @@ cudaError_t set_bwd_smem(size_t bytes) {
     cudaError_t e;
     for (const void *f : {(const void *)bwd_causal_pass1_kernel<T>, (const void *)bwd_causal_pass2_kernel<T>,
                           (const void *)nc_bwd_sums_kernel<T>, (const void *)nc_bwd_q_kernel<T>,
-                          (const void *)nc_bwd_kv_kernel<T>})
+                          (const void *)nc_bwd_kv_kernel<T>, (const void *)bwd_qg_sums_kernel<T>})
         if ((e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes)) != cudaSuccess)
             return e;
     return cudaSuccess;
@@ -486,21 +553,51 @@ cudaError_t set_bwd_smem(size_t bytes) {
 
 size_t bwd_max_smem(int D, int M) { return std::max(bwd_smem_bytes(D, M), nc_bwd_smem_bytes(D, M)); }
 
+// Segments per head of the causal backward: about four CTAs per SM over the
+// grid, at least four chunks per segment, rows a multiple of the chunk.
+void bwd_seg_grid(long long BH, int N, int sm_count, int &nseg, int &L) {
+    const long long nch = (N + kCs - 1) / kCs;
+    const long long want = (4LL * std::max(sm_count, 1) + BH - 1) / std::max(1LL, BH);
+    nseg = (int)std::max(1LL, std::min(std::min(want, std::max(1LL, nch / 4)), 64LL));
+    L = (N + nseg - 1) / nseg;
+    L = (L + kCs - 1) / kCs * kCs;
+    nseg = (N + L - 1) / L;
+}
+
+// The causal backward in four launches: segment sums of phi(K)^T V (the state
+// entering each segment), pass 1 per segment, segment sums of phi(Q)^T g and
+// e phi(Q) (the reverse sums entering each segment from the right), pass 2.
 template <typename T>
-cudaError_t causal_bwd_t(const BwdProblem &p) {
-    const size_t sm = bwd_smem_bytes(p.D, p.M);
+cudaError_t causal_bwd_t(const BwdProblem &p, const DeviceInfo &dev) {
+    int nseg, L;
+    bwd_seg_grid(p.BH, p.N, dev.sm_count, nseg, L);
+    const long long W = (long long)p.D * p.M + p.D;
+    if (p.ws_bytes < (size_t)(p.BH * ((long long)p.N * (p.M + 1) + 2 * nseg * W)) * sizeof(float))
+        return cudaErrorInvalidValue;
+    const size_t sm = bwd_smem_bytes(p.D, p.M), smn = nc_bwd_smem_bytes(p.D, p.M);
     cudaError_t e = set_bwd_smem<T>(bwd_max_smem(p.D, p.M));
     if (e != cudaSuccess) return e;
     float *g_ws = (float *)p.ws;
     float *e_ws = g_ws + p.BH * (long long)p.N * p.M;
-    bwd_causal_pass1_kernel<T><<<(unsigned)p.BH, kThreads, sm, p.stream>>>(
-        (const T *)p.q, (const T *)p.k, (const T *)p.v, (const T *)p.dout, (T *)p.dq, g_ws, e_ws, p.S0, p.z0,
-        p.N, p.D, p.M);
+    float *seg_s = e_ws + p.BH * (long long)p.N;
+    float *seg_r = seg_s + p.BH * nseg * W;
+    const unsigned grid = (unsigned)(p.BH * nseg);
+    nc_bwd_sums_kernel<T><<<dim3((unsigned)p.BH, (unsigned)nseg), kThreads, smn, p.stream>>>(
+        (const T *)p.k, (const T *)p.v, seg_s, p.N, p.D, p.M, nseg, L);
     count_launches(1);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    bwd_causal_pass2_kernel<T><<<(unsigned)p.BH, kThreads, sm, p.stream>>>(
+    bwd_causal_pass1_kernel<T><<<grid, kThreads, sm, p.stream>>>(
+        (const T *)p.q, (const T *)p.k, (const T *)p.v, (const T *)p.dout, (T *)p.dq, g_ws, e_ws, p.S0, p.z0,
+        seg_s, p.N, p.D, p.M, nseg, L);
+    count_launches(1);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    bwd_qg_sums_kernel<T><<<grid, kThreads, smn, p.stream>>>((const T *)p.q, g_ws, e_ws, seg_r, p.N, p.D, p.M,
+                                                             nseg, L);
+    count_launches(1);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    bwd_causal_pass2_kernel<T><<<grid, kThreads, sm, p.stream>>>(
         (const T *)p.q, (const T *)p.k, (const T *)p.v, g_ws, e_ws, (T *)p.dk, (T *)p.dv, p.dSN, p.dzN,
-        p.dS0, p.dz0, p.N, p.D, p.M);
+        p.dS0, p.dz0, seg_r, p.N, p.D, p.M, nseg, L);
     count_launches(1);
     return cudaGetLastError();
 }
@@ -533,7 +630,14 @@ cudaError_t noncausal_bwd_t(const BwdProblem &p, const DeviceInfo &dev) {
 }  // namespace
 
 size_t causal_bwd_ws_bytes(const la_shape &s) {
-    return (size_t)s.B * s.H * (size_t)s.N * ((size_t)s.M + 1) * sizeof(float);
+    // g and e of every token, and two segment sums per (head, segment) for the
+    // most segments any device picks (up to 192 SMs)
+    const long long BH = (long long)s.B * s.H;
+    if (BH <= 0 || s.N <= 0) return 0;
+    int nseg, L;
+    bwd_seg_grid(BH, s.N, 192, nseg, L);
+    return (size_t)BH * ((size_t)s.N * ((size_t)s.M + 1) + 2 * (size_t)nseg * ((size_t)s.D * s.M + s.D)) *
+           sizeof(float);
 }
 
 size_t noncausal_bwd_ws_bytes(const la_shape &s) {
@@ -545,8 +649,8 @@ size_t noncausal_bwd_ws_bytes(const la_shape &s) {
     return (size_t)2 * BH * nsplit * ((size_t)s.D * s.M + s.D) * sizeof(float);
 }
 
-cudaError_t causal_backward(const BwdProblem &p) {
-    return p.dtype == LA_DTYPE_F32 ? causal_bwd_t<float>(p) : causal_bwd_t<__nv_bfloat16>(p);
+cudaError_t causal_backward(const BwdProblem &p, const DeviceInfo &dev) {
+    return p.dtype == LA_DTYPE_F32 ? causal_bwd_t<float>(p, dev) : causal_bwd_t<__nv_bfloat16>(p, dev);
 }
 
 cudaError_t noncausal_backward(const BwdProblem &p, const DeviceInfo &dev) {

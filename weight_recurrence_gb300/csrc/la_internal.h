@@ -53,8 +53,11 @@ struct BwdProblem {
 // ---- backward (la_bwd.cu): CUDA cores, any D, M in {16,32,64,128}, fp32 or bf16.
 size_t causal_bwd_ws_bytes(const la_shape &s);
 size_t noncausal_bwd_ws_bytes(const la_shape &s);
-cudaError_t causal_backward(const BwdProblem &p);
+cudaError_t causal_backward(const BwdProblem &p, const DeviceInfo &dev);
 cudaError_t noncausal_backward(const BwdProblem &p, const DeviceInfo &dev);
+// tensor-core causal backward (la_tc_bwd.cu): bf16, D = M = 64
+bool tc_backward_supported(const la_shape &s);
+cudaError_t tc_causal_backward(const BwdProblem &p, const DeviceInfo &dev);
 
 // ---- SIMT kernels (la_simt.cu): any D, M in {16,32,64,128}, fp32 or bf16.
 size_t simt_noncausal_ws_bytes(const la_shape &s);

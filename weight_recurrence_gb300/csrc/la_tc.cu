@@ -50,6 +50,7 @@
 #include "la_internal.h"
 #include "tc_host.h"
 #include "tc_ptx.cuh"
+#include "tc_kernels.cuh"
 
 // Optional timeline of CTA 0 for performance work: compiled only with
 // -DLA_TRACE (never in the library build); read with la_trace_read().
@@ -70,174 +71,6 @@ namespace la {
 namespace {
 
 using namespace tc;
-
-constexpr int kC = 128;                          // chunk rows (MMA M)
-constexpr int kGrp = 128;                        // threads of one warpgroup
-constexpr int kThreads = 64 + 2 * kGrp;          // producer, MMA, epilogue group, phi group
-constexpr uint64_t kWaitNs = 2000000000ull;      // 2 s per wait
-constexpr uint32_t kSmemMax = 232448;            // 227 KB opt-in per CTA
-constexpr int kOnesBytes = 1024;                 // one 8-row swizzle atom of a ones operand
-
-// ---------------------------------------------------------------- helpers
-
-__device__ __forceinline__ uint64_t now_ns() { return globaltimer_ns(); }
-
-// Bounded wait that also gives up as soon as another role has aborted.
-__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort) {
-    if (*abort) return false;
-    if (mbar_try_wait(bar, parity)) return true;
-    return mbar_wait_bounded(bar, parity, now_ns() + kWaitNs, abort);
-}
-
-// Warp-uniform variant: the whole warp proceeds only if every lane's wait succeeded.
-__device__ __forceinline__ bool wait_bar_warp(uint64_t *bar, uint32_t parity, volatile int *abort) {
-    return __all_sync(0xffffffffu, wait_bar(bar, parity, abort));
-}
-
-__device__ __forceinline__ void set_abort(volatile int *abort, int *err) {
-    *abort = 1;
-    record_error(err, kErrTimeout);
-}
-
-// Named barrier for the 128 threads of the epilogue group.
-__device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
-
-// phi(x) = elu(x) + 1 on two bf16 values, written as max(x, 0) + min(e^x, 1):
-// for x > 0 that is x + 1 and for x <= 0 it is e^x.  e^x = 2^(x log2 e) is taken
-// in fp32 on the MUFU unit and rounded once to bf16; the max, min and add run
-// on packed bf16 pairs.  Each result is rounded exactly once (x + 1, or e^x),
-// so it equals the fp32 evaluation rounded to bf16.  NaN propagates.
-__device__ __forceinline__ uint32_t phi_bf16x2(uint32_t w) {
-    float el, eh;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(el) : "f"(bf16lo(w) * 1.4426950408889634f));
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(eh) : "f"(bf16hi(w) * 1.4426950408889634f));
-    const uint32_t e = pack_bf16x2(el, eh);
-    uint32_t m, n, r;
-    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(m) : "r"(w), "r"(0u));
-    asm("min.NaN.bf16x2 %0, %1, %2;" : "=r"(n) : "r"(e), "r"(0x3F803F80u));
-    asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(m), "r"(n));
-    return r;
-}
-
-// Applies phi in place to a C x DD tile (sub-tiles of 64 columns, each C rows
-// x 128 bytes); rows >= zero_from are written as zeros.  Each thread handles
-// four 16-byte chunks at a time (loads, then 16 independent phi pairs, then
-// stores) so that enough exponentials are in flight.
-template <int DD>
-__device__ __forceinline__ void phi_tile(uint8_t *tile, int t, int zero_from) {
-    constexpr int CHUNKS = kC * DD * 2 / 16;
-    static_assert(CHUNKS % (4 * kGrp) == 0, "whole rounds of four chunks per thread");
-#pragma unroll 1
-    for (int u0 = t; u0 < CHUNKS; u0 += 4 * kGrp) {
-        uint4 v[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) v[i] = *reinterpret_cast<const uint4 *>(tile + (u0 + i * kGrp) * 16);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            v[i].x = phi_bf16x2(v[i].x);
-            v[i].y = phi_bf16x2(v[i].y);
-            v[i].z = phi_bf16x2(v[i].z);
-            v[i].w = phi_bf16x2(v[i].w);
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t off = (uint32_t)(u0 + i * kGrp) * 16u;
-            const int row = (int)((off % (kC * 128u)) >> 7);
-            *reinterpret_cast<uint4 *>(tile + off) = row >= zero_from ? make_uint4(0u, 0u, 0u, 0u) : v[i];
-        }
-    }
-}
-
-// Writes columns [c0, c0+32) of row r of a D x M fp32 state as bf16 into the
-// MN-major swizzled snapshot [D rows x M cols] (sub-tiles of 64 columns).
-template <int D>
-__device__ __forceinline__ void store_snap32(uint8_t *snap, int r, int c0, const float *v) {
-#pragma unroll
-    for (int c8 = 0; c8 < 4; ++c8) {
-        const int c = c0 + c8 * 8;
-        uint8_t *dst = snap + (c / 64) * D * 128 + sw128_offset(r, c % 64);
-        const float *x = v + c8 * 8;
-        uint4 w;
-        w.x = pack_bf16x2(x[0], x[1]);
-        w.y = pack_bf16x2(x[2], x[3]);
-        w.z = pack_bf16x2(x[4], x[5]);
-        w.w = pack_bf16x2(x[6], x[7]);
-        *reinterpret_cast<uint4 *>(dst) = w;
-    }
-}
-
-// phi(Q)_r . z with phi(Q) read back (bf16) from the swizzled tile.
-template <int D>
-__device__ __forceinline__ float q_dot_z(const uint8_t *qt, int r, const float *zs) {
-    float acc = 0.f;
-#pragma unroll
-    for (int c8 = 0; c8 < D / 8; ++c8) {
-        const int c = c8 * 8;
-        const uint4 w = *reinterpret_cast<const uint4 *>(qt + (c / 64) * kC * 128 + sw128_offset(r, c % 64));
-        const float4 z0 = *reinterpret_cast<const float4 *>(zs + c);
-        const float4 z1 = *reinterpret_cast<const float4 *>(zs + c + 4);
-        acc = fmaf(bf16lo(w.x), z0.x, acc);
-        acc = fmaf(bf16hi(w.x), z0.y, acc);
-        acc = fmaf(bf16lo(w.y), z0.z, acc);
-        acc = fmaf(bf16hi(w.y), z0.w, acc);
-        acc = fmaf(bf16lo(w.z), z1.x, acc);
-        acc = fmaf(bf16hi(w.z), z1.y, acc);
-        acc = fmaf(bf16lo(w.w), z1.z, acc);
-        acc = fmaf(bf16hi(w.w), z1.w, acc);
-    }
-    return acc;
-}
-
-// Loads 32 consecutive fp32 TMEM columns of this thread's lane.
-__device__ __forceinline__ void tmem_ld32f(uint32_t taddr, float (&v)[32]) {
-    uint32_t a[16], b[16];
-    tmem_ld16(taddr, a);
-    tmem_ld16(taddr + 16, b);
-    tmem_wait_ld();
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-        v[j] = __uint_as_float(a[j]);
-        v[16 + j] = __uint_as_float(b[j]);
-    }
-}
-
-__device__ __forceinline__ void tmem_st32f(uint32_t taddr, const float (&v)[32]) {
-    uint32_t a[16], b[16];
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-        a[j] = __float_as_uint(v[j]);
-        b[j] = __float_as_uint(v[16 + j]);
-    }
-    tmem_st16(taddr, a);
-    tmem_st16(taddr + 16, b);
-}
-
-// A (TMEM) x B (shared memory) MMA, kind::f16.
-__device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                           uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// Descriptors of the operand tiles (all 128-byte swizzled, 1024-byte aligned).
-// A descriptor's start-address field counts 16-byte units in its low bits, so
-// a K-step is a constant added to a base descriptor built once per chunk: the
-// single thread issuing MMAs must not spend its time on descriptor arithmetic.
-// K-major tile with rows of up to 128 elements stored as 64-element sub-tiles
-// of kC rows: K-step ks (16 elements) starts 32 bytes further, or in the next
-// sub-tile after 4 steps.
-__device__ __forceinline__ uint64_t kmajor_base(uint32_t tile) { return smem_desc(tile, 16, 1024); }
-__host__ __device__ constexpr uint64_t kmajor_step(int ks, int rows = kC) {
-    return (uint64_t)((ks / 4) * rows * 128 / 16 + (ks % 4) * 2);
-}
-// MN-major: K-step ks covers rows 16ks..16ks+15, 2048 bytes further.
-__host__ __device__ constexpr uint64_t mnmajor_step(int ks) { return (uint64_t)(ks * 128); }
-// B operand of 16 K-rows made of one 8-row atom read twice (K-group stride 0):
-// valid because every row of the ones operand is the same.
-__device__ __forceinline__ uint64_t ones_desc(uint32_t tile) { return smem_desc(tile, 1024, 0); }
 
 // ------------------------------------------------------------ causal kernel
 
@@ -1455,24 +1288,6 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
 }
 
 // ---------------------------------------------------------------- launchers
-
-// Opts a kernel in to `bytes` of dynamic shared memory, once per (kernel,
-// device): the memo is keyed by the kernel's address, since all instances
-// of a kernel template share one function type.
-template <typename K>
-cudaError_t set_smem(K kernel, int bytes) {
-    static std::mutex mu;
-    static std::vector<std::pair<const void *, int>> done;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
-    const void *key = reinterpret_cast<const void *>(kernel);
-    std::lock_guard<std::mutex> lock(mu);
-    for (const auto &d : done)
-        if (d.first == key && d.second == dev) return cudaSuccess;
-    const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    if (e == cudaSuccess) done.emplace_back(key, dev);
-    return e;
-}
 
 // Segments per head for the causal kernel: enough CTAs to cover the SMs
 // (one CTA per SM), at least 8 chunks per segment.
