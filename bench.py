@@ -477,6 +477,23 @@ def _leg_decode(torch, la, inputs, dev, stream, flush, pk, args, max_over_ranks,
             del g
         except Exception as e:  # report, do not hide
             leg["graph_4096"] = {"error": repr(e)}
+    # all 4096 steps in one launch (la_decode_steps): the state stays on chip
+    # across the steps, so they cost their q, k, v, y traffic only
+    Sf, zf = S.clone(), z.clone()
+    yf = torch.empty((steps, B, H, M), dtype=w.dtype, device=dev)
+    fused = lambda: la.la_decode_steps(qs, ks, vs, Sf, zf, y=yf, stream=stream)  # noqa: E731
+    ft = _timed_steps(torch, fused, 3, 1, lambda: None, stream)
+    fms = max_over_ranks(sum(ft) / len(ft))
+    fbytes = 2 * B * H * (D * M + D) * 4 + steps * B * H * (2 * D + 2 * M) * 2
+    leg["fused_4096"] = {"steps_per_s": round(world * steps / (fms / 1e3), 1), "ms_total": round(fms, 3),
+                         "launches": 1, "hbm_gbs": round(fbytes / (fms / 1e3) / 1e9, 1),
+                         "roofline": {"bound": "hbm", "achieved": round(fbytes / (fms / 1e3) / 1e9, 1),
+                                      "peak": pk["hbm_gbs"], "unit": "GB/s",
+                                      "frac": round(fbytes / (fms / 1e3) / 1e9 / pk["hbm_gbs"], 4),
+                                      "alg_bytes_per_launch": fbytes},
+                         "note": "la_decode_steps: for steps whose inputs are known together; "
+                                 "state read and written once, tokens streamed"}
+    del Sf, zf, yf
     del qs, ks, vs, S, z, y
     torch.cuda.empty_cache()
     return leg

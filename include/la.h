@@ -126,6 +126,35 @@ la_status la_decode_step(const void *q, const void *k, const void *v, void *y,
                          float *S, float *z, la_shape s, la_stream_t stream);
 
 /*
+ * Causal attention over a batch of sequences of different lengths (a prefill
+ * of several prompts at once): as la_forward_causal, but batch entry b has
+ * lens[b] tokens (clamped to [0, N]); rows at or past its length are read but
+ * add nothing, and their rows of `out` are unspecified.  With S, z the call
+ * starts each head from its state and leaves the state after its own length
+ * (a zero length leaves it unchanged).
+ *   lens: device pointer to B int32 lengths (4-byte aligned).
+ *   q, k, v, out, S, z, workspace: as la_forward_causal (chunk = 0).
+ */
+la_status la_forward_causal_varlen(const void *q, const void *k, const void *v, void *out, const int *lens,
+                                   la_shape s, float *S, float *z, void *workspace, size_t ws_bytes,
+                                   la_stream_t stream);
+
+/*
+ * T recurrent steps, sec. 3.4 eqs. (18)-(20), in one launch: each head's state
+ * is read once, updated and read out T times on chip, and written back once.
+ * Step-major inputs: q, k [T,B,H,D]; v, y [T,B,H,M]; S, z as la_decode_step.
+ * For when several steps' inputs are known together (a verified draft, a
+ * teacher-forced continuation): the result equals T calls of la_decode_step,
+ * which is the causal form over those T tokens started from (S, z); for bf16
+ * with D, M in {64, 128} it runs the chunked tensor-core causal kernel.
+ *   steps: device pointer to B int32 step counts (clamped to [0, T]; batch
+ *      entry b runs its first steps[b] steps; its later y rows are
+ *      unspecified), or NULL for all T.  s.N is ignored.
+ */
+la_status la_decode_steps(const void *q, const void *k, const void *v, void *y, float *S, float *z,
+                          const int *steps, int T, la_shape s, la_stream_t stream);
+
+/*
  * Backward of the causal form (the gradient sec. 3.3.1 computes as cumulative
  * sums in constant extra memory; its eqs. (13)-(15) are not printed on the
  * page, so this is the chain rule through eqs. (10)-(12)).  Given

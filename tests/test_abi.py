@@ -144,3 +144,22 @@ def test_backward_argument_checks(lib):
         == la.LA_OK
     assert lib.la_backward_causal(None, None, None, None, None, None, None, _shape(B=0), None, None, None, None,
                                   None, None, None, 0, None) == la.LA_OK
+
+
+def test_generation_argument_checks(lib):
+    sh = _shape(B=2, N=64, D=16, M=16)
+    q, k, v, o = (_addr(i) for i in range(4))
+    # per-sequence lengths are required and 4-byte aligned
+    assert lib.la_forward_causal_varlen(q, k, v, o, None, sh, None, None, None, 0, None) == la.LA_ERR_INVALID_ARG
+    assert lib.la_forward_causal_varlen(q, k, v, o, ctypes.c_void_p(0x10002), sh, None, None, None, 0, None) \
+        == la.LA_ERR_INVALID_ARG
+    assert lib.la_forward_causal_varlen(q, k, v, o, _addr(5), sh, FAKE, None, None, 0, None) == la.LA_ERR_INVALID_ARG
+    assert lib.la_forward_causal_varlen(None, None, None, None, None, _shape(N=0), None, None, None, 0, None) \
+        == la.LA_OK
+    # negative step count, misaligned step counts, missing state
+    assert lib.la_decode_steps(q, k, v, o, _addr(5), _addr(6), None, -1, sh, None) == la.LA_ERR_INVALID_ARG
+    assert lib.la_decode_steps(q, k, v, o, _addr(5), _addr(6), ctypes.c_void_p(0x10002), 4, sh, None) \
+        == la.LA_ERR_INVALID_ARG
+    assert lib.la_decode_steps(q, k, v, o, None, _addr(6), None, 4, sh, None) == la.LA_ERR_INVALID_ARG
+    assert lib.la_decode_steps(None, None, None, None, None, None, None, 0, sh, None) == la.LA_OK
+    assert lib.la_decode_steps(q, k, v, o, _addr(5), _addr(6), None, 4, _shape(D=24), None) == la.LA_ERR_UNSUPPORTED

@@ -237,6 +237,62 @@ la_status la_forward_causal(const void *q, const void *k, const void *v, void *o
     return from_cuda(simt_causal(p, *dev));
 }
 
+la_status la_forward_causal_varlen(const void *q, const void *k, const void *v, void *out, const int *lens,
+                                   la_shape s, float *S, float *z, void *workspace, size_t ws_bytes,
+                                   la_stream_t stream) {
+    la_status st = check_shape(s, true);
+    if (st != LA_OK) return st;
+    if ((S == nullptr) != (z == nullptr)) return LA_ERR_INVALID_ARG;
+    const long long BH = (long long)s.B * s.H;
+    const bool work = BH > 0 && s.N > 0;
+    if ((st = check_ptr(S, S != nullptr && BH > 0)) || (st = check_ptr(z, z != nullptr && BH > 0)))
+        return st;
+    if ((st = check_ptr(q, work)) || (st = check_ptr(k, work)) || (st = check_ptr(v, work)) ||
+        (st = check_ptr(out, work && out != nullptr)))
+        return st;
+    if (!work) return LA_OK;
+    if (lens == nullptr || (reinterpret_cast<uintptr_t>(lens) & 3u) != 0) return LA_ERR_INVALID_ARG;
+    if (out != nullptr && (out == q || out == k || out == v)) return LA_ERR_INVALID_ARG;
+    const size_t need = la_workspace_bytes(LA_OP_CAUSAL, s, 0);
+    if (ws_bytes < need || (need > 0 && check_ptr(workspace, true) != LA_OK)) return LA_ERR_INVALID_ARG;
+    const DeviceInfo *dev = device_info();
+    if (!dev) return LA_ERR_CUDA;
+    Problem p{q, k, v, out, S, z, BH, s.N, s.D, s.M, s.dtype, 0, workspace, ws_bytes, (cudaStream_t)stream};
+    p.lens = lens;
+    p.H = s.H;
+    if (tc_causal_supported(s, 0)) return from_cuda(tc_causal(p, *dev));
+    return from_cuda(simt_causal(p, *dev));
+}
+
+la_status la_decode_steps(const void *q, const void *k, const void *v, void *y, float *S, float *z,
+                          const int *steps, int T, la_shape s, la_stream_t stream) {
+    la_status st = check_shape(s, false);
+    if (st != LA_OK) return st;
+    if (T < 0) return LA_ERR_INVALID_ARG;
+    const long long BH = (long long)s.B * s.H;
+    const bool work = BH > 0 && T > 0;
+    if ((st = check_ptr(q, work)) || (st = check_ptr(k, work)) || (st = check_ptr(v, work)) ||
+        (st = check_ptr(y, work)) || (st = check_ptr(S, work)) || (st = check_ptr(z, work)))
+        return st;
+    if (!work) return LA_OK;
+    if (steps != nullptr && (reinterpret_cast<uintptr_t>(steps) & 3u) != 0) return LA_ERR_INVALID_ARG;
+    if (BH > 0x7fffffffLL) return LA_ERR_UNSUPPORTED;
+    const DeviceInfo *dev = device_info();
+    if (!dev) return LA_ERR_CUDA;
+    Problem p{q, k, v, y, S, z, BH, T, s.D, s.M, s.dtype, 0, nullptr, 0, (cudaStream_t)stream};
+    p.H = s.H;
+    p.lens = steps;
+    // several steps with known inputs are the causal form over those tokens,
+    // starting from the state: the tensor-core kernel reads the step-major
+    // tensors through strided tensor maps
+    if (tc_causal_supported(s, 0)) {
+        p.step_major = true;
+        return from_cuda(tc_causal(p, *dev));
+    }
+    p.lens = nullptr;
+    return from_cuda(decode_steps(p, steps, T));
+}
+
 la_status la_decode_step(const void *q, const void *k, const void *v, void *y, float *S, float *z,
                          la_shape s, la_stream_t stream) {
     la_status st = check_shape(s, false);

@@ -33,6 +33,9 @@ struct Problem {
     void *ws;
     size_t ws_bytes;
     cudaStream_t stream;
+    const int *lens = nullptr;   // causal: per-batch sequence lengths (device, [B]) or null
+    int H = 1;                   // heads per batch entry (to index lens)
+    bool step_major = false;     // causal: q, k, v, out laid out [N][B*H][.] (decode steps)
 };
 
 // Backward-pass problem (sizes already validated).
@@ -64,6 +67,9 @@ size_t simt_noncausal_ws_bytes(const la_shape &s);
 cudaError_t simt_noncausal(const Problem &p, const DeviceInfo &dev);
 cudaError_t simt_causal(const Problem &p, const DeviceInfo &dev);
 cudaError_t decode_step(const Problem &p, const DeviceInfo &dev);
+// T recurrent steps in one launch, the state held on chip (inputs [T, B*H, .]);
+// steps: per-batch step counts (device, [B]) or null (all T)
+cudaError_t decode_steps(const Problem &p, const int *steps, int T);
 // Same two kernels as simt_noncausal with at most max_splits partial sums in p.ws.
 cudaError_t simt_noncausal_capped(const Problem &p, const DeviceInfo &dev, int max_splits);
 

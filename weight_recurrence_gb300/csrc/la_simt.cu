@@ -34,7 +34,7 @@ template <typename T>
 __global__ void __launch_bounds__(kThreads)
 causal_simt_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
                    T *__restrict__ out, float *__restrict__ S_io, float *__restrict__ z_io,
-                   int N, int D, int M)
+                   int N, int D, int M, const int *__restrict__ lens, int H)
 {
     extern __shared__ float sm[];
     const int ldq = D + 1, lda = kCs + 1;
@@ -54,8 +54,10 @@ causal_simt_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__
     for (int i = tid; i < D; i += kThreads) z[i] = z_io ? z_io[h * D + i] : 0.f;
     __syncthreads();
 
-    for (int t0 = 0; t0 < N; t0 += kCs) {
-        const int rows = min(kCs, N - t0);
+    // this head's sequence length (rows past it are ignored)
+    const int Nh = lens ? max(0, min(N, lens[h / H])) : N;
+    for (int t0 = 0; t0 < Nh; t0 += kCs) {
+        const int rows = min(kCs, Nh - t0);
         for (int idx = tid; idx < kCs * D; idx += kThreads) {
             const int i = idx / D, d = idx - i * D;
             float a = 0.f, b = 0.f;
@@ -351,9 +353,148 @@ cudaError_t simt_causal_t(const Problem &p) {
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     causal_simt_kernel<T><<<(unsigned)p.BH, kThreads, smem, p.stream>>>(
-        (const T *)p.q, (const T *)p.k, (const T *)p.v, (T *)p.out, p.S, p.z, p.N, p.D, p.M);
+        (const T *)p.q, (const T *)p.k, (const T *)p.v, (T *)p.out, p.S, p.z, p.N, p.D, p.M, p.lens,
+        p.H > 0 ? p.H : 1);
     count_launches(1);
     return cudaGetLastError();
+}
+
+// T recurrent steps of sec. 3.4 eqs. (18)-(20) in one launch, one CTA per
+// head: the head's state is read into registers once (same thread layout as
+// decode_kernel), updated and read out T times, and written back once, so the
+// steps cost only their q, k, v, y traffic.  Inputs are step-major:
+// q, k [T][BH][D], v, y [T][BH][M].  Batch entry b runs steps[b] steps (all
+// T if steps is null); its later outputs are left untouched.
+template <typename T, int D, int M>
+__global__ void __launch_bounds__(kThreads)
+decode_steps_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restrict__ v,
+                    T *__restrict__ y, float *__restrict__ S, float *__restrict__ z,
+                    const int *__restrict__ steps, int Tn, long long BH, int H)
+{
+    constexpr int C4 = M / 4;
+    constexpr int RP = kThreads / C4;
+    constexpr int NR = (D + RP - 1) / RP;
+    __shared__ float fq[D], fk[D], vs[M], dz[D];
+    __shared__ float4 red[RP][C4];
+    __shared__ float den_s;
+    const long long h = blockIdx.x;
+    const int tid = threadIdx.x;
+    const int c4 = tid % C4, r = tid / C4;
+    const int nsteps = steps ? max(0, min(Tn, steps[h / H])) : Tn;
+
+    float4 s[NR];
+    float4 *Sh = reinterpret_cast<float4 *>(S + h * D * M);
+#pragma unroll
+    for (int i = 0; i < NR; ++i) {
+        const int d = r + i * RP;
+        if (d < D) s[i] = Sh[d * C4 + c4];
+    }
+    float zr = tid < D ? z[h * D + tid] : 0.f;
+    // the inputs of the next kPre steps are in flight while a step runs: each
+    // thread prefetches its own element of q, k (tid < D) and v (tid < M)
+    constexpr int kPre = 8;
+    float pq[kPre], pk[kPre], pv[kPre];
+    auto fetch = [&](int t, float &a, float &b, float &c) {
+        if (t < nsteps) {
+            const long long row = (long long)t * BH + h;
+            a = tid < D ? to_f32(q[row * D + tid]) : 0.f;
+            b = tid < D ? to_f32(k[row * D + tid]) : 0.f;
+            c = tid < M ? to_f32(v[row * M + tid]) : 0.f;
+        }
+    };
+#pragma unroll
+    for (int u = 0; u < kPre; ++u) fetch(u, pq[u], pk[u], pv[u]);
+    for (int t0 = 0; t0 < nsteps; t0 += kPre) {
+#pragma unroll
+        for (int u = 0; u < kPre; ++u) {
+            const int t = t0 + u;
+            if (t >= nsteps) break;   // CTA-uniform
+            const long long row = (long long)t * BH + h;
+            if (tid < D) {
+                fq[tid] = phi_accurate(pq[u]);
+                fk[tid] = phi_accurate(pk[u]);
+            }
+            if (tid < M) vs[tid] = pv[u];
+            fetch(t + kPre, pq[u], pk[u], pv[u]);
+            __syncthreads();
+            const float4 v4 = make_float4(vs[4 * c4], vs[4 * c4 + 1], vs[4 * c4 + 2], vs[4 * c4 + 3]);
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int i = 0; i < NR; ++i) {
+                const int d = r + i * RP;
+                if (d < D) {
+                    const float a = fk[d], b = fq[d];
+                    float4 w4 = s[i];
+                    w4.x = fmaf(a, v4.x, w4.x);      // eq. (18)
+                    w4.y = fmaf(a, v4.y, w4.y);
+                    w4.z = fmaf(a, v4.z, w4.z);
+                    w4.w = fmaf(a, v4.w, w4.w);
+                    s[i] = w4;
+                    acc.x = fmaf(b, w4.x, acc.x);    // eq. (20) numerator, updated state
+                    acc.y = fmaf(b, w4.y, acc.y);
+                    acc.z = fmaf(b, w4.z, acc.z);
+                    acc.w = fmaf(b, w4.w, acc.w);
+                }
+            }
+            if (r < RP) red[r][c4] = acc;
+            if (tid < D) {
+                zr += fk[tid];                       // eq. (19)
+                dz[tid] = fq[tid] * zr;
+            }
+            __syncthreads();
+            if (tid < 32) {
+                float a = 0.f;
+                for (int d = tid; d < D; d += 32) a += dz[d];
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+                if (tid == 0) den_s = a;
+            }
+            __syncthreads();
+            if (tid < M) {
+                const float *redf = reinterpret_cast<const float *>(red);
+                float num = 0.f;
+#pragma unroll 4
+                for (int rr = 0; rr < RP && rr < D; ++rr) num += redf[rr * M + tid];
+                y[row * M + tid] = from_f32<T>(num / den_s);
+            }
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < NR; ++i) {
+        const int d = r + i * RP;
+        if (d < D) Sh[d * C4 + c4] = s[i];
+    }
+    if (tid < D) z[h * D + tid] = zr;
+}
+
+template <typename T, int D, int M>
+cudaError_t launch_decode_steps(const Problem &p, const int *steps, int Tn) {
+    decode_steps_kernel<T, D, M><<<(unsigned)p.BH, kThreads, 0, p.stream>>>(
+        (const T *)p.q, (const T *)p.k, (const T *)p.v, (T *)p.out, p.S, p.z, steps, Tn, p.BH, p.H > 0 ? p.H : 1);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+template <typename T, int D>
+cudaError_t decode_steps_m(const Problem &p, const int *steps, int Tn) {
+    switch (p.M) {
+        case 16: return launch_decode_steps<T, D, 16>(p, steps, Tn);
+        case 32: return launch_decode_steps<T, D, 32>(p, steps, Tn);
+        case 64: return launch_decode_steps<T, D, 64>(p, steps, Tn);
+        case 128: return launch_decode_steps<T, D, 128>(p, steps, Tn);
+    }
+    return cudaErrorInvalidValue;
+}
+
+template <typename T>
+cudaError_t decode_steps_dm(const Problem &p, const int *steps, int Tn) {
+    switch (p.D) {
+        case 16: return decode_steps_m<T, 16>(p, steps, Tn);
+        case 32: return decode_steps_m<T, 32>(p, steps, Tn);
+        case 64: return decode_steps_m<T, 64>(p, steps, Tn);
+        case 128: return decode_steps_m<T, 128>(p, steps, Tn);
+    }
+    return cudaErrorInvalidValue;
 }
 
 template <typename T>
@@ -406,6 +547,10 @@ cudaError_t simt_causal(const Problem &p, const DeviceInfo &) {
 
 cudaError_t decode_step(const Problem &p, const DeviceInfo &) {
     return p.dtype == LA_DTYPE_F32 ? decode_dm<float>(p) : decode_dm<__nv_bfloat16>(p);
+}
+
+cudaError_t decode_steps(const Problem &p, const int *steps, int Tn) {
+    return p.dtype == LA_DTYPE_F32 ? decode_steps_dm<float>(p, steps, Tn) : decode_steps_dm<__nv_bfloat16>(p, steps, Tn);
 }
 
 }  // namespace la

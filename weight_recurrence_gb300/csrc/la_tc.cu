@@ -162,6 +162,9 @@ struct CausalArgs {
     int cps;                 // chunks per segment
     int *err;
     uint64_t inject_ns;      // test hook: wait this long on a flag nobody sets
+    const int *lens;         // per-batch sequence lengths (device) or null: rows past them are ignored
+    int H;                   // heads per batch entry
+    long long o_rs, o_hs;    // output row and head strides (elements) for the direct stores
 };
 
 // Named barrier of the O group's 128 threads.
@@ -179,7 +182,9 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     volatile int *abort = reinterpret_cast<volatile int *>(smem + C::OFF_TSLOT + 4);
 
     const int bh = blockIdx.x / args.nseg, seg = blockIdx.x % args.nseg;
-    const int nch_total = (args.N + kC - 1) / kC;
+    // this head's sequence length (rows past it are read but ignored)
+    const int Nseq = args.lens ? max(0, min(args.N, args.lens[bh / args.H])) : args.N;
+    const int nch_total = (Nseq + kC - 1) / kC;
     const int c_begin = seg * args.cps;
     const int n = max(0, min(nch_total, c_begin + args.cps) - c_begin);
 
@@ -539,8 +544,8 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     den = __uint_as_float(dv[0]) + __uint_as_float(zv[0]);
                 }
                 const float inv = 1.f / den;
-                uint4 *dst = !C::OUT_TMA && args.out && t < args.N
-                                 ? reinterpret_cast<uint4 *>(args.out + ((size_t)bh * args.N + t) * M)
+                uint4 *dst = !C::OUT_TMA && args.out && t < Nseq
+                                 ? reinterpret_cast<uint4 *>(args.out + (size_t)bh * args.o_hs + (size_t)t * args.o_rs)
                                  : nullptr;
 #pragma unroll 1
                 for (int c0 = 0; c0 < M; c0 += 32) {
@@ -729,7 +734,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 if (t == 0) LA_TRACE_AT(3, it, 3 * grp + 1);
                 uint8_t *st = smem + s * C::STAGE;
                 if (grp == 0) phi_tile<D>(st, t, kC);
-                if (grp == C::NPHI - 1) phi_tile<D>(st + C::TILE_QK, t, min(kC, args.N - (c_begin + it) * kC));
+                if (grp == C::NPHI - 1) phi_tile<D>(st + C::TILE_QK, t, min(kC, Nseq - (c_begin + it) * kC));
                 if (t == 0) LA_TRACE_AT(3, it, 3 * grp + 2);
             }
             fence_proxy_async();
@@ -1299,15 +1304,22 @@ int causal_nseg(long long BH, int N, int sm_count) {
     return (int)nseg;
 }
 
+// Tensor map of a [BH][N][cols] tensor, or of a step-major [N][BH][cols] one
+// read in the same [BH][N][cols] order.
+bool causal_tmap(CUtensorMap *m, const Problem &p, const void *base, int cols) {
+    if (!p.step_major) return cached_tmap_bf16_3d(m, base, cols, p.N, p.BH, 64, kC);
+    return make_tmap_bf16_3d_strided(m, base, cols, p.N, p.BH, (uint64_t)p.BH * cols * 2, (uint64_t)cols * 2, 64, kC);
+}
+
 template <int D, int M>
 cudaError_t launch_causal(const Problem &p, const DeviceInfo &dev) {
     using C = Cfg<D, M>;
     CUtensorMap tq, tk, tv;
-    if (!cached_tmap_bf16_3d(&tq, p.q, D, p.N, p.BH, 64, kC) || !cached_tmap_bf16_3d(&tk, p.k, D, p.N, p.BH, 64, kC) ||
-        !cached_tmap_bf16_3d(&tv, p.v, M, p.N, p.BH, 64, kC))
+    if (!causal_tmap(&tq, p, p.q, D) || !causal_tmap(&tk, p, p.k, D) || !causal_tmap(&tv, p, p.v, M))
         return cudaErrorInvalidValue;
     const int nch = (p.N + kC - 1) / kC;
-    int nseg = causal_nseg(p.BH, p.N, dev.sm_count);
+    // per-sequence lengths or step-major decode inputs: no segments
+    int nseg = (p.lens || p.step_major) ? 1 : causal_nseg(p.BH, p.N, dev.sm_count);
     const int cps = (nch + nseg - 1) / nseg;
     nseg = (nch + cps - 1) / cps;
     cudaError_t e;
@@ -1320,7 +1332,7 @@ cudaError_t launch_causal(const Problem &p, const DeviceInfo &dev) {
         if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
     CUtensorMap to;
-    if (p.out && !cached_tmap_bf16_3d(&to, p.out, M, p.N, p.BH, 64, kC)) return cudaErrorInvalidValue;
+    if (p.out && !causal_tmap(&to, p, p.out, M)) return cudaErrorInvalidValue;
     if (!p.out) to = tq;   // never used
     CausalArgs a;
     a.out = reinterpret_cast<__nv_bfloat16 *>(p.out);
@@ -1332,6 +1344,10 @@ cudaError_t launch_causal(const Problem &p, const DeviceInfo &dev) {
     a.cps = cps;
     a.err = dev.err_word;
     a.inject_ns = g_inject_timeout ? (uint64_t)g_inject_limit_us * 1000ull : 0ull;
+    a.lens = p.lens;
+    a.H = p.H > 0 ? p.H : 1;
+    a.o_rs = p.step_major ? p.BH * (long long)M : (long long)M;
+    a.o_hs = p.step_major ? (long long)M : (long long)p.N * M;
     if ((e = set_smem(causal_tc_kernel<D, M>, C::SMEM)) != cudaSuccess) return e;
     causal_tc_kernel<D, M><<<(unsigned)(p.BH * nseg), C::THREADS, C::SMEM, p.stream>>>(tq, tk, tv, to, a);
     count_launches(1);

@@ -45,6 +45,24 @@ inline bool make_tmap_bf16_3d(CUtensorMap *map, const void *base, uint64_t cols,
     return r == CUDA_SUCCESS;
 }
 
+// Tensor map over a bf16 tensor with explicit strides (bytes, multiples of 16):
+// element (c, r, o) at base + 2c + r * row_stride + o * outer_stride.  Used for
+// step-major decode inputs [T][B*H][cols], read as [B*H][T][cols].
+inline bool make_tmap_bf16_3d_strided(CUtensorMap *map, const void *base, uint64_t cols, uint64_t rows,
+                                      uint64_t outer, uint64_t row_stride, uint64_t outer_stride,
+                                      uint32_t box_cols, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[3] = {cols, rows, outer};
+    cuuint64_t strides[2] = {row_stride, outer_stride};
+    cuuint32_t box[3] = {box_cols, box_rows, 1};
+    cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 // Same as make_tmap_bf16_3d, served from a small per-thread cache keyed by
 // (base, cols, rows, outer, box): encoding a tensor map costs host time on
 // every call, and a caller usually passes the same buffers again and again.

@@ -23,7 +23,7 @@ LA_OP_NONCAUSAL, LA_OP_CAUSAL, LA_OP_DECODE, LA_OP_NONCAUSAL_BWD, LA_OP_CAUSAL_B
 EXPORTED = ("la_workspace_bytes", "la_forward_noncausal", "la_forward_causal", "la_decode_step",
             "la_get_last_error", "la_status_string", "la_version", "la_launch_count",
             "la_debug_inject_timeout", "la_forward_noncausal_noalloc", "la_backward_causal",
-            "la_backward_noncausal")
+            "la_backward_noncausal", "la_forward_causal_varlen", "la_decode_steps")
 
 
 class LAError(RuntimeError):
@@ -69,6 +69,10 @@ def lib() -> ctypes.CDLL:
         L.la_debug_inject_timeout.argtypes = [i, i]
         L.la_backward_causal.restype = i
         L.la_backward_causal.argtypes = [vp, vp, vp, vp, vp, vp, vp, la_shape, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+        L.la_forward_causal_varlen.restype = i
+        L.la_forward_causal_varlen.argtypes = [vp, vp, vp, vp, vp, la_shape, vp, vp, vp, sz, vp]
+        L.la_decode_steps.restype = i
+        L.la_decode_steps.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, la_shape, vp]
         L.la_backward_noncausal.restype = i
         L.la_backward_noncausal.argtypes = [vp, vp, vp, vp, vp, vp, vp, la_shape, vp, sz, vp]
         _lib = L
@@ -204,6 +208,44 @@ def la_decode_step(q, k, v, S, z, y=None, stream=None):
     st = lib().la_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(y), _ptr(S), _ptr(z), s,
                               _stream(stream, q.device))
     _check(st, "la_decode_step")
+    return y
+
+
+def la_forward_causal_varlen(q, k, v, lens, out=None, S=None, z=None, want_out=True, stream=None):
+    """Causal form for a batch of sequences of lengths lens [B] (int32, on the
+    device); rows past a sequence's length are ignored (their output rows are
+    unspecified).  S, z as in la_forward_causal, per sequence."""
+    _contig(q, k, v, S, z, lens)
+    if lens.dtype != torch.int32:
+        raise ValueError("lens must be int32")
+    s = shape_of(q, v)
+    if out is None and want_out:
+        out = torch.empty(q.shape[:-1] + (v.shape[-1],), dtype=q.dtype, device=q.device)
+    _contig(out)
+    need = la_workspace_bytes(LA_OP_CAUSAL, s, 0)
+    sp = _stream_ptr(stream, q.device)
+    ws = _workspace(need, q.device, sp)
+    st = lib().la_forward_causal_varlen(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lens), s, _ptr(S), _ptr(z),
+                                        _ptr(ws), need, ctypes.c_void_p(sp))
+    _check(st, "la_forward_causal_varlen")
+    return out
+
+
+def la_decode_steps(q, k, v, S, z, y=None, steps=None, stream=None):
+    """T recurrent steps in one launch: q, k [T,B,H,D], v [T,B,H,M]; S, z fp32
+    updated in place; steps: optional int32 [B] per-sequence step counts."""
+    _contig(q, k, v, S, z, steps)
+    T, B, H, D = q.shape
+    M = v.shape[-1]
+    if y is None:
+        y = torch.empty((T, B, H, M), dtype=q.dtype, device=q.device)
+    _contig(y)
+    if steps is not None and steps.dtype != torch.int32:
+        raise ValueError("steps must be int32")
+    s = la_shape(B, H, 1, D, M, _dtype_code(q.dtype))
+    st = lib().la_decode_steps(_ptr(q), _ptr(k), _ptr(v), _ptr(y), _ptr(S), _ptr(z), _ptr(steps), int(T), s,
+                               _stream(stream, q.device))
+    _check(st, "la_decode_steps")
     return y
 
 
