@@ -13,6 +13,11 @@ its Chinese translation):
 * ``definition`` (numpy, ``definition.py``): sec. 3.1 eq. (3) with
   sim(q, k) = phi(q)^T phi(k) (sec. 3.2 eq. (4)) and the causal mask of
   sec. 3.3 eq. (8), as a dense quadratic form.
+* ``variant_*`` (C, ``la_variants.c``): the same recurrence with the other
+  feature maps (DPFP-nu of "Linear Transformers Are Secretly Fast Weight
+  Programmers", the degree-2 polynomial map of sec. 3.2.1), sum-normalised
+  features without a denominator, and the delta update rule with a per-token
+  beta; ``definition_variant`` (numpy) is their quadratic form (sum update).
 * ``causal_backward`` / ``noncausal_backward`` (C): gradients by the chain
   rule through eqs. (10)-(12) (forward sweep for dQ, reverse cumulative sums
   for dK, dV - the constant-memory scheme sec. 3.3.1 describes, whose own
@@ -21,7 +26,11 @@ its Chinese translation):
 Parity status: pinned (see tests/test_oracle.py) by the hand-derived fixtures
 under tests/golden/, closed forms, invariants and planted-mistake checks; the
 backward (tests/test_oracle_backward.py) by central finite differences and by
-autograd of the definition form, closed forms and planted-mistake checks.
+autograd of the definition form, closed forms and planted-mistake checks; the
+variants (tests/test_oracle_variants.py) by hand-derived features, the
+polynomial kernel's closed form, the definition form, an independent chunked
+(UT-transform) evaluation of the delta rule, closed forms of the delta rule
+with one-hot keys, and planted-mistake checks.
 """
 from __future__ import annotations
 
@@ -31,20 +40,22 @@ import subprocess
 
 import numpy as np
 
-from .definition import definition_causal, definition_noncausal, definition_rows, phi_np  # noqa: F401
+from .definition import (definition_causal, definition_noncausal, definition_rows,  # noqa: F401
+                         definition_variant, features_np, phi_np)
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SO = os.path.join(_HERE, "liblaoracle.so")
-_SRC = os.path.join(_HERE, "la_oracle.c")
+_SRCS = [os.path.join(_HERE, "la_oracle.c"), os.path.join(_HERE, "la_variants.c")]
 _lib = None
 
 
 def build(force: bool = False) -> str:
-    """Compile la_oracle.c with gcc (-O2 -fopenmp); returns the .so path."""
-    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < os.path.getmtime(_SRC):
+    """Compile la_oracle.c and la_variants.c with gcc (-O2 -fopenmp); returns the .so path."""
+    newest = max(os.path.getmtime(s) for s in _SRCS)
+    if force or not os.path.exists(_SO) or os.path.getmtime(_SO) < newest:
         tmp = _SO + ".tmp%d" % os.getpid()
         subprocess.check_call(["gcc", "-O2", "-fopenmp", "-fPIC", "-shared", "-std=c11",
-                               "-o", tmp, _SRC, "-lm"])
+                               "-o", tmp] + _SRCS + ["-lm"])
         os.replace(tmp, _SO)
     return _SO
 
@@ -74,6 +85,16 @@ def _load():
         lib.lao_noncausal_backward_mut.restype = ctypes.c_int
         lib.lao_noncausal_backward_mut.argtypes = [f32p, f32p, f32p, f32p, L, L, L, L, dp, dp, dp,
                                                    ctypes.c_int, ctypes.c_int]
+        I = ctypes.c_int
+        lib.lav_feature_dim.restype = L
+        lib.lav_feature_dim.argtypes = [I, L, I]
+        lib.lav_features.restype = I
+        lib.lav_features.argtypes = [f32p, L, L, I, I, I, dp]
+        lib.lav_causal_mut.restype = I
+        lib.lav_causal_mut.argtypes = [f32p, f32p, f32p, dp, L, L, L, L, I, I, I, I,
+                                       dp, dp, dp, dp, dp, I, I]
+        lib.lav_noncausal.restype = I
+        lib.lav_noncausal.argtypes = [f32p, f32p, f32p, L, L, L, L, I, I, I, dp, I]
         _lib = lib
     return _lib
 
@@ -215,3 +236,70 @@ MUTANTS = {
     # backward
     "bwd_no_e": 11, "bwd_dphi_is_phi": 12, "bwd_excl_diag": 13, "bwd_dv_uses_q": 14,
 }
+
+
+# Variant identifiers of la_variants.c (feature map, read-out normalisation, update rule).
+FEATURE_MAPS = {"elu1": 0, "dpfp": 1, "poly2": 2}
+NORMS = {"den": 0, "sum": 1, "none": 2}
+UPDATES = {"sum": 0, "delta": 1}
+VARIANT_MUTANTS = {"dpfp_pos_only": 21, "poly_upper": 22, "sumnorm_k_only": 23,
+                   "delta_after": 24, "delta_sign": 25, "delta_beta_v": 26}
+
+
+def feature_dim(fm: str, D: int, nu: int = 1) -> int:
+    """F, the width of phi(x) for x in R^D (0 if the variant is invalid)."""
+    return int(_load().lav_feature_dim(FEATURE_MAPS[fm], int(D), int(nu)))
+
+
+def features(x, fm: str, nu: int = 1, sumnorm: bool = False) -> np.ndarray:
+    """phi of every row of x [..., D] -> [..., F] in fp64 (C loops)."""
+    x = _f32(x)
+    D = x.shape[-1]
+    F = feature_dim(fm, D, nu)
+    R = int(np.prod(x.shape[:-1])) if x.ndim > 1 else 1
+    out = np.empty(x.shape[:-1] + (F,), np.float64)
+    rc = _load().lav_features(x.reshape(-1), R, D, FEATURE_MAPS[fm], int(nu), int(bool(sumnorm)), _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle: bad feature map")
+    return out
+
+
+def variant_causal(q, k, v, fm="elu1", nu=1, norm="den", update="sum", beta=None,
+                   S0=None, z0=None, want_out=True, nthreads=0, mutant=0):
+    """Causal recurrence of a variant (la_variants.c).
+
+    q, k: [..., N, D]; v: [..., N, M]; beta: [..., N] (delta update).
+    Returns (out [..., N, M] or None, S [..., F, M], z [..., F]), fp64."""
+    q, k, v = _f32(q), _f32(k), _f32(v)
+    lead = q.shape[:-2]
+    N, D = q.shape[-2], q.shape[-1]
+    M = v.shape[-1]
+    F = feature_dim(fm, D, nu)
+    BH = int(np.prod(lead)) if lead else 1
+    b = None if beta is None else _f32(beta).reshape(-1)
+    out = np.empty(lead + (N, M), np.float64) if want_out else None
+    S = np.empty(lead + (F, M), np.float64)
+    z = np.empty(lead + (F,), np.float64)
+    S0a, z0a = _f64_or_none(S0, lead + (F, M)), _f64_or_none(z0, lead + (F,))
+    rc = _load().lav_causal_mut(q.reshape(-1), k.reshape(-1), v.reshape(-1), _ptr(b), BH, N, D, M,
+                                FEATURE_MAPS[fm], int(nu), NORMS[norm], UPDATES[update],
+                                _ptr(S0a), _ptr(z0a), _ptr(out), _ptr(S), _ptr(z),
+                                int(nthreads), int(mutant))
+    if rc != 0:
+        raise ValueError("oracle: bad variant or shape")
+    return out, S, z
+
+
+def variant_noncausal(q, k, v, fm="elu1", nu=1, norm="den", nthreads=0):
+    """Non-causal form of a variant (sum update).  Returns out [..., N, M] fp64."""
+    q, k, v = _f32(q), _f32(k), _f32(v)
+    lead = q.shape[:-2]
+    N, D = q.shape[-2], q.shape[-1]
+    M = v.shape[-1]
+    BH = int(np.prod(lead)) if lead else 1
+    out = np.empty(lead + (N, M), np.float64)
+    rc = _load().lav_noncausal(q.reshape(-1), k.reshape(-1), v.reshape(-1), BH, N, D, M,
+                               FEATURE_MAPS[fm], int(nu), NORMS[norm], _ptr(out), int(nthreads))
+    if rc != 0:
+        raise ValueError("oracle: bad variant or shape")
+    return out

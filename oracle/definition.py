@@ -66,3 +66,47 @@ def definition_rows(q, k, v, rows, causal: bool, prefix_state=None) -> np.ndarra
             den = den + fq[r] @ np.asarray(z0, np.float64)
         out[r] = num / den
     return out
+
+
+def features_np(x, fm: str, nu: int = 1, sumnorm: bool = False) -> np.ndarray:
+    """The variants' feature maps in vectorised numpy fp64, [..., D] -> [..., F].
+
+    * "elu1": eq. (7) of "Transformers are RNNs".
+    * "dpfp": DPFP-nu of "Linear Transformers Are Secretly Fast Weight
+      Programmers": r = [relu(x), relu(-x)], then for s = 1..nu the products
+      r * (r rolled left by s), concatenated in order of s.
+    * "poly2": the degree-2 polynomial map of "Transformers are RNNs"
+      sec. 3.2.1, the outer product x x^T flattened row by row.
+    sumnorm divides each feature vector by the sum of its components.
+    """
+    x = _as64(x)
+    if fm == "elu1":
+        f = phi_np(x)
+    elif fm == "dpfp":
+        r = np.concatenate([np.maximum(x, 0.0), np.maximum(-x, 0.0)], axis=-1)
+        f = np.concatenate([r * np.roll(r, -s, axis=-1) for s in range(1, nu + 1)], axis=-1)
+    elif fm == "poly2":
+        D = x.shape[-1]
+        f = (x[..., :, None] * x[..., None, :]).reshape(x.shape[:-1] + (D * D,))
+    else:
+        raise ValueError(fm)
+    if sumnorm:
+        f = f / f.sum(axis=-1, keepdims=True)
+    return f
+
+
+def definition_variant(q, k, v, fm: str, nu: int = 1, norm: str = "den", causal: bool = True) -> np.ndarray:
+    """Quadratic form of a sum-update variant: w_ij = phi(q_i)^T phi(k_j)
+    (eq. (4) with the variant's phi), masked to j <= i when causal (eq. (8));
+    "den" divides by sum_j w_ij (eq. (3)), "sum" uses sum-normalised features
+    and no denominator, "none" no denominator."""
+    v = _as64(v)
+    sn = norm == "sum"
+    w = features_np(q, fm, nu, sn) @ np.swapaxes(features_np(k, fm, nu, sn), -1, -2)
+    if causal:
+        N = w.shape[-1]
+        w = w * np.tril(np.ones((N, N)))
+    out = w @ v
+    if norm == "den":
+        out = out / w.sum(axis=-1, keepdims=True)
+    return out
