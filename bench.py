@@ -239,7 +239,10 @@ def run_ours(args, rank, world, dist):
                                 args.steps, max_over_ranks, world, rank, warmup=args.warmup)
             return {"only": args.only, "leg": leg, "gpu_launches_total": la.la_launch_count()}
         w = inputs.WORKLOADS[args.only]
-        if w.op == "decode":
+        if w.op == "causal_variant":
+            leg = _leg_variant(torch, la, inputs, args.only, dev, stream, flush, pk, args.steps, max_over_ranks,
+                               world, rank, warmup=args.warmup)
+        elif w.op == "decode":
             leg = _leg_decode(torch, la, inputs, dev, stream, flush, pk, args, max_over_ranks, world, rank)
         else:
             leg = _leg_fwd(torch, la, inputs, args.only, dev, stream, flush, pk, args.steps, max_over_ranks,
@@ -358,6 +361,9 @@ def run_ours(args, rank, world, dist):
                                                max_over_ranks, world, rank)
         result["legs"]["backward"] = _leg_backward(torch, la, inputs, MAIN, dev, stream, flush, pk, 5,
                                                    max_over_ranks, world, rank)
+        for name in ("delta_b16h8n3072d64", "dpfp_b16h8n3072d64"):
+            result["legs"][name.split("_")[0]] = _leg_variant(torch, la, inputs, name, dev, stream, flush, pk, 5,
+                                                              max_over_ranks, world, rank)
 
     # ------------------------------------------------- CPU baseline (rank 0)
     if rank == 0 and not args.no_cpu:
@@ -414,6 +420,49 @@ def _leg_backward(torch, la, inputs, name, dev, stream, flush, pk, steps, max_ov
            "note": "tcgen05 kernels (bf16 D = M = 64): a forward sweep (dQ, keeps g and e) and a reverse "
                    "sweep (dK, dV), one CTA per head each"}
     del q, k, v, G, dq, dk, dv
+    torch.cuda.empty_cache()
+    return leg
+
+
+# fp32 CUDA-core peak of a GB300: 152 SMs x 128 FP32 lanes x 2 flop (FMA) x 2070 MHz
+FP32_ALU_TFLOPS = 152 * 128 * 2 * 2.070e9 / 1e12
+
+
+def _leg_variant(torch, la, inputs, name, dev, stream, flush, pk, steps, max_over_ranks, world, rank, warmup=3):
+    """Causal variant forward (feature map / sum normalisation / delta rule) on CUDA cores."""
+    w = inputs.WORKLOADS[name]
+    fm, nu, norm, update = w.variant
+    var = la.variant(fm, nu, norm, update)
+    F = la.la_feature_dim(var, w.D)
+    q, k, v = [t.to(dev) for t in inputs.workload_inputs(w, rank)]
+    beta = inputs.workload_betas(w, rank).to(dev) if update == "delta" else None
+    out = torch.empty(w.B, w.H, w.N, w.M, dtype=w.dtype, device=dev)
+    fn = lambda: la.la_forward_causal_variant(q, k, v, var, beta=beta, out=out, stream=stream)  # noqa: E731
+    el = q.element_size()
+    in_bytes = (2 * q.numel() + v.numel() + (beta.numel() if beta is not None else 0)) * el
+    l0 = la.la_launch_count()
+    t = _timed_steps(torch, fn, steps, warmup, flush.for_inputs(in_bytes), stream)
+    launches = (la.la_launch_count() - l0) // (steps + warmup)
+    ms = max_over_ranks(sum(t) / len(t))
+    alg = in_bytes + out.numel() * el                          # read Q, K, V (beta) once, write O once
+    gbs = alg / (ms / 1e3) / 1e9
+    # per head-token: state update 2FM (+ retrieval 2FM for the delta rule) and read-out 2FM
+    flops = w.B * w.H * w.N * (6 if update == "delta" else 4) * F * w.M
+    tf = flops / (ms / 1e3) / 1e12
+    leg = {"workload": name, "op": "causal_variant", "variant": {"feature_map": fm, "nu": nu, "norm": norm,
+                                                                 "update": update, "F": F},
+           "value": round(world * w.B * w.N / (ms / 1e3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 5),
+           "steps": steps, "launches_per_step": launches,
+           "roofline": {"bound": "alu", "achieved": round(tf, 2), "peak": round(FP32_ALU_TFLOPS, 1),
+                        "unit": "TFLOP/s", "frac": round(tf / FP32_ALU_TFLOPS, 4),
+                        "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 x 2070 MHz",
+                        "alg_flops_per_launch": flops},
+           "hbm": {"achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                   "frac": round(gbs / pk["hbm_gbs"], 4), "alg_bytes_per_launch": alg},
+           "l2": flush.describe(in_bytes),
+           "note": "CUDA-core recurrence: one CTA per (head, 16 state columns), each warp walking the tokens "
+                   "of a chunk on its own columns"}
+    del q, k, v, beta, out
     torch.cuda.empty_cache()
     return leg
 
@@ -573,7 +622,8 @@ def main():
     ap.add_argument("--no-graph", action="store_true")
     ap.add_argument("--only", default=None,
                     choices=["causal_b16h8n3072d64", "noncausal_b8h8n4096d64", "causal_b1h16n65536d128",
-                             "decode_b256h16d64", "backward_causal_b16h8n3072d64"],
+                             "decode_b256h16d64", "backward_causal_b16h8n3072d64",
+                             "delta_b16h8n3072d64", "dpfp_b16h8n3072d64"],
                     help="time this one workload alone (--steps/--warmup; decode: --decode-steps) and print "
                          "its leg object; for profiler captures, not a bench line")
     args = ap.parse_args()

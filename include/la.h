@@ -191,6 +191,95 @@ la_status la_backward_noncausal(const void *q, const void *k, const void *v, con
                                 void *dq, void *dk, void *dv, la_shape s,
                                 void *workspace, size_t ws_bytes, la_stream_t stream);
 
+/* ------------------------------------------------------------------ variants
+ * Other feature maps, read-out normalisations and the delta update rule.
+ * Sources: "Transformers are RNNs" (TaR) sec. 3.2.1 (the degree-2 polynomial
+ * kernel and its exact feature map) and "Linear Transformers Are Secretly
+ * Fast Weight Programmers" (FWP: the DPFP feature map, sum normalisation, the
+ * delta update rule), whose summary page lost its equations; each rule below
+ * is the plainest reading of its prose.
+ *
+ * Feature map phi: R^D -> R^F, applied to every row of Q and K:
+ *   LA_FM_ELU1   elu(x) + 1 (TaR eq. (7)); F = D.
+ *   LA_FM_DPFP   DPFP-nu (FWP): r = [relu(x), relu(-x)] in R^{2D}; feature
+ *                (s-1)*2D + i is r_i * r_{(i+s) mod 2D} for s = 1..nu,
+ *                i = 0..2D-1; F = 2*D*nu, 1 <= nu < 2D.
+ *   LA_FM_POLY2  degree-2 polynomial kernel (q.k)^2 (TaR sec. 3.2.1):
+ *                feature a*D + b is x_a x_b; F = D^2.
+ * Read-out (norm):
+ *   LA_NORM_DEN  y_i = phi(q_i)^T S_i / phi(q_i)^T z_i, z_i = sum phi(k_j)
+ *                (TaR eq. (12); FWP's "accumulator").
+ *   LA_NORM_SUM  phi(q) and phi(k) are divided by the sum of their
+ *                components (FWP); y_i = phi(q_i)^T S_i, no denominator.
+ *   LA_NORM_NONE y_i = phi(q_i)^T S_i.
+ * Update of the state S (F x M):
+ *   LA_UPDATE_SUM    S_i = S_{i-1} + phi(k_i) v_i^T (TaR eq. (10)).
+ *   LA_UPDATE_DELTA  vbar_i = S_{i-1}^T phi(k_i) (the value now paired with
+ *                    k_i); S_i = S_{i-1} + phi(k_i) (beta_i (v_i - vbar_i))^T,
+ *                    which stores beta_i v_i + (1 - beta_i) vbar_i in its place
+ *                    (FWP); beta_i in [0, 1] is an input per token and head.
+ * The read-out of token i follows its update (TaR eqs. (18)-(20)).
+ * Supported: F <= 512; DPFP with LA_NORM_SUM or LA_NORM_NONE (with the
+ * denominator, a query whose adjacent sign pairs match no earlier key gets
+ * 0/0); POLY2 with LA_NORM_DEN or LA_NORM_NONE (its features can be
+ * negative); LA_UPDATE_DELTA with LA_NORM_SUM only (|phi(k)|^2 <= 1 keeps
+ * the state bounded).  Other combinations return LA_ERR_UNSUPPORTED;
+ * unknown enum values LA_ERR_INVALID_ARG.
+ * State layout: S [B, H, F, M] fp32 (S[f][m]); z [B, H, F] fp32 (LA_NORM_DEN
+ * only).  Arithmetic fp32 on CUDA cores for every dtype.
+ */
+typedef enum { LA_FM_ELU1 = 0, LA_FM_DPFP = 1, LA_FM_POLY2 = 2 } la_feature_map;
+typedef enum { LA_NORM_DEN = 0, LA_NORM_SUM = 1, LA_NORM_NONE = 2 } la_norm;
+typedef enum { LA_UPDATE_SUM = 0, LA_UPDATE_DELTA = 1 } la_update;
+
+typedef struct {
+    la_feature_map feature_map;
+    int nu;                 /* DPFP shifts (ignored by the other maps) */
+    la_norm norm;
+    la_update update;
+} la_variant;
+
+/* F, the width of phi(x) for x in R^D under `var`; 0 if `var` is invalid. */
+int la_feature_dim(la_variant var, int D);
+
+/*
+ * Bytes of device workspace la_forward_noncausal_variant needs (0 for the
+ * causal and decode calls, which need none); (size_t)-1 if invalid.
+ */
+size_t la_variant_workspace_bytes(la_op op, la_shape s, la_variant var);
+
+/*
+ * Causal form of a variant over [B,H,N,.] inputs:
+ *   q, k: [B,H,N,D]; v, out: [B,H,N,M]; beta: [B,H,N] (LA_UPDATE_DELTA,
+ *      else ignored and may be NULL); all of dtype s.dtype.
+ *   out may be NULL (state only).
+ *   S: [B,H,F,M] fp32 or NULL; z: [B,H,F] fp32 or NULL.  With LA_NORM_DEN
+ *      both or neither (as la_forward_causal); otherwise z must be NULL.  A
+ *      given state is the starting state and receives the final state.
+ * Errors as la_forward_causal.
+ */
+la_status la_forward_causal_variant(const void *q, const void *k, const void *v, const void *beta,
+                                    void *out, la_shape s, la_variant var, float *S, float *z,
+                                    la_stream_t stream);
+
+/*
+ * Non-causal form of a variant (LA_UPDATE_SUM only): KV = sum_j phi(K_j) V_j^T
+ * and, for LA_NORM_DEN, sum_j phi(K_j) over all N keys, then y_i =
+ * phi(Q_i)^T KV (/ phi(Q_i)^T sum_j phi(K_j)).
+ *   workspace: la_variant_workspace_bytes(LA_OP_NONCAUSAL, s, var) bytes.
+ */
+la_status la_forward_noncausal_variant(const void *q, const void *k, const void *v, void *out,
+                                       la_shape s, la_variant var, void *workspace, size_t ws_bytes,
+                                       la_stream_t stream);
+
+/*
+ * One recurrent step of a variant: q, k [B,H,D]; v, y [B,H,M]; beta [B,H]
+ * (delta rule); S [B,H,F,M] and (LA_NORM_DEN) z [B,H,F] fp32 updated in
+ * place; z must be NULL otherwise.  s.N is ignored.
+ */
+la_status la_decode_step_variant(const void *q, const void *k, const void *v, const void *beta, void *y,
+                                 float *S, float *z, la_shape s, la_variant var, la_stream_t stream);
+
 /*
  * Non-causal attention that allocates nothing, for callers that cannot
  * allocate device memory: code that only receives pointers from a host

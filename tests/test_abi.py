@@ -163,3 +163,53 @@ def test_generation_argument_checks(lib):
     assert lib.la_decode_steps(q, k, v, o, None, _addr(6), None, 4, sh, None) == la.LA_ERR_INVALID_ARG
     assert lib.la_decode_steps(None, None, None, None, None, None, None, 0, sh, None) == la.LA_OK
     assert lib.la_decode_steps(q, k, v, o, _addr(5), _addr(6), None, 4, _shape(D=24), None) == la.LA_ERR_UNSUPPORTED
+
+
+def test_variant_feature_dims(lib):
+    V = la.variant
+    assert la.la_feature_dim(V("elu1"), 64) == 64
+    assert la.la_feature_dim(V("dpfp", 1, "sum"), 64) == 128
+    assert la.la_feature_dim(V("dpfp", 3, "none"), 64) == 384
+    assert la.la_feature_dim(V("poly2", 1, "den"), 16) == 256
+    assert la.la_feature_dim(V("dpfp", 0, "sum"), 64) == 0            # nu out of range
+    assert la.la_feature_dim(la.la_variant(7, 1, 0, 0), 64) == 0       # unknown feature map
+
+
+def test_variant_argument_checks(lib):
+    V = la.variant
+    sh = _shape(B=2, N=64, D=16, M=16)
+    q, k, v, b, o, S, z = (_addr(i) for i in range(7))
+    call = lib.la_forward_causal_variant
+    # unsupported combinations
+    assert call(q, k, v, None, o, sh, V("dpfp", 1, "den"), None, None, None) == la.LA_ERR_UNSUPPORTED
+    assert call(q, k, v, None, o, sh, V("poly2", 1, "sum"), None, None, None) == la.LA_ERR_UNSUPPORTED
+    assert call(q, k, v, b, o, sh, V("elu1", 1, "den", "delta"), S, z, None) == la.LA_ERR_UNSUPPORTED
+    assert call(q, k, v, None, o, _shape(D=64), V("poly2", 1, "den"), None, None, None) \
+        == la.LA_ERR_UNSUPPORTED                                      # F = 4096 > 512
+    assert call(q, k, v, None, o, _shape(D=128), V("dpfp", 3, "sum"), None, None, None) \
+        == la.LA_ERR_UNSUPPORTED                                      # F = 768 > 512
+    # unknown enum values, nu out of range
+    assert call(q, k, v, None, o, sh, la.la_variant(0, 1, 5, 0), None, None, None) == la.LA_ERR_INVALID_ARG
+    assert call(q, k, v, None, o, sh, la.la_variant(0, 1, 0, 3), None, None, None) == la.LA_ERR_INVALID_ARG
+    assert call(q, k, v, None, o, sh, V("dpfp", 40, "sum"), None, None, None) == la.LA_ERR_INVALID_ARG
+    # delta rule needs beta; z only with the denominator; S and z together there
+    assert call(q, k, v, None, o, sh, V("elu1", 1, "sum", "delta"), None, None, None) == la.LA_ERR_INVALID_ARG
+    assert call(q, k, v, None, o, sh, V("elu1", 1, "sum"), S, z, None) == la.LA_ERR_INVALID_ARG
+    assert call(q, k, v, None, o, sh, V("elu1", 1, "den"), S, None, None) == la.LA_ERR_INVALID_ARG
+    assert call(q, k, v, None, o, sh, V("elu1", 1, "den"), None, z, None) == la.LA_ERR_INVALID_ARG
+    # misaligned, aliasing, empty
+    assert call(MISALIGNED, k, v, None, o, sh, V(), None, None, None) == la.LA_ERR_INVALID_ARG
+    assert call(q, k, v, None, q, sh, V(), None, None, None) == la.LA_ERR_INVALID_ARG
+    assert call(None, None, None, None, None, _shape(N=0), V("dpfp", 2, "none"), None, None, None) == la.LA_OK
+    # non-causal: sum update only; workspace
+    nc = lib.la_forward_noncausal_variant
+    need = la.lib().la_variant_workspace_bytes(la.LA_OP_NONCAUSAL, sh, V("dpfp", 1, "sum"))
+    assert need == 2 * 2 * (32 * 16 + 32) * 4                      # 2 heads, 2 key splits, F = 2 * 16
+    assert nc(q, k, v, o, sh, V("elu1", 1, "sum", "delta"), _addr(9), 1 << 20, None) == la.LA_ERR_UNSUPPORTED
+    assert nc(q, k, v, o, sh, V("dpfp", 1, "sum"), _addr(9), need - 4, None) == la.LA_ERR_INVALID_ARG
+    assert nc(None, None, None, None, _shape(B=0), V(), None, 0, None) == la.LA_OK
+    # decode: the state is required
+    dec = lib.la_decode_step_variant
+    assert dec(q, k, v, None, o, None, None, sh, V("elu1", 1, "sum"), None) == la.LA_ERR_INVALID_ARG
+    assert dec(q, k, v, None, o, S, None, sh, V("elu1", 1, "sum", "delta"), None) == la.LA_ERR_INVALID_ARG
+    assert dec(None, None, None, None, None, None, None, _shape(B=0), V(), None) == la.LA_OK

@@ -310,6 +310,100 @@ la_status la_decode_step(const void *q, const void *k, const void *v, void *y, f
     return from_cuda(decode_step(p, *dev));
 }
 
+int la_feature_dim(la_variant var, int D) {
+    if (fw_check_variant(var, D) == LA_ERR_INVALID_ARG) return 0;
+    return fw_feature_dim(var, D);
+}
+
+size_t la_variant_workspace_bytes(la_op op, la_shape s, la_variant var) {
+    if (check_shape(s, op != LA_OP_DECODE) != LA_OK || fw_check_variant(var, s.D) != LA_OK) return (size_t)-1;
+    switch (op) {
+        case LA_OP_NONCAUSAL: return var.update == LA_UPDATE_SUM ? fw_noncausal_ws_bytes(s, var) : (size_t)-1;
+        case LA_OP_CAUSAL:
+        case LA_OP_DECODE: return 0;
+        default: return (size_t)-1;
+    }
+}
+
+namespace {
+
+// Checks shared by the causal and decode variants: the variant, the state
+// pointers (z only with the denominator) and beta (delta rule).
+la_status check_variant_state(const la_shape &s, const la_variant &var, const void *beta, const float *S,
+                              const float *z, bool work, bool state_required) {
+    la_status st = fw_check_variant(var, s.D);
+    if (st != LA_OK) return st;
+    const long long BH = (long long)s.B * s.H;
+    if (var.norm == LA_NORM_DEN) {
+        if ((S == nullptr) != (z == nullptr)) return LA_ERR_INVALID_ARG;
+    } else if (z != nullptr) {
+        return LA_ERR_INVALID_ARG;
+    }
+    if (state_required && BH > 0 && S == nullptr) return LA_ERR_INVALID_ARG;
+    if ((st = check_ptr(S, S != nullptr && BH > 0)) || (st = check_ptr(z, z != nullptr && BH > 0))) return st;
+    if (var.update == LA_UPDATE_DELTA && (st = check_ptr(beta, work)) != LA_OK) return st;
+    if (BH > 0x7fffffffLL) return LA_ERR_UNSUPPORTED;
+    return LA_OK;
+}
+
+}  // namespace
+
+la_status la_forward_causal_variant(const void *q, const void *k, const void *v, const void *beta, void *out,
+                                    la_shape s, la_variant var, float *S, float *z, la_stream_t stream) {
+    la_status st = check_shape(s, true);
+    if (st != LA_OK) return st;
+    const long long BH = (long long)s.B * s.H;
+    const bool work = BH > 0 && s.N > 0;
+    if ((st = check_variant_state(s, var, beta, S, z, work, false)) != LA_OK) return st;
+    if ((st = check_ptr(q, work)) || (st = check_ptr(k, work)) || (st = check_ptr(v, work)) ||
+        (st = check_ptr(out, work && out != nullptr)))
+        return st;
+    if (!work) return LA_OK;   // an empty sequence leaves the state as it is
+    if (out != nullptr && (out == q || out == k || out == v || out == beta)) return LA_ERR_INVALID_ARG;
+    Problem p{q, k, v, out, S, z, BH, s.N, s.D, s.M, s.dtype, 0, nullptr, 0, (cudaStream_t)stream};
+    return from_cuda(fw_causal(p, var.update == LA_UPDATE_DELTA ? beta : nullptr, var));
+}
+
+la_status la_forward_noncausal_variant(const void *q, const void *k, const void *v, void *out, la_shape s,
+                                       la_variant var, void *workspace, size_t ws_bytes, la_stream_t stream) {
+    la_status st = check_shape(s, true);
+    if (st != LA_OK) return st;
+    if ((st = fw_check_variant(var, s.D)) != LA_OK) return st;
+    if (var.update != LA_UPDATE_SUM) return LA_ERR_UNSUPPORTED;
+    const long long BH = (long long)s.B * s.H;
+    const bool work = BH > 0 && s.N > 0;
+    if ((st = check_ptr(q, work)) || (st = check_ptr(k, work)) || (st = check_ptr(v, work)) ||
+        (st = check_ptr(out, work)))
+        return st;
+    if (!work) return LA_OK;
+    if (BH > 0x7fffffffLL) return LA_ERR_UNSUPPORTED;
+    if (out == q || out == k || out == v) return LA_ERR_INVALID_ARG;
+    const size_t need = la_variant_workspace_bytes(LA_OP_NONCAUSAL, s, var);
+    if (ws_bytes < need || (need > 0 && check_ptr(workspace, true) != LA_OK)) return LA_ERR_INVALID_ARG;
+    const DeviceInfo *dev = device_info();
+    if (!dev) return LA_ERR_CUDA;
+    Problem p{q, k, v, out, nullptr, nullptr, BH, s.N, s.D, s.M, s.dtype, 0, workspace, ws_bytes,
+              (cudaStream_t)stream};
+    return from_cuda(fw_noncausal(p, var, *dev));
+}
+
+la_status la_decode_step_variant(const void *q, const void *k, const void *v, const void *beta, void *y,
+                                 float *S, float *z, la_shape s, la_variant var, la_stream_t stream) {
+    la_status st = check_shape(s, false);
+    if (st != LA_OK) return st;
+    const long long BH = (long long)s.B * s.H;
+    const bool work = BH > 0;
+    if ((st = check_variant_state(s, var, beta, S, z, work, true)) != LA_OK) return st;
+    if ((st = check_ptr(q, work)) || (st = check_ptr(k, work)) || (st = check_ptr(v, work)) ||
+        (st = check_ptr(y, work)))
+        return st;
+    if (!work) return LA_OK;
+    if (y == q || y == k || y == v || y == beta) return LA_ERR_INVALID_ARG;
+    // one step is the causal form over a single token, started from (S, z)
+    Problem p{q, k, v, y, S, z, BH, 1, s.D, s.M, s.dtype, 0, nullptr, 0, (cudaStream_t)stream};
+    return from_cuda(fw_causal(p, var.update == LA_UPDATE_DELTA ? beta : nullptr, var));
+}
+
 la_status la_get_last_error(la_stream_t stream) {
     if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return LA_ERR_CUDA;
     if (cudaGetLastError() != cudaSuccess) return LA_ERR_CUDA;

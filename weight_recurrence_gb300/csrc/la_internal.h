@@ -81,6 +81,15 @@ bool tc_noncausal_supported(const la_shape &s);
 size_t tc_noncausal_ws_bytes(const la_shape &s);
 cudaError_t tc_noncausal(const Problem &p, const DeviceInfo &dev);
 
+// ---- variants (la_fw.cu): feature maps, sum normalisation, delta rule; CUDA cores.
+constexpr int kFwMaxFeatures = 512;          // largest feature width F
+int fw_feature_dim(const la_variant &v, int D);
+la_status fw_check_variant(const la_variant &v, int D);
+size_t fw_noncausal_ws_bytes(const la_shape &s, const la_variant &v);
+// causal form (also one decode step with N = 1); beta [BH, N] for the delta rule
+cudaError_t fw_causal(const Problem &p, const void *beta, const la_variant &v);
+cudaError_t fw_noncausal(const Problem &p, const la_variant &v, const DeviceInfo &dev);
+
 // Counts kernel launches made through the library (la_api.cu).
 void count_launches(int n);
 

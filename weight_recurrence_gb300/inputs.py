@@ -35,6 +35,7 @@ class Workload:
     chunk: int = 0     # causal chunk length (0 = library default)
     steps: int = 0     # decode: sequential steps after the prefill
     seed: int = 0
+    variant: tuple = ()  # (feature map, nu, norm, update) of a variant workload; () = elu + 1
 
     @property
     def tokens(self) -> int:
@@ -55,7 +56,20 @@ WORKLOADS = {
                                        torch.bfloat16, 1.0 / math.sqrt(128), 128, 0, 1004),
     "decode_b256h16d64": Workload("decode_b256h16d64", "decode", 256, 16, 1024, 64, 64,
                                   torch.bfloat16, 1.0, 0, 4096, 1005),
+    # Variants on the training shape: the delta rule with sum-normalised elu + 1
+    # features, and the sum rule with sum-normalised DPFP-1 features (F = 128).
+    "delta_b16h8n3072d64": Workload("delta_b16h8n3072d64", "causal_variant", 16, 8, 3072, 64, 64,
+                                    torch.bfloat16, 1.0 / math.sqrt(64), 0, 0, 1006, ("elu1", 1, "sum", "delta")),
+    "dpfp_b16h8n3072d64": Workload("dpfp_b16h8n3072d64", "causal_variant", 16, 8, 3072, 64, 64,
+                                   torch.bfloat16, 1.0 / math.sqrt(64), 0, 0, 1007, ("dpfp", 1, "sum", "sum")),
 }
+
+
+def betas(B, H, N, dtype=torch.bfloat16, seed=0, device="cpu"):
+    """Per-token interpolation weights of the delta rule, [B, H, N], drawn
+    uniform on [0, 1) and cast to dtype."""
+    g = torch.Generator(device=device).manual_seed(int(seed))
+    return torch.rand((B, H, N), generator=g, dtype=torch.float32, device=device).to(dtype).contiguous()
 
 
 def qkv(B, H, N, D, M, dtype=torch.bfloat16, scale=1.0, seed=0, device="cpu"):
@@ -110,3 +124,8 @@ def rank_seed(seed: int, rank: int) -> int:
 def workload_inputs(w: Workload, rank: int = 0):
     """Inputs of a named workload: (q, k, v) on the CPU, rank ``rank``'s batch."""
     return qkv(w.B, w.H, w.N, w.D, w.M, w.dtype, w.scale, rank_seed(w.seed, rank))
+
+
+def workload_betas(w: Workload, rank: int = 0):
+    """Delta-rule weights of a named workload, [B, H, N], from their own seed stream."""
+    return betas(w.B, w.H, w.N, w.dtype, rank_seed(w.seed, rank) + 1000000)

@@ -23,7 +23,13 @@ LA_OP_NONCAUSAL, LA_OP_CAUSAL, LA_OP_DECODE, LA_OP_NONCAUSAL_BWD, LA_OP_CAUSAL_B
 EXPORTED = ("la_workspace_bytes", "la_forward_noncausal", "la_forward_causal", "la_decode_step",
             "la_get_last_error", "la_status_string", "la_version", "la_launch_count",
             "la_debug_inject_timeout", "la_forward_noncausal_noalloc", "la_backward_causal",
-            "la_backward_noncausal", "la_forward_causal_varlen", "la_decode_steps")
+            "la_backward_noncausal", "la_forward_causal_varlen", "la_decode_steps",
+            "la_feature_dim", "la_variant_workspace_bytes", "la_forward_causal_variant",
+            "la_forward_noncausal_variant", "la_decode_step_variant")
+
+LA_FM = {"elu1": 0, "dpfp": 1, "poly2": 2}
+LA_NORM = {"den": 0, "sum": 1, "none": 2}
+LA_UPDATE = {"sum": 0, "delta": 1}
 
 
 class LAError(RuntimeError):
@@ -35,6 +41,17 @@ class LAError(RuntimeError):
 class la_shape(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int), ("H", ctypes.c_int), ("N", ctypes.c_int),
                 ("D", ctypes.c_int), ("M", ctypes.c_int), ("dtype", ctypes.c_int)]
+
+
+class la_variant(ctypes.Structure):
+    _fields_ = [("feature_map", ctypes.c_int), ("nu", ctypes.c_int), ("norm", ctypes.c_int),
+                ("update", ctypes.c_int)]
+
+
+def variant(fm: str = "elu1", nu: int = 1, norm: str = "den", update: str = "sum") -> la_variant:
+    """la_variant from names: fm in {"elu1", "dpfp", "poly2"}, norm in {"den",
+    "sum", "none"}, update in {"sum", "delta"}."""
+    return la_variant(LA_FM[fm], int(nu), LA_NORM[norm], LA_UPDATE[update])
 
 
 _lib = None
@@ -75,6 +92,16 @@ def lib() -> ctypes.CDLL:
         L.la_decode_steps.argtypes = [vp, vp, vp, vp, vp, vp, vp, i, la_shape, vp]
         L.la_backward_noncausal.restype = i
         L.la_backward_noncausal.argtypes = [vp, vp, vp, vp, vp, vp, vp, la_shape, vp, sz, vp]
+        L.la_feature_dim.restype = i
+        L.la_feature_dim.argtypes = [la_variant, i]
+        L.la_variant_workspace_bytes.restype = sz
+        L.la_variant_workspace_bytes.argtypes = [i, la_shape, la_variant]
+        L.la_forward_causal_variant.restype = i
+        L.la_forward_causal_variant.argtypes = [vp, vp, vp, vp, vp, la_shape, la_variant, vp, vp, vp]
+        L.la_forward_noncausal_variant.restype = i
+        L.la_forward_noncausal_variant.argtypes = [vp, vp, vp, vp, la_shape, la_variant, vp, sz, vp]
+        L.la_decode_step_variant.restype = i
+        L.la_decode_step_variant.argtypes = [vp, vp, vp, vp, vp, vp, vp, la_shape, la_variant, vp]
         _lib = L
     return _lib
 
@@ -285,6 +312,61 @@ def la_backward_noncausal(q, k, v, dout, dq=None, dk=None, dv=None, stream=None)
                                      _ptr(ws), need, ctypes.c_void_p(sp))
     _check(st, "la_backward_noncausal")
     return dq, dk, dv
+
+
+def la_feature_dim(var: la_variant, D: int) -> int:
+    """Width F of phi(x) for x in R^D under the variant (0 if invalid)."""
+    return int(lib().la_feature_dim(var, int(D)))
+
+
+def la_forward_causal_variant(q, k, v, var: la_variant, beta=None, out=None, S=None, z=None, want_out=True,
+                              stream=None):
+    """Causal form of a variant: q, k [B,H,N,D], v [B,H,N,M], beta [B,H,N]
+    (delta rule).  S [B,H,F,M] (and z [B,H,F] with the denominator) fp32, if
+    given, hold the starting state and receive the final one."""
+    _contig(q, k, v, beta, S, z)
+    s = shape_of(q, v)
+    if out is None and want_out:
+        out = torch.empty(q.shape[:-1] + (v.shape[-1],), dtype=q.dtype, device=q.device)
+    _contig(out)
+    st = lib().la_forward_causal_variant(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(out), s, var, _ptr(S),
+                                         _ptr(z), _stream(stream, q.device))
+    _check(st, "la_forward_causal_variant")
+    return out
+
+
+def la_forward_noncausal_variant(q, k, v, var: la_variant, out=None, stream=None):
+    """Non-causal form of a variant (sum update)."""
+    _contig(q, k, v)
+    s = shape_of(q, v)
+    if out is None:
+        out = torch.empty(q.shape[:-1] + (v.shape[-1],), dtype=q.dtype, device=q.device)
+    _contig(out)
+    need = lib().la_variant_workspace_bytes(LA_OP_NONCAUSAL, s, var)
+    if need == _SIZE_MAX:
+        raise LAError(LA_ERR_UNSUPPORTED, "la_variant_workspace_bytes")
+    sp = _stream_ptr(stream, q.device)
+    ws = _workspace(int(need), q.device, sp)
+    st = lib().la_forward_noncausal_variant(_ptr(q), _ptr(k), _ptr(v), _ptr(out), s, var, _ptr(ws), int(need),
+                                            ctypes.c_void_p(sp))
+    _check(st, "la_forward_noncausal_variant")
+    return out
+
+
+def la_decode_step_variant(q, k, v, S, var: la_variant, z=None, beta=None, y=None, stream=None):
+    """One recurrent step of a variant: q, k [B,H,D], v [B,H,M], beta [B,H];
+    S [B,H,F,M] (and z [B,H,F] with the denominator) updated in place."""
+    _contig(q, k, v, S, z, beta)
+    B, H, D = q.shape
+    M = v.shape[-1]
+    if y is None:
+        y = torch.empty((B, H, M), dtype=q.dtype, device=q.device)
+    _contig(y)
+    s = la_shape(B, H, 1, D, M, _dtype_code(q.dtype))
+    st = lib().la_decode_step_variant(_ptr(q), _ptr(k), _ptr(v), _ptr(beta), _ptr(y), _ptr(S), _ptr(z), s, var,
+                                      _stream(stream, q.device))
+    _check(st, "la_decode_step_variant")
+    return y
 
 
 def la_get_last_error(stream=None, device=None) -> int:
