@@ -449,19 +449,31 @@ def _leg_variant(torch, la, inputs, name, dev, stream, flush, pk, steps, max_ove
     # per head-token: state update 2FM (+ retrieval 2FM for the delta rule) and read-out 2FM
     flops = w.B * w.H * w.N * (6 if update == "delta" else 4) * F * w.M
     tf = flops / (ms / 1e3) / 1e12
+    # the library's routing rule: bf16 sum-update variants without the
+    # denominator and with F, M in {64, 128} run the chunked tcgen05 kernel
+    tc = (w.dtype == torch.bfloat16 and update == "sum" and norm != "den" and F in (64, 128)
+          and w.M in (64, 128))
+    hbm = {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+           "frac": round(gbs / pk["hbm_gbs"], 4), "alg_bytes_per_launch": alg,
+           "traffic": _traffic("causal_variant_" + name)}
+    alu = {"bound": "alu", "achieved": round(tf, 2), "peak": round(FP32_ALU_TFLOPS, 1), "unit": "TFLOP/s",
+           "frac": round(tf / FP32_ALU_TFLOPS, 4), "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 x 2070 MHz",
+           "alg_flops_per_launch": flops}
     leg = {"workload": name, "op": "causal_variant", "variant": {"feature_map": fm, "nu": nu, "norm": norm,
                                                                  "update": update, "F": F},
            "value": round(world * w.B * w.N / (ms / 1e3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 5),
            "steps": steps, "launches_per_step": launches,
-           "roofline": {"bound": "alu", "achieved": round(tf, 2), "peak": round(FP32_ALU_TFLOPS, 1),
-                        "unit": "TFLOP/s", "frac": round(tf / FP32_ALU_TFLOPS, 4),
-                        "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 x 2070 MHz",
-                        "alg_flops_per_launch": flops},
-           "hbm": {"achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                   "frac": round(gbs / pk["hbm_gbs"], 4), "alg_bytes_per_launch": alg},
-           "l2": flush.describe(in_bytes),
-           "note": "CUDA-core recurrence: one CTA per (head, 16 state columns), each warp walking the tokens "
-                   "of a chunk on its own columns"}
+           "roofline": hbm if tc else alu,
+           "l2": flush.describe(in_bytes)}
+    if tc:
+        leg["tensor"] = {"alg_tflops": round(tf, 2), "peak": pk["bf16_tflops"], "unit": "TFLOP/s",
+                         "frac_alg": round(tf / pk["bf16_tflops"], 4)}
+        leg["note"] = ("chunked tcgen05 causal kernel, the feature map applied row by row in shared memory "
+                       "between TMA and MMA")
+    else:
+        leg["hbm"] = hbm
+        leg["note"] = ("CUDA-core recurrence: one CTA per (head, 16 state columns), each warp walking the tokens "
+                       "of a chunk on its own columns")
     del q, k, v, beta, out
     torch.cuda.empty_cache()
     return leg

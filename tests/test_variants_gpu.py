@@ -67,7 +67,24 @@ def _ids(c):
                                                "f32" if c[9] == torch.float32 else "bf16")
 
 
-@pytest.mark.parametrize("case", CASES, ids=_ids)
+# bf16, sum update, no denominator, F in {64, 128}: these run on the chunked
+# tensor-core kernel, the feature map applied row by row on chip
+TC_CASES = [
+    ("dpfp", 1, "sum", "sum", 2, 2, 1000, 64, 64, torch.bfloat16, 0.125),
+    ("dpfp", 1, "none", "sum", 1, 2, 300, 64, 128, torch.bfloat16, 0.125),
+    ("dpfp", 1, "sum", "sum", 1, 3, 257, 32, 64, torch.bfloat16, 0.25),
+    ("dpfp", 2, "sum", "sum", 1, 2, 129, 16, 128, torch.bfloat16, 0.5),
+    ("dpfp", 2, "none", "sum", 2, 1, 400, 32, 64, torch.bfloat16, 0.25),
+    ("dpfp", 4, "sum", "sum", 1, 2, 200, 16, 128, torch.bfloat16, 0.5),
+    ("elu1", 1, "sum", "sum", 2, 2, 777, 64, 64, torch.bfloat16, 0.125),
+    ("elu1", 1, "sum", "sum", 1, 2, 300, 128, 128, torch.bfloat16, 1.0 / math.sqrt(128)),
+    ("elu1", 1, "none", "sum", 1, 2, 300, 64, 128, torch.bfloat16, 0.125),
+    ("elu1", 1, "none", "sum", 1, 1, 1, 128, 64, torch.bfloat16, 1.0),
+    ("dpfp", 1, "sum", "sum", 1, 1, 1, 64, 64, torch.bfloat16, 0.125),
+]
+
+
+@pytest.mark.parametrize("case", CASES + TC_CASES, ids=_ids)
 @pytest.mark.parametrize("with_state", [False, True])
 def test_causal_variant_vs_oracle(case, with_state):
     fm, nu, norm, update, B, H, N, D, M, dtype, scale = case
@@ -104,16 +121,20 @@ def test_variant_without_state_matches_zero_state():
     assert torch.equal(a, b)
 
 
-@pytest.mark.parametrize("fm,nu,norm,update", [("elu1", 1, "den", "sum"), ("dpfp", 2, "sum", "delta"),
-                                               ("poly2", 1, "none", "sum")])
-def test_state_only_and_split_carry(fm, nu, norm, update):
+@pytest.mark.parametrize("fm,nu,norm,update,D,M,dtype", [("elu1", 1, "den", "sum", 16, 32, torch.float32),
+                                                         ("dpfp", 2, "sum", "delta", 16, 32, torch.float32),
+                                                         ("poly2", 1, "none", "sum", 16, 32, torch.float32),
+                                                         ("dpfp", 1, "sum", "sum", 64, 64, torch.bfloat16),
+                                                         ("elu1", 1, "none", "sum", 64, 128, torch.bfloat16)])
+def test_state_only_and_split_carry(fm, nu, norm, update, D, M, dtype):
     """A state-only call (out = NULL) leaves the same state as a full call, and two
-    calls chained through the state equal one call over the whole sequence."""
-    B, H, N, D, M = 2, 2, 150, 16, 32
+    calls chained through the state equal one call over the whole sequence (the
+    bf16 cases run on the tensor-core kernel; their split is not chunk-aligned)."""
+    B, H, N = 2, 2, 450
     var = la.variant(fm, nu, norm, update)
     F = la.la_feature_dim(var, D)
-    q, k, v = [t.to(DEV) for t in inputs.qkv(B, H, N, D, M, torch.float32, 1.0, seed=41)]
-    beta = inputs.betas(B, H, N, torch.float32, seed=42).to(DEV) if update == "delta" else None
+    q, k, v = [t.to(DEV) for t in inputs.qkv(B, H, N, D, M, dtype, 0.25, seed=41)]
+    beta = inputs.betas(B, H, N, dtype, seed=42).to(DEV) if update == "delta" else None
 
     def state():
         return torch.zeros(B, H, F, M, device=DEV), (torch.zeros(B, H, F, device=DEV) if norm == "den" else None)
@@ -122,7 +143,7 @@ def test_state_only_and_split_carry(fm, nu, norm, update):
     whole = la.la_forward_causal_variant(q, k, v, var, beta=beta, S=Sw, z=zw)
     So, zo = state()
     la.la_forward_causal_variant(q, k, v, var, beta=beta, S=So, z=zo, want_out=False)
-    cut = 67
+    cut = 197
     Ss, zs = state()
     sl = lambda t, a, b: None if t is None else t[:, :, a:b].contiguous()
     first = la.la_forward_causal_variant(sl(q, 0, cut), sl(k, 0, cut), sl(v, 0, cut), var,
@@ -130,9 +151,10 @@ def test_state_only_and_split_carry(fm, nu, norm, update):
     second = la.la_forward_causal_variant(sl(q, cut, N), sl(k, cut, N), sl(v, cut, N), var,
                                           beta=sl(beta, cut, N), S=Ss, z=zs)
     torch.cuda.synchronize()
+    tol = 1e-4 if dtype == torch.float32 else 2e-2
     assert head_rel_err(So, Sw) <= 1e-6
-    assert row_rel_err(torch.cat([first, second], 2), whole) <= 1e-4
-    assert head_rel_err(Ss, Sw) <= 1e-4
+    assert row_rel_err(torch.cat([first, second], 2), whole) <= tol
+    assert head_rel_err(Ss, Sw) <= tol
 
 
 NC_CASES = [

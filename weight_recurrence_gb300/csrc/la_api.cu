@@ -361,6 +361,13 @@ la_status la_forward_causal_variant(const void *q, const void *k, const void *v,
     if (!work) return LA_OK;   // an empty sequence leaves the state as it is
     if (out != nullptr && (out == q || out == k || out == v || out == beta)) return LA_ERR_INVALID_ARG;
     Problem p{q, k, v, out, S, z, BH, s.N, s.D, s.M, s.dtype, 0, nullptr, 0, (cudaStream_t)stream};
+    if (tc_variant_route(s, var, p)) {
+        // bf16, sum update, no denominator, F in {64, 128}: the chunked
+        // tensor-core kernel with the feature map applied row by row on chip
+        const DeviceInfo *dev = device_info();
+        if (!dev) return LA_ERR_CUDA;
+        return from_cuda(tc_causal(p, *dev));
+    }
     return from_cuda(fw_causal(p, var.update == LA_UPDATE_DELTA ? beta : nullptr, var));
 }
 

@@ -36,6 +36,11 @@ struct Problem {
     const int *lens = nullptr;   // causal: per-batch sequence lengths (device, [B]) or null
     int H = 1;                   // heads per batch entry (to index lens)
     bool step_major = false;     // causal: q, k, v, out laid out [N][B*H][.] (decode steps)
+    // variants on the tensor-core causal kernel (D above is then the feature width F)
+    int feat = 0;                // 0: elu + 1; 1: elu + 1 sum-normalised; 2: DPFP (row feature maps)
+    int dr = 0, nu = 0;          // raw width of q, k rows and DPFP shifts (feat != 0)
+    bool sum_norm = false;       // DPFP: rows divided by their sums
+    bool no_den = false;         // output = numerator (no denominator)
 };
 
 // Backward-pass problem (sizes already validated).
@@ -89,6 +94,10 @@ size_t fw_noncausal_ws_bytes(const la_shape &s, const la_variant &v);
 // causal form (also one decode step with N = 1); beta [BH, N] for the delta rule
 cudaError_t fw_causal(const Problem &p, const void *beta, const la_variant &v);
 cudaError_t fw_noncausal(const Problem &p, const la_variant &v, const DeviceInfo &dev);
+
+// tensor-core route of a sum-update variant, if it has one: fills p.feat, dr,
+// nu, sum_norm, no_den and sets p.D to the feature width; false otherwise
+bool tc_variant_route(const la_shape &s, const la_variant &v, Problem &p);
 
 // Counts kernel launches made through the library (la_api.cu).
 void count_launches(int n);

@@ -165,12 +165,18 @@ struct CausalArgs {
     const int *lens;         // per-batch sequence lengths (device) or null: rows past them are ignored
     int H;                   // heads per batch entry
     long long o_rs, o_hs;    // output row and head strides (elements) for the direct stores
+    int feat;                // kFeatPhi (elu + 1 in place) or a row feature map of a variant
+    int dr, nu;              // raw width of Q, K rows and DPFP shifts (feat != kFeatPhi)
+    int sum_norm;            // DPFP: divide each feature row by its sum
+    int no_den;              // read-out without the denominator: out = num
 };
 
 // Named barrier of the O group's 128 threads.
 __device__ __forceinline__ void o_sync() { asm volatile("bar.sync 2, 128;" ::: "memory"); }
 
-template <int D, int M>
+// VAR: a variant's feature map and read-out (CausalArgs feat, no_den); the
+// plain instantiation compiles without that code.
+template <int D, int M, bool VAR>
 __global__ void __launch_bounds__(Cfg<D, M>::THREADS, 1)
 causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -276,11 +282,12 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 uint8_t *st = smem + s * C::STAGE;
                 const int t0 = (c_begin + it) * kC;
                 LA_TRACE_AT(0, it, 0);
-                mbar_arrive_expect_tx(&full[s], C::STAGE);
-#pragma unroll
-                for (int j = 0; j < D / 64; ++j) tma_load_3d(st + j * kC * 128, &tm_q, &full[s], j * 64, t0, bh);
-#pragma unroll
-                for (int j = 0; j < D / 64; ++j)
+                // DPFP rows arrive raw (at most 64 columns, one box each), the
+                // feature-map group expands them to the D feature columns
+                const int qk_boxes = VAR && args.feat == kFeatDpfp ? 1 : D / 64;
+                mbar_arrive_expect_tx(&full[s], 2 * qk_boxes * kC * 128 + C::TILE_V);
+                for (int j = 0; j < qk_boxes; ++j) tma_load_3d(st + j * kC * 128, &tm_q, &full[s], j * 64, t0, bh);
+                for (int j = 0; j < qk_boxes; ++j)
                     tma_load_3d(st + C::TILE_QK + j * kC * 128, &tm_k, &full[s], j * 64, t0, bh);
 #pragma unroll
                 for (int j = 0; j < M / 64; ++j)
@@ -543,7 +550,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     tmem_wait_ld();
                     den = __uint_as_float(dv[0]) + __uint_as_float(zv[0]);
                 }
-                const float inv = 1.f / den;
+                const float inv = VAR && args.no_den ? 1.f : 1.f / den;
                 uint4 *dst = !C::OUT_TMA && args.out && t < Nseq
                                  ? reinterpret_cast<uint4 *>(args.out + (size_t)bh * args.o_hs + (size_t)t * args.o_rs)
                                  : nullptr;
@@ -636,7 +643,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
 #pragma unroll
                 for (int j = 0; j < 32; j += 4)
                     *reinterpret_cast<float4 *>(S_h + d * M + 32 * h + j) = make_float4(sv[j], sv[j + 1], sv[j + 2], sv[j + 3]);
-                if (h == 0) z_h[d] = zr;
+                if (h == 0 && z_h) z_h[d] = zr;
             }
         } else {
             const bool srow = r < D;                 // owns a state row
@@ -718,7 +725,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     uint32_t zv[16];
                     tmem_ld16(tmem + lane_off + C::COL_Z, zv);
                     tmem_wait_ld();
-                    if (srow) z_h[r] = __uint_as_float(zv[0]);
+                    if (srow && z_h) z_h[r] = __uint_as_float(zv[0]);
                 }
             }
         }
@@ -733,8 +740,15 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             if (wait_bar(&full[s], (it / C::NS) & 1, abort)) {
                 if (t == 0) LA_TRACE_AT(3, it, 3 * grp + 1);
                 uint8_t *st = smem + s * C::STAGE;
-                if (grp == 0) phi_tile<D>(st, t, kC);
-                if (grp == C::NPHI - 1) phi_tile<D>(st + C::TILE_QK, t, min(kC, Nseq - (c_begin + it) * kC));
+                const int kz = min(kC, Nseq - (c_begin + it) * kC);
+                if (!VAR || args.feat == kFeatPhi) {
+                    if (grp == 0) phi_tile<D>(st, t, kC);
+                    if (grp == C::NPHI - 1) phi_tile<D>(st + C::TILE_QK, t, kz);
+                } else if constexpr (VAR) {   // a variant's feature map, one row per thread
+                    if (grp == 0) feature_row<D>(st, t, kC, args.feat, args.dr, args.nu, args.sum_norm);
+                    if (grp == C::NPHI - 1)
+                        feature_row<D>(st + C::TILE_QK, t, kz, args.feat, args.dr, args.nu, args.sum_norm);
+                }
                 if (t == 0) LA_TRACE_AT(3, it, 3 * grp + 2);
             }
             fence_proxy_async();
@@ -1315,11 +1329,15 @@ template <int D, int M>
 cudaError_t launch_causal(const Problem &p, const DeviceInfo &dev) {
     using C = Cfg<D, M>;
     CUtensorMap tq, tk, tv;
-    if (!causal_tmap(&tq, p, p.q, D) || !causal_tmap(&tk, p, p.k, D) || !causal_tmap(&tv, p, p.v, M))
+    // Q, K of a variant with a row feature map arrive raw (dr columns)
+    const int qk_cols = p.feat != kFeatPhi ? p.dr : D;
+    if (!causal_tmap(&tq, p, p.q, qk_cols) || !causal_tmap(&tk, p, p.k, qk_cols) || !causal_tmap(&tv, p, p.v, M))
         return cudaErrorInvalidValue;
     const int nch = (p.N + kC - 1) / kC;
-    // per-sequence lengths or step-major decode inputs: no segments
-    int nseg = (p.lens || p.step_major) ? 1 : causal_nseg(p.BH, p.N, dev.sm_count);
+    // per-sequence lengths, step-major decode inputs or a variant (the
+    // segment-sum pre-pass applies elu + 1 and variant calls pass no
+    // workspace): no segments
+    int nseg = (p.lens || p.step_major || p.feat != kFeatPhi || p.no_den) ? 1 : causal_nseg(p.BH, p.N, dev.sm_count);
     const int cps = (nch + nseg - 1) / nseg;
     nseg = (nch + cps - 1) / cps;
     cudaError_t e;
@@ -1348,8 +1366,18 @@ cudaError_t launch_causal(const Problem &p, const DeviceInfo &dev) {
     a.H = p.H > 0 ? p.H : 1;
     a.o_rs = p.step_major ? p.BH * (long long)M : (long long)M;
     a.o_hs = p.step_major ? (long long)M : (long long)p.N * M;
-    if ((e = set_smem(causal_tc_kernel<D, M>, C::SMEM)) != cudaSuccess) return e;
-    causal_tc_kernel<D, M><<<(unsigned)(p.BH * nseg), C::THREADS, C::SMEM, p.stream>>>(tq, tk, tv, to, a);
+    a.feat = p.feat;
+    a.dr = p.dr;
+    a.nu = p.nu;
+    a.sum_norm = p.sum_norm ? 1 : 0;
+    a.no_den = p.no_den ? 1 : 0;
+    if (p.feat != kFeatPhi || p.no_den) {
+        if ((e = set_smem(causal_tc_kernel<D, M, true>, C::SMEM)) != cudaSuccess) return e;
+        causal_tc_kernel<D, M, true><<<(unsigned)(p.BH * nseg), C::THREADS, C::SMEM, p.stream>>>(tq, tk, tv, to, a);
+    } else {
+        if ((e = set_smem(causal_tc_kernel<D, M, false>, C::SMEM)) != cudaSuccess) return e;
+        causal_tc_kernel<D, M, false><<<(unsigned)(p.BH * nseg), C::THREADS, C::SMEM, p.stream>>>(tq, tk, tv, to, a);
+    }
     count_launches(1);
     return cudaGetLastError();
 }
@@ -1401,6 +1429,31 @@ bool tc_dims(const la_shape &s) {
 }  // namespace
 
 bool tc_causal_supported(const la_shape &s, int chunk) { return tc_dims(s) && (chunk == 0 || chunk == 128); }
+
+bool tc_variant_route(const la_shape &s, const la_variant &v, Problem &p) {
+    // sum update without the denominator, bf16, feature width 64 or 128
+    if (s.dtype != LA_DTYPE_BF16 || v.update != LA_UPDATE_SUM || v.norm == LA_NORM_DEN) return false;
+    if (s.M != 64 && s.M != 128) return false;
+    const int F = fw_feature_dim(v, s.D);
+    if (F != 64 && F != 128) return false;
+    if (v.feature_map == LA_FM_ELU1) {
+        p.feat = v.norm == LA_NORM_SUM ? kFeatElu1Sum : kFeatPhi;
+    } else if (v.feature_map == LA_FM_DPFP) {
+        // the raw widths and shifts feature_row instantiates
+        const bool ok = F == 128 ? ((s.D == 64 && v.nu == 1) || (s.D == 32 && v.nu == 2) || (s.D == 16 && v.nu == 4))
+                                 : ((s.D == 32 && v.nu == 1) || (s.D == 16 && v.nu == 2));
+        if (!ok) return false;
+        p.feat = kFeatDpfp;
+        p.sum_norm = v.norm == LA_NORM_SUM;
+    } else {
+        return false;
+    }
+    p.dr = s.D;
+    p.nu = v.nu;
+    p.no_den = true;
+    p.D = F;
+    return true;
+}
 
 size_t tc_causal_ws_bytes(const la_shape &s, int) {
     // Sized for the most segments any device picks (one CTA per SM, up to

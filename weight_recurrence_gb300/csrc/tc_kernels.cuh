@@ -95,6 +95,132 @@ __device__ __forceinline__ void phi_tile(uint8_t *tile, int t, int zero_from) {
     }
 }
 
+// ------------------------------------------------- feature maps of the variants
+// Feature maps computed row by row in place: thread t owns row t of a C x F
+// tile (F/64 sub-tiles of C rows x 128 bytes, 128-byte swizzle).  The raw row
+// (DR columns) sits in the first DR columns of the tile as TMA left it; the
+// features overwrite the whole row, rounded once to bf16.  Rows >= zero_from
+// are written as zeros (keys past the end of a sequence).
+//   kFeatElu1Sum: elu(x) + 1, divided by its component sum (DR = F).
+//   kFeatDpfp:    DPFP-NU ("Linear Transformers Are Secretly Fast Weight
+//                 Programmers"): r = [relu(x), relu(-x)], feature
+//                 (s-1)*2DR + i = r_i r_{(i+s) mod 2DR}, F = 2 DR NU; divided by
+//                 the component sum if SUM.
+constexpr int kFeatPhi = 0, kFeatElu1Sum = 1, kFeatDpfp = 2;
+
+template <int DR>
+__device__ __forceinline__ void load_raw_row(const uint8_t *tile, int r, uint32_t (&w)[DR / 2]) {
+#pragma unroll
+    for (int c8 = 0; c8 < DR / 8; ++c8) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(tile + (c8 / 8) * kC * 128 + sw128_offset(r, (c8 % 8) * 8));
+        w[4 * c8] = v.x;
+        w[4 * c8 + 1] = v.y;
+        w[4 * c8 + 2] = v.z;
+        w[4 * c8 + 3] = v.w;
+    }
+}
+
+template <int DR>
+__device__ __forceinline__ float raw_at(const uint32_t (&w)[DR / 2], int i) {
+    return (i & 1) ? bf16hi(w[i >> 1]) : bf16lo(w[i >> 1]);
+}
+
+// r_i of DPFP from the packed raw row (i a compile-time index after unrolling)
+template <int DR>
+__device__ __forceinline__ float dpfp_r(const uint32_t (&w)[DR / 2], int i) {
+    return i < DR ? fmaxf(raw_at<DR>(w, i), 0.f) : fmaxf(-raw_at<DR>(w, i - DR), 0.f);
+}
+
+template <int DR, int NU>
+__device__ __forceinline__ float dpfp_feature(const uint32_t (&w)[DR / 2], int f) {
+    const int s = f / (2 * DR) + 1, i = f % (2 * DR);
+    return dpfp_r<DR>(w, i) * dpfp_r<DR>(w, (i + s) % (2 * DR));
+}
+
+template <int F, int DR, int NU, bool SUM>
+__device__ __forceinline__ void dpfp_row(uint8_t *tile, int r, bool zero) {
+    static_assert(F == 2 * DR * NU && DR <= 64, "DPFP width");
+    uint32_t w[DR / 2];
+    load_raw_row<DR>(tile, r, w);
+    float scale = 1.f;
+    if (SUM) {
+        float s = 0.f;
+#pragma unroll
+        for (int f = 0; f < F; ++f) s += dpfp_feature<DR, NU>(w, f);
+        scale = s > 0.f ? 1.f / s : 0.f;
+        // recompute the features below instead of keeping all F of them live
+#pragma unroll
+        for (int j = 0; j < DR / 2; ++j) asm volatile("" : "+r"(w[j]));
+    }
+#pragma unroll
+    for (int c8 = 0; c8 < F / 8; ++c8) {
+        const int c = 8 * c8;
+        uint4 o = make_uint4(0u, 0u, 0u, 0u);
+        if (!zero) {
+            o.x = pack_bf16x2(dpfp_feature<DR, NU>(w, c) * scale, dpfp_feature<DR, NU>(w, c + 1) * scale);
+            o.y = pack_bf16x2(dpfp_feature<DR, NU>(w, c + 2) * scale, dpfp_feature<DR, NU>(w, c + 3) * scale);
+            o.z = pack_bf16x2(dpfp_feature<DR, NU>(w, c + 4) * scale, dpfp_feature<DR, NU>(w, c + 5) * scale);
+            o.w = pack_bf16x2(dpfp_feature<DR, NU>(w, c + 6) * scale, dpfp_feature<DR, NU>(w, c + 7) * scale);
+        }
+        *reinterpret_cast<uint4 *>(tile + (c / 64) * kC * 128 + sw128_offset(r, c % 64)) = o;
+    }
+}
+
+// Elementwise, so each 8-column chunk is read, mapped and written back in
+// place; the row sum needs a first pass over the same chunks.
+template <int F>
+__device__ __forceinline__ void elu1_sum_row(uint8_t *tile, int r, bool zero) {
+    auto at = [&](int c) { return tile + (c / 64) * kC * 128 + sw128_offset(r, c % 64); };
+    auto phi8 = [&](const uint4 &w, float (&v)[8]) {
+        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float a = bf16lo(u[j]), b = bf16hi(u[j]);
+            v[2 * j] = a > 0.f ? a + 1.f : __expf(a);
+            v[2 * j + 1] = b > 0.f ? b + 1.f : __expf(b);
+        }
+    };
+    float s = 0.f;
+#pragma unroll 4
+    for (int c = 0; c < F; c += 8) {
+        float v[8];
+        phi8(*reinterpret_cast<const uint4 *>(at(c)), v);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) s += v[j];
+    }
+    const float scale = 1.f / s;
+    asm volatile("" ::: "memory");   // read the chunks again rather than keep them live
+#pragma unroll 4
+    for (int c = 0; c < F; c += 8) {
+        float v[8];
+        phi8(*reinterpret_cast<const uint4 *>(at(c)), v);
+        uint4 o = make_uint4(0u, 0u, 0u, 0u);
+        if (!zero)
+            o = make_uint4(pack_bf16x2(v[0] * scale, v[1] * scale), pack_bf16x2(v[2] * scale, v[3] * scale),
+                           pack_bf16x2(v[4] * scale, v[5] * scale), pack_bf16x2(v[6] * scale, v[7] * scale));
+        *reinterpret_cast<uint4 *>(at(c)) = o;
+    }
+}
+
+// Applies feature map `feat` (kFeatElu1Sum or kFeatDpfp with raw width dr,
+// nu shifts, sum normalisation if sum) to row t of an F-wide tile.
+template <int F>
+__device__ __forceinline__ void feature_row(uint8_t *tile, int t, int zero_from, int feat, int dr, int nu, bool sum) {
+    const bool zero = t >= zero_from;
+    if (feat == kFeatElu1Sum) {
+        elu1_sum_row<F>(tile, t, zero);
+        return;
+    }
+    if constexpr (F == 128) {
+        if (dr == 64 && nu == 1) sum ? dpfp_row<F, 64, 1, true>(tile, t, zero) : dpfp_row<F, 64, 1, false>(tile, t, zero);
+        else if (dr == 32 && nu == 2) sum ? dpfp_row<F, 32, 2, true>(tile, t, zero) : dpfp_row<F, 32, 2, false>(tile, t, zero);
+        else if (dr == 16 && nu == 4) sum ? dpfp_row<F, 16, 4, true>(tile, t, zero) : dpfp_row<F, 16, 4, false>(tile, t, zero);
+    } else if constexpr (F == 64) {
+        if (dr == 32 && nu == 1) sum ? dpfp_row<F, 32, 1, true>(tile, t, zero) : dpfp_row<F, 32, 1, false>(tile, t, zero);
+        else if (dr == 16 && nu == 2) sum ? dpfp_row<F, 16, 2, true>(tile, t, zero) : dpfp_row<F, 16, 2, false>(tile, t, zero);
+    }
+}
+
 // Writes columns [c0, c0+32) of row r of a D x M fp32 state as bf16 into the
 // MN-major swizzled snapshot [D rows x M cols] (sub-tiles of 64 columns).
 template <int D>
