@@ -131,11 +131,25 @@ class ClockSampler:
 
 # ---------------------------------------------------------------- helpers
 
-def _kernel_source_hash():
-    import glob
+# Source files each captured kernel is built from: a capture's traffic figure
+# stands only while these hash to what they were when it was taken.
+TC_SOURCES = ("la_tc.cu", "tc_kernels.cuh", "tc_ptx.cuh", "tc_host.h", "la_common.cuh")
+KERNEL_SOURCES = {
+    "causal_causal_b16h8n3072d64": TC_SOURCES,
+    "causal_causal_b1h16n65536d128": TC_SOURCES,
+    "noncausal_noncausal_b8h8n4096d64": TC_SOURCES,
+    "causal_variant_dpfp_b16h8n3072d64": TC_SOURCES,
+    "decode_decode_b256h16d64": ("la_simt.cu", "la_common.cuh"),
+    "causal_variant_delta_b16h8n3072d64": ("la_fw.cu", "la_common.cuh"),
+    "backward_causal_b16h8n3072d64": ("la_tc_bwd.cu", "tc_kernels.cuh", "tc_ptx.cuh", "tc_host.h", "la_common.cuh"),
+}
+
+
+def _kernel_source_hash(kernel_key):
+    """sha256 (first 16 hex digits) of the kernel's source files, in the listed order."""
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "weight_recurrence_gb300", "csrc", "*"))):
-        with open(p, "rb") as f:
+    for name in KERNEL_SOURCES.get(kernel_key, ()):
+        with open(os.path.join(ROOT, "weight_recurrence_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
@@ -146,7 +160,7 @@ def _traffic(kernel_key):
         with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
             t = json.load(f)
         e = t.get(kernel_key)
-        if e and e.get("source_sha") == _kernel_source_hash():
+        if e and kernel_key in KERNEL_SOURCES and e.get("source_sha") == _kernel_source_hash(kernel_key):
             return e.get("dram_bytes_per_launch")
     except (OSError, ValueError):
         pass

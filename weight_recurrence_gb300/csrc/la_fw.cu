@@ -63,6 +63,24 @@ __device__ __forceinline__ float feature_at(const float *x, int f, int fm, int D
     return x[a] * x[b];
 }
 
+// feature_at on a raw row of dtype T (values converted as read).
+template <typename T>
+__device__ __forceinline__ float feature_raw(const T *x, int f, int fm, int D, int nu, int F) {
+    if (f >= F) return 0.f;
+    if (fm == LA_FM_ELU1) return phi_accurate(to_f32(x[f]));
+    if (fm == LA_FM_DPFP) {
+        const int twoD = 2 * D;
+        const int s = f / twoD + 1, i = f - (s - 1) * twoD;
+        int j = i + s;
+        if (j >= twoD) j -= twoD;                // s <= nu < 2D
+        const float a = i < D ? fmaxf(to_f32(x[i]), 0.f) : fmaxf(-to_f32(x[i - D]), 0.f);
+        const float b = j < D ? fmaxf(to_f32(x[j]), 0.f) : fmaxf(-to_f32(x[j - D]), 0.f);
+        return a * b;
+    }
+    const int a = f / D, b = f - a * D;          // degree-2 polynomial: x_a x_b
+    return to_f32(x[a]) * to_f32(x[b]);
+}
+
 __device__ __forceinline__ float half_warp_sum(float x) {
 #pragma unroll
     for (int o = kFwG / 2; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
@@ -120,22 +138,48 @@ __device__ void chunk_features(const FwArgs &a, long long h, int t0, int rows, f
     }
 }
 
+// 16-byte asynchronous copy global -> shared; src_bytes < 16 zero-fills the
+// rest (0: nothing is read, the source address is then only a placeholder).
+__device__ __forceinline__ void cp_async16(void *dst, const void *src, int src_bytes) {
+    const uint32_t d = (uint32_t)__cvta_generic_to_shared(dst);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(d), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+// Raw inputs of one chunk as they are in memory (dtype T): q, k rows [L][D],
+// the CTA's 16 value columns [L][16], beta [L].
+template <typename T>
+struct RawChunk {
+    T *q, *k, *v;
+    float *b;
+};
+
 // Causal form of every variant, one CTA per (head, 16 state columns).
 // Lane layout: warp w, lane = c * 16 + g owns column m0 + 2 w + c and the
 // entries f = g + 16 e (e < E) of that column.
+// Per chunk: the raw rows of the next chunk are copied asynchronously into the
+// other raw buffer while this chunk's tokens run; the features of a chunk are
+// evaluated from its raw buffer into fq, fk [L][Fp].
 template <typename T, int E, bool DELTA, bool DEN>
 __global__ void __launch_bounds__(kFwThreads)
 fw_causal_kernel(FwArgs a)
 {
-    extern __shared__ float sm[];
-    float *xq = sm;                           // [L][D] raw rows
-    float *xk = xq + kFwL * a.D;              // [L][D]
-    float *fq = xk + kFwL * a.D;              // [L][Fp] features
+    extern __shared__ __align__(16) float sm[];
+    const int rawqk = kFwL * a.D * (int)sizeof(T);            // bytes of one raw q or k chunk
+    const int rawv = kFwL * kFwCols * (int)sizeof(T);
+    const int rawb = kFwL * 4;
+    const int rawsz = 2 * rawqk + rawv + rawb;                 // multiple of 16
+    uint8_t *rawbase = reinterpret_cast<uint8_t *>(sm);
+    auto raw = [&](int buf) {
+        uint8_t *p = rawbase + buf * rawsz;
+        return RawChunk<T>{reinterpret_cast<T *>(p), reinterpret_cast<T *>(p + rawqk),
+                           reinterpret_cast<T *>(p + 2 * rawqk), reinterpret_cast<float *>(p + 2 * rawqk + rawv)};
+    };
+    float *fq = reinterpret_cast<float *>(rawbase + 2 * rawsz);   // [L][Fp] features
     float *fk = fq + kFwL * a.Fp;             // [L][Fp]
-    float *vs = fk + kFwL * a.Fp;             // [L][16] this CTA's value columns
-    float *ys = vs + kFwL * kFwCols;          // [L][16] outputs of the chunk
-    float *bs = ys + kFwL * kFwCols;          // [L] beta
-    float *den = bs + kFwL;                   // [L]
+    float *ys = fk + kFwL * a.Fp;             // [L][16] outputs of the chunk
+    float *den = ys + kFwL * kFwCols;         // [L]
     float *dpart = den + kFwL;                // [warps][L]
     float *zs = dpart + kFwWarps * kFwL;      // [Fp] running z (DEN)
 
@@ -145,7 +189,44 @@ fw_causal_kernel(FwArgs a)
     const int c = lane >> 4, g = lane & 15;
     const int mc = warp * 2 + c;              // column within the CTA's 16
 
-    // carried-in state, staged through shared memory for coalesced loads
+    const T *qh = (const T *)a.q + h * a.N * a.D, *kh = (const T *)a.k + h * a.N * a.D;
+    const T *vh = (const T *)a.v + h * a.N * a.M;
+    const T *bh = DELTA ? (const T *)a.beta + h * a.N : nullptr;
+    T *oh = a.out ? (T *)a.out + h * a.N * a.M : nullptr;
+    const bool want_q = oh != nullptr;
+
+    // copies of chunk t0's raw rows into buffer `buf` (one commit group);
+    // beta (whose rows need not be 16-byte aligned) is loaded into a register
+    // by the first 32 threads and stored after the current chunk's tokens
+    auto issue = [&](int buf, int t0, float &bnext) {
+        const int rows = min(kFwL, a.N - t0);
+        RawChunk<T> r = raw(buf);
+        const int rowb = a.D * (int)sizeof(T);                 // multiple of 32 bytes
+        for (int vi = tid; vi < rawqk / 16; vi += kFwThreads) {
+            const int row = vi * 16 / rowb;
+            const bool ok = row < rows;
+            const size_t off = (size_t)t0 * rowb + (size_t)vi * 16;
+            cp_async16(reinterpret_cast<uint8_t *>(r.k) + vi * 16,
+                       ok ? reinterpret_cast<const uint8_t *>(kh) + off : reinterpret_cast<const uint8_t *>(kh),
+                       ok ? 16 : 0);
+            if (want_q)
+                cp_async16(reinterpret_cast<uint8_t *>(r.q) + vi * 16,
+                           ok ? reinterpret_cast<const uint8_t *>(qh) + off : reinterpret_cast<const uint8_t *>(qh),
+                           ok ? 16 : 0);
+        }
+        constexpr int vpr = kFwCols * (int)sizeof(T) / 16;     // 16-byte pieces per value row
+        for (int vi = tid; vi < kFwL * vpr; vi += kFwThreads) {
+            const int row = vi / vpr, part = vi - row * vpr;
+            const bool ok = row < rows;
+            const T *src = ok ? vh + (size_t)(t0 + row) * a.M + m0 : vh;
+            cp_async16(reinterpret_cast<uint8_t *>(r.v) + vi * 16, reinterpret_cast<const uint8_t *>(src) + (ok ? part * 16 : 0),
+                       ok ? 16 : 0);
+        }
+        cp_async_commit();
+        if (DELTA && tid < kFwL) bnext = tid < rows ? to_f32(bh[t0 + tid]) : 0.f;
+    };
+
+    // carried-in state, staged through shared memory (the fk buffer) for coalesced loads
     float s[E];
     {
         float *stage = fk;                    // [Fp][16], fits in [L][Fp]
@@ -158,22 +239,45 @@ fw_causal_kernel(FwArgs a)
         __syncthreads();
 #pragma unroll
         for (int e = 0; e < E; ++e) s[e] = stage[(g + kFwG * e) * kFwCols + mc];
-        __syncthreads();
     }
 
-    const T *vh = (const T *)a.v + h * a.N * a.M;
-    const T *bh = DELTA ? (const T *)a.beta + h * a.N : nullptr;
-    T *oh = a.out ? (T *)a.out + h * a.N * a.M : nullptr;
-    const bool want_q = oh != nullptr;
-
-    for (int t0 = 0; t0 < a.N; t0 += kFwL) {
+    float bnext = 0.f;
+    if (a.N > 0) issue(0, 0, bnext);
+    if (DELTA && tid < kFwL) raw(0).b[tid] = bnext;
+    int buf = 0;
+    for (int t0 = 0; t0 < a.N; t0 += kFwL, buf ^= 1) {
         const int rows = min(kFwL, a.N - t0);
-        for (int idx = tid; idx < kFwL * kFwCols; idx += kFwThreads) {
-            const int t = idx / kFwCols, cc = idx - t * kFwCols;
-            vs[idx] = t < rows ? to_f32(vh[(long long)(t0 + t) * a.M + m0 + cc]) : 0.f;
+        const RawChunk<T> r = raw(buf);
+        cp_async_wait_all();
+        __syncthreads();                      // chunk t0's raw rows (and beta) are in shared memory
+        // features of the chunk (rows past `rows` are zero)
+        for (int idx = tid; idx < kFwL * a.Fp; idx += kFwThreads) {
+            const int t = idx / a.Fp, f = idx - t * a.Fp;
+            const bool ok = t < rows;
+            float vk = 0.f, vq = 0.f;
+            if (ok) {
+                vk = feature_raw<T>(r.k + t * a.D, f, a.fm, a.D, a.nu, a.F);
+                if (want_q) vq = feature_raw<T>(r.q + t * a.D, f, a.fm, a.D, a.nu, a.F);
+            }
+            fk[idx] = vk;
+            if (want_q) fq[idx] = vq;
         }
-        if (DELTA && tid < kFwL) bs[tid] = tid < rows ? to_f32(bh[t0 + tid]) : 0.f;
-        chunk_features<T>(a, h, t0, rows, xq, xk, fq, fk, want_q);   // ends with a barrier
+        __syncthreads();
+        if (a.norm == LA_NORM_SUM) {
+            for (int rr = warp; rr < 2 * kFwL; rr += kFwWarps) {
+                if (rr >= kFwL && !want_q) continue;
+                float *row = (rr < kFwL ? fk : fq) + (rr % kFwL) * a.Fp;
+                float sum = 0.f;
+                for (int f = lane; f < a.Fp; f += 32) sum += row[f];
+                sum = warp_sum(sum);
+                if (sum > 0.f)
+                    for (int f = lane; f < a.Fp; f += 32) row[f] = row[f] / sum;
+            }
+            __syncthreads();
+        }
+        // the next chunk's raw rows stream in while this chunk's tokens run (its
+        // buffer was last read by the previous chunk's tokens, before the barriers above)
+        if (t0 + kFwL < a.N) issue(buf ^ 1, t0 + kFwL, bnext);
 
         if (DEN && want_q) {
             // den_t = phi(q_t) . (z_prev + sum_{s <= t} phi(k_s)): warp w owns the
@@ -208,30 +312,61 @@ fw_causal_kernel(FwArgs a)
         }
 
         // the recurrence over the chunk's tokens, each warp on its own columns
-        for (int t = 0; t < rows; ++t) {
-            const float *fkt = fk + t * a.Fp + g, *fqt = fq + t * a.Fp + g;
-            const float vt = vs[t * kFwCols + mc];
-            float kr[E];
+        if (DELTA) {
+            // the read-out of token t-1 and the retrieval of token t both read the
+            // state after token t-1, so their half-warp reductions run together
+            for (int t = 0; t <= rows; ++t) {
+                const bool has_k = t < rows, has_y = want_q && t > 0;   // warp-uniform
+                float kr[E];
+                float r0 = 0.f, r1 = 0.f, y0 = 0.f, y1 = 0.f;
+                if (has_k) {
+                    const float *fkt = fk + t * a.Fp + g;
 #pragma unroll
-            for (int e = 0; e < E; ++e) kr[e] = fkt[kFwG * e];
-            if (DELTA) {
-                float r = 0.f;                            // retrieval S^T phi(k), this column
+                    for (int e = 0; e < E; ++e) kr[e] = fkt[kFwG * e];
 #pragma unroll
-                for (int e = 0; e < E; ++e) r = fmaf(kr[e], s[e], r);
-                r = half_warp_sum(r);
-                const float u = bs[t] * (vt - r);
+                    for (int e = 0; e < E; e += 2) {
+                        r0 = fmaf(kr[e], s[e], r0);
+                        if (e + 1 < E) r1 = fmaf(kr[e + 1], s[e + 1], r1);
+                    }
+                }
+                if (has_y) {
+                    const float *fqt = fq + (t - 1) * a.Fp + g;
 #pragma unroll
-                for (int e = 0; e < E; ++e) s[e] = fmaf(kr[e], u, s[e]);
-            } else {
+                    for (int e = 0; e < E; e += 2) {
+                        y0 = fmaf(fqt[kFwG * e], s[e], y0);
+                        if (e + 1 < E) y1 = fmaf(fqt[kFwG * (e + 1)], s[e + 1], y1);
+                    }
+                }
+                float rr = r0 + r1, y = y0 + y1;
 #pragma unroll
-                for (int e = 0; e < E; ++e) s[e] = fmaf(kr[e], vt, s[e]);
+                for (int o = kFwG / 2; o > 0; o >>= 1) {
+                    rr += __shfl_xor_sync(0xffffffffu, rr, o);
+                    y += __shfl_xor_sync(0xffffffffu, y, o);
+                }
+                if (has_y && g == 0) ys[(t - 1) * kFwCols + mc] = y;
+                if (has_k) {
+                    const float u = r.b[t] * (to_f32(r.v[t * kFwCols + mc]) - rr);
+#pragma unroll
+                    for (int e = 0; e < E; ++e) s[e] = fmaf(kr[e], u, s[e]);
+                }
             }
-            if (want_q) {
-                float y = 0.f;                            // read-out S^T phi(q), after the update
+        } else {
+#pragma unroll 2
+            for (int t = 0; t < rows; ++t) {
+                const float *fkt = fk + t * a.Fp + g, *fqt = fq + t * a.Fp + g;
+                const float vt = to_f32(r.v[t * kFwCols + mc]);
 #pragma unroll
-                for (int e = 0; e < E; ++e) y = fmaf(fqt[kFwG * e], s[e], y);
-                y = half_warp_sum(y);
-                if (g == 0) ys[t * kFwCols + mc] = DEN ? y / den[t] : y;
+                for (int e = 0; e < E; ++e) s[e] = fmaf(fkt[kFwG * e], vt, s[e]);
+                if (want_q) {
+                    float y0 = 0.f, y1 = 0.f;            // read-out S^T phi(q), after the update
+#pragma unroll
+                    for (int e = 0; e < E; e += 2) {
+                        y0 = fmaf(fqt[kFwG * e], s[e], y0);
+                        if (e + 1 < E) y1 = fmaf(fqt[kFwG * (e + 1)], s[e + 1], y1);
+                    }
+                    const float y = half_warp_sum(y0 + y1);
+                    if (g == 0) ys[t * kFwCols + mc] = DEN ? y / den[t] : y;
+                }
             }
         }
         __syncthreads();
@@ -240,8 +375,8 @@ fw_causal_kernel(FwArgs a)
                 const int t = idx / kFwCols, cc = idx - t * kFwCols;
                 oh[(long long)(t0 + t) * a.M + m0 + cc] = from_f32<T>(ys[idx]);
             }
-        // the next chunk overwrites vs, bs, xq, xk, fq, fk only after the
-        // barrier inside chunk_features; ys is rewritten after two barriers
+        if (DELTA && tid < kFwL && t0 + kFwL < a.N) raw(buf ^ 1).b[tid] = bnext;
+        // the next iteration's first barrier orders these stores before any reuse
     }
 
     if (a.S) {
@@ -376,14 +511,15 @@ int entries_for(int F) {
     return 0;
 }
 
+template <typename T>
 size_t causal_smem(int D, int Fp) {
-    return sizeof(float) * ((size_t)2 * kFwL * D + (size_t)2 * kFwL * Fp + 2 * kFwL * kFwCols + 2 * kFwL +
-                            kFwWarps * kFwL + Fp);
+    const size_t raw = (size_t)2 * kFwL * D * sizeof(T) + (size_t)kFwL * kFwCols * sizeof(T) + kFwL * 4;
+    return 2 * raw + sizeof(float) * ((size_t)2 * kFwL * Fp + kFwL * kFwCols + kFwL + kFwWarps * kFwL + Fp);
 }
 
 template <typename T, int E, bool DELTA, bool DEN>
 cudaError_t launch_causal_e(const FwArgs &a, long long BH, cudaStream_t st) {
-    const size_t smem = causal_smem(a.D, a.Fp);
+    const size_t smem = causal_smem<T>(a.D, a.Fp);
     cudaError_t e = cudaFuncSetAttribute(fw_causal_kernel<T, E, DELTA, DEN>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
