@@ -97,8 +97,9 @@ struct FwArgs {
     const void *q, *k, *v, *beta;
     void *out;               // may be null (state only)
     float *S, *z;            // [BH, F, M], [BH, F] or null
-    int N, D, M, F, Fp;
+    int N, D, M, F, Fp;      // Fp: padded feature width of the kernel's layout
     int fm, nu, norm;
+    int cpc;                 // causal kernel: state columns per CTA
 };
 
 // Loads `rows` raw rows of q and k (and of v's 16-column slice) for the chunk
@@ -155,19 +156,26 @@ struct RawChunk {
     float *b;
 };
 
-// Causal form of every variant, one CTA per (head, 16 state columns).
-// Lane layout: warp w, lane = c * 16 + g owns column m0 + 2 w + c and the
-// entries f = g + 16 e (e < E) of that column.
+// Causal form of every variant.  A warp owns CW = 32 / G state columns, G
+// lanes per column; lane = cl * G + g owns column warp * CW + cl of the CTA's
+// block and the column entries f = 4 (e4 G + g) + j (e4 < E / 4, j < 4), so a
+// lane's features come in float4 loads and the G lanes of a column read one
+// contiguous span (no bank conflicts; the other columns of the warp read the
+// same addresses).  A CTA holds a.cpc columns (one warp per CW of them) and
+// evaluates its head's features once per chunk.
 // Per chunk: the raw rows of the next chunk are copied asynchronously into the
-// other raw buffer while this chunk's tokens run; the features of a chunk are
-// evaluated from its raw buffer into fq, fk [L][Fp].
-template <typename T, int E, bool DELTA, bool DEN>
+// other raw buffer while this chunk's tokens run.
+template <typename T, int G, int E, bool DELTA, bool DEN>
 __global__ void __launch_bounds__(kFwThreads)
 fw_causal_kernel(FwArgs a)
 {
+    static_assert(E % 4 == 0 && 32 % G == 0, "lane layout");
+    constexpr int CW = 32 / G;
     extern __shared__ __align__(16) float sm[];
+    const int nthr = blockDim.x, nwarps = nthr >> 5;
+    const int cpc = a.cpc;                                     // columns of this CTA
     const int rawqk = kFwL * a.D * (int)sizeof(T);            // bytes of one raw q or k chunk
-    const int rawv = kFwL * kFwCols * (int)sizeof(T);
+    const int rawv = kFwL * cpc * (int)sizeof(T);
     const int rawb = kFwL * 4;
     const int rawsz = 2 * rawqk + rawv + rawb;                 // multiple of 16
     uint8_t *rawbase = reinterpret_cast<uint8_t *>(sm);
@@ -178,16 +186,16 @@ fw_causal_kernel(FwArgs a)
     };
     float *fq = reinterpret_cast<float *>(rawbase + 2 * rawsz);   // [L][Fp] features
     float *fk = fq + kFwL * a.Fp;             // [L][Fp]
-    float *ys = fk + kFwL * a.Fp;             // [L][16] outputs of the chunk
-    float *den = ys + kFwL * kFwCols;         // [L]
-    float *dpart = den + kFwL;                // [warps][L]
+    float *ys = fk + kFwL * a.Fp;             // [L][cpc] outputs of the chunk
+    float *den = ys + kFwL * cpc;             // [L]
+    float *dpart = den + kFwL;                // [8 warps][L]
     float *zs = dpart + kFwWarps * kFwL;      // [Fp] running z (DEN)
 
     const long long h = blockIdx.x;
-    const int m0 = blockIdx.y * kFwCols;
+    const int m0 = blockIdx.y * cpc;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int c = lane >> 4, g = lane & 15;
-    const int mc = warp * 2 + c;              // column within the CTA's 16
+    const int cl = lane / G, g = lane % G;
+    const int mc = warp * CW + cl;            // column within the CTA's block
 
     const T *qh = (const T *)a.q + h * a.N * a.D, *kh = (const T *)a.k + h * a.N * a.D;
     const T *vh = (const T *)a.v + h * a.N * a.M;
@@ -202,7 +210,7 @@ fw_causal_kernel(FwArgs a)
         const int rows = min(kFwL, a.N - t0);
         RawChunk<T> r = raw(buf);
         const int rowb = a.D * (int)sizeof(T);                 // multiple of 32 bytes
-        for (int vi = tid; vi < rawqk / 16; vi += kFwThreads) {
+        for (int vi = tid; vi < rawqk / 16; vi += nthr) {
             const int row = vi * 16 / rowb;
             const bool ok = row < rows;
             const size_t off = (size_t)t0 * rowb + (size_t)vi * 16;
@@ -214,31 +222,32 @@ fw_causal_kernel(FwArgs a)
                            ok ? reinterpret_cast<const uint8_t *>(qh) + off : reinterpret_cast<const uint8_t *>(qh),
                            ok ? 16 : 0);
         }
-        constexpr int vpr = kFwCols * (int)sizeof(T) / 16;     // 16-byte pieces per value row
-        for (int vi = tid; vi < kFwL * vpr; vi += kFwThreads) {
+        const int vpr = cpc * (int)sizeof(T) / 16;             // 16-byte pieces per value row
+        for (int vi = tid; vi < kFwL * vpr; vi += nthr) {
             const int row = vi / vpr, part = vi - row * vpr;
             const bool ok = row < rows;
             const T *src = ok ? vh + (size_t)(t0 + row) * a.M + m0 : vh;
-            cp_async16(reinterpret_cast<uint8_t *>(r.v) + vi * 16, reinterpret_cast<const uint8_t *>(src) + (ok ? part * 16 : 0),
-                       ok ? 16 : 0);
+            cp_async16(reinterpret_cast<uint8_t *>(r.v) + vi * 16,
+                       reinterpret_cast<const uint8_t *>(src) + (ok ? part * 16 : 0), ok ? 16 : 0);
         }
         cp_async_commit();
         if (DELTA && tid < kFwL) bnext = tid < rows ? to_f32(bh[t0 + tid]) : 0.f;
     };
 
-    // carried-in state, staged through shared memory (the fk buffer) for coalesced loads
+    // carried-in state, staged through shared memory (the fq, fk buffers) for coalesced loads
     float s[E];
+    auto ent = [&](int e) { return 4 * ((e >> 2) * G + g) + (e & 3); };   // feature index of entry e
     {
-        float *stage = fk;                    // [Fp][16], fits in [L][Fp]
-        for (int idx = tid; idx < a.Fp * kFwCols; idx += kFwThreads) {
-            const int f = idx / kFwCols, cc = idx - f * kFwCols;
+        float *stage = fq;                    // [Fp][cpc], fits in 2 [L][Fp] (cpc <= 64)
+        for (int idx = tid; idx < a.Fp * cpc; idx += nthr) {
+            const int f = idx / cpc, cc = idx - f * cpc;
             stage[idx] = (a.S && f < a.F) ? a.S[(h * a.F + f) * a.M + m0 + cc] : 0.f;
         }
         if (DEN)
-            for (int f = tid; f < a.Fp; f += kFwThreads) zs[f] = (a.z && f < a.F) ? a.z[h * a.F + f] : 0.f;
+            for (int f = tid; f < a.Fp; f += nthr) zs[f] = (a.z && f < a.F) ? a.z[h * a.F + f] : 0.f;
         __syncthreads();
 #pragma unroll
-        for (int e = 0; e < E; ++e) s[e] = stage[(g + kFwG * e) * kFwCols + mc];
+        for (int e = 0; e < E; ++e) s[e] = stage[ent(e) * cpc + mc];
     }
 
     float bnext = 0.f;
@@ -251,11 +260,10 @@ fw_causal_kernel(FwArgs a)
         cp_async_wait_all();
         __syncthreads();                      // chunk t0's raw rows (and beta) are in shared memory
         // features of the chunk (rows past `rows` are zero)
-        for (int idx = tid; idx < kFwL * a.Fp; idx += kFwThreads) {
+        for (int idx = tid; idx < kFwL * a.Fp; idx += nthr) {
             const int t = idx / a.Fp, f = idx - t * a.Fp;
-            const bool ok = t < rows;
             float vk = 0.f, vq = 0.f;
-            if (ok) {
+            if (t < rows) {
                 vk = feature_raw<T>(r.k + t * a.D, f, a.fm, a.D, a.nu, a.F);
                 if (want_q) vq = feature_raw<T>(r.q + t * a.D, f, a.fm, a.D, a.nu, a.F);
             }
@@ -264,7 +272,7 @@ fw_causal_kernel(FwArgs a)
         }
         __syncthreads();
         if (a.norm == LA_NORM_SUM) {
-            for (int rr = warp; rr < 2 * kFwL; rr += kFwWarps) {
+            for (int rr = warp; rr < 2 * kFwL; rr += nwarps) {
                 if (rr >= kFwL && !want_q) continue;
                 float *row = (rr < kFwL ? fk : fq) + (rr % kFwL) * a.Fp;
                 float sum = 0.f;
@@ -281,13 +289,13 @@ fw_causal_kernel(FwArgs a)
 
         if (DEN && want_q) {
             // den_t = phi(q_t) . (z_prev + sum_{s <= t} phi(k_s)): warp w owns the
-            // features w*32 + lane + 256 p and keeps their running z
-            for (int t = 0; t < kFwL; ++t)
-                if (lane == 0) dpart[warp * kFwL + t] = 0.f;
+            // features w*32 + lane + 32 nwarps p and keeps their running z
+            if (lane == 0)
+                for (int t = 0; t < kFwL; ++t) dpart[warp * kFwL + t] = 0.f;
             __syncwarp();
-            for (int f0 = warp * 32; f0 < a.Fp; f0 += kFwThreads) {   // warp-uniform
+            for (int f0 = warp * 32; f0 < a.Fp; f0 += nthr) {   // warp-uniform
                 const int f = f0 + lane;
-                const bool ok = f < a.Fp;             // Fp = 16 leaves half a warp idle
+                const bool ok = f < a.Fp;
                 float zf = ok ? zs[f] : 0.f;
                 for (int t = 0; t < rows; ++t) {
                     zf += ok ? fk[t * a.Fp + f] : 0.f;
@@ -299,12 +307,12 @@ fw_causal_kernel(FwArgs a)
             __syncthreads();
             if (tid < kFwL) {
                 float d = 0.f;
-                for (int w = 0; w < kFwWarps; ++w) d += dpart[w * kFwL + tid];
+                for (int w = 0; w < nwarps; ++w) d += dpart[w * kFwL + tid];
                 den[tid] = d;
             }
             __syncthreads();
         } else if (DEN) {
-            for (int f = tid; f < a.Fp; f += kFwThreads) {
+            for (int f = tid; f < a.Fp; f += nthr) {
                 float zf = zs[f];
                 for (int t = 0; t < rows; ++t) zf += fk[t * a.Fp + f];
                 zs[f] = zf;
@@ -312,40 +320,49 @@ fw_causal_kernel(FwArgs a)
         }
 
         // the recurrence over the chunk's tokens, each warp on its own columns
+        auto dot = [&](const float *row, float &acc0, float &acc1) {   // row points at [f = 0]
+#pragma unroll
+            for (int e4 = 0; e4 < E / 4; ++e4) {
+                const float4 x = *reinterpret_cast<const float4 *>(row + 4 * (e4 * G + g));
+                acc0 = fmaf(x.x, s[4 * e4], acc0);
+                acc1 = fmaf(x.y, s[4 * e4 + 1], acc1);
+                acc0 = fmaf(x.z, s[4 * e4 + 2], acc0);
+                acc1 = fmaf(x.w, s[4 * e4 + 3], acc1);
+            }
+        };
         if (DELTA) {
             // the read-out of token t-1 and the retrieval of token t both read the
-            // state after token t-1, so their half-warp reductions run together
+            // state after token t-1, so their reductions run together
             for (int t = 0; t <= rows; ++t) {
                 const bool has_k = t < rows, has_y = want_q && t > 0;   // warp-uniform
                 float kr[E];
                 float r0 = 0.f, r1 = 0.f, y0 = 0.f, y1 = 0.f;
                 if (has_k) {
-                    const float *fkt = fk + t * a.Fp + g;
+                    const float *fkt = fk + t * a.Fp;
 #pragma unroll
-                    for (int e = 0; e < E; ++e) kr[e] = fkt[kFwG * e];
+                    for (int e4 = 0; e4 < E / 4; ++e4) {
+                        const float4 x = *reinterpret_cast<const float4 *>(fkt + 4 * (e4 * G + g));
+                        kr[4 * e4] = x.x;
+                        kr[4 * e4 + 1] = x.y;
+                        kr[4 * e4 + 2] = x.z;
+                        kr[4 * e4 + 3] = x.w;
+                    }
 #pragma unroll
                     for (int e = 0; e < E; e += 2) {
                         r0 = fmaf(kr[e], s[e], r0);
-                        if (e + 1 < E) r1 = fmaf(kr[e + 1], s[e + 1], r1);
+                        r1 = fmaf(kr[e + 1], s[e + 1], r1);
                     }
                 }
-                if (has_y) {
-                    const float *fqt = fq + (t - 1) * a.Fp + g;
-#pragma unroll
-                    for (int e = 0; e < E; e += 2) {
-                        y0 = fmaf(fqt[kFwG * e], s[e], y0);
-                        if (e + 1 < E) y1 = fmaf(fqt[kFwG * (e + 1)], s[e + 1], y1);
-                    }
-                }
+                if (has_y) dot(fq + (t - 1) * a.Fp, y0, y1);
                 float rr = r0 + r1, y = y0 + y1;
 #pragma unroll
-                for (int o = kFwG / 2; o > 0; o >>= 1) {
+                for (int o = G / 2; o > 0; o >>= 1) {
                     rr += __shfl_xor_sync(0xffffffffu, rr, o);
                     y += __shfl_xor_sync(0xffffffffu, y, o);
                 }
-                if (has_y && g == 0) ys[(t - 1) * kFwCols + mc] = y;
+                if (has_y && g == 0) ys[(t - 1) * cpc + mc] = y;
                 if (has_k) {
-                    const float u = r.b[t] * (to_f32(r.v[t * kFwCols + mc]) - rr);
+                    const float u = r.b[t] * (to_f32(r.v[t * cpc + mc]) - rr);
 #pragma unroll
                     for (int e = 0; e < E; ++e) s[e] = fmaf(kr[e], u, s[e]);
                 }
@@ -353,26 +370,30 @@ fw_causal_kernel(FwArgs a)
         } else {
 #pragma unroll 2
             for (int t = 0; t < rows; ++t) {
-                const float *fkt = fk + t * a.Fp + g, *fqt = fq + t * a.Fp + g;
-                const float vt = to_f32(r.v[t * kFwCols + mc]);
+                const float *fkt = fk + t * a.Fp;
+                const float vt = to_f32(r.v[t * cpc + mc]);
 #pragma unroll
-                for (int e = 0; e < E; ++e) s[e] = fmaf(fkt[kFwG * e], vt, s[e]);
+                for (int e4 = 0; e4 < E / 4; ++e4) {
+                    const float4 x = *reinterpret_cast<const float4 *>(fkt + 4 * (e4 * G + g));
+                    s[4 * e4] = fmaf(x.x, vt, s[4 * e4]);
+                    s[4 * e4 + 1] = fmaf(x.y, vt, s[4 * e4 + 1]);
+                    s[4 * e4 + 2] = fmaf(x.z, vt, s[4 * e4 + 2]);
+                    s[4 * e4 + 3] = fmaf(x.w, vt, s[4 * e4 + 3]);
+                }
                 if (want_q) {
                     float y0 = 0.f, y1 = 0.f;            // read-out S^T phi(q), after the update
+                    dot(fq + t * a.Fp, y0, y1);
+                    float y = y0 + y1;
 #pragma unroll
-                    for (int e = 0; e < E; e += 2) {
-                        y0 = fmaf(fqt[kFwG * e], s[e], y0);
-                        if (e + 1 < E) y1 = fmaf(fqt[kFwG * (e + 1)], s[e + 1], y1);
-                    }
-                    const float y = half_warp_sum(y0 + y1);
-                    if (g == 0) ys[t * kFwCols + mc] = DEN ? y / den[t] : y;
+                    for (int o = G / 2; o > 0; o >>= 1) y += __shfl_xor_sync(0xffffffffu, y, o);
+                    if (g == 0) ys[t * cpc + mc] = DEN ? y / den[t] : y;
                 }
             }
         }
         __syncthreads();
         if (want_q)
-            for (int idx = tid; idx < rows * kFwCols; idx += kFwThreads) {
-                const int t = idx / kFwCols, cc = idx - t * kFwCols;
+            for (int idx = tid; idx < rows * cpc; idx += nthr) {
+                const int t = idx / cpc, cc = idx - t * cpc;
                 oh[(long long)(t0 + t) * a.M + m0 + cc] = from_f32<T>(ys[idx]);
             }
         if (DELTA && tid < kFwL && t0 + kFwL < a.N) raw(buf ^ 1).b[tid] = bnext;
@@ -381,18 +402,18 @@ fw_causal_kernel(FwArgs a)
 
     if (a.S) {
         __syncthreads();
-        float *stage = fk;
+        float *stage = fq;
 #pragma unroll
-        for (int e = 0; e < E; ++e) stage[(g + kFwG * e) * kFwCols + mc] = s[e];
+        for (int e = 0; e < E; ++e) stage[ent(e) * cpc + mc] = s[e];
         __syncthreads();
-        for (int idx = tid; idx < a.F * kFwCols; idx += kFwThreads) {
-            const int f = idx / kFwCols, cc = idx - f * kFwCols;
+        for (int idx = tid; idx < a.F * cpc; idx += nthr) {
+            const int f = idx / cpc, cc = idx - f * cpc;
             a.S[(h * a.F + f) * a.M + m0 + cc] = stage[idx];
         }
     }
     if (DEN && a.z && blockIdx.y == 0) {
         __syncthreads();
-        for (int f = tid; f < a.F; f += kFwThreads) a.z[h * a.F + f] = zs[f];
+        for (int f = tid; f < a.F; f += nthr) a.z[h * a.F + f] = zs[f];
     }
 }
 
@@ -512,32 +533,51 @@ int entries_for(int F) {
 }
 
 template <typename T>
-size_t causal_smem(int D, int Fp) {
-    const size_t raw = (size_t)2 * kFwL * D * sizeof(T) + (size_t)kFwL * kFwCols * sizeof(T) + kFwL * 4;
-    return 2 * raw + sizeof(float) * ((size_t)2 * kFwL * Fp + kFwL * kFwCols + kFwL + kFwWarps * kFwL + Fp);
+size_t causal_smem(int D, int Fp, int cpc) {
+    const size_t raw = (size_t)2 * kFwL * D * sizeof(T) + (size_t)kFwL * cpc * sizeof(T) + kFwL * 4;
+    return 2 * raw + sizeof(float) * ((size_t)2 * kFwL * Fp + (size_t)kFwL * cpc + kFwL + kFwWarps * kFwL + Fp);
 }
 
-template <typename T, int E, bool DELTA, bool DEN>
-cudaError_t launch_causal_e(const FwArgs &a, long long BH, cudaStream_t st) {
-    const size_t smem = causal_smem<T>(a.D, a.Fp);
-    cudaError_t e = cudaFuncSetAttribute(fw_causal_kernel<T, E, DELTA, DEN>,
+// Lane layout of the causal kernel for feature width F: G lanes per column and
+// E entries per lane, Fp = G * E >= F; the instantiated (G, E) pairs.
+struct CausalLayout {
+    int G, E;
+};
+CausalLayout causal_layout(int F) {
+    static const CausalLayout kLayouts[] = {{4, 4}, {4, 8}, {4, 16}, {4, 24}, {4, 32},
+                                            {8, 24}, {8, 32}, {16, 24}, {16, 32}};
+    for (const CausalLayout &l : kLayouts)
+        if (l.G * l.E >= F) return l;
+    return {0, 0};
+}
+
+template <typename T, int G, int E, bool DELTA, bool DEN>
+cudaError_t launch_causal_ge(FwArgs a, long long BH, cudaStream_t st) {
+    constexpr int CW = 32 / G;
+    a.Fp = G * E;
+    a.cpc = std::min(a.M, kFwWarps * CW);            // columns per CTA, one warp per CW columns
+    const size_t smem = causal_smem<T>(a.D, a.Fp, a.cpc);
+    cudaError_t e = cudaFuncSetAttribute(fw_causal_kernel<T, G, E, DELTA, DEN>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    fw_causal_kernel<T, E, DELTA, DEN><<<dim3((unsigned)BH, a.M / kFwCols), kFwThreads, smem, st>>>(a);
+    fw_causal_kernel<T, G, E, DELTA, DEN><<<dim3((unsigned)BH, a.M / a.cpc), 32 * (a.cpc / CW), smem, st>>>(a);
     count_launches(1);
     return cudaGetLastError();
 }
 
 template <typename T, bool DELTA, bool DEN>
 cudaError_t launch_causal_upd(const FwArgs &a, long long BH, cudaStream_t st) {
-    switch (a.Fp / kFwG) {
-        case 1: return launch_causal_e<T, 1, DELTA, DEN>(a, BH, st);
-        case 2: return launch_causal_e<T, 2, DELTA, DEN>(a, BH, st);
-        case 4: return launch_causal_e<T, 4, DELTA, DEN>(a, BH, st);
-        case 8: return launch_causal_e<T, 8, DELTA, DEN>(a, BH, st);
-        case 16: return launch_causal_e<T, 16, DELTA, DEN>(a, BH, st);
-        case 24: return launch_causal_e<T, 24, DELTA, DEN>(a, BH, st);
-        case 32: return launch_causal_e<T, 32, DELTA, DEN>(a, BH, st);
+    const CausalLayout l = causal_layout(a.F);
+    switch (l.G * 100 + l.E) {
+        case 404: return launch_causal_ge<T, 4, 4, DELTA, DEN>(a, BH, st);
+        case 408: return launch_causal_ge<T, 4, 8, DELTA, DEN>(a, BH, st);
+        case 416: return launch_causal_ge<T, 4, 16, DELTA, DEN>(a, BH, st);
+        case 424: return launch_causal_ge<T, 4, 24, DELTA, DEN>(a, BH, st);
+        case 432: return launch_causal_ge<T, 4, 32, DELTA, DEN>(a, BH, st);
+        case 824: return launch_causal_ge<T, 8, 24, DELTA, DEN>(a, BH, st);
+        case 832: return launch_causal_ge<T, 8, 32, DELTA, DEN>(a, BH, st);
+        case 1624: return launch_causal_ge<T, 16, 24, DELTA, DEN>(a, BH, st);
+        case 1632: return launch_causal_ge<T, 16, 32, DELTA, DEN>(a, BH, st);
     }
     return cudaErrorInvalidValue;
 }
@@ -633,7 +673,7 @@ size_t fw_noncausal_ws_bytes(const la_shape &s, const la_variant &v) {
 static FwArgs make_args(const Problem &p, const void *beta, const la_variant &v) {
     const int F = fw_feature_dim(v, p.D);
     const int E = entries_for(F);
-    return FwArgs{p.q, p.k, p.v, beta, p.out, p.S, p.z, p.N, p.D, p.M, F, E * kFwG, v.feature_map, v.nu, v.norm};
+    return FwArgs{p.q, p.k, p.v, beta, p.out, p.S, p.z, p.N, p.D, p.M, F, E * kFwG, v.feature_map, v.nu, v.norm, 0};
 }
 
 cudaError_t fw_causal(const Problem &p, const void *beta, const la_variant &v) {
