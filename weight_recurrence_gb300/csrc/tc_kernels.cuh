@@ -50,16 +50,16 @@ __device__ __forceinline__ void set_abort(volatile int *abort, int *err) {
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 // phi(x) = elu(x) + 1 on two bf16 values, written as max(x, 0) + min(e^x, 1):
-// for x > 0 that is x + 1 and for x <= 0 it is e^x.  e^x = 2^(x log2 e) is taken
-// in fp32 on the MUFU unit and rounded once to bf16; the max, min and add run
-// on packed bf16 pairs.  Each result is rounded exactly once (x + 1, or e^x),
-// so it equals the fp32 evaluation rounded to bf16.  NaN propagates.
+// for x > 0 that is x + 1 and for x <= 0 it is e^x.  e^x = 2^(x log2 e) with
+// both steps on packed bf16 pairs: the product x log2 e rounded to bf16 (a
+// relative error of 2^-9 in the exponent, i.e. about |x| 2^-9 in e^x), then
+// the MUFU's packed 2^t, two exponentials per instruction (the feature map of
+// a 128-row chunk is bound by the MUFU rate).  max, min and add also run on
+// the packed pairs.  NaN propagates.
 __device__ __forceinline__ uint32_t phi_bf16x2(uint32_t w) {
-    float el, eh;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(el) : "f"(bf16lo(w) * 1.4426950408889634f));
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(eh) : "f"(bf16hi(w) * 1.4426950408889634f));
-    const uint32_t e = pack_bf16x2(el, eh);
-    uint32_t m, n, r;
+    uint32_t t, e, m, n, r;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(t) : "r"(w), "r"(0x3FB93FB9u));   // log2(e) = 1.4427 -> bf16 0x3FB9
+    asm("ex2.approx.ftz.bf16x2 %0, %1;" : "=r"(e) : "r"(t));
     asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(m) : "r"(w), "r"(0u));
     asm("min.NaN.bf16x2 %0, %1, %2;" : "=r"(n) : "r"(e), "r"(0x3F803F80u));
     asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(m), "r"(n));
@@ -125,45 +125,62 @@ __device__ __forceinline__ float raw_at(const uint32_t (&w)[DR / 2], int i) {
     return (i & 1) ? bf16hi(w[i >> 1]) : bf16lo(w[i >> 1]);
 }
 
-// r_i of DPFP from the packed raw row (i a compile-time index after unrolling)
-template <int DR>
-__device__ __forceinline__ float dpfp_r(const uint32_t (&w)[DR / 2], int i) {
-    return i < DR ? fmaxf(raw_at<DR>(w, i), 0.f) : fmaxf(-raw_at<DR>(w, i - DR), 0.f);
-}
-
+// DPFP from products of raw values: for shift s and i < DR, the two features
+// r_i r_{i+s} (first half) and r_{DR+i} r_{DR+i+s} (second half, indices mod
+// 2DR) are relu(x_i) relu(sg x_j) and relu(-x_i) relu(-sg x_j), where x_j is
+// the partner value (j = i + s, or i + s - DR with sg = -1 past the end).  At
+// most one of the two is non-zero and their sum is p = max(sg x_i x_j, 0):
+// the first when x_i > 0, the second otherwise.
 template <int DR, int NU>
-__device__ __forceinline__ float dpfp_feature(const uint32_t (&w)[DR / 2], int f) {
-    const int s = f / (2 * DR) + 1, i = f % (2 * DR);
-    return dpfp_r<DR>(w, i) * dpfp_r<DR>(w, (i + s) % (2 * DR));
+__device__ __forceinline__ float dpfp_pair(const uint32_t (&w)[DR / 2], int s, int i) {
+    const int j = i + s;
+    const float xj = j < DR ? raw_at<DR>(w, j) : -raw_at<DR>(w, j - DR);
+    return fmaxf(raw_at<DR>(w, i) * xj, 0.f);
 }
 
 template <int F, int DR, int NU, bool SUM>
 __device__ __forceinline__ void dpfp_row(uint8_t *tile, int r, bool zero) {
-    static_assert(F == 2 * DR * NU && DR <= 64, "DPFP width");
+    static_assert(F == 2 * DR * NU && DR <= 64 && DR % 8 == 0, "DPFP width");
     uint32_t w[DR / 2];
     load_raw_row<DR>(tile, r, w);
     float scale = 1.f;
     if (SUM) {
-        float s = 0.f;
+        float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-        for (int f = 0; f < F; ++f) s += dpfp_feature<DR, NU>(w, f);
-        scale = s > 0.f ? 1.f / s : 0.f;
-        // recompute the features below instead of keeping all F of them live
+        for (int s = 1; s <= NU; ++s)
+#pragma unroll
+            for (int i = 0; i < DR; i += 2) {
+                s0 += dpfp_pair<DR, NU>(w, s, i);
+                s1 += dpfp_pair<DR, NU>(w, s, i + 1);
+            }
+        const float sum = s0 + s1;
+        scale = sum > 0.f ? 1.f / sum : 0.f;
+        // recompute the pairs below instead of keeping them all live
 #pragma unroll
         for (int j = 0; j < DR / 2; ++j) asm volatile("" : "+r"(w[j]));
     }
-#pragma unroll
-    for (int c8 = 0; c8 < F / 8; ++c8) {
-        const int c = 8 * c8;
+    auto put = [&](int c, const float (&v)[8]) {
         uint4 o = make_uint4(0u, 0u, 0u, 0u);
-        if (!zero) {
-            o.x = pack_bf16x2(dpfp_feature<DR, NU>(w, c) * scale, dpfp_feature<DR, NU>(w, c + 1) * scale);
-            o.y = pack_bf16x2(dpfp_feature<DR, NU>(w, c + 2) * scale, dpfp_feature<DR, NU>(w, c + 3) * scale);
-            o.z = pack_bf16x2(dpfp_feature<DR, NU>(w, c + 4) * scale, dpfp_feature<DR, NU>(w, c + 5) * scale);
-            o.w = pack_bf16x2(dpfp_feature<DR, NU>(w, c + 6) * scale, dpfp_feature<DR, NU>(w, c + 7) * scale);
-        }
+        if (!zero)
+            o = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                           pack_bf16x2(v[6], v[7]));
         *reinterpret_cast<uint4 *>(tile + (c / 64) * kC * 128 + sw128_offset(r, c % 64)) = o;
-    }
+    };
+#pragma unroll
+    for (int s = 1; s <= NU; ++s)
+#pragma unroll
+        for (int i0 = 0; i0 < DR; i0 += 8) {
+            float hi[8], lo[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const float p = dpfp_pair<DR, NU>(w, s, i0 + k) * scale;
+                const bool pos = raw_at<DR>(w, i0 + k) > 0.f;
+                hi[k] = pos ? p : 0.f;
+                lo[k] = pos ? 0.f : p;
+            }
+            put((s - 1) * 2 * DR + i0, hi);
+            put((s - 1) * 2 * DR + DR + i0, lo);
+        }
 }
 
 // Elementwise, so each 8-column chunk is read, mapped and written back in
