@@ -163,6 +163,12 @@ NC_CASES = [
     ("dpfp", 1, "sum", 2, 2, 700, 64, 64, torch.bfloat16, 0.125),
     ("dpfp", 3, "none", 1, 1, 90, 32, 16, torch.float32, 1.0),
     ("poly2", 1, "den", 1, 2, 333, 16, 128, torch.float32, 1.0),
+    # bf16 without the denominator, F in {64, 128}: the one-launch tensor-core kernel
+    ("dpfp", 1, "sum", 2, 3, 1000, 32, 128, torch.bfloat16, 0.25),
+    ("dpfp", 4, "none", 1, 2, 257, 16, 64, torch.bfloat16, 0.5),
+    ("elu1", 1, "sum", 2, 2, 3000, 64, 64, torch.bfloat16, 0.125),
+    ("elu1", 1, "none", 1, 2, 129, 128, 128, torch.bfloat16, 1.0 / math.sqrt(128)),
+    ("dpfp", 2, "sum", 1, 1, 1, 32, 64, torch.bfloat16, 0.25),
 ]
 
 

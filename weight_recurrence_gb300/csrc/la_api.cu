@@ -318,7 +318,16 @@ int la_feature_dim(la_variant var, int D) {
 size_t la_variant_workspace_bytes(la_op op, la_shape s, la_variant var) {
     if (check_shape(s, op != LA_OP_DECODE) != LA_OK || fw_check_variant(var, s.D) != LA_OK) return (size_t)-1;
     switch (op) {
-        case LA_OP_NONCAUSAL: return var.update == LA_UPDATE_SUM ? fw_noncausal_ws_bytes(s, var) : (size_t)-1;
+        case LA_OP_NONCAUSAL: {
+            if (var.update != LA_UPDATE_SUM) return (size_t)-1;
+            Problem p{};
+            if (tc_variant_route(s, var, p)) {   // the tensor-core kernel's exchange slots, feature width F
+                la_shape sf = s;
+                sf.D = p.D;
+                return tc_noncausal_ws_bytes(sf);
+            }
+            return fw_noncausal_ws_bytes(s, var);
+        }
         case LA_OP_CAUSAL:
         case LA_OP_DECODE: return 0;
         default: return (size_t)-1;
@@ -391,6 +400,9 @@ la_status la_forward_noncausal_variant(const void *q, const void *k, const void 
     if (!dev) return LA_ERR_CUDA;
     Problem p{q, k, v, out, nullptr, nullptr, BH, s.N, s.D, s.M, s.dtype, 0, workspace, ws_bytes,
               (cudaStream_t)stream};
+    // bf16, no denominator, F in {64, 128}: the one-launch tensor-core kernel
+    // with the feature map applied row by row on chip
+    if (tc_variant_route(s, var, p)) return from_cuda(tc_noncausal(p, *dev));
     return from_cuda(fw_noncausal(p, var, *dev));
 }
 

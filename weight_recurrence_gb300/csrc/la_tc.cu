@@ -185,6 +185,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     using C = Cfg<D, M>;
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (tid == 0) LA_TRACE_AT(0, 63, 0);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + C::OFF_TSLOT + 4);
 
     const int bh = blockIdx.x / args.nseg, seg = blockIdx.x % args.nseg;
@@ -256,6 +257,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
+    if (tid == 0) LA_TRACE_AT(0, 63, 1);
 
     // Test hook: wait on a barrier that nothing arrives on, then give up.
     if (args.inject_ns && tid == 0) {
@@ -638,6 +640,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 output_rows(it);
             }
             if (leader && C::OUT_TMA && args.out) tma_store_wait_all0();
+            if (leader) LA_TRACE_AT(0, 63, 2);
             // state after the last token (last segment only)
             if (S_h && seg == args.nseg - 1 && n > 0 && !*abort) {
 #pragma unroll
@@ -757,6 +760,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     }
     // no MMA may still be running when the CTA frees its TMEM
     if (tid == 0) mbar_wait_bounded(drain, 0, now_ns() + kWaitNs, nullptr);
+    if (tid == 0) LA_TRACE_AT(0, 63, 3);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -1004,9 +1008,11 @@ struct NoncausalArgs {
     int G;                   // CTAs per head (cluster size)
     int cps;                 // chunks per CTA
     int *err;
+    int feat, dr, nu, sum_norm, no_den;   // a variant's feature map and read-out (VAR only)
 };
 
-template <int D, int M>
+// VAR: a variant's feature map and read-out, as in causal_tc_kernel.
+template <int D, int M, bool VAR>
 __global__ void __launch_bounds__(kThreads, NCfg<D, M>::CTAS_PER_SM)
 noncausal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -1076,19 +1082,19 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 const int s = idx % C::NS, k = idx / C::NS;
                 if (idx >= C::NS && !wait_bar(&empty[s], (k - 1) & 1, abort)) break;
                 uint8_t *st = smem + s * C::STAGE;
+                // DPFP rows arrive raw (at most 64 columns, one box)
+                const int qk_boxes = VAR && args.feat == kFeatDpfp ? 1 : D / 64;
                 if (idx < n) {
                     const int t0 = (c_begin + idx) * kC;
-                    mbar_arrive_expect_tx(&full[s], C::STAGE);
-#pragma unroll
-                    for (int j = 0; j < D / 64; ++j) tma_load_3d(st + j * kC * 128, &tm_k, &full[s], j * 64, t0, bh);
+                    mbar_arrive_expect_tx(&full[s], qk_boxes * kC * 128 + C::TILE_V);
+                    for (int j = 0; j < qk_boxes; ++j) tma_load_3d(st + j * kC * 128, &tm_k, &full[s], j * 64, t0, bh);
 #pragma unroll
                     for (int j = 0; j < M / 64; ++j)
                         tma_load_3d(st + C::TILE_K + j * kC * 128, &tm_v, &full[s], j * 64, t0, bh);
                 } else {
                     const int t0 = (c_begin + idx - n) * kC;
-                    mbar_arrive_expect_tx(&full[s], C::TILE_K);
-#pragma unroll
-                    for (int j = 0; j < D / 64; ++j) tma_load_3d(st + j * kC * 128, &tm_q, &full[s], j * 64, t0, bh);
+                    mbar_arrive_expect_tx(&full[s], qk_boxes * kC * 128);
+                    for (int j = 0; j < qk_boxes; ++j) tma_load_3d(st + j * kC * 128, &tm_q, &full[s], j * 64, t0, bh);
                 }
                 ++issued;
             }
@@ -1252,7 +1258,7 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 uint32_t dv[16];
                 tmem_ld16(tmem + lane_off + C::col_o(ob) + M, dv);
                 tmem_wait_ld();
-                const float inv = 1.f / (__uint_as_float(dv[0]) + __uint_as_float(dv[1]));
+                const float inv = VAR && args.no_den ? 1.f : 1.f / (__uint_as_float(dv[0]) + __uint_as_float(dv[1]));
 #pragma unroll 1
                 for (int c0 = 0; c0 < M; c0 += 32) {
                     float o[32];
@@ -1292,8 +1298,10 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         for (int idx = 0; idx < total; ++idx) {
             const int s = idx % C::NS;
             if (wait_bar(&full[s], (idx / C::NS) & 1, abort)) {
-                if (idx < n) phi_tile<D>(smem + s * C::STAGE, t, min(kC, args.N - (c_begin + idx) * kC));
-                else phi_tile<D>(smem + s * C::STAGE, t, kC);
+                const int zf = idx < n ? min(kC, args.N - (c_begin + idx) * kC) : kC;
+                if (!VAR || args.feat == kFeatPhi) phi_tile<D>(smem + s * C::STAGE, t, zf);
+                else if constexpr (VAR)   // a variant's feature map, one row per thread
+                    feature_row<D>(smem + s * C::STAGE, t, zf, args.feat, args.dr, args.nu, args.sum_norm);
             }
             fence_proxy_async();
             mbar_arrive(&phi_done[s]);
@@ -1392,18 +1400,20 @@ void nc_grid(long long BH, int N, int slots, int &G, int &cps) {
     G = (nch + cps - 1) / cps;
 }
 
-template <int D, int M>
-cudaError_t launch_noncausal(const Problem &p, const DeviceInfo &dev) {
+template <int D, int M, bool VAR>
+cudaError_t launch_noncausal_v(const Problem &p, const DeviceInfo &dev) {
     using C = NCfg<D, M>;
     CUtensorMap tq, tk, tv, to;
-    if (!cached_tmap_bf16_3d(&tq, p.q, D, p.N, p.BH, 64, kC) || !cached_tmap_bf16_3d(&tk, p.k, D, p.N, p.BH, 64, kC) ||
+    const int qk_cols = p.feat != kFeatPhi ? p.dr : D;   // raw rows of a variant's feature map
+    if (!cached_tmap_bf16_3d(&tq, p.q, qk_cols, p.N, p.BH, 64, kC) ||
+        !cached_tmap_bf16_3d(&tk, p.k, qk_cols, p.N, p.BH, 64, kC) ||
         !cached_tmap_bf16_3d(&tv, p.v, M, p.N, p.BH, 64, kC) || !cached_tmap_bf16_3d(&to, p.out, M, p.N, p.BH, 64, kC))
         return cudaErrorInvalidValue;
     int G, cps;
     nc_grid(p.BH, p.N, C::CTAS_PER_SM * dev.sm_count, G, cps);
     if (p.ws_bytes < (size_t)p.BH * G * (D * M + D) * sizeof(float)) return cudaErrorInvalidValue;
     cudaError_t e;
-    if ((e = set_smem(noncausal_tc_kernel<D, M>, C::SMEM)) != cudaSuccess) return e;
+    if ((e = set_smem(noncausal_tc_kernel<D, M, VAR>, C::SMEM)) != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(p.BH * G));
     cfg.blockDim = dim3(kThreads);
@@ -1416,10 +1426,17 @@ cudaError_t launch_noncausal(const Problem &p, const DeviceInfo &dev) {
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    const NoncausalArgs a{(float *)p.ws, p.N, G, cps, dev.err_word};
-    e = cudaLaunchKernelEx(&cfg, noncausal_tc_kernel<D, M>, tq, tk, tv, to, a);
+    const NoncausalArgs a{(float *)p.ws, p.N, G, cps, dev.err_word, p.feat, p.dr, p.nu, p.sum_norm ? 1 : 0,
+                          p.no_den ? 1 : 0};
+    e = cudaLaunchKernelEx(&cfg, noncausal_tc_kernel<D, M, VAR>, tq, tk, tv, to, a);
     count_launches(1);
     return e;
+}
+
+template <int D, int M>
+cudaError_t launch_noncausal(const Problem &p, const DeviceInfo &dev) {
+    return (p.feat != kFeatPhi || p.no_den) ? launch_noncausal_v<D, M, true>(p, dev)
+                                            : launch_noncausal_v<D, M, false>(p, dev);
 }
 
 bool tc_dims(const la_shape &s) {
