@@ -81,6 +81,13 @@ TC_CASES = [
     ("elu1", 1, "none", "sum", 1, 2, 300, 64, 128, torch.bfloat16, 0.125),
     ("elu1", 1, "none", "sum", 1, 1, 1, 128, 64, torch.bfloat16, 1.0),
     ("dpfp", 1, "sum", "sum", 1, 1, 1, 64, 64, torch.bfloat16, 0.125),
+    # bf16 delta rule, F = M = 64: chunks of 128 tokens on tensor cores
+    ("elu1", 1, "sum", "delta", 2, 2, 1000, 64, 64, torch.bfloat16, 0.125),
+    ("elu1", 1, "sum", "delta", 1, 3, 3000, 64, 64, torch.bfloat16, 0.125),
+    ("elu1", 1, "sum", "delta", 1, 2, 128, 64, 64, torch.bfloat16, 1.0),
+    ("elu1", 1, "sum", "delta", 1, 1, 1, 64, 64, torch.bfloat16, 1.0),
+    ("dpfp", 1, "sum", "delta", 2, 1, 777, 32, 64, torch.bfloat16, 0.25),
+    ("dpfp", 2, "sum", "delta", 1, 2, 129, 16, 64, torch.bfloat16, 0.5),
 ]
 
 
@@ -125,7 +132,8 @@ def test_variant_without_state_matches_zero_state():
                                                          ("dpfp", 2, "sum", "delta", 16, 32, torch.float32),
                                                          ("poly2", 1, "none", "sum", 16, 32, torch.float32),
                                                          ("dpfp", 1, "sum", "sum", 64, 64, torch.bfloat16),
-                                                         ("elu1", 1, "none", "sum", 64, 128, torch.bfloat16)])
+                                                         ("elu1", 1, "none", "sum", 64, 128, torch.bfloat16),
+                                                         ("elu1", 1, "sum", "delta", 64, 64, torch.bfloat16)])
 def test_state_only_and_split_carry(fm, nu, norm, update, D, M, dtype):
     """A state-only call (out = NULL) leaves the same state as a full call, and two
     calls chained through the state equal one call over the whole sequence (the

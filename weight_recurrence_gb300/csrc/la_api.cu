@@ -377,6 +377,13 @@ la_status la_forward_causal_variant(const void *q, const void *k, const void *v,
         if (!dev) return LA_ERR_CUDA;
         return from_cuda(tc_causal(p, *dev));
     }
+    if (tc_delta_supported(s, var)) {
+        // bf16 delta rule, F = M = 64: chunks of 128 tokens on tensor cores with
+        // the triangular solve for the pseudo-values on CUDA cores
+        const DeviceInfo *dev = device_info();
+        if (!dev) return LA_ERR_CUDA;
+        return from_cuda(tc_delta(p, beta, var, *dev));
+    }
     return from_cuda(fw_causal(p, var.update == LA_UPDATE_DELTA ? beta : nullptr, var));
 }
 

@@ -99,6 +99,12 @@ cudaError_t fw_noncausal(const Problem &p, const la_variant &v, const DeviceInfo
 // nu, sum_norm, no_den and sets p.D to the feature width; false otherwise
 bool tc_variant_route(const la_shape &s, const la_variant &v, Problem &p);
 
+// chunked delta rule on tensor cores (la_tc_delta.cu): bf16, sum-normalised
+// features of width 64 (elu + 1 at D = 64, DPFP at D = 32 / nu = 1 or
+// D = 16 / nu = 2), M = 64
+bool tc_delta_supported(const la_shape &s, const la_variant &v);
+cudaError_t tc_delta(const Problem &p, const void *beta, const la_variant &v, const DeviceInfo &dev);
+
 // Counts kernel launches made through the library (la_api.cu).
 void count_launches(int n);
 

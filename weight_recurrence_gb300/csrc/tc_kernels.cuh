@@ -183,39 +183,35 @@ __device__ __forceinline__ void dpfp_row(uint8_t *tile, int r, bool zero) {
         }
 }
 
-// Elementwise, so each 8-column chunk is read, mapped and written back in
-// place; the row sum needs a first pass over the same chunks.
+// Elementwise: pass 1 maps each 8-column chunk in place with the packed
+// phi_bf16x2 (two exponentials per MUFU instruction) and sums the bf16 results
+// in fp32; pass 2 scales the chunks by 1 / sum (a second bf16 rounding).
 template <int F>
 __device__ __forceinline__ void elu1_sum_row(uint8_t *tile, int r, bool zero) {
-    auto at = [&](int c) { return tile + (c / 64) * kC * 128 + sw128_offset(r, c % 64); };
-    auto phi8 = [&](const uint4 &w, float (&v)[8]) {
-        const uint32_t u[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float a = bf16lo(u[j]), b = bf16hi(u[j]);
-            v[2 * j] = a > 0.f ? a + 1.f : __expf(a);
-            v[2 * j + 1] = b > 0.f ? b + 1.f : __expf(b);
-        }
-    };
-    float s = 0.f;
+    auto at = [&](int c) { return reinterpret_cast<uint4 *>(tile + (c / 64) * kC * 128 + sw128_offset(r, c % 64)); };
+    float s0 = 0.f, s1 = 0.f;
 #pragma unroll 4
     for (int c = 0; c < F; c += 8) {
-        float v[8];
-        phi8(*reinterpret_cast<const uint4 *>(at(c)), v);
-#pragma unroll
-        for (int j = 0; j < 8; ++j) s += v[j];
+        uint4 w = *at(c);
+        w.x = phi_bf16x2(w.x);
+        w.y = phi_bf16x2(w.y);
+        w.z = phi_bf16x2(w.z);
+        w.w = phi_bf16x2(w.w);
+        s0 += (bf16lo(w.x) + bf16hi(w.x)) + (bf16lo(w.y) + bf16hi(w.y));
+        s1 += (bf16lo(w.z) + bf16hi(w.z)) + (bf16lo(w.w) + bf16hi(w.w));
+        *at(c) = w;
     }
-    const float scale = 1.f / s;
-    asm volatile("" ::: "memory");   // read the chunks again rather than keep them live
+    const float scale = 1.f / (s0 + s1);
 #pragma unroll 4
     for (int c = 0; c < F; c += 8) {
-        float v[8];
-        phi8(*reinterpret_cast<const uint4 *>(at(c)), v);
+        const uint4 w = *at(c);
         uint4 o = make_uint4(0u, 0u, 0u, 0u);
         if (!zero)
-            o = make_uint4(pack_bf16x2(v[0] * scale, v[1] * scale), pack_bf16x2(v[2] * scale, v[3] * scale),
-                           pack_bf16x2(v[4] * scale, v[5] * scale), pack_bf16x2(v[6] * scale, v[7] * scale));
-        *reinterpret_cast<uint4 *>(at(c)) = o;
+            o = make_uint4(pack_bf16x2(bf16lo(w.x) * scale, bf16hi(w.x) * scale),
+                           pack_bf16x2(bf16lo(w.y) * scale, bf16hi(w.y) * scale),
+                           pack_bf16x2(bf16lo(w.z) * scale, bf16hi(w.z) * scale),
+                           pack_bf16x2(bf16lo(w.w) * scale, bf16hi(w.w) * scale));
+        *at(c) = o;
     }
 }
 
