@@ -521,6 +521,9 @@ def _leg_variant(torch, la, inputs, name, dev, stream, rot, pk, steps, max_over_
     # denominator and with F, M in {64, 128} run the chunked tcgen05 kernel
     tc = (w.dtype == torch.bfloat16 and update == "sum" and norm != "den" and F in (64, 128)
           and w.M in (64, 128))
+    # ... and bf16 delta-rule variants with sum-normalised features of width 64, M = 64
+    tc_delta = (w.dtype == torch.bfloat16 and update == "delta" and norm == "sum" and F == 64 and w.M == 64
+                and (fm == "elu1" or (fm == "dpfp" and (w.D, nu) in ((32, 1), (16, 2)))))
     hbm = {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
            "frac": round(gbs / pk["hbm_gbs"], 4), "alg_bytes_per_launch": alg,
            "traffic": _traffic("causal_variant_" + name)}
@@ -538,6 +541,11 @@ def _leg_variant(torch, la, inputs, name, dev, stream, rot, pk, steps, max_over_
                          "frac_alg": round(tf / pk["bf16_tflops"], 4)}
         leg["note"] = ("chunked tcgen05 causal kernel, the feature map applied row by row in shared memory "
                        "between TMA and MMA")
+    elif tc_delta:
+        leg["hbm"] = hbm
+        leg["note"] = ("chunked delta rule: K K^T, Q K^T, K S, Q S + tril(Q K^T) U and K^T U on tcgen05, the "
+                       "triangular solve for the pseudo-values U (C^2 M / 2 fp32 FMAs per chunk of C = 128) on "
+                       "CUDA cores; alu = the recurrence's 6 F M flops per head-token against the fp32 peak")
     else:
         leg["hbm"] = hbm
         leg["note"] = ("CUDA-core recurrence: one CTA per (head, 16 state columns), each warp walking the tokens "

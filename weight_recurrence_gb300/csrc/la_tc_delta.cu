@@ -33,6 +33,14 @@
 // -DLA_TRACE (never in the library build); read with la_trace_read_delta().
 #ifdef LA_TRACE
 __device__ unsigned long long g_la_trace_delta[64][8];
+__device__ unsigned long long g_la_trace_solve[8][3];
+extern "C" int la_trace_read_solve(unsigned long long *dst) {
+    return (int)cudaMemcpyFromSymbol(dst, g_la_trace_solve, sizeof(g_la_trace_solve));
+}
+#define SOLVE_TRACE(it, b, ev)                                                                            \
+    do {                                                                                                  \
+        if (blockIdx.x == 0 && threadIdx.x == 0 && (it) == 2) g_la_trace_solve[b][ev] = clock64();        \
+    } while (0)
 extern "C" int la_trace_read_delta(unsigned long long *dst) {
     return (int)cudaMemcpyFromSymbol(dst, g_la_trace_delta, sizeof(g_la_trace_delta));
 }
@@ -42,6 +50,7 @@ extern "C" int la_trace_read_delta(unsigned long long *dst) {
     } while (0)
 #else
 #define DELTA_TRACE(it, ev) ((void)0)
+#define SOLVE_TRACE(it, b, ev) ((void)0)
 #endif
 
 namespace la {
@@ -55,9 +64,10 @@ constexpr int kDSnap = kDF * kDF * 2;         // state as bf16, [64 rows][64], 8
 constexpr int kDOffSnap = 2 * kDStage;        // S hi, S lo
 constexpr int kDOffL = kDOffSnap + 2 * kDSnap;                 // L by 16-column blocks, fp32; later U hi, U lo tiles
 constexpr int kDLBytes = 16 * (128 * 8 - 8 * 8 * 7) * 4;       // column blocks b = 0..7: rows 16 b .. 127 x 16
-constexpr int kDOffU = kDOffL + kDLBytes;                      // U work rows [128][64] fp32
-constexpr int kDOffA = kDOffU + kC * 64 * 4;                   // block right-hand sides [16][64] fp32
-constexpr int kDOffT = kDOffA + 16 * 64 * 4;                   // diagonal block inverses [8][16][16] fp32
+constexpr int kDUS = 68;                                       // row stride of the U work rows (floats)
+constexpr int kDOffU = kDOffL + kDLBytes;                      // U work rows [128][kDUS] fp32
+constexpr int kDOffA = kDOffU + kC * kDUS * 4;                   // a block's right-hand sides and solution, 2 x [16][64] fp32
+constexpr int kDOffT = kDOffA + 2 * 16 * 64 * 4;               // diagonal block inverses [8][16][16] fp32
 constexpr int kDOffB = kDOffT + 8 * 16 * 16 * 4;               // beta [128] fp32
 constexpr int kDOffBar = kDOffB + kC * 4;
 constexpr int kDOffSlot = kDOffBar + 8 * 4;
@@ -83,9 +93,13 @@ struct DeltaArgs {
 
 // L = diag(beta) tril(K K^T, -1) is kept by 16-column blocks: block b holds
 // rows 16 b .. 127 of columns 16 b .. 16 b + 15, 16 floats per row (64-byte
-// aligned rows).  Offset of L[i][16 b + j] for i >= 16 b:
+// aligned rows), the four float4 slots of row i permuted by (i >> 1) & 3 so
+// that 32 rows written at once by 32 lanes spread over all banks.  Offset of
+// L[i][16 b + j] for i >= 16 b:
 __device__ __forceinline__ int lblk(int b) { return 16 * (128 * b - 8 * b * (b - 1)); }
-__device__ __forceinline__ int lidx(int i, int b, int j) { return lblk(b) + (i - 16 * b) * 16 + j; }
+__device__ __forceinline__ int lrow16(int i, int b) { return lblk(b) + (i - 16 * b) * 16; }
+__device__ __forceinline__ int lslot(int i, int j4) { return 4 * (j4 ^ ((i >> 1) & 3)); }
+__device__ __forceinline__ int lidx(int i, int b, int j) { return lrow16(i, b) + lslot(i, j >> 2) + (j & 3); }
 
 // Thread 0 commits the MMAs it issued to `bar`; every thread waits for that
 // phase.  CTA-uniform result: false if any wait gave up (the phase is then
@@ -242,9 +256,16 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 float x[32];
                 tmem_ld32f(trow + kTColG + c0, x);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const int c = c0 + j, b = c >> 4;
-                    if (16 * b <= r) Lp[lidx(r, b, c & 15)] = c < r ? br * x[j] : 0.f;
+                for (int j4 = 0; j4 < 8; ++j4) {
+                    const int c = c0 + 4 * j4, b = c >> 4;
+                    if (16 * b <= r) {
+                        float4 o;
+                        o.x = c < r ? br * x[4 * j4] : 0.f;
+                        o.y = c + 1 < r ? br * x[4 * j4 + 1] : 0.f;
+                        o.z = c + 2 < r ? br * x[4 * j4 + 2] : 0.f;
+                        o.w = c + 3 < r ? br * x[4 * j4 + 3] : 0.f;
+                        *reinterpret_cast<float4 *>(Lp + lrow16(r, b) + lslot(r, (c & 15) >> 2)) = o;
+                    }
                 }
             }
             uint32_t packed[4][16];
@@ -279,8 +300,8 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 o1.y = br * (bf16hi(ww[2]) - w[8 * c8 + 5]);
                 o1.z = br * (bf16lo(ww[3]) - w[8 * c8 + 6]);
                 o1.w = br * (bf16hi(ww[3]) - w[8 * c8 + 7]);
-                *reinterpret_cast<float4 *>(Us + r * 64 + 8 * c8) = o0;
-                *reinterpret_cast<float4 *>(Us + r * 64 + 8 * c8 + 4) = o1;
+                *reinterpret_cast<float4 *>(Us + r * kDUS + 8 * c8) = o0;
+                *reinterpret_cast<float4 *>(Us + r * kDUS + 8 * c8 + 4) = o1;
             }
         }
         tmem_wait_st();
@@ -294,9 +315,17 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
                 float a = i == c ? 1.f : 0.f;
-                const float *Li = Lp + lidx(base + i, b, 0);
+                if (i > 0) {
+                    // row i of the diagonal block: its (i + 3) / 4 first float4 slots
+                    float lv[16];
 #pragma unroll
-                for (int j = 0; j < i; ++j) a = fmaf(-Li[j], x[j], a);
+                    for (int j4 = 0; j4 < (i + 3) / 4; ++j4) {
+                        const float4 t = *reinterpret_cast<const float4 *>(Lp + lrow16(base + i, b) + lslot(base + i, j4));
+                        lv[4 * j4] = t.x; lv[4 * j4 + 1] = t.y; lv[4 * j4 + 2] = t.z; lv[4 * j4 + 3] = t.w;
+                    }
+#pragma unroll
+                    for (int j = 0; j < i; ++j) a = fmaf(-lv[j], x[j], a);
+                }
                 x[i] = i < c ? 0.f : a;
             }
 #pragma unroll
@@ -304,51 +333,83 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         }
         __syncthreads();
         DELTA_TRACE(it, 5);
-        // ---- forward substitution by blocks of 16 rows, right-looking: block b
-        // is solved with its 16 x 16 inverse (thread t: row 16 b + t / 16,
-        // columns 4 (t % 16) .. +3, into Ab), then every later row i takes off
-        // L[i][block b] U_b (thread t: column t % 64, rows of its group t / 64)
+        // ---- forward substitution by blocks of 16 rows, right-looking, with the
+        // right-hand sides in registers: warp g owns rows i = g (mod 8), lane l
+        // columns l and l + 32.  For block b the two owned rows of the block go
+        // to Ab, are solved with the block's 16 x 16 inverse into Ab2, and every
+        // later owned row takes off L[i][block b] U_b.
         {
-            const int ib = tid >> 4, m0 = 4 * (tid & 15);
-            const int m = tid & 63, grp = tid >> 6;
-#pragma unroll 1
+            const int g = tid >> 5, l = tid & 31;
+            float acc[16][2];
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                acc[k][0] = Us[(g + 8 * k) * kDUS + l];
+                acc[k][1] = Us[(g + 8 * k) * kDUS + l + 32];
+            }
+            float *Ab2 = Ab + 16 * 64;
+#pragma unroll
             for (int b = 0; b < kC / 16; ++b) {
-                const int i = 16 * b + ib;
-                float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-                const float *Ti = Tb + (b * 16 + ib) * 16;
+                SOLVE_TRACE(it, b, 0);
+                // the block's rows owned here: local rows g and g + 8 (k = 2b, 2b + 1)
+                Ab[g * 64 + l] = acc[2 * b][0];
+                Ab[g * 64 + l + 32] = acc[2 * b][1];
+                Ab[(g + 8) * 64 + l] = acc[2 * b + 1][0];
+                Ab[(g + 8) * 64 + l + 32] = acc[2 * b + 1][1];
+                __syncthreads();
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int lr = g + 8 * h;                       // local row, warp-uniform
+                    const float *Ti = Tb + (b * 16 + lr) * 16;
+                    float x0 = 0.f, x1 = 0.f;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        if (j > lr) break;
+                        const float t = Ti[j];
+                        x0 = fmaf(t, Ab[j * 64 + l], x0);
+                        x1 = fmaf(t, Ab[j * 64 + l + 32], x1);
+                    }
+                    acc[2 * b + h][0] = x0;
+                    acc[2 * b + h][1] = x1;
+                    Ab2[lr * 64 + l] = x0;
+                    Ab2[lr * 64 + l + 32] = x1;
+                }
+                __syncthreads();
+                SOLVE_TRACE(it, b, 1);
+                float ub[16][2];
 #pragma unroll
                 for (int j = 0; j < 16; ++j) {
-                    if (j > ib) break;
-                    const float tij = Ti[j];
-                    const float4 a = *reinterpret_cast<const float4 *>(Us + (16 * b + j) * 64 + m0);
-                    x.x = fmaf(tij, a.x, x.x);
-                    x.y = fmaf(tij, a.y, x.y);
-                    x.z = fmaf(tij, a.z, x.z);
-                    x.w = fmaf(tij, a.w, x.w);
+                    ub[j][0] = Ab2[j * 64 + l];
+                    ub[j][1] = Ab2[j * 64 + l + 32];
                 }
-                *reinterpret_cast<float4 *>(Ab + ib * 64 + m0) = x;
-                __syncthreads();
-                // this thread's entries of U_b, kept as the solution rows of Us
-                *reinterpret_cast<float4 *>(Us + i * 64 + m0) = x;
-                float ub[16];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) ub[j] = Ab[j * 64 + m];
-#pragma unroll 2
-                for (int i2 = 16 * (b + 1) + grp; i2 < kC; i2 += 4) {
-                    const float4 *Lr = reinterpret_cast<const float4 *>(Lp + lidx(i2, b, 0));
-                    float acc0 = Us[i2 * 64 + m], acc1 = 0.f;
+                for (int k = 2 * b + 2; k < 16; ++k) {
+                    const int row = g + 8 * k;
+                    const float *Lr = Lp + lrow16(row, b);
+                    float a0 = acc[k][0], a1 = acc[k][1], c0 = 0.f, c1 = 0.f;
 #pragma unroll
                     for (int j4 = 0; j4 < 4; ++j4) {
-                        const float4 l = Lr[j4];
-                        acc0 = fmaf(-l.x, ub[4 * j4], acc0);
-                        acc1 = fmaf(-l.y, ub[4 * j4 + 1], acc1);
-                        acc0 = fmaf(-l.z, ub[4 * j4 + 2], acc0);
-                        acc1 = fmaf(-l.w, ub[4 * j4 + 3], acc1);
+                        const float4 lv = *reinterpret_cast<const float4 *>(Lr + lslot(row, j4));
+                        a0 = fmaf(-lv.x, ub[4 * j4][0], a0);
+                        a1 = fmaf(-lv.x, ub[4 * j4][1], a1);
+                        c0 = fmaf(-lv.y, ub[4 * j4 + 1][0], c0);
+                        c1 = fmaf(-lv.y, ub[4 * j4 + 1][1], c1);
+                        a0 = fmaf(-lv.z, ub[4 * j4 + 2][0], a0);
+                        a1 = fmaf(-lv.z, ub[4 * j4 + 2][1], a1);
+                        c0 = fmaf(-lv.w, ub[4 * j4 + 3][0], c0);
+                        c1 = fmaf(-lv.w, ub[4 * j4 + 3][1], c1);
                     }
-                    Us[i2 * 64 + m] = acc0 + acc1;
+                    acc[k][0] = a0 + c0;
+                    acc[k][1] = a1 + c1;
                 }
-                __syncthreads();
+                SOLVE_TRACE(it, b, 2);
             }
+            // U (all rows) back to the work rows for the tile conversion below
+#pragma unroll
+            for (int k = 0; k < 16; ++k) {
+                Us[(g + 8 * k) * kDUS + l] = acc[k][0];
+                Us[(g + 8 * k) * kDUS + l + 32] = acc[k][1];
+            }
+            __syncthreads();
         }
         DELTA_TRACE(it, 6);
         // ---- U as bf16 hi + lo operand tiles (over the dead L): row r, half wg
@@ -356,7 +417,7 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             float u[32];
 #pragma unroll
             for (int j = 0; j < 32; j += 4) {
-                const float4 x = *reinterpret_cast<const float4 *>(Us + r * 64 + 32 * wg + j);
+                const float4 x = *reinterpret_cast<const float4 *>(Us + r * kDUS + 32 * wg + j);
                 u[j] = x.x; u[j + 1] = x.y; u[j + 2] = x.z; u[j + 3] = x.w;
             }
             store_hilo32<kC>(uhi, ulo, r, 32 * wg, u);
