@@ -29,6 +29,21 @@
 #include "tc_kernels.cuh"
 #include "tc_ptx.cuh"
 
+// Optional per-phase timeline of CTA 0 of the forward sweep for performance
+// work: compiled only with -DLA_TRACE (never in the library build).
+#ifdef LA_TRACE
+__device__ unsigned long long g_la_trace_bwd[32][12];
+extern "C" int la_trace_read_bwd(unsigned long long *dst) {
+    return (int)cudaMemcpyFromSymbol(dst, g_la_trace_bwd, sizeof(g_la_trace_bwd));
+}
+#define BWD_TRACE(it, ev)                                                                            \
+    do {                                                                                             \
+        if (blockIdx.x == 0 && threadIdx.x == 0 && (it) < 32) g_la_trace_bwd[it][ev] = clock64();    \
+    } while (0)
+#else
+#define BWD_TRACE(it, ev) ((void)0)
+#endif
+
 namespace la {
 namespace {
 
@@ -277,6 +292,7 @@ bwd_tc_pass1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     constexpr uint32_t ID_KK = idesc_bf16(128, kBD, 0, 0);    // K-major A and B
     constexpr uint32_t ID_S = idesc_bf16(128, kBD, 1, 1);     // MN-major A and B
     for (int it = 0; it < nch && ok; ++it) {
+        BWD_TRACE(it, 0);
         const int s = it & 1, t0 = it * kC;
         uint8_t *st = smem + s * kStage;
         uint8_t *tq = st, *tk = st + kTile, *tv = st + 2 * kTile, *tdo = st + 3 * kTile;
@@ -292,6 +308,7 @@ bwd_tc_pass1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         psi_tile(tk, smem + kOffPsi, r, min(kC, N - t0));
         phi_tile<kBD>(tk, r, min(kC, N - t0));
         operands_ready();
+        BWD_TRACE(it, 1);
         const uint32_t aq = smem_u32(tq), ak = smem_u32(tk), av = smem_u32(tv), ag = smem_u32(gt), as = smem_u32(snap);
         // P = phi(Q) phi(K)^T
         if (r == 0)
@@ -299,11 +316,13 @@ bwd_tc_pass1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             for (int ks = 0; ks < kBD / 16; ++ks)
                 mma_f16_ss(tmem + kColP, kmajor_base(aq) + kmajor_step(ks), kmajor_base(ak) + kmajor_step(ks), ID_P, ks > 0);
         if (!(ok = mma_sync_all(mbar, phase, ok, args.err))) break;
+        BWD_TRACE(it, 2);
         // mask (j <= i), row sums, A as bf16 hi and lo parts (num feeds e, where
         // the output's error would enter every entry of A)
         const float rowsum = mask_to_bf16(trow + kColP, r, true, 0.f, nullptr, true);
         const float den = rowsum + q_dot_z<kBD>(tq, r, zs);
         operands_ready();
+        BWD_TRACE(it, 3);
         // num = A V + phi(Q) S
         if (r == 0) {
             const uint64_t dv = smem_desc(av, kC * 128, 1024), ds = smem_desc(as, kBD * 128, 1024);
@@ -321,6 +340,7 @@ bwd_tc_pass1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                                ds + (uint64_t)(part2 * kSnap / 16) + mnmajor_step(ks), ID_MN, 1);
         }
         if (!(ok = mma_sync_all(mbar, phase, ok, args.err))) break;
+        BWD_TRACE(it, 4);
         // g_i = dO_i / den_i, e_i = -(g_i . num_i) / den_i; g as bf16 into the
         // operand tile and the workspace, e into the workspace
         const bool valid = t0 + r < N;
@@ -356,15 +376,18 @@ bwd_tc_pass1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             }
         }
         operands_ready();
+        BWD_TRACE(it, 5);
         // A2 = g V^T
         if (r == 0)
 #pragma unroll
             for (int ks = 0; ks < kBD / 16; ++ks)
                 mma_f16_ss(tmem + kColP, kmajor_base(ag) + kmajor_step(ks), kmajor_base(av) + kmajor_step(ks), ID_P, ks > 0);
         if (!(ok = mma_sync_all(mbar, phase, ok, args.err))) break;
+        BWD_TRACE(it, 6);
         // A = (A2 + e_i) masked to j <= i, as bf16; asum its fp32 row sum
         const float asum = mask_to_bf16(trow + kColP, r, true, e, nullptr);
         operands_ready();
+        BWD_TRACE(it, 7);
         // dphi(Q) = A psi(K) + g S^T  (+ asum: the product with the 1 of phi = psi + 1)
         if (r == 0) {
             const uint64_t dk = smem_desc(smem_u32(smem + kOffPsi), kC * 128, 1024);
@@ -379,6 +402,7 @@ bwd_tc_pass1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                                kmajor_base(as + part2 * kSnap) + kmajor_step(ks, kBD), ID_KK, 1);
         }
         if (!(ok = mma_sync_all(mbar, phase, ok, args.err))) break;
+        BWD_TRACE(it, 8);
         // dQ = (dphi(Q) + e_i Z) * phi'(Q)
         {
             float dq[64];
@@ -399,6 +423,7 @@ bwd_tc_pass1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         }
         colsum_add(tk, nullptr, part, zs);
         if (!(ok = mma_sync_all(mbar, phase, ok, args.err))) break;
+        BWD_TRACE(it, 9);
         // the new state's bf16 snapshot for the next chunk
         if (r < kBD) {
             float v[32];
@@ -408,6 +433,7 @@ bwd_tc_pass1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             }
         }
         operands_ready();   // also: every thread is done with this stage
+        BWD_TRACE(it, 10);
     }
     tc_fence_before();
     __syncthreads();
