@@ -18,11 +18,19 @@
 //     dK = dphi(K) * min(phi(K), 1);  R += phi(Q)^T g,  r += sum_i e_i phi(Q_i).
 // Every product is a tcgen05 MMA (bf16 operands, fp32 accumulators in TMEM);
 // the masks, divisions and the rank-one terms run on CUDA cores between the
-// MMAs.  One CTA of 128 threads per head; thread t owns row t of every
-// 128-row accumulator (TMEM lane t).  The phases of a chunk run one after
-// the other, the next chunk's tiles loading by TMA meanwhile (two stages).
-// Every wait is bounded; a CTA that gives up records LA_ERR_TIMEOUT and
-// skips the rest of its work.
+// MMAs.  One CTA of two warpgroups (256 threads) per head: thread t owns row
+// t % 128 of every 128-row accumulator (TMEM lane t % 128), and the two
+// warpgroups split each CUDA-core phase by columns (or by operand), meeting
+// in shared memory where a row reduction spans both halves.  The phases of a
+// chunk run one after the other, the next chunk's tiles loading by TMA
+// meanwhile (two stages); the state products (S += phi(K)^T V in pass 1,
+// R += phi(Q)^T g in pass 2) and the column sums of Z and r are issued with
+// the chunk's first product, since the chunk's own gradient terms read the
+// bf16 snapshot of the state taken before it.  g, dQ, dK and dV leave
+// through TMA stores from swizzled tiles (dQ, dK and dV from stage tiles
+// whose last reader has finished); the next chunk's loads are issued after
+// the chunk's first products, once those stores have read their sources.  Every wait is bounded; a
+// CTA that gives up records LA_ERR_TIMEOUT and skips the rest of its work.
 #include "la_common.cuh"
 #include "la_internal.h"
 #include "tc_host.h"
@@ -32,48 +40,49 @@
 // Optional per-phase timeline of CTA 0 of the forward sweep for performance
 // work: compiled only with -DLA_TRACE (never in the library build).
 #ifdef LA_TRACE
-__device__ unsigned long long g_la_trace_bwd[32][12];
+__device__ unsigned long long g_la_trace_bwd[2][32][12];
 extern "C" int la_trace_read_bwd(unsigned long long *dst) {
     return (int)cudaMemcpyFromSymbol(dst, g_la_trace_bwd, sizeof(g_la_trace_bwd));
 }
-#define BWD_TRACE(it, ev)                                                                            \
+#define BWD_TRACE(pass, it, ev)                                                                      \
     do {                                                                                             \
-        if (blockIdx.x == 0 && threadIdx.x == 0 && (it) < 32) g_la_trace_bwd[it][ev] = clock64();    \
+        if (blockIdx.x == 0 && threadIdx.x == 0 && (it) < 32) g_la_trace_bwd[pass][it][ev] = clock64(); \
     } while (0)
 #else
-#define BWD_TRACE(it, ev) ((void)0)
+#define BWD_TRACE(pass, it, ev) ((void)0)
 #endif
 
 namespace la {
 namespace {
 
 constexpr int kBD = 64;                     // D = M
-constexpr int kBT = 128;                    // threads
+constexpr int kBT = 256;                    // threads: two warpgroups
 constexpr int kTile = kC * kBD * 2;         // one 128 x 64 bf16 tile, 16 KB
 constexpr int kStage = 4 * kTile;           // Q, K, V, dO (pass 1) or Q, K, V, g (pass 2)
-constexpr int kOffGT = 2 * kStage;          // pass 1: g of the chunk as an MMA operand
-constexpr int kOffSnap = kOffGT + kTile;    // state S or R as bf16 hi then lo parts, [64 rows][64] each
+constexpr int kOffGT = 2 * kStage;          // pass 1: g of the chunk (MMA operand, store source)
+constexpr int kOffPsi = kOffGT + kTile;     // psi(K) (pass 1) or psi(Q) (pass 2), an MMA operand
+constexpr int kOffSnap = kOffPsi + kTile;   // state S or R as bf16 hi then lo parts, [64 rows][64] each
 constexpr int kSnap = kBD * kBD * 2;        // 8 KB
-constexpr int kOffZ = kOffSnap + 2 * kSnap; // fp32 Z or r [64]
-constexpr int kOffE = kOffZ + kBD * 4;      // fp32 e of the chunk [128]
-constexpr int kOffPart = kOffE + kC * 4;    // fp32 [2][64] column-sum halves
-constexpr int kOffPsi = ((kOffPart + 2 * kBD * 4 + 1023) / 1024) * 1024;   // psi(K) (pass 1) or psi(Q) (pass 2)
-constexpr int kOffBar = kOffPsi + kTile;
-constexpr int kOffSlot = kOffBar + 8 * 4;
+constexpr int kOffZ = kOffSnap + 2 * kSnap; // fp32 Z or r, [2][64]: before and after the chunk
+constexpr int kOffE = kOffZ + 2 * kBD * 4;  // pass 2: fp32 e of the chunk [128]
+constexpr int kOffPart = kOffE + kC * 4;    // fp32 [8][64] column-sum parts
+constexpr int kOffX = kOffPart + 8 * kBD * 4;   // fp32 [3][2][128] row-reduction halves
+constexpr int kOffBar = kOffX + 3 * 2 * kC * 4;
+constexpr int kOffSlot = kOffBar + 8 * 8;
 constexpr int kBwdSmem = kOffSlot + 16;
 constexpr uint32_t kBwdTmemCols = 512;
 static_assert(kBwdSmem <= (int)kSmemMax, "shared memory budget");
+static_assert(kOffGT % 1024 == 0 && kOffPsi % 1024 == 0 && kOffSnap % 1024 == 0, "swizzled tiles on 1 KB");
 
-// TMEM columns.  Pass 1: P, then A, in [0, 128) (A as bf16 in [0, 64)); num
-// in [128, 192); dphi(Q) in [192, 256); S in [256, 320).  Pass 2: P^T in
-// [0, 128) (bf16 in [0, 64)), A^T in [128, 256) (bf16 in [128, 192)); dV in
-// [256, 320); dphi(K) in [320, 384); R in [384, 448).
-constexpr uint32_t kColP = 0, kColA2 = 128, kColNum = 128, kColDQ = 192, kColS = 256;
-constexpr uint32_t kColDV = 256, kColDK = 320, kColR = 384;
+// TMEM columns.  Pass 1: P, then A, in [0, 128); num in [128, 192); dphi(Q)
+// in [192, 256); S in [256, 320); P as bf16 hi parts in [320, 384) (later A
+// as bf16) and lo parts in [384, 448).  Pass 2: P^T in [0, 128) (bf16 in
+// [0, 64)), A^T in [128, 256) (bf16 in [128, 192)); dV in [256, 320);
+// dphi(K) in [320, 384); R in [384, 448).
+constexpr uint32_t kColP = 0, kColNum = 128, kColDQ = 192, kColS = 256, kColPH = 320, kColPL = 384;
+constexpr uint32_t kColA2 = 128, kColDV = 256, kColDK = 320, kColR = 384;
 
 struct BwdArgs {
-    __nv_bfloat16 *dq, *dk, *dv;
-    __nv_bfloat16 *g_ws;     // [BH, N, 64] bf16
     float *e_ws;             // [BH, N]
     const float *S0, *z0, *dSN, *dzN;
     float *dS0, *dz0;
@@ -81,28 +90,31 @@ struct BwdArgs {
     int *err;
 };
 
-// Synchronous MMA step: thread 0 commits everything it issued to `bar`;
-// every thread waits for that phase.  Returns false (CTA-uniform) if the wait
-// gave up.
-__device__ __forceinline__ bool mma_sync_all(uint64_t *bar, uint32_t &phase, bool ok, int *err) {
-    if (threadIdx.x == 0 && ok) mma_commit(bar);
-    bool mine = ok && mbar_wait_bounded(bar, phase, now_ns() + kWaitNs, nullptr);
-    if (ok && !mine && threadIdx.x == 0) record_error(err, kErrTimeout);
-    const bool all = __syncthreads_and(mine ? 1 : 0) != 0;
-    if (ok) phase ^= 1u;
+// This thread waits (bounded) for the next phase of an MMA-completion
+// barrier, which thread 0 arrives on with tcgen05.commit; TMEM reads may
+// follow.  Returns false if the wait gave up (the caller makes it CTA-uniform
+// at its next barrier_and).
+__device__ __forceinline__ bool mma_wait(uint64_t *bar, uint32_t &phase) {
+    const bool got = mbar_wait_bounded(bar, phase, now_ns() + kWaitNs, nullptr);
+    phase ^= 1u;
     tc_fence_after();
-    return all;
+    return got;
 }
 
 // All threads finished their TMEM stores and generic shared-memory writes:
-// make them visible to the MMAs thread 0 issues next.
-__device__ __forceinline__ void operands_ready() {
+// make them visible to the MMAs and TMA stores thread 0 issues next.  Returns
+// true iff every thread passed `mine`; records a timeout otherwise.
+__device__ __forceinline__ bool barrier_and(bool mine, int *err) {
     tmem_wait_st();
     fence_proxy_async();
     tc_fence_before();
-    __syncthreads();
+    const bool all = __syncthreads_and(mine ? 1 : 0) != 0;
     tc_fence_after();
+    if (!all && threadIdx.x == 0) record_error(err, kErrTimeout);
+    return all;
 }
+
+__device__ __forceinline__ void operands_ready() { barrier_and(true, nullptr); }
 
 // Loads the chunk's four tiles (64-column boxes) into stage `st`.
 __device__ __forceinline__ void load_chunk(uint8_t *st, uint64_t *full, const CUtensorMap *t0m,
@@ -115,70 +127,68 @@ __device__ __forceinline__ void load_chunk(uint8_t *st, uint64_t *full, const CU
     tma_load_3d(st + 3 * kTile, t3m, full, 0, t0, bh);
 }
 
-// Reads this thread's row of a 128-column fp32 accumulator, applies the
-// causal mask (pass 1 keeps columns j <= r, pass 2 keeps i >= r) and adds
-// `colv[c]` (if given) or `rowv` to the kept entries, writes the row back as
-// bf16 in the first 64 columns of the block, and returns the fp32 sum of
-// the kept entries (after the addition, before rounding).
-__device__ __forceinline__ float mask_to_bf16(uint32_t tbase, int r, bool lower, float rowv, const float *colv,
-                                              bool hilo = false) {
+// Columns [c0, c0 + 64) of this thread's row r of a 128-column fp32
+// accumulator at `src`: keeps columns j <= r (lower) or j >= r, adds colv[j]
+// (if given) or rowv to the kept entries, writes them as 32 packed bf16
+// pairs at `dst` and, if HILO, the rounding error of each as a second bf16
+// operand at `dst_lo`.  Returns the fp32 sum of the kept entries (after the
+// addition, before rounding).  All four loads are in flight before the wait.
+template <bool HILO>
+__device__ __forceinline__ float mask64(uint32_t src, int c0, int r, bool lower, float rowv, const float *colv,
+                                        uint32_t dst, uint32_t dst_lo) {
+    uint32_t x[4][16];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) tmem_ld16(src + c0 + 16 * b, x[b]);
+    tmem_wait_ld();
     float sum = 0.f;
-    uint32_t packed[4][16], packed_lo[4][16];
+    uint32_t hp[2][16], lp[2][16];
 #pragma unroll
-    for (int b = 0; b < 4; ++b) {
-        const int c0 = 32 * b;
-        float x[32];
-        tmem_ld32f(tbase + c0, x);
-#pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-            const int c = c0 + j;
-            const bool k0 = lower ? (c <= r) : (c >= r);
-            const bool k1 = lower ? (c + 1 <= r) : (c + 1 >= r);
-            const float add0 = colv ? colv[c] : rowv, add1 = colv ? colv[c + 1] : rowv;
-            const float a0 = k0 ? x[j] + add0 : 0.f, a1 = k1 ? x[j + 1] + add1 : 0.f;
-            sum += a0 + a1;
-            const uint32_t hp = pack_bf16x2(a0, a1);
-            packed[b][j / 2] = hp;
-            packed_lo[b][j / 2] = pack_bf16x2(a0 - bf16lo(hp), a1 - bf16hi(hp));
-        }
+    for (int j = 0; j < 64; j += 2) {
+        const int c = c0 + j;
+        const bool k0 = lower ? (c <= r) : (c >= r);
+        const bool k1 = lower ? (c + 1 <= r) : (c + 1 >= r);
+        const float2 cv = colv ? *reinterpret_cast<const float2 *>(colv + c) : make_float2(rowv, rowv);
+        const float add0 = cv.x, add1 = cv.y;
+        const float a0 = k0 ? __uint_as_float(x[j / 16][j % 16]) + add0 : 0.f;
+        const float a1 = k1 ? __uint_as_float(x[j / 16][j % 16 + 1]) + add1 : 0.f;
+        sum += a0 + a1;
+        const uint32_t h = pack_bf16x2(a0, a1);
+        hp[j / 32][(j % 32) / 2] = h;
+        if (HILO) lp[j / 32][(j % 32) / 2] = pack_bf16x2(a0 - bf16lo(h), a1 - bf16hi(h));
     }
-#pragma unroll
-    for (int b = 0; b < 4; ++b) tmem_st16(tbase + 16 * b, packed[b]);
-    if (hilo)   // the rounding error of each entry as a second bf16 operand
-#pragma unroll
-        for (int b = 0; b < 4; ++b) tmem_st16(tbase + 64 + 16 * b, packed_lo[b]);
+    tmem_st16(dst, hp[0]);
+    tmem_st16(dst + 16, hp[1]);
+    if (HILO) {
+        tmem_st16(dst_lo, lp[0]);
+        tmem_st16(dst_lo + 16, lp[1]);
+    }
     return sum;
 }
 
-// Column sums over the chunk's 128 rows of a phi-applied bf16 tile, each row
-// weighted by w[row] (or 1): thread t sums column t % 64 over rows of half
-// t / 64; the halves meet in `part`; threads 0..63 add the total to acc[t].
-__device__ __forceinline__ void colsum_add(const uint8_t *tile, const float *w, float *part, float *acc) {
-    const int t = threadIdx.x, d = t & 63, half = t >> 6;
-    float s = 0.f;
-#pragma unroll 8
-    for (int i = 64 * half; i < 64 * half + 64; ++i) {
-        const float x = __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(tile + sw128_offset(i, d)));
-        s = fmaf(w ? w[i] : 1.f, x, s);
+// Column sums of a 128 x 64 bf16 tile (swizzled), each row weighted by w[row]
+// (or 1), in eight parts: thread t sums the column pair 2(t % 32), 2(t % 32)+1
+// over rows 16(t / 32) .. +16 into part[t / 32][.].  A warp reads one
+// 128-byte row per step.
+__device__ __forceinline__ void colsum_part(const uint8_t *tile, const float *w, float *part) {
+    const int t = threadIdx.x, cp = t & 31, rg = t >> 5;
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+    for (int i = 16 * rg; i < 16 * rg + 16; ++i) {
+        const uint32_t x = *reinterpret_cast<const uint32_t *>(tile + sw128_offset(i, 2 * cp));
+        const float wi = w ? w[i] : 1.f;
+        s0 = fmaf(wi, bf16lo(x), s0);
+        s1 = fmaf(wi, bf16hi(x), s1);
     }
-    part[half * 64 + d] = s;
-    __syncthreads();
-    if (t < 64) acc[t] += part[t] + part[64 + t];
+    part[rg * kBD + 2 * cp] = s0;
+    part[rg * kBD + 2 * cp + 1] = s1;
 }
 
-// Stores this thread's 64-column fp32 row `v` (scaled elementwise by `scale`
-// when given) as bf16 to `dst` (128 bytes).
-__device__ __forceinline__ void store_row_bf16(__nv_bfloat16 *dst, const float *v) {
-    uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+// The eight parts of column c summed.
+__device__ __forceinline__ float colsum_total(const float *part, int c) {
+    float s = 0.f;
 #pragma unroll
-    for (int c8 = 0; c8 < 8; ++c8) {
-        uint4 w;
-        w.x = pack_bf16x2(v[8 * c8], v[8 * c8 + 1]);
-        w.y = pack_bf16x2(v[8 * c8 + 2], v[8 * c8 + 3]);
-        w.z = pack_bf16x2(v[8 * c8 + 4], v[8 * c8 + 5]);
-        w.w = pack_bf16x2(v[8 * c8 + 6], v[8 * c8 + 7]);
-        d4[c8] = w;
-    }
+    for (int g = 0; g < 8; ++g) s += part[g * kBD + c];
+    return s;
 }
 
 // Row r, columns c0..c0+31 of a fp32 state as two bf16 parts (hi, then lo =
@@ -195,67 +205,113 @@ __device__ __forceinline__ void store_state32(uint8_t *snap, int r, int c0, cons
     store_snap32<kBD>(snap + kSnap, r, c0, lo);
 }
 
-// psi(x) = phi(x) - 1 (x for x > 0, e^x - 1 otherwise) of a raw bf16 tile into
-// `dst` (same layout), rows >= zero_from as zeros.  Where the inputs are
-// small, phi(x) is close to 1 and its bf16 rounding swamps x; the gradient
-// products use psi and add the row sums of the other factor separately.
-// Same chunk-to-thread assignment as phi_tile, so a thread may apply phi_tile
-// to `raw` right after this without a barrier.
-__device__ __forceinline__ void psi_tile(const uint8_t *raw, uint8_t *dst, int t, int zero_from) {
-    constexpr int CHUNKS = kC * kBD * 2 / 16;
-#pragma unroll 1
-    for (int u0 = t; u0 < CHUNKS; u0 += 4 * kGrp) {
+// sum_c a[c] z[c] over 32 columns, z 16-byte aligned in shared memory.
+__device__ __forceinline__ float dot32(const float *a, const float *z) {
+    float acc = 0.f;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t off = (uint32_t)(u0 + i * kGrp) * 16u;
-            const int row = (int)((off % (kC * 128u)) >> 7);
-            const uint4 w = *reinterpret_cast<const uint4 *>(raw + off);
-            const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-            uint32_t o[4];
+    for (int c4 = 0; c4 < 8; ++c4) {
+        const float4 w = reinterpret_cast<const float4 *>(z)[c4];
+        acc = fmaf(a[4 * c4], w.x, acc);
+        acc = fmaf(a[4 * c4 + 1], w.y, acc);
+        acc = fmaf(a[4 * c4 + 2], w.z, acc);
+        acc = fmaf(a[4 * c4 + 3], w.w, acc);
+    }
+    return acc;
+}
+
+// Columns [c0, c0 + 32) of row r of a swizzled 128 x 64 bf16 tile as fp32.
+__device__ __forceinline__ void tile_row32(const uint8_t *tile, int r, int c0, float *v) {
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float a = bf16lo(ww[u]), b = bf16hi(ww[u]);
-                float ea, eb;
-                asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(ea) : "f"(a * 1.4426950408889634f));
-                asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(eb) : "f"(b * 1.4426950408889634f));
-                o[u] = pack_bf16x2(a > 0.f ? a : ea - 1.f, b > 0.f ? b : eb - 1.f);
-            }
-            *reinterpret_cast<uint4 *>(dst + off) =
-                row >= zero_from ? make_uint4(0u, 0u, 0u, 0u) : make_uint4(o[0], o[1], o[2], o[3]);
+    for (int c8 = 0; c8 < 4; ++c8) {
+        const uint4 w = *reinterpret_cast<const uint4 *>(tile + sw128_offset(r, c0 + 8 * c8));
+        const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            v[8 * c8 + 2 * u] = bf16lo(ww[u]);
+            v[8 * c8 + 2 * u + 1] = bf16hi(ww[u]);
         }
     }
 }
 
-// phi'(x) from the stored bf16 phi(x): 1 where phi > 1 (x > 0), else phi.
-__device__ __forceinline__ float dphi_at(const uint8_t *tile, int r, int c) {
-    return fminf(__bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(tile + sw128_offset(r, c))), 1.f);
+// phi in place on a 128 x 64 bf16 tile by all 256 threads, four 16-byte
+// chunks per thread (rows >= zero_from become zeros).
+__device__ __forceinline__ void phi_tile_all(uint8_t *tile, int t, int zero_from) {
+    uint4 v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = *reinterpret_cast<const uint4 *>(tile + (t + i * kBT) * 16);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        v[i].x = phi_bf16x2(v[i].x);
+        v[i].y = phi_bf16x2(v[i].y);
+        v[i].z = phi_bf16x2(v[i].z);
+        v[i].w = phi_bf16x2(v[i].w);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t off = (uint32_t)(t + i * kBT) * 16u;
+        *reinterpret_cast<uint4 *>(tile + off) = (int)(off >> 7) >= zero_from ? make_uint4(0u, 0u, 0u, 0u) : v[i];
+    }
+}
+
+// psi(x) = phi(x) - 1 (x for x > 0, e^x - 1 otherwise) of a raw bf16 tile into
+// `psi` (same layout) and phi(x) = psi(x) + 1 in place, from one fp32
+// exponential per element; rows >= zero_from as zeros in both.  Where the
+// inputs are small, phi(x) is close to 1 and its bf16 rounding swamps x; the
+// gradient products use psi and add the row sums of the other factor
+// separately.
+__device__ __forceinline__ void psi_phi_tile(uint8_t *tile, uint8_t *psi, int t, int zero_from) {
+    uint4 v[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = *reinterpret_cast<const uint4 *>(tile + (t + i * kBT) * 16);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t off = (uint32_t)(t + i * kBT) * 16u;
+        const uint32_t ww[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+        uint32_t ps[4], ph[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float a = bf16lo(ww[u]), b = bf16hi(ww[u]);
+            float ea, eb;
+            asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(ea) : "f"(a * 1.4426950408889634f));
+            asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(eb) : "f"(b * 1.4426950408889634f));
+            ps[u] = pack_bf16x2(a > 0.f ? a : ea - 1.f, b > 0.f ? b : eb - 1.f);
+            ph[u] = pack_bf16x2(a > 0.f ? a + 1.f : ea, b > 0.f ? b + 1.f : eb);
+        }
+        const bool zero = (int)(off >> 7) >= zero_from;
+        *reinterpret_cast<uint4 *>(psi + off) = zero ? make_uint4(0u, 0u, 0u, 0u) : make_uint4(ps[0], ps[1], ps[2], ps[3]);
+        *reinterpret_cast<uint4 *>(tile + off) = zero ? make_uint4(0u, 0u, 0u, 0u) : make_uint4(ph[0], ph[1], ph[2], ph[3]);
+    }
 }
 
 // ------------------------------------------------------------------ pass 1
 __global__ void __launch_bounds__(kBT, 1)
 bwd_tc_pass1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                    const __grid_constant__ CUtensorMap tm_g, const __grid_constant__ CUtensorMap tm_dq,
                     const BwdArgs args)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
-    const int r = threadIdx.x, q4 = r >> 5;
+    const int tid = threadIdx.x, r = tid & (kC - 1), wg = tid >> 7, q4 = (tid >> 5) & 3;
     const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
     const int bh = blockIdx.x, N = args.N;
     const int nch = (N + kC - 1) / kC;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + kOffBar), *mbar = full + 2;
     uint32_t *slot = reinterpret_cast<uint32_t *>(smem + kOffSlot);
-    uint8_t *gt = smem + kOffGT, *snap = smem + kOffSnap;
+    uint8_t *gt = smem + kOffGT, *psi = smem + kOffPsi, *snap = smem + kOffSnap;
     float *zs = reinterpret_cast<float *>(smem + kOffZ), *part = reinterpret_cast<float *>(smem + kOffPart);
+    float *xr = reinterpret_cast<float *>(smem + kOffX), *xg = xr + 2 * kC, *xa = xg + 2 * kC;
 
     bool ok = (smem_u32(smem) & 1023u) == 0;
-    if (r == 0) {
+    if (tid == 0) {
         if (!ok) record_error(args.err, kErrTimeout);
         mbar_init(&full[0], 1);
         mbar_init(&full[1], 1);
-        mbar_init(mbar, 1);
+        mbar_init(&mbar[0], 1);
+        mbar_init(&mbar[1], 1);
+        mbar_init(&mbar[2], 1);
         fence_mbar_init();
     }
-    if (q4 == 0) {
+    if (tid < 32) {
         tmem_alloc(slot, kBwdTmemCols);
         tmem_relinquish();
     }
@@ -266,71 +322,91 @@ bwd_tc_pass1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     const uint32_t trow = tmem + lane_off;
 
     // the starting state: S (TMEM, fp32; lanes 64-127 unused) and its bf16
-    // snapshot, Z (shared memory, fp32)
+    // snapshot, Z (shared memory, fp32); warpgroup h takes columns 32h..32h+31
     {
         float v[32];
-        for (int c0 = 0; c0 < kBD; c0 += 32) {
+        const int c0 = 32 * wg;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = (r < kBD && args.S0) ? args.S0[((size_t)bh * kBD + r) * kBD + c0 + j] : 0.f;
-            tmem_st32f(trow + kColS + c0, v);
-            if (r < kBD) store_state32(snap, r, c0, v);
-        }
-        if (r < kBD) zs[r] = args.z0 ? args.z0[(size_t)bh * kBD + r] : 0.f;
+        for (int j = 0; j < 32; ++j) v[j] = (r < kBD && args.S0) ? args.S0[((size_t)bh * kBD + r) * kBD + c0 + j] : 0.f;
+        tmem_st32f(trow + kColS + c0, v);
+        if (r < kBD) store_state32(snap, r, c0, v);
+        if (tid < kBD) zs[tid] = args.z0 ? args.z0[(size_t)bh * kBD + tid] : 0.f;
     }
-    if (r == 0 && ok && nch > 0) {
+    if (tid == 0 && ok && nch > 0) {
         prefetch_tmap(&tm_q);
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
         prefetch_tmap(&tm_do);
+        prefetch_tmap(&tm_g);
+        prefetch_tmap(&tm_dq);
         load_chunk(smem, &full[0], &tm_q, &tm_k, &tm_v, &tm_do, 0, bh);
     }
     operands_ready();
 
-    uint32_t phase = 0;
+    uint32_t ph0 = 0, ph1 = 0, ph2 = 0;
     constexpr uint32_t ID_P = idesc_bf16(128, 128, 0, 0);     // K-major A and B
     constexpr uint32_t ID_MN = idesc_bf16(128, kBD, 0, 1);    // K-major A, MN-major B
     constexpr uint32_t ID_KK = idesc_bf16(128, kBD, 0, 0);    // K-major A and B
     constexpr uint32_t ID_S = idesc_bf16(128, kBD, 1, 1);     // MN-major A and B
     for (int it = 0; it < nch && ok; ++it) {
-        BWD_TRACE(it, 0);
-        const int s = it & 1, t0 = it * kC;
+        BWD_TRACE(0, it, 0);
+        const int s = it & 1, t0 = it * kC, rows = min(kC, N - t0);
         uint8_t *st = smem + s * kStage;
         uint8_t *tq = st, *tk = st + kTile, *tv = st + 2 * kTile, *tdo = st + 3 * kTile;
-        // next chunk's tiles into the other stage (freed at the end of the previous chunk)
-        if (r == 0 && it + 1 < nch)
-            load_chunk(smem + (s ^ 1) * kStage, &full[s ^ 1], &tm_q, &tm_k, &tm_v, &tm_do, t0 + kC, bh);
+        const float *zc = zs + kBD * s;   // Z before this chunk
+        float *zn = zs + kBD * (s ^ 1);   // Z after it
         const bool landed = mbar_wait_bounded(&full[s], (it >> 1) & 1, now_ns() + kWaitNs, nullptr);
-        if (!landed && r == 0) record_error(args.err, kErrTimeout);
-        if (!(ok = __syncthreads_and(landed) != 0)) break;
-        // feature map in place (rows past the sequence end become zero), and
+        if (!(ok = barrier_and(landed, args.err))) break;
+        // feature maps in place (rows past the sequence end become zero), and
         // psi(K) = phi(K) - 1 for the dQ product
-        phi_tile<kBD>(tq, r, min(kC, N - t0));
-        psi_tile(tk, smem + kOffPsi, r, min(kC, N - t0));
-        phi_tile<kBD>(tk, r, min(kC, N - t0));
+        phi_tile_all(tq, tid, rows);
+        psi_phi_tile(tk, psi, tid, rows);
         operands_ready();
-        BWD_TRACE(it, 1);
+        BWD_TRACE(0, it, 1);
         const uint32_t aq = smem_u32(tq), ak = smem_u32(tk), av = smem_u32(tv), ag = smem_u32(gt), as = smem_u32(snap);
-        // P = phi(Q) phi(K)^T
-        if (r == 0)
+        // P = phi(Q) phi(K)^T;  S += phi(K)^T V (A read MN-major with M-atom
+        // stride 0: lanes 64-127 repeat lanes 0-63).  Then the next chunk's
+        // tiles into the other stage, once the TMA stores out of it (dQ) and
+        // of the g tile have read their sources.
+        if (tid == 0) {
 #pragma unroll
             for (int ks = 0; ks < kBD / 16; ++ks)
                 mma_f16_ss(tmem + kColP, kmajor_base(aq) + kmajor_step(ks), kmajor_base(ak) + kmajor_step(ks), ID_P, ks > 0);
-        if (!(ok = mma_sync_all(mbar, phase, ok, args.err))) break;
-        BWD_TRACE(it, 2);
-        // mask (j <= i), row sums, A as bf16 hi and lo parts (num feeds e, where
-        // the output's error would enter every entry of A)
-        const float rowsum = mask_to_bf16(trow + kColP, r, true, 0.f, nullptr, true);
-        const float den = rowsum + q_dot_z<kBD>(tq, r, zs);
-        operands_ready();
-        BWD_TRACE(it, 3);
-        // num = A V + phi(Q) S
-        if (r == 0) {
+            const uint64_t da = smem_desc(ak, 0, 1024), db = smem_desc(av, kC * 128, 1024);
+#pragma unroll
+            for (int ks = 0; ks < kC / 16; ++ks)
+                mma_f16_ss(tmem + kColS, da + mnmajor_step(ks), db + mnmajor_step(ks), ID_S, 1);
+            mma_commit(&mbar[0]);
+            tma_store_wait_read0();
+            if (it + 1 < nch) load_chunk(smem + (s ^ 1) * kStage, &full[s ^ 1], &tm_q, &tm_k, &tm_v, &tm_do, t0 + kC, bh);
+        }
+        // meanwhile: the column sums of phi(K), this half of phi(Q_i) . Z
+        colsum_part(tk, nullptr, part);
+        float qz;
+        {
+            float pq[32];
+            tile_row32(tq, r, 32 * wg, pq);
+            qz = dot32(pq, zc + 32 * wg);
+        }
+        bool mine = mma_wait(&mbar[0], ph0);
+        BWD_TRACE(0, it, 2);
+        // mask (j <= i) as bf16 hi and lo parts (num feeds e, where the output's
+        // error would enter every entry of A); the halves of the row sums
+        xr[wg * kC + r] = qz + mask64<true>(trow + kColP, 64 * wg, r, true, 0.f, nullptr, trow + kColPH + 32 * wg,
+                                            trow + kColPL + 32 * wg);
+        if (!(ok = barrier_and(mine, args.err))) break;
+        BWD_TRACE(0, it, 3);
+        if (tid < kBD) zn[tid] = zc[tid] + colsum_total(part, tid);
+        const bool valid = t0 + r < N;
+        const float inv = valid ? 1.f / (xr[r] + xr[kC + r]) : 0.f;
+        // num = P V + phi(Q) S
+        if (tid == 0) {
             const uint64_t dv = smem_desc(av, kC * 128, 1024), ds = smem_desc(as, kBD * 128, 1024);
 #pragma unroll
             for (int part2 = 0; part2 < 2; ++part2)
 #pragma unroll
                 for (int ks = 0; ks < kC / 16; ++ks)
-                    mma_f16_ts(tmem + kColNum, tmem + kColP + 64 * part2 + ks * 8, dv + mnmajor_step(ks), ID_MN,
+                    mma_f16_ts(tmem + kColNum, tmem + (part2 ? kColPL : kColPH) + ks * 8, dv + mnmajor_step(ks), ID_MN,
                                part2 > 0 || ks > 0);
 #pragma unroll
             for (int part2 = 0; part2 < 2; ++part2)
@@ -338,135 +414,130 @@ bwd_tc_pass1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 for (int ks = 0; ks < kBD / 16; ++ks)
                     mma_f16_ss(tmem + kColNum, kmajor_base(aq) + kmajor_step(ks),
                                ds + (uint64_t)(part2 * kSnap / 16) + mnmajor_step(ks), ID_MN, 1);
+            mma_commit(&mbar[1]);
         }
-        if (!(ok = mma_sync_all(mbar, phase, ok, args.err))) break;
-        BWD_TRACE(it, 4);
-        // g_i = dO_i / den_i, e_i = -(g_i . num_i) / den_i; g as bf16 into the
-        // operand tile and the workspace, e into the workspace
-        const bool valid = t0 + r < N;
-        float e = 0.f;
-        {
-            float num[64], g[64];
-            tmem_ld32f(trow + kColNum, *reinterpret_cast<float(*)[32]>(num));
-            tmem_ld32f(trow + kColNum + 32, *reinterpret_cast<float(*)[32]>(num + 32));
-            const float inv = valid ? 1.f / den : 0.f;
-            float gn = 0.f;
+        // meanwhile g_i = dO_i / den_i (columns 32h..32h+31 by warpgroup h),
+        // rounded to bf16 as the MMAs (and pass 2) use it, into the operand tile
+        float g[32];
+        tile_row32(tdo, r, 32 * wg, g);
 #pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8) {
-                const uint4 w = *reinterpret_cast<const uint4 *>(tdo + sw128_offset(r, 8 * c8));
-                const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    g[8 * c8 + 2 * u] = bf16lo(ww[u]) * inv;
-                    g[8 * c8 + 2 * u + 1] = bf16hi(ww[u]) * inv;
-                }
-            }
-            // the MMAs (and pass 2) use g rounded to bf16; e is formed from that same
-            // g, so that the terms A phi(K), g S^T and e Z stay consistent
-#pragma unroll
-            for (int c = 0; c < 64; ++c) g[c] = __bfloat162float(__float2bfloat16_rn(g[c]));
-#pragma unroll
-            for (int c0 = 0; c0 < 64; c0 += 32) store_snap32<kC>(gt, r, c0, g + c0);
-#pragma unroll
-            for (int c = 0; c < 64; ++c) gn = fmaf(g[c], num[c], gn);
-            e = valid ? -gn * inv : 0.f;
-            if (valid) {
-                store_row_bf16(args.g_ws + ((size_t)bh * N + t0 + r) * kBD, g);
-                args.e_ws[(size_t)bh * N + t0 + r] = e;
-            }
-        }
+        for (int c = 0; c < 32; ++c) g[c] = __bfloat162float(__float2bfloat16_rn(g[c] * inv));
+        store_snap32<kC>(gt, r, 32 * wg, g);
         operands_ready();
-        BWD_TRACE(it, 5);
-        // A2 = g V^T
-        if (r == 0)
+        // g to the workspace (rows past the end are not written); A2 = g V^T
+        // and the g S^T part of dphi(Q)
+        if (tid == 0) {
+            tma_store_3d(&tm_g, gt, 0, t0, bh);
+            tma_store_commit();
 #pragma unroll
             for (int ks = 0; ks < kBD / 16; ++ks)
                 mma_f16_ss(tmem + kColP, kmajor_base(ag) + kmajor_step(ks), kmajor_base(av) + kmajor_step(ks), ID_P, ks > 0);
-        if (!(ok = mma_sync_all(mbar, phase, ok, args.err))) break;
-        BWD_TRACE(it, 6);
-        // A = (A2 + e_i) masked to j <= i, as bf16; asum its fp32 row sum
-        const float asum = mask_to_bf16(trow + kColP, r, true, e, nullptr);
-        operands_ready();
-        BWD_TRACE(it, 7);
-        // dphi(Q) = A psi(K) + g S^T  (+ asum: the product with the 1 of phi = psi + 1)
-        if (r == 0) {
-            const uint64_t dk = smem_desc(smem_u32(smem + kOffPsi), kC * 128, 1024);
-#pragma unroll
-            for (int ks = 0; ks < kC / 16; ++ks)
-                mma_f16_ts(tmem + kColDQ, tmem + kColP + ks * 8, dk + mnmajor_step(ks), ID_MN, ks > 0);
+            mma_commit(&mbar[2]);
 #pragma unroll
             for (int part2 = 0; part2 < 2; ++part2)
 #pragma unroll
                 for (int ks = 0; ks < kBD / 16; ++ks)
                     mma_f16_ss(tmem + kColDQ, kmajor_base(ag) + kmajor_step(ks),
-                               kmajor_base(as + part2 * kSnap) + kmajor_step(ks, kBD), ID_KK, 1);
+                               kmajor_base(as + part2 * kSnap) + kmajor_step(ks, kBD), ID_KK, part2 > 0 || ks > 0);
         }
-        if (!(ok = mma_sync_all(mbar, phase, ok, args.err))) break;
-        BWD_TRACE(it, 8);
-        // dQ = (dphi(Q) + e_i Z) * phi'(Q)
+        // e_i = -(g_i . num_i) / den_i, from the same bf16 g, so that the terms
+        // A phi(K), g S^T and e Z stay consistent
+        mine = mma_wait(&mbar[1], ph1);
+        BWD_TRACE(0, it, 4);
         {
-            float dq[64];
-            tmem_ld32f(trow + kColDQ, *reinterpret_cast<float(*)[32]>(dq));
-            tmem_ld32f(trow + kColDQ + 32, *reinterpret_cast<float(*)[32]>(dq + 32));
+            float num[32];
+            tmem_ld32f(trow + kColNum + 32 * wg, num);
+            float gn = 0.f;
 #pragma unroll
-            for (int c = 0; c < 64; ++c) dq[c] = (fmaf(e, zs[c], dq[c]) + asum) * dphi_at(tq, r, c);
-            if (valid) store_row_bf16(args.dq + ((size_t)bh * N + t0 + r) * kBD, dq);
+            for (int c = 0; c < 32; ++c) gn = fmaf(g[c], num[c], gn);
+            xg[wg * kC + r] = gn;
         }
-        __syncthreads();   // every thread has read Z before it changes
-        // S += phi(K)^T V (A read MN-major with M-atom stride 0: lanes 64-127
-        // repeat lanes 0-63), Z += column sums of phi(K)
-        if (r == 0) {
-            const uint64_t da = smem_desc(ak, 0, 1024), db = smem_desc(av, kC * 128, 1024);
+        if (!(ok = barrier_and(mine, args.err))) break;
+        const float e = valid ? -(xg[r] + xg[kC + r]) * inv : 0.f;
+        if (wg == 0 && valid) args.e_ws[(size_t)bh * N + t0 + r] = e;
+        mine = mma_wait(&mbar[2], ph2);
+        BWD_TRACE(0, it, 5);
+        // A = (A2 + e_i) masked to j <= i, as bf16; the halves of its row sum
+        xa[wg * kC + r] = mask64<false>(trow + kColP, 64 * wg, r, true, e, nullptr, trow + kColPH + 32 * wg, 0u);
+        if (!(ok = barrier_and(mine, args.err))) break;
+        BWD_TRACE(0, it, 6);
+        const float asum = xa[r] + xa[kC + r];
+        // dphi(Q) += A psi(K)  (+ asum: the product with the 1 of phi = psi + 1)
+        if (tid == 0) {
+            const uint64_t dk = smem_desc(smem_u32(psi), kC * 128, 1024);
 #pragma unroll
             for (int ks = 0; ks < kC / 16; ++ks)
-                mma_f16_ss(tmem + kColS, da + mnmajor_step(ks), db + mnmajor_step(ks), ID_S, 1);
+                mma_f16_ts(tmem + kColDQ, tmem + kColPH + ks * 8, dk + mnmajor_step(ks), ID_MN, 1);
+            mma_commit(&mbar[0]);
         }
-        colsum_add(tk, nullptr, part, zs);
-        if (!(ok = mma_sync_all(mbar, phase, ok, args.err))) break;
-        BWD_TRACE(it, 9);
-        // the new state's bf16 snapshot for the next chunk
-        if (r < kBD) {
-            float v[32];
-            for (int c0 = 0; c0 < kBD; c0 += 32) {
-                tmem_ld32f(trow + kColS + c0, v);
-                store_state32(snap, r, c0, v);
+        mine = mma_wait(&mbar[0], ph0);
+        BWD_TRACE(0, it, 7);
+        // dQ = (dphi(Q) + e_i Z) * phi'(Q), phi' = min(phi, 1), into the dO tile
+        // (its last reader has finished) for the TMA store; the new state's
+        // bf16 snapshot for the next chunk
+        {
+            float dq[32], pq[32];
+            tmem_ld32f(trow + kColDQ + 32 * wg, dq);
+            tile_row32(tq, r, 32 * wg, pq);
+            const float4 *z4 = reinterpret_cast<const float4 *>(zc + 32 * wg);
+#pragma unroll
+            for (int c4 = 0; c4 < 8; ++c4) {
+                const float4 z = z4[c4];
+                dq[4 * c4] = (fmaf(e, z.x, dq[4 * c4]) + asum) * fminf(pq[4 * c4], 1.f);
+                dq[4 * c4 + 1] = (fmaf(e, z.y, dq[4 * c4 + 1]) + asum) * fminf(pq[4 * c4 + 1], 1.f);
+                dq[4 * c4 + 2] = (fmaf(e, z.z, dq[4 * c4 + 2]) + asum) * fminf(pq[4 * c4 + 2], 1.f);
+                dq[4 * c4 + 3] = (fmaf(e, z.w, dq[4 * c4 + 3]) + asum) * fminf(pq[4 * c4 + 3], 1.f);
+            }
+            store_snap32<kC>(tdo, r, 32 * wg, dq);
+            if (q4 < 2) {
+                float v[32];
+                tmem_ld32f(trow + kColS + 32 * wg, v);
+                store_state32(snap, r, 32 * wg, v);
             }
         }
-        operands_ready();   // also: every thread is done with this stage
-        BWD_TRACE(it, 10);
+        if (!(ok = barrier_and(mine, args.err))) break;   // also: every thread is done with this stage
+        if (tid == 0) {
+            tma_store_3d(&tm_dq, tdo, 0, t0, bh);
+            tma_store_commit();
+        }
+        BWD_TRACE(0, it, 8);
     }
+    if (tid == 0) tma_store_wait_all0();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (q4 == 0) tmem_dealloc(tmem, kBwdTmemCols);
+    if (tid < 32) tmem_dealloc(tmem, kBwdTmemCols);
 }
 
 // ------------------------------------------------------------------ pass 2
 __global__ void __launch_bounds__(kBT, 1)
 bwd_tc_pass2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
+                    const __grid_constant__ CUtensorMap tm_dk, const __grid_constant__ CUtensorMap tm_dv,
                     const BwdArgs args)
 {
     extern __shared__ __align__(1024) uint8_t smem[];
-    const int r = threadIdx.x, q4 = r >> 5;
+    const int tid = threadIdx.x, r = tid & (kC - 1), wg = tid >> 7, q4 = (tid >> 5) & 3;
     const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
     const int bh = blockIdx.x, N = args.N;
     const int nch = (N + kC - 1) / kC;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + kOffBar), *mbar = full + 2;
     uint32_t *slot = reinterpret_cast<uint32_t *>(smem + kOffSlot);
-    uint8_t *snap = smem + kOffSnap;
+    uint8_t *psi = smem + kOffPsi, *snap = smem + kOffSnap;
     float *rs = reinterpret_cast<float *>(smem + kOffZ), *es = reinterpret_cast<float *>(smem + kOffE);
-    float *part = reinterpret_cast<float *>(smem + kOffPart);
+    float *part = reinterpret_cast<float *>(smem + kOffPart), *xa = reinterpret_cast<float *>(smem + kOffX);
 
     bool ok = (smem_u32(smem) & 1023u) == 0;
-    if (r == 0) {
+    if (tid == 0) {
         if (!ok) record_error(args.err, kErrTimeout);
         mbar_init(&full[0], 1);
         mbar_init(&full[1], 1);
-        mbar_init(mbar, 1);
+        mbar_init(&mbar[0], 1);
+        mbar_init(&mbar[1], 1);
+        mbar_init(&mbar[2], 1);
         fence_mbar_init();
     }
-    if (q4 == 0) {
+    if (tid < 32) {
         tmem_alloc(slot, kBwdTmemCols);
         tmem_relinquish();
     }
@@ -479,60 +550,87 @@ bwd_tc_pass2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     // R, r start from the gradient reaching the final state (or zero)
     {
         float v[32];
-        for (int c0 = 0; c0 < kBD; c0 += 32) {
+        const int c0 = 32 * wg;
 #pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = (r < kBD && args.dSN) ? args.dSN[((size_t)bh * kBD + r) * kBD + c0 + j] : 0.f;
-            tmem_st32f(trow + kColR + c0, v);
-            if (r < kBD) store_state32(snap, r, c0, v);
-        }
-        if (r < kBD) rs[r] = args.dzN ? args.dzN[(size_t)bh * kBD + r] : 0.f;
+        for (int j = 0; j < 32; ++j) v[j] = (r < kBD && args.dSN) ? args.dSN[((size_t)bh * kBD + r) * kBD + c0 + j] : 0.f;
+        tmem_st32f(trow + kColR + c0, v);
+        if (r < kBD) store_state32(snap, r, c0, v);
+        if (tid < kBD) rs[tid] = args.dzN ? args.dzN[(size_t)bh * kBD + tid] : 0.f;
     }
-    if (r == 0 && ok && nch > 0) {
+    if (tid == 0 && ok && nch > 0) {
         prefetch_tmap(&tm_q);
         prefetch_tmap(&tm_k);
         prefetch_tmap(&tm_v);
         prefetch_tmap(&tm_g);
+        prefetch_tmap(&tm_dk);
+        prefetch_tmap(&tm_dv);
         load_chunk(smem, &full[0], &tm_q, &tm_k, &tm_v, &tm_g, (nch - 1) * kC, bh);
     }
     operands_ready();
 
-    uint32_t phase = 0;
+    uint32_t ph0 = 0, ph1 = 0, ph2 = 0;
     constexpr uint32_t ID_P = idesc_bf16(128, 128, 0, 0);
     constexpr uint32_t ID_MN = idesc_bf16(128, kBD, 0, 1);
     constexpr uint32_t ID_KK = idesc_bf16(128, kBD, 0, 0);
     constexpr uint32_t ID_S = idesc_bf16(128, kBD, 1, 1);
     for (int it = 0; it < nch && ok; ++it) {
-        const int c = nch - 1 - it, s = it & 1, t0 = c * kC;
+        BWD_TRACE(1, it, 0);
+        const int c = nch - 1 - it, s = it & 1, t0 = c * kC, rows = min(kC, N - t0);
         uint8_t *st = smem + s * kStage;
         uint8_t *tq = st, *tk = st + kTile, *tv = st + 2 * kTile, *tg = st + 3 * kTile;
-        if (r == 0 && it + 1 < nch)
-            load_chunk(smem + (s ^ 1) * kStage, &full[s ^ 1], &tm_q, &tm_k, &tm_v, &tm_g, t0 - kC, bh);
-        es[r] = t0 + r < N ? args.e_ws[(size_t)bh * N + t0 + r] : 0.f;
+        const float *rc = rs + kBD * s;   // r after this chunk (the reverse sum of the later ones)
+        float *rn = rs + kBD * (s ^ 1);   // r including this chunk
+        if (wg == 0) es[r] = t0 + r < N ? args.e_ws[(size_t)bh * N + t0 + r] : 0.f;
         const bool landed = mbar_wait_bounded(&full[s], (it >> 1) & 1, now_ns() + kWaitNs, nullptr);
-        if (!landed && r == 0) record_error(args.err, kErrTimeout);
-        if (!(ok = __syncthreads_and(landed) != 0)) break;
-        psi_tile(tq, smem + kOffPsi, r, min(kC, N - t0));
-        phi_tile<kBD>(tq, r, min(kC, N - t0));
-        phi_tile<kBD>(tk, r, min(kC, N - t0));
+        if (!(ok = barrier_and(landed, args.err))) break;
+        psi_phi_tile(tq, psi, tid, rows);
+        phi_tile_all(tk, tid, rows);
         operands_ready();
+        BWD_TRACE(1, it, 1);
         const uint32_t aq = smem_u32(tq), ak = smem_u32(tk), av = smem_u32(tv), ag = smem_u32(tg), as = smem_u32(snap);
-        // P^T = phi(K) phi(Q)^T and A^T = V g^T (rows j, columns i)
-        if (r == 0) {
+        // P^T = phi(K) phi(Q)^T, then A^T = V g^T (rows j, columns i) and
+        // R += phi(Q)^T g (A read MN-major, M-atom stride 0); then the next
+        // chunk's tiles into the other stage, once the TMA stores out of it
+        // (dV, dK) have read their sources
+        if (tid == 0) {
 #pragma unroll
             for (int ks = 0; ks < kBD / 16; ++ks)
                 mma_f16_ss(tmem + kColP, kmajor_base(ak) + kmajor_step(ks), kmajor_base(aq) + kmajor_step(ks), ID_P, ks > 0);
+            mma_commit(&mbar[0]);
 #pragma unroll
             for (int ks = 0; ks < kBD / 16; ++ks)
                 mma_f16_ss(tmem + kColA2, kmajor_base(av) + kmajor_step(ks), kmajor_base(ag) + kmajor_step(ks), ID_P, ks > 0);
+            const uint64_t da = smem_desc(aq, 0, 1024), db = smem_desc(ag, kC * 128, 1024);
+#pragma unroll
+            for (int ks = 0; ks < kC / 16; ++ks)
+                mma_f16_ss(tmem + kColR, da + mnmajor_step(ks), db + mnmajor_step(ks), ID_S, 1);
+            mma_commit(&mbar[1]);
+            tma_store_wait_read0();
+            if (it + 1 < nch) load_chunk(smem + (s ^ 1) * kStage, &full[s ^ 1], &tm_q, &tm_k, &tm_v, &tm_g, t0 - kC, bh);
         }
-        if (!(ok = mma_sync_all(mbar, phase, ok, args.err))) break;
-        // masks (i >= j), e_i added to the kept entries of A^T; both as bf16
-        mask_to_bf16(trow + kColP, r, false, 0.f, nullptr);
-        const float asum = mask_to_bf16(trow + kColA2, r, false, 0.f, es);
-        operands_ready();
+        // meanwhile the column sums sum_i e_i phi(Q_i)
+        colsum_part(tq, es, part);
+        // masks (i >= j) as bf16: warpgroup 0 P^T, warpgroup 1 A^T with e_i
+        // added to the kept entries (and its row sums)
+        bool mine = mma_wait(&mbar[0], ph0);
+        if (wg == 0) {
+            mask64<false>(trow + kColP, 0, r, false, 0.f, nullptr, trow + kColP, 0u);
+            mask64<false>(trow + kColP, 64, r, false, 0.f, nullptr, trow + kColP + 32, 0u);
+        }
+        mine = mma_wait(&mbar[1], ph1) && mine;
+        BWD_TRACE(1, it, 2);
+        if (wg == 1) {
+            float a = mask64<false>(trow + kColA2, 0, r, false, 0.f, es, trow + kColA2, 0u);
+            a += mask64<false>(trow + kColA2, 64, r, false, 0.f, es, trow + kColA2 + 32, 0u);
+            xa[r] = a;
+        }
+        if (!(ok = barrier_and(mine, args.err))) break;
+        BWD_TRACE(1, it, 3);
+        if (tid < kBD) rn[tid] = rc[tid] + colsum_total(part, tid);
+        const float asum = xa[r];
         // dV = P^T g + phi(K) R;  dphi(K) = A^T psi(Q) + V R^T (+ asum)
-        if (r == 0) {
-            const uint64_t dg = smem_desc(ag, kC * 128, 1024), dqm = smem_desc(smem_u32(smem + kOffPsi), kC * 128, 1024);
+        if (tid == 0) {
+            const uint64_t dg = smem_desc(ag, kC * 128, 1024), dqm = smem_desc(smem_u32(psi), kC * 128, 1024);
             const uint64_t ds = smem_desc(as, kBD * 128, 1024);
 #pragma unroll
             for (int ks = 0; ks < kC / 16; ++ks)
@@ -543,6 +641,7 @@ bwd_tc_pass2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 for (int ks = 0; ks < kBD / 16; ++ks)
                     mma_f16_ss(tmem + kColDV, kmajor_base(ak) + kmajor_step(ks),
                                ds + (uint64_t)(part2 * kSnap / 16) + mnmajor_step(ks), ID_MN, 1);
+            mma_commit(&mbar[2]);
 #pragma unroll
             for (int ks = 0; ks < kC / 16; ++ks)
                 mma_f16_ts(tmem + kColDK, tmem + kColA2 + ks * 8, dqm + mnmajor_step(ks), ID_MN, ks > 0);
@@ -552,53 +651,60 @@ bwd_tc_pass2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 for (int ks = 0; ks < kBD / 16; ++ks)
                     mma_f16_ss(tmem + kColDK, kmajor_base(av) + kmajor_step(ks),
                                kmajor_base(as + part2 * kSnap) + kmajor_step(ks, kBD), ID_KK, 1);
+            mma_commit(&mbar[0]);
         }
-        if (!(ok = mma_sync_all(mbar, phase, ok, args.err))) break;
+        // dV into the V tile (its last reader, the dphi(K) product, runs after
+        // dV's: wait for both before writing), dK = (dphi(K) + r + asum) * phi'(K)
+        // into the g tile (columns 32h..32h+31 by warpgroup h); the new R's
+        // bf16 snapshot
+        float x[32];
+        mine = mma_wait(&mbar[2], ph2) && mine;
+        BWD_TRACE(1, it, 4);
+        tmem_ld32f(trow + kColDV + 32 * wg, x);
+        mine = mma_wait(&mbar[0], ph0) && mine;
+        BWD_TRACE(1, it, 5);
+        store_snap32<kC>(tv, r, 32 * wg, x);
         {
-            const bool valid = t0 + r < N;
-            float x[64];
-            tmem_ld32f(trow + kColDV, *reinterpret_cast<float(*)[32]>(x));
-            tmem_ld32f(trow + kColDV + 32, *reinterpret_cast<float(*)[32]>(x + 32));
-            if (valid) store_row_bf16(args.dv + ((size_t)bh * N + t0 + r) * kBD, x);
-            tmem_ld32f(trow + kColDK, *reinterpret_cast<float(*)[32]>(x));
-            tmem_ld32f(trow + kColDK + 32, *reinterpret_cast<float(*)[32]>(x + 32));
+            float pk[32];
+            tmem_ld32f(trow + kColDK + 32 * wg, x);
+            tile_row32(tk, r, 32 * wg, pk);
+            const float4 *r4 = reinterpret_cast<const float4 *>(rc + 32 * wg);
 #pragma unroll
-            for (int cc = 0; cc < 64; ++cc) x[cc] = (x[cc] + rs[cc] + asum) * dphi_at(tk, r, cc);
-            if (valid) store_row_bf16(args.dk + ((size_t)bh * N + t0 + r) * kBD, x);
-        }
-        __syncthreads();   // every thread has read r before it changes
-        // R += phi(Q)^T g (A read MN-major, M-atom stride 0), r += sum_i e_i phi(Q_i)
-        if (r == 0) {
-            const uint64_t da = smem_desc(aq, 0, 1024), db = smem_desc(ag, kC * 128, 1024);
-#pragma unroll
-            for (int ks = 0; ks < kC / 16; ++ks)
-                mma_f16_ss(tmem + kColR, da + mnmajor_step(ks), db + mnmajor_step(ks), ID_S, 1);
-        }
-        colsum_add(tq, es, part, rs);
-        if (!(ok = mma_sync_all(mbar, phase, ok, args.err))) break;
-        if (r < kBD) {
-            float v[32];
-            for (int c0 = 0; c0 < kBD; c0 += 32) {
-                tmem_ld32f(trow + kColR + c0, v);
-                store_state32(snap, r, c0, v);
+            for (int c4 = 0; c4 < 8; ++c4) {
+                const float4 rv = r4[c4];
+                x[4 * c4] = (x[4 * c4] + rv.x + asum) * fminf(pk[4 * c4], 1.f);
+                x[4 * c4 + 1] = (x[4 * c4 + 1] + rv.y + asum) * fminf(pk[4 * c4 + 1], 1.f);
+                x[4 * c4 + 2] = (x[4 * c4 + 2] + rv.z + asum) * fminf(pk[4 * c4 + 2], 1.f);
+                x[4 * c4 + 3] = (x[4 * c4 + 3] + rv.w + asum) * fminf(pk[4 * c4 + 3], 1.f);
+            }
+            store_snap32<kC>(tg, r, 32 * wg, x);
+            if (q4 < 2) {
+                float v[32];
+                tmem_ld32f(trow + kColR + 32 * wg, v);
+                store_state32(snap, r, 32 * wg, v);
             }
         }
-        operands_ready();
+        if (!(ok = barrier_and(mine, args.err))) break;   // also: every thread is done with this stage
+        if (tid == 0) {
+            tma_store_3d(&tm_dv, tv, 0, t0, bh);
+            tma_store_3d(&tm_dk, tg, 0, t0, bh);
+            tma_store_commit();
+        }
+        BWD_TRACE(1, it, 6);
     }
     // dL/dS_0 = R, dL/dZ_0 = r after the first chunk
     if (ok && args.dS0 && r < kBD) {
         float v[32];
-        for (int c0 = 0; c0 < kBD; c0 += 32) {
-            tmem_ld32f(trow + kColR + c0, v);
+        tmem_ld32f(trow + kColR + 32 * wg, v);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) args.dS0[((size_t)bh * kBD + r) * kBD + c0 + j] = v[j];
-        }
-        args.dz0[(size_t)bh * kBD + r] = rs[r];
+        for (int j = 0; j < 32; ++j) args.dS0[((size_t)bh * kBD + r) * kBD + 32 * wg + j] = v[j];
+        if (wg == 0) args.dz0[(size_t)bh * kBD + r] = rs[kBD * (nch & 1) + r];
     }
+    if (tid == 0) tma_store_wait_all0();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (q4 == 0) tmem_dealloc(tmem, kBwdTmemCols);
+    if (tid < 32) tmem_dealloc(tmem, kBwdTmemCols);
 }
 
 }  // namespace
@@ -612,17 +718,16 @@ cudaError_t tc_causal_backward(const BwdProblem &p, const DeviceInfo &dev) {
     if (p.ws_bytes < g_bytes + (size_t)p.BH * p.N * 4) return cudaErrorInvalidValue;
     __nv_bfloat16 *g_ws = (__nv_bfloat16 *)p.ws;
     float *e_ws = (float *)((uint8_t *)p.ws + g_bytes);
-    CUtensorMap tq, tk, tv, tdo, tg;
+    CUtensorMap tq, tk, tv, tdo, tg, tdq, tdk, tdv;
     if (!cached_tmap_bf16_3d(&tq, p.q, kBD, p.N, p.BH, 64, kC) || !cached_tmap_bf16_3d(&tk, p.k, kBD, p.N, p.BH, 64, kC) ||
         !cached_tmap_bf16_3d(&tv, p.v, kBD, p.N, p.BH, 64, kC) ||
         !cached_tmap_bf16_3d(&tdo, p.dout, kBD, p.N, p.BH, 64, kC) ||
-        !cached_tmap_bf16_3d(&tg, g_ws, kBD, p.N, p.BH, 64, kC))
+        !cached_tmap_bf16_3d(&tg, g_ws, kBD, p.N, p.BH, 64, kC) ||
+        !cached_tmap_bf16_3d(&tdq, p.dq, kBD, p.N, p.BH, 64, kC) ||
+        !cached_tmap_bf16_3d(&tdk, p.dk, kBD, p.N, p.BH, 64, kC) ||
+        !cached_tmap_bf16_3d(&tdv, p.dv, kBD, p.N, p.BH, 64, kC))
         return cudaErrorInvalidValue;
     BwdArgs a;
-    a.dq = (__nv_bfloat16 *)p.dq;
-    a.dk = (__nv_bfloat16 *)p.dk;
-    a.dv = (__nv_bfloat16 *)p.dv;
-    a.g_ws = g_ws;
     a.e_ws = e_ws;
     a.S0 = p.S0;
     a.z0 = p.z0;
@@ -635,10 +740,10 @@ cudaError_t tc_causal_backward(const BwdProblem &p, const DeviceInfo &dev) {
     cudaError_t e;
     if ((e = set_smem(bwd_tc_pass1_kernel, kBwdSmem)) != cudaSuccess) return e;
     if ((e = set_smem(bwd_tc_pass2_kernel, kBwdSmem)) != cudaSuccess) return e;
-    bwd_tc_pass1_kernel<<<(unsigned)p.BH, kBT, kBwdSmem, p.stream>>>(tq, tk, tv, tdo, a);
+    bwd_tc_pass1_kernel<<<(unsigned)p.BH, kBT, kBwdSmem, p.stream>>>(tq, tk, tv, tdo, tg, tdq, a);
     count_launches(1);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    bwd_tc_pass2_kernel<<<(unsigned)p.BH, kBT, kBwdSmem, p.stream>>>(tq, tk, tv, tg, a);
+    bwd_tc_pass2_kernel<<<(unsigned)p.BH, kBT, kBwdSmem, p.stream>>>(tq, tk, tv, tg, tdk, tdv, a);
     count_launches(1);
     return cudaGetLastError();
 }
