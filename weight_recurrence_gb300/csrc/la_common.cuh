@@ -28,6 +28,14 @@ __device__ __forceinline__ void record_error(int *err, int code) {
     if (err) atomicCAS(err, 0, code);
 }
 
+// Programmatic dependent launch: pdl_wait() returns once the grids this
+// launch depends on have completed and their writes are visible (at once for
+// a launch without such a dependency); pdl_launch_dependents() lets the next
+// launch on the stream be scheduled (its own pdl_wait() still waits for this
+// grid to complete).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

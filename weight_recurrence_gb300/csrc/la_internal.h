@@ -105,6 +105,34 @@ bool tc_variant_route(const la_shape &s, const la_variant &v, Problem &p);
 bool tc_delta_supported(const la_shape &s, const la_variant &v);
 cudaError_t tc_delta(const Problem &p, const void *beta, const la_variant &v, const DeviceInfo &dev);
 
+// Launches `kernel` with programmatic stream serialization, so that its
+// set-up overlaps the tail of the previous launch on the stream: every such
+// kernel calls pdl_wait() before its first global-memory access.  cluster_x
+// > 0 also sets a cluster shape (cluster_x, 1, 1) (a cluster kernel keeps its
+// cluster launch even at one CTA per cluster).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                       unsigned cluster_x, Args &&...args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.numAttrs = 1;
+    if (cluster_x > 0) {
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = cluster_x;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
+    }
+    cfg.attrs = attr;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<Args &&>(args)...);
+}
+
 // Counts kernel launches made through the library (la_api.cu).
 void count_launches(int n);
 

@@ -228,6 +228,8 @@ decode_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
     const long long h = blockIdx.x;
     const int tid = threadIdx.x;
     const int c4 = tid % C4, r = tid / C4;
+    pdl_launch_dependents();
+    pdl_wait();
 
     float4 s[NR];
     float4 *Sh = reinterpret_cast<float4 *>(S + h * D * M);
@@ -287,10 +289,10 @@ decode_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
 
 template <typename T, int D, int M>
 cudaError_t launch_decode(const Problem &p) {
-    decode_kernel<T, D, M><<<(unsigned)p.BH, kThreads, 0, p.stream>>>(
-        (const T *)p.q, (const T *)p.k, (const T *)p.v, (T *)p.out, p.S, p.z);
+    const cudaError_t e = launch_pdl(decode_kernel<T, D, M>, dim3((unsigned)p.BH), dim3(kThreads), 0, p.stream, 0u,
+                                     (const T *)p.q, (const T *)p.k, (const T *)p.v, (T *)p.out, p.S, p.z);
     count_launches(1);
-    return cudaGetLastError();
+    return e;
 }
 
 template <typename T, int D>
@@ -380,6 +382,8 @@ decode_steps_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *_
     const long long h = blockIdx.x;
     const int tid = threadIdx.x;
     const int c4 = tid % C4, r = tid / C4;
+    pdl_launch_dependents();
+    pdl_wait();
     const int nsteps = steps ? max(0, min(Tn, steps[h / H])) : Tn;
 
     float4 s[NR];
@@ -469,10 +473,11 @@ decode_steps_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *_
 
 template <typename T, int D, int M>
 cudaError_t launch_decode_steps(const Problem &p, const int *steps, int Tn) {
-    decode_steps_kernel<T, D, M><<<(unsigned)p.BH, kThreads, 0, p.stream>>>(
-        (const T *)p.q, (const T *)p.k, (const T *)p.v, (T *)p.out, p.S, p.z, steps, Tn, p.BH, p.H > 0 ? p.H : 1);
+    const cudaError_t e = launch_pdl(decode_steps_kernel<T, D, M>, dim3((unsigned)p.BH), dim3(kThreads), 0, p.stream,
+                                     0u, (const T *)p.q, (const T *)p.k, (const T *)p.v, (T *)p.out, p.S, p.z, steps,
+                                     Tn, p.BH, (int)(p.H > 0 ? p.H : 1));
     count_launches(1);
-    return cudaGetLastError();
+    return e;
 }
 
 template <typename T, int D>

@@ -189,11 +189,10 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     volatile int *abort = reinterpret_cast<volatile int *>(smem + C::OFF_TSLOT + 4);
 
     const int bh = blockIdx.x / args.nseg, seg = blockIdx.x % args.nseg;
-    // this head's sequence length (rows past it are read but ignored)
-    const int Nseq = args.lens ? max(0, min(args.N, args.lens[bh / args.H])) : args.N;
-    const int nch_total = (Nseq + kC - 1) / kC;
     const int c_begin = seg * args.cps;
-    const int n = max(0, min(nch_total, c_begin + args.cps) - c_begin);
+    // the next launch on the stream may start its own set-up now (it reads
+    // nothing of ours before its griddepcontrol.wait)
+    pdl_launch_dependents();
 
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
     uint64_t *full = bar, *empty = bar + C::NS, *phi_done = bar + 2 * C::NS;
@@ -258,6 +257,13 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     tc_fence_after();
     const uint32_t tmem = *tslot;
     if (tid == 0) LA_TRACE_AT(0, 63, 1);
+    // everything above touched no global memory; from here on the previous
+    // launch on the stream has completed and its writes are visible
+    pdl_wait();
+    // this head's sequence length (rows past it are read but ignored)
+    const int Nseq = args.lens ? max(0, min(args.N, args.lens[bh / args.H])) : args.N;
+    const int nch_total = (Nseq + kC - 1) / kC;
+    const int n = max(0, min(nch_total, c_begin + args.cps) - c_begin);
 
     // Test hook: wait on a barrier that nothing arrives on, then give up.
     if (args.inject_ns && tid == 0) {
@@ -814,6 +820,7 @@ state_reduce_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     volatile int *abort = reinterpret_cast<volatile int *>(smem + C::OFF_TSLOT + 4);
+    pdl_launch_dependents();
     const int bh = blockIdx.x / args.nred, sp = blockIdx.x % args.nred;
     const int nch_total = (args.N + kC - 1) / kC;
     const int c_begin = sp * args.cps;
@@ -850,6 +857,7 @@ state_reduce_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
+    pdl_wait();   // set-up above touched no global memory
 
     if (warp == 0) {
         if (lane == 0 && !*abort) {
@@ -1022,6 +1030,7 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     volatile int *abort = reinterpret_cast<volatile int *>(smem + C::OFF_TSLOT + 4);
+    pdl_launch_dependents();
     const int bh = blockIdx.x / args.G, g = blockIdx.x % args.G;
     const int nch_total = (args.N + kC - 1) / kC;
     const int c_begin = g * args.cps;
@@ -1066,6 +1075,7 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
+    pdl_wait();   // set-up above touched no global memory
     const bool epi = warp >= 2 && warp < 6;
     // every thread arrives on the cluster barrier exactly once; the epilogue
     // group only after its partial sums are in the workspace
@@ -1353,9 +1363,10 @@ cudaError_t launch_causal(const Problem &p, const DeviceInfo &dev) {
         if (p.ws_bytes < (size_t)p.BH * nseg * (D * M + D) * sizeof(float)) return cudaErrorInvalidValue;
         ReduceArgs r{(float *)p.ws, p.S, p.z, p.N, nseg, nseg - 1, cps, nseg - 1, dev.err_word};
         if ((e = set_smem(state_reduce_kernel<D, M>, RCfg<D, M>::SMEM)) != cudaSuccess) return e;
-        state_reduce_kernel<D, M><<<(unsigned)(p.BH * (nseg - 1)), kThreads, RCfg<D, M>::SMEM, p.stream>>>(tk, tv, r);
+        e = launch_pdl(state_reduce_kernel<D, M>, dim3((unsigned)(p.BH * (nseg - 1))), dim3(kThreads),
+                       RCfg<D, M>::SMEM, p.stream, 0u, tk, tv, r);
         count_launches(1);
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if (e != cudaSuccess) return e;
     }
     CUtensorMap to;
     if (p.out && !causal_tmap(&to, p, p.out, M)) return cudaErrorInvalidValue;
@@ -1379,15 +1390,16 @@ cudaError_t launch_causal(const Problem &p, const DeviceInfo &dev) {
     a.nu = p.nu;
     a.sum_norm = p.sum_norm ? 1 : 0;
     a.no_den = p.no_den ? 1 : 0;
+    const dim3 grid((unsigned)(p.BH * nseg)), block(C::THREADS);
     if (p.feat != kFeatPhi || p.no_den) {
         if ((e = set_smem(causal_tc_kernel<D, M, true>, C::SMEM)) != cudaSuccess) return e;
-        causal_tc_kernel<D, M, true><<<(unsigned)(p.BH * nseg), C::THREADS, C::SMEM, p.stream>>>(tq, tk, tv, to, a);
+        e = launch_pdl(causal_tc_kernel<D, M, true>, grid, block, C::SMEM, p.stream, 0u, tq, tk, tv, to, a);
     } else {
         if ((e = set_smem(causal_tc_kernel<D, M, false>, C::SMEM)) != cudaSuccess) return e;
-        causal_tc_kernel<D, M, false><<<(unsigned)(p.BH * nseg), C::THREADS, C::SMEM, p.stream>>>(tq, tk, tv, to, a);
+        e = launch_pdl(causal_tc_kernel<D, M, false>, grid, block, C::SMEM, p.stream, 0u, tq, tk, tv, to, a);
     }
     count_launches(1);
-    return cudaGetLastError();
+    return e;
 }
 
 // CTAs per head of the fused non-causal kernel (the cluster size, at most 8)
@@ -1414,21 +1426,10 @@ cudaError_t launch_noncausal_v(const Problem &p, const DeviceInfo &dev) {
     if (p.ws_bytes < (size_t)p.BH * G * (D * M + D) * sizeof(float)) return cudaErrorInvalidValue;
     cudaError_t e;
     if ((e = set_smem(noncausal_tc_kernel<D, M, VAR>, C::SMEM)) != cudaSuccess) return e;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(p.BH * G));
-    cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = C::SMEM;
-    cfg.stream = p.stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)G;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
     const NoncausalArgs a{(float *)p.ws, p.N, G, cps, dev.err_word, p.feat, p.dr, p.nu, p.sum_norm ? 1 : 0,
                           p.no_den ? 1 : 0};
-    e = cudaLaunchKernelEx(&cfg, noncausal_tc_kernel<D, M, VAR>, tq, tk, tv, to, a);
+    e = launch_pdl(noncausal_tc_kernel<D, M, VAR>, dim3((unsigned)(p.BH * G)), dim3(kThreads), C::SMEM, p.stream,
+                   (unsigned)G, tq, tk, tv, to, a);
     count_launches(1);
     return e;
 }

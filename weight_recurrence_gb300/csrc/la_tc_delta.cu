@@ -146,6 +146,7 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int tid = threadIdx.x, wg = tid >> 7, r = tid & 127, q4 = (tid >> 5) & 3;
     const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
     const int bh = blockIdx.x, N = args.N;
+    pdl_launch_dependents();
     const int nch = (N + kC - 1) / kC;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + kDOffBar), *mbar = full + 2;
     uint32_t *slot = reinterpret_cast<uint32_t *>(smem + kDOffSlot);
@@ -174,6 +175,7 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     tc_fence_after();
     const uint32_t tmem = *slot;
     const uint32_t trow = tmem + lane_off;
+    pdl_wait();   // set-up above touched no global memory
 
     // the starting state: S in TMEM (fp32, lanes 0-63) and its bf16 hi/lo snapshot
     if (wg == 0) {
@@ -527,9 +529,9 @@ cudaError_t tc_delta(const Problem &p, const void *beta, const la_variant &v, co
     a.err = dev.err_word;
     cudaError_t e = set_smem(delta_tc_kernel, kDeltaSmem);
     if (e != cudaSuccess) return e;
-    delta_tc_kernel<<<(unsigned)p.BH, kDT, kDeltaSmem, p.stream>>>(tq, tk, tv, a);
+    e = launch_pdl(delta_tc_kernel, dim3((unsigned)p.BH), dim3(kDT), kDeltaSmem, p.stream, 0u, tq, tk, tv, a);
     count_launches(1);
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace la
