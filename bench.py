@@ -200,17 +200,19 @@ def _rotating(torch, tensors, n):
 
 
 def _timed_steps(torch, fn, steps, warmup, stream):
-    """Per-step CUDA-event times (ms) on `stream`, steps back to back."""
+    """Mean time per step (ms): one CUDA-event pair on `stream` around `steps`
+    steps issued back to back (an event between two launches would hold the
+    second until the first has drained, hiding nothing of its set-up)."""
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-    for a, b in evs:
-        a.record(stream)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
         fn()
-        b.record(stream)
+    b.record(stream)
     torch.cuda.synchronize()
-    return [a.elapsed_time(b) for a, b in evs]
+    return a.elapsed_time(b) / steps
 
 
 def _alg_bytes_fwd(w):
@@ -296,20 +298,19 @@ def run_ours(args, rank, world, dist):
     l0 = la.la_launch_count()
     sampler.mark(True)
     t_wall0 = time.perf_counter()
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    for a, b in evs:
-        a.record(stream)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for _ in range(args.steps):
         step()
-        b.record(stream)
+    ev1.record(stream)
     torch.cuda.synchronize()
     t_wall1 = time.perf_counter()
     sampler.mark(False)
     barrier()
     torch.cuda.synchronize()
     launches = la.la_launch_count() - l0
-    times = [a.elapsed_time(b) for a, b in evs]
     assert la.la_get_last_error() == la.LA_OK
-    ms_local = sum(times) / len(times)
+    ms_local = ev0.elapsed_time(ev1) / args.steps
     ms = max_over_ranks(ms_local)
     clocks = sampler.stop()
     tokens_per_step = w.B * w.N
@@ -388,7 +389,7 @@ def run_ours(args, rank, world, dist):
 
         n_e2e = max(3, min(args.steps, 20))
         et = _timed_steps(torch, e2e_step, n_e2e, 2, stream)
-        e_ms = max_over_ranks(sum(et) / len(et))
+        e_ms = max_over_ranks(et)
         nb = q.numel() * q.element_size()
         result["e2e"] = {"value": round(world * tokens_per_step / (e_ms / 1e3), 1), "unit": "tokens/s",
                          "h2d_bytes_per_step": 3 * nb, "d2h_bytes_per_step": out.numel() * out.element_size(),
@@ -437,7 +438,7 @@ def _leg_fwd(torch, la, inputs, name, dev, stream, rot, pk, steps, max_over_rank
     l0 = la.la_launch_count()
     t = _timed_steps(torch, fn, steps, warmup, stream)
     launches = (la.la_launch_count() - l0) // (steps + warmup)
-    ms = max_over_ranks(sum(t) / len(t))
+    ms = max_over_ranks(t)
     gbs = _alg_bytes_fwd(w) / (ms / 1e3) / 1e9
     leg = {"workload": name, "op": w.op, "value": round(world * w.B * w.N / (ms / 1e3), 1), "unit": "tokens/s",
            "ms_per_step": round(ms, 5), "steps": steps, "launches_per_step": launches,
@@ -468,7 +469,7 @@ def _leg_backward(torch, la, inputs, name, dev, stream, rot, pk, steps, max_over
     l0 = la.la_launch_count()
     t = _timed_steps(torch, fn, steps, warmup, stream)
     launches = (la.la_launch_count() - l0) // (steps + warmup)
-    ms = max_over_ranks(sum(t) / len(t))
+    ms = max_over_ranks(t)
     el = q.element_size()
     alg = w.B * w.H * w.N * (4 * w.D + 3 * w.M) * el      # read Q, K, V, dO; write dQ, dK, dV
     gbs = alg / (ms / 1e3) / 1e9
@@ -511,7 +512,7 @@ def _leg_variant(torch, la, inputs, name, dev, stream, rot, pk, steps, max_over_
     l0 = la.la_launch_count()
     t = _timed_steps(torch, fn, steps, warmup, stream)
     launches = (la.la_launch_count() - l0) // (steps + warmup)
-    ms = max_over_ranks(sum(t) / len(t))
+    ms = max_over_ranks(t)
     alg = in_bytes + out.numel() * el                          # read Q, K, V (beta) once, write O once
     gbs = alg / (ms / 1e3) / 1e9
     # per head-token: state update 2FM (+ retrieval 2FM for the delta rule) and read-out 2FM
@@ -582,7 +583,7 @@ def _leg_decode(torch, la, inputs, dev, stream, rot, pk, args, max_over_ranks, w
         t_idx[0] += 1
 
     times = _timed_steps(torch, one, n_flush, args.warmup if args.only else 3, stream)
-    ms = max_over_ranks(sum(times) / len(times))
+    ms = max_over_ranks(times)
     bytes_step = B * H * (2 * D * M * 4 + 2 * D * 4 + (2 * D + 2 * M) * 2)
     gbs = bytes_step / (ms / 1e3) / 1e9
     leg = {"workload": "decode_b256h16d64", "value": round(world / (ms / 1e3), 1), "unit": "steps/s",
@@ -625,7 +626,7 @@ def _leg_decode(torch, la, inputs, dev, stream, rot, pk, args, max_over_ranks, w
     yf = torch.empty((steps, B, H, M), dtype=w.dtype, device=dev)
     fused = lambda: la.la_decode_steps(qs, ks, vs, Sf, zf, y=yf, stream=stream)  # noqa: E731
     ft = _timed_steps(torch, fused, 3, 1, stream)
-    fms = max_over_ranks(sum(ft) / len(ft))
+    fms = max_over_ranks(ft)
     fbytes = 2 * B * H * (D * M + D) * 4 + steps * B * H * (2 * D + 2 * M) * 2
     leg["fused_4096"] = {"steps_per_s": round(world * steps / (fms / 1e3), 1), "ms_total": round(fms, 3),
                          "launches": 1, "hbm_gbs": round(fbytes / (fms / 1e3) / 1e9, 1),

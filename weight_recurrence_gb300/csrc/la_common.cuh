@@ -35,6 +35,13 @@ __device__ __forceinline__ void record_error(int *err, int code) {
 // grid to complete).
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+// pdl_wait() for a whole CTA (every thread calls it): one thread waits, the
+// others at the barrier; the prerequisite grids' writes are then visible to
+// every thread of this grid.
+__device__ __forceinline__ void pdl_wait_cta() {
+    if (threadIdx.x == 0) pdl_wait();
+    __syncthreads();
+}
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {
     uint64_t t;

@@ -105,9 +105,11 @@ bool tc_variant_route(const la_shape &s, const la_variant &v, Problem &p);
 bool tc_delta_supported(const la_shape &s, const la_variant &v);
 cudaError_t tc_delta(const Problem &p, const void *beta, const la_variant &v, const DeviceInfo &dev);
 
-// Launches `kernel` with programmatic stream serialization, so that its
-// set-up overlaps the tail of the previous launch on the stream: every such
-// kernel calls pdl_wait() before its first global-memory access.  cluster_x
+// Launches `kernel` with programmatic stream serialization: it may start as
+// soon as the previous launch on the stream triggers (explicitly, or
+// implicitly as its CTAs exit), its set-up overlapping that launch's tail;
+// every such kernel calls pdl_wait_cta() before its first global-memory
+// access.  cluster_x
 // > 0 also sets a cluster shape (cluster_x, 1, 1) (a cluster kernel keeps its
 // cluster launch even at one CTA per cluster).
 template <typename... KArgs, typename... Args>

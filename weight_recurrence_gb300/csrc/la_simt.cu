@@ -228,8 +228,7 @@ decode_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__restr
     const long long h = blockIdx.x;
     const int tid = threadIdx.x;
     const int c4 = tid % C4, r = tid / C4;
-    pdl_launch_dependents();
-    pdl_wait();
+    pdl_wait_cta();
 
     float4 s[NR];
     float4 *Sh = reinterpret_cast<float4 *>(S + h * D * M);
@@ -382,8 +381,7 @@ decode_steps_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *_
     const long long h = blockIdx.x;
     const int tid = threadIdx.x;
     const int c4 = tid % C4, r = tid / C4;
-    pdl_launch_dependents();
-    pdl_wait();
+    pdl_wait_cta();
     const int nsteps = steps ? max(0, min(Tn, steps[h / H])) : Tn;
 
     float4 s[NR];

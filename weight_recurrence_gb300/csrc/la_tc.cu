@@ -191,8 +191,11 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     const int bh = blockIdx.x / args.nseg, seg = blockIdx.x % args.nseg;
     const int c_begin = seg * args.cps;
     // the next launch on the stream may start its own set-up now (it reads
-    // nothing of ours before its griddepcontrol.wait)
-    pdl_launch_dependents();
+    // nothing of ours before its griddepcontrol.wait).  Measured: this early
+    // trigger helps the plain kernel; with a variant's feature map the next
+    // grid's early CTAs slowed the running one (91 -> 105 us for DPFP-1), so
+    // that instantiation triggers implicitly, at exit.
+    if (!VAR) pdl_launch_dependents();
 
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
     uint64_t *full = bar, *empty = bar + C::NS, *phi_done = bar + 2 * C::NS;
@@ -259,7 +262,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     if (tid == 0) LA_TRACE_AT(0, 63, 1);
     // everything above touched no global memory; from here on the previous
     // launch on the stream has completed and its writes are visible
-    pdl_wait();
+    pdl_wait_cta();
     // this head's sequence length (rows past it are read but ignored)
     const int Nseq = args.lens ? max(0, min(args.N, args.lens[bh / args.H])) : args.N;
     const int nch_total = (Nseq + kC - 1) / kC;
@@ -820,7 +823,6 @@ state_reduce_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     volatile int *abort = reinterpret_cast<volatile int *>(smem + C::OFF_TSLOT + 4);
-    pdl_launch_dependents();
     const int bh = blockIdx.x / args.nred, sp = blockIdx.x % args.nred;
     const int nch_total = (args.N + kC - 1) / kC;
     const int c_begin = sp * args.cps;
@@ -857,7 +859,7 @@ state_reduce_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    pdl_wait();   // set-up above touched no global memory
+    pdl_wait_cta();   // set-up above touched no global memory
 
     if (warp == 0) {
         if (lane == 0 && !*abort) {
@@ -1030,7 +1032,7 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     volatile int *abort = reinterpret_cast<volatile int *>(smem + C::OFF_TSLOT + 4);
-    pdl_launch_dependents();
+    if (!VAR) pdl_launch_dependents();   // as in causal_tc_kernel (measured)
     const int bh = blockIdx.x / args.G, g = blockIdx.x % args.G;
     const int nch_total = (args.N + kC - 1) / kC;
     const int c_begin = g * args.cps;
@@ -1075,7 +1077,7 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
-    pdl_wait();   // set-up above touched no global memory
+    pdl_wait_cta();   // set-up above touched no global memory
     const bool epi = warp >= 2 && warp < 6;
     // every thread arrives on the cluster barrier exactly once; the epilogue
     // group only after its partial sums are in the workspace

@@ -292,7 +292,6 @@ bwd_tc_pass1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
 {
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x, r = tid & (kC - 1), wg = tid >> 7, q4 = (tid >> 5) & 3;
-    pdl_launch_dependents();
     const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
     const int bh = blockIdx.x, N = args.N;
     const int nch = (N + kC - 1) / kC;
@@ -321,7 +320,7 @@ bwd_tc_pass1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     tc_fence_after();
     const uint32_t tmem = *slot;
     const uint32_t trow = tmem + lane_off;
-    pdl_wait();   // set-up above touched no global memory
+    pdl_wait_cta();   // set-up above touched no global memory
 
     // the starting state: S (TMEM, fp32; lanes 64-127 unused) and its bf16
     // snapshot, Z (shared memory, fp32); warpgroup h takes columns 32h..32h+31
@@ -520,7 +519,6 @@ bwd_tc_pass2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
 {
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x, r = tid & (kC - 1), wg = tid >> 7, q4 = (tid >> 5) & 3;
-    pdl_launch_dependents();
     const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
     const int bh = blockIdx.x, N = args.N;
     const int nch = (N + kC - 1) / kC;
@@ -549,7 +547,7 @@ bwd_tc_pass2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     tc_fence_after();
     const uint32_t tmem = *slot;
     const uint32_t trow = tmem + lane_off;
-    pdl_wait();   // set-up above touched no global memory
+    pdl_wait_cta();   // set-up above touched no global memory
 
     // R, r start from the gradient reaching the final state (or zero)
     {
@@ -748,7 +746,7 @@ cudaError_t tc_causal_backward(const BwdProblem &p, const DeviceInfo &dev) {
                    tdq, a);
     count_launches(1);
     if (e != cudaSuccess) return e;
-    // the reverse sweep's pdl_wait() holds it until the forward sweep's g and e are written
+    // the reverse sweep's pdl_wait_cta() holds it until the forward sweep's g and e are written
     e = launch_pdl(bwd_tc_pass2_kernel, dim3((unsigned)p.BH), dim3(kBT), kBwdSmem, p.stream, 0u, tq, tk, tv, tg, tdk,
                    tdv, a);
     count_launches(1);

@@ -146,7 +146,6 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     const int tid = threadIdx.x, wg = tid >> 7, r = tid & 127, q4 = (tid >> 5) & 3;
     const uint32_t lane_off = (uint32_t)(32 * q4) << 16;
     const int bh = blockIdx.x, N = args.N;
-    pdl_launch_dependents();
     const int nch = (N + kC - 1) / kC;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + kDOffBar), *mbar = full + 2;
     uint32_t *slot = reinterpret_cast<uint32_t *>(smem + kDOffSlot);
@@ -175,7 +174,7 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
     tc_fence_after();
     const uint32_t tmem = *slot;
     const uint32_t trow = tmem + lane_off;
-    pdl_wait();   // set-up above touched no global memory
+    pdl_wait_cta();   // set-up above touched no global memory
 
     // the starting state: S in TMEM (fp32, lanes 0-63) and its bf16 hi/lo snapshot
     if (wg == 0) {
