@@ -63,8 +63,40 @@ extern "C" int la_trace_read(unsigned long long *dst) {
     do {                                                                              \
         if (blockIdx.x == 0 && (it) < 64) g_la_trace[role][it][ev] = (unsigned long long)clock64(); \
     } while (0)
+// per-CTA global-timer events of the last eight launches (slot = launch % 8);
+// event 11 holds the SM id
+__device__ unsigned long long g_la_cta[8][512][12];
+__device__ unsigned int g_la_cta_ctr;
+extern "C" int la_trace_read_cta(unsigned long long *dst) {
+    return (int)cudaMemcpyFromSymbol(dst, g_la_cta, sizeof(g_la_cta));
+}
+extern "C" int la_trace_reset_cta() {
+    const unsigned int z = 0;
+    return (int)cudaMemcpyToSymbol(g_la_cta_ctr, &z, sizeof(z));
+}
+// (the slot of each CTA lives in global memory: no static shared memory,
+// which would change the CTAs' shared-memory footprint and so the occupancy)
+__device__ unsigned int g_la_cta_slot[512];
+#define LA_CTA_BEGIN()                                                                \
+    if (threadIdx.x == 0 && blockIdx.x < 512) {                                       \
+        const unsigned int sl_ = atomicAdd(&g_la_cta_ctr, 1u) / gridDim.x;            \
+        g_la_cta_slot[blockIdx.x] = sl_;                                              \
+        unsigned int sm_;                                                             \
+        asm volatile("mov.u32 %0, %%smid;" : "=r"(sm_));                              \
+        g_la_cta[sl_ & 7][blockIdx.x][11] = sm_;                                      \
+    }
+#define LA_CTA_AT(ev)                                                                 \
+    do {                                                                              \
+        if (blockIdx.x < 512) {                                                       \
+            unsigned long long t_;                                                    \
+            asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t_));                    \
+            g_la_cta[*(volatile unsigned int *)&g_la_cta_slot[blockIdx.x] & 7][blockIdx.x][ev] = t_; \
+        }                                                                             \
+    } while (0)
 #else
 #define LA_TRACE_AT(role, it, ev) ((void)0)
+#define LA_CTA_BEGIN()
+#define LA_CTA_AT(ev) ((void)0)
 #endif
 
 namespace la {
@@ -1032,6 +1064,8 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     volatile int *abort = reinterpret_cast<volatile int *>(smem + C::OFF_TSLOT + 4);
+    LA_CTA_BEGIN();
+    if (tid == 0) LA_CTA_AT(0);
     if (!VAR) pdl_launch_dependents();   // as in causal_tc_kernel (measured)
     const int bh = blockIdx.x / args.G, g = blockIdx.x % args.G;
     const int nch_total = (args.N + kC - 1) / kC;
@@ -1078,6 +1112,7 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     tc_fence_after();
     const uint32_t tmem = *tslot;
     pdl_wait_cta();   // set-up above touched no global memory
+    if (tid == 0) LA_CTA_AT(1);
     const bool epi = warp >= 2 && warp < 6;
     // every thread arrives on the cluster barrier exactly once; the epilogue
     // group only after its partial sums are in the workspace
@@ -1179,6 +1214,7 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         mbar_arrive(init);
         // this CTA's partial sums into its workspace slot
         const bool ok1 = wait_bar_warp(red_done, 0, abort);
+        if (leader) LA_CTA_AT(3);
         if (ok1 && swarp) {
             tc_fence_after();
 #pragma unroll 1
@@ -1196,9 +1232,12 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             if (r < D) slot[D * M + r] = __uint_as_float(zv[0]);
         }
         tc_fence_before();
-        __threadfence();
+        // the slots are read only by this cluster's CTAs: the barrier's
+        // cluster-scope release (and the readers' acquire) orders them
+        if (leader) LA_CTA_AT(4);
         cluster_arrive_release();
         cluster_wait_acquire();
+        if (leader) LA_CTA_AT(5);
         // the head's state: sum of the cluster's slots, as bf16 [S | z_hi z_lo].
         // All 128 threads take 16-column blocks (consecutive threads, consecutive
         // blocks of a row) and load up to four slots' blocks before adding, so
@@ -1206,6 +1245,11 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         if (!*abort) {
             const float *src = args.ws + (size_t)bh * args.G * W;
             const int tg = tid - 64;
+            // z's slot entries first, so that their loads share the first
+            // round trip with the state blocks'
+            float zr = 0.f;
+            if (r < D)
+                for (int j = 0; j < args.G; ++j) zr += __ldcg(src + (size_t)j * W + D * M + r);
             constexpr int BPR = M / 16;                  // 16-column blocks per row
 #pragma unroll 1
             for (int b = tg; b < D * BPR; b += kGrp) {
@@ -1246,8 +1290,6 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 }
             }
             if (r < D) {
-                float zr = 0.f;
-                for (int j = 0; j < args.G; ++j) zr += __ldcg(src + (size_t)j * W + D * M + r);
                 uint8_t *za = snap + (M / 64) * D * 128;
                 for (int c = 0; c < 64; c += 8)
                     *reinterpret_cast<uint4 *>(za + sw128_offset(r, c)) = make_uint4(0u, 0u, 0u, 0u);
@@ -1259,6 +1301,7 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         }
         fence_proxy_async();
         mbar_arrive(snap_bar);
+        if (leader) LA_CTA_AT(6);
         if (leader) prefetch_tmap(&tm_o);
         for (int i = 0; i < n; ++i) {
             const int idx = n + i, s = idx % C::NS, ob = i % C::NOBUF, kb = i / C::NOBUF;
@@ -1302,6 +1345,7 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             }
         }
         if (leader) tma_store_wait_all0();
+        if (leader) LA_CTA_AT(7);
     } else {
         // ------------------------------------------------------ feature-map group
         // phase 1 K tiles (rows past the sequence end zeroed: they must add
@@ -1310,6 +1354,7 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         for (int idx = 0; idx < total; ++idx) {
             const int s = idx % C::NS;
             if (wait_bar(&full[s], (idx / C::NS) & 1, abort)) {
+                if (t == 0 && idx == 0) LA_CTA_AT(2);
                 const int zf = idx < n ? min(kC, args.N - (c_begin + idx) * kC) : kC;
                 if (!VAR || args.feat == kFeatPhi) phi_tile<D>(smem + s * C::STAGE, t, zf);
                 else if constexpr (VAR)   // a variant's feature map, one row per thread
@@ -1323,6 +1368,7 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (tid == 0) LA_CTA_AT(8);
     if (warp == 0) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
