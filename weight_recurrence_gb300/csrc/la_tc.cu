@@ -1111,6 +1111,13 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tslot;
+    if (tid == 0) {   // kernel parameters, which no earlier launch writes: may overlap the wait
+        // (measured 33.1 -> 32.7 us here; the causal kernel measured slower with it)
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+        prefetch_tmap(&tm_o);
+    }
     pdl_wait_cta();   // set-up above touched no global memory
     if (tid == 0) LA_CTA_AT(1);
     const bool epi = warp >= 2 && warp < 6;
@@ -1121,9 +1128,6 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     if (warp == 0) {
         // ------------------------------------------------------ producer
         if (lane == 0 && !*abort) {
-            prefetch_tmap(&tm_q);
-            prefetch_tmap(&tm_k);
-            prefetch_tmap(&tm_v);
             int issued = 0;
             for (int idx = 0; idx < total; ++idx) {
                 const int s = idx % C::NS, k = idx / C::NS;
