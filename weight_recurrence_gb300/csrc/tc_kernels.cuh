@@ -120,67 +120,92 @@ __device__ __forceinline__ void load_raw_row(const uint8_t *tile, int r, uint32_
     }
 }
 
+// Packed bf16x2 helpers of the DPFP rows.
+__device__ __forceinline__ uint32_t bmax0(uint32_t x) {
+    uint32_t r;
+    asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(0u));
+    return r;
+}
+__device__ __forceinline__ uint32_t bmin0(uint32_t x) {
+    uint32_t r;
+    asm("min.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(x), "r"(0u));
+    return r;
+}
+__device__ __forceinline__ uint32_t bmul(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+__device__ __forceinline__ uint32_t badd(uint32_t a, uint32_t b) {
+    uint32_t r;
+    asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+    return r;
+}
+
+// Word k of the partner values x'_i of shift s for the elements 2k, 2k+1 of
+// a raw row w (DR bf16 values, two per word): x'_i = x_{i+s} for i + s < DR,
+// else -x_{i+s-DR} (the second half of r = [relu(x), relu(-x)]).  k and s are
+// compile-time after unrolling, so the wrap tests fold away.
 template <int DR>
-__device__ __forceinline__ float raw_at(const uint32_t (&w)[DR / 2], int i) {
-    return (i & 1) ? bf16hi(w[i >> 1]) : bf16lo(w[i >> 1]);
+__device__ __forceinline__ uint32_t dpfp_partner(const uint32_t (&w)[DR / 2], int k, int s) {
+    constexpr int NW = DR / 2;
+    auto word = [&](int a) { return a < NW ? w[a] : (w[a - NW] ^ 0x80008000u); };
+    if ((s & 1) == 0) return word(k + s / 2);
+    const int a = k + (s - 1) / 2;
+    return __byte_perm(word(a), word(a + 1), 0x5432);   // high half of word a, low half of word a + 1
 }
 
-// DPFP from products of raw values: for shift s and i < DR, the two features
-// r_i r_{i+s} (first half) and r_{DR+i} r_{DR+i+s} (second half, indices mod
-// 2DR) are relu(x_i) relu(sg x_j) and relu(-x_i) relu(-sg x_j), where x_j is
-// the partner value (j = i + s, or i + s - DR with sg = -1 past the end).  At
-// most one of the two is non-zero and their sum is p = max(sg x_i x_j, 0):
-// the first when x_i > 0, the second otherwise.
-template <int DR, int NU>
-__device__ __forceinline__ float dpfp_pair(const uint32_t (&w)[DR / 2], int s, int i) {
-    const int j = i + s;
-    const float xj = j < DR ? raw_at<DR>(w, j) : -raw_at<DR>(w, j - DR);
-    return fmaxf(raw_at<DR>(w, i) * xj, 0.f);
-}
-
+// DPFP ("Linear Transformers Are Secretly Fast Weight Programmers", sec. 5.2)
+// of row r from its raw values, in packed bf16x2 arithmetic: for shift s and
+// i < DR the features (s-1)*2DR + i = relu(x_i) relu(x'_i) and
+// (s-1)*2DR + DR + i = relu(-x_i) relu(-x'_i) = min(x_i, 0) min(x'_i, 0), each
+// product rounded to bf16 once.  With SUM the row is then divided by its
+// feature sum (fp32; the two products of an element never both differ from
+// zero, so their packed sum is exact) in a second pass over the stored row,
+// a second bf16 rounding.  The row's DR/2 raw words stay in registers.
 template <int F, int DR, int NU, bool SUM>
 __device__ __forceinline__ void dpfp_row(uint8_t *tile, int r, bool zero) {
     static_assert(F == 2 * DR * NU && DR <= 64 && DR % 8 == 0, "DPFP width");
-    uint32_t w[DR / 2];
+    constexpr int NW = DR / 2;
+    uint32_t w[NW];
     load_raw_row<DR>(tile, r, w);
-    float scale = 1.f;
-    if (SUM) {
-        float s0 = 0.f, s1 = 0.f;
-#pragma unroll
-        for (int s = 1; s <= NU; ++s)
-#pragma unroll
-            for (int i = 0; i < DR; i += 2) {
-                s0 += dpfp_pair<DR, NU>(w, s, i);
-                s1 += dpfp_pair<DR, NU>(w, s, i + 1);
-            }
-        const float sum = s0 + s1;
-        scale = sum > 0.f ? 1.f / sum : 0.f;
-        // recompute the pairs below instead of keeping them all live
-#pragma unroll
-        for (int j = 0; j < DR / 2; ++j) asm volatile("" : "+r"(w[j]));
-    }
-    auto put = [&](int c, const float (&v)[8]) {
-        uint4 o = make_uint4(0u, 0u, 0u, 0u);
-        if (!zero)
-            o = make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
-                           pack_bf16x2(v[6], v[7]));
-        *reinterpret_cast<uint4 *>(tile + (c / 64) * kC * 128 + sw128_offset(r, c % 64)) = o;
-    };
+    auto at = [&](int c) { return reinterpret_cast<uint4 *>(tile + (c / 64) * kC * 128 + sw128_offset(r, c % 64)); };
+    float s0 = 0.f, s1 = 0.f;
+    // all raw words are read before the first feature chunk overwrites them
 #pragma unroll
     for (int s = 1; s <= NU; ++s)
 #pragma unroll
-        for (int i0 = 0; i0 < DR; i0 += 8) {
-            float hi[8], lo[8];
+        for (int k0 = 0; k0 < NW; k0 += 4) {
+            uint32_t hi[4], lo[4];
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const float p = dpfp_pair<DR, NU>(w, s, i0 + k) * scale;
-                const bool pos = raw_at<DR>(w, i0 + k) > 0.f;
-                hi[k] = pos ? p : 0.f;
-                lo[k] = pos ? 0.f : p;
+            for (int u = 0; u < 4; ++u) {
+                const uint32_t xp = dpfp_partner<DR>(w, k0 + u, s);
+                hi[u] = bmul(bmax0(w[k0 + u]), bmax0(xp));
+                lo[u] = bmul(bmin0(w[k0 + u]), bmin0(xp));
+                if (SUM) {
+                    const uint32_t t = badd(hi[u], lo[u]);
+                    s0 += bf16lo(t);
+                    s1 += bf16hi(t);
+                }
             }
-            put((s - 1) * 2 * DR + i0, hi);
-            put((s - 1) * 2 * DR + DR + i0, lo);
+            const int c = (s - 1) * 2 * DR + 2 * k0;
+            *at(c) = zero ? make_uint4(0u, 0u, 0u, 0u) : make_uint4(hi[0], hi[1], hi[2], hi[3]);
+            *at(c + DR) = zero ? make_uint4(0u, 0u, 0u, 0u) : make_uint4(lo[0], lo[1], lo[2], lo[3]);
         }
+    if (SUM && !zero) {
+        const float sum = s0 + s1;
+        const float sc = sum > 0.f ? 1.f / sum : 0.f;
+        const uint32_t scw = pack_bf16x2(sc, sc);
+#pragma unroll 4
+        for (int c = 0; c < F; c += 8) {
+            uint4 v = *at(c);
+            v.x = bmul(v.x, scw);
+            v.y = bmul(v.y, scw);
+            v.z = bmul(v.z, scw);
+            v.w = bmul(v.w, scw);
+            *at(c) = v;
+        }
+    }
 }
 
 // Elementwise: pass 1 maps each 8-column chunk in place with the packed
