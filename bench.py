@@ -133,15 +133,17 @@ class ClockSampler:
 
 # Source files each captured kernel is built from: a capture's traffic figure
 # stands only while these hash to what they were when it was taken.
-TC_SOURCES = ("la_tc.cu", "tc_kernels.cuh", "tc_ptx.cuh", "tc_host.h", "la_common.cuh")
+TC_SOURCES = ("la_tc.cu", "tc_kernels.cuh", "tc_ptx.cuh", "tc_host.h", "la_common.cuh", "la_internal.h")
 KERNEL_SOURCES = {
     "causal_causal_b16h8n3072d64": TC_SOURCES,
     "causal_causal_b1h16n65536d128": TC_SOURCES,
     "noncausal_noncausal_b8h8n4096d64": TC_SOURCES,
     "causal_variant_dpfp_b16h8n3072d64": TC_SOURCES,
-    "decode_decode_b256h16d64": ("la_simt.cu", "la_common.cuh"),
-    "causal_variant_delta_b16h8n3072d64": ("la_fw.cu", "la_common.cuh"),
-    "backward_causal_b16h8n3072d64": ("la_tc_bwd.cu", "tc_kernels.cuh", "tc_ptx.cuh", "tc_host.h", "la_common.cuh"),
+    "decode_decode_b256h16d64": ("la_simt.cu", "la_common.cuh", "la_internal.h"),
+    "causal_variant_delta_b16h8n3072d64": ("la_tc_delta.cu", "tc_kernels.cuh", "tc_ptx.cuh", "tc_host.h",
+                                           "la_common.cuh", "la_internal.h"),
+    "backward_causal_b16h8n3072d64": ("la_tc_bwd.cu", "tc_kernels.cuh", "tc_ptx.cuh", "tc_host.h", "la_common.cuh",
+                                      "la_internal.h"),
 }
 
 
