@@ -60,12 +60,12 @@ constexpr int kBT = 256;                    // threads: two warpgroups
 constexpr int kTile = kC * kBD * 2;         // one 128 x 64 bf16 tile, 16 KB
 constexpr int kStage = 4 * kTile;           // Q, K, V, dO (pass 1) or Q, K, V, g (pass 2)
 constexpr int kOffGT = 2 * kStage;          // pass 1: g of the chunk (MMA operand, store source)
-constexpr int kOffPsi = kOffGT + kTile;     // psi(K) (pass 1) or psi(Q) (pass 2), an MMA operand
-constexpr int kOffSnap = kOffPsi + kTile;   // state S or R as bf16 hi then lo parts, [64 rows][64] each
+constexpr int kOffPsi = kOffGT + kTile;     // [2] psi(K) (pass 1) or psi(Q) (pass 2), an MMA operand, per chunk parity
+constexpr int kOffSnap = kOffPsi + 2 * kTile;   // state S or R as bf16 hi then lo parts, [64 rows][64] each
 constexpr int kSnap = kBD * kBD * 2;        // 8 KB
 constexpr int kOffZ = kOffSnap + 2 * kSnap; // fp32 Z or r, [2][64]: before and after the chunk
-constexpr int kOffE = kOffZ + 2 * kBD * 4;  // pass 2: fp32 e of the chunk [128]
-constexpr int kOffPart = kOffE + kC * 4;    // fp32 [8][64] column-sum parts
+constexpr int kOffE = kOffZ + 2 * kBD * 4;  // pass 2: fp32 e of the chunk, [2][128] by chunk parity
+constexpr int kOffPart = kOffE + 2 * kC * 4;    // fp32 [8][64] column-sum parts
 constexpr int kOffX = kOffPart + 8 * kBD * 4;   // fp32 [3][2][128] row-reduction halves
 constexpr int kOffBar = kOffX + 3 * 2 * kC * 4;
 constexpr int kOffSlot = kOffBar + 8 * 8;
@@ -356,13 +356,18 @@ bwd_tc_pass1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         uint8_t *tq = st, *tk = st + kTile, *tv = st + 2 * kTile, *tdo = st + 3 * kTile;
         const float *zc = zs + kBD * s;   // Z before this chunk
         float *zn = zs + kBD * (s ^ 1);   // Z after it
-        const bool landed = mbar_wait_bounded(&full[s], (it >> 1) & 1, now_ns() + kWaitNs, nullptr);
-        if (!(ok = barrier_and(landed, args.err))) break;
+        uint8_t *psi_c = psi + s * kTile;
         // feature maps in place (rows past the sequence end become zero), and
-        // psi(K) = phi(K) - 1 for the dQ product
-        phi_tile_all(tq, tid, rows);
-        psi_phi_tile(tk, psi, tid, rows);
-        operands_ready();
+        // psi(K) = phi(K) - 1 for the dQ product: the first chunk's here, every
+        // later chunk's while the previous chunk's num product runs (made
+        // visible by that chunk's last barrier)
+        if (it == 0) {
+            const bool landed = mbar_wait_bounded(&full[0], 0, now_ns() + kWaitNs, nullptr);
+            if (!(ok = barrier_and(landed, args.err))) break;
+            phi_tile_all(tq, tid, rows);
+            psi_phi_tile(tk, psi_c, tid, rows);
+            operands_ready();
+        }
         BWD_TRACE(0, it, 1);
         const uint32_t aq = smem_u32(tq), ak = smem_u32(tk), av = smem_u32(tv), ag = smem_u32(gt), as = smem_u32(snap);
         // P = phi(Q) phi(K)^T;  S += phi(K)^T V (A read MN-major with M-atom
@@ -441,9 +446,21 @@ bwd_tc_pass1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                     mma_f16_ss(tmem + kColDQ, kmajor_base(ag) + kmajor_step(ks),
                                kmajor_base(as + part2 * kSnap) + kmajor_step(ks, kBD), ID_KK, part2 > 0 || ks > 0);
         }
+        // meanwhile the next chunk's feature maps (its tiles were issued after
+        // this chunk's first products)
+        bool nxt = true;
+        if (it + 1 < nch) {
+            nxt = mbar_wait_bounded(&full[s ^ 1], ((it + 1) >> 1) & 1, now_ns() + kWaitNs, nullptr);
+            if (nxt) {
+                uint8_t *st1 = smem + (s ^ 1) * kStage;
+                const int rows1 = min(kC, N - t0 - kC);
+                phi_tile_all(st1, tid, rows1);
+                psi_phi_tile(st1 + kTile, psi + (s ^ 1) * kTile, tid, rows1);
+            }
+        }
         // e_i = -(g_i . num_i) / den_i, from the same bf16 g, so that the terms
         // A phi(K), g S^T and e Z stay consistent
-        mine = mma_wait(&mbar[1], ph1);
+        mine = mma_wait(&mbar[1], ph1) && nxt;
         BWD_TRACE(0, it, 4);
         {
             float num[32];
@@ -465,7 +482,7 @@ bwd_tc_pass1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         const float asum = xa[r] + xa[kC + r];
         // dphi(Q) += A psi(K)  (+ asum: the product with the 1 of phi = psi + 1)
         if (tid == 0) {
-            const uint64_t dk = smem_desc(smem_u32(psi), kC * 128, 1024);
+            const uint64_t dk = smem_desc(smem_u32(psi_c), kC * 128, 1024);
 #pragma unroll
             for (int ks = 0; ks < kC / 16; ++ks)
                 mma_f16_ts(tmem + kColDQ, tmem + kColPH + ks * 8, dk + mnmajor_step(ks), ID_MN, 1);
@@ -582,12 +599,22 @@ bwd_tc_pass2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         uint8_t *tq = st, *tk = st + kTile, *tv = st + 2 * kTile, *tg = st + 3 * kTile;
         const float *rc = rs + kBD * s;   // r after this chunk (the reverse sum of the later ones)
         float *rn = rs + kBD * (s ^ 1);   // r including this chunk
-        if (wg == 0) es[r] = t0 + r < N ? args.e_ws[(size_t)bh * N + t0 + r] : 0.f;
-        const bool landed = mbar_wait_bounded(&full[s], (it >> 1) & 1, now_ns() + kWaitNs, nullptr);
-        if (!(ok = barrier_and(landed, args.err))) break;
-        psi_phi_tile(tq, psi, tid, rows);
-        phi_tile_all(tk, tid, rows);
-        operands_ready();
+        uint8_t *psi_c = psi + s * kTile;
+        float *es_c = es + kC * s;
+        // the first chunk's feature maps and e here, every later chunk's while
+        // the previous chunk's dV and dphi(K) products run (made visible by
+        // that chunk's last barrier)
+        if (it == 0) {
+            if (wg == 0) es_c[r] = t0 + r < N ? args.e_ws[(size_t)bh * N + t0 + r] : 0.f;
+            const bool landed = mbar_wait_bounded(&full[0], 0, now_ns() + kWaitNs, nullptr);
+            if (!(ok = barrier_and(landed, args.err))) break;
+            psi_phi_tile(tq, psi_c, tid, rows);
+            phi_tile_all(tk, tid, rows);
+            operands_ready();
+        }
+        // the next chunk's e, loaded now and stored below, so that the load's
+        // latency passes under this chunk's work
+        const float e_next = (wg == 0 && it + 1 < nch) ? args.e_ws[(size_t)bh * N + t0 - kC + r] : 0.f;
         BWD_TRACE(1, it, 1);
         const uint32_t aq = smem_u32(tq), ak = smem_u32(tk), av = smem_u32(tv), ag = smem_u32(tg), as = smem_u32(snap);
         // P^T = phi(K) phi(Q)^T, then A^T = V g^T (rows j, columns i) and
@@ -611,7 +638,7 @@ bwd_tc_pass2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             if (it + 1 < nch) load_chunk(smem + (s ^ 1) * kStage, &full[s ^ 1], &tm_q, &tm_k, &tm_v, &tm_g, t0 - kC, bh);
         }
         // meanwhile the column sums sum_i e_i phi(Q_i)
-        colsum_part(tq, es, part);
+        colsum_part(tq, es_c, part);
         // masks (i >= j) as bf16: warpgroup 0 P^T, warpgroup 1 A^T with e_i
         // added to the kept entries (and its row sums)
         bool mine = mma_wait(&mbar[0], ph0);
@@ -622,8 +649,8 @@ bwd_tc_pass2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         mine = mma_wait(&mbar[1], ph1) && mine;
         BWD_TRACE(1, it, 2);
         if (wg == 1) {
-            float a = mask64<false>(trow + kColA2, 0, r, false, 0.f, es, trow + kColA2, 0u);
-            a += mask64<false>(trow + kColA2, 64, r, false, 0.f, es, trow + kColA2 + 32, 0u);
+            float a = mask64<false>(trow + kColA2, 0, r, false, 0.f, es_c, trow + kColA2, 0u);
+            a += mask64<false>(trow + kColA2, 64, r, false, 0.f, es_c, trow + kColA2 + 32, 0u);
             xa[r] = a;
         }
         if (!(ok = barrier_and(mine, args.err))) break;
@@ -632,7 +659,7 @@ bwd_tc_pass2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         const float asum = xa[r];
         // dV = P^T g + phi(K) R;  dphi(K) = A^T psi(Q) + V R^T (+ asum)
         if (tid == 0) {
-            const uint64_t dg = smem_desc(ag, kC * 128, 1024), dqm = smem_desc(smem_u32(psi), kC * 128, 1024);
+            const uint64_t dg = smem_desc(ag, kC * 128, 1024), dqm = smem_desc(smem_u32(psi_c), kC * 128, 1024);
             const uint64_t ds = smem_desc(as, kBD * 128, 1024);
 #pragma unroll
             for (int ks = 0; ks < kC / 16; ++ks)
@@ -659,6 +686,18 @@ bwd_tc_pass2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         // dV's: wait for both before writing), dK = (dphi(K) + r + asum) * phi'(K)
         // into the g tile (columns 32h..32h+31 by warpgroup h); the new R's
         // bf16 snapshot
+        // meanwhile the next (earlier) chunk's e and feature maps
+        if (it + 1 < nch) {
+            if (wg == 0) es[kC * (s ^ 1) + r] = e_next;
+            const bool nxt = mbar_wait_bounded(&full[s ^ 1], ((it + 1) >> 1) & 1, now_ns() + kWaitNs, nullptr);
+            if (nxt) {
+                uint8_t *st1 = smem + (s ^ 1) * kStage;
+                const int rows1 = min(kC, N - (t0 - kC));
+                psi_phi_tile(st1, psi + (s ^ 1) * kTile, tid, rows1);
+                phi_tile_all(st1 + kTile, tid, rows1);
+            }
+            mine = mine && nxt;
+        }
         float x[32];
         mine = mma_wait(&mbar[2], ph2) && mine;
         BWD_TRACE(1, it, 4);
