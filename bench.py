@@ -532,7 +532,7 @@ def _leg_variant(torch, la, inputs, name, dev, stream, rot, pk, steps, max_over_
            "traffic": _traffic("causal_variant_" + name)}
     alu = {"bound": "alu", "achieved": round(tf, 2), "peak": round(FP32_ALU_TFLOPS, 1), "unit": "TFLOP/s",
            "frac": round(tf / FP32_ALU_TFLOPS, 4), "peak_source": "derived: 152 SMs x 128 FP32 lanes x 2 x 2070 MHz",
-           "alg_flops_per_launch": flops}
+           "alg_flops_per_launch": flops, "traffic": _traffic("causal_variant_" + name)}
     leg = {"workload": name, "op": "causal_variant", "variant": {"feature_map": fm, "nu": nu, "norm": norm,
                                                                  "update": update, "F": F},
            "value": round(world * w.B * w.N / (ms / 1e3), 1), "unit": "tokens/s", "ms_per_step": round(ms, 5),

@@ -207,6 +207,55 @@ def test_noncausal_vs_oracle(B, H, N, D, M, dtype, scale):
     assert row_rel_err(out, ref) <= tol_for(dtype)
 
 
+# ------------------------------------------- back-to-back dependent launches
+
+def _bf16(x):
+    return torch.from_numpy(np.ascontiguousarray(x)).to(torch.bfloat16)
+
+
+def test_back_to_back_calls_read_the_previous_output():
+    """Each call reads the output of the call just before it, with no host
+    synchronisation in between: the launches overlap their set-up with the
+    previous launch's tail, and their first global reads must still see that
+    launch's writes.  The oracle runs the same chain on its own outputs
+    (rounded to bf16 as the library's are)."""
+    B, H, N, D = 2, 4, 700, 64
+    q, k, v = inputs.qkv(B, H, N, D, D, torch.bfloat16, 1.0, seed=95)
+    qd, kd, vd = _dev(q, k, v)
+    o1 = la.la_forward_causal(qd, kd, vd)
+    o2 = la.la_forward_noncausal(o1, kd, vd)
+    o3 = la.la_forward_causal(qd, o2, vd)
+    o4 = la.la_forward_noncausal(o3, o3, o1)
+    torch.cuda.synchronize()
+    r1 = _bf16(oracle.causal(q, k, v)[0])
+    r2 = _bf16(oracle.noncausal(r1, k, v)[0])
+    r3 = _bf16(oracle.causal(q, r2, v)[0])
+    r4 = oracle.noncausal(r3, r3, r1)[0]
+    assert row_rel_err(o3, r3) <= TOL_BF16
+    assert row_rel_err(o4, r4) <= TOL_BF16
+
+
+def test_back_to_back_decode_steps_feed_their_outputs_forward():
+    """Decode steps whose query is the previous step's output, issued back to
+    back (the state is read and rewritten in place by every step)."""
+    B, H, D, steps = 3, 4, 64, 6
+    S0, z0 = inputs.state(B, H, D, D, seed=96)
+    _, ks, vs = inputs.decode_tokens(steps, B, H, D, D, torch.bfloat16, seed=97)
+    q0 = inputs.decode_tokens(1, B, H, D, D, torch.bfloat16, seed=98)[0][0]
+    S, z = _dev(S0.clone(), z0.clone())
+    ys, y = [], q0.to(DEV)
+    for t in range(steps):
+        y = la.la_decode_step(y, *_dev(ks[t], vs[t]), S, z)
+        ys.append(y)
+    torch.cuda.synchronize()
+    Sr, zr = S0.double().numpy().copy(), z0.double().numpy().copy()
+    yr = q0
+    for t in range(steps):
+        yr = _bf16(oracle.decode_step(yr, ks[t], vs[t], Sr, zr))
+        assert row_rel_err(ys[t], yr) <= TOL_BF16
+    assert head_rel_err(S, Sr) <= 1e-5
+
+
 # ------------------------------------------------------------------- decode
 
 @pytest.mark.parametrize("dtype,D,M", [(torch.float32, 16, 16), (torch.float32, 64, 64),
