@@ -68,8 +68,8 @@ constexpr int kDUS = 68;                                       // row stride of 
 constexpr int kDOffU = kDOffL + kDLBytes;                      // U work rows [128][kDUS] fp32
 constexpr int kDOffA = kDOffU + kC * kDUS * 4;                   // a block's right-hand sides and solution, 2 x [16][64] fp32
 constexpr int kDOffT = kDOffA + 2 * 16 * 64 * 4;               // diagonal block inverses [8][16][16] fp32
-constexpr int kDOffB = kDOffT + 8 * 16 * 16 * 4;               // beta [128] fp32
-constexpr int kDOffBar = kDOffB + kC * 4;
+constexpr int kDOffB = kDOffT + 8 * 16 * 16 * 4;               // beta [2][128] fp32, by chunk parity
+constexpr int kDOffBar = kDOffB + 2 * kC * 4;
 constexpr int kDOffSlot = kDOffBar + 8 * 4;
 constexpr int kDeltaSmem = kDOffSlot + 16;
 static_assert(kDOffL % 1024 == 0 && kDOffSnap % 1024 == 0, "swizzled operand tiles need 1024-byte alignment");
@@ -213,18 +213,26 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         const int valid = min(kC, N - t0);
         uint8_t *st = smem + s * kDStage;
         uint8_t *tq = st, *tk = st + kDTile, *tv = st + 2 * kDTile;
+        float *bs_c = bs + kC * s;
         DELTA_TRACE(it, 0);
         if (tid == 0 && it + 1 < nch) load_chunk(s ^ 1, t0 + kC);
-        if (wg == 1) bs[r] = r < valid ? __bfloat162float(args.beta[(size_t)bh * N + t0 + r]) : 0.f;
-        const bool landed = mbar_wait_bounded(&full[s], (it >> 1) & 1, now_ns() + kWaitNs, nullptr);
-        if (!landed && tid == 0) record_error(args.err, kErrTimeout);
-        if (!(ok = __syncthreads_and(landed) != 0)) break;
-        ++consumed;
-        DELTA_TRACE(it, 1);
+        // the next chunk's beta, loaded now and stored under this chunk's last
+        // products, so that the load's latency passes under this chunk's work
+        const int valid1 = it + 1 < nch ? min(kC, N - t0 - kC) : 0;
+        const float b_next = (wg == 1 && r < valid1) ? __bfloat162float(args.beta[(size_t)bh * N + t0 + kC + r]) : 0.f;
         // ---- features in place: K rows (rows past the end zeroed) by the first
-        // warpgroup, Q rows by the second
-        feature_row<kDF>(wg == 0 ? tk : tq, r, wg == 0 ? valid : kC, args.feat, args.dr, args.nu, true);
-        delta_operands_ready();
+        // warpgroup, Q rows by the second; the first chunk's here, every later
+        // chunk's (and its beta) under the previous chunk's last products
+        if (it == 0) {
+            if (wg == 1) bs_c[r] = r < valid ? __bfloat162float(args.beta[(size_t)bh * N + t0 + r]) : 0.f;
+            const bool landed = mbar_wait_bounded(&full[s], 0, now_ns() + kWaitNs, nullptr);
+            if (!landed && tid == 0) record_error(args.err, kErrTimeout);
+            if (!(ok = __syncthreads_and(landed) != 0)) break;
+            ++consumed;
+            feature_row<kDF>(wg == 0 ? tk : tq, r, wg == 0 ? valid : kC, args.feat, args.dr, args.nu, true);
+            delta_operands_ready();
+        }
+        DELTA_TRACE(it, 1);
         DELTA_TRACE(it, 2);
         const uint32_t aq = smem_u32(tq), ak = smem_u32(tk), as = smem_u32(snap);
         // ---- G = K K^T, P = Q K^T, W = K S_0 (S as hi + lo)
@@ -250,7 +258,7 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         if (wg == 0) {
             // row r of L = diag(beta) tril(G, -1) into the column blocks that hold
             // row r (zeros on and above the diagonal); P masked to j <= r as bf16 in place
-            const float br = bs[r];
+            const float br = bs_c[r];
 #pragma unroll 1
             for (int c0 = 0; c0 < kC; c0 += 32) {
                 if (c0 > 32 * q4 + 31) break;        // warp-uniform: past every row of this warp
@@ -284,7 +292,7 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
             for (int b = 0; b < 4; ++b) tmem_st16(trow + kTColP + 16 * b, packed[b]);
         } else {
             // row r of the right-hand side diag(beta) (V - K S_0), fp32
-            const float br = bs[r];
+            const float br = bs_c[r];
             float w[64];
             tmem_ld32f(trow + kTColW, *reinterpret_cast<float(*)[32]>(w));
             tmem_ld32f(trow + kTColW + 32, *reinterpret_cast<float(*)[32]>(w + 32));
@@ -451,10 +459,27 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     mma_f16_ss(tmem + kTColS, da + mnmajor_step(ks), du + mnmajor_step(ks), ID_S, 1);
             }
         }
+        // meanwhile the next chunk's beta and feature maps (its tiles were
+        // requested at the top of this chunk)
+        bool nxt = true;
+        if (it + 1 < nch) {
+            if (wg == 1) bs[kC * (s ^ 1) + r] = b_next;
+            nxt = mbar_wait_bounded(&full[s ^ 1], ((it + 1) >> 1) & 1, now_ns() + kWaitNs, nullptr);
+            if (nxt) {
+                uint8_t *st1 = smem + (s ^ 1) * kDStage;
+                feature_row<kDF>(wg == 0 ? st1 + kDTile : st1, r, wg == 0 ? valid1 : kC, args.feat, args.dr, args.nu,
+                                 true);
+            }
+        }
         if (!(ok = delta_mma_sync(mbar, phase, ok, args.err))) {
             mma_pending = true;
             break;
         }
+        if (!(ok = __syncthreads_and(nxt) != 0)) {
+            if (tid == 0) record_error(args.err, kErrTimeout);
+            break;
+        }
+        if (it + 1 < nch) ++consumed;
         // ---- output rows; the new state's bf16 snapshot for the next chunk
         if (wg == 0) {
             if (args.out) {                          // warp-uniform: the TMEM loads are warp-collective
