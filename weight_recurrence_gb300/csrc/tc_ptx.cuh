@@ -86,6 +86,15 @@ __device__ __forceinline__ void tma_load_3d(void *smem_dst, const void *tmap, ui
         : "memory");
 }
 
+// 3-D tiled prefetch of a box into L2 (a hint: no completion, no data moved
+// to shared memory; boxes past the tensor's extent are clipped).
+__device__ __forceinline__ void tma_prefetch_3d(const void *tmap, int x, int y, int z) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(tmap)),
+                 "r"(x), "r"(y), "r"(z)
+                 : "memory");
+}
+
 // 3-D tiled store shared -> global (rows past the tensor's extent are not written).
 __device__ __forceinline__ void tma_store_3d(const void *tmap, const void *smem_src, int x, int y, int z) {
     asm volatile(
