@@ -81,12 +81,6 @@ __device__ __forceinline__ float feature_raw(const T *x, int f, int fm, int D, i
     return to_f32(x[a]) * to_f32(x[b]);
 }
 
-__device__ __forceinline__ float half_warp_sum(float x) {
-#pragma unroll
-    for (int o = kFwG / 2; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-    return x;
-}
-
 __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);

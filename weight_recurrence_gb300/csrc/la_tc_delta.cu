@@ -99,7 +99,6 @@ struct DeltaArgs {
 __device__ __forceinline__ int lblk(int b) { return 16 * (128 * b - 8 * b * (b - 1)); }
 __device__ __forceinline__ int lrow16(int i, int b) { return lblk(b) + (i - 16 * b) * 16; }
 __device__ __forceinline__ int lslot(int i, int j4) { return 4 * (j4 ^ ((i >> 1) & 3)); }
-__device__ __forceinline__ int lidx(int i, int b, int j) { return lrow16(i, b) + lslot(i, j >> 2) + (j & 3); }
 
 // Thread 0 commits the MMAs it issued to `bar`; every thread waits for that
 // phase.  CTA-uniform result: false if any wait gave up (the phase is then
