@@ -74,13 +74,15 @@ constexpr uint32_t kBwdTmemCols = 512;
 static_assert(kBwdSmem <= (int)kSmemMax, "shared memory budget");
 static_assert(kOffGT % 1024 == 0 && kOffPsi % 1024 == 0 && kOffSnap % 1024 == 0, "swizzled tiles on 1 KB");
 
-// TMEM columns.  Pass 1: P, then A, in [0, 128); num in [128, 192); dphi(Q)
-// in [192, 256); S in [256, 320); P as bf16 hi parts in [320, 384) (later A
-// as bf16) and lo parts in [384, 448).  Pass 2: P^T in [0, 128) (bf16 in
-// [0, 64)), A^T in [128, 256) (bf16 in [128, 192)); dV in [256, 320);
-// dphi(K) in [320, 384); R in [384, 448).
-constexpr uint32_t kColP = 0, kColNum = 128, kColDQ = 192, kColS = 256, kColPH = 320, kColPL = 384;
-constexpr uint32_t kColA2 = 128, kColDV = 256, kColDK = 320, kColR = 384;
+// TMEM columns.  Pass 1: P, then A, in [0, 128); num in [128, 256) as two
+// halves to be added (P V + phi(Q) S_hi, then phi(Q) S_lo: one N = 128
+// product against [S_hi | S_lo]); S in [256, 320); P as bf16 hi parts in
+// [320, 384) (later A as bf16) and lo parts in [384, 448); dphi(Q) in
+// [448, 512).  Pass 2: P^T in [0, 128) (bf16 in [0, 64)), A^T in [128, 256)
+// (bf16 in [128, 192)); dV in [256, 384) as two halves (P^T g + phi(K) R_hi,
+// then phi(K) R_lo); R in [384, 448); dphi(K) in [448, 512).
+constexpr uint32_t kColP = 0, kColNum = 128, kColS = 256, kColPH = 320, kColPL = 384, kColDQ = 448;
+constexpr uint32_t kColA2 = 128, kColDV = 256, kColR = 384, kColDK = 448;
 
 struct BwdArgs {
     float *e_ws;             // [BH, N]
@@ -347,6 +349,7 @@ bwd_tc_pass1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     uint32_t ph0 = 0, ph1 = 0, ph2 = 0;
     constexpr uint32_t ID_P = idesc_bf16(128, 128, 0, 0);     // K-major A and B
     constexpr uint32_t ID_MN = idesc_bf16(128, kBD, 0, 1);    // K-major A, MN-major B
+    constexpr uint32_t ID_MN2 = idesc_bf16(128, 2 * kBD, 0, 1);   // ... N = 128: [hi | lo] of the state
     constexpr uint32_t ID_KK = idesc_bf16(128, kBD, 0, 0);    // K-major A and B
     constexpr uint32_t ID_S = idesc_bf16(128, kBD, 1, 1);     // MN-major A and B
     for (int it = 0; it < nch && ok; ++it) {
@@ -405,21 +408,18 @@ bwd_tc_pass1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         if (tid < kBD) zn[tid] = zc[tid] + colsum_total(part, tid);
         const bool valid = t0 + r < N;
         const float inv = valid ? 1.f / (xr[r] + xr[kC + r]) : 0.f;
-        // num = P V + phi(Q) S
+        // num = phi(Q) [S_hi | S_lo] (one N = 128 product: the snapshot's lo part
+        // is its second 64-column atom), then + P V into the first half
         if (tid == 0) {
-            const uint64_t dv = smem_desc(av, kC * 128, 1024), ds = smem_desc(as, kBD * 128, 1024);
+            const uint64_t dv = smem_desc(av, kC * 128, 1024), ds = smem_desc(as, kSnap, 1024);
+#pragma unroll
+            for (int ks = 0; ks < kBD / 16; ++ks)
+                mma_f16_ss(tmem + kColNum, kmajor_base(aq) + kmajor_step(ks), ds + mnmajor_step(ks), ID_MN2, ks > 0);
 #pragma unroll
             for (int part2 = 0; part2 < 2; ++part2)
 #pragma unroll
                 for (int ks = 0; ks < kC / 16; ++ks)
-                    mma_f16_ts(tmem + kColNum, tmem + (part2 ? kColPL : kColPH) + ks * 8, dv + mnmajor_step(ks), ID_MN,
-                               part2 > 0 || ks > 0);
-#pragma unroll
-            for (int part2 = 0; part2 < 2; ++part2)
-#pragma unroll
-                for (int ks = 0; ks < kBD / 16; ++ks)
-                    mma_f16_ss(tmem + kColNum, kmajor_base(aq) + kmajor_step(ks),
-                               ds + (uint64_t)(part2 * kSnap / 16) + mnmajor_step(ks), ID_MN, 1);
+                    mma_f16_ts(tmem + kColNum, tmem + (part2 ? kColPL : kColPH) + ks * 8, dv + mnmajor_step(ks), ID_MN, 1);
             mma_commit(&mbar[1]);
         }
         // meanwhile g_i = dO_i / den_i (columns 32h..32h+31 by warpgroup h),
@@ -463,11 +463,12 @@ bwd_tc_pass1_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         mine = mma_wait(&mbar[1], ph1) && nxt;
         BWD_TRACE(0, it, 4);
         {
-            float num[32];
+            float num[32], lo[32];
             tmem_ld32f(trow + kColNum + 32 * wg, num);
+            tmem_ld32f(trow + kColNum + kBD + 32 * wg, lo);
             float gn = 0.f;
 #pragma unroll
-            for (int c = 0; c < 32; ++c) gn = fmaf(g[c], num[c], gn);
+            for (int c = 0; c < 32; ++c) gn = fmaf(g[c], num[c] + lo[c], gn);
             xg[wg * kC + r] = gn;
         }
         if (!(ok = barrier_and(mine, args.err))) break;
@@ -590,6 +591,7 @@ bwd_tc_pass2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     uint32_t ph0 = 0, ph1 = 0, ph2 = 0;
     constexpr uint32_t ID_P = idesc_bf16(128, 128, 0, 0);
     constexpr uint32_t ID_MN = idesc_bf16(128, kBD, 0, 1);
+    constexpr uint32_t ID_MN2 = idesc_bf16(128, 2 * kBD, 0, 1);
     constexpr uint32_t ID_KK = idesc_bf16(128, kBD, 0, 0);
     constexpr uint32_t ID_S = idesc_bf16(128, kBD, 1, 1);
     for (int it = 0; it < nch && ok; ++it) {
@@ -657,19 +659,17 @@ bwd_tc_pass2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         BWD_TRACE(1, it, 3);
         if (tid < kBD) rn[tid] = rc[tid] + colsum_total(part, tid);
         const float asum = xa[r];
-        // dV = P^T g + phi(K) R;  dphi(K) = A^T psi(Q) + V R^T (+ asum)
+        // dV = phi(K) [R_hi | R_lo] (one N = 128 product) + P^T g into its first
+        // half;  dphi(K) = A^T psi(Q) + V R^T (+ asum)
         if (tid == 0) {
             const uint64_t dg = smem_desc(ag, kC * 128, 1024), dqm = smem_desc(smem_u32(psi_c), kC * 128, 1024);
-            const uint64_t ds = smem_desc(as, kBD * 128, 1024);
+            const uint64_t ds = smem_desc(as, kSnap, 1024);
+#pragma unroll
+            for (int ks = 0; ks < kBD / 16; ++ks)
+                mma_f16_ss(tmem + kColDV, kmajor_base(ak) + kmajor_step(ks), ds + mnmajor_step(ks), ID_MN2, ks > 0);
 #pragma unroll
             for (int ks = 0; ks < kC / 16; ++ks)
-                mma_f16_ts(tmem + kColDV, tmem + kColP + ks * 8, dg + mnmajor_step(ks), ID_MN, ks > 0);
-#pragma unroll
-            for (int part2 = 0; part2 < 2; ++part2)
-#pragma unroll
-                for (int ks = 0; ks < kBD / 16; ++ks)
-                    mma_f16_ss(tmem + kColDV, kmajor_base(ak) + kmajor_step(ks),
-                               ds + (uint64_t)(part2 * kSnap / 16) + mnmajor_step(ks), ID_MN, 1);
+                mma_f16_ts(tmem + kColDV, tmem + kColP + ks * 8, dg + mnmajor_step(ks), ID_MN, 1);
             mma_commit(&mbar[2]);
 #pragma unroll
             for (int ks = 0; ks < kC / 16; ++ks)
@@ -701,7 +701,13 @@ bwd_tc_pass2_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         float x[32];
         mine = mma_wait(&mbar[2], ph2) && mine;
         BWD_TRACE(1, it, 4);
-        tmem_ld32f(trow + kColDV + 32 * wg, x);
+        {
+            float lo[32];
+            tmem_ld32f(trow + kColDV + 32 * wg, x);
+            tmem_ld32f(trow + kColDV + kBD + 32 * wg, lo);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) x[c] += lo[c];
+        }
         mine = mma_wait(&mbar[0], ph0) && mine;
         BWD_TRACE(1, it, 5);
         store_snap32<kC>(tv, r, 32 * wg, x);
