@@ -76,6 +76,10 @@ CASES = [
     (1, 2, 77, 64, 64, torch.bfloat16, 0.125),
     (2, 1, 128, 64, 64, torch.bfloat16, 1.0),
     (1, 3, 645, 64, 64, torch.bfloat16, 0.5),
+    # two chunks exactly, and a last chunk of one row (the sweeps prepare the
+    # next chunk's feature maps while the current one's products run)
+    (1, 2, 256, 64, 64, torch.bfloat16, 0.25),
+    (2, 1, 129, 64, 64, torch.bfloat16, 0.25),
 ]
 
 

@@ -88,6 +88,7 @@ TC_CASES = [
     ("elu1", 1, "sum", "delta", 1, 1, 1, 64, 64, torch.bfloat16, 1.0),
     ("dpfp", 1, "sum", "delta", 2, 1, 777, 32, 64, torch.bfloat16, 0.25),
     ("dpfp", 2, "sum", "delta", 1, 2, 129, 16, 64, torch.bfloat16, 0.5),
+    ("elu1", 1, "sum", "delta", 2, 1, 256, 64, 64, torch.bfloat16, 0.25),   # two chunks exactly
 ]
 
 
