@@ -22,15 +22,20 @@
 // t % 128 of every 128-row accumulator (TMEM lane t % 128), and the two
 // warpgroups split each CUDA-core phase by columns (or by operand), meeting
 // in shared memory where a row reduction spans both halves.  The phases of a
-// chunk run one after the other, the next chunk's tiles loading by TMA
-// meanwhile (two stages); the state products (S += phi(K)^T V in pass 1,
-// R += phi(Q)^T g in pass 2) and the column sums of Z and r are issued with
-// the chunk's first product, since the chunk's own gradient terms read the
-// bf16 snapshot of the state taken before it.  g, dQ, dK and dV leave
-// through TMA stores from swizzled tiles (dQ, dK and dV from stage tiles
-// whose last reader has finished); the next chunk's loads are issued after
-// the chunk's first products, once those stores have read their sources.  Every wait is bounded; a
-// CTA that gives up records LA_ERR_TIMEOUT and skips the rest of its work.
+// chunk run one after the other; around them:
+//   - the state products (S += phi(K)^T V in pass 1, R += phi(Q)^T g in
+//     pass 2) and the column sums of Z and r are issued with the chunk's
+//     first product, since the chunk's own gradient terms read the bf16
+//     snapshot of the state taken before it;
+//   - the next chunk's tiles are requested by TMA after the chunk's first
+//     products (two stages), and its feature maps (and, in pass 2, its e)
+//     are computed while the chunk's largest products run;
+//   - the products against the state's bf16 hi and lo parts that share an
+//     A operand run as one N = 128 MMA ([hi | lo] are adjacent atoms);
+//   - g, dQ, dK and dV leave through TMA stores from swizzled tiles (dQ, dK
+//     and dV from stage tiles whose last reader has finished).
+// Every wait is bounded; a CTA that gives up records LA_ERR_TIMEOUT and skips
+// the rest of its work.
 #include "la_common.cuh"
 #include "la_internal.h"
 #include "tc_host.h"
