@@ -30,12 +30,17 @@
 //   warps 7-10  O group: keeps the state (in registers at D = M = 64, adding
 //               each increment; else in TMEM), writes the bf16 shared-memory
 //               snapshot that is the B operand of phi(Q) S_prev, divides the
-//               output rows and stores them straight to global memory;
+//               output rows and writes them out (at D = M = 64 staged in the
+//               stage's dead Q and K tiles for one TMA store per chunk; else
+//               straight from registers);
 //   warps 11-14 feature-map group: applies phi in place to the Q and K tiles as
 //               they land, running ahead of the MMAs by up to NS chunks.
 // The segment-sum and non-causal kernels use warps 0-9 the same way with one
 // epilogue group (320 threads).
-// The state S (D x M) and z (D) stay in TMEM in fp32 for the whole segment.
+// The state S (D x M) and z (D) stay on chip in fp32 for the whole segment.
+// Launches are programmatic (launch_pdl): a CTA's set-up overlaps the previous
+// launch's tail, it may prefetch its first tiles into L2 meanwhile, and one
+// thread waits for the previous grid before any global-memory read.
 // Long sequences with few heads are cut into segments; the state entering
 // segment g is the carried-in state plus the fp32 sums of segments < g,
 // computed beforehand by state_reduce_kernel (two passes, no inter-CTA waits).
