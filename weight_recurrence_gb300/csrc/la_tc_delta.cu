@@ -78,8 +78,14 @@ static_assert(kDeltaSmem <= (int)kSmemMax, "shared memory budget");
 
 // TMEM columns: G = K K^T at [0, 128) (then O at [0, 64)); P = Q K^T at
 // [128, 256) (its masked bf16 form in [128, 192)); W = K S at [256, 320);
-// the fp32 state S at [320, 384) (lanes 0-63).
-constexpr uint32_t kTColG = 0, kTColO = 0, kTColP = 128, kTColW = 256, kTColS = 320;
+// the fp32 state S at [320, 384) (lanes 0-63); the solve's off-diagonal
+// product L[64:128, 0:64] U[0:64] at [384, 448) (lanes 64-127).
+constexpr uint32_t kTColG = 0, kTColO = 0, kTColP = 128, kTColW = 256, kTColS = 320, kTColC = 384;
+// Bytes of L's column blocks 0-3 (the left 64 columns), free once the
+// off-diagonal operand has been built from them: the top half of U goes
+// there as bf16 hi and lo operand tiles ([64 rows][64], 8 KB each).
+constexpr int kDLLeft = 16 * (128 * 4 - 8 * 4 * 3) * 4;
+static_assert(kDLLeft >= 2 * 64 * 128 && kDLLeft % 1024 == 0, "left column blocks hold the U top tiles");
 constexpr uint32_t kDeltaTmemCols = 512;
 
 struct DeltaArgs {
@@ -345,7 +351,10 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
         // right-hand sides in registers: warp g owns rows i = g (mod 8), lane l
         // columns l and l + 32.  For block b the two owned rows of the block go
         // to Ab, are solved with the block's 16 x 16 inverse into Ab2, and every
-        // later owned row takes off L[i][block b] U_b.
+        // later owned row of the same half takes off L[i][block b] U_b.  The
+        // two 64-row halves are solved apart: between them the bottom rows
+        // take off L[64:128, 0:64] U[0:64] in one tensor-core product (L in
+        // bf16, U as bf16 hi + lo), which is 4/7 of the solve's FMAs.
         {
             const int g = tid >> 5, l = tid & 31;
             float acc[16][2];
@@ -355,8 +364,7 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 acc[k][1] = Us[(g + 8 * k) * kDUS + l + 32];
             }
             float *Ab2 = Ab + 16 * 64;
-#pragma unroll
-            for (int b = 0; b < kC / 16; ++b) {
+            auto solve_block = [&](const int b, const int kend) {
                 SOLVE_TRACE(it, b, 0);
                 // the block's rows owned here: local rows g and g + 8 (k = 2b, 2b + 1)
                 Ab[g * 64 + l] = acc[2 * b][0];
@@ -390,7 +398,7 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     ub[j][1] = Ab2[j * 64 + l + 32];
                 }
 #pragma unroll
-                for (int k = 2 * b + 2; k < 16; ++k) {
+                for (int k = 2 * b + 2; k < kend; ++k) {
                     const int row = g + 8 * k;
                     const float *Lr = Lp + lrow16(row, b);
                     float a0 = acc[k][0], a1 = acc[k][1], c0 = 0.f, c1 = 0.f;
@@ -410,7 +418,76 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                     acc[k][1] = a1 + c1;
                 }
                 SOLVE_TRACE(it, b, 2);
+            };
+#pragma unroll
+            for (int b = 0; b < 4; ++b) solve_block(b, 8);
+            // U[0:64] to the work rows
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                Us[(g + 8 * k) * kDUS + l] = acc[k][0];
+                Us[(g + 8 * k) * kDUS + l + 32] = acc[k][1];
             }
+            __syncthreads();
+            // operands of the off-diagonal product: A = L[:, 0:64] as bf16 (rows
+            // 0-63 zero) into the V tile, dead since the right-hand sides were
+            // formed; then U[0:64] as bf16 hi + lo into L's left column blocks
+            {
+                const int row = tid & (kC - 1), c0 = 32 * (tid >> 7);
+                float a[32];
+#pragma unroll
+                for (int j4 = 0; j4 < 8; ++j4) {
+                    const int c = c0 + 4 * j4, b = c >> 4;
+                    float4 lv = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (row >= kDF) lv = *reinterpret_cast<const float4 *>(Lp + lrow16(row, b) + lslot(row, (c & 15) >> 2));
+                    a[4 * j4] = lv.x; a[4 * j4 + 1] = lv.y; a[4 * j4 + 2] = lv.z; a[4 * j4 + 3] = lv.w;
+                }
+                store_snap32<kC>(tv, row, c0, a);
+            }
+            __syncthreads();
+            uint8_t *uth = smem + kDOffL, *utl = uth + kDF * 128;
+            if (tid < 2 * kDF) {
+                const int row = tid & (kDF - 1), c0 = 32 * (tid >> 6);
+                float u[32];
+#pragma unroll
+                for (int j = 0; j < 32; j += 4) {
+                    const float4 x = *reinterpret_cast<const float4 *>(Us + row * kDUS + c0 + j);
+                    u[j] = x.x; u[j + 1] = x.y; u[j + 2] = x.z; u[j + 3] = x.w;
+                }
+                store_hilo32<kDF>(uth, utl, row, c0, u);
+            }
+            delta_operands_ready();
+            if (tid == 0) {
+#pragma unroll
+                for (int part = 0; part < 2; ++part) {
+                    const uint64_t du = smem_desc(smem_u32(part ? utl : uth), kDF * 128, 1024);
+#pragma unroll
+                    for (int ks = 0; ks < kDF / 16; ++ks)
+                        mma_f16_ss(tmem + kTColC, kmajor_base(smem_u32(tv)) + kmajor_step(ks), du + mnmajor_step(ks), ID_MN,
+                                   part > 0 || ks > 0);
+                }
+            }
+            if (!(ok = delta_mma_sync(mbar, phase, ok, args.err))) {
+                mma_pending = true;
+                break;
+            }
+            // the bottom rows' corrections through the work rows (TMEM lanes
+            // 64-127: warps 2, 3 and 6, 7, 32 columns each)
+            if (q4 >= 2) {
+                float cv[32];
+                tmem_ld32f(trow + kTColC + 32 * wg, cv);
+#pragma unroll
+                for (int j = 0; j < 32; j += 4)
+                    *reinterpret_cast<float4 *>(Us + r * kDUS + 32 * wg + j) = make_float4(cv[j], cv[j + 1], cv[j + 2], cv[j + 3]);
+            }
+            __syncthreads();
+#pragma unroll
+            for (int k = 8; k < 16; ++k) {
+                acc[k][0] -= Us[(g + 8 * k) * kDUS + l];
+                acc[k][1] -= Us[(g + 8 * k) * kDUS + l + 32];
+            }
+            __syncthreads();   // the corrections are read before the rows are overwritten below
+#pragma unroll
+            for (int b = 4; b < 8; ++b) solve_block(b, 16);
             // U (all rows) back to the work rows for the tile conversion below
 #pragma unroll
             for (int k = 0; k < 16; ++k) {
