@@ -18,11 +18,14 @@
 // state and U enter as bf16 hi + lo pairs); the triangular solve runs on CUDA
 // cores in fp32, by blocks of 16 rows: rows of block b first take the product
 // with the finished rows before it, then the block's own 16 x 16 unit lower
-// triangular inverse.  One CTA of 256 threads per head; thread r < 128 owns row
-// r of every 128-row accumulator (TMEM lane r), threads 128..255 share the
-// CUDA-core phases.  The next chunk's tiles load by TMA meanwhile (two
-// stages).  Every wait is bounded; a CTA that gives up records LA_ERR_TIMEOUT
-// and skips the rest of its work.
+// triangular inverse.  It is done in two 64-row halves: between them the
+// bottom rows take off L[64:128, 0:64] U[0:64] in one tcgen05 product (L as
+// bf16, U as bf16 hi + lo).  One CTA of 256 threads per head; thread r < 128
+// owns row r of every 128-row accumulator (TMEM lane r), threads 128..255
+// share the CUDA-core phases.  The next chunk's tiles load by TMA meanwhile
+// (two stages), and its beta and feature maps are computed while this chunk's
+// last products run.  Every wait is bounded; a CTA that gives up records
+// LA_ERR_TIMEOUT and skips the rest of its work.
 #include "la_common.cuh"
 #include "la_internal.h"
 #include "tc_host.h"
