@@ -235,6 +235,15 @@ def _exec_flops_causal(w, chunk):
 
 # -------------------------------------------------------------- our arm
 
+def main_config(w, world, l2):
+    """The `config` object of the main line (both arms)."""
+    return {"workload": w.name, "B": w.B, "H": w.H, "N": w.N, "D": w.D, "M": w.M, "chunk": w.chunk,
+            "chunk_note": "passed as chunk=64; the library takes it as a hint and its tcgen05 path groups "
+                          "128 rows (one M=128 tile): the same sums in exact arithmetic",
+            "global_batch": w.B * world, "seq_len": w.N,
+            "parallelism": "dp%d (independent heads per rank)" % world, "l2": l2}
+
+
 def run_ours(args, rank, world, dist):
     import torch
 
@@ -320,7 +329,7 @@ def run_ours(args, rank, world, dist):
     launches_per_call = launches / max(1, args.steps)
     bytes_step = _alg_bytes_fwd(w)
     achieved_gbs = bytes_step / (ms / 1e3) / 1e9
-    chunk_exec = w.chunk if w.chunk else 128
+    chunk_exec = 128   # the tensor-core path's row grouping, whatever chunk hint is passed
     roofline = {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved_gbs / pk["hbm_gbs"], 4), "traffic": _traffic("causal_" + MAIN),
                 "peak_source": pk["source"], "alg_bytes_per_launch": bytes_step,
@@ -338,13 +347,7 @@ def run_ours(args, rank, world, dist):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1)/sqrt(D) bf16; no dataset)",
-        "config": {"workload": MAIN, "B": w.B, "H": w.H, "N": w.N, "D": w.D, "M": w.M,
-                   "chunk": w.chunk, "chunk_configured": 64,
-                   "chunk_note": "tensor-core path regroups by 128-row chunks (one tcgen05 M=128 tile); "
-                                 "same sums as C=64 in exact arithmetic",
-                   "global_batch": w.B * world, "seq_len": w.N,
-                   "parallelism": "dp%d (independent heads per rank)" % world,
-                   "l2": rot.describe(in_bytes)},
+        "config": main_config(w, world, rot.describe(in_bytes)),
         "roofline": roofline, "tensor": tensor, "clocks": clocks, "gpu_launches": launches,
         "wall_s_timed_region": round(t_wall1 - t_wall0, 4),
     }
@@ -415,9 +418,25 @@ def run_ours(args, rank, world, dist):
             result["legs"][name.split("_")[0]] = _leg_variant(torch, la, inputs, name, dev, stream, rot, pk, 5,
                                                               max_over_ranks, world, rank)
 
-    # ------------------------------------------------- CPU baseline (rank 0)
+    # ------------------------------------------------- CPU baselines (rank 0)
     if rank == 0 and not args.no_cpu:
-        result["cpu_baseline"] = cpu_baseline(w, budget_s=args.cpu_seconds)
+        cs = args.cpu_seconds
+        result["cpu_baseline"] = cpu_baseline(w, budget_s=cs)
+        legs = result.get("legs", {})
+        if "noncausal" in legs:
+            legs["noncausal"]["cpu_baseline"] = cpu_baseline(inputs.WORKLOADS["noncausal_b8h8n4096d64"], budget_s=cs)
+        if "long_causal" in legs:
+            # all 16 heads over their first 8192 tokens (the recurrence costs the same per token)
+            legs["long_causal"]["cpu_baseline"] = cpu_baseline(inputs.WORKLOADS["causal_b1h16n65536d128"],
+                                                               budget_s=cs, heads=16, rows=8192)
+        if "decode" in legs:
+            legs["decode"]["cpu_baseline"] = cpu_baseline_decode(inputs.WORKLOADS["decode_b256h16d64"], budget_s=cs)
+        if "backward" in legs:
+            legs["backward"]["cpu_baseline"] = cpu_baseline_backward(w, budget_s=cs)
+        for name in ("delta_b16h8n3072d64", "dpfp_b16h8n3072d64"):
+            key = name.split("_")[0]
+            if key in legs:
+                legs[key]["cpu_baseline"] = cpu_baseline_variant(inputs.WORKLOADS[name], budget_s=cs)
     return result
 
 
@@ -646,30 +665,123 @@ def _leg_decode(torch, la, inputs, dev, stream, rot, pk, args, max_over_ranks, w
 
 # ------------------------------------------------------------ CPU oracle
 
-def cpu_baseline(w, budget_s=4.0):
-    """The fp64 recurrence oracle on the host cores, on a bounded sample of heads."""
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), or 'unknown'."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.split(":")[0].strip() == "Model name":
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":")[0].strip().lower()
+                if key in ("model name", "cpu model"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return "unknown"
+
+
+def _cpu_timed(fn, budget_s):
+    """Seconds per call of fn, repeating it for at least budget_s (and once at least)."""
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        fn()
+        reps += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    return (time.perf_counter() - t0) / reps, reps
+
+
+def _cpu_entry(value, unit, nthreads, sample):
+    return {"value": round(value, 1), "unit": unit, "cores": nthreads,
+            "omp_num_threads": os.environ.get("OMP_NUM_THREADS"), "cpu_model": cpu_model(),
+            "kind": "oracle", "sample": sample}
+
+
+def cpu_baseline(w, budget_s=4.0, heads=None, rows=None):
+    """The fp64 recurrence oracle (eqs. (10)-(12)) on the host cores, on a
+    bounded sample of heads (and of their rows); tokens/s = head-tokens/s / H."""
+    import oracle
+    from weight_recurrence_gb300 import inputs
+
+    oracle.build()
+    nthreads = oracle.max_threads()
+    heads = max(1, min(w.B * w.H, heads or 2 * nthreads))
+    n = min(w.N, rows or w.N)
+    # the sample's own seeded draw, with the workload's shape per head and distribution
+    qs, ks, vs = inputs.qkv(1, heads, n, w.D, w.M, w.dtype, w.scale, seed=w.seed)
+    fn = oracle.noncausal if w.op == "noncausal" else oracle.causal
+    dt, reps = _cpu_timed(lambda: fn(qs, ks, vs, nthreads=nthreads), budget_s)
+    return _cpu_entry(heads * n / dt / w.H, "tokens/s", nthreads,
+                      "%d heads x %d rows of the %d-head, N=%d workload (fp64 %s oracle), %d reps; tokens/s = "
+                      "head-tokens/s / H" % (heads, n, w.B * w.H, w.N,
+                                             "non-causal" if w.op == "noncausal" else "recurrence", reps))
+
+
+def cpu_baseline_decode(w, budget_s=4.0):
+    """The fp64 recurrence over all T decode steps (eqs. (16)-(20), one token at
+    a time from the prefilled state) on a sample of heads, scaled to the whole
+    batch: steps/s = 1 / (time for T steps x (B*H / heads) / T)."""
+    import oracle
+    from weight_recurrence_gb300 import inputs
+
+    oracle.build()
+    nthreads = oracle.max_threads()
+    heads = max(1, min(w.B * w.H, 8 * nthreads))
+    # the sampled heads' own draws (same distributions; the whole batch's
+    # 4096 steps would be 13 GB on the host)
+    qp, kp, vp = inputs.qkv(1, heads, w.N, w.D, w.M, w.dtype, w.scale, seed=w.seed)
+    _, S0, z0 = oracle.causal(qp, kp, vp, want_out=False, nthreads=nthreads)   # the 1024-token prefill
+    qs, ks, vs = inputs.decode_tokens(w.steps, 1, heads, w.D, w.M, w.dtype, seed=w.seed + 1000)
+    # step-major [T, 1, heads, .] -> [1, heads, T, .]: the steps of each head in order
+    per_head = [x.transpose(0, 2).contiguous() for x in (qs, ks, vs)]
+    dt, reps = _cpu_timed(lambda: oracle.causal(*per_head, S0=S0, z0=z0, nthreads=nthreads), budget_s)
+    t_step_all = dt / w.steps * (w.B * w.H) / heads
+    return _cpu_entry(1.0 / t_step_all, "steps/s", nthreads,
+                      "%d of %d heads x all %d steps after the %d-token prefill (fp64 recurrence, one token "
+                      "at a time from the state), %d reps; scaled to all heads"
+                      % (heads, w.B * w.H, w.steps, w.N, reps))
+
+
+def cpu_baseline_backward(w, budget_s=4.0):
+    """The fp64 causal backward oracle on a sample of heads; tokens/s as the forward."""
+    import oracle
+    import torch
+    from weight_recurrence_gb300 import inputs
+
+    oracle.build()
+    nthreads = oracle.max_threads()
+    heads = max(1, min(w.B * w.H, 2 * nthreads))
+    q, k, v = inputs.qkv(1, heads, w.N, w.D, w.M, w.dtype, w.scale, seed=w.seed)
+    g = torch.Generator().manual_seed(w.seed + 2000)
+    G = torch.randn(v.shape, generator=g).to(w.dtype)
+    dt, reps = _cpu_timed(lambda: oracle.causal_backward(q, k, v, G, nthreads=nthreads), budget_s)
+    return _cpu_entry(heads * w.N / dt / w.H, "tokens/s", nthreads,
+                      "%d of %d heads x N=%d (fp64 backward oracle), %d reps; tokens/s = head-tokens/s / H"
+                      % (heads, w.B * w.H, w.N, reps))
+
+
+def cpu_baseline_variant(w, budget_s=4.0):
+    """The fp64 variant recurrence oracle on a sample of heads."""
     import oracle
     from weight_recurrence_gb300 import inputs
 
     oracle.build()
     nthreads = oracle.max_threads()
     heads = max(1, min(w.B * w.H, 2 * nthreads))
-    q, k, v = inputs.workload_inputs(w)
-    qs = q.reshape(-1, w.N, w.D)[:heads].contiguous()
-    ks = k.reshape(-1, w.N, w.D)[:heads].contiguous()
-    vs = v.reshape(-1, w.N, w.M)[:heads].contiguous()
-    t0 = time.perf_counter()
-    reps = 0
-    while True:
-        oracle.causal(qs, ks, vs, nthreads=nthreads)
-        reps += 1
-        if time.perf_counter() - t0 >= budget_s:
-            break
-    dt = (time.perf_counter() - t0) / reps
-    head_tokens_per_s = heads * w.N / dt
-    return {"value": round(head_tokens_per_s / w.H, 1), "unit": "tokens/s", "cores": nthreads, "kind": "oracle",
-            "sample": "%d of %d heads x N=%d (fp64 recurrence), %d reps; tokens/s = head-tokens/s / H"
-                      % (heads, w.B * w.H, w.N, reps)}
+    fm, nu, norm, update = w.variant
+    q, k, v = inputs.qkv(1, heads, w.N, w.D, w.M, w.dtype, w.scale, seed=w.seed)
+    beta = inputs.betas(1, heads, w.N, w.dtype, seed=w.seed + 1000000) if update == "delta" else None
+    dt, reps = _cpu_timed(lambda: oracle.variant_causal(q, k, v, fm=fm, nu=nu, norm=norm, update=update,
+                                                        beta=beta, nthreads=nthreads), budget_s)
+    return _cpu_entry(heads * w.N / dt / w.H, "tokens/s", nthreads,
+                      "%d of %d heads x N=%d (fp64 %s/%s variant recurrence), %d reps; tokens/s = "
+                      "head-tokens/s / H" % (heads, w.B * w.H, w.N, fm, update, reps))
 
 
 def run_reference(args, rank, world):
@@ -698,9 +810,8 @@ def run_reference(args, rank, world):
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded N(0,1)/sqrt(D) bf16 widened to f64)",
-            "config": {"workload": MAIN, "B": w.B, "H": w.H, "N": w.N, "D": w.D, "M": w.M, "chunk": w.chunk},
-            "cpu_baseline": {"value": round(value, 1), "unit": "tokens/s", "cores": nthreads, "kind": "oracle",
-                             "sample": sample},
+            "config": main_config(w, world, "host cores: no GPU cache involved (CPU oracle)"),
+            "cpu_baseline": _cpu_entry(value, "tokens/s", nthreads, sample),
             "e2e": {"value": round(value, 1), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -711,7 +822,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--decode-steps", type=int, default=256, help="flushed decode steps to time")
-    ap.add_argument("--cpu-seconds", type=float, default=4.0)
+    ap.add_argument("--cpu-seconds", type=float, default=3.0, help="time budget of each CPU-baseline leg")
     ap.add_argument("--main-only", action="store_true", help="skip the non-causal, long and decode legs")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")

@@ -100,12 +100,17 @@ la_status la_forward_noncausal(const void *q, const void *k, const void *v, void
 
 /*
  * Causal attention, sec. 3.3 eqs. (9)-(12), computed chunk by chunk: within a
- * chunk of `chunk` rows the masked products phi(Q) phi(K)^T (j <= i, the
- * diagonal kept) multiply V; the rows see earlier chunks through the carried
- * fp32 state (S, z).  This regrouping of the sums of eq. (9) is exact in real
+ * chunk of rows the masked products phi(Q) phi(K)^T (j <= i, the diagonal
+ * kept) multiply V; the rows see earlier chunks through the carried fp32
+ * state (S, z).  This regrouping of the sums of eq. (9) is exact in real
  * arithmetic; results for different chunk lengths differ only by rounding.
  *   out: [B,H,N,M] or NULL (state only, e.g. to prefill a decoder).
- *   chunk: 0 (library default) or 64 or 128; the fp32 SIMT path ignores it.
+ *   chunk: 0 (library default), 64 or 128 (anything else is
+ *      LA_ERR_UNSUPPORTED).  It is a hint, not a contract: the bf16
+ *      tensor-core path (D, M in {64, 128}) always groups 128 rows, one
+ *      tcgen05 M = 128 tile per chunk, and the CUDA-core path (fp32, other
+ *      D, M) always groups 32 rows; every accepted value gives the same
+ *      result up to rounding.
  *   S: [B,H,D,M] fp32, z: [B,H,D] fp32: both NULL (start from s_0 = 0, z_0 = 0,
  *      eqs. (16)-(17)) or both non-NULL: the call starts from the state they
  *      hold and overwrites them with the state after the last token.  Exactly
@@ -172,8 +177,11 @@ la_status la_decode_steps(const void *q, const void *k, const void *v, void *y, 
  *      not wanted).  Chaining the backward of consecutive segments through
  *      dS0 -> dSN reproduces the backward of the whole sequence.
  *   workspace: la_workspace_bytes(LA_OP_CAUSAL_BWD, s, 0) bytes: g and e of
- *      every token, B*H*N*(M+1) floats (no per-token state is stored).
- * Arithmetic fp32 on CUDA cores; errors as la_forward_causal.
+ *      every token (no per-token state is stored).
+ * bf16 with D = M = 64 runs on tensor cores (tcgen05: bf16 operands, the
+ * state and the reverse sums entering the products as bf16 hi + lo pairs,
+ * fp32 accumulation); every other dtype and size runs fp32 arithmetic on
+ * CUDA cores.  Errors as la_forward_causal.
  */
 la_status la_backward_causal(const void *q, const void *k, const void *v, const void *dout,
                              void *dq, void *dk, void *dv, la_shape s,
@@ -226,7 +234,14 @@ la_status la_backward_noncausal(const void *q, const void *k, const void *v, con
  * the state bounded).  Other combinations return LA_ERR_UNSUPPORTED;
  * unknown enum values LA_ERR_INVALID_ARG.
  * State layout: S [B, H, F, M] fp32 (S[f][m]); z [B, H, F] fp32 (LA_NORM_DEN
- * only).  Arithmetic fp32 on CUDA cores for every dtype.
+ * only).  Arithmetic: bf16 inputs of a sum-update variant without the
+ * denominator with F, M in {64, 128} (elu + 1 raw or sum-normalised; DPFP
+ * from D = 64 / nu = 1, D = 32 / nu = 1 or 2, D = 16 / nu = 2 or 4), and of
+ * the delta rule with sum-normalised features of width 64 (elu + 1 at
+ * D = 64, DPFP at D = 32 / nu = 1 or D = 16 / nu = 2) and M = 64, run on
+ * tensor cores (bf16 feature rows and operands, fp32 accumulation and
+ * state; the delta rule's triangular solve in fp32 on CUDA cores); every
+ * other case runs fp32 arithmetic on CUDA cores.
  */
 typedef enum { LA_FM_ELU1 = 0, LA_FM_DPFP = 1, LA_FM_POLY2 = 2 } la_feature_map;
 typedef enum { LA_NORM_DEN = 0, LA_NORM_SUM = 1, LA_NORM_NONE = 2 } la_norm;

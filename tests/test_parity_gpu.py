@@ -3,8 +3,10 @@
 Every case draws seeded inputs from weight_recurrence_gb300.inputs, runs the
 library on cuda:0, and compares with the oracle on the same values:
 fp32 inputs within 1e-4, bf16 inputs within 2e-2 (per-row relative measure,
-tests/helpers.py).  Small cases compare every element; the full-size
-workloads compare sampled rows with the definition form.
+tests/helpers.py).  Every case compares every output element with the
+recurrence oracle (the full decode workload: six replayed heads); small
+cases and sampled rows of the full-size workloads are also compared with the
+definition form.
 """
 import math
 
@@ -54,6 +56,10 @@ CAUSAL_CASES = [
     (2, 2, 127, 64, 64, torch.bfloat16, 1.0, 0),
     (1, 3, 200, 16, 32, torch.bfloat16, 1.0, 0),
     (1, 1, 1, 64, 64, torch.bfloat16, 1.0, 0),
+    # large inputs (|x| up to ~20): phi's exponential far from 0 on the tensor path
+    (2, 2, 700, 64, 64, torch.bfloat16, 4.0, 0),
+    (1, 2, 400, 128, 128, torch.bfloat16, 3.0, 0),
+    (1, 2, 300, 64, 128, torch.bfloat16, 5.0, 0),
     # long sequences with few heads: split into segments (two-pass state carry)
     (1, 2, 5000, 64, 64, torch.bfloat16, 0.125, 0),
     (1, 1, 9000, 128, 128, torch.bfloat16, 1.0 / math.sqrt(128), 0),
@@ -195,6 +201,10 @@ NC_CASES = [
     (2, 2, 333, 64, 128, torch.bfloat16, 1.0),
     (1, 2, 200, 128, 64, torch.bfloat16, 1.0),
     (2, 2, 100, 16, 64, torch.bfloat16, 1.0),
+    # large inputs on the tensor path
+    (2, 2, 700, 64, 64, torch.bfloat16, 4.0),
+    (1, 2, 500, 128, 128, torch.bfloat16, 5.0),
+    (1, 2, 333, 128, 64, torch.bfloat16, 3.0),
 ]
 
 
@@ -306,37 +316,87 @@ def test_decode_from_zero_state_returns_v():
 
 # ------------------------------------------------------ full-size workloads
 
-def _full_causal(w, heads_to_check, rows_per_head):
+def _row_err_by_head(out, ref):
+    """row_rel_err over [BH, N, M] arrays, one head at a time (bounded host memory)."""
+    worst = 0.0
+    for i in range(out.shape[0]):
+        worst = max(worst, row_rel_err(out[i], ref[i]))
+    return worst
+
+
+def _full_causal(w, chunk=None, spot_heads=3, spot_rows=24):
+    """The full workload in the bench's launch configuration, every element:
+    all rows of all heads against the fp64 recurrence (eqs. (10)-(12)), every
+    head's final S and z, and a few sampled rows against the independent
+    definition form (eq. (9))."""
     q, k, v = inputs.workload_inputs(w)
     qd, kd, vd = _dev(q, k, v)
     S = torch.zeros(w.B, w.H, w.D, w.M, device=DEV)
     z = torch.zeros(w.B, w.H, w.D, device=DEV)
-    out = la.la_forward_causal(qd, kd, vd, chunk=w.chunk, S=S, z=z)
+    out = la.la_forward_causal(qd, kd, vd, chunk=w.chunk if chunk is None else chunk, S=S, z=z)
     torch.cuda.synchronize()
     assert la.la_get_last_error() == la.LA_OK
-    out = out.cpu()
+    del qd, kd, vd
+    out = out.cpu().reshape(w.B * w.H, w.N, w.M)
+    ref, Sref, zref = oracle.causal(q, k, v)
+    err = _row_err_by_head(out, ref.reshape(w.B * w.H, w.N, w.M))
+    assert err <= TOL_BF16, err
+    assert head_rel_err(S.cpu(), Sref) <= TOL_BF16
+    assert head_rel_err(z.cpu(), zref) <= TOL_BF16
+    del ref
     rng = np.random.default_rng(w.seed)
-    worst = 0.0
     flat = [(b, h) for b in range(w.B) for h in range(w.H)]
-    for idx in rng.choice(len(flat), size=min(heads_to_check, len(flat)), replace=False):
+    worst = 0.0
+    for idx in rng.choice(len(flat), size=min(spot_heads, len(flat)), replace=False):
         b, h = flat[idx]
-        rows = sample_rows(w.N, 128, rows_per_head, seed=int(idx))
-        ref = definition_rows(q[b, h], k[b, h], v[b, h], rows, True)
-        worst = max(worst, row_rel_err(out[b, h][rows], ref))
+        rows = sample_rows(w.N, 128, spot_rows, seed=int(idx))
+        d = definition_rows(q[b, h], k[b, h], v[b, h], rows, True)
+        worst = max(worst, row_rel_err(out[b * w.H + h][rows], d))
     assert worst <= TOL_BF16, worst
-    # final state of one head against the recurrence oracle
-    b, h = flat[0]
-    _, Sref, zref = oracle.causal(q[b, h][None], k[b, h][None], v[b, h][None], want_out=False)
-    assert head_rel_err(S[b, h][None].cpu(), Sref, nlead=1) <= TOL_BF16
-    assert head_rel_err(z[b, h][None].cpu(), zref, nlead=1) <= TOL_BF16
 
 
 def test_full_causal_b16h8n3072d64():
-    _full_causal(inputs.WORKLOADS["causal_b16h8n3072d64"], heads_to_check=12, rows_per_head=24)
+    """Every output element of B16 H8 N3072 D64 at the configured chunk hint (64)."""
+    _full_causal(inputs.WORKLOADS["causal_b16h8n3072d64"])
+
+
+def test_full_causal_b16h8n3072d64_default_chunk():
+    _full_causal(inputs.WORKLOADS["causal_b16h8n3072d64"], chunk=0, spot_heads=1)
 
 
 def test_full_causal_b1h16n65536d128():
-    _full_causal(inputs.WORKLOADS["causal_b1h16n65536d128"], heads_to_check=4, rows_per_head=24)
+    """Every output element of the long workload (segments carried through the
+    segment-sum pre-pass)."""
+    _full_causal(inputs.WORKLOADS["causal_b1h16n65536d128"], spot_heads=2, spot_rows=16)
+
+
+def test_full_causal_b16h8n3072d64_three_calls_back_to_back():
+    """Three full-size calls issued back to back with no host synchronisation,
+    each continuing from the state the previous one left (consecutive
+    segments of one 9216-token sequence).  Each launch overlaps its set-up
+    (and its L2 prefetch of its first tiles) with the previous launch's tail;
+    every element of all three outputs and the final state are compared with
+    the recurrence over the whole sequence."""
+    w = inputs.WORKLOADS["causal_b16h8n3072d64"]
+    parts = [inputs.qkv(w.B, w.H, w.N, w.D, w.M, w.dtype, w.scale, seed=w.seed + 100 * (i + 1))
+             for i in range(3)]
+    S = torch.zeros(w.B, w.H, w.D, w.M, device=DEV)
+    z = torch.zeros(w.B, w.H, w.D, device=DEV)
+    devs = [_dev(*p) for p in parts]
+    outs = [torch.empty(w.B, w.H, w.N, w.M, dtype=w.dtype, device=DEV) for _ in range(3)]
+    torch.cuda.synchronize()
+    for (qd, kd, vd), o in zip(devs, outs):
+        la.la_forward_causal(qd, kd, vd, out=o, chunk=w.chunk, S=S, z=z)
+    torch.cuda.synchronize()
+    assert la.la_get_last_error() == la.LA_OK
+    del devs
+    q, k, v = (torch.cat([p[j] for p in parts], dim=2) for j in range(3))
+    ref, Sref, zref = oracle.causal(q, k, v)
+    out = torch.cat([o.cpu() for o in outs], dim=2).reshape(w.B * w.H, 3 * w.N, w.M)
+    err = _row_err_by_head(out, ref.reshape(w.B * w.H, 3 * w.N, w.M))
+    assert err <= TOL_BF16, err
+    assert head_rel_err(S.cpu(), Sref) <= TOL_BF16
+    assert head_rel_err(z.cpu(), zref) <= TOL_BF16
 
 
 def test_full_noncausal_b8h8n4096d64():

@@ -5,13 +5,17 @@ memory (they get pointers from a framework that owns the memory pool, or run
 a loop that must not call the allocator).  Its partial sums live in a fixed
 8 MiB array inside the library.  This test calls it twice in a row through
 the C ABI and checks each result against la_forward_noncausal (which uses a
-caller workspace) within the bf16 / fp32 tolerances of the other tests.
+caller workspace) and against the fp64 oracle, within the bf16 / fp32
+tolerances of the other tests.  One case is large enough that the array
+holds fewer key splits than the workspace entry point would use, so the
+capped split count is exercised too.
 """
 import ctypes
 
 import pytest
 import torch
 
+import oracle
 from tests.helpers import row_rel_err, tol_for
 from weight_recurrence_gb300 import inputs, la
 
@@ -23,6 +27,7 @@ def _setup():
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     la.lib()
+    oracle.build()
 
 
 def _call_noalloc(q, k, v, out):
@@ -35,17 +40,24 @@ def _call_noalloc(q, k, v, out):
 
 @pytest.mark.parametrize("B,H,N,D,M,dtype", [(2, 4, 1000, 64, 64, torch.bfloat16),
                                              (1, 3, 777, 128, 128, torch.bfloat16),
-                                             (2, 2, 300, 32, 64, torch.float32)])
+                                             (2, 2, 300, 32, 64, torch.float32),
+                                             # 16 heads x (128*128 + 128) floats = 1.06 MB per key
+                                             # split: the array holds 7 splits, fewer than the 16
+                                             # the workspace entry point picks for N = 4096
+                                             (4, 4, 4096, 128, 128, torch.bfloat16)])
 def test_noalloc_matches_workspace_entry_point_twice(B, H, N, D, M, dtype):
     outs = []
     for seed in (123, 124):   # two calls in a row, different data
-        q, k, v = [t.cuda() for t in inputs.qkv(B, H, N, D, M, dtype, 0.25, seed=seed)]
+        qh, kh, vh = inputs.qkv(B, H, N, D, M, dtype, 0.25, seed=seed)
+        q, k, v = qh.cuda(), kh.cuda(), vh.cuda()
         ref = la.la_forward_noncausal(q, k, v)
         out = torch.full_like(ref, float("nan"))
         assert _call_noalloc(q, k, v, out) == la.LA_OK
         torch.cuda.synchronize()
         assert la.la_get_last_error() == la.LA_OK
         assert row_rel_err(out, ref) <= tol_for(dtype)
+        exact, _, _ = oracle.noncausal(qh, kh, vh)
+        assert row_rel_err(out, exact) <= tol_for(dtype)
         outs.append(out)
     assert not torch.equal(outs[0], outs[1])
 

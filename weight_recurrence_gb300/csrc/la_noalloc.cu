@@ -51,9 +51,11 @@ extern "C" la_status la_forward_noncausal_noalloc(const void *q, const void *k, 
     for (const void *p : {q, k, v, (const void *)out})
         if (p == nullptr || !aligned16(p)) return LA_ERR_INVALID_ARG;
     if (out == q || out == k || out == v) return LA_ERR_INVALID_ARG;
-    // One split of partial sums needs BH * (D*M + D) floats; at least one must fit.
-    const size_t per_split = (size_t)BH * ((size_t)s.D * s.M + s.D) * sizeof(float);
-    if (per_split > kScratchBytes) return LA_ERR_UNSUPPORTED;
+    // One split of partial sums needs BH * (D*M + D) floats; at least one must
+    // fit.  BH is bounded first, so that the product below cannot wrap.
+    const size_t per_head = ((size_t)s.D * s.M + s.D) * sizeof(float);
+    if (BH > (long long)(kScratchBytes / per_head)) return LA_ERR_UNSUPPORTED;
+    const size_t per_split = (size_t)BH * per_head;
     const int max_splits = (int)(kScratchBytes / per_split);
     const DeviceInfo *dev = device_info();
     float *scratch = scratch_on_current_device();

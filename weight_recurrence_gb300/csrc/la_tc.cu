@@ -1526,7 +1526,9 @@ bool tc_dims(const la_shape &s) {
 
 }  // namespace
 
-bool tc_causal_supported(const la_shape &s, int chunk) { return tc_dims(s) && (chunk == 0 || chunk == 128); }
+// The chunk length is a hint (la.h): every accepted value (0, 64, 128) takes
+// the 128-row regrouping here, one tcgen05 M = 128 tile per chunk.
+bool tc_causal_supported(const la_shape &s, int) { return tc_dims(s); }
 
 bool tc_variant_route(const la_shape &s, const la_variant &v, Problem &p) {
     // sum update without the denominator, bf16, feature width 64 or 128

@@ -49,21 +49,20 @@ __device__ __forceinline__ void set_abort(volatile int *abort, int *err) {
 // Named barrier for the 128 threads of the epilogue group.
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
-// phi(x) = elu(x) + 1 on two bf16 values, written as max(x, 0) + min(e^x, 1):
-// for x > 0 that is x + 1 and for x <= 0 it is e^x.  e^x = 2^(x log2 e) with
-// both steps on packed bf16 pairs: the product x log2 e rounded to bf16 (a
-// relative error of 2^-9 in the exponent, i.e. about |x| 2^-9 in e^x), then
-// the MUFU's packed 2^t, two exponentials per instruction (the feature map of
-// a 128-row chunk is bound by the MUFU rate).  max, min and add also run on
-// the packed pairs.  NaN propagates.
+// phi(x) = elu(x) + 1 of one value in fp32: x + 1 for x > 0, else e^x =
+// 2^(x log2 e) from the MUFU's fp32 exponential (ex2.approx.ftz.f32, relative
+// error about 2^-22; results below 2^-126 flush to zero).  NaN propagates.
+__device__ __forceinline__ float phi_f32(float x) {
+    float e;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(x * 1.4426950408889634f));
+    return x > 0.f ? x + 1.f : e;
+}
+
+// phi of two packed bf16 values: each widened to fp32 (exact), phi_f32, and
+// the pair rounded to nearest-even bf16 once, so every feature value is the
+// correctly rounded bf16 of phi up to the exponential's 2^-22.
 __device__ __forceinline__ uint32_t phi_bf16x2(uint32_t w) {
-    uint32_t t, e, m, n, r;
-    asm("mul.rn.bf16x2 %0, %1, %2;" : "=r"(t) : "r"(w), "r"(0x3FB93FB9u));   // log2(e) = 1.4427 -> bf16 0x3FB9
-    asm("ex2.approx.ftz.bf16x2 %0, %1;" : "=r"(e) : "r"(t));
-    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(m) : "r"(w), "r"(0u));
-    asm("min.NaN.bf16x2 %0, %1, %2;" : "=r"(n) : "r"(e), "r"(0x3F803F80u));
-    asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(m), "r"(n));
-    return r;
+    return pack_bf16x2(phi_f32(__uint_as_float(w << 16)), phi_f32(__uint_as_float(w & 0xFFFF0000u)));
 }
 
 // Applies phi in place to a C x DD tile (sub-tiles of 64 columns, each C rows
@@ -208,9 +207,9 @@ __device__ __forceinline__ void dpfp_row(uint8_t *tile, int r, bool zero) {
     }
 }
 
-// Elementwise: pass 1 maps each 8-column chunk in place with the packed
-// phi_bf16x2 (two exponentials per MUFU instruction) and sums the bf16 results
-// in fp32; pass 2 scales the chunks by 1 / sum (a second bf16 rounding).
+// Elementwise: pass 1 maps each 8-column chunk in place with phi_bf16x2 and
+// sums the bf16 results in fp32; pass 2 scales the chunks by 1 / sum (a
+// second bf16 rounding).
 template <int F>
 __device__ __forceinline__ void elu1_sum_row(uint8_t *tile, int r, bool zero) {
     auto at = [&](int c) { return reinterpret_cast<uint4 *>(tile + (c / 64) * kC * 128 + sw128_offset(r, c % 64)); };

@@ -46,14 +46,14 @@ WORKLOADS = {
     "causal_tiny_f32": Workload("causal_tiny_f32", "causal", 1, 1, 64, 16, 16, torch.float32, 1.0, 0, 0, 1001),
     "noncausal_b8h8n4096d64": Workload("noncausal_b8h8n4096d64", "noncausal", 8, 8, 4096, 64, 64,
                                        torch.bfloat16, 1.0, 0, 0, 1002),
-    # The causal workloads are configured with chunk C = 64; the tensor-core
-    # path regroups the same sums by 128-row chunks (one tcgen05 M = 128 tile),
-    # which is the same computation in exact arithmetic (chunk-length
-    # invariance is a parity test); C = 64 itself runs on the CUDA-core path.
+    # The causal workloads are configured with chunk C = 64.  The library takes
+    # the chunk length as a hint: its tensor-core path groups the same sums by
+    # 128 rows (one tcgen05 M = 128 tile), the same computation in exact
+    # arithmetic (chunk-length invariance is a parity test).
     "causal_b16h8n3072d64": Workload("causal_b16h8n3072d64", "causal", 16, 8, 3072, 64, 64,
-                                     torch.bfloat16, 1.0 / math.sqrt(64), 128, 0, 1003),
+                                     torch.bfloat16, 1.0 / math.sqrt(64), 64, 0, 1003),
     "causal_b1h16n65536d128": Workload("causal_b1h16n65536d128", "causal", 1, 16, 65536, 128, 128,
-                                       torch.bfloat16, 1.0 / math.sqrt(128), 128, 0, 1004),
+                                       torch.bfloat16, 1.0 / math.sqrt(128), 64, 0, 1004),
     "decode_b256h16d64": Workload("decode_b256h16d64", "decode", 256, 16, 1024, 64, 64,
                                   torch.bfloat16, 1.0, 0, 4096, 1005),
     # Variants on the training shape: the delta rule with sum-normalised elu + 1
