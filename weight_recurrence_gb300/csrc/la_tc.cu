@@ -824,6 +824,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     __syncthreads();
     tc_fence_after();
     if (warp == 0) tmem_dealloc(tmem, C::TMEM_COLS);
+    if (tid == 0 && *abort) record_error(args.err, kErrTimeout);
 }
 
 // ------------------------------------------------- state reduction kernel
@@ -1012,6 +1013,7 @@ state_reduce_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
     __syncthreads();
     tc_fence_after();
     if (warp == 0) tmem_dealloc(tmem, C::TMEM_COLS);
+    if (tid == 0 && *abort) record_error(args.err, kErrTimeout);
 }
 
 // ------------------------------------------------ fused non-causal kernel
@@ -1034,7 +1036,11 @@ template <int D, int M>
 struct NCfg {
     static constexpr int TILE_K = kC * D * 2;
     static constexpr int TILE_V = kC * M * 2;
-    static constexpr int STAGE = TILE_K + TILE_V;       // also holds a Q tile and its output tile
+    // The ring is made of units of one tile each: a phase-1 item takes two
+    // consecutive units (its K tile, then its V tile), a phase-2 item one (its
+    // Q tile, then its output tile in place), so that twice as many Q tiles as
+    // K/V pairs can be in flight while the partial sums are exchanged.
+    static constexpr int UNIT = TILE_K > TILE_V ? TILE_K : TILE_V;
     static constexpr bool VONES = (M == 64);            // V read as [V | ones], z in column M
     static constexpr int ONES = VONES ? kC * 128 : kOnesBytes;
     static constexpr int SNAP = D * M * 2 + D * 128;    // M/64 state atoms then the z atom
@@ -1042,14 +1048,20 @@ struct NCfg {
     static constexpr bool SHARE = ONES >= SNAP;
     static constexpr int CTAS_PER_SM = (D == 64 && M == 64) ? 2 : 1;
     static constexpr int BUDGET = (int)kSmemMax / CTAS_PER_SM - 1024;
-    static constexpr int FIXED = (SHARE ? ONES : ONES + SNAP) + 256;
-    static constexpr int NS_FIT = (BUDGET - FIXED) / STAGE;
-    static constexpr int NS = NS_FIT > 4 ? 4 : NS_FIT;
-    static_assert(NS >= 2, "pipeline needs two stages");
-    static constexpr int OFF_ONES = NS * STAGE;
+    // D = M = 64: the partial sums are exchanged through the cluster's shared
+    // memory (clusters of 2, 4 or 8): RECV holds, for the D / G rows this CTA
+    // owns, every CTA's fp32 partial rows and z entries
+    static constexpr bool DSX = (D == 64 && M == 64);
+    static constexpr int RECV = DSX ? D * (M + 1) * 4 : 0;
+    static constexpr int FIXED = (SHARE ? ONES : ONES + SNAP) + RECV + 256;
+    static constexpr int NU_FIT = (BUDGET - FIXED) / UNIT;
+    static constexpr int NU = NU_FIT > 8 ? 8 : NU_FIT;
+    static_assert(NU >= 4, "pipeline needs two phase-1 items in flight");
+    static constexpr int OFF_ONES = NU * UNIT;
     static constexpr int OFF_SNAP = SHARE ? OFF_ONES : OFF_ONES + ONES;
-    static constexpr int NBARS = 3 * NS + 2 + 2 + 4;
-    static constexpr int OFF_BAR = OFF_SNAP + (SHARE ? ONES : SNAP);
+    static constexpr int OFF_RECV = OFF_SNAP + (SHARE ? ONES : SNAP);
+    static constexpr int NBARS = 3 * NU + 3 + 3 + 4 + 2;
+    static constexpr int OFF_BAR = OFF_RECV + RECV;
     static constexpr int OFF_TSLOT = OFF_BAR + 8 * NBARS;
     static constexpr int SMEM = OFF_TSLOT + 16;
     static_assert(SMEM <= BUDGET + 1024, "shared memory budget");
@@ -1058,7 +1070,7 @@ struct NCfg {
     static constexpr uint32_t TMEM_COLS = CTAS_PER_SM == 2 ? 256 : 512;
     static constexpr uint32_t COL_S = 0, COL_Z = M;
     static constexpr int NO = M + 16;                   // numerator, z_hi, z_lo
-    static constexpr int NOBUF = 2 * NO <= (int)TMEM_COLS ? 2 : 1;
+    static constexpr int NOBUF = (int)TMEM_COLS / NO >= 3 ? 3 : (int)TMEM_COLS / NO;
     static __device__ __forceinline__ uint32_t col_o(int b) { return (uint32_t)(b * NO); }
 };
 
@@ -1089,12 +1101,21 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     const int nch_total = (args.N + kC - 1) / kC;
     const int c_begin = g * args.cps;
     const int n = max(0, min(nch_total, c_begin + args.cps) - c_begin);
-    const int total = 2 * n;                 // ring slots used: n K/V tiles, then n Q tiles
+    const int total = 2 * n;                 // ring items: n K/V pairs, then n Q tiles
 
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR);
-    uint64_t *full = bar, *empty = bar + C::NS, *phi_done = bar + 2 * C::NS;
-    uint64_t *o_full = bar + 3 * C::NS, *o_free = o_full + 2;
-    uint64_t *init = o_free + 2, *red_done = init + 1, *snap_bar = red_done + 1, *drain = snap_bar + 1;
+    uint64_t *full = bar, *empty = bar + C::NU, *phi_done = bar + 2 * C::NU;
+    uint64_t *o_full = bar + 3 * C::NU, *o_free = o_full + 3;
+    // Units are used in one global sequence u = 0, 1, 2, ...: K/V pair i takes
+    // units 2i and 2i + 1, Q tile i unit 2n + i.  Use u of a unit is its
+    // (u / NU)-th use, so each of its barriers completes one phase per use.
+    auto unit = [&](int u) { return smem + (u % C::NU) * C::UNIT; };
+    auto ph = [&](int u) { return (uint32_t)((u / C::NU) & 1); };
+    uint64_t *init = o_free + 3, *red_done = init + 1, *snap_bar = red_done + 1, *drain = snap_bar + 1;
+    uint64_t *recv_bar = drain + 1, *snapx_bar = recv_bar + 1;   // exchange through shared memory
+    // partial sums exchanged through the cluster's shared memory (else
+    // through the workspace and L2)
+    const bool dsx = C::DSX && (args.G == 2 || args.G == 4 || args.G == 8);
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + C::OFF_TSLOT);
     uint8_t *ones = smem + C::OFF_ONES;
     uint8_t *snap = smem + C::OFF_SNAP;
@@ -1102,12 +1123,12 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     if (tid == 0) {
         *abort = (smem_u32(smem) & 1023u) ? 1 : 0;
         if (*abort) record_error(args.err, kErrTimeout);
-        for (int s = 0; s < C::NS; ++s) {
+        for (int s = 0; s < C::NU; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);   // phase 1: MMA commit; phase 2: epilogue after the store read the tile
             mbar_init(&phi_done[s], kGrp);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < 3; ++b) {
             mbar_init(&o_full[b], 1);
             mbar_init(&o_free[b], kGrp);
         }
@@ -1115,6 +1136,15 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         mbar_init(red_done, 1);
         mbar_init(snap_bar, kGrp);
         mbar_init(drain, 1);
+        mbar_init(recv_bar, 1);
+        mbar_init(snapx_bar, 1);
+        if (dsx) {
+            // every CTA of the cluster (this one included) stores here, by
+            // st.async, its fp32 partial rows r with r % G == rank (and their z),
+            // then the owners of all D rows store the bf16 snapshot rows
+            mbar_arrive_expect_tx(recv_bar, (uint32_t)C::RECV);
+            mbar_arrive_expect_tx(snapx_bar, (uint32_t)(D * (M / 8 + 1) * 16));
+        }
         fence_mbar_init();
     }
     for (int i = tid; i < C::ONES / 4; i += kThreads) reinterpret_cast<uint32_t *>(ones)[i] = 0u;
@@ -1149,37 +1179,45 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
     pdl_wait_cta();   // set-up above touched no global memory
     if (tid == 0) LA_CTA_AT(1);
     const bool epi = warp >= 2 && warp < 6;
-    // every thread arrives on the cluster barrier exactly once; the epilogue
-    // group only after its partial sums are in the workspace
-    if (!epi) cluster_arrive_release();
+    // Cluster barrier.  Exchange through the workspace: one phase; every
+    // thread arrives once, the epilogue group only after its partial sums are
+    // in the workspace.  Through shared memory: phase A (every thread now:
+    // the barriers above are initialised; the epilogue waits on it before its
+    // first store into another CTA) and phase B at the end (no CTA exits while
+    // another may still store into it).
+    if (dsx || !epi) cluster_arrive_release();
 
     if (warp == 0) {
         // ------------------------------------------------------ producer
         if (lane == 0 && !*abort) {
-            int issued = 0;
+            int u = 0;                   // next unit of the sequence
             for (int idx = 0; idx < total; ++idx) {
-                const int s = idx % C::NS, k = idx / C::NS;
-                if (idx >= C::NS && !wait_bar(&empty[s], (k - 1) & 1, abort)) break;
-                uint8_t *st = smem + s * C::STAGE;
+                const int nun = idx < n ? 2 : 1;
+                bool ok = true;
+                for (int j = 0; j < nun && ok; ++j)
+                    if (u + j >= C::NU) ok = wait_bar(&empty[(u + j) % C::NU], ph(u + j) ^ 1u, abort);
+                if (!ok) break;
                 // DPFP rows arrive raw (at most 64 columns, one box)
                 const int qk_boxes = VAR && args.feat == kFeatDpfp ? 1 : D / 64;
+                uint64_t *f0 = &full[u % C::NU];
                 if (idx < n) {
                     const int t0 = (c_begin + idx) * kC;
-                    mbar_arrive_expect_tx(&full[s], qk_boxes * kC * 128 + C::TILE_V);
-                    for (int j = 0; j < qk_boxes; ++j) tma_load_3d(st + j * kC * 128, &tm_k, &full[s], j * 64, t0, bh);
+                    uint64_t *f1 = &full[(u + 1) % C::NU];
+                    mbar_arrive_expect_tx(f0, qk_boxes * kC * 128);
+                    for (int j = 0; j < qk_boxes; ++j) tma_load_3d(unit(u) + j * kC * 128, &tm_k, f0, j * 64, t0, bh);
+                    mbar_arrive_expect_tx(f1, C::TILE_V);
 #pragma unroll
-                    for (int j = 0; j < M / 64; ++j)
-                        tma_load_3d(st + C::TILE_K + j * kC * 128, &tm_v, &full[s], j * 64, t0, bh);
+                    for (int j = 0; j < M / 64; ++j) tma_load_3d(unit(u + 1) + j * kC * 128, &tm_v, f1, j * 64, t0, bh);
                 } else {
                     const int t0 = (c_begin + idx - n) * kC;
-                    mbar_arrive_expect_tx(&full[s], qk_boxes * kC * 128);
-                    for (int j = 0; j < qk_boxes; ++j) tma_load_3d(st + j * kC * 128, &tm_q, &full[s], j * 64, t0, bh);
+                    mbar_arrive_expect_tx(f0, qk_boxes * kC * 128);
+                    for (int j = 0; j < qk_boxes; ++j) tma_load_3d(unit(u) + j * kC * 128, &tm_q, f0, j * 64, t0, bh);
                 }
-                ++issued;
+                u += nun;
             }
-            if (*abort)
-                for (int idx = max(0, issued - C::NS); idx < issued; ++idx)
-                    mbar_wait_bounded(&full[idx % C::NS], (idx / C::NS) & 1, now_ns() + kWaitNs, nullptr);
+            if (*abort)   // let the copies in flight land before the CTA exits
+                for (int w = max(0, u - C::NU); w < u; ++w)
+                    mbar_wait_bounded(&full[w % C::NU], ph(w), now_ns() + kWaitNs, nullptr);
         }
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer
@@ -1191,10 +1229,11 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             bool ok = wait_bar(init, 0, abort);   // accumulator zeroed
             // phase 1: [S | z] += phi(K)^T [V | 1]
             for (int it = 0; ok && it < n; ++it) {
-                const int s = it % C::NS;
-                if (!(ok = wait_bar(&phi_done[s], (it / C::NS) & 1, abort))) break;
+                const int u = 2 * it;    // K unit; V in unit u + 1
+                if (!(ok = wait_bar(&phi_done[u % C::NU], ph(u), abort))) break;
+                if (!(ok = wait_bar(&full[(u + 1) % C::NU], ph(u + 1), abort))) break;
                 tc_fence_after();
-                const uint32_t ka = smem_u32(smem + s * C::STAGE), va = ka + C::TILE_K;
+                const uint32_t ka = smem_u32(unit(u)), va = smem_u32(unit(u + 1));
                 const uint64_t dk = smem_desc(ka, kC * 128, 1024);
                 const uint64_t dv = smem_desc(va, C::VONES ? ones_a - va : (uint32_t)(kC * 128), 1024);
                 const uint64_t dones = ones_desc(ones_a);
@@ -1203,18 +1242,19 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                     mma_f16_ss(tmem + C::COL_S, dk + mnmajor_step(ks), dv + mnmajor_step(ks), ID_S, 1);
                     if (!C::VONES) mma_f16_ss(tmem + C::COL_Z, dk + mnmajor_step(ks), dones, ID_Z, 1);
                 }
-                mma_commit(&empty[s]);
+                mma_commit(&empty[u % C::NU]);
+                mma_commit(&empty[(u + 1) % C::NU]);
             }
             mma_commit(red_done);
             // phase 2: O = phi(Q) [S | z_hi z_lo]
             ok = ok && wait_bar(snap_bar, 0, abort);
             const uint32_t snap_a = smem_u32(snap);
             for (int i = 0; ok && i < n; ++i) {
-                const int idx = n + i, s = idx % C::NS, ob = i % C::NOBUF, kb = i / C::NOBUF;
-                if (!(ok = wait_bar(&phi_done[s], (idx / C::NS) & 1, abort))) break;
+                const int u = 2 * n + i, ob = i % C::NOBUF, kb = i / C::NOBUF;
+                if (!(ok = wait_bar(&phi_done[u % C::NU], ph(u), abort))) break;
                 if (kb > 0 && !(ok = wait_bar(&o_free[ob], (kb - 1) & 1, abort))) break;
                 tc_fence_after();
-                const uint64_t dq = kmajor_base(smem_u32(smem + s * C::STAGE));
+                const uint64_t dq = kmajor_base(smem_u32(unit(u)));
                 const uint64_t ds = smem_desc(snap_a, D * 128, 1024);
 #pragma unroll
                 for (int ks = 0; ks < D / 16; ++ks)
@@ -1244,9 +1284,90 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         }
         tc_fence_before();
         mbar_arrive(init);
-        // this CTA's partial sums into its workspace slot
         const bool ok1 = wait_bar_warp(red_done, 0, abort);
         if (leader) LA_CTA_AT(3);
+        if (dsx) {
+            // Exchange through shared memory.  Row r of the head's state is owned
+            // by the CTA of rank r % G; every CTA stores its fp32 partial of row r
+            // (and z_r) into the owner's RECV slot of its own rank, the owner sums
+            // the G partials of its D / G rows, rounds them to the bf16 snapshot
+            // [S | z_hi z_lo] and stores those snapshot rows into every CTA of the
+            // cluster (itself included).  Each store counts its bytes on the
+            // receiver's mbarrier.
+            const uint32_t rank = cluster_ctarank();
+            const int G = args.G, RPO = D / G;
+            const uint32_t slot_bytes = (uint32_t)(C::RECV / G);
+            const uint32_t recv_a = smem_u32(smem + C::OFF_RECV);
+            const uint32_t snap_a = smem_u32(snap);
+            cluster_wait_acquire();   // phase A: every CTA's barriers are initialised
+            if (ok1 && swarp) {       // thread r holds row r of this CTA's partial
+                tc_fence_after();
+                const uint32_t owner = (uint32_t)(r % G), i = (uint32_t)(r / G);
+                const uint32_t dst = mapa_shared(recv_a + rank * slot_bytes + i * (M * 4), owner);
+                const uint32_t dbar = mapa_shared(smem_u32(recv_bar), owner);
+#pragma unroll 1
+                for (int c0 = 0; c0 < M; c0 += 32) {
+                    float v[32];
+                    tmem_ld32f(tmem + lane_off + C::COL_S + c0, v);
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4)
+                        st_async_v4(dst + (uint32_t)(c0 + j) * 4u,
+                                    make_uint4(__float_as_uint(v[j]), __float_as_uint(v[j + 1]),
+                                               __float_as_uint(v[j + 2]), __float_as_uint(v[j + 3])),
+                                    dbar);
+                }
+                uint32_t zv[16];
+                tmem_ld16(tmem + lane_off + C::COL_Z, zv);
+                tmem_wait_ld();
+                st_async_b32(mapa_shared(recv_a + rank * slot_bytes + (uint32_t)(RPO * M * 4) + i * 4u, owner), zv[0],
+                             dbar);
+            }
+            tc_fence_before();
+            if (leader) LA_CTA_AT(4);
+            const bool ok2 = ok1 && wait_bar_warp(recv_bar, 0, abort);
+            if (leader) LA_CTA_AT(5);
+            if (ok2) {
+                const int tg = tid - 64;
+                const uint8_t *rb = smem + C::OFF_RECV;
+                // rows this CTA owns, 8 columns per item: the sum of the G slots
+#pragma unroll 1
+                for (int it = tg; it < RPO * (M / 8); it += kGrp) {
+                    const int i = it / (M / 8), c8 = it % (M / 8);
+                    const int row = i * G + (int)rank;
+                    float a[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) a[j] = 0.f;
+#pragma unroll 1
+                    for (int sl = 0; sl < G; ++sl) {
+                        const float4 *pp = reinterpret_cast<const float4 *>(rb + sl * slot_bytes + (i * M + c8 * 8) * 4);
+                        const float4 x0 = pp[0], x1 = pp[1];
+                        a[0] += x0.x; a[1] += x0.y; a[2] += x0.z; a[3] += x0.w;
+                        a[4] += x1.x; a[5] += x1.y; a[6] += x1.z; a[7] += x1.w;
+                    }
+                    const uint4 w = make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]),
+                                               pack_bf16x2(a[4], a[5]), pack_bf16x2(a[6], a[7]));
+                    const uint32_t off = (uint32_t)((c8 / 8) * D * 128) + sw128_offset(row, (c8 % 8) * 8);
+                    for (int t = 0; t < G; ++t)
+                        st_async_v4(mapa_shared(snap_a + off, (uint32_t)t), w, mapa_shared(smem_u32(snapx_bar), (uint32_t)t));
+                }
+                // z of the owned rows as a bf16 pair (hi, lo) in columns 0 and 1
+                // of the z atom; its other columns are the ones tile's zeros
+                for (int i = tg; i < RPO; i += kGrp) {
+                    const int row = i * G + (int)rank;
+                    float zr = 0.f;
+                    for (int sl = 0; sl < G; ++sl)
+                        zr += *reinterpret_cast<const float *>(rb + sl * slot_bytes + RPO * M * 4 + i * 4);
+                    const float hi = __bfloat162float(__float2bfloat16_rn(zr));
+                    const uint4 w = make_uint4(pack_bf16x2(hi, zr - hi), 0u, 0u, 0u);
+                    const uint32_t off = (uint32_t)((M / 64) * D * 128) + sw128_offset(row, 0);
+                    for (int t = 0; t < G; ++t)
+                        st_async_v4(mapa_shared(snap_a + off, (uint32_t)t), w, mapa_shared(smem_u32(snapx_bar), (uint32_t)t));
+                }
+            }
+            // the snapshot is complete once every owner's rows have landed
+            if (ok2) wait_bar_warp(snapx_bar, 0, abort);
+        } else {
+        // this CTA's partial sums into its workspace slot
         if (ok1 && swarp) {
             tc_fence_after();
 #pragma unroll 1
@@ -1331,14 +1452,18 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                 *reinterpret_cast<__nv_bfloat16 *>(za + sw128_offset(r, 1)) = lo;
             }
         }
+        }   // exchange through the workspace
         fence_proxy_async();
         mbar_arrive(snap_bar);
         if (leader) LA_CTA_AT(6);
         if (leader) prefetch_tmap(&tm_o);
+        // the leader hands a unit back once its output store has read it,
+        // checked one tile later so that the store overlaps the next tile
+        int pend = -1;
         for (int i = 0; i < n; ++i) {
-            const int idx = n + i, s = idx % C::NS, ob = i % C::NOBUF, kb = i / C::NOBUF;
+            const int u = 2 * n + i, ob = i % C::NOBUF, kb = i / C::NOBUF;
             const int t0 = (c_begin + i) * kC;
-            uint8_t *tile = smem + s * C::STAGE;   // phi(Q) is dead once o_full fires
+            uint8_t *tile = unit(u);   // phi(Q) is dead once o_full fires
             const bool ok = wait_bar_warp(&o_full[ob], kb & 1, abort);
             if (ok) {
                 tc_fence_after();
@@ -1371,37 +1496,62 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
 #pragma unroll
                     for (int j = 0; j < M / 64; ++j) tma_store_3d(&tm_o, tile + j * kC * 128, j * 64, t0, bh);
                     tma_store_commit();
+                    tma_store_wait_read1();   // every store but this one has read its tile
+                } else {
                     tma_store_wait_read0();
                 }
-                mbar_arrive(&empty[s]);
+                if (pend >= 0) mbar_arrive(&empty[pend % C::NU]);
+                pend = u;
             }
         }
-        if (leader) tma_store_wait_all0();
+        if (leader) {
+            tma_store_wait_read0();
+            if (pend >= 0) mbar_arrive(&empty[pend % C::NU]);
+            tma_store_wait_all0();
+        }
         if (leader) LA_CTA_AT(7);
     } else {
         // ------------------------------------------------------ feature-map group
         // phase 1 K tiles (rows past the sequence end zeroed: they must add
         // nothing), then phase 2 Q tiles
         const int t = tid - 64 - kGrp;
+        int u = 0;
         for (int idx = 0; idx < total; ++idx) {
-            const int s = idx % C::NS;
-            if (wait_bar(&full[s], (idx / C::NS) & 1, abort)) {
+            // the K or Q tile is in unit u; a K/V pair's V unit (u + 1) is the
+            // MMA issuer's to wait for, but its phi_done still completes one
+            // phase per use
+            if (wait_bar(&full[u % C::NU], ph(u), abort)) {
                 if (t == 0 && idx == 0) LA_CTA_AT(2);
                 const int zf = idx < n ? min(kC, args.N - (c_begin + idx) * kC) : kC;
-                if (!VAR || args.feat == kFeatPhi) phi_tile<D>(smem + s * C::STAGE, t, zf);
+                if (!VAR || args.feat == kFeatPhi) phi_tile<D>(unit(u), t, zf);
                 else if constexpr (VAR)   // a variant's feature map, one row per thread
-                    feature_row<D>(smem + s * C::STAGE, t, zf, args.feat, args.dr, args.nu, args.sum_norm);
+                    feature_row<D>(unit(u), t, zf, args.feat, args.dr, args.nu, args.sum_norm);
             }
             fence_proxy_async();
-            mbar_arrive(&phi_done[s]);
+            // the V unit's arrival first: once the MMA issuer has seen every
+            // thread's arrival on the K unit, none is still to arrive on the V
+            // unit for this use (a late arrival would land in its next phase)
+            if (idx < n) mbar_arrive(&phi_done[(u + 1) % C::NU]);
+            mbar_arrive(&phi_done[u % C::NU]);
+            u += idx < n ? 2 : 1;
         }
     }
     if (!epi) cluster_wait_acquire();
+    if (dsx) {
+        // phase B: every CTA has finished storing into the others
+        cluster_arrive_release();
+        cluster_wait_acquire();
+        if (*abort && tid == 0) {   // stores into this CTA that are still in flight land first
+            mbar_wait_bounded(recv_bar, 0, now_ns() + 1000000ull, nullptr);
+            mbar_wait_bounded(snapx_bar, 0, now_ns() + 1000000ull, nullptr);
+        }
+    }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     if (tid == 0) LA_CTA_AT(8);
     if (warp == 0) tmem_dealloc(tmem, C::TMEM_COLS);
+    if (tid == 0 && *abort) record_error(args.err, kErrTimeout);
 }
 
 // ---------------------------------------------------------------- launchers

@@ -29,11 +29,15 @@ constexpr int kOnesBytes = 1024;                 // one 8-row swizzle atom of a 
 
 __device__ __forceinline__ uint64_t now_ns() { return globaltimer_ns(); }
 
-// Bounded wait that also gives up as soon as another role has aborted.
+// Bounded wait that also gives up as soon as another role has aborted.  A
+// wait that gives up raises the CTA's abort flag, so that every role winds
+// down; the kernel records LA_ERR_TIMEOUT at its exit.
 __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort) {
     if (*abort) return false;
     if (mbar_try_wait(bar, parity)) return true;
-    return mbar_wait_bounded(bar, parity, now_ns() + kWaitNs, abort);
+    if (mbar_wait_bounded(bar, parity, now_ns() + kWaitNs, abort)) return true;
+    *abort = 1;
+    return false;
 }
 
 // Warp-uniform variant: the whole warp proceeds only if every lane's wait succeeded.
@@ -49,20 +53,23 @@ __device__ __forceinline__ void set_abort(volatile int *abort, int *err) {
 // Named barrier for the 128 threads of the epilogue group.
 __device__ __forceinline__ void epi_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
-// phi(x) = elu(x) + 1 of one value in fp32: x + 1 for x > 0, else e^x =
-// 2^(x log2 e) from the MUFU's fp32 exponential (ex2.approx.ftz.f32, relative
-// error about 2^-22; results below 2^-126 flush to zero).  NaN propagates.
-__device__ __forceinline__ float phi_f32(float x) {
-    float e;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(x * 1.4426950408889634f));
-    return x > 0.f ? x + 1.f : e;
-}
-
-// phi of two packed bf16 values: each widened to fp32 (exact), phi_f32, and
-// the pair rounded to nearest-even bf16 once, so every feature value is the
-// correctly rounded bf16 of phi up to the exponential's 2^-22.
+// phi(x) = elu(x) + 1 (x + 1 for x > 0, e^x otherwise) of two packed bf16
+// values.  The exponentials in fp32: each value
+// widened (exact), e = 2^(x log2 e) by the MUFU's fp32 exponential, and the
+// pair rounded to bf16 once; the rest on the packed pair: max(x, 0) +
+// min(e, 1), which is x + 1 rounded once for x > 0 and the rounded e itself
+// for x <= 0.  Every feature value is therefore the correctly rounded bf16 of
+// phi, up to the exponential's 2^-22.  NaN propagates.
 __device__ __forceinline__ uint32_t phi_bf16x2(uint32_t w) {
-    return pack_bf16x2(phi_f32(__uint_as_float(w << 16)), phi_f32(__uint_as_float(w & 0xFFFF0000u)));
+    float ea, eb;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(ea) : "f"(__uint_as_float(w << 16) * 1.4426950408889634f));
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(eb) : "f"(__uint_as_float(w & 0xFFFF0000u) * 1.4426950408889634f));
+    const uint32_t e = pack_bf16x2(ea, eb);
+    uint32_t m, n, r;
+    asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(m) : "r"(w), "r"(0u));
+    asm("min.NaN.bf16x2 %0, %1, %2;" : "=r"(n) : "r"(e), "r"(0x3F803F80u));
+    asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(m), "r"(n));
+    return r;
 }
 
 // Applies phi in place to a C x DD tile (sub-tiles of 64 columns, each C rows
