@@ -147,12 +147,18 @@ struct Cfg {
     // (measured choices: at D = M = 128 the feature map, not the stage ring,
     // limits the pipeline).
     static constexpr bool OUT_TMA = DS;
+    // D = M = 64: a stage is two parts with barriers of their own, the Q and K
+    // tiles and the V tile, and the output rows are staged in the V tile.  The
+    // Q and K tiles are handed back as soon as the chunk's MMAs have read them,
+    // so the next loads into the stage (and their feature map, on the critical
+    // path) start before the output store has read the staged rows.
+    static constexpr bool SPLITV = DS;
     static constexpr int NPHI = DS ? 1 : 2;
     static constexpr int THREADS = 32 * (kWarpPhi + 4 * NPHI);
     static constexpr int NDZ = ZMMA ? 1 : 2;           // phi(Q).z_prev hand-over slots (TMEM)
     static constexpr int ONES = O_IN_P ? kC * 128 : kOnesBytes;
     static constexpr int ZS_BYTES = ZMMA ? 0 : 2 * D * 4;
-    static constexpr int NBARS_MAX = 3 * 4 + 4 * 3 + 2 + 5 + 4;
+    static constexpr int NBARS_MAX = 3 * 4 + 4 * 3 + 2 + 5 + 4 + 2 * 4;
     static constexpr int FIXED1 = SNAP + ONES + ZS_BYTES + 8 * NBARS_MAX + 16;
     // two state snapshots when two stages still fit beside them
     static constexpr bool DB = (kSmemMax - FIXED1 - SNAP) / STAGE >= 2;
@@ -161,7 +167,7 @@ struct Cfg {
     static constexpr int NS_FIT = (int)((kSmemMax - FIXED) / STAGE);
     static constexpr int NS = NS_FIT > 4 ? 4 : NS_FIT;
     static_assert(NS >= 2, "pipeline needs two stages");
-    static constexpr int NBARS = 3 * NS + 4 * NPB + NDZ + 5 + 4;
+    static constexpr int NBARS = 3 * NS + 4 * NPB + NDZ + 5 + 4 + 2 * NS;
     static constexpr int OFF_SNAP = NS * STAGE;
     static constexpr int OFF_ONES = OFF_SNAP + NSB * SNAP;
     static constexpr int OFF_Z = OFF_ONES + ONES;           // z snapshots [2][D] fp32 (without ZMMA)
@@ -242,6 +248,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     // barriers, so that no waiter can fall two phases behind one barrier)
     uint64_t *snap_bar = dz_ready + C::NDZ, *s_full = snap_bar + 2, *never = s_full + 1, *drain = never + 1;
     uint64_t *ds_full = drain + 1, *ds_free = ds_full + 2;   // increment buffers (DS)
+    uint64_t *full_v = ds_free + 2, *empty_v = full_v + C::NS;  // the V part of each stage (SPLITV)
     auto snap_wait = [&](int j) { return wait_bar(&snap_bar[j & 1], (j >> 1) & 1, abort); };
     uint32_t *tslot = reinterpret_cast<uint32_t *>(smem + C::OFF_TSLOT);
     uint8_t *snap0 = smem + C::OFF_SNAP;
@@ -260,8 +267,12 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             // released by the output issuer's commit, with DS also by the P
             // issuer's (state increment), and without ZMMA by the P group once it
             // has read phi(Q) for phi(Q).z_prev
-            mbar_init(&empty[s], (C::DS ? 2 : 1) + (C::ZMMA ? 0 : kGrp) + (C::OUT_TMA ? 1 : 0));
+            mbar_init(&empty[s], (C::DS ? 2 : 1) + (C::ZMMA ? 0 : kGrp) + (C::OUT_TMA && !C::SPLITV ? 1 : 0));
             mbar_init(&phi_done[s], C::NPHI * kGrp);
+            // V part: the state increment's and the output MMAs' commits, and the
+            // output store having read the staged rows
+            mbar_init(&full_v[s], 1);
+            mbar_init(&empty_v[s], 3);
         }
         for (int b = 0; b < C::NPB; ++b) {
             mbar_init(&p_full[b], 1);
@@ -336,7 +347,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             prefetch_tmap(&tm_q);
             prefetch_tmap(&tm_k);
             prefetch_tmap(&tm_v);
-            int issued = 0;
+            int issued = 0, issued_v = 0;
             for (int it = 0; it < n; ++it) {
                 const int s = it % C::NS, k = it / C::NS;
                 if (it >= C::NS && !wait_bar(&empty[s], (k - 1) & 1, abort)) break;
@@ -346,18 +357,28 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 // DPFP rows arrive raw (at most 64 columns, one box each), the
                 // feature-map group expands them to the D feature columns
                 const int qk_boxes = VAR && args.feat == kFeatDpfp ? 1 : D / 64;
-                mbar_arrive_expect_tx(&full[s], 2 * qk_boxes * kC * 128 + C::TILE_V);
+                mbar_arrive_expect_tx(&full[s], 2 * qk_boxes * kC * 128 + (C::SPLITV ? 0 : C::TILE_V));
                 for (int j = 0; j < qk_boxes; ++j) tma_load_3d(st + j * kC * 128, &tm_q, &full[s], j * 64, t0, bh);
                 for (int j = 0; j < qk_boxes; ++j)
                     tma_load_3d(st + C::TILE_QK + j * kC * 128, &tm_k, &full[s], j * 64, t0, bh);
+                ++issued;
+                uint64_t *fv = &full[s];
+                if (C::SPLITV) {
+                    if (it >= C::NS && !wait_bar(&empty_v[s], (k - 1) & 1, abort)) break;
+                    fv = &full_v[s];
+                    mbar_arrive_expect_tx(fv, C::TILE_V);
+                }
 #pragma unroll
                 for (int j = 0; j < M / 64; ++j)
-                    tma_load_3d(st + 2 * C::TILE_QK + j * kC * 128, &tm_v, &full[s], j * 64, t0, bh);
-                ++issued;
+                    tma_load_3d(st + 2 * C::TILE_QK + j * kC * 128, &tm_v, fv, j * 64, t0, bh);
+                ++issued_v;
             }
             if (*abort) {   // let the copies in flight land before the CTA exits
                 for (int it = max(0, issued - C::NS); it < issued; ++it)
                     mbar_wait_bounded(&full[it % C::NS], (it / C::NS) & 1, now_ns() + kWaitNs, nullptr);
+                if (C::SPLITV)
+                    for (int it = max(0, issued_v - C::NS); it < issued_v; ++it)
+                        mbar_wait_bounded(&full_v[it % C::NS], (it / C::NS) & 1, now_ns() + kWaitNs, nullptr);
             }
         }
     } else if (warp == 1) {
@@ -390,6 +411,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 LA_TRACE_AT(1, j, 2);
                 if (C::DS) {
                     if (j >= 2 && !wait_bar(&ds_free[j & 1], ((j >> 1) - 1) & 1, abort)) break;
+                    if (C::SPLITV && !wait_bar(&full_v[s], (j / C::NS) & 1, abort)) break;   // V landed
                     LA_TRACE_AT(1, j, 3);
                     tc_fence_after();
                     // A = phi(K)^T read MN-major with M-atom stride 0 (rows 64-127 repeat 0-63)
@@ -399,6 +421,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         mma_f16_ss(tmem + C::col_ds(j), dk + mnmajor_step(ks), dv + mnmajor_step(ks), ID_DS, ks > 0);
                     mma_commit(&ds_full[j & 1]);
                     mma_commit(&empty[s]);
+                    if (C::SPLITV) mma_commit(&empty_v[s]);
                     LA_TRACE_AT(1, j, 4);
                 }
             }
@@ -424,6 +447,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             for (int it = 0; it < n; ++it) {
                 const int s = it % C::NS, pb = it % C::NPB, kb = it / C::NPB;
                 if (!wait_bar(&phi_done[s], (it / C::NS) & 1, abort)) break;
+                if (C::SPLITV && !wait_bar(&full_v[s], (it / C::NS) & 1, abort)) break;   // V landed
                 if (!snap_wait(it)) break;   // S(it-1) has been read out
                 LA_TRACE_AT(4, it, 5);
                 tc_fence_after();
@@ -473,6 +497,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 }
                 mma_commit(&o_full[pb]);
                 mma_commit(&empty[s]);
+                if (C::SPLITV) mma_commit(&empty_v[s]);
                 LA_TRACE_AT(4, it, 7);
             }
         }
@@ -593,7 +618,8 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         auto output_rows = [&](int it) {
             const int pb = it % C::NPB, kb = it / C::NPB;
             const int t = (c_begin + it) * kC + r;
-            uint8_t *stage_out = smem + (it % C::NS) * C::STAGE;
+            // the rows are staged in the stage's V tile (SPLITV) or its Q and K tiles
+            uint8_t *stage_out = smem + (it % C::NS) * C::STAGE + (C::SPLITV ? 2 * C::TILE_QK : 0);
             bool ok = wait_bar_warp(&o_full[pb], kb & 1, abort);
             if (!C::ZMMA) ok = ok && wait_bar_warp(&dz_ready[it % C::NDZ], (it / C::NDZ) & 1, abort);
             if (tracer) LA_TRACE_AT(4, it, 3);
@@ -649,7 +675,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                         tma_store_commit();
                     }
                     tma_store_wait_read0();
-                    mbar_arrive(&empty[it % C::NS]);
+                    mbar_arrive(C::SPLITV ? &empty_v[it % C::NS] : &empty[it % C::NS]);
                 }
             }
             if (tracer) LA_TRACE_AT(4, it, 4);
