@@ -229,6 +229,8 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     if (tid == 0) LA_TRACE_AT(0, 63, 0);
+    LA_CTA_BEGIN();
+    if (tid == 0) LA_CTA_AT(0);
     volatile int *abort = reinterpret_cast<volatile int *>(smem + C::OFF_TSLOT + 4);
 
     const int bh = blockIdx.x / args.nseg, seg = blockIdx.x % args.nseg;
@@ -324,6 +326,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     // everything above read no global memory; from here on the previous
     // launch on the stream has completed and its writes are visible
     pdl_wait_cta();
+    if (tid == 0) LA_CTA_AT(1);
     // this head's sequence length (rows past it are read but ignored)
     const int Nseq = args.lens ? max(0, min(args.N, args.lens[bh / args.H])) : args.N;
     const int nch_total = (Nseq + kC - 1) / kC;
@@ -726,6 +729,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             }
             if (leader && C::OUT_TMA && args.out) tma_store_wait_all0();
             if (leader) LA_TRACE_AT(0, 63, 2);
+            if (leader) LA_CTA_AT(7);
             // state after the last token (last segment only)
             if (S_h && seg == args.nseg - 1 && n > 0 && !*abort) {
 #pragma unroll
@@ -827,6 +831,8 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             if (t == 0) LA_TRACE_AT(3, it, 3 * grp);
             if (wait_bar(&full[s], (it / C::NS) & 1, abort)) {
                 if (t == 0) LA_TRACE_AT(3, it, 3 * grp + 1);
+                if (t == 0 && grp == 0 && it == 0) LA_CTA_AT(2);
+                if (t == 0 && grp == 0 && it == n - 1) LA_CTA_AT(3);
                 uint8_t *st = smem + s * C::STAGE;
                 const int kz = min(kC, Nseq - (c_begin + it) * kC);
                 if (!VAR || args.feat == kFeatPhi) {
@@ -846,6 +852,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     // no MMA may still be running when the CTA frees its TMEM
     if (tid == 0) mbar_wait_bounded(drain, 0, now_ns() + kWaitNs, nullptr);
     if (tid == 0) LA_TRACE_AT(0, 63, 3);
+    if (tid == 0) LA_CTA_AT(8);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
