@@ -644,11 +644,15 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                 uint4 *dst = !C::OUT_TMA && args.out && t < Nseq
                                  ? reinterpret_cast<uint4 *>(args.out + (size_t)bh * args.o_hs + (size_t)t * args.o_rs)
                                  : nullptr;
+                // rows of 256-bit stores when the output's base allows them (each
+                // store of a warp writes one 32-byte sector of 32 rows)
+                const bool v8 = (reinterpret_cast<uintptr_t>(args.out) & 31u) == 0;
 #pragma unroll 1
                 for (int c0 = 0; c0 < M; c0 += 32) {
                     float o[32];
                     tmem_ld32f(tmem + lane_off + C::col_o(pb) + c0, o);
                     if (args.out) {
+                        uint4 w4[4];
 #pragma unroll
                         for (int c8 = 0; c8 < 4; ++c8) {
                             const int c = c0 + 8 * c8;
@@ -657,10 +661,15 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                             w.y = pack_bf16x2(o[8 * c8 + 2] * inv, o[8 * c8 + 3] * inv);
                             w.z = pack_bf16x2(o[8 * c8 + 4] * inv, o[8 * c8 + 5] * inv);
                             w.w = pack_bf16x2(o[8 * c8 + 6] * inv, o[8 * c8 + 7] * inv);
+                            w4[c8] = w;
                             if (C::OUT_TMA)
                                 *reinterpret_cast<uint4 *>(stage_out + (c / 64) * kC * 128 + sw128_offset(r, c % 64)) = w;
-                            else if (dst)
+                            else if (dst && !v8)
                                 dst[c / 8] = w;
+                        }
+                        if (!C::OUT_TMA && dst && v8) {
+                            st_global_v8(dst + c0 / 8, w4[0], w4[1]);
+                            st_global_v8(dst + c0 / 8 + 2, w4[2], w4[3]);
                         }
                     }
                 }
