@@ -567,10 +567,18 @@ delta_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant_
                 tmem_ld32f(trow + kTColO + 32, *reinterpret_cast<float(*)[32]>(o + 32));
                 if (r < valid) {
                     uint4 *dst = reinterpret_cast<uint4 *>(args.out + ((size_t)bh * N + t0 + r) * kDF);
+                    uint4 w[8];
 #pragma unroll
                     for (int c8 = 0; c8 < 8; ++c8)
-                        dst[c8] = make_uint4(pack_bf16x2(o[8 * c8], o[8 * c8 + 1]), pack_bf16x2(o[8 * c8 + 2], o[8 * c8 + 3]),
-                                             pack_bf16x2(o[8 * c8 + 4], o[8 * c8 + 5]), pack_bf16x2(o[8 * c8 + 6], o[8 * c8 + 7]));
+                        w[c8] = make_uint4(pack_bf16x2(o[8 * c8], o[8 * c8 + 1]), pack_bf16x2(o[8 * c8 + 2], o[8 * c8 + 3]),
+                                           pack_bf16x2(o[8 * c8 + 4], o[8 * c8 + 5]), pack_bf16x2(o[8 * c8 + 6], o[8 * c8 + 7]));
+                    if ((reinterpret_cast<uintptr_t>(args.out) & 31u) == 0) {   // 256-bit stores
+#pragma unroll
+                        for (int c16 = 0; c16 < 4; ++c16) st_global_v8(dst + 2 * c16, w[2 * c16], w[2 * c16 + 1]);
+                    } else {
+#pragma unroll
+                        for (int c8 = 0; c8 < 8; ++c8) dst[c8] = w[c8];
+                    }
                 }
             }
         } else if (r < kDF) {
