@@ -62,7 +62,8 @@ typedef enum {
     LA_ERR_INVALID_ARG = 1,
     LA_ERR_UNSUPPORTED = 2,
     LA_ERR_CUDA = 3,
-    LA_ERR_TIMEOUT = 4
+    LA_ERR_TIMEOUT = 4,
+    LA_ERR_BOUNDS = 5      /* checked build only: an access outside a buffer was caught and skipped */
 } la_status;
 
 typedef enum { LA_DTYPE_F32 = 0, LA_DTYPE_BF16 = 1 } la_dtype;
@@ -339,6 +340,37 @@ int la_version(void);
  * (all devices).  Benchmarks read it before and after a timed region.
  */
 unsigned long long la_launch_count(void);
+
+/*
+ * 1 if this library is the checked build (liblinattn_checked.so, compiled
+ * with -DLA_CHECKED), 0 for the release build (liblinattn.so).  The checked
+ * build has no counterpart in the method: it is the release kernels with a
+ * bounds check in front of each global-memory access whose index is computed
+ * from run-time values other than the launch grid -- in the causal
+ * tensor-core kernel the per-sequence length read, the carried-in state and
+ * segment-workspace loads, the final-state stores and the direct output-row
+ * stores; in the segment-sum pre-pass its workspace slot writes; in the
+ * non-causal tensor-core kernel (exchange through the workspace) and in the
+ * non-causal CUDA-core kernels (also used by la_forward_noncausal_noalloc)
+ * the workspace slot writes and reads.  TMA copies are clipped to their tensor
+ * maps by the hardware, and the decode kernels index by block and thread
+ * alone, so neither carries a check.  A failed check skips its access and
+ * records LA_ERR_BOUNDS in the device error word, which la_get_last_error()
+ * reports; nothing traps.  Results are otherwise identical to the release
+ * build's; it is slower and meant for testing.
+ */
+int la_checked_build(void);
+
+/*
+ * Test hook of the checked build (a no-op in the release build): while
+ * `enable` is non-zero, launches made by this process index past a buffer on
+ * purpose, where the check catches it: the causal tensor-core kernel offsets
+ * the rows of its carried-in state loads by D, the segment-sum pre-pass and
+ * the non-causal CUDA-core reduction offset their workspace slot by the
+ * workspace's whole length.  The call then reports LA_ERR_BOUNDS, and no access left
+ * its buffer.
+ */
+void la_debug_inject_bounds(int enable);
 
 /*
  * Test hook (no counterpart in the method): when `enable` is non-zero, the

@@ -39,8 +39,9 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_status_strings(lib):
-    for st in range(5):
+    for st in range(6):
         assert la.status_string(st)
+    assert la.status_string(la.LA_ERR_BOUNDS) != la.status_string(la.LA_ERR_TIMEOUT)
     assert la.status_string(la.LA_ERR_TIMEOUT) != la.status_string(la.LA_OK)
     assert la.la_version() >= 10000
 
@@ -213,3 +214,22 @@ def test_variant_argument_checks(lib):
     assert dec(q, k, v, None, o, None, None, sh, V("elu1", 1, "sum"), None) == la.LA_ERR_INVALID_ARG
     assert dec(q, k, v, None, o, S, None, sh, V("elu1", 1, "sum", "delta"), None) == la.LA_ERR_INVALID_ARG
     assert dec(None, None, None, None, None, None, None, _shape(B=0), V(), None) == la.LA_OK
+
+
+def test_checked_build_exports_the_same_abi(lib):
+    """The bounds-checked twin builds from the same sources, exports every
+    declared entry point and says which build it is."""
+    path = labuild.build(checked=True)
+    assert path == la.LIB_CHECKED_PATH
+    checked = la._load(path)
+    for name in _declared():
+        assert ctypes.cast(getattr(checked, name), ctypes.c_void_p).value, name
+    assert checked.la_checked_build() == 1
+    assert lib.la_checked_build() == 0
+    # selecting a build routes the module's calls, and back
+    try:
+        assert la.select_library(True) is checked and la.la_checked_build()
+        la.la_debug_inject_bounds(False)   # host-side flag only: no device work
+    finally:
+        la.select_library(False)
+    assert not la.la_checked_build()

@@ -14,6 +14,7 @@ namespace la {
 
 volatile int g_inject_timeout = 0;
 volatile int g_inject_limit_us = 1000;
+volatile int g_inject_bounds = 0;
 
 static std::atomic<unsigned long long> g_launches{0};
 void count_launches(int n) { g_launches.fetch_add((unsigned long long)n, std::memory_order_relaxed); }
@@ -88,6 +89,7 @@ const char *la_status_string(la_status st) {
         case LA_ERR_UNSUPPORTED: return "unsupported shape or dtype";
         case LA_ERR_CUDA: return "CUDA error";
         case LA_ERR_TIMEOUT: return "a kernel gave up a bounded wait";
+        case LA_ERR_BOUNDS: return "a checked build found an access outside a buffer";
     }
     return "unknown status";
 }
@@ -95,6 +97,22 @@ const char *la_status_string(la_status st) {
 void la_debug_inject_timeout(int enable, int limit_us) {
     g_inject_limit_us = limit_us > 0 ? limit_us : 1;
     g_inject_timeout = enable ? 1 : 0;
+}
+
+int la_checked_build(void) {
+#ifdef LA_CHECKED
+    return 1;
+#else
+    return 0;
+#endif
+}
+
+void la_debug_inject_bounds(int enable) {
+#ifdef LA_CHECKED
+    g_inject_bounds = enable ? 1 : 0;
+#else
+    (void)enable;   // the release build has no bounds checks to catch it
+#endif
 }
 
 size_t la_workspace_bytes(la_op op, la_shape s, int chunk) {

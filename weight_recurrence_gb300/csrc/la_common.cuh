@@ -9,6 +9,17 @@ namespace la {
 
 // Error codes a kernel may record in the device error word (values of la_status).
 constexpr int kErrTimeout = 4;
+constexpr int kErrBounds = 5;
+
+// Bounds checks of the checked build (compiled with -DLA_CHECKED, a separate
+// library): LA_IN_BOUNDS(cond, err) is true when cond holds; otherwise it
+// records LA_ERR_BOUNDS in the error word and is false, and the caller skips
+// the access it guards.  In the release build it is `true` and costs nothing.
+#ifdef LA_CHECKED
+#define LA_IN_BOUNDS(cond, err) ((cond) ? true : (::la::record_error((err), ::la::kErrBounds), false))
+#else
+#define LA_IN_BOUNDS(cond, err) true
+#endif
 
 // phi(x) = elu(x) + 1 with alpha = 1 ("Transformers are RNNs", sec. 3.2.1,
 // eq. (7)): x + 1 for x > 0, exp(x) otherwise.  Accurate exp for the SIMT path.

@@ -141,5 +141,8 @@ void count_launches(int n);
 // Test hook state (la_api.cu).
 extern volatile int g_inject_timeout;
 extern volatile int g_inject_limit_us;
+// checked build only: the next causal tensor-core launches offset the row of
+// their state loads past the state (caught by the bounds checks)
+extern volatile int g_inject_bounds;
 
 }  // namespace la

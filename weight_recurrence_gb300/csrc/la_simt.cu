@@ -123,7 +123,7 @@ causal_simt_kernel(const T *__restrict__ q, const T *__restrict__ k, const T *__
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
 nc_reduce_simt_kernel(const T *__restrict__ k, const T *__restrict__ v, float *__restrict__ ws,
-                      int N, int D, int M, int nsplit, int L)
+                      int N, int D, int M, int nsplit, int L, long long ws_floats, int *err, int inject_oob)
 {
     extern __shared__ float sm[];
     const int ldq = D + 1;
@@ -160,7 +160,12 @@ nc_reduce_simt_kernel(const T *__restrict__ k, const T *__restrict__ v, float *_
         }
     }
     __syncthreads();
-    float *dst = ws + (h * nsplit + sp) * (long long)(D * M + D);
+    long long base = (h * nsplit + sp) * (long long)(D * M + D);
+#ifdef LA_CHECKED
+    if (inject_oob) base += ws_floats;   // test hook: one workspace length past, caught below
+#endif
+    if (!LA_IN_BOUNDS(base + D * M + D <= ws_floats, tid == 0 ? err : nullptr)) return;
+    float *dst = ws + base;
     for (int i = tid; i < D * M + D; i += kThreads) dst[i] = acc[i];
 }
 
@@ -169,7 +174,7 @@ nc_reduce_simt_kernel(const T *__restrict__ k, const T *__restrict__ v, float *_
 template <typename T>
 __global__ void __launch_bounds__(kThreads)
 nc_readout_simt_kernel(const T *__restrict__ q, const float *__restrict__ ws, T *__restrict__ out,
-                       int N, int D, int M, int nsplit, int R)
+                       int N, int D, int M, int nsplit, int R, long long ws_floats, int *err)
 {
     extern __shared__ float sm[];
     const int ldq = D + 1;
@@ -179,6 +184,7 @@ nc_readout_simt_kernel(const T *__restrict__ q, const float *__restrict__ ws, T 
     const long long h = blockIdx.x;
     const int tid = threadIdx.x;
     const int r0 = blockIdx.y * R, r1 = min(N, r0 + R);
+    if (!LA_IN_BOUNDS((h + 1) * nsplit * (long long)(D * M + D) <= ws_floats, tid == 0 ? err : nullptr)) return;
     const float *src = ws + h * nsplit * (long long)(D * M + D);
     for (int i = tid; i < D * M + D; i += kThreads) {
         float s = 0.f;
@@ -336,13 +342,15 @@ cudaError_t simt_noncausal_t(const Problem &p, const DeviceInfo &dev) {
                              (int)sm2);
     if (e != cudaSuccess) return e;
     nc_reduce_simt_kernel<T><<<dim3((unsigned)p.BH, nsplit), kThreads, sm1, p.stream>>>(
-        (const T *)p.k, (const T *)p.v, (float *)p.ws, p.N, p.D, p.M, nsplit, L);
+        (const T *)p.k, (const T *)p.v, (float *)p.ws, p.N, p.D, p.M, nsplit, L,
+        (long long)(p.ws_bytes / sizeof(float)), dev.err_word, g_inject_bounds);
     count_launches(1);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const int R = 256;
     const int nrb = (p.N + R - 1) / R;
     nc_readout_simt_kernel<T><<<dim3((unsigned)p.BH, nrb), kThreads, sm2, p.stream>>>(
-        (const T *)p.q, (const float *)p.ws, (T *)p.out, p.N, p.D, p.M, nsplit, R);
+        (const T *)p.q, (const float *)p.ws, (T *)p.out, p.N, p.D, p.M, nsplit, R,
+        (long long)(p.ws_bytes / sizeof(float)), dev.err_word);
     count_launches(1);
     return cudaGetLastError();
 }
@@ -514,13 +522,15 @@ cudaError_t simt_noncausal_capped_t(const Problem &p, const DeviceInfo &dev, int
                              (int)sm2);
     if (e != cudaSuccess) return e;
     nc_reduce_simt_kernel<T><<<dim3((unsigned)p.BH, nsplit), kThreads, sm1, p.stream>>>(
-        (const T *)p.k, (const T *)p.v, (float *)p.ws, p.N, p.D, p.M, nsplit, L);
+        (const T *)p.k, (const T *)p.v, (float *)p.ws, p.N, p.D, p.M, nsplit, L,
+        (long long)(p.ws_bytes / sizeof(float)), dev.err_word, g_inject_bounds);
     count_launches(1);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     const int R = 256;
     const int nrb = (p.N + R - 1) / R;
     nc_readout_simt_kernel<T><<<dim3((unsigned)p.BH, nrb), kThreads, sm2, p.stream>>>(
-        (const T *)p.q, (const float *)p.ws, (T *)p.out, p.N, p.D, p.M, nsplit, R);
+        (const T *)p.q, (const float *)p.ws, (T *)p.out, p.N, p.D, p.M, nsplit, R,
+        (long long)(p.ws_bytes / sizeof(float)), dev.err_word);
     count_launches(1);
     return cudaGetLastError();
 }

@@ -212,6 +212,9 @@ struct CausalArgs {
     int dr, nu;              // raw width of Q, K rows and DPFP shifts (feat != kFeatPhi)
     int sum_norm;            // DPFP: divide each feature row by its sum
     int no_den;              // read-out without the denominator: out = num
+    // extents the checked build tests direct accesses against (elements)
+    long long nheads, state_elems, ws_floats, out_elems;
+    int inject_oob;          // checked build test hook: state loads offset past the state
 };
 
 // Named barrier of the O group's 128 threads.
@@ -328,7 +331,8 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
     pdl_wait_cta();
     if (tid == 0) LA_CTA_AT(1);
     // this head's sequence length (rows past it are read but ignored)
-    const int Nseq = args.lens ? max(0, min(args.N, args.lens[bh / args.H])) : args.N;
+    const int Nseq = args.lens ? max(0, min(args.N, LA_IN_BOUNDS(bh < args.nheads, args.err) ? args.lens[bh / args.H] : 0))
+                               : args.N;
     const int nch_total = (Nseq + kC - 1) / kC;
     const int n = max(0, min(nch_total, c_begin + args.cps) - c_begin);
 
@@ -589,22 +593,35 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
         auto load_state32 = [&](int row, int c0, float (&v)[32]) {
 #pragma unroll
             for (int j = 0; j < 32; ++j) v[j] = 0.f;
-            auto add = [&](const float *src) {
+#ifdef LA_CHECKED
+            if (args.inject_oob) row += D;   // test hook: caught below
+#endif
+            // src is the start of a D x M block at element `base` of a buffer of `extent` elements
+            auto add = [&](const float *src, long long base, long long extent) {
+                if (!LA_IN_BOUNDS(row < D && c0 + 32 <= M && base + (long long)row * M + c0 + 32 <= extent, args.err))
+                    return;
 #pragma unroll
                 for (int j = 0; j < 32; j += 4) {
                     const float4 x = *reinterpret_cast<const float4 *>(src + row * M + c0 + j);
                     v[j] += x.x; v[j + 1] += x.y; v[j + 2] += x.z; v[j + 3] += x.w;
                 }
             };
+            const long long wsb = (long long)bh * args.nseg * (D * M + D);
             if (ws_h) {
-                add(ws_h + (size_t)(args.nseg - 1) * (D * M + D));
-                for (int g = 0; g < seg; ++g) add(ws_h + (size_t)g * (D * M + D));
+                add(ws_h + (size_t)(args.nseg - 1) * (D * M + D), wsb + (long long)(args.nseg - 1) * (D * M + D),
+                    args.ws_floats);
+                for (int g = 0; g < seg; ++g)
+                    add(ws_h + (size_t)g * (D * M + D), wsb + (long long)g * (D * M + D), args.ws_floats);
             } else if (S_h) {
-                add(S_h);
+                add(S_h, (long long)bh * D * M, args.state_elems);
             }
         };
         auto load_z = [&](int row) {
             float zr = 0.f;
+            if (!LA_IN_BOUNDS(row < D && bh < args.nheads &&
+                                  (!ws_h || ((long long)bh * args.nseg + args.nseg) * (D * M + D) <= args.ws_floats),
+                              args.err))
+                return zr;
             if (ws_h) {
                 zr = ws_h[(size_t)(args.nseg - 1) * (D * M + D) + D * M + row];
                 for (int g = 0; g < seg; ++g) zr += ws_h[(size_t)g * (D * M + D) + D * M + row];
@@ -641,7 +658,9 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     den = __uint_as_float(dv[0]) + __uint_as_float(zv[0]);
                 }
                 const float inv = VAR && args.no_den ? 1.f : 1.f / den;
-                uint4 *dst = !C::OUT_TMA && args.out && t < Nseq
+                uint4 *dst = !C::OUT_TMA && args.out && t < Nseq &&
+                                     LA_IN_BOUNDS((long long)bh * args.o_hs + (long long)t * args.o_rs + M <= args.out_elems,
+                                                  args.err)
                                  ? reinterpret_cast<uint4 *>(args.out + (size_t)bh * args.o_hs + (size_t)t * args.o_rs)
                                  : nullptr;
                 // rows of 256-bit stores when the output's base allows them (each
@@ -740,7 +759,8 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
             if (leader) LA_TRACE_AT(0, 63, 2);
             if (leader) LA_CTA_AT(7);
             // state after the last token (last segment only)
-            if (S_h && seg == args.nseg - 1 && n > 0 && !*abort) {
+            if (S_h && seg == args.nseg - 1 && n > 0 && !*abort &&
+                LA_IN_BOUNDS(((long long)bh * D + d) * M + 32 * h + 32 <= args.state_elems, args.err)) {
 #pragma unroll
                 for (int j = 0; j < 32; j += 4)
                     *reinterpret_cast<float4 *>(S_h + d * M + 32 * h + j) = make_float4(sv[j], sv[j + 1], sv[j + 2], sv[j + 3]);
@@ -817,7 +837,7 @@ causal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant
                     for (int c0 = 0; c0 < M; c0 += 32) {
                         float v[32];
                         tmem_ld32f(tmem + lane_off + C::COL_S + c0, v);
-                        if (srow)
+                        if (srow && LA_IN_BOUNDS(((long long)bh * D + r) * M + c0 + 32 <= args.state_elems, args.err))
 #pragma unroll
                             for (int j = 0; j < 32; j += 4)
                                 *reinterpret_cast<float4 *>(S_h + r * M + c0 + j) =
@@ -905,6 +925,9 @@ struct ReduceArgs {
     int cps;                 // chunks per split
     int init_slot;           // -1: none
     int *err;
+    long long ws_floats;     // extents the checked build tests writes against
+    long long nheads;
+    int inject_oob;          // checked build test hook: slot offset past the workspace
 };
 
 template <int D, int M>
@@ -1014,8 +1037,14 @@ state_reduce_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
         }
         tc_fence_before();
         mbar_arrive(init);
-        float *dst = args.ws + ((size_t)bh * args.nslot + sp) * (D * M + D);
-        if (args.init_slot >= 0 && sp == 0 && r < D) {
+        long long base = ((long long)bh * args.nslot + sp) * (D * M + D);
+#ifdef LA_CHECKED
+        if (args.inject_oob) base += args.ws_floats;   // test hook: one workspace length past, caught below
+#endif
+        const bool dst_ok = LA_IN_BOUNDS(bh < args.nheads && base + (D * M + D) <= args.ws_floats, args.err);
+        float *dst = args.ws + base;
+        if (args.init_slot >= 0 && sp == 0 && r < D &&
+            LA_IN_BOUNDS(((long long)bh * args.nslot + args.init_slot + 1) * (D * M + D) <= args.ws_floats, args.err)) {
             float *di = args.ws + ((size_t)bh * args.nslot + args.init_slot) * (D * M + D);
             const float *Si = args.S_init ? args.S_init + (size_t)bh * D * M : nullptr;
             for (int c = 0; c < M; c += 4)
@@ -1030,7 +1059,7 @@ state_reduce_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
             for (int c0 = 0; c0 < M; c0 += 32) {
                 float v[32];
                 tmem_ld32f(tmem + lane_off + C::COL_S + c0, v);
-                if (r < D)
+                if (r < D && dst_ok)
 #pragma unroll
                     for (int j = 0; j < 32; j += 4)
                         *reinterpret_cast<float4 *>(dst + r * M + c0 + j) =
@@ -1039,7 +1068,7 @@ state_reduce_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
             uint32_t zv[16];
             tmem_ld16(tmem + lane_off + C::COL_Z, zv);
             tmem_wait_ld();
-            if (r < D) dst[D * M + r] = __uint_as_float(zv[0]);
+            if (r < D && dst_ok) dst[D * M + r] = __uint_as_float(zv[0]);
         }
     } else {
         const int t = tid - 64 - kGrp;
@@ -1123,6 +1152,7 @@ struct NoncausalArgs {
     int cps;                 // chunks per CTA
     int *err;
     int feat, dr, nu, sum_norm, no_den;   // a variant's feature map and read-out (VAR only)
+    long long ws_floats, nheads;          // extents the checked build tests accesses against
 };
 
 // VAR: a variant's feature map and read-out, as in causal_tc_kernel.
@@ -1317,6 +1347,9 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         const bool leader = tid == 64;
         constexpr int W = D * M + D;
         float *slot = args.ws + ((size_t)bh * args.G + g) * W;
+        // the head's G slots lie inside the workspace (checked build)
+        const bool ws_ok =
+            dsx || LA_IN_BOUNDS(bh < args.nheads && ((long long)bh + 1) * args.G * W <= args.ws_floats, args.err);
         if (swarp) {
             float zero[32];
 #pragma unroll
@@ -1410,7 +1443,7 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             if (ok2) wait_bar_warp(snapx_bar, 0, abort);
         } else {
         // this CTA's partial sums into its workspace slot
-        if (ok1 && swarp) {
+        if (ok1 && swarp && ws_ok) {
             tc_fence_after();
 #pragma unroll 1
             for (int c0 = 0; c0 < M; c0 += 32) {
@@ -1437,7 +1470,7 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         // All 128 threads take 16-column blocks (consecutive threads, consecutive
         // blocks of a row) and load up to four slots' blocks before adding, so
         // that the reads overlap instead of paying one L2 round trip each.
-        if (!*abort) {
+        if (!*abort && ws_ok) {
             const float *src = args.ws + (size_t)bh * args.G * W;
             const int tg = tid - 64;
             // z's slot entries first, so that their loads share the first
@@ -1633,7 +1666,8 @@ cudaError_t launch_causal(const Problem &p, const DeviceInfo &dev) {
     cudaError_t e;
     if (nseg > 1) {
         if (p.ws_bytes < (size_t)p.BH * nseg * (D * M + D) * sizeof(float)) return cudaErrorInvalidValue;
-        ReduceArgs r{(float *)p.ws, p.S, p.z, p.N, nseg, nseg - 1, cps, nseg - 1, dev.err_word};
+        ReduceArgs r{(float *)p.ws, p.S, p.z, p.N, nseg, nseg - 1, cps, nseg - 1, dev.err_word,
+                     (long long)(p.ws_bytes / sizeof(float)), p.BH, g_inject_bounds};
         if ((e = set_smem(state_reduce_kernel<D, M>, RCfg<D, M>::SMEM)) != cudaSuccess) return e;
         e = launch_pdl(state_reduce_kernel<D, M>, dim3((unsigned)(p.BH * (nseg - 1))), dim3(kThreads),
                        RCfg<D, M>::SMEM, p.stream, 0u, tk, tv, r);
@@ -1662,6 +1696,11 @@ cudaError_t launch_causal(const Problem &p, const DeviceInfo &dev) {
     a.nu = p.nu;
     a.sum_norm = p.sum_norm ? 1 : 0;
     a.no_den = p.no_den ? 1 : 0;
+    a.nheads = p.BH;
+    a.state_elems = p.S ? p.BH * D * M : 0;
+    a.ws_floats = nseg > 1 ? (long long)(p.ws_bytes / sizeof(float)) : 0;
+    a.out_elems = p.out ? p.BH * (long long)p.N * M : 0;
+    a.inject_oob = g_inject_bounds;
     const dim3 grid((unsigned)(p.BH * nseg)), block(C::THREADS);
     if (p.feat != kFeatPhi || p.no_den) {
         if ((e = set_smem(causal_tc_kernel<D, M, true>, C::SMEM)) != cudaSuccess) return e;
@@ -1699,7 +1738,7 @@ cudaError_t launch_noncausal_v(const Problem &p, const DeviceInfo &dev) {
     cudaError_t e;
     if ((e = set_smem(noncausal_tc_kernel<D, M, VAR>, C::SMEM)) != cudaSuccess) return e;
     const NoncausalArgs a{(float *)p.ws, p.N, G, cps, dev.err_word, p.feat, p.dr, p.nu, p.sum_norm ? 1 : 0,
-                          p.no_den ? 1 : 0};
+                          p.no_den ? 1 : 0, (long long)(p.ws_bytes / sizeof(float)), p.BH};
     e = launch_pdl(noncausal_tc_kernel<D, M, VAR>, dim3((unsigned)(p.BH * G)), dim3(kThreads), C::SMEM, p.stream,
                    (unsigned)G, tq, tk, tv, to, a);
     count_launches(1);

@@ -5,6 +5,12 @@ Every function here has the name of the C entry point it calls (see
 provides device memory and the current CUDA stream, nothing else.  All work
 runs in the library's kernels.  If the library is missing the first call
 raises: there is no fallback.
+
+Two builds of the library exist: liblinattn.so (the product) and
+liblinattn_checked.so, the same kernels compiled with in-kernel bounds checks
+that record LA_ERR_BOUNDS in the error word instead of making an access out
+of range.  The environment variable LA_CHECKED=1 (read at the first load) or
+select_library(checked=True) makes every call below go to the checked build.
 """
 from __future__ import annotations
 
@@ -15,8 +21,9 @@ import torch
 
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "lib", "liblinattn.so")
+LIB_CHECKED_PATH = os.path.join(_PKG, "lib", "liblinattn_checked.so")
 
-LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_CUDA, LA_ERR_TIMEOUT = range(5)
+LA_OK, LA_ERR_INVALID_ARG, LA_ERR_UNSUPPORTED, LA_ERR_CUDA, LA_ERR_TIMEOUT, LA_ERR_BOUNDS = range(6)
 LA_DTYPE_F32, LA_DTYPE_BF16 = 0, 1
 LA_OP_NONCAUSAL, LA_OP_CAUSAL, LA_OP_DECODE, LA_OP_NONCAUSAL_BWD, LA_OP_CAUSAL_BWD = 0, 1, 2, 3, 4
 
@@ -25,7 +32,8 @@ EXPORTED = ("la_workspace_bytes", "la_forward_noncausal", "la_forward_causal", "
             "la_debug_inject_timeout", "la_forward_noncausal_noalloc", "la_backward_causal",
             "la_backward_noncausal", "la_forward_causal_varlen", "la_decode_steps",
             "la_feature_dim", "la_variant_workspace_bytes", "la_forward_causal_variant",
-            "la_forward_noncausal_variant", "la_decode_step_variant")
+            "la_forward_noncausal_variant", "la_decode_step_variant", "la_checked_build",
+            "la_debug_inject_bounds")
 
 LA_FM = {"elu1": 0, "dpfp": 1, "poly2": 2}
 LA_NORM = {"den": 0, "sum": 1, "none": 2}
@@ -55,16 +63,33 @@ def variant(fm: str = "elu1", nu: int = 1, norm: str = "den", update: str = "sum
 
 
 _lib = None
+_loaded = {}
+
+
+def select_library(checked: bool) -> ctypes.CDLL:
+    """Routes the calls of this module to the checked build (True) or to the
+    product build (False); returns the library now in use."""
+    global _lib
+    _lib = _load(LIB_CHECKED_PATH if checked else LIB_PATH)
+    return _lib
 
 
 def lib() -> ctypes.CDLL:
-    """The loaded library (raises if it has not been built)."""
+    """The library in use (raises if it has not been built)."""
     global _lib
     if _lib is None:
-        if not os.path.exists(LIB_PATH):
-            raise RuntimeError("liblinattn.so is not built (%s); run "
-                               "`python -m weight_recurrence_gb300.build`" % LIB_PATH)
-        L = ctypes.CDLL(LIB_PATH)
+        _lib = _load(LIB_CHECKED_PATH if os.environ.get("LA_CHECKED", "0") not in ("", "0") else LIB_PATH)
+    return _lib
+
+
+def _load(path: str) -> ctypes.CDLL:
+    L = _loaded.get(path)
+    if L is None:
+        if not os.path.exists(path):
+            flag = " --checked" if path == LIB_CHECKED_PATH else ""
+            raise RuntimeError("%s is not built; run `python -m weight_recurrence_gb300.build%s`"
+                               % (path, flag))
+        L = ctypes.CDLL(path)
         vp, sz, i = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
         L.la_workspace_bytes.restype = sz
         L.la_workspace_bytes.argtypes = [i, la_shape, i]
@@ -102,8 +127,12 @@ def lib() -> ctypes.CDLL:
         L.la_forward_noncausal_variant.argtypes = [vp, vp, vp, vp, la_shape, la_variant, vp, sz, vp]
         L.la_decode_step_variant.restype = i
         L.la_decode_step_variant.argtypes = [vp, vp, vp, vp, vp, vp, vp, la_shape, la_variant, vp]
-        _lib = L
-    return _lib
+        L.la_checked_build.restype = i
+        L.la_checked_build.argtypes = []
+        L.la_debug_inject_bounds.restype = None
+        L.la_debug_inject_bounds.argtypes = [i]
+        _loaded[path] = L
+    return L
 
 
 def status_string(st: int) -> str:
@@ -377,6 +406,18 @@ def la_get_last_error(stream=None, device=None) -> int:
 
 def la_debug_inject_timeout(enable: bool, limit_us: int = 1000):
     lib().la_debug_inject_timeout(1 if enable else 0, int(limit_us))
+
+
+def la_checked_build() -> bool:
+    """True when the library in use is the bounds-checked build."""
+    return bool(lib().la_checked_build())
+
+
+def la_debug_inject_bounds(enable: bool):
+    """Checked build only (a no-op otherwise): while enabled, the kernels that
+    read a carried-in state or a workspace slot offset that index past its
+    buffer, so that their check records LA_ERR_BOUNDS and skips the access."""
+    lib().la_debug_inject_bounds(1 if enable else 0)
 
 
 def la_version() -> int:
