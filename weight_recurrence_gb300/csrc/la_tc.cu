@@ -1598,7 +1598,7 @@ noncausal_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             if (wait_bar(&full[u % C::NU], ph(u), abort)) {
                 if (t == 0 && idx == 0) LA_CTA_AT(2);
                 const int zf = idx < n ? min(kC, args.N - (c_begin + idx) * kC) : kC;
-                if (!VAR || args.feat == kFeatPhi) phi_tile<D>(unit(u), t, zf);
+                if (!VAR || args.feat == kFeatPhi) phi_tile<D, true>(unit(u), t, zf);
                 else if constexpr (VAR)   // a variant's feature map, one row per thread
                     feature_row<D>(unit(u), t, zf, args.feat, args.dr, args.nu, args.sum_norm);
             }
