@@ -267,6 +267,10 @@ def run_ours(args, rank, world, dist):
 
     if args.only:
         # one workload alone, for profiler captures: no clocks, e2e or CPU legs
+        if args.only.startswith("backward_nc_"):
+            leg = _leg_backward(torch, la, inputs, args.only[len("backward_nc_"):], dev, stream, rot, pk,
+                                args.steps, max_over_ranks, world, rank, warmup=args.warmup, noncausal=True)
+            return {"only": args.only, "leg": leg, "gpu_launches_total": la.la_launch_count()}
         if args.only.startswith("backward_"):
             leg = _leg_backward(torch, la, inputs, args.only[len("backward_"):], dev, stream, rot, pk,
                                 args.steps, max_over_ranks, world, rank, warmup=args.warmup)
@@ -414,6 +418,8 @@ def run_ours(args, rank, world, dist):
                                                max_over_ranks, world, rank)
         result["legs"]["backward"] = _leg_backward(torch, la, inputs, MAIN, dev, stream, rot, pk, 5,
                                                    max_over_ranks, world, rank)
+        result["legs"]["backward_noncausal"] = _leg_backward(torch, la, inputs, MAIN, dev, stream, rot, pk, 5,
+                                                             max_over_ranks, world, rank, noncausal=True)
         for name in ("delta_b16h8n3072d64", "dpfp_b16h8n3072d64"):
             result["legs"][name.split("_")[0]] = _leg_variant(torch, la, inputs, name, dev, stream, rot, pk, 5,
                                                               max_over_ranks, world, rank)
@@ -433,6 +439,8 @@ def run_ours(args, rank, world, dist):
             legs["decode"]["cpu_baseline"] = cpu_baseline_decode(inputs.WORKLOADS["decode_b256h16d64"], budget_s=cs)
         if "backward" in legs:
             legs["backward"]["cpu_baseline"] = cpu_baseline_backward(w, budget_s=cs)
+        if "backward_noncausal" in legs:
+            legs["backward_noncausal"]["cpu_baseline"] = cpu_baseline_backward(w, budget_s=cs, noncausal=True)
         for name in ("delta_b16h8n3072d64", "dpfp_b16h8n3072d64"):
             key = name.split("_")[0]
             if key in legs:
@@ -471,8 +479,9 @@ def _leg_fwd(torch, la, inputs, name, dev, stream, rot, pk, steps, max_over_rank
     return leg
 
 
-def _leg_backward(torch, la, inputs, name, dev, stream, rot, pk, steps, max_over_ranks, world, rank, warmup=3):
-    """Causal backward (dQ, dK, dV from dL/dV') on a forward workload's shape."""
+def _leg_backward(torch, la, inputs, name, dev, stream, rot, pk, steps, max_over_ranks, world, rank, warmup=3,
+                  noncausal=False):
+    """Causal (or non-causal) backward, dQ, dK, dV from dL/dV', on a forward workload's shape."""
     w = inputs.WORKLOADS[name]
     q, k, v = [t.to(dev) for t in inputs.workload_inputs(w, rank)]
     g = torch.Generator(device=dev).manual_seed(inputs.rank_seed(w.seed + 2000, rank))
@@ -485,7 +494,10 @@ def _leg_backward(torch, la, inputs, name, dev, stream, rot, pk, steps, max_over
     def fn():
         q_, k_, v_, G_, dq_, dk_, dv_ = sets[it[0] % len(sets)]
         it[0] += 1
-        la.la_backward_causal(q_, k_, v_, G_, dq=dq_, dk=dk_, dv=dv_, stream=stream)
+        if noncausal:
+            la.la_backward_noncausal(q_, k_, v_, G_, dq=dq_, dk=dk_, dv=dv_, stream=stream)
+        else:
+            la.la_backward_causal(q_, k_, v_, G_, dq=dq_, dk=dk_, dv=dv_, stream=stream)
 
     l0 = la.la_launch_count()
     t = _timed_steps(torch, fn, steps, warmup, stream)
@@ -494,14 +506,19 @@ def _leg_backward(torch, la, inputs, name, dev, stream, rot, pk, steps, max_over
     el = q.element_size()
     alg = w.B * w.H * w.N * (4 * w.D + 3 * w.M) * el      # read Q, K, V, dO; write dQ, dK, dV
     gbs = alg / (ms / 1e3) / 1e9
-    leg = {"workload": name, "op": "causal_backward", "value": round(world * w.B * w.N / (ms / 1e3), 1),
+    leg = {"workload": name, "op": "noncausal_backward" if noncausal else "causal_backward",
+           "value": round(world * w.B * w.N / (ms / 1e3), 1),
            "unit": "tokens/s", "ms_per_step": round(ms, 5), "steps": steps, "launches_per_step": launches,
            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
-                        "frac": round(gbs / pk["hbm_gbs"], 4), "traffic": _traffic("backward_" + name),
+                        "frac": round(gbs / pk["hbm_gbs"], 4),
+                        "traffic": _traffic(("backward_nc_" if noncausal else "backward_") + name),
                         "alg_bytes_per_launch": alg},
            "l2": rot.describe(in_bytes),
-           "note": "tcgen05 kernels (bf16 D = M = 64): a forward sweep (dQ, keeps g and e) and a reverse "
-                   "sweep (dK, dV), one CTA per head each"}
+           "note": ("tcgen05 kernels: key sums [S | z], a query pass (dQ and partial sums of phi(Q)^T [g | e]), "
+                    "a key pass (dK, dV); K and V are read twice, so traffic is 9 tensors against 7 algorithmic"
+                    if noncausal else
+                    "tcgen05 kernels (bf16 D = M = 64): a forward sweep (dQ, keeps g and e) and a reverse "
+                    "sweep (dK, dV), one CTA per head each")}
     del q, k, v, G, dq, dk, dv, sets
     torch.cuda.empty_cache()
     return leg
@@ -748,8 +765,8 @@ def cpu_baseline_decode(w, budget_s=4.0):
                       % (heads, w.B * w.H, w.steps, w.N, reps))
 
 
-def cpu_baseline_backward(w, budget_s=4.0):
-    """The fp64 causal backward oracle on a sample of heads; tokens/s as the forward."""
+def cpu_baseline_backward(w, budget_s=4.0, noncausal=False):
+    """The fp64 causal (or non-causal) backward oracle on a sample of heads; tokens/s as the forward."""
     import oracle
     import torch
     from weight_recurrence_gb300 import inputs
@@ -760,10 +777,11 @@ def cpu_baseline_backward(w, budget_s=4.0):
     q, k, v = inputs.qkv(1, heads, w.N, w.D, w.M, w.dtype, w.scale, seed=w.seed)
     g = torch.Generator().manual_seed(w.seed + 2000)
     G = torch.randn(v.shape, generator=g).to(w.dtype)
-    dt, reps = _cpu_timed(lambda: oracle.causal_backward(q, k, v, G, nthreads=nthreads), budget_s)
+    fn = oracle.noncausal_backward if noncausal else oracle.causal_backward
+    dt, reps = _cpu_timed(lambda: fn(q, k, v, G, nthreads=nthreads), budget_s)
     return _cpu_entry(heads * w.N / dt / w.H, "tokens/s", nthreads,
-                      "%d of %d heads x N=%d (fp64 backward oracle), %d reps; tokens/s = head-tokens/s / H"
-                      % (heads, w.B * w.H, w.N, reps))
+                      "%d of %d heads x N=%d (fp64 %s backward oracle), %d reps; tokens/s = head-tokens/s / H"
+                      % (heads, w.B * w.H, w.N, "non-causal" if noncausal else "causal", reps))
 
 
 def cpu_baseline_variant(w, budget_s=4.0):

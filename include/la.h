@@ -194,7 +194,12 @@ la_status la_backward_causal(const void *q, const void *k, const void *v, const 
  * Backward of the non-causal form, sec. 3.2 eq. (5): the same steps with the
  * sums over all N keys (S, Z the full sums, R and r summed over all queries).
  *   Arguments as la_backward_causal without the state ones;
- *   workspace: la_workspace_bytes(LA_OP_NONCAUSAL_BWD, s, 0) bytes.
+ *   workspace: la_workspace_bytes(LA_OP_NONCAUSAL_BWD, s, 0) bytes (fp32
+ *      partial sums of S, Z and of R, r per key or query range).
+ * bf16 with D, M in {64, 128} runs on tensor cores in three launches (key
+ * sums; a query pass giving dQ and the partial R, r; a key pass giving dK,
+ * dV), the sums entering the products as bf16 hi + lo pairs; every other
+ * dtype and size runs fp32 arithmetic on CUDA cores.
  */
 la_status la_backward_noncausal(const void *q, const void *k, const void *v, const void *dout,
                                 void *dq, void *dk, void *dv, la_shape s,

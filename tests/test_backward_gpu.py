@@ -185,3 +185,43 @@ def test_full_causal_backward_b16h8n3072d64():
         ref = oracle.causal_backward(q[b, h][None], k[b, h][None], v[b, h][None], G[b, h][None])[:3]
         for got, r in zip((dq, dk, dv), ref):
             assert grad_err(got[b, h][None], r, G[b, h][None], nlead=1) <= 2e-2
+
+
+# Non-causal backward on tensor cores (bf16, D, M in {64, 128}): key ranges
+# split across CTAs (several ranges per head, ragged last chunk, a range
+# shorter than a chunk), all four (D, M) pairs.
+NC_TC_CASES = [
+    (1, 1, 1, 64, 64, 1.0),
+    (1, 2, 100, 64, 64, 0.5),
+    (2, 3, 1300, 64, 64, 0.125),
+    (1, 2, 4000, 64, 64, 1.0),
+    (1, 1, 777, 64, 128, 0.25),
+    (1, 2, 640, 128, 64, 1.0 / math.sqrt(128)),
+    (2, 1, 1025, 128, 128, 1.0 / math.sqrt(128)),
+]
+
+
+@pytest.mark.parametrize("B,H,N,D,M,scale", NC_TC_CASES)
+def test_noncausal_backward_tensor_cores(B, H, N, D, M, scale):
+    dtype = torch.bfloat16
+    q, k, v = inputs.qkv(B, H, N, D, M, dtype, scale, seed=1100 + N)
+    G = _dout(B, H, N, M, dtype, 1200 + N)
+    ref = oracle.noncausal_backward(q, k, v, G)
+    n0 = la.la_launch_count()
+    got = la.la_backward_noncausal(*_dev(q, k, v, G))
+    torch.cuda.synchronize()
+    assert la.la_get_last_error() == la.LA_OK
+    assert la.la_launch_count() - n0 == 3      # key sums, query kernel, key kernel
+    _check_grads(got, ref, dtype, G, "noncausal tc")
+
+
+def test_full_noncausal_backward_b16h8n3072d64():
+    """The training-shaped shape at full size, every element against the oracle."""
+    w = inputs.WORKLOADS["causal_b16h8n3072d64"]
+    q, k, v = inputs.workload_inputs(w)
+    G = _dout(w.B, w.H, w.N, w.M, w.dtype, 940)
+    got = la.la_backward_noncausal(*_dev(q, k, v, G))
+    torch.cuda.synchronize()
+    assert la.la_get_last_error() == la.LA_OK
+    ref = oracle.noncausal_backward(q, k, v, G)
+    _check_grads(got, ref, w.dtype, G, "noncausal full")

@@ -170,6 +170,7 @@ la_status la_backward_noncausal(const void *q, const void *k, const void *v, con
     if (!dev) return LA_ERR_CUDA;
     BwdProblem p{q, k, v, dout, dq, dk, dv, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr,
                  (long long)s.B * s.H, s.N, s.D, s.M, s.dtype, workspace, ws_bytes, (cudaStream_t)stream};
+    if (tc_nc_backward_supported(s)) return from_cuda(tc_noncausal_backward(p, *dev));
     return from_cuda(noncausal_backward(p, *dev));
 }
 

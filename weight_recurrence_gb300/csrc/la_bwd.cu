@@ -646,7 +646,8 @@ size_t noncausal_bwd_ws_bytes(const la_shape &s) {
     if (BH <= 0 || s.N <= 0) return 0;
     int nsplit, L;
     nc_bwd_grid(BH, s.N, 192, nsplit, L);
-    return (size_t)2 * BH * nsplit * ((size_t)s.D * s.M + s.D) * sizeof(float);
+    const size_t simt = (size_t)2 * BH * nsplit * ((size_t)s.D * s.M + s.D) * sizeof(float);
+    return tc_nc_backward_supported(s) ? std::max(simt, tc_nc_backward_ws_bytes(s)) : simt;
 }
 
 cudaError_t causal_backward(const BwdProblem &p, const DeviceInfo &dev) {

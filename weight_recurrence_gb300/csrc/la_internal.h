@@ -65,6 +65,13 @@ cudaError_t causal_backward(const BwdProblem &p, const DeviceInfo &dev);
 cudaError_t noncausal_backward(const BwdProblem &p, const DeviceInfo &dev);
 // tensor-core causal backward (la_tc_bwd.cu): bf16, D = M = 64
 bool tc_backward_supported(const la_shape &s);
+// per-split key sums [S | z] on tensor cores (la_tc.cu), bf16, D, M in {64, 128}
+cudaError_t tc_key_sums(const void *k, const void *v, long long BH, int N, int D, int M, int nsplit, int cps,
+                        float *ws, size_t ws_bytes, cudaStream_t stream, const DeviceInfo &dev);
+// tensor-core non-causal backward (la_tc_bwd_nc.cu): bf16, D, M in {64, 128}
+bool tc_nc_backward_supported(const la_shape &s);
+size_t tc_nc_backward_ws_bytes(const la_shape &s);
+cudaError_t tc_noncausal_backward(const BwdProblem &p, const DeviceInfo &dev);
 cudaError_t tc_causal_backward(const BwdProblem &p, const DeviceInfo &dev);
 
 // ---- SIMT kernels (la_simt.cu): any D, M in {16,32,64,128}, fp32 or bf16.

@@ -1797,6 +1797,35 @@ size_t tc_causal_ws_bytes(const la_shape &s, int) {
     return (size_t)BH * nseg * ((size_t)s.D * s.M + s.D) * sizeof(float);
 }
 
+// Partial sums sum phi(K_j) [V_j | 1] of `nsplit` consecutive key ranges of
+// cps chunks per head, into ws[bh][split] = [S (D x M) | z (D)] fp32: the
+// segment-sum pre-pass run over every split (no carried-in slot).
+template <int D, int M>
+cudaError_t launch_key_sums(const void *k, const void *v, long long BH, int N, int nsplit, int cps, float *ws,
+                            size_t ws_bytes, cudaStream_t stream, const DeviceInfo &dev) {
+    CUtensorMap tk, tv;
+    if (!cached_tmap_bf16_3d(&tk, k, D, N, BH, 64, kC) || !cached_tmap_bf16_3d(&tv, v, M, N, BH, 64, kC))
+        return cudaErrorInvalidValue;
+    if (ws_bytes < (size_t)BH * nsplit * (D * M + D) * sizeof(float)) return cudaErrorInvalidValue;
+    ReduceArgs r{ws, nullptr, nullptr, N, nsplit, nsplit, cps, -1, dev.err_word,
+                 (long long)(ws_bytes / sizeof(float)), BH, g_inject_bounds};
+    cudaError_t e = set_smem(state_reduce_kernel<D, M>, RCfg<D, M>::SMEM);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(state_reduce_kernel<D, M>, dim3((unsigned)(BH * nsplit)), dim3(kThreads), RCfg<D, M>::SMEM, stream,
+                   0u, tk, tv, r);
+    count_launches(1);
+    return e;
+}
+
+cudaError_t tc_key_sums(const void *k, const void *v, long long BH, int N, int D, int M, int nsplit, int cps,
+                        float *ws, size_t ws_bytes, cudaStream_t stream, const DeviceInfo &dev) {
+    if (D == 64 && M == 64) return launch_key_sums<64, 64>(k, v, BH, N, nsplit, cps, ws, ws_bytes, stream, dev);
+    if (D == 64 && M == 128) return launch_key_sums<64, 128>(k, v, BH, N, nsplit, cps, ws, ws_bytes, stream, dev);
+    if (D == 128 && M == 64) return launch_key_sums<128, 64>(k, v, BH, N, nsplit, cps, ws, ws_bytes, stream, dev);
+    if (D == 128 && M == 128) return launch_key_sums<128, 128>(k, v, BH, N, nsplit, cps, ws, ws_bytes, stream, dev);
+    return cudaErrorInvalidValue;
+}
+
 cudaError_t tc_causal(const Problem &p, const DeviceInfo &dev) {
     if (p.D == 64 && p.M == 64) return launch_causal<64, 64>(p, dev);
     if (p.D == 64 && p.M == 128) return launch_causal<64, 128>(p, dev);

@@ -1,0 +1,571 @@
+// la_tc_bwd_nc.cu - tensor-core (tcgen05 + TMA) backward of the non-causal
+// form, "Transformers are RNNs" sec. 3.2 eq. (5), for bf16 tensors with D, M
+// in {64, 128}.
+//
+// With S = sum_j phi(K_j) V_j^T and z = sum_j phi(K_j) over all N keys, the
+// forward is V'_i = phi(Q_i)^T S / phi(Q_i)^T z.  Given dO = dL/dV' the chain
+// rule gives, per query row i and key row j,
+//   den_i = phi(Q_i) . z,  g_i = dO_i / den_i,  e_i = -(dO_i . V'_i) / den_i,
+//   dphi(Q_i) = S g_i + e_i z,    dS = sum_i phi(Q_i) g_i^T,  dz = sum_i e_i phi(Q_i),
+//   dphi(K_j) = dS V_j + dz,      dV_j = dS^T phi(K_j),
+// and dQ = dphi(Q) phi'(Q), dK = dphi(K) phi'(K) with phi'(x) = 1 for x > 0,
+// e^x otherwise, i.e. min(phi(x), 1).  Three launches, each over BH x nsplit
+// CTAs (a head's rows in nsplit ranges of cps chunks of C = 128 rows):
+//   1. key sums: [S | z] partials of each key range (the segment-sum pre-pass
+//      of the causal forward, la_tc.cu);
+//   2. query kernel: sums the head's [S | z] partials into the bf16 operand
+//      below; per query chunk: [num | den] = phi(Q) [S | z] (MMAs), g and e
+//      on CUDA cores (V' recomputed, not read), dphi(Q) = S g + z e (MMAs),
+//      dQ; and the partials dS += phi(Q)^T g, dz += phi(Q)^T e (MMAs
+//      accumulating over the range);
+//   3. key kernel: sums the [dS | dz] partials into the same form; per key
+//      chunk: dphi(K) = dS V + dz and dV = dS^T phi(K) (MMAs), dK.
+// The sums enter the products as bf16 hi + lo pairs, in one row-major tile
+// [X_hi | w | X_lo] of 64-column swizzled atoms whose w atom holds
+// (w_hi, w_lo, w_hi, w_lo) in its first four columns; the tile is read both
+// as an MN-major B operand ([K = D] x [N]: phi(Q) [S | z]) and as a K-major
+// one ([N = D] x [K]: [g | e | g] [S_hi | z | S_lo]^T), so one copy serves
+// both products.  e also enters as (e_hi, e_hi, e_lo, e_lo), so that the
+// four columns meet as (e_hi + e_lo)(z_hi + z_lo), and e is formed from the
+// bf16 g the products use: where the terms S g and e z cancel (one key: the
+// output is V whatever Q is) they cancel to fp32 rounding.  One CTA of 128 threads: thread r owns row r of each chunk (TMEM
+// lane r); the phases of a chunk run in order, the next chunk's tiles load
+// by TMA meanwhile (two stages).  Every wait is bounded; a CTA that gives up
+// records LA_ERR_TIMEOUT and skips the rest of its work.
+#include <algorithm>
+
+#include "la_common.cuh"
+#include "la_internal.h"
+#include "tc_host.h"
+#include "tc_kernels.cuh"
+#include "tc_ptx.cuh"
+
+namespace la {
+namespace {
+
+using namespace tc;
+
+constexpr int kNT = 128;   // threads of the query and key kernels
+
+// Row-major operand [X_hi | w | X_lo] (X: rows x cols) in 64-column swizzled
+// atoms of `rows` rows each.
+template <int ROWS, int COLS>
+struct XwTile {
+    static constexpr int ATOM = ROWS * 128;
+    static constexpr int W_ATOM = (COLS / 64) * ATOM;   // byte offset of the w atom
+    static constexpr int LO = W_ATOM + ATOM;            // byte offset of X_lo
+    static constexpr int BYTES = LO + W_ATOM;
+};
+
+// Sum of the head's nsplit fp32 partial slots [X (D x M) | w (D)] (slot stride
+// D*M + D floats) into the bf16 operand tile [X_hi | w | X_lo]: thread r < D
+// takes row r.
+template <int D, int M>
+__device__ __forceinline__ void sum_partials_to_tile(const float *slots, int nsplit, uint8_t *tile, int r) {
+    constexpr int W = D * M + D;
+    if (r >= D) return;
+#pragma unroll 1
+    for (int c0 = 0; c0 < M; c0 += 32) {
+        float x[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) x[j] = 0.f;
+        for (int sp = 0; sp < nsplit; ++sp) {
+            const float4 *src = reinterpret_cast<const float4 *>(slots + (size_t)sp * W + r * M + c0);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float4 a = __ldcg(src + j);
+                x[4 * j] += a.x; x[4 * j + 1] += a.y; x[4 * j + 2] += a.z; x[4 * j + 3] += a.w;
+            }
+        }
+        float lo[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const float h = __bfloat162float(__float2bfloat16_rn(x[j]));
+            lo[j] = x[j] - h;
+            x[j] = h;
+        }
+        store_snap32<D>(tile, r, c0, x);
+        store_snap32<D>(tile + XwTile<D, M>::LO, r, c0, lo);
+    }
+    float w = 0.f;
+    for (int sp = 0; sp < nsplit; ++sp) w += __ldcg(slots + (size_t)sp * W + D * M + r);
+    const float hi = __bfloat162float(__float2bfloat16_rn(w));
+    const uint32_t hl = pack_bf16x2(hi, w - hi);
+    uint8_t *wa = tile + XwTile<D, M>::W_ATOM;
+#pragma unroll
+    for (int c = 0; c < 64; c += 8)
+        *reinterpret_cast<uint4 *>(wa + sw128_offset(r, c)) = make_uint4(c == 0 ? hl : 0u, c == 0 ? hl : 0u, 0u, 0u);
+}
+
+// Row r of a bf16 result (n columns, fp32 in x) to global memory: 256-bit
+// stores when the row start allows, else 128-bit.
+template <int NCOL>
+__device__ __forceinline__ void store_row_bf16(__nv_bfloat16 *dst, const float *x) {
+    uint4 w[NCOL / 8];
+#pragma unroll
+    for (int c8 = 0; c8 < NCOL / 8; ++c8)
+        w[c8] = make_uint4(pack_bf16x2(x[8 * c8], x[8 * c8 + 1]), pack_bf16x2(x[8 * c8 + 2], x[8 * c8 + 3]),
+                           pack_bf16x2(x[8 * c8 + 4], x[8 * c8 + 5]), pack_bf16x2(x[8 * c8 + 6], x[8 * c8 + 7]));
+    uint4 *d = reinterpret_cast<uint4 *>(dst);
+    if ((reinterpret_cast<uintptr_t>(dst) & 31u) == 0) {
+#pragma unroll
+        for (int c16 = 0; c16 < NCOL / 16; ++c16) st_global_v8(d + 2 * c16, w[2 * c16], w[2 * c16 + 1]);
+    } else {
+#pragma unroll
+        for (int c8 = 0; c8 < NCOL / 8; ++c8) d[c8] = w[c8];
+    }
+}
+
+// Columns c0..c0+31 of bf16 row r of a swizzled [kC x cols] tile as fp32.
+__device__ __forceinline__ void load_row32(const uint8_t *tile, int r, int c0, float (&x)[32]) {
+#pragma unroll
+    for (int c8 = 0; c8 < 4; ++c8) {
+        const int c = c0 + 8 * c8;
+        const uint4 v = *reinterpret_cast<const uint4 *>(tile + (c / 64) * kC * 128 + sw128_offset(r, c % 64));
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            x[8 * c8 + 2 * e] = bf16lo(w[e]);
+            x[8 * c8 + 2 * e + 1] = bf16hi(w[e]);
+        }
+    }
+}
+
+// Every thread's shared-memory writes and TMEM stores visible to the MMAs
+// thread 0 issues next; false (CTA-uniform) if any thread's `mine` is false.
+__device__ __forceinline__ bool operands_ready(bool mine) {
+    tmem_wait_st();
+    fence_proxy_async();
+    tc_fence_before();
+    const bool all = __syncthreads_and(mine ? 1 : 0) != 0;
+    tc_fence_after();
+    return all;
+}
+
+// Thread 0 commits its MMAs to `bar`; every thread waits for that phase.
+__device__ __forceinline__ bool mma_done(uint64_t *bar, uint32_t &phase) {
+    if (threadIdx.x == 0) mma_commit(bar);
+    const bool got = mbar_wait_bounded(bar, phase, now_ns() + kWaitNs, nullptr);
+    phase ^= 1u;
+    tc_fence_after();
+    return __syncthreads_and(got ? 1 : 0) != 0;
+}
+
+struct NcBwdArgs {
+    const float *ws_in;      // [BH, nsplit, D*M + D]: the partials this kernel sums
+    float *ws_out;           // [BH, nsplit, D*M + D]: the partials this kernel writes (query kernel)
+    __nv_bfloat16 *g0, *g1;  // query kernel: dQ; key kernel: dK, dV
+    int N, nsplit, cps;
+    int *err;
+};
+
+// ------------------------------------------------------------ query kernel
+template <int D, int M>
+struct QCfg {
+    static constexpr int TQ = kC * D * 2, TG = kC * M * 2;
+    static constexpr int STAGE = TQ + TG;
+    static constexpr int OFF_SNAP = 2 * STAGE;                       // [S_hi | z | S_lo]
+    static constexpr int OFF_E = OFF_SNAP + XwTile<D, M>::BYTES;     // (e_hi, e_hi, e_lo, e_lo) atom, 128 rows
+    static constexpr int OFF_BAR = OFF_E + kC * 128;
+    static constexpr int SMEM = OFF_BAR + 64;
+    // TMEM: [num | den parts] (M + 16), then dphi(Q) (D) over it once read;
+    // [dS | dz parts] (M + 16)
+    static constexpr uint32_t COL_O = 0, COL_DQ = 0, COL_DS = (M + 16 > D ? M + 16 : D);
+    static constexpr uint32_t TMEM_COLS = COL_DS + M + 16 <= 256 ? 256 : 512;
+    static_assert(SMEM <= (int)kSmemMax, "shared memory budget");
+};
+
+template <int D, int M>
+__global__ void __launch_bounds__(kNT)
+nc_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_g,
+                    const NcBwdArgs args)
+{
+    using C = QCfg<D, M>;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int r = threadIdx.x;
+    const int bh = blockIdx.x / args.nsplit, sp = blockIdx.x % args.nsplit;
+    const int nch = (args.N + kC - 1) / kC;
+    const int c_begin = sp * args.cps;
+    const int n = max(0, min(nch, c_begin + args.cps) - c_begin);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR), *mbar = full + 2;
+    uint32_t *slot = reinterpret_cast<uint32_t *>(mbar + 1);
+    uint8_t *snap = smem + C::OFF_SNAP, *eat = smem + C::OFF_E;
+
+    bool ok = (smem_u32(smem) & 1023u) == 0;
+    if (r == 0) {
+        mbar_init(&full[0], 1);
+        mbar_init(&full[1], 1);
+        mbar_init(mbar, 1);
+        fence_mbar_init();
+    }
+    if (r < 32) {
+        tmem_alloc(slot, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *slot;
+    const uint32_t trow = tmem + ((uint32_t)(32 * (r >> 5)) << 16);
+    pdl_wait_cta();   // the key sums of the previous launch are complete
+
+    int issued = 0, consumed = 0;
+    auto load_chunk = [&](int it) {
+        ++issued;
+        uint8_t *st = smem + (it & 1) * C::STAGE;
+        const int t0 = (c_begin + it) * kC;
+        mbar_arrive_expect_tx(&full[it & 1], C::STAGE);
+#pragma unroll
+        for (int j = 0; j < D / 64; ++j) tma_load_3d(st + j * kC * 128, &tm_q, &full[it & 1], j * 64, t0, bh);
+#pragma unroll
+        for (int j = 0; j < M / 64; ++j) tma_load_3d(st + C::TQ + j * kC * 128, &tm_g, &full[it & 1], j * 64, t0, bh);
+    };
+    if (r == 0 && ok && n > 0) {
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_g);
+        load_chunk(0);
+    }
+    // [S | z_hi z_lo] of the head from the key-sum partials
+    sum_partials_to_tile<D, M>(args.ws_in + (size_t)bh * args.nsplit * (D * M + D), args.nsplit, snap, r);
+    ok = operands_ready(ok);
+    if (!ok && r == 0) record_error(args.err, kErrTimeout);
+
+    constexpr uint32_t ID_O = idesc_bf16(128, M + 16, 0, 1);   // phi(Q) K-major, [S | z] MN-major
+    constexpr uint32_t ID_OL = idesc_bf16(128, M, 0, 1);
+    constexpr uint32_t ID_DQ = idesc_bf16(128, D, 0, 0);       // [g | e] K-major, [S | z] K-major
+    constexpr uint32_t ID_DS = idesc_bf16(128, M, 1, 1);       // phi(Q)^T MN-major, g MN-major
+    constexpr uint32_t ID_DZ = idesc_bf16(128, 16, 1, 1);
+    uint32_t phase = 0;
+    bool mma_pending = false;
+    for (int it = 0; it < n && ok; ++it) {
+        const int s = it & 1, t0 = (c_begin + it) * kC;
+        const int valid = min(kC, args.N - t0);
+        uint8_t *tq = smem + s * C::STAGE, *tg = tq + C::TQ;
+        if (r == 0 && it + 1 < n) load_chunk(it + 1);   // into the stage released at the end of it - 1
+        const bool landed = mbar_wait_bounded(&full[s], (it >> 1) & 1, now_ns() + kWaitNs, nullptr);
+        if (!(ok = __syncthreads_and(landed) != 0)) {
+            if (r == 0) record_error(args.err, kErrTimeout);
+            break;
+        }
+        ++consumed;
+        phi_tile<D>(tq, r, valid);   // rows past the end become zeros
+        ok = operands_ready(true);
+        // ---- [num | den] = phi(Q) [S_hi | z] + phi(Q) [S_lo | -]
+        if (r == 0) {
+            const uint64_t dq = kmajor_base(smem_u32(tq));
+            const uint64_t db = smem_desc(smem_u32(snap), D * 128, 1024);
+            const uint64_t dl = smem_desc(smem_u32(snap + XwTile<D, M>::LO), D * 128, 1024);
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks)
+                mma_f16_ss(tmem + C::COL_O, dq + kmajor_step(ks), db + mnmajor_step(ks), ID_O, ks > 0);
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks)
+                mma_f16_ss(tmem + C::COL_O, dq + kmajor_step(ks), dl + mnmajor_step(ks), ID_OL, 1);
+        }
+        if (!(ok = mma_done(mbar, phase))) {
+            mma_pending = true;
+            break;
+        }
+        // ---- g = dO / den as bf16 (over dO in place), e = -(g . V'), V' = num / den
+        {
+            float dz[32];
+            tmem_ld32f(trow + C::COL_O + M, dz);   // den parts (z_hi, z_lo columns), then unused columns
+            const float den = dz[0] + dz[1];
+            const float inv = r < valid ? 1.f / den : 0.f;
+            float dot = 0.f;
+#pragma unroll 1
+            for (int c0 = 0; c0 < M; c0 += 32) {
+                float x[32], gv[32];
+                tmem_ld32f(trow + C::COL_O + c0, x);
+                load_row32(tg, r, c0, gv);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    gv[j] = __bfloat162float(__float2bfloat16_rn(gv[j] * inv));
+                    dot = fmaf(gv[j], x[j] * inv, dot);
+                }
+                store_snap32<kC>(tg, r, c0, gv);
+            }
+            const float e = -dot;
+            const float eh = __bfloat162float(__float2bfloat16_rn(e));
+            const uint32_t hh = pack_bf16x2(eh, eh), ll = pack_bf16x2(e - eh, e - eh);
+#pragma unroll
+            for (int c = 0; c < 64; c += 8)
+                *reinterpret_cast<uint4 *>(eat + sw128_offset(r, c)) =
+                    make_uint4(c == 0 ? hh : 0u, c == 0 ? ll : 0u, 0u, 0u);
+        }
+        ok = operands_ready(ok);
+        // ---- dphi(Q) = [g | e | g] [S_hi | z | S_lo]^T;  [dS | dz] += phi(Q)^T [g | e]
+        if (r == 0) {
+            const uint64_t dg = kmajor_base(smem_u32(tg)), de = kmajor_base(smem_u32(eat));
+            const uint64_t db = kmajor_base(smem_u32(snap)), dl = kmajor_base(smem_u32(snap + XwTile<D, M>::LO));
+#pragma unroll
+            for (int ks = 0; ks < M / 16; ++ks)
+                mma_f16_ss(tmem + C::COL_DQ, dg + kmajor_step(ks), db + kmajor_step(ks, D), ID_DQ, ks > 0);
+            mma_f16_ss(tmem + C::COL_DQ, de, db + kmajor_step(M / 16, D), ID_DQ, 1);   // the z atom
+#pragma unroll
+            for (int ks = 0; ks < M / 16; ++ks)
+                mma_f16_ss(tmem + C::COL_DQ, dg + kmajor_step(ks), dl + kmajor_step(ks, D), ID_DQ, 1);
+            // phi(Q)^T read MN-major; at D = 64 its 64 rows are read twice
+            // (M-atom stride 0) and accumulator lanes 64-127 are not used
+            const uint64_t da = smem_desc(smem_u32(tq), D == 64 ? 0 : kC * 128, 1024);
+            const uint64_t dgb = smem_desc(smem_u32(tg), kC * 128, 1024), deb = smem_desc(smem_u32(eat), kC * 128, 1024);
+#pragma unroll
+            for (int ks = 0; ks < kC / 16; ++ks) {
+                mma_f16_ss(tmem + C::COL_DS, da + mnmajor_step(ks), dgb + mnmajor_step(ks), ID_DS, it > 0 || ks > 0);
+                mma_f16_ss(tmem + C::COL_DS + M, da + mnmajor_step(ks), deb + mnmajor_step(ks), ID_DZ, it > 0 || ks > 0);
+            }
+        }
+        if (!(ok = mma_done(mbar, phase))) {
+            mma_pending = true;
+            break;
+        }
+        // ---- dQ = dphi(Q) min(phi(Q), 1)
+        {
+            float x[D];
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                float d32[32], f[32];
+                tmem_ld32f(trow + C::COL_DQ + c0, d32);
+                load_row32(tq, r, c0, f);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) x[c0 + j] = d32[j] * fminf(f[j], 1.f);
+            }
+            if (r < valid) store_row_bf16<D>(args.g0 + ((size_t)bh * args.N + t0 + r) * D, x);
+        }
+        __syncthreads();   // the stage is free for the load two chunks on
+    }
+    // [dS | dz] partial of this query range (zero for an empty range)
+    if (ok && r < D) {
+        float *dst = args.ws_out + ((size_t)bh * args.nsplit + sp) * (D * M + D);
+        float x[32];
+        for (int c0 = 0; c0 < M; c0 += 32) {
+            if (n > 0) {
+                tmem_ld32f(trow + C::COL_DS + c0, x);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) x[j] = 0.f;
+            }
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+                *reinterpret_cast<float4 *>(dst + r * M + c0 + j) = make_float4(x[j], x[j + 1], x[j + 2], x[j + 3]);
+        }
+        if (n > 0) tmem_ld32f(trow + C::COL_DS + M, x);
+        dst[D * M + r] = n > 0 ? x[0] + x[2] : 0.f;   // the e_hi and e_lo columns
+    }
+    if (!ok && r == 0) {
+        record_error(args.err, kErrTimeout);
+        for (int c = consumed; c < issued; ++c)
+            mbar_wait_bounded(&full[c & 1], (c >> 1) & 1, now_ns() + kWaitNs, nullptr);
+        if (mma_pending) mbar_wait_bounded(mbar, phase, now_ns() + kWaitNs, nullptr);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (r < 32) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+// -------------------------------------------------------------- key kernel
+template <int D, int M>
+struct KCfg {
+    static constexpr int TK = kC * D * 2, TV = kC * M * 2;
+    static constexpr int STAGE = TK + TV;
+    static constexpr int OFF_SNAP = 2 * STAGE;                       // [dS_hi | dz | dS_lo]
+    static constexpr int OFF_ONES = OFF_SNAP + XwTile<D, M>::BYTES;  // [1 1 0 ..] atom, 128 rows
+    static constexpr int OFF_BAR = OFF_ONES + kC * 128;
+    static constexpr int SMEM = OFF_BAR + 64;
+    static constexpr uint32_t COL_DK = 0, COL_DV = D;
+    static constexpr uint32_t TMEM_COLS = D + M <= 256 ? 256 : 512;
+    static_assert(SMEM <= (int)kSmemMax, "shared memory budget");
+};
+
+template <int D, int M>
+__global__ void __launch_bounds__(kNT)
+nc_bwd_key_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
+                  const NcBwdArgs args)
+{
+    using C = KCfg<D, M>;
+    extern __shared__ __align__(1024) uint8_t smem[];
+    const int r = threadIdx.x;
+    const int bh = blockIdx.x / args.nsplit, sp = blockIdx.x % args.nsplit;
+    const int nch = (args.N + kC - 1) / kC;
+    const int c_begin = sp * args.cps;
+    const int n = max(0, min(nch, c_begin + args.cps) - c_begin);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR), *mbar = full + 2;
+    uint32_t *slot = reinterpret_cast<uint32_t *>(mbar + 1);
+    uint8_t *snap = smem + C::OFF_SNAP, *ones = smem + C::OFF_ONES;
+
+    bool ok = (smem_u32(smem) & 1023u) == 0;
+    if (r == 0) {
+        mbar_init(&full[0], 1);
+        mbar_init(&full[1], 1);
+        mbar_init(mbar, 1);
+        fence_mbar_init();
+    }
+    if (r < 32) {
+        tmem_alloc(slot, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    // the ones atom: columns 0 and 1 of every row are 1 (they meet dz_hi, dz_lo)
+#pragma unroll
+    for (int c = 0; c < 64; c += 8)
+        *reinterpret_cast<uint4 *>(ones + sw128_offset(r, c)) = make_uint4(c == 0 ? 0x3F803F80u : 0u, 0u, 0u, 0u);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *slot;
+    const uint32_t trow = tmem + ((uint32_t)(32 * (r >> 5)) << 16);
+    pdl_wait_cta();   // the query kernel's partials are complete
+
+    int issued = 0, consumed = 0;
+    auto load_chunk = [&](int it) {
+        ++issued;
+        uint8_t *st = smem + (it & 1) * C::STAGE;
+        const int t0 = (c_begin + it) * kC;
+        mbar_arrive_expect_tx(&full[it & 1], C::STAGE);
+#pragma unroll
+        for (int j = 0; j < D / 64; ++j) tma_load_3d(st + j * kC * 128, &tm_k, &full[it & 1], j * 64, t0, bh);
+#pragma unroll
+        for (int j = 0; j < M / 64; ++j) tma_load_3d(st + C::TK + j * kC * 128, &tm_v, &full[it & 1], j * 64, t0, bh);
+    };
+    if (r == 0 && ok && n > 0) {
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_v);
+        load_chunk(0);
+    }
+    sum_partials_to_tile<D, M>(args.ws_in + (size_t)bh * args.nsplit * (D * M + D), args.nsplit, snap, r);
+    ok = operands_ready(ok);
+    if (!ok && r == 0) record_error(args.err, kErrTimeout);
+
+    constexpr uint32_t ID_DK = idesc_bf16(128, D, 0, 0);   // [V | 1 1] K-major, [dS | dz] K-major
+    constexpr uint32_t ID_DV = idesc_bf16(128, M, 0, 1);   // phi(K) K-major, dS MN-major
+    uint32_t phase = 0;
+    bool mma_pending = false;
+    for (int it = 0; it < n && ok; ++it) {
+        const int s = it & 1, t0 = (c_begin + it) * kC;
+        const int valid = min(kC, args.N - t0);
+        uint8_t *tk = smem + s * C::STAGE, *tv = tk + C::TK;
+        if (r == 0 && it + 1 < n) load_chunk(it + 1);
+        const bool landed = mbar_wait_bounded(&full[s], (it >> 1) & 1, now_ns() + kWaitNs, nullptr);
+        if (!(ok = __syncthreads_and(landed) != 0)) {
+            if (r == 0) record_error(args.err, kErrTimeout);
+            break;
+        }
+        ++consumed;
+        phi_tile<D>(tk, r, valid);
+        ok = operands_ready(true);
+        // ---- dphi(K) = [V | 1 | V] [dS_hi | dz | dS_lo]^T,  dV = phi(K) (dS_hi + dS_lo)
+        if (r == 0) {
+            const uint64_t dv = kmajor_base(smem_u32(tv)), d1 = kmajor_base(smem_u32(ones));
+            const uint64_t db = kmajor_base(smem_u32(snap)), dl = kmajor_base(smem_u32(snap + XwTile<D, M>::LO));
+#pragma unroll
+            for (int ks = 0; ks < M / 16; ++ks)
+                mma_f16_ss(tmem + C::COL_DK, dv + kmajor_step(ks), db + kmajor_step(ks, D), ID_DK, ks > 0);
+            mma_f16_ss(tmem + C::COL_DK, d1, db + kmajor_step(M / 16, D), ID_DK, 1);   // the dz atom
+#pragma unroll
+            for (int ks = 0; ks < M / 16; ++ks)
+                mma_f16_ss(tmem + C::COL_DK, dv + kmajor_step(ks), dl + kmajor_step(ks, D), ID_DK, 1);
+            const uint64_t dk = kmajor_base(smem_u32(tk));
+            const uint64_t ds = smem_desc(smem_u32(snap), D * 128, 1024);
+            const uint64_t dsl = smem_desc(smem_u32(snap + XwTile<D, M>::LO), D * 128, 1024);
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks)
+                mma_f16_ss(tmem + C::COL_DV, dk + kmajor_step(ks), ds + mnmajor_step(ks), ID_DV, ks > 0);
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks)
+                mma_f16_ss(tmem + C::COL_DV, dk + kmajor_step(ks), dsl + mnmajor_step(ks), ID_DV, 1);
+        }
+        if (!(ok = mma_done(mbar, phase))) {
+            mma_pending = true;
+            break;
+        }
+        // ---- dK = dphi(K) min(phi(K), 1), dV
+        {
+            float x[D > M ? D : M];
+#pragma unroll
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                float d32[32], f[32];
+                tmem_ld32f(trow + C::COL_DK + c0, d32);
+                load_row32(tk, r, c0, f);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) x[c0 + j] = d32[j] * fminf(f[j], 1.f);
+            }
+            if (r < valid) store_row_bf16<D>(args.g0 + ((size_t)bh * args.N + t0 + r) * D, x);
+#pragma unroll
+            for (int c0 = 0; c0 < M; c0 += 32) tmem_ld32f(trow + C::COL_DV + c0, *reinterpret_cast<float(*)[32]>(x + c0));
+            if (r < valid) store_row_bf16<M>(args.g1 + ((size_t)bh * args.N + t0 + r) * M, x);
+        }
+        __syncthreads();
+    }
+    if (!ok && r == 0) {
+        record_error(args.err, kErrTimeout);
+        for (int c = consumed; c < issued; ++c)
+            mbar_wait_bounded(&full[c & 1], (c >> 1) & 1, now_ns() + kWaitNs, nullptr);
+        if (mma_pending) mbar_wait_bounded(mbar, phase, now_ns() + kWaitNs, nullptr);
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (r < 32) tmem_dealloc(tmem, C::TMEM_COLS);
+}
+
+// Key/query ranges per head: enough CTAs to fill the device (two per SM at
+// D = M = 64, where both kernels fit twice), at most 16, whole chunks each.
+void nc_tc_grid(long long BH, int N, int sm_count, bool two_per_sm, int &nsplit, int &cps) {
+    const long long nch = (N + kC - 1) / kC;
+    const long long slots = (long long)std::max(sm_count, 1) * (two_per_sm ? 2 : 1);
+    long long want = (slots + BH - 1) / BH;
+    want = std::max(1LL, std::min(std::min(want, nch), 16LL));
+    cps = (int)((nch + want - 1) / want);
+    nsplit = (int)((nch + cps - 1) / cps);
+}
+
+template <int D, int M>
+cudaError_t launch_nc_bwd(const BwdProblem &p, const DeviceInfo &dev) {
+    int nsplit, cps;
+    nc_tc_grid(p.BH, p.N, dev.sm_count, D == 64 && M == 64, nsplit, cps);
+    const size_t part = (size_t)p.BH * nsplit * (D * M + D) * sizeof(float);
+    if (p.ws_bytes < 2 * part) return cudaErrorInvalidValue;
+    float *ws_s = (float *)p.ws, *ws_r = ws_s + part / sizeof(float);
+    CUtensorMap tq, tg, tk, tv;
+    if (!cached_tmap_bf16_3d(&tq, p.q, D, p.N, p.BH, 64, kC) || !cached_tmap_bf16_3d(&tg, p.dout, M, p.N, p.BH, 64, kC) ||
+        !cached_tmap_bf16_3d(&tk, p.k, D, p.N, p.BH, 64, kC) || !cached_tmap_bf16_3d(&tv, p.v, M, p.N, p.BH, 64, kC))
+        return cudaErrorInvalidValue;
+    cudaError_t e = tc_key_sums(p.k, p.v, p.BH, p.N, D, M, nsplit, cps, ws_s, part, p.stream, dev);
+    if (e != cudaSuccess) return e;
+    const dim3 grid((unsigned)(p.BH * nsplit)), block(kNT);
+    NcBwdArgs qa{ws_s, ws_r, (__nv_bfloat16 *)p.dq, nullptr, p.N, nsplit, cps, dev.err_word};
+    if ((e = set_smem(nc_bwd_query_kernel<D, M>, QCfg<D, M>::SMEM)) != cudaSuccess) return e;
+    e = launch_pdl(nc_bwd_query_kernel<D, M>, grid, block, QCfg<D, M>::SMEM, p.stream, 0u, tq, tg, qa);
+    count_launches(1);
+    if (e != cudaSuccess) return e;
+    NcBwdArgs ka{ws_r, nullptr, (__nv_bfloat16 *)p.dk, (__nv_bfloat16 *)p.dv, p.N, nsplit, cps, dev.err_word};
+    if ((e = set_smem(nc_bwd_key_kernel<D, M>, KCfg<D, M>::SMEM)) != cudaSuccess) return e;
+    e = launch_pdl(nc_bwd_key_kernel<D, M>, grid, block, KCfg<D, M>::SMEM, p.stream, 0u, tk, tv, ka);
+    count_launches(1);
+    return e;
+}
+
+}  // namespace
+
+size_t tc_nc_backward_ws_bytes(const la_shape &s) {
+    // the most ranges nc_tc_grid picks on any device (up to 192 SMs, two CTAs each)
+    const long long BH = (long long)s.B * s.H;
+    if (BH <= 0 || s.N <= 0) return 0;
+    int nsplit, cps;
+    nc_tc_grid(BH, s.N, 192, true, nsplit, cps);
+    return (size_t)2 * BH * nsplit * ((size_t)s.D * s.M + s.D) * sizeof(float);
+}
+
+bool tc_nc_backward_supported(const la_shape &s) {
+    return s.dtype == LA_DTYPE_BF16 && (s.D == 64 || s.D == 128) && (s.M == 64 || s.M == 128);
+}
+
+cudaError_t tc_noncausal_backward(const BwdProblem &p, const DeviceInfo &dev) {
+    if (p.D == 64 && p.M == 64) return launch_nc_bwd<64, 64>(p, dev);
+    if (p.D == 64 && p.M == 128) return launch_nc_bwd<64, 128>(p, dev);
+    if (p.D == 128 && p.M == 64) return launch_nc_bwd<128, 64>(p, dev);
+    if (p.D == 128 && p.M == 128) return launch_nc_bwd<128, 128>(p, dev);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace la
