@@ -848,6 +848,7 @@ def main():
     ap.add_argument("--only", default=None,
                     choices=["causal_b16h8n3072d64", "noncausal_b8h8n4096d64", "causal_b1h16n65536d128",
                              "decode_b256h16d64", "backward_causal_b16h8n3072d64",
+                             "backward_nc_causal_b16h8n3072d64",
                              "delta_b16h8n3072d64", "dpfp_b16h8n3072d64"],
                     help="time this one workload alone (--steps/--warmup; decode: --decode-steps) and print "
                          "its leg object; for profiler captures, not a bench line")

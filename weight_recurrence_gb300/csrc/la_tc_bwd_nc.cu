@@ -40,6 +40,21 @@
 #include "tc_kernels.cuh"
 #include "tc_ptx.cuh"
 
+// Optional per-phase timeline of CTA 0 of the query kernel for performance
+// work: compiled only with -DLA_TRACE (never in the library build).
+#ifdef LA_TRACE
+__device__ unsigned long long g_la_trace_ncbwd[32][8];
+extern "C" int la_trace_read_ncbwd(unsigned long long *dst) {
+    return (int)cudaMemcpyFromSymbol(dst, g_la_trace_ncbwd, sizeof(g_la_trace_ncbwd));
+}
+#define NCB_TRACE(it, ev)                                                                          \
+    do {                                                                                           \
+        if (blockIdx.x == 0 && threadIdx.x == 0 && (it) < 32) g_la_trace_ncbwd[it][ev] = clock64(); \
+    } while (0)
+#else
+#define NCB_TRACE(it, ev) ((void)0)
+#endif
+
 namespace la {
 namespace {
 
@@ -241,6 +256,7 @@ nc_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         const int s = it & 1, t0 = (c_begin + it) * kC;
         const int valid = min(kC, args.N - t0);
         uint8_t *tq = smem + s * C::STAGE, *tg = tq + C::TQ;
+        NCB_TRACE(it, 0);
         if (r == 0 && it + 1 < n) load_chunk(it + 1);   // into the stage released at the end of it - 1
         const bool landed = mbar_wait_bounded(&full[s], (it >> 1) & 1, now_ns() + kWaitNs, nullptr);
         if (!(ok = __syncthreads_and(landed) != 0)) {
@@ -248,8 +264,10 @@ nc_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             break;
         }
         ++consumed;
+        NCB_TRACE(it, 1);
         phi_tile<D>(tq, r, valid);   // rows past the end become zeros
         ok = operands_ready(true);
+        NCB_TRACE(it, 2);
         // ---- [num | den] = phi(Q) [S_hi | z] + phi(Q) [S_lo | -]
         if (r == 0) {
             const uint64_t dq = kmajor_base(smem_u32(tq));
@@ -266,6 +284,7 @@ nc_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             mma_pending = true;
             break;
         }
+        NCB_TRACE(it, 3);
         // ---- g = dO / den as bf16 (over dO in place), e = -(g . V'), V' = num / den
         {
             float dz[32];
@@ -294,6 +313,7 @@ nc_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
                     make_uint4(c == 0 ? hh : 0u, c == 0 ? ll : 0u, 0u, 0u);
         }
         ok = operands_ready(ok);
+        NCB_TRACE(it, 4);
         // ---- dphi(Q) = [g | e | g] [S_hi | z | S_lo]^T;  [dS | dz] += phi(Q)^T [g | e]
         if (r == 0) {
             const uint64_t dg = kmajor_base(smem_u32(tg)), de = kmajor_base(smem_u32(eat));
@@ -319,6 +339,7 @@ nc_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             mma_pending = true;
             break;
         }
+        NCB_TRACE(it, 5);
         // ---- dQ = dphi(Q) min(phi(Q), 1)
         {
             float x[D];
@@ -332,6 +353,7 @@ nc_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             }
             if (r < valid) store_row_bf16<D>(args.g0 + ((size_t)bh * args.N + t0 + r) * D, x);
         }
+        NCB_TRACE(it, 6);
         __syncthreads();   // the stage is free for the load two chunks on
     }
     // [dS | dz] partial of this query range (zero for an empty range)
@@ -508,12 +530,15 @@ nc_bwd_key_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
     if (r < 32) tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
-// Key/query ranges per head: enough CTAs to fill the device (two per SM at
-// D = M = 64, where both kernels fit twice), at most 16, whole chunks each.
+// Key/query ranges per head: as many CTAs as fit on the device at once (two
+// per SM at D = M = 64, where both kernels fit twice), so that all run in one
+// wave (measured on 128 heads x 3072 rows: 3 ranges a head, 1.26 waves,
+// 185 us for the three launches; 2 ranges, one wave, 137 us), at most 16,
+// whole chunks each.
 void nc_tc_grid(long long BH, int N, int sm_count, bool two_per_sm, int &nsplit, int &cps) {
     const long long nch = (N + kC - 1) / kC;
     const long long slots = (long long)std::max(sm_count, 1) * (two_per_sm ? 2 : 1);
-    long long want = (slots + BH - 1) / BH;
+    long long want = slots / BH;
     want = std::max(1LL, std::min(std::min(want, nch), 16LL));
     cps = (int)((nch + want - 1) / want);
     nsplit = (int)((nch + cps - 1) / cps);
