@@ -357,7 +357,8 @@ unsigned long long la_launch_count(void);
  * stores; in the segment-sum pre-pass its workspace slot writes; in the
  * non-causal tensor-core kernel (exchange through the workspace) and in the
  * non-causal CUDA-core kernels (also used by la_forward_noncausal_noalloc)
- * the workspace slot writes and reads.  TMA copies are clipped to their tensor
+ * the workspace slot writes and reads; in the non-causal tensor-core backward
+ * the reads and writes of its partial sums.  TMA copies are clipped to their tensor
  * maps by the hardware, and the decode kernels index by block and thread
  * alone, so neither carries a check.  A failed check skips its access and
  * records LA_ERR_BOUNDS in the device error word, which la_get_last_error()

@@ -142,3 +142,22 @@ def test_release_build_ignores_the_hook():
     finally:
         assert la.select_library(True) is not release
     assert np.isfinite(out.float().cpu().numpy()).all()
+
+
+@pytest.mark.parametrize("D,M", [(64, 64), (128, 128)])
+def test_noncausal_backward_is_clean_and_exact(D, M):
+    """The tensor-core non-causal backward (key sums, query and key passes) through the checked build."""
+    B, H, N = 1, 2, 700
+    qh, kh, vh = inputs.qkv(B, H, N, D, M, torch.bfloat16, 0.25, seed=39)
+    G = torch.randn((B, H, N, M), generator=torch.Generator().manual_seed(40)).to(torch.bfloat16)
+    got = la.la_backward_noncausal(qh.to(DEV), kh.to(DEV), vh.to(DEV), G.to(DEV))
+    assert _err() == la.LA_OK
+    ref = oracle.noncausal_backward(qh, kh, vh, G)
+    for g, r in zip(got, ref):
+        y = g.float().cpu().numpy().astype(np.float64).reshape(B * H, -1)
+        rr = np.asarray(r, np.float64).reshape(B * H, -1)
+        den = np.maximum(np.abs(rr).max(axis=-1), 1e-3 * float(G.float().abs().max()))
+        assert float((np.abs(y - rr).max(axis=-1) / den).max()) <= 2e-2
+    # the key-sum pass offsets its workspace slot past the workspace: caught
+    qd, kd, vd, Gd = qh.to(DEV), kh.to(DEV), vh.to(DEV), G.to(DEV)
+    assert _injected(lambda: la.la_backward_noncausal(qd, kd, vd, Gd)) == la.LA_ERR_BOUNDS

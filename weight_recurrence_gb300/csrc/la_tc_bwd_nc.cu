@@ -172,6 +172,7 @@ struct NcBwdArgs {
     __nv_bfloat16 *g0, *g1;  // query kernel: dQ; key kernel: dK, dV
     int N, nsplit, cps;
     int *err;
+    long long ws_floats;     // floats in each of ws_in, ws_out (checked build)
 };
 
 // ------------------------------------------------------------ query kernel
@@ -241,7 +242,10 @@ nc_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         load_chunk(0);
     }
     // [S | z_hi z_lo] of the head from the key-sum partials
-    sum_partials_to_tile<D, M>(args.ws_in + (size_t)bh * args.nsplit * (D * M + D), args.nsplit, snap, r);
+    // the head's slots lie inside the workspace (checked build)
+    const bool ws_ok = LA_IN_BOUNDS(((long long)bh + 1) * args.nsplit * (D * M + D) <= args.ws_floats, args.err);
+    if (ws_ok)
+        sum_partials_to_tile<D, M>(args.ws_in + (size_t)bh * args.nsplit * (D * M + D), args.nsplit, snap, r);
     ok = operands_ready(ok);
     if (!ok && r == 0) record_error(args.err, kErrTimeout);
 
@@ -357,7 +361,7 @@ nc_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         __syncthreads();   // the stage is free for the load two chunks on
     }
     // [dS | dz] partial of this query range (zero for an empty range)
-    if (ok && r < D) {
+    if (ok && r < D && ws_ok) {
         float *dst = args.ws_out + ((size_t)bh * args.nsplit + sp) * (D * M + D);
         float x[32];
         for (int c0 = 0; c0 < M; c0 += 32) {
@@ -454,7 +458,10 @@ nc_bwd_key_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         prefetch_tmap(&tm_v);
         load_chunk(0);
     }
-    sum_partials_to_tile<D, M>(args.ws_in + (size_t)bh * args.nsplit * (D * M + D), args.nsplit, snap, r);
+    // the head's slots lie inside the workspace (checked build)
+    const bool ws_ok = LA_IN_BOUNDS(((long long)bh + 1) * args.nsplit * (D * M + D) <= args.ws_floats, args.err);
+    if (ws_ok)
+        sum_partials_to_tile<D, M>(args.ws_in + (size_t)bh * args.nsplit * (D * M + D), args.nsplit, snap, r);
     ok = operands_ready(ok);
     if (!ok && r == 0) record_error(args.err, kErrTimeout);
 
@@ -558,12 +565,14 @@ cudaError_t launch_nc_bwd(const BwdProblem &p, const DeviceInfo &dev) {
     cudaError_t e = tc_key_sums(p.k, p.v, p.BH, p.N, D, M, nsplit, cps, ws_s, part, p.stream, dev);
     if (e != cudaSuccess) return e;
     const dim3 grid((unsigned)(p.BH * nsplit)), block(kNT);
-    NcBwdArgs qa{ws_s, ws_r, (__nv_bfloat16 *)p.dq, nullptr, p.N, nsplit, cps, dev.err_word};
+    const long long part_floats = (long long)(part / sizeof(float));
+    NcBwdArgs qa{ws_s, ws_r, (__nv_bfloat16 *)p.dq, nullptr, p.N, nsplit, cps, dev.err_word, part_floats};
     if ((e = set_smem(nc_bwd_query_kernel<D, M>, QCfg<D, M>::SMEM)) != cudaSuccess) return e;
     e = launch_pdl(nc_bwd_query_kernel<D, M>, grid, block, QCfg<D, M>::SMEM, p.stream, 0u, tq, tg, qa);
     count_launches(1);
     if (e != cudaSuccess) return e;
-    NcBwdArgs ka{ws_r, nullptr, (__nv_bfloat16 *)p.dk, (__nv_bfloat16 *)p.dv, p.N, nsplit, cps, dev.err_word};
+    NcBwdArgs ka{ws_r, nullptr, (__nv_bfloat16 *)p.dk, (__nv_bfloat16 *)p.dv, p.N, nsplit, cps, dev.err_word,
+                 part_floats};
     if ((e = set_smem(nc_bwd_key_kernel<D, M>, KCfg<D, M>::SMEM)) != cudaSuccess) return e;
     e = launch_pdl(nc_bwd_key_kernel<D, M>, grid, block, KCfg<D, M>::SMEM, p.stream, 0u, tk, tv, ka);
     count_launches(1);
