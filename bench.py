@@ -144,6 +144,9 @@ KERNEL_SOURCES = {
                                            "la_common.cuh", "la_internal.h"),
     "backward_causal_b16h8n3072d64": ("la_tc_bwd.cu", "tc_kernels.cuh", "tc_ptx.cuh", "tc_host.h", "la_common.cuh",
                                       "la_internal.h"),
+    # key sums (la_tc.cu), then the query and key passes
+    "backward_nc_causal_b16h8n3072d64": ("la_tc_bwd_nc.cu", "la_tc.cu", "tc_kernels.cuh", "tc_ptx.cuh", "tc_host.h",
+                                         "la_common.cuh", "la_internal.h"),
 }
 
 
