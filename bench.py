@@ -559,10 +559,10 @@ def _leg_variant(torch, la, inputs, name, dev, stream, rot, pk, steps, max_over_
     # per head-token: state update 2FM (+ retrieval 2FM for the delta rule) and read-out 2FM
     flops = w.B * w.H * w.N * (6 if update == "delta" else 4) * F * w.M
     tf = flops / (ms / 1e3) / 1e12
-    # the library's routing rule: bf16 sum-update variants without the
-    # denominator and with F, M in {64, 128} run the chunked tcgen05 kernel
-    tc = (w.dtype == torch.bfloat16 and update == "sum" and norm != "den" and F in (64, 128)
-          and w.M in (64, 128))
+    # the library's routing rule: bf16 sum-update variants with F, M in
+    # {64, 128} (elu + 1 or DPFP) run the chunked tcgen05 kernel
+    tc = (w.dtype == torch.bfloat16 and update == "sum" and F in (64, 128) and w.M in (64, 128)
+          and fm in ("elu1", "dpfp"))
     # ... and bf16 delta-rule variants with sum-normalised features of width 64, M = 64
     tc_delta = (w.dtype == torch.bfloat16 and update == "delta" and norm == "sum" and F == 64 and w.M == 64
                 and (fm == "elu1" or (fm == "dpfp" and (w.D, nu) in ((32, 1), (16, 2)))))

@@ -240,9 +240,9 @@ la_status la_backward_noncausal(const void *q, const void *k, const void *v, con
  * the state bounded).  Other combinations return LA_ERR_UNSUPPORTED;
  * unknown enum values LA_ERR_INVALID_ARG.
  * State layout: S [B, H, F, M] fp32 (S[f][m]); z [B, H, F] fp32 (LA_NORM_DEN
- * only).  Arithmetic: bf16 inputs of a sum-update variant without the
- * denominator with F, M in {64, 128} (elu + 1 raw or sum-normalised; DPFP
- * from D = 64 / nu = 1, D = 32 / nu = 1 or 2, D = 16 / nu = 2 or 4), and of
+ * only).  Arithmetic: bf16 inputs of a sum-update variant with F, M in
+ * {64, 128} (elu + 1 raw, sum-normalised or with the denominator; DPFP from
+ * D = 64 / nu = 1, D = 32 / nu = 1 or 2, D = 16 / nu = 2 or 4), and of
  * the delta rule with sum-normalised features of width 64 (elu + 1 at
  * D = 64, DPFP at D = 32 / nu = 1 or D = 16 / nu = 2) and M = 64, run on
  * tensor cores (bf16 feature rows and operands, fp32 accumulation and

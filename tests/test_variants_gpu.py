@@ -67,9 +67,13 @@ def _ids(c):
                                                "f32" if c[9] == torch.float32 else "bf16")
 
 
-# bf16, sum update, no denominator, F in {64, 128}: these run on the chunked
-# tensor-core kernel, the feature map applied row by row on chip
+# bf16, sum update, F in {64, 128}: these run on the chunked tensor-core
+# kernel, the feature map applied row by row on chip (elu + 1 also with the
+# denominator, long enough that the plain form would split it into segments)
 TC_CASES = [
+    ("elu1", 1, "den", "sum", 1, 2, 9000, 64, 64, torch.bfloat16, 0.125),
+    ("elu1", 1, "den", "sum", 2, 2, 1000, 64, 64, torch.bfloat16, 0.125),
+    ("elu1", 1, "den", "sum", 1, 2, 300, 128, 128, torch.bfloat16, 1.0 / math.sqrt(128)),
     ("dpfp", 1, "sum", "sum", 2, 2, 1000, 64, 64, torch.bfloat16, 0.125),
     ("dpfp", 1, "none", "sum", 1, 2, 300, 64, 128, torch.bfloat16, 0.125),
     ("dpfp", 1, "sum", "sum", 1, 3, 257, 32, 64, torch.bfloat16, 0.25),
@@ -172,7 +176,8 @@ NC_CASES = [
     ("dpfp", 1, "sum", 2, 2, 700, 64, 64, torch.bfloat16, 0.125),
     ("dpfp", 3, "none", 1, 1, 90, 32, 16, torch.float32, 1.0),
     ("poly2", 1, "den", 1, 2, 333, 16, 128, torch.float32, 1.0),
-    # bf16 without the denominator, F in {64, 128}: the one-launch tensor-core kernel
+    # bf16, F in {64, 128}: the one-launch tensor-core kernel
+    ("elu1", 1, "den", 1, 2, 777, 128, 64, torch.bfloat16, 1.0 / math.sqrt(128)),
     ("dpfp", 1, "sum", 2, 3, 1000, 32, 128, torch.bfloat16, 0.25),
     ("dpfp", 4, "none", 1, 2, 257, 16, 64, torch.bfloat16, 0.5),
     ("elu1", 1, "sum", 2, 2, 3000, 64, 64, torch.bfloat16, 0.125),

@@ -41,6 +41,7 @@ struct Problem {
     int dr = 0, nu = 0;          // raw width of q, k rows and DPFP shifts (feat != 0)
     bool sum_norm = false;       // DPFP: rows divided by their sums
     bool no_den = false;         // output = numerator (no denominator)
+    bool no_segments = false;    // causal: one CTA per head (the call has no workspace)
 };
 
 // Backward-pass problem (sizes already validated).

@@ -1660,7 +1660,9 @@ cudaError_t launch_causal(const Problem &p, const DeviceInfo &dev) {
     // per-sequence lengths, step-major decode inputs or a variant (the
     // segment-sum pre-pass applies elu + 1 and variant calls pass no
     // workspace): no segments
-    int nseg = (p.lens || p.step_major || p.feat != kFeatPhi || p.no_den) ? 1 : causal_nseg(p.BH, p.N, dev.sm_count);
+    int nseg = (p.lens || p.step_major || p.feat != kFeatPhi || p.no_den || p.no_segments)
+                   ? 1
+                   : causal_nseg(p.BH, p.N, dev.sm_count);
     const int cps = (nch + nseg - 1) / nseg;
     nseg = (nch + cps - 1) / cps;
     cudaError_t e;
@@ -1762,8 +1764,10 @@ bool tc_dims(const la_shape &s) {
 bool tc_causal_supported(const la_shape &s, int) { return tc_dims(s); }
 
 bool tc_variant_route(const la_shape &s, const la_variant &v, Problem &p) {
-    // sum update without the denominator, bf16, feature width 64 or 128
-    if (s.dtype != LA_DTYPE_BF16 || v.update != LA_UPDATE_SUM || v.norm == LA_NORM_DEN) return false;
+    // sum update, bf16, feature width 64 or 128; with the denominator elu + 1
+    // only (it is then the plain form, run without segments: the variant
+    // calls have no workspace)
+    if (s.dtype != LA_DTYPE_BF16 || v.update != LA_UPDATE_SUM) return false;
     if (s.M != 64 && s.M != 128) return false;
     const int F = fw_feature_dim(v, s.D);
     if (F != 64 && F != 128) return false;
@@ -1781,7 +1785,8 @@ bool tc_variant_route(const la_shape &s, const la_variant &v, Problem &p) {
     }
     p.dr = s.D;
     p.nu = v.nu;
-    p.no_den = true;
+    p.no_den = v.norm != LA_NORM_DEN;
+    p.no_segments = true;   // a variant call passes no workspace
     p.D = F;
     return true;
 }
