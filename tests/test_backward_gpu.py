@@ -103,10 +103,13 @@ def test_noncausal_backward_vs_oracle(B, H, N, D, M, dtype, scale):
     _check_grads(got, ref, dtype, G, "noncausal")
 
 
-@pytest.mark.parametrize("dtype,D", [(torch.float32, 32), (torch.bfloat16, 32), (torch.bfloat16, 64)])
-def test_causal_backward_with_state(dtype, D):
-    """Carried-in state, gradient through the final state, and dS0/dz0 out."""
-    B, H, N, M = 2, 2, 150, 64
+@pytest.mark.parametrize("dtype,D,M", [(torch.float32, 32, 64), (torch.bfloat16, 32, 64), (torch.bfloat16, 64, 64),
+                                       (torch.bfloat16, 128, 128), (torch.bfloat16, 64, 128),
+                                       (torch.bfloat16, 128, 64)])
+def test_causal_backward_with_state(dtype, D, M):
+    """Carried-in state, gradient through the final state, and dS0/dz0 out
+    (bf16 with D, M >= 64: the tensor-core paths, sequential and chunked)."""
+    B, H, N = 2, 2, 150 if D == M == 64 else 400
     q, k, v = inputs.qkv(B, H, N, D, M, dtype, 0.25, seed=901)
     G = _dout(B, H, N, M, dtype, 902)
     S0, z0 = inputs.state(B, H, D, M, seed=903, scale=0.05)
@@ -119,14 +122,16 @@ def test_causal_backward_with_state(dtype, D):
     got = la.la_backward_causal(qd, kd, vd, Gd, S0=S0d, z0=z0d, dSN=dSNd, dzN=dzNd, dS0=dS0, dz0=dz0)
     torch.cuda.synchronize()
     _check_grads(got, (rq, rk, rv), dtype, G, "state")
-    assert head_rel_err(dS0.cpu(), rS) <= (1e-4 if D != 64 else 2e-2)
-    assert head_rel_err(dz0.cpu(), rz) <= (1e-4 if D != 64 else 2e-2)
+    tc = dtype == torch.bfloat16 and D >= 64
+    assert head_rel_err(dS0.cpu(), rS) <= (2e-2 if tc else 1e-4)
+    assert head_rel_err(dz0.cpu(), rz) <= (2e-2 if tc else 1e-4)
 
 
-@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
-def test_causal_backward_split_chains(dtype):
+@pytest.mark.parametrize("dtype,D,M", [(torch.float32, 64, 64), (torch.bfloat16, 64, 64),
+                                       (torch.bfloat16, 128, 128)])
+def test_causal_backward_split_chains(dtype, D, M):
     """Backward of two segments joined through dS0 -> dSN equals the whole backward."""
-    B, H, N, D, M, split = 1, 2, 333, 64, 64, 130
+    B, H, N, split = 1, 2, 333, 130
     q, k, v = inputs.qkv(B, H, N, D, M, dtype, 0.125, seed=910)
     G = _dout(B, H, N, M, dtype, 911)
     qd, kd, vd, Gd = _dev(q, k, v, G)
@@ -185,6 +190,51 @@ def test_full_causal_backward_b16h8n3072d64():
         ref = oracle.causal_backward(q[b, h][None], k[b, h][None], v[b, h][None], G[b, h][None])[:3]
         for got, r in zip((dq, dk, dv), ref):
             assert grad_err(got[b, h][None], r, G[b, h][None], nlead=1) <= 2e-2
+
+
+# Chunk-parallel causal backward on tensor cores (bf16, D, M in {64, 128}
+# other than D = M = 64): one row, shorter than a chunk, one chunk exactly, a
+# last chunk of one row, many chunks with a ragged tail, all three (D, M).
+CHUNK_TC_CASES = [
+    (1, 1, 1, 128, 128, 1.0 / math.sqrt(128)),
+    (1, 2, 77, 128, 128, 1.0 / math.sqrt(128)),
+    (2, 1, 128, 64, 128, 0.25),
+    (1, 2, 129, 128, 64, 1.0 / math.sqrt(128)),
+    (1, 2, 1000, 128, 128, 1.0 / math.sqrt(128)),
+    (2, 2, 3000, 64, 128, 0.125),
+    (1, 1, 4097, 128, 64, 1.0),
+]
+
+
+@pytest.mark.parametrize("B,H,N,D,M,scale", CHUNK_TC_CASES)
+def test_causal_backward_chunked_tensor_cores(B, H, N, D, M, scale):
+    dtype = torch.bfloat16
+    q, k, v = inputs.qkv(B, H, N, D, M, dtype, scale, seed=1300 + N)
+    G = _dout(B, H, N, M, dtype, 1400 + N)
+    ref = oracle.causal_backward(q, k, v, G)[:3]
+    n0 = la.la_launch_count()
+    got = la.la_backward_causal(*_dev(q, k, v, G))
+    torch.cuda.synchronize()
+    assert la.la_get_last_error() == la.LA_OK
+    # chunk sums, forward scan, query pass, reverse scan, key pass
+    assert la.la_launch_count() - n0 == 5
+    _check_grads(got, ref, dtype, G, "causal chunked tc")
+
+
+def test_full_causal_backward_b1h16n65536d128():
+    """The long-context shape (D = M = 128) at full size; sampled heads against the oracle."""
+    w = inputs.WORKLOADS["causal_b1h16n65536d128"]
+    q, k, v = inputs.workload_inputs(w)
+    G = _dout(w.B, w.H, w.N, w.M, w.dtype, 950)
+    dq, dk, dv = la.la_backward_causal(*_dev(q, k, v, G))
+    torch.cuda.synchronize()
+    assert la.la_get_last_error() == la.LA_OK
+    rng = np.random.default_rng(951)
+    for h in rng.choice(w.H, size=2, replace=False):
+        h = int(h)
+        ref = oracle.causal_backward(q[0, h][None], k[0, h][None], v[0, h][None], G[0, h][None])[:3]
+        for got, r in zip((dq, dk, dv), ref):
+            assert grad_err(got[0, h][None], r, G[0, h][None], nlead=1) <= 2e-2
 
 
 # Non-causal backward on tensor cores (bf16, D, M in {64, 128}): key ranges

@@ -206,6 +206,7 @@ la_status la_backward_causal(const void *q, const void *k, const void *v, const 
     BwdProblem p{q, k, v, dout, dq, dk, dv, S0, z0, dSN, dzN, dS0, dz0,
                  BH, s.N, s.D, s.M, s.dtype, workspace, ws_bytes, (cudaStream_t)stream};
     if (tc_backward_supported(s)) return from_cuda(tc_causal_backward(p, *dev));
+    if (tc_chunk_backward_supported(s)) return from_cuda(tc_chunk_causal_backward(p, *dev));
     return from_cuda(causal_backward(p, *dev));
 }
 

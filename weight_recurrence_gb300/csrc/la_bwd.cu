@@ -636,8 +636,9 @@ size_t causal_bwd_ws_bytes(const la_shape &s) {
     if (BH <= 0 || s.N <= 0) return 0;
     int nseg, L;
     bwd_seg_grid(BH, s.N, 192, nseg, L);
-    return (size_t)BH * ((size_t)s.N * ((size_t)s.M + 1) + 2 * (size_t)nseg * ((size_t)s.D * s.M + s.D)) *
-           sizeof(float);
+    const size_t simt = (size_t)BH * ((size_t)s.N * ((size_t)s.M + 1) + 2 * (size_t)nseg * ((size_t)s.D * s.M + s.D)) *
+                        sizeof(float);
+    return tc_chunk_backward_supported(s) ? std::max(simt, tc_chunk_backward_ws_bytes(s)) : simt;
 }
 
 size_t noncausal_bwd_ws_bytes(const la_shape &s) {

@@ -72,6 +72,11 @@ cudaError_t tc_key_sums(const void *k, const void *v, long long BH, int N, int D
 // tensor-core non-causal backward (la_tc_bwd_nc.cu): bf16, D, M in {64, 128}
 bool tc_nc_backward_supported(const la_shape &s);
 size_t tc_nc_backward_ws_bytes(const la_shape &s);
+// chunk-parallel tensor-core causal backward (la_tc_bwd_chunk.cu): bf16,
+// D, M in {64, 128} other than D = M = 64
+bool tc_chunk_backward_supported(const la_shape &s);
+size_t tc_chunk_backward_ws_bytes(const la_shape &s);
+cudaError_t tc_chunk_causal_backward(const BwdProblem &p, const DeviceInfo &dev);
 cudaError_t tc_noncausal_backward(const BwdProblem &p, const DeviceInfo &dev);
 cudaError_t tc_causal_backward(const BwdProblem &p, const DeviceInfo &dev);
 
