@@ -145,8 +145,11 @@ KERNEL_SOURCES = {
     "backward_causal_b16h8n3072d64": ("la_tc_bwd.cu", "tc_kernels.cuh", "tc_ptx.cuh", "tc_host.h", "la_common.cuh",
                                       "la_internal.h"),
     # key sums (la_tc.cu), then the query and key passes
-    "backward_nc_causal_b16h8n3072d64": ("la_tc_bwd_nc.cu", "la_tc.cu", "tc_kernels.cuh", "tc_ptx.cuh", "tc_host.h",
-                                         "la_common.cuh", "la_internal.h"),
+    "backward_nc_causal_b16h8n3072d64": ("la_tc_bwd_nc.cu", "tc_bwd_common.cuh", "la_tc.cu", "tc_kernels.cuh",
+                                         "tc_ptx.cuh", "tc_host.h", "la_common.cuh", "la_internal.h"),
+    # per-chunk key sums (la_tc.cu), two scans, the query and key passes
+    "backward_causal_b1h16n65536d128": ("la_tc_bwd_chunk.cu", "tc_bwd_common.cuh", "la_tc.cu", "tc_kernels.cuh",
+                                        "tc_ptx.cuh", "tc_host.h", "la_common.cuh", "la_internal.h"),
 }
 
 
@@ -423,6 +426,8 @@ def run_ours(args, rank, world, dist):
                                                    max_over_ranks, world, rank)
         result["legs"]["backward_noncausal"] = _leg_backward(torch, la, inputs, MAIN, dev, stream, rot, pk, 5,
                                                              max_over_ranks, world, rank, noncausal=True)
+        result["legs"]["backward_long"] = _leg_backward(torch, la, inputs, "causal_b1h16n65536d128", dev, stream,
+                                                        rot, pk, 5, max_over_ranks, world, rank)
         for name in ("delta_b16h8n3072d64", "dpfp_b16h8n3072d64"):
             result["legs"][name.split("_")[0]] = _leg_variant(torch, la, inputs, name, dev, stream, rot, pk, 5,
                                                               max_over_ranks, world, rank)
@@ -444,6 +449,10 @@ def run_ours(args, rank, world, dist):
             legs["backward"]["cpu_baseline"] = cpu_baseline_backward(w, budget_s=cs)
         if "backward_noncausal" in legs:
             legs["backward_noncausal"]["cpu_baseline"] = cpu_baseline_backward(w, budget_s=cs, noncausal=True)
+        if "backward_long" in legs:
+            # all 16 heads over their first 4096 tokens (the recurrence costs the same per token)
+            legs["backward_long"]["cpu_baseline"] = cpu_baseline_backward(inputs.WORKLOADS["causal_b1h16n65536d128"],
+                                                                          budget_s=cs, rows=4096)
         for name in ("delta_b16h8n3072d64", "dpfp_b16h8n3072d64"):
             key = name.split("_")[0]
             if key in legs:
@@ -521,7 +530,11 @@ def _leg_backward(torch, la, inputs, name, dev, stream, rot, pk, steps, max_over
                     "a key pass (dK, dV); K and V are read twice, so traffic is 9 tensors against 7 algorithmic"
                     if noncausal else
                     "tcgen05 kernels (bf16 D = M = 64): a forward sweep (dQ, keeps g and e) and a reverse "
-                    "sweep (dK, dV), one CTA per head each")}
+                    "sweep (dK, dV), one CTA per head each" if w.D == 64 and w.M == 64 else
+                    "tcgen05 kernels, chunk-parallel (bf16 D, M in {64, 128}): per-chunk key sums, an exclusive "
+                    "scan into each chunk's entering state, a query pass (dQ, g, e, per-chunk phi(Q)^T [g | e]), "
+                    "the reverse scan, a key pass (dK, dV), one CTA per 128-row chunk; the per-chunk fp32 sums "
+                    "(D*M + D floats per chunk) move through HBM five times")}
     del q, k, v, G, dq, dk, dv, sets
     torch.cuda.empty_cache()
     return leg
@@ -768,8 +781,9 @@ def cpu_baseline_decode(w, budget_s=4.0):
                       % (heads, w.B * w.H, w.steps, w.N, reps))
 
 
-def cpu_baseline_backward(w, budget_s=4.0, noncausal=False):
-    """The fp64 causal (or non-causal) backward oracle on a sample of heads; tokens/s as the forward."""
+def cpu_baseline_backward(w, budget_s=4.0, noncausal=False, rows=None):
+    """The fp64 causal (or non-causal) backward oracle on a sample of heads (and
+    of their first `rows` tokens, if given); tokens/s as the forward."""
     import oracle
     import torch
     from weight_recurrence_gb300 import inputs
@@ -777,14 +791,16 @@ def cpu_baseline_backward(w, budget_s=4.0, noncausal=False):
     oracle.build()
     nthreads = oracle.max_threads()
     heads = max(1, min(w.B * w.H, 2 * nthreads))
-    q, k, v = inputs.qkv(1, heads, w.N, w.D, w.M, w.dtype, w.scale, seed=w.seed)
+    n = min(w.N, rows) if rows else w.N
+    q, k, v = inputs.qkv(1, heads, n, w.D, w.M, w.dtype, w.scale, seed=w.seed)
     g = torch.Generator().manual_seed(w.seed + 2000)
     G = torch.randn(v.shape, generator=g).to(w.dtype)
     fn = oracle.noncausal_backward if noncausal else oracle.causal_backward
     dt, reps = _cpu_timed(lambda: fn(q, k, v, G, nthreads=nthreads), budget_s)
-    return _cpu_entry(heads * w.N / dt / w.H, "tokens/s", nthreads,
-                      "%d of %d heads x N=%d (fp64 %s backward oracle), %d reps; tokens/s = head-tokens/s / H"
-                      % (heads, w.B * w.H, w.N, "non-causal" if noncausal else "causal", reps))
+    return _cpu_entry(heads * n / dt / w.H, "tokens/s", nthreads,
+                      "%d of %d heads x N=%d%s (fp64 %s backward oracle), %d reps; tokens/s = head-tokens/s / H"
+                      % (heads, w.B * w.H, n, " (first rows of N=%d)" % w.N if n < w.N else "",
+                         "non-causal" if noncausal else "causal", reps))
 
 
 def cpu_baseline_variant(w, budget_s=4.0):
@@ -851,7 +867,7 @@ def main():
     ap.add_argument("--only", default=None,
                     choices=["causal_b16h8n3072d64", "noncausal_b8h8n4096d64", "causal_b1h16n65536d128",
                              "decode_b256h16d64", "backward_causal_b16h8n3072d64",
-                             "backward_nc_causal_b16h8n3072d64",
+                             "backward_nc_causal_b16h8n3072d64", "backward_causal_b1h16n65536d128",
                              "delta_b16h8n3072d64", "dpfp_b16h8n3072d64"],
                     help="time this one workload alone (--steps/--warmup; decode: --decode-steps) and print "
                          "its leg object; for profiler captures, not a bench line")

@@ -1053,23 +1053,25 @@ state_reduce_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_const
             di[D * M + r] = args.z_init ? args.z_init[(size_t)bh * D + r] : 0.f;
         }
         const bool ok = wait_bar_warp(done, 0, abort);
+        // S leaves through the stages (free once every MMA has completed) so
+        // that its stores are coalesced
+        float *stage = reinterpret_cast<float *>(smem);
+        static_assert(D * M * 4 <= C::NS * C::STAGE, "staging area");
         if (ok && swarp) {
             tc_fence_after();
 #pragma unroll 1
             for (int c0 = 0; c0 < M; c0 += 32) {
                 float v[32];
                 tmem_ld32f(tmem + lane_off + C::COL_S + c0, v);
-                if (r < D && dst_ok)
-#pragma unroll
-                    for (int j = 0; j < 32; j += 4)
-                        *reinterpret_cast<float4 *>(dst + r * M + c0 + j) =
-                            make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+                if (r < D) stage_row32_f32<M>(stage, r, c0, v);
             }
             uint32_t zv[16];
             tmem_ld16(tmem + lane_off + C::COL_Z, zv);
             tmem_wait_ld();
             if (r < D && dst_ok) dst[D * M + r] = __uint_as_float(zv[0]);
         }
+        epi_sync();
+        if (ok && dst_ok) store_staged_f32<D, M>(dst, stage, r, kGrp);
     } else {
         const int t = tid - 64 - kGrp;
         for (int it = 0; it < n; ++it) {

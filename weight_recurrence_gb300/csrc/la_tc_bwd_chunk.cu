@@ -36,53 +36,77 @@
 #include "tc_kernels.cuh"
 #include "tc_ptx.cuh"
 
+// Optional per-phase timestamps of the first 1024 CTAs of the query (0) and
+// key (1) kernels for performance work: compiled only with -DLA_TRACE (never
+// in the library build).  Slot 15 holds %globaltimer at the CTA's start.
+#ifdef LA_TRACE
+__device__ unsigned long long g_la_trace_chunk[2][1024][16];
+extern "C" int la_trace_read_chunk(unsigned long long *dst) {
+    return (int)cudaMemcpyFromSymbol(dst, g_la_trace_chunk, sizeof(g_la_trace_chunk));
+}
+#define CH_TRACE(pass, ev)                                                                    \
+    do {                                                                                      \
+        if (blockIdx.x < 1024 && threadIdx.x == 0) {                                          \
+            g_la_trace_chunk[pass][blockIdx.x][ev] = clock64();                               \
+            if ((ev) == 0) g_la_trace_chunk[pass][blockIdx.x][15] = globaltimer_ns();         \
+        }                                                                                     \
+    } while (0)
+#else
+#define CH_TRACE(pass, ev) ((void)0)
+#endif
+
 namespace la {
 namespace {
 
 using namespace tc;
 
 // ------------------------------------------------------------------ scans
-// Exclusive scan of per-chunk vectors of W floats, in place, over the chunks
-// of each head (reverse: from the last chunk down).  The running sum starts
-// from `init` ([BH][D*M] then [BH][D], the vector's two parts; null: zero)
-// and its final value goes to `total` (same layout; may be null).  Thread
-// (head, e) owns element e; the loads of eight chunks are issued before
-// their sums.
+// Exclusive scan of per-chunk vectors of W = D*M + D floats, in place, over
+// the chunks of each head (reverse: from the last chunk down).  The running
+// sum starts from `init` ([BH][D*M] then [BH][D], the vector's two parts;
+// null: zero) and its final value goes to `total` (same layout; may be null).
+// Thread (head, e4) owns elements 4 e4 .. 4 e4 + 3; the loads of sixteen
+// chunks are issued before their sums.
 __global__ void __launch_bounds__(256)
 chunk_scan_kernel(float *ws, int nch, int DM, int D, const float *init_s, const float *init_z, float *tot_s,
                   float *tot_z, int reverse)
 {
-    const long long W = (long long)DM + D;
-    const int e = blockIdx.y * 256 + threadIdx.x;
+    const long long W4 = ((long long)DM + D) / 4;   // float4 per vector (DM and D are multiples of 4)
+    const int e4 = blockIdx.y * 256 + threadIdx.x;
     const long long bh = blockIdx.x;
     pdl_wait_cta();
-    if (e >= W) return;
-    float run = 0.f;
+    if (e4 >= W4) return;
+    const int e = 4 * e4;   // elements e..e+3: all of S or all of z
+    float4 run = make_float4(0.f, 0.f, 0.f, 0.f);
     if (e < DM) {
-        if (init_s) run = init_s[bh * DM + e];
+        if (init_s) run = *reinterpret_cast<const float4 *>(init_s + bh * DM + e);
     } else if (init_z) {
-        run = init_z[bh * D + (e - DM)];
+        run = *reinterpret_cast<const float4 *>(init_z + bh * D + (e - DM));
     }
-    float *base = ws + bh * nch * W + e;
-    for (int c0 = 0; c0 < nch; c0 += 8) {
-        float x[8];
+    float4 *base = reinterpret_cast<float4 *>(ws) + bh * nch * W4 + e4;
+    constexpr int U = 16;
+    for (int c0 = 0; c0 < nch; c0 += U) {
+        float4 x[U];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int u = 0; u < U; ++u) {
             const int c = reverse ? nch - 1 - (c0 + u) : c0 + u;
-            x[u] = (c0 + u < nch) ? __ldcg(base + (long long)c * W) : 0.f;
+            x[u] = (c0 + u < nch) ? __ldcg(base + (long long)c * W4) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int u = 0; u < U; ++u) {
             if (c0 + u >= nch) break;
             const int c = reverse ? nch - 1 - (c0 + u) : c0 + u;
-            base[(long long)c * W] = run;
-            run += x[u];
+            base[(long long)c * W4] = run;
+            run.x += x[u].x;
+            run.y += x[u].y;
+            run.z += x[u].z;
+            run.w += x[u].w;
         }
     }
     if (e < DM) {
-        if (tot_s) tot_s[bh * DM + e] = run;
+        if (tot_s) *reinterpret_cast<float4 *>(tot_s + bh * DM + e) = run;
     } else if (tot_z) {
-        tot_z[bh * D + (e - DM)] = run;
+        *reinterpret_cast<float4 *>(tot_z + bh * D + (e - DM)) = run;
     }
 }
 
@@ -177,6 +201,7 @@ chunk_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR), *mbar = full + 1;
     uint32_t *slot = reinterpret_cast<uint32_t *>(mbar + 1);
 
+    CH_TRACE(0, 0);
     bool ok = (smem_u32(smem) & 1023u) == 0;
     if (r == 0) {
         mbar_init(full, 1);
@@ -192,7 +217,9 @@ chunk_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
     tc_fence_after();
     const uint32_t tmem = *slot;
     const uint32_t trow = tmem + ((uint32_t)(32 * (r >> 5)) << 16);
+    CH_TRACE(0, 1);
     pdl_wait_cta();   // the scanned sums of the previous launch are complete
+    CH_TRACE(0, 2);
 
     if (r == 0 && ok) {
         mbar_arrive_expect_tx(full, 2 * C::TQ + 2 * C::TV);
@@ -208,9 +235,11 @@ chunk_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         }
     }
     // [S_c hi | z_c | S_c lo]
-    sum_partials_to_tile<D, M>(args.ws_s + ((size_t)bh * args.nch + c) * (D * M + D), 1, snap, r);
+    load_sum_tile<D, M>(args.ws_s + ((size_t)bh * args.nch + c) * (D * M + D), snap, r);
+    CH_TRACE(0, 3);
     const bool landed = !ok || mbar_wait_bounded(full, 0, now_ns() + kWaitNs, nullptr);
     ok = __syncthreads_and(ok && landed) != 0;
+    CH_TRACE(0, 4);
     uint32_t phase = 0;
     bool pending = false;   // MMAs committed but not waited for (error path)
     constexpr uint32_t ID_P = idesc_bf16(128, 128, 0, 0);      // K-major A and B
@@ -236,6 +265,7 @@ chunk_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         ok = operands_ready(true);
         sq = row_sum<D>(tq, r);
     }
+    CH_TRACE(0, 5);
     // ---- phi(Q) psi(K)^T
     if (ok) {
         if (r == 0)
@@ -247,6 +277,7 @@ chunk_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         ok = mma_wait_all();
         pending = !ok;
     }
+    CH_TRACE(0, 6);
     // ---- A = P = phi(Q) psi(K)^T + sq masked to j <= r, as bf16 hi and lo
     // parts (num feeds e, which enters every entry of A2'); its row sum
     float rs = 0.f;
@@ -255,6 +286,7 @@ chunk_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
                                      [&](int) { return sq; });
         ok = operands_ready(true);
     }
+    CH_TRACE(0, 7);
     // ---- [num | den] = phi(Q) [S_hi | z] + A_hi V + A_lo V + phi(Q) [S_lo | -]
     // (the first product covers all M + 16 columns, so it starts the sum)
     if (ok) {
@@ -280,6 +312,7 @@ chunk_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         ok = mma_wait_all();
         pending = !ok;
     }
+    CH_TRACE(0, 8);
     // ---- g = dO / den as bf16 (over dO), e = -(g . num) / den; g, e kept for the key pass
     float e = 0.f;
     if (ok) {
@@ -315,6 +348,7 @@ chunk_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         }
         ok = operands_ready(true);
     }
+    CH_TRACE(0, 9);
     // ---- A2 = g V^T;  dphi(Q) = [g | e | g] [S_hi | z | S_lo]^T;  [dR | dr] = phi(Q)^T [g | e]
     if (ok) {
         if (r == 0) {
@@ -344,14 +378,32 @@ chunk_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         ok = mma_wait_all();
         pending = !ok;
     }
+    CH_TRACE(0, 10);
     // ---- A2' = (A2 + e_r) masked to j <= r, as bf16; its row sum (the
-    // product with the 1 of phi(K) = psi(K) + 1)
+    // product with the 1 of phi(K) = psi(K) + 1).  [dR_c | dr_c] is final:
+    // its rows are staged in the operand tile of the sums (last read by the
+    // products just completed) and leave with coalesced stores while the
+    // last product runs
     float asum = 0.f;
+    float *dst_r = args.ws_r + ((size_t)bh * args.nch + c) * (D * M + D);
+    float *stage = reinterpret_cast<float *>(snap);
+    static_assert(D * M * 4 <= XwTile<D, M>::BYTES, "staging area");
     if (ok) {
         asum = tmem_mask_to_bf16<false>(trow + T::Q_A2, trow + T::Q_A2B, 0u, [&](int j) { return j <= r; },
                                         [&](int) { return e; });
+        if (r < D) {
+            float y[32];
+#pragma unroll 1
+            for (int c0 = 0; c0 < M; c0 += 32) {
+                tmem_ld32f(trow + T::Q_R + c0, y);
+                stage_row32_f32<M>(stage, r, c0, y);
+            }
+            tmem_ld32f(trow + T::Q_R + M, y);
+            dst_r[D * M + r] = y[0] + y[2];   // the e_hi and e_lo columns
+        }
         ok = operands_ready(true);
     }
+    CH_TRACE(0, 11);
     // ---- dphi(Q) += A2' psi(K)
     if (ok) {
         if (r == 0) {
@@ -360,10 +412,12 @@ chunk_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
             for (int ks = 0; ks < kC / 16; ++ks)
                 mma_f16_ts(tmem + T::Q_DQ, tmem + T::Q_A2B + ks * 8, dk + mnmajor_step(ks), ID_DQ2, 1);
         }
+        store_staged_f32<D, M>(dst_r, stage, r, kNT);
         pending = true;
         ok = mma_wait_all();
         pending = !ok;
     }
+    CH_TRACE(0, 12);
     // ---- dQ = (dphi(Q) + asum) min(phi(Q), 1); [dR_c | dr_c] to the workspace
     if (ok) {
         float x[D];
@@ -376,19 +430,8 @@ chunk_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
             for (int j = 0; j < 32; ++j) x[c0 + j] = (d32[j] + asum) * fminf(f[j], 1.f);
         }
         if (r < valid) store_row_bf16<D>(args.g0 + ((size_t)bh * args.N + t0 + r) * D, x);
-        if (r < D) {
-            float *dst = args.ws_r + ((size_t)bh * args.nch + c) * (D * M + D);
-            float y[32];
-            for (int c0 = 0; c0 < M; c0 += 32) {
-                tmem_ld32f(trow + T::Q_R + c0, y);
-#pragma unroll
-                for (int j = 0; j < 32; j += 4)
-                    *reinterpret_cast<float4 *>(dst + r * M + c0 + j) = make_float4(y[j], y[j + 1], y[j + 2], y[j + 3]);
-            }
-            tmem_ld32f(trow + T::Q_R + M, y);
-            dst[D * M + r] = y[0] + y[2];   // the e_hi and e_lo columns
-        }
     }
+    CH_TRACE(0, 13);
     if (!ok && r == 0) {
         record_error(args.err, kErrTimeout);
         mbar_wait_bounded(full, 0, now_ns() + kWaitNs, nullptr);
@@ -398,6 +441,7 @@ chunk_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
     __syncthreads();
     tc_fence_after();
     if (r < 32) tmem_dealloc(tmem, T::COLS);
+    CH_TRACE(0, 14);
 }
 
 // --------------------------------------------------------------- key pass
@@ -431,6 +475,7 @@ chunk_bwd_key_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR), *mbar = full + 1;
     uint32_t *slot = reinterpret_cast<uint32_t *>(mbar + 1);
 
+    CH_TRACE(1, 0);
     bool ok = (smem_u32(smem) & 1023u) == 0;
     if (r == 0) {
         mbar_init(full, 1);
@@ -449,7 +494,9 @@ chunk_bwd_key_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     tc_fence_after();
     const uint32_t tmem = *slot;
     const uint32_t trow = tmem + ((uint32_t)(32 * (r >> 5)) << 16);
+    CH_TRACE(1, 1);
     pdl_wait_cta();   // the query pass and the reverse scan are complete
+    CH_TRACE(1, 2);
 
     if (r == 0 && ok) {
         mbar_arrive_expect_tx(full, 2 * C::TQ + 2 * C::TV);
@@ -466,9 +513,11 @@ chunk_bwd_key_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     }
     es[r] = r < valid ? __ldcg(args.ws_e + (size_t)bh * args.N + t0 + r) : 0.f;
     // [R_c hi | r_c | R_c lo]
-    sum_partials_to_tile<D, M>(args.ws_r + ((size_t)bh * args.nch + c) * (D * M + D), 1, snap, r);
+    load_sum_tile<D, M>(args.ws_r + ((size_t)bh * args.nch + c) * (D * M + D), snap, r);
+    CH_TRACE(1, 3);
     const bool landed = !ok || mbar_wait_bounded(full, 0, now_ns() + kWaitNs, nullptr);
     ok = __syncthreads_and(ok && landed) != 0;
+    CH_TRACE(1, 4);
     uint32_t phase = 0;
     bool pending = false;
     constexpr uint32_t ID_P = idesc_bf16(128, 128, 0, 0);      // K-major A and B
@@ -491,6 +540,7 @@ chunk_bwd_key_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         ok = operands_ready(true);
         sk = row_sum<D>(tk, r);
     }
+    CH_TRACE(1, 5);
     // ---- phi(K) psi(Q)^T;  A^T (raw) = V g^T
     if (ok) {
         if (r == 0) {
@@ -507,6 +557,7 @@ chunk_bwd_key_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         ok = mma_wait_all();
         pending = !ok;
     }
+    CH_TRACE(1, 6);
     // ---- P^T = phi(K) psi(Q)^T + sk and A^T + e_i, masked to r <= i < valid
     // (key r, query i), as bf16 in place; the row sum of A^T (its product
     // with the 1 of phi(Q) = psi(Q) + 1)
@@ -517,6 +568,7 @@ chunk_bwd_key_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         asum = tmem_mask_to_bf16<false>(trow + T::K_AT, trow + T::K_AT, 0u, keep, [&](int i) { return es[i]; });
         ok = operands_ready(true);
     }
+    CH_TRACE(1, 7);
     // ---- dV = P^T g + phi(K) (R_hi + R_lo);  dphi(K) = A^T psi(Q) + [V | 1 | V] [R_hi | r | R_lo]^T
     if (ok) {
         if (r == 0) {
@@ -551,6 +603,7 @@ chunk_bwd_key_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         ok = mma_wait_all();
         pending = !ok;
     }
+    CH_TRACE(1, 8);
     // ---- dK = (dphi(K) + asum) min(phi(K), 1), dV
     if (ok) {
         float x[D > M ? D : M];
@@ -567,6 +620,7 @@ chunk_bwd_key_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         for (int c0 = 0; c0 < M; c0 += 32) tmem_ld32f(trow + T::K_DV + c0, *reinterpret_cast<float(*)[32]>(x + c0));
         if (r < valid) store_row_bf16<M>(args.g1 + ((size_t)bh * args.N + t0 + r) * M, x);
     }
+    CH_TRACE(1, 9);
     if (!ok && r == 0) {
         record_error(args.err, kErrTimeout);
         mbar_wait_bounded(full, 0, now_ns() + kWaitNs, nullptr);
@@ -576,6 +630,7 @@ chunk_bwd_key_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     __syncthreads();
     tc_fence_after();
     if (r < 32) tmem_dealloc(tmem, T::COLS);
+    CH_TRACE(1, 10);
 }
 
 struct ChunkWs {
@@ -613,7 +668,7 @@ cudaError_t launch_chunk_bwd(const BwdProblem &p, const DeviceInfo &dev) {
     cudaError_t e = tc_key_sums(p.k, p.v, p.BH, p.N, D, M, nch, 1, ws_s, w.s_floats * sizeof(float), p.stream, dev);
     if (e != cudaSuccess) return e;
     const int W = D * M + D;
-    const dim3 sgrid((unsigned)p.BH, (unsigned)((W + 255) / 256));
+    const dim3 sgrid((unsigned)p.BH, (unsigned)((W / 4 + 255) / 256));
     e = launch_pdl(chunk_scan_kernel, sgrid, dim3(256), 0, p.stream, 0u, ws_s, nch, D * M, D, p.S0, p.z0,
                    (float *)nullptr, (float *)nullptr, 0);
     count_launches(1);

@@ -293,6 +293,31 @@ __device__ __forceinline__ void feature_row(uint8_t *tile, int t, int zero_from,
     }
 }
 
+// A D x M fp32 block held one row per thread leaves through shared memory so
+// that its global stores are coalesced: stage_row32_f32 puts columns
+// [c0, c0+32) of row r into the staging area (16-byte units, unit c4 of row
+// r at c4 ^ (r mod M/4): a warp's rows land in distinct banks), and, after a
+// barrier over the writing threads, store_staged_f32 copies the block to the
+// contiguous D*M floats at dst with 16-byte stores by threads t of nthr.
+template <int M>
+__device__ __forceinline__ void stage_row32_f32(float *stage, int r, int c0, const float *v) {
+    constexpr int R4 = M / 4;
+    float4 *row = reinterpret_cast<float4 *>(stage) + r * R4;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+        row[(c0 / 4 + j) ^ (r % R4)] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+}
+template <int D, int M>
+__device__ __forceinline__ void store_staged_f32(float *dst, const float *stage, int t, int nthr) {
+    constexpr int R4 = M / 4;
+    const float4 *s4 = reinterpret_cast<const float4 *>(stage);
+    float4 *d4 = reinterpret_cast<float4 *>(dst);
+    for (int f = t; f < D * R4; f += nthr) {
+        const int row = f / R4, c4 = f % R4;
+        d4[f] = s4[row * R4 + (c4 ^ (row % R4))];
+    }
+}
+
 // Writes columns [c0, c0+32) of row r of a D x M fp32 state as bf16 into the
 // MN-major swizzled snapshot [D rows x M cols] (sub-tiles of 64 columns).
 template <int D>
