@@ -117,6 +117,7 @@ struct ChunkBwdArgs {
     float *ws_e;             // [BH, N]: e
     __nv_bfloat16 *g0, *g1;  // query pass: dQ; key pass: dK, dV
     int N, nch;
+    int total;               // BH * nch chunks, walked by the grid's CTAs in strides of gridDim.x
     int *err;
 };
 
@@ -194,8 +195,6 @@ chunk_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
     using T = ChunkCols<D, M>;
     extern __shared__ __align__(1024) uint8_t smem[];
     const int r = threadIdx.x;
-    const int bh = blockIdx.x / args.nch, c = blockIdx.x % args.nch;
-    const int t0 = c * kC, valid = min(kC, args.N - t0);
     uint8_t *tq = smem, *tk = smem + C::OFF_K, *tv = smem + C::OFF_V, *tg = smem + C::OFF_G;
     uint8_t *snap = smem + C::OFF_SNAP, *eat = smem + C::OFF_E;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR), *mbar = full + 1;
@@ -219,9 +218,32 @@ chunk_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
     const uint32_t trow = tmem + ((uint32_t)(32 * (r >> 5)) << 16);
     CH_TRACE(0, 1);
     pdl_wait_cta();   // the scanned sums of the previous launch are complete
-    CH_TRACE(0, 2);
 
-    if (r == 0 && ok) {
+    uint32_t phase = 0, fphase = 0;
+    bool pending = false;   // MMAs committed but not complete (error path)
+    bool loading = false;   // tiles requested but not landed (error path)
+    constexpr uint32_t ID_P = idesc_bf16(128, 128, 0, 0);      // K-major A and B
+    constexpr uint32_t ID_NV = idesc_bf16(128, M, 0, 1);       // A (TMEM) x V MN-major
+    constexpr uint32_t ID_NS = idesc_bf16(128, M + 16, 0, 1);  // phi(Q) x [S_hi | z] MN-major
+    constexpr uint32_t ID_DQ = idesc_bf16(128, D, 0, 0);       // [g | e | g] x [S_hi | z | S_lo]^T, K-major
+    constexpr uint32_t ID_DQ2 = idesc_bf16(128, D, 0, 1);      // A2' (TMEM) x phi(K) MN-major
+    constexpr uint32_t ID_R = idesc_bf16(128, M, 1, 1);        // phi(Q)^T x g, MN-major
+    constexpr uint32_t ID_RZ = idesc_bf16(128, 16, 1, 1);
+    auto mma_wait_all = [&]() {
+        if (r == 0) mma_commit(mbar);
+        const bool got = mbar_wait_bounded(mbar, phase, now_ns() + kWaitNs, nullptr);
+        if (got) phase ^= 1u;
+        tc_fence_after();
+        return __syncthreads_and(got ? 1 : 0) != 0;
+    };
+    // Chunks u = blockIdx.x, + gridDim.x, ...: once one's tiles have landed,
+    // the next one's tiles and sums are prefetched into L2 while it computes,
+    // so that HBM is not idle between the CTAs' load phases
+    for (int u = blockIdx.x; ok && u < args.total; u += gridDim.x) {
+    const int bh = u / args.nch, c = u % args.nch;
+    const int t0 = c * kC, valid = min(kC, args.N - t0);
+    CH_TRACE(0, 2);
+    if (r == 0) {
         mbar_arrive_expect_tx(full, 2 * C::TQ + 2 * C::TV);
 #pragma unroll
         for (int j = 0; j < D / 64; ++j) {
@@ -234,28 +256,37 @@ chunk_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
             tma_load_3d(tg + j * kC * 128, &tm_g, full, j * 64, t0, bh);
         }
     }
+    loading = true;
     // [S_c hi | z_c | S_c lo]
-    load_sum_tile<D, M>(args.ws_s + ((size_t)bh * args.nch + c) * (D * M + D), snap, r);
+    load_sum_tile<D, M>(args.ws_s + (size_t)u * (D * M + D), snap, r);
     CH_TRACE(0, 3);
-    const bool landed = !ok || mbar_wait_bounded(full, 0, now_ns() + kWaitNs, nullptr);
-    ok = __syncthreads_and(ok && landed) != 0;
+    {
+        const bool landed = mbar_wait_bounded(full, fphase, now_ns() + kWaitNs, nullptr);
+        if (landed) {
+            fphase ^= 1u;
+            loading = false;
+        }
+        ok = __syncthreads_and(landed) != 0;
+    }
+    // the next chunk into L2 while this one computes
+    if (r == 0 && ok) {
+        const int un = u + gridDim.x;
+        if (un < args.total) {
+            const int bn = un / args.nch, tn = (un % args.nch) * kC;
+#pragma unroll
+            for (int j = 0; j < D / 64; ++j) {
+                tma_prefetch_3d(&tm_q, j * 64, tn, bn);
+                tma_prefetch_3d(&tm_k, j * 64, tn, bn);
+            }
+#pragma unroll
+            for (int j = 0; j < M / 64; ++j) {
+                tma_prefetch_3d(&tm_v, j * 64, tn, bn);
+                tma_prefetch_3d(&tm_g, j * 64, tn, bn);
+            }
+            bulk_prefetch_l2(args.ws_s + (size_t)un * (D * M + D), (D * M + D) * 4);
+        }
+    }
     CH_TRACE(0, 4);
-    uint32_t phase = 0;
-    bool pending = false;   // MMAs committed but not waited for (error path)
-    constexpr uint32_t ID_P = idesc_bf16(128, 128, 0, 0);      // K-major A and B
-    constexpr uint32_t ID_NV = idesc_bf16(128, M, 0, 1);       // A (TMEM) x V MN-major
-    constexpr uint32_t ID_NS = idesc_bf16(128, M + 16, 0, 1);  // phi(Q) x [S_hi | z] MN-major
-    constexpr uint32_t ID_DQ = idesc_bf16(128, D, 0, 0);       // [g | e | g] x [S_hi | z | S_lo]^T, K-major
-    constexpr uint32_t ID_DQ2 = idesc_bf16(128, D, 0, 1);      // A2' (TMEM) x phi(K) MN-major
-    constexpr uint32_t ID_R = idesc_bf16(128, M, 1, 1);        // phi(Q)^T x g, MN-major
-    constexpr uint32_t ID_RZ = idesc_bf16(128, 16, 1, 1);
-    auto mma_wait_all = [&]() {
-        if (r == 0) mma_commit(mbar);
-        const bool got = mbar_wait_bounded(mbar, phase, now_ns() + kWaitNs, nullptr);
-        phase ^= 1u;
-        tc_fence_after();
-        return __syncthreads_and(got ? 1 : 0) != 0;
-    };
     // phi(Q); psi(K) = phi(K) - 1 (the 1 enters as the row sums of phi(Q));
     // rows past the end become zeros
     float sq = 0.f;
@@ -385,7 +416,7 @@ chunk_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
     // products just completed) and leave with coalesced stores while the
     // last product runs
     float asum = 0.f;
-    float *dst_r = args.ws_r + ((size_t)bh * args.nch + c) * (D * M + D);
+    float *dst_r = args.ws_r + (size_t)u * (D * M + D);
     float *stage = reinterpret_cast<float *>(snap);
     static_assert(D * M * 4 <= XwTile<D, M>::BYTES, "staging area");
     if (ok) {
@@ -431,10 +462,16 @@ chunk_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         }
         if (r < valid) store_row_bf16<D>(args.g0 + ((size_t)bh * args.N + t0 + r) * D, x);
     }
+    // the chunk's tiles, tile of sums and TMEM are free for the next one
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    }
     CH_TRACE(0, 13);
     if (!ok && r == 0) {
         record_error(args.err, kErrTimeout);
-        mbar_wait_bounded(full, 0, now_ns() + kWaitNs, nullptr);
+        if (loading) mbar_wait_bounded(full, fphase, now_ns() + kWaitNs, nullptr);
         if (pending) mbar_wait_bounded(mbar, phase, now_ns() + kWaitNs, nullptr);
     }
     tc_fence_before();
@@ -467,8 +504,6 @@ chunk_bwd_key_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     using T = ChunkCols<D, M>;
     extern __shared__ __align__(1024) uint8_t smem[];
     const int r = threadIdx.x;
-    const int bh = blockIdx.x / args.nch, c = blockIdx.x % args.nch;
-    const int t0 = c * kC, valid = min(kC, args.N - t0);
     uint8_t *tq = smem, *tk = smem + C::OFF_K, *tv = smem + C::OFF_V, *tg = smem + C::OFF_G;
     uint8_t *snap = smem + C::OFF_SNAP, *ones = smem + C::OFF_ONES;
     float *es = reinterpret_cast<float *>(smem + C::OFF_E);
@@ -496,9 +531,27 @@ chunk_bwd_key_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     const uint32_t trow = tmem + ((uint32_t)(32 * (r >> 5)) << 16);
     CH_TRACE(1, 1);
     pdl_wait_cta();   // the query pass and the reverse scan are complete
-    CH_TRACE(1, 2);
 
-    if (r == 0 && ok) {
+    uint32_t phase = 0, fphase = 0;
+    bool pending = false, loading = false;
+    constexpr uint32_t ID_P = idesc_bf16(128, 128, 0, 0);      // K-major A and B
+    constexpr uint32_t ID_DV = idesc_bf16(128, M, 0, 1);       // P^T (TMEM) or phi(K) x MN-major
+    constexpr uint32_t ID_DK = idesc_bf16(128, D, 0, 0);       // [V | 1 | V] x [R_hi | r | R_lo]^T, K-major
+    constexpr uint32_t ID_DK2 = idesc_bf16(128, D, 0, 1);      // A^T (TMEM) x phi(Q) MN-major
+    auto mma_wait_all = [&]() {
+        if (r == 0) mma_commit(mbar);
+        const bool got = mbar_wait_bounded(mbar, phase, now_ns() + kWaitNs, nullptr);
+        if (got) phase ^= 1u;
+        tc_fence_after();
+        return __syncthreads_and(got ? 1 : 0) != 0;
+    };
+    // chunks in strides of gridDim.x, the next one prefetched into L2 (as in
+    // the query pass)
+    for (int u = blockIdx.x; ok && u < args.total; u += gridDim.x) {
+    const int bh = u / args.nch, c = u % args.nch;
+    const int t0 = c * kC, valid = min(kC, args.N - t0);
+    CH_TRACE(1, 2);
+    if (r == 0) {
         mbar_arrive_expect_tx(full, 2 * C::TQ + 2 * C::TV);
 #pragma unroll
         for (int j = 0; j < D / 64; ++j) {
@@ -511,26 +564,38 @@ chunk_bwd_key_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             tma_load_3d(tg + j * kC * 128, &tm_gw, full, j * 64, t0, bh);
         }
     }
+    loading = true;
     es[r] = r < valid ? __ldcg(args.ws_e + (size_t)bh * args.N + t0 + r) : 0.f;
     // [R_c hi | r_c | R_c lo]
-    load_sum_tile<D, M>(args.ws_r + ((size_t)bh * args.nch + c) * (D * M + D), snap, r);
+    load_sum_tile<D, M>(args.ws_r + (size_t)u * (D * M + D), snap, r);
     CH_TRACE(1, 3);
-    const bool landed = !ok || mbar_wait_bounded(full, 0, now_ns() + kWaitNs, nullptr);
-    ok = __syncthreads_and(ok && landed) != 0;
+    {
+        const bool landed = mbar_wait_bounded(full, fphase, now_ns() + kWaitNs, nullptr);
+        if (landed) {
+            fphase ^= 1u;
+            loading = false;
+        }
+        ok = __syncthreads_and(landed) != 0;
+    }
+    // the next chunk into L2 while this one computes
+    if (r == 0 && ok) {
+        const int un = u + gridDim.x;
+        if (un < args.total) {
+            const int bn = un / args.nch, tn = (un % args.nch) * kC;
+#pragma unroll
+            for (int j = 0; j < D / 64; ++j) {
+                tma_prefetch_3d(&tm_q, j * 64, tn, bn);
+                tma_prefetch_3d(&tm_k, j * 64, tn, bn);
+            }
+#pragma unroll
+            for (int j = 0; j < M / 64; ++j) {
+                tma_prefetch_3d(&tm_v, j * 64, tn, bn);
+                tma_prefetch_3d(&tm_gw, j * 64, tn, bn);
+            }
+            bulk_prefetch_l2(args.ws_r + (size_t)un * (D * M + D), (D * M + D) * 4);
+        }
+    }
     CH_TRACE(1, 4);
-    uint32_t phase = 0;
-    bool pending = false;
-    constexpr uint32_t ID_P = idesc_bf16(128, 128, 0, 0);      // K-major A and B
-    constexpr uint32_t ID_DV = idesc_bf16(128, M, 0, 1);       // P^T (TMEM) or phi(K) x MN-major
-    constexpr uint32_t ID_DK = idesc_bf16(128, D, 0, 0);       // [V | 1 | V] x [R_hi | r | R_lo]^T, K-major
-    constexpr uint32_t ID_DK2 = idesc_bf16(128, D, 0, 1);      // A^T (TMEM) x phi(Q) MN-major
-    auto mma_wait_all = [&]() {
-        if (r == 0) mma_commit(mbar);
-        const bool got = mbar_wait_bounded(mbar, phase, now_ns() + kWaitNs, nullptr);
-        phase ^= 1u;
-        tc_fence_after();
-        return __syncthreads_and(got ? 1 : 0) != 0;
-    };
     // psi(Q) = phi(Q) - 1 (the 1 enters as the row sums of phi(K)); phi(K);
     // rows past the end become zeros
     float sk = 0.f;
@@ -620,10 +685,16 @@ chunk_bwd_key_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         for (int c0 = 0; c0 < M; c0 += 32) tmem_ld32f(trow + T::K_DV + c0, *reinterpret_cast<float(*)[32]>(x + c0));
         if (r < valid) store_row_bf16<M>(args.g1 + ((size_t)bh * args.N + t0 + r) * M, x);
     }
+    // the chunk's tiles, tile of sums, e values and TMEM are free for the next one
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    }
     CH_TRACE(1, 9);
     if (!ok && r == 0) {
         record_error(args.err, kErrTimeout);
-        mbar_wait_bounded(full, 0, now_ns() + kWaitNs, nullptr);
+        if (loading) mbar_wait_bounded(full, fphase, now_ns() + kWaitNs, nullptr);
         if (pending) mbar_wait_bounded(mbar, phase, now_ns() + kWaitNs, nullptr);
     }
     tc_fence_before();
@@ -673,8 +744,12 @@ cudaError_t launch_chunk_bwd(const BwdProblem &p, const DeviceInfo &dev) {
                    (float *)nullptr, (float *)nullptr, 0);
     count_launches(1);
     if (e != cudaSuccess) return e;
-    const dim3 grid((unsigned)(p.BH * nch)), block(kNT);
-    ChunkBwdArgs a{ws_s, ws_r, ws_g, ws_e, (__nv_bfloat16 *)p.dq, nullptr, p.N, nch, dev.err_word};
+    // one CTA per SM (the shared memory and the 512 TMEM columns each CTA
+    // holds allow no more), each walking chunks in strides of the grid
+    const long long total = p.BH * nch;
+    if (total > INT32_MAX) return cudaErrorInvalidValue;
+    const dim3 grid((unsigned)std::min<long long>(total, std::max(1, dev.sm_count))), block(kNT);
+    ChunkBwdArgs a{ws_s, ws_r, ws_g, ws_e, (__nv_bfloat16 *)p.dq, nullptr, p.N, nch, (int)total, dev.err_word};
     if ((e = set_smem(chunk_bwd_query_kernel<D, M>, CQCfg<D, M>::SMEM)) != cudaSuccess) return e;
     e = launch_pdl(chunk_bwd_query_kernel<D, M>, grid, block, CQCfg<D, M>::SMEM, p.stream, 0u, tq, tk, tv, tg, a);
     count_launches(1);
