@@ -138,40 +138,39 @@ struct ChunkCols {
     static_assert(Q_R + M + 16 <= COLS && K_DK + D <= COLS, "TMEM budget");
 };
 
-// Row r of a [128 x 128] fp32 TMEM block at `src`: x_j = value + add(j) where
-// keep(j), else 0, as bf16 into the 64 columns at `dst_hi` and, if `lo`, the
-// rounding remainders x_j - bf16(x_j) as bf16 into the 64 columns at
-// `dst_lo`.  Returns the fp32 sum of the x_j (lo) or of their bf16 roundings
-// (no lo): the row sum of what the products will see.  A destination may be
-// `src`: each 32-column piece is read before the 16 packed columns it yields
-// are written, at or below it.
-template <bool LO, typename Keep, typename Add>
-__device__ __forceinline__ float tmem_mask_to_bf16(uint32_t src, uint32_t dst_hi, uint32_t dst_lo, Keep keep, Add add) {
+// Row r of the fp32 TMEM columns [c_begin, c_end) of a 128-column block at
+// `src`: x_j = value + add(j) where keep(j), else 0, as bf16 into the packed
+// columns at dst + j / 2.  Returns the fp32 sum of the x_j's bf16 roundings:
+// the row sum of what the products will see.  dst may be src: each
+// 32-column piece is read before the 16 packed columns it yields are
+// written, at or below it, as long as no other thread writes this range.
+template <typename Keep, typename Add>
+__device__ __forceinline__ float tmem_mask_to_bf16(uint32_t src, uint32_t dst, int c_begin, int c_end, Keep keep,
+                                                   Add add) {
     float sum = 0.f;
 #pragma unroll 1
-    for (int c0 = 0; c0 < 128; c0 += 32) {
+    for (int c0 = c_begin; c0 < c_end; c0 += 32) {
         float x[32];
         tmem_ld32f(src + c0, x);
-        uint32_t w[16], l[16];
+        uint32_t w[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
             const int c = c0 + 2 * j;
             const float a = keep(c) ? x[2 * j] + add(c) : 0.f;
             const float b = keep(c + 1) ? x[2 * j + 1] + add(c + 1) : 0.f;
             w[j] = pack_bf16x2(a, b);
-            if (LO) {
-                l[j] = pack_bf16x2(a - bf16lo(w[j]), b - bf16hi(w[j]));
-                sum += a + b;
-            } else {
-                sum += bf16lo(w[j]) + bf16hi(w[j]);
-            }
+            sum += bf16lo(w[j]) + bf16hi(w[j]);
         }
-        tmem_st16(dst_hi + c0 / 2, w);
-        if (LO) tmem_st16(dst_lo + c0 / 2, l);
+        tmem_st16(dst + c0 / 2, w);
         tmem_wait_st();
     }
     return sum;
 }
+
+// Both passes run two warpgroups: thread t handles row r = t mod 128 (TMEM
+// lane r) and half h = t / 128 of the columns of every CUDA-core phase (or,
+// where two operands are formed at once, one of them).
+constexpr int kCT = 256;
 
 // ------------------------------------------------------------- query pass
 template <int D, int M>
@@ -180,34 +179,37 @@ struct CQCfg {
     static constexpr int OFF_K = TQ, OFF_V = 2 * TQ, OFF_G = 2 * TQ + TV;
     static constexpr int OFF_SNAP = 2 * TQ + 2 * TV;                 // [S_hi | z | S_lo]
     static constexpr int OFF_E = OFF_SNAP + XwTile<D, M>::BYTES;     // (e_hi, e_hi, e_lo, e_lo) atom
-    static constexpr int OFF_BAR = OFF_E + kC * 128;
+    static constexpr int OFF_X = OFF_E + kC * 128;                   // fp32 [2][2][128] row-sum halves
+    static constexpr int OFF_BAR = OFF_X + 2 * 2 * kC * 4;
     static constexpr int SMEM = OFF_BAR + 64;
     static_assert(SMEM <= (int)kSmemMax, "shared memory budget");
 };
 
 template <int D, int M>
-__global__ void __launch_bounds__(kNT)
+__global__ void __launch_bounds__(kCT, 1)
 chunk_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
                        const ChunkBwdArgs args)
 {
     using C = CQCfg<D, M>;
     using T = ChunkCols<D, M>;
+    constexpr int MH = M / 2, DH = D / 2;
     extern __shared__ __align__(1024) uint8_t smem[];
-    const int r = threadIdx.x;
+    const int t = threadIdx.x, r = t & (kC - 1), h = t >> 7;
     uint8_t *tq = smem, *tk = smem + C::OFF_K, *tv = smem + C::OFF_V, *tg = smem + C::OFF_G;
     uint8_t *snap = smem + C::OFF_SNAP, *eat = smem + C::OFF_E;
+    float *xa = reinterpret_cast<float *>(smem + C::OFF_X), *xb = xa + 2 * kC;   // [half][row] each
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + C::OFF_BAR), *mbar = full + 1;
     uint32_t *slot = reinterpret_cast<uint32_t *>(mbar + 1);
 
     CH_TRACE(0, 0);
     bool ok = (smem_u32(smem) & 1023u) == 0;
-    if (r == 0) {
+    if (t == 0) {
         mbar_init(full, 1);
         mbar_init(mbar, 1);
         fence_mbar_init();
     }
-    if (r < 32) {
+    if (t < 32) {
         tmem_alloc(slot, T::COLS);
         tmem_relinquish();
     }
@@ -226,11 +228,11 @@ chunk_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
     constexpr uint32_t ID_NV = idesc_bf16(128, M, 0, 1);       // A (TMEM) x V MN-major
     constexpr uint32_t ID_NS = idesc_bf16(128, M + 16, 0, 1);  // phi(Q) x [S_hi | z] MN-major
     constexpr uint32_t ID_DQ = idesc_bf16(128, D, 0, 0);       // [g | e | g] x [S_hi | z | S_lo]^T, K-major
-    constexpr uint32_t ID_DQ2 = idesc_bf16(128, D, 0, 1);      // A2' (TMEM) x phi(K) MN-major
+    constexpr uint32_t ID_DQ2 = idesc_bf16(128, D, 0, 1);      // A2' (TMEM) x psi(K) MN-major
     constexpr uint32_t ID_R = idesc_bf16(128, M, 1, 1);        // phi(Q)^T x g, MN-major
     constexpr uint32_t ID_RZ = idesc_bf16(128, 16, 1, 1);
     auto mma_wait_all = [&]() {
-        if (r == 0) mma_commit(mbar);
+        if (t == 0) mma_commit(mbar);
         const bool got = mbar_wait_bounded(mbar, phase, now_ns() + kWaitNs, nullptr);
         if (got) phase ^= 1u;
         tc_fence_after();
@@ -243,7 +245,7 @@ chunk_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
     const int bh = u / args.nch, c = u % args.nch;
     const int t0 = c * kC, valid = min(kC, args.N - t0);
     CH_TRACE(0, 2);
-    if (r == 0) {
+    if (t == 0) {
         mbar_arrive_expect_tx(full, 2 * C::TQ + 2 * C::TV);
 #pragma unroll
         for (int j = 0; j < D / 64; ++j) {
@@ -258,7 +260,7 @@ chunk_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
     }
     loading = true;
     // [S_c hi | z_c | S_c lo]
-    load_sum_tile<D, M>(args.ws_s + (size_t)u * (D * M + D), snap, r);
+    load_sum_tile<D, M, kCT>(args.ws_s + (size_t)u * (D * M + D), snap, t);
     CH_TRACE(0, 3);
     {
         const bool landed = mbar_wait_bounded(full, fphase, now_ns() + kWaitNs, nullptr);
@@ -269,7 +271,7 @@ chunk_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         ok = __syncthreads_and(landed) != 0;
     }
     // the next chunk into L2 while this one computes
-    if (r == 0 && ok) {
+    if (t == 0 && ok) {
         const int un = u + gridDim.x;
         if (un < args.total) {
             const int bn = un / args.nch, tn = (un % args.nch) * kC;
@@ -287,19 +289,19 @@ chunk_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         }
     }
     CH_TRACE(0, 4);
-    // phi(Q); psi(K) = phi(K) - 1 (the 1 enters as the row sums of phi(Q));
-    // rows past the end become zeros
+    // phi(Q) (half 0) and psi(K) = phi(K) - 1 (half 1; the 1 enters as the
+    // row sums of phi(Q)); rows past the end become zeros
     float sq = 0.f;
     if (ok) {
-        phi_tile<D>(tq, r, valid);
-        psi_tile<D>(tk, r, valid);
+        if (h == 0) phi_tile<D>(tq, r, valid);
+        else psi_tile<D>(tk, r, valid);
         ok = operands_ready(true);
         sq = row_sum<D>(tq, r);
     }
     CH_TRACE(0, 5);
     // ---- phi(Q) psi(K)^T
     if (ok) {
-        if (r == 0)
+        if (t == 0)
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks)
                 mma_f16_ss(tmem + T::Q_P, kmajor_base(smem_u32(tq)) + kmajor_step(ks),
@@ -310,18 +312,40 @@ chunk_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
     }
     CH_TRACE(0, 6);
     // ---- A = P = phi(Q) psi(K)^T + sq masked to j <= r, as bf16 hi and lo
-    // parts (num feeds e, which enters every entry of A2'); its row sum
-    float rs = 0.f;
+    // parts (num feeds e, which enters every entry of A2'); its row sum.  Each
+    // half reads its 64 columns of P before either writes (A_lo replaces P's
+    // first 64 columns)
     if (ok) {
-        rs = tmem_mask_to_bf16<true>(trow + T::Q_P, trow + T::Q_AH, trow + T::Q_AL, [&](int j) { return j <= r; },
-                                     [&](int) { return sq; });
+        float x[64];
+        tmem_ld32f(trow + T::Q_P + 64 * h, *reinterpret_cast<float(*)[32]>(x));
+        tmem_ld32f(trow + T::Q_P + 64 * h + 32, *reinterpret_cast<float(*)[32]>(x + 32));
+        tc_fence_before();
+        __syncthreads();
+        tc_fence_after();
+        float rsp = 0.f;
+#pragma unroll
+        for (int p = 0; p < 2; ++p) {
+            uint32_t w[16], l[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const int cc = 64 * h + 32 * p + 2 * j;
+                const float a = cc <= r ? x[32 * p + 2 * j] + sq : 0.f;
+                const float b = cc + 1 <= r ? x[32 * p + 2 * j + 1] + sq : 0.f;
+                w[j] = pack_bf16x2(a, b);
+                l[j] = pack_bf16x2(a - bf16lo(w[j]), b - bf16hi(w[j]));
+                rsp += a + b;
+            }
+            tmem_st16(trow + T::Q_AH + 32 * h + 16 * p, w);
+            tmem_st16(trow + T::Q_AL + 32 * h + 16 * p, l);
+        }
+        xa[h * kC + r] = rsp;
         ok = operands_ready(true);
     }
     CH_TRACE(0, 7);
     // ---- [num | den] = phi(Q) [S_hi | z] + A_hi V + A_lo V + phi(Q) [S_lo | -]
     // (the first product covers all M + 16 columns, so it starts the sum)
     if (ok) {
-        if (r == 0) {
+        if (t == 0) {
             const uint64_t dq = kmajor_base(smem_u32(tq));
             const uint64_t db = smem_desc(smem_u32(snap), D * 128, 1024);
             const uint64_t dl = smem_desc(smem_u32(snap + XwTile<D, M>::LO), D * 128, 1024);
@@ -344,45 +368,47 @@ chunk_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         pending = !ok;
     }
     CH_TRACE(0, 8);
-    // ---- g = dO / den as bf16 (over dO), e = -(g . num) / den; g, e kept for the key pass
+    // ---- g = dO / den as bf16 (over dO; columns of half h), e = -(g . num) / den;
+    // g and e kept for the key pass
     float e = 0.f;
     if (ok) {
         float dz[32];
         tmem_ld32f(trow + T::Q_NUM + M, dz);   // phi(Q) . z: the z_hi and z_lo columns
-        const float den = rs + dz[0] + dz[1];
+        const float den = xa[r] + xa[kC + r] + dz[0] + dz[1];
         const float inv = r < valid ? 1.f / den : 0.f;
-        float dot = 0.f;
-#pragma unroll 1
-        for (int c0 = 0; c0 < M; c0 += 32) {
+        float dot = 0.f, gh[MH];
+#pragma unroll
+        for (int c0 = 0; c0 < MH; c0 += 32) {
             float x[32], gv[32];
-            tmem_ld32f(trow + T::Q_NUM + c0, x);
-            load_row32(tg, r, c0, gv);
+            tmem_ld32f(trow + T::Q_NUM + MH * h + c0, x);
+            load_row32(tg, r, MH * h + c0, gv);
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
                 gv[j] = __bfloat162float(__float2bfloat16_rn(gv[j] * inv));
                 dot = fmaf(gv[j], x[j], dot);
+                gh[c0 + j] = gv[j];
             }
-            store_snap32<kC>(tg, r, c0, gv);
+            store_snap32<kC>(tg, r, MH * h + c0, gv);
         }
-        e = -dot * inv;
-        const float eh = __bfloat162float(__float2bfloat16_rn(e));
-        const uint32_t hh = pack_bf16x2(eh, eh), ll = pack_bf16x2(e - eh, e - eh);
+        if (r < valid) store_row_bf16<MH>(args.ws_g + ((size_t)bh * args.N + t0 + r) * M + MH * h, gh);
+        xb[h * kC + r] = dot;
+        __syncthreads();
+        e = -(xb[r] + xb[kC + r]) * inv;
+        if (h == 0) {
+            const float eh = __bfloat162float(__float2bfloat16_rn(e));
+            const uint32_t hh = pack_bf16x2(eh, eh), ll = pack_bf16x2(e - eh, e - eh);
 #pragma unroll
-        for (int cc = 0; cc < 64; cc += 8)
-            *reinterpret_cast<uint4 *>(eat + sw128_offset(r, cc)) = make_uint4(cc == 0 ? hh : 0u, cc == 0 ? ll : 0u, 0u, 0u);
-        if (r < valid) {
-            float gr[M];
-#pragma unroll
-            for (int c0 = 0; c0 < M; c0 += 32) load_row32(tg, r, c0, *reinterpret_cast<float(*)[32]>(gr + c0));
-            store_row_bf16<M>(args.ws_g + ((size_t)bh * args.N + t0 + r) * M, gr);
-            args.ws_e[(size_t)bh * args.N + t0 + r] = e;
+            for (int cc = 0; cc < 64; cc += 8)
+                *reinterpret_cast<uint4 *>(eat + sw128_offset(r, cc)) =
+                    make_uint4(cc == 0 ? hh : 0u, cc == 0 ? ll : 0u, 0u, 0u);
+            if (r < valid) args.ws_e[(size_t)bh * args.N + t0 + r] = e;
         }
         ok = operands_ready(true);
     }
     CH_TRACE(0, 9);
     // ---- A2 = g V^T;  dphi(Q) = [g | e | g] [S_hi | z | S_lo]^T;  [dR | dr] = phi(Q)^T [g | e]
     if (ok) {
-        if (r == 0) {
+        if (t == 0) {
             const uint64_t dg = kmajor_base(smem_u32(tg)), de = kmajor_base(smem_u32(eat));
 #pragma unroll
             for (int ks = 0; ks < M / 16; ++ks)
@@ -410,66 +436,69 @@ chunk_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
         pending = !ok;
     }
     CH_TRACE(0, 10);
-    // ---- A2' = (A2 + e_r) masked to j <= r, as bf16; its row sum (the
-    // product with the 1 of phi(K) = psi(K) + 1).  [dR_c | dr_c] is final:
-    // its rows are staged in the operand tile of the sums (last read by the
-    // products just completed) and leave with coalesced stores while the
-    // last product runs
-    float asum = 0.f;
+    // ---- A2' = (A2 + e_r) masked to j <= r, as bf16 (columns of half h); its
+    // row sum (the product with the 1 of phi(K) = psi(K) + 1).  [dR_c | dr_c]
+    // is final: its rows are staged in the operand tile of the sums (last read
+    // by the products just completed) and leave with coalesced stores while
+    // the last product runs
     float *dst_r = args.ws_r + (size_t)u * (D * M + D);
     float *stage = reinterpret_cast<float *>(snap);
     static_assert(D * M * 4 <= XwTile<D, M>::BYTES, "staging area");
     if (ok) {
-        asum = tmem_mask_to_bf16<false>(trow + T::Q_A2, trow + T::Q_A2B, 0u, [&](int j) { return j <= r; },
-                                        [&](int) { return e; });
+        xa[h * kC + r] = tmem_mask_to_bf16(trow + T::Q_A2, trow + T::Q_A2B, 64 * h, 64 * h + 64,
+                                           [&](int j) { return j <= r; }, [&](int) { return e; });
         if (r < D) {
             float y[32];
 #pragma unroll 1
-            for (int c0 = 0; c0 < M; c0 += 32) {
+            for (int c0 = MH * h; c0 < MH * h + MH; c0 += 32) {
                 tmem_ld32f(trow + T::Q_R + c0, y);
                 stage_row32_f32<M>(stage, r, c0, y);
             }
-            tmem_ld32f(trow + T::Q_R + M, y);
-            dst_r[D * M + r] = y[0] + y[2];   // the e_hi and e_lo columns
+            if (h == 0) {
+                tmem_ld32f(trow + T::Q_R + M, y);
+                dst_r[D * M + r] = y[0] + y[2];   // the e_hi and e_lo columns
+            }
         }
         ok = operands_ready(true);
     }
     CH_TRACE(0, 11);
     // ---- dphi(Q) += A2' psi(K)
     if (ok) {
-        if (r == 0) {
+        if (t == 0) {
             const uint64_t dk = smem_desc(smem_u32(tk), kC * 128, 1024);
 #pragma unroll
             for (int ks = 0; ks < kC / 16; ++ks)
                 mma_f16_ts(tmem + T::Q_DQ, tmem + T::Q_A2B + ks * 8, dk + mnmajor_step(ks), ID_DQ2, 1);
         }
-        store_staged_f32<D, M>(dst_r, stage, r, kNT);
+        store_staged_f32<D, M>(dst_r, stage, t, kCT);
         pending = true;
         ok = mma_wait_all();
         pending = !ok;
     }
     CH_TRACE(0, 12);
-    // ---- dQ = (dphi(Q) + asum) min(phi(Q), 1); [dR_c | dr_c] to the workspace
+    // ---- dQ = (dphi(Q) + asum) min(phi(Q), 1), columns of half h
     if (ok) {
-        float x[D];
+        const float asum = xa[r] + xa[kC + r];
+        float x[DH];
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
+        for (int c0 = 0; c0 < DH; c0 += 32) {
             float d32[32], f[32];
-            tmem_ld32f(trow + T::Q_DQ + c0, d32);
-            load_row32(tq, r, c0, f);
+            tmem_ld32f(trow + T::Q_DQ + DH * h + c0, d32);
+            load_row32(tq, r, DH * h + c0, f);
 #pragma unroll
             for (int j = 0; j < 32; ++j) x[c0 + j] = (d32[j] + asum) * fminf(f[j], 1.f);
         }
-        if (r < valid) store_row_bf16<D>(args.g0 + ((size_t)bh * args.N + t0 + r) * D, x);
+        if (r < valid) store_row_bf16<DH>(args.g0 + ((size_t)bh * args.N + t0 + r) * D + DH * h, x);
     }
-    // the chunk's tiles, tile of sums and TMEM are free for the next one
+    // the chunk's tiles, tile of sums, row-sum halves and TMEM are free for
+    // the next one
     fence_proxy_async();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     }
     CH_TRACE(0, 13);
-    if (!ok && r == 0) {
+    if (!ok && t == 0) {
         record_error(args.err, kErrTimeout);
         if (loading) mbar_wait_bounded(full, fphase, now_ns() + kWaitNs, nullptr);
         if (pending) mbar_wait_bounded(mbar, phase, now_ns() + kWaitNs, nullptr);
@@ -477,7 +506,7 @@ chunk_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_co
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (r < 32) tmem_dealloc(tmem, T::COLS);
+    if (t < 32) tmem_dealloc(tmem, T::COLS);
     CH_TRACE(0, 14);
 }
 
@@ -495,7 +524,7 @@ struct CKCfg {
 };
 
 template <int D, int M>
-__global__ void __launch_bounds__(kNT)
+__global__ void __launch_bounds__(kCT, 1)
 chunk_bwd_key_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_gw,
                      const ChunkBwdArgs args)
@@ -503,7 +532,7 @@ chunk_bwd_key_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     using C = CKCfg<D, M>;
     using T = ChunkCols<D, M>;
     extern __shared__ __align__(1024) uint8_t smem[];
-    const int r = threadIdx.x;
+    const int t = threadIdx.x, r = t & (kC - 1), h = t >> 7;
     uint8_t *tq = smem, *tk = smem + C::OFF_K, *tv = smem + C::OFF_V, *tg = smem + C::OFF_G;
     uint8_t *snap = smem + C::OFF_SNAP, *ones = smem + C::OFF_ONES;
     float *es = reinterpret_cast<float *>(smem + C::OFF_E);
@@ -512,18 +541,19 @@ chunk_bwd_key_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
 
     CH_TRACE(1, 0);
     bool ok = (smem_u32(smem) & 1023u) == 0;
-    if (r == 0) {
+    if (t == 0) {
         mbar_init(full, 1);
         mbar_init(mbar, 1);
         fence_mbar_init();
     }
-    if (r < 32) {
+    if (t < 32) {
         tmem_alloc(slot, T::COLS);
         tmem_relinquish();
     }
+    if (h == 0)
 #pragma unroll
-    for (int cc = 0; cc < 64; cc += 8)
-        *reinterpret_cast<uint4 *>(ones + sw128_offset(r, cc)) = make_uint4(cc == 0 ? 0x3F803F80u : 0u, 0u, 0u, 0u);
+        for (int cc = 0; cc < 64; cc += 8)
+            *reinterpret_cast<uint4 *>(ones + sw128_offset(r, cc)) = make_uint4(cc == 0 ? 0x3F803F80u : 0u, 0u, 0u, 0u);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -537,9 +567,9 @@ chunk_bwd_key_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     constexpr uint32_t ID_P = idesc_bf16(128, 128, 0, 0);      // K-major A and B
     constexpr uint32_t ID_DV = idesc_bf16(128, M, 0, 1);       // P^T (TMEM) or phi(K) x MN-major
     constexpr uint32_t ID_DK = idesc_bf16(128, D, 0, 0);       // [V | 1 | V] x [R_hi | r | R_lo]^T, K-major
-    constexpr uint32_t ID_DK2 = idesc_bf16(128, D, 0, 1);      // A^T (TMEM) x phi(Q) MN-major
+    constexpr uint32_t ID_DK2 = idesc_bf16(128, D, 0, 1);      // A^T (TMEM) x psi(Q) MN-major
     auto mma_wait_all = [&]() {
-        if (r == 0) mma_commit(mbar);
+        if (t == 0) mma_commit(mbar);
         const bool got = mbar_wait_bounded(mbar, phase, now_ns() + kWaitNs, nullptr);
         if (got) phase ^= 1u;
         tc_fence_after();
@@ -551,7 +581,7 @@ chunk_bwd_key_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     const int bh = u / args.nch, c = u % args.nch;
     const int t0 = c * kC, valid = min(kC, args.N - t0);
     CH_TRACE(1, 2);
-    if (r == 0) {
+    if (t == 0) {
         mbar_arrive_expect_tx(full, 2 * C::TQ + 2 * C::TV);
 #pragma unroll
         for (int j = 0; j < D / 64; ++j) {
@@ -565,9 +595,9 @@ chunk_bwd_key_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         }
     }
     loading = true;
-    es[r] = r < valid ? __ldcg(args.ws_e + (size_t)bh * args.N + t0 + r) : 0.f;
+    if (h == 0) es[r] = r < valid ? __ldcg(args.ws_e + (size_t)bh * args.N + t0 + r) : 0.f;
     // [R_c hi | r_c | R_c lo]
-    load_sum_tile<D, M>(args.ws_r + (size_t)u * (D * M + D), snap, r);
+    load_sum_tile<D, M, kCT>(args.ws_r + (size_t)u * (D * M + D), snap, t);
     CH_TRACE(1, 3);
     {
         const bool landed = mbar_wait_bounded(full, fphase, now_ns() + kWaitNs, nullptr);
@@ -578,7 +608,7 @@ chunk_bwd_key_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         ok = __syncthreads_and(landed) != 0;
     }
     // the next chunk into L2 while this one computes
-    if (r == 0 && ok) {
+    if (t == 0 && ok) {
         const int un = u + gridDim.x;
         if (un < args.total) {
             const int bn = un / args.nch, tn = (un % args.nch) * kC;
@@ -596,19 +626,19 @@ chunk_bwd_key_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         }
     }
     CH_TRACE(1, 4);
-    // psi(Q) = phi(Q) - 1 (the 1 enters as the row sums of phi(K)); phi(K);
-    // rows past the end become zeros
+    // psi(Q) = phi(Q) - 1 (half 0; the 1 enters as the row sums of phi(K))
+    // and phi(K) (half 1); rows past the end become zeros
     float sk = 0.f;
     if (ok) {
-        psi_tile<D>(tq, r, valid);
-        phi_tile<D>(tk, r, valid);
+        if (h == 0) psi_tile<D>(tq, r, valid);
+        else phi_tile<D>(tk, r, valid);
         ok = operands_ready(true);
-        sk = row_sum<D>(tk, r);
+        if (h == 0) sk = row_sum<D>(tk, r);
     }
     CH_TRACE(1, 5);
     // ---- phi(K) psi(Q)^T;  A^T (raw) = V g^T
     if (ok) {
-        if (r == 0) {
+        if (t == 0) {
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks)
                 mma_f16_ss(tmem + T::K_PT, kmajor_base(smem_u32(tk)) + kmajor_step(ks),
@@ -623,20 +653,20 @@ chunk_bwd_key_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         pending = !ok;
     }
     CH_TRACE(1, 6);
-    // ---- P^T = phi(K) psi(Q)^T + sk and A^T + e_i, masked to r <= i < valid
-    // (key r, query i), as bf16 in place; the row sum of A^T (its product
-    // with the 1 of phi(Q) = psi(Q) + 1)
+    // ---- P^T = phi(K) psi(Q)^T + sk (half 0) and A^T + e_i (half 1), masked
+    // to r <= i < valid (key r, query i), as bf16 in place; the row sum of A^T
+    // (its product with the 1 of phi(Q) = psi(Q) + 1)
     float asum = 0.f;
     if (ok) {
         auto keep = [&](int i) { return i >= r && i < valid; };
-        tmem_mask_to_bf16<false>(trow + T::K_PT, trow + T::K_PT, 0u, keep, [&](int) { return sk; });
-        asum = tmem_mask_to_bf16<false>(trow + T::K_AT, trow + T::K_AT, 0u, keep, [&](int i) { return es[i]; });
+        if (h == 0) tmem_mask_to_bf16(trow + T::K_PT, trow + T::K_PT, 0, 128, keep, [&](int) { return sk; });
+        else asum = tmem_mask_to_bf16(trow + T::K_AT, trow + T::K_AT, 0, 128, keep, [&](int i) { return es[i]; });
         ok = operands_ready(true);
     }
     CH_TRACE(1, 7);
     // ---- dV = P^T g + phi(K) (R_hi + R_lo);  dphi(K) = A^T psi(Q) + [V | 1 | V] [R_hi | r | R_lo]^T
     if (ok) {
-        if (r == 0) {
+        if (t == 0) {
             const uint64_t dgb = smem_desc(smem_u32(tg), kC * 128, 1024);
 #pragma unroll
             for (int ks = 0; ks < kC / 16; ++ks)
@@ -669,21 +699,25 @@ chunk_bwd_key_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         pending = !ok;
     }
     CH_TRACE(1, 8);
-    // ---- dK = (dphi(K) + asum) min(phi(K), 1), dV
+    // ---- dK = (dphi(K) + asum) min(phi(K), 1) (half 1, which holds asum); dV (half 0)
     if (ok) {
-        float x[D > M ? D : M];
+        if (h == 1) {
+            float x[D];
 #pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 32) {
-            float d32[32], f[32];
-            tmem_ld32f(trow + T::K_DK + c0, d32);
-            load_row32(tk, r, c0, f);
+            for (int c0 = 0; c0 < D; c0 += 32) {
+                float d32[32], f[32];
+                tmem_ld32f(trow + T::K_DK + c0, d32);
+                load_row32(tk, r, c0, f);
 #pragma unroll
-            for (int j = 0; j < 32; ++j) x[c0 + j] = (d32[j] + asum) * fminf(f[j], 1.f);
+                for (int j = 0; j < 32; ++j) x[c0 + j] = (d32[j] + asum) * fminf(f[j], 1.f);
+            }
+            if (r < valid) store_row_bf16<D>(args.g0 + ((size_t)bh * args.N + t0 + r) * D, x);
+        } else {
+            float x[M];
+#pragma unroll
+            for (int c0 = 0; c0 < M; c0 += 32) tmem_ld32f(trow + T::K_DV + c0, *reinterpret_cast<float(*)[32]>(x + c0));
+            if (r < valid) store_row_bf16<M>(args.g1 + ((size_t)bh * args.N + t0 + r) * M, x);
         }
-        if (r < valid) store_row_bf16<D>(args.g0 + ((size_t)bh * args.N + t0 + r) * D, x);
-#pragma unroll
-        for (int c0 = 0; c0 < M; c0 += 32) tmem_ld32f(trow + T::K_DV + c0, *reinterpret_cast<float(*)[32]>(x + c0));
-        if (r < valid) store_row_bf16<M>(args.g1 + ((size_t)bh * args.N + t0 + r) * M, x);
     }
     // the chunk's tiles, tile of sums, e values and TMEM are free for the next one
     fence_proxy_async();
@@ -692,7 +726,7 @@ chunk_bwd_key_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     tc_fence_after();
     }
     CH_TRACE(1, 9);
-    if (!ok && r == 0) {
+    if (!ok && t == 0) {
         record_error(args.err, kErrTimeout);
         if (loading) mbar_wait_bounded(full, fphase, now_ns() + kWaitNs, nullptr);
         if (pending) mbar_wait_bounded(mbar, phase, now_ns() + kWaitNs, nullptr);
@@ -700,7 +734,7 @@ chunk_bwd_key_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if (r < 32) tmem_dealloc(tmem, T::COLS);
+    if (t < 32) tmem_dealloc(tmem, T::COLS);
     CH_TRACE(1, 10);
 }
 
@@ -748,7 +782,7 @@ cudaError_t launch_chunk_bwd(const BwdProblem &p, const DeviceInfo &dev) {
     // holds allow no more), each walking chunks in strides of the grid
     const long long total = p.BH * nch;
     if (total > INT32_MAX) return cudaErrorInvalidValue;
-    const dim3 grid((unsigned)std::min<long long>(total, std::max(1, dev.sm_count))), block(kNT);
+    const dim3 grid((unsigned)std::min<long long>(total, std::max(1, dev.sm_count))), block(kCT);
     ChunkBwdArgs a{ws_s, ws_r, ws_g, ws_e, (__nv_bfloat16 *)p.dq, nullptr, p.N, nch, (int)total, dev.err_word};
     if ((e = set_smem(chunk_bwd_query_kernel<D, M>, CQCfg<D, M>::SMEM)) != cudaSuccess) return e;
     e = launch_pdl(chunk_bwd_query_kernel<D, M>, grid, block, CQCfg<D, M>::SMEM, p.stream, 0u, tq, tk, tv, tg, a);

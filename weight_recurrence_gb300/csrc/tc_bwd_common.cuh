@@ -11,7 +11,7 @@
 namespace la {
 namespace tc {
 
-constexpr int kNT = 128;   // threads of the query and key kernels
+constexpr int kNT = 128;   // threads of the non-causal backward's kernels; one row of a 128-row tile each
 
 // Row-major operand [X_hi | w | X_lo] (X: rows x cols) in 64-column swizzled
 // atoms of `rows` rows each.
@@ -65,19 +65,19 @@ __device__ __forceinline__ void sum_partials_to_tile(const float *slots, int nsp
 
 // One fp32 slot [X (D x M) | w (D)] into the bf16 operand tile
 // [X_hi | w | X_lo], read with coalesced 16-byte loads, all in flight at
-// once: thread t of kNT takes float4 t, t + kNT, ... of X and entry t of w.
-template <int D, int M>
+// once: thread t of NT takes float4 t, t + NT, ... of X and entry t of w.
+template <int D, int M, int NT>
 __device__ __forceinline__ void load_sum_tile(const float *slot, uint8_t *tile, int t) {
-    constexpr int NF4 = D * M / 4 / kNT;
-    static_assert((D * M / 4) % kNT == 0 && D <= kNT, "whole float4 rounds");
+    constexpr int NF4 = D * M / 4 / NT;
+    static_assert((D * M / 4) % NT == 0 && D <= NT, "whole float4 rounds");
     const float4 *src = reinterpret_cast<const float4 *>(slot);
     float4 a[NF4];
 #pragma unroll
-    for (int i = 0; i < NF4; ++i) a[i] = __ldcg(src + i * kNT + t);
+    for (int i = 0; i < NF4; ++i) a[i] = __ldcg(src + i * NT + t);
     const float w = t < D ? __ldcg(slot + D * M + t) : 0.f;
 #pragma unroll
     for (int i = 0; i < NF4; ++i) {
-        const int e = 4 * (i * kNT + t);
+        const int e = 4 * (i * NT + t);
         const int row = e / M, col = e % M;
         const uint32_t off = (uint32_t)(col / 64) * D * 128 + sw128_offset(row, col % 64);
         const uint32_t h0 = pack_bf16x2(a[i].x, a[i].y), h1 = pack_bf16x2(a[i].z, a[i].w);
