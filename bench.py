@@ -531,10 +531,10 @@ def _leg_backward(torch, la, inputs, name, dev, stream, rot, pk, steps, max_over
                     if noncausal else
                     "tcgen05 kernels (bf16 D = M = 64): a forward sweep (dQ, keeps g and e) and a reverse "
                     "sweep (dK, dV), one CTA per head each" if w.D == 64 and w.M == 64 else
-                    "tcgen05 kernels, chunk-parallel (bf16 D, M in {64, 128}): per-chunk key sums, an exclusive "
-                    "scan into each chunk's entering state, a query pass (dQ, g, e, per-chunk phi(Q)^T [g | e]), "
-                    "the reverse scan, a key pass (dK, dV), one CTA per 128-row chunk; the per-chunk fp32 sums "
-                    "(D*M + D floats per chunk) move through HBM five times")}
+                    "tcgen05 kernels, segmented (bf16 D, M in {64, 128}): segment key sums, an exclusive scan "
+                    "into each segment's entering state, a query pass (dQ, g, e; S in TMEM along the segment), the "
+                    "reverse scan, a key pass (dK, dV; R in TMEM), one CTA per segment of consecutive chunks (about "
+                    "one per SM); K and V are read a second time by the segment key sums")}
     del q, k, v, G, dq, dk, dv, sets
     torch.cuda.empty_cache()
     return leg

@@ -178,15 +178,16 @@ la_status la_decode_steps(const void *q, const void *k, const void *v, void *y, 
  *      not wanted).  Chaining the backward of consecutive segments through
  *      dS0 -> dSN reproduces the backward of the whole sequence.
  *   workspace: la_workspace_bytes(LA_OP_CAUSAL_BWD, s, 0) bytes: g and e of
- *      every token, and (chunk-parallel route) the fp32 sums [S | Z] and
- *      [R | r] entering every 128-row chunk, D*M + D floats each.
+ *      every token, and (segmented route) the fp32 sums [S | Z] and [R | r]
+ *      entering and leaving every segment, D*M + D floats each.
  * bf16 runs on tensor cores (tcgen05: bf16 operands, the state and the
  * reverse sums entering the products as bf16 hi + lo pairs, fp32
  * accumulation): with D = M = 64 in two sweeps of one CTA per head; with
- * D, M in {64, 128} otherwise chunk-parallel in five launches (per-chunk key
- * sums, a scan into each chunk's entering state, a query pass, the reverse
- * scan, a key pass; one CTA per chunk).  fp32, and bf16 at other sizes, run
- * fp32 arithmetic on CUDA cores.  Errors as la_forward_causal.
+ * D, M in {64, 128} otherwise in segments of consecutive 128-row chunks,
+ * about one CTA per SM, the state held in TMEM along each segment (segment
+ * key sums, a scan, a query pass, the reverse scan, a key pass).  fp32, and
+ * bf16 at other sizes, run fp32 arithmetic on CUDA cores.  Errors as
+ * la_forward_causal.
  */
 la_status la_backward_causal(const void *q, const void *k, const void *v, const void *dout,
                              void *dq, void *dk, void *dv, la_shape s,

@@ -774,11 +774,13 @@ seg_bwd_key_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         }
     }
     loading = true;
-    if (h == 0) es[r] = r < valid ? __ldcg(args.ws_e + (size_t)bh * args.N + t0 + r) : 0.f;
+    // e of the chunk's rows (the load is in flight during the operand tile)
+    const float ev = (h == 0 && r < valid) ? __ldcg(args.ws_e + (size_t)bh * args.N + t0 + r) : 0.f;
     // [R_c hi | R_c lo] from the TMEM sums plus the column sums of g
     if (r < D)
 #pragma unroll 1
         for (int c0 = MH * h; c0 < MH * h + MH; c0 += 32) snap_from_tmem<D, M>(trow, T::K_R, r, c0, cg, snap);
+    if (h == 0) es[r] = ev;
     CH_TRACE(1, 3);
     {
         const bool landed = mbar_wait_bounded(full, fphase, now_ns() + kWaitNs, nullptr);
