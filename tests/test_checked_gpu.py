@@ -144,6 +144,30 @@ def test_release_build_ignores_the_hook():
     assert np.isfinite(out.float().cpu().numpy()).all()
 
 
+@pytest.mark.parametrize("D,M", [(64, 128), (128, 128)])
+def test_segmented_causal_backward_is_clean_and_exact(D, M):
+    """The segmented tensor-core causal backward (segment key sums, scans, query
+    and key passes) through the checked build, with a carried-in state and a
+    final-state gradient: no check fires and the results are the oracle's."""
+    B, H, N = 1, 2, 1500   # one head cut into several segments
+    qh, kh, vh = inputs.qkv(B, H, N, D, M, torch.bfloat16, 0.125, seed=41)
+    G = torch.randn((B, H, N, M), generator=torch.Generator().manual_seed(42)).to(torch.bfloat16)
+    S0, z0 = inputs.state(B, H, D, M, seed=43, scale=0.05)
+    dSN, dzN = inputs.state(B, H, D, M, seed=44, scale=0.001)
+    dS0 = torch.empty(B, H, D, M, device=DEV)
+    dz0 = torch.empty(B, H, D, device=DEV)
+    got = la.la_backward_causal(qh.to(DEV), kh.to(DEV), vh.to(DEV), G.to(DEV), S0=S0.to(DEV), z0=z0.to(DEV),
+                                dSN=dSN.to(DEV), dzN=dzN.to(DEV), dS0=dS0, dz0=dz0)
+    assert _err() == la.LA_OK
+    ref = oracle.causal_backward(qh, kh, vh, G, S0=S0, z0=z0, dSN=dSN, dzN=dzN)
+    for g, r in zip(got, ref[:3]):
+        y = g.float().cpu().numpy().astype(np.float64).reshape(B * H, -1)
+        rr = np.asarray(r, np.float64).reshape(B * H, -1)
+        den = np.maximum(np.abs(rr).max(axis=-1), 1e-3 * float(G.float().abs().max()))
+        assert float((np.abs(y - rr).max(axis=-1) / den).max()) <= 2e-2
+    assert head_rel_err(dS0.cpu(), ref[3]) <= 2e-2 and head_rel_err(dz0.cpu(), ref[4]) <= 2e-2
+
+
 @pytest.mark.parametrize("D,M", [(64, 64), (128, 128)])
 def test_noncausal_backward_is_clean_and_exact(D, M):
     """The tensor-core non-causal backward (key sums, query and key passes) through the checked build."""
