@@ -1,4 +1,4 @@
-"""Seeded random shapes through the forward entry points, against the fp64 oracle.
+"""Seeded random shapes through the forward and backward entry points, against the fp64 oracle.
 
 The other GPU tests pick their shapes by hand (chunk edges, ragged tails,
 segment splits, full-size workloads).  Here a fixed seed draws batch, heads,
@@ -88,3 +88,71 @@ def test_decode_random_shapes(i):
         assert row_rel_err(y, yr) <= tol_for(dtype), (B, H, D, M, dtype, t)
     assert la.la_get_last_error() == la.LA_OK
     assert head_rel_err(S, Sr) <= tol_for(dtype) and head_rel_err(z, zr) <= tol_for(dtype)
+
+
+def _draw_bwd(i):
+    """Backward case i: as _draw, with the tensor-core sizes (bf16, D, M in
+    {64, 128}) half of the time and long sequences (up to 1500 rows, several
+    chunks) more often."""
+    rng = np.random.default_rng(9100 + i)
+    B, H = int(rng.integers(1, 4)), int(rng.integers(1, 5))
+    N = int(rng.choice([1, int(rng.integers(2, 129)), int(rng.integers(129, 1501)), int(rng.integers(129, 1501))]))
+    if rng.random() < 0.5:
+        dtype, D, M = torch.bfloat16, int(rng.choice((64, 128))), int(rng.choice((64, 128)))
+    else:
+        dtype = torch.bfloat16 if rng.random() < 0.5 else torch.float32
+        D, M = int(rng.choice(SIZES)), int(rng.choice(SIZES))
+    scale = float(rng.choice([0.125, 0.5, 1.0])) / (1.0 if D <= 64 else 2.0)
+    carry = bool(rng.random() < 0.5)
+    return B, H, N, D, M, dtype, scale, carry
+
+
+def _grad_err(y, r, G):
+    """Per head: max |y - r| / max(max |r|, 1e-3 max |dout|) (the backward tests' measure)."""
+    y = y.detach().float().cpu().numpy().astype(np.float64)
+    r = np.asarray(r, np.float64)
+    lead = y.shape[:2]
+    y, r = y.reshape(lead + (-1,)), r.reshape(lead + (-1,))
+    g = np.abs(G.float().numpy().astype(np.float64)).reshape(lead + (-1,)).max(axis=-1)
+    den = np.maximum(np.abs(r).max(axis=-1), 1e-3 * g)
+    den = np.where(den == 0, 1.0, den)
+    return float((np.abs(y - r).max(axis=-1) / den).max())
+
+
+@pytest.mark.parametrize("i", CASES[:24])
+def test_causal_backward_random_shapes(i):
+    """Random shapes through la_backward_causal (the two-sweep, segmented and CUDA-core routes), with a
+    carried-in state and a final-state gradient half of the time."""
+    B, H, N, D, M, dtype, scale, carry = _draw_bwd(i)
+    q, k, v = inputs.qkv(B, H, N, D, M, dtype, scale, seed=7500 + i)
+    G = torch.randn((B, H, N, M), generator=torch.Generator().manual_seed(7600 + i)).to(dtype)
+    if carry:
+        S0, z0 = inputs.state(B, H, D, M, seed=7700 + i, scale=0.05)
+        dSN, dzN = inputs.state(B, H, D, M, seed=7800 + i, scale=0.001)
+        dS0 = torch.empty(B, H, D, M, device=DEV)
+        dz0 = torch.empty(B, H, D, device=DEV)
+        got = la.la_backward_causal(q.to(DEV), k.to(DEV), v.to(DEV), G.to(DEV), S0=S0.to(DEV), z0=z0.to(DEV),
+                                    dSN=dSN.to(DEV), dzN=dzN.to(DEV), dS0=dS0, dz0=dz0)
+        ref = oracle.causal_backward(q, k, v, G, S0=S0, z0=z0, dSN=dSN, dzN=dzN)
+    else:
+        got = la.la_backward_causal(q.to(DEV), k.to(DEV), v.to(DEV), G.to(DEV))
+        ref = oracle.causal_backward(q, k, v, G)
+    torch.cuda.synchronize()
+    assert la.la_get_last_error() == la.LA_OK
+    tol = tol_for(dtype)
+    for name, g, r in zip(("dq", "dk", "dv"), got, ref[:3]):
+        assert _grad_err(g, r, G) <= tol, (name, B, H, N, D, M, dtype, carry)
+    if carry:
+        assert head_rel_err(dS0.cpu(), ref[3]) <= 2e-2 and head_rel_err(dz0.cpu(), ref[4]) <= 2e-2
+
+
+@pytest.mark.parametrize("i", CASES[:16])
+def test_noncausal_backward_random_shapes(i):
+    B, H, N, D, M, dtype, scale, _ = _draw_bwd(100 + i)
+    q, k, v = inputs.qkv(B, H, N, D, M, dtype, scale, seed=7900 + i)
+    G = torch.randn((B, H, N, M), generator=torch.Generator().manual_seed(8000 + i)).to(dtype)
+    got = la.la_backward_noncausal(q.to(DEV), k.to(DEV), v.to(DEV), G.to(DEV))
+    torch.cuda.synchronize()
+    assert la.la_get_last_error() == la.LA_OK
+    for name, g, r in zip(("dq", "dk", "dv"), got, oracle.noncausal_backward(q, k, v, G)):
+        assert _grad_err(g, r, G) <= tol_for(dtype), (name, B, H, N, D, M, dtype)
