@@ -87,9 +87,9 @@ struct QCfg {
 };
 
 template <int D, int M>
-__global__ void __launch_bounds__(kNT)
+__global__ void __launch_bounds__(kNT, 1)
 nc_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_g,
-                    const NcBwdArgs args)
+                    const __grid_constant__ CUtensorMap tm_dq, const NcBwdArgs args)
 {
     using C = QCfg<D, M>;
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -156,7 +156,10 @@ nc_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
         const int valid = min(kC, args.N - t0);
         uint8_t *tq = smem + s * C::STAGE, *tg = tq + C::TQ;
         NCB_TRACE(it, 0);
-        if (r == 0 && it + 1 < n) load_chunk(it + 1);   // into the stage released at the end of it - 1
+        if (r == 0 && it + 1 < n) {
+            tma_store_wait_read0();   // chunk it - 1's dQ store has read the stage
+            load_chunk(it + 1);       // into the stage released at the end of it - 1
+        }
         const bool landed = mbar_wait_bounded(&full[s], (it >> 1) & 1, now_ns() + kWaitNs, nullptr);
         if (!(ok = __syncthreads_and(landed) != 0)) {
             if (r == 0) record_error(args.err, kErrTimeout);
@@ -239,21 +242,26 @@ nc_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             break;
         }
         NCB_TRACE(it, 5);
-        // ---- dQ = dphi(Q) min(phi(Q), 1)
-        {
-            float x[D];
+        // ---- dQ = dphi(Q) min(phi(Q), 1), over phi(Q) in its tile (each thread
+        // reads its row's values before writing them), then stored by TMA (rows
+        // past the end are not written)
 #pragma unroll
-            for (int c0 = 0; c0 < D; c0 += 32) {
-                float d32[32], f[32];
-                tmem_ld32f(trow + C::COL_DQ + c0, d32);
-                load_row32(tq, r, c0, f);
+        for (int c0 = 0; c0 < D; c0 += 32) {
+            float d32[32], f[32];
+            tmem_ld32f(trow + C::COL_DQ + c0, d32);
+            load_row32(tq, r, c0, f);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) x[c0 + j] = d32[j] * fminf(f[j], 1.f);
-            }
-            if (r < valid) store_row_bf16<D>(args.g0 + ((size_t)bh * args.N + t0 + r) * D, x);
+            for (int j = 0; j < 32; ++j) f[j] = d32[j] * fminf(f[j], 1.f);
+            store_snap32<kC>(tq, r, c0, f);
         }
         NCB_TRACE(it, 6);
-        __syncthreads();   // the stage is free for the load two chunks on
+        fence_proxy_async();
+        __syncthreads();   // the stage is free for the load two chunks on, once the store has read it
+        if (r == 0) {
+#pragma unroll
+            for (int j = 0; j < D / 64; ++j) tma_store_3d(&tm_dq, tq + j * kC * 128, j * 64, t0, bh);
+            tma_store_commit();
+        }
     }
     // [dS | dz] partial of this query range (zero for an empty range)
     if (ok && r < D && ws_ok) {
@@ -279,6 +287,7 @@ nc_bwd_query_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_const
             mbar_wait_bounded(&full[c & 1], (c >> 1) & 1, now_ns() + kWaitNs, nullptr);
         if (mma_pending) mbar_wait_bounded(mbar, phase, now_ns() + kWaitNs, nullptr);
     }
+    if (r == 0) tma_store_wait_all0();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -300,9 +309,10 @@ struct KCfg {
 };
 
 template <int D, int M>
-__global__ void __launch_bounds__(kNT)
+__global__ void __launch_bounds__(kNT, 1)
 nc_bwd_key_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                  const NcBwdArgs args)
+                  const __grid_constant__ CUtensorMap tm_dk,
+                  const __grid_constant__ CUtensorMap tm_dv, const NcBwdArgs args)
 {
     using C = KCfg<D, M>;
     extern __shared__ __align__(1024) uint8_t smem[];
@@ -368,7 +378,10 @@ nc_bwd_key_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
         const int s = it & 1, t0 = (c_begin + it) * kC;
         const int valid = min(kC, args.N - t0);
         uint8_t *tk = smem + s * C::STAGE, *tv = tk + C::TK;
-        if (r == 0 && it + 1 < n) load_chunk(it + 1);
+        if (r == 0 && it + 1 < n) {
+            tma_store_wait_read0();   // chunk it - 1's dK, dV stores have read the stage
+            load_chunk(it + 1);
+        }
         const bool landed = mbar_wait_bounded(&full[s], (it >> 1) & 1, now_ns() + kWaitNs, nullptr);
         if (!(ok = __syncthreads_and(landed) != 0)) {
             if (r == 0) record_error(args.err, kErrTimeout);
@@ -402,23 +415,33 @@ nc_bwd_key_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             mma_pending = true;
             break;
         }
-        // ---- dK = dphi(K) min(phi(K), 1), dV
-        {
-            float x[D > M ? D : M];
+        // ---- dK = dphi(K) min(phi(K), 1) over phi(K) in its tile, dV over V in
+        // its tile (last read by the products just completed); then stored by
+        // TMA (rows past the end are not written)
 #pragma unroll
-            for (int c0 = 0; c0 < D; c0 += 32) {
-                float d32[32], f[32];
-                tmem_ld32f(trow + C::COL_DK + c0, d32);
-                load_row32(tk, r, c0, f);
+        for (int c0 = 0; c0 < D; c0 += 32) {
+            float d32[32], f[32];
+            tmem_ld32f(trow + C::COL_DK + c0, d32);
+            load_row32(tk, r, c0, f);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) x[c0 + j] = d32[j] * fminf(f[j], 1.f);
-            }
-            if (r < valid) store_row_bf16<D>(args.g0 + ((size_t)bh * args.N + t0 + r) * D, x);
-#pragma unroll
-            for (int c0 = 0; c0 < M; c0 += 32) tmem_ld32f(trow + C::COL_DV + c0, *reinterpret_cast<float(*)[32]>(x + c0));
-            if (r < valid) store_row_bf16<M>(args.g1 + ((size_t)bh * args.N + t0 + r) * M, x);
+            for (int j = 0; j < 32; ++j) f[j] = d32[j] * fminf(f[j], 1.f);
+            store_snap32<kC>(tk, r, c0, f);
         }
-        __syncthreads();
+#pragma unroll
+        for (int c0 = 0; c0 < M; c0 += 32) {
+            float x[32];
+            tmem_ld32f(trow + C::COL_DV + c0, x);
+            store_snap32<kC>(tv, r, c0, x);
+        }
+        fence_proxy_async();
+        __syncthreads();   // the stage is free for the load two chunks on, once the stores have read it
+        if (r == 0) {
+#pragma unroll
+            for (int j = 0; j < D / 64; ++j) tma_store_3d(&tm_dk, tk + j * kC * 128, j * 64, t0, bh);
+#pragma unroll
+            for (int j = 0; j < M / 64; ++j) tma_store_3d(&tm_dv, tv + j * kC * 128, j * 64, t0, bh);
+            tma_store_commit();
+        }
     }
     if (!ok && r == 0) {
         record_error(args.err, kErrTimeout);
@@ -426,6 +449,7 @@ nc_bwd_key_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constan
             mbar_wait_bounded(&full[c & 1], (c >> 1) & 1, now_ns() + kWaitNs, nullptr);
         if (mma_pending) mbar_wait_bounded(mbar, phase, now_ns() + kWaitNs, nullptr);
     }
+    if (r == 0) tma_store_wait_all0();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -453,9 +477,11 @@ cudaError_t launch_nc_bwd(const BwdProblem &p, const DeviceInfo &dev) {
     const size_t part = (size_t)p.BH * nsplit * (D * M + D) * sizeof(float);
     if (p.ws_bytes < 2 * part) return cudaErrorInvalidValue;
     float *ws_s = (float *)p.ws, *ws_r = ws_s + part / sizeof(float);
-    CUtensorMap tq, tg, tk, tv;
+    CUtensorMap tq, tg, tk, tv, tdq, tdk, tdv;
     if (!cached_tmap_bf16_3d(&tq, p.q, D, p.N, p.BH, 64, kC) || !cached_tmap_bf16_3d(&tg, p.dout, M, p.N, p.BH, 64, kC) ||
-        !cached_tmap_bf16_3d(&tk, p.k, D, p.N, p.BH, 64, kC) || !cached_tmap_bf16_3d(&tv, p.v, M, p.N, p.BH, 64, kC))
+        !cached_tmap_bf16_3d(&tk, p.k, D, p.N, p.BH, 64, kC) || !cached_tmap_bf16_3d(&tv, p.v, M, p.N, p.BH, 64, kC) ||
+        !cached_tmap_bf16_3d(&tdq, p.dq, D, p.N, p.BH, 64, kC) || !cached_tmap_bf16_3d(&tdk, p.dk, D, p.N, p.BH, 64, kC) ||
+        !cached_tmap_bf16_3d(&tdv, p.dv, M, p.N, p.BH, 64, kC))
         return cudaErrorInvalidValue;
     cudaError_t e = tc_key_sums(p.k, p.v, p.BH, p.N, D, M, nsplit, cps, ws_s, part, p.stream, dev);
     if (e != cudaSuccess) return e;
@@ -463,13 +489,13 @@ cudaError_t launch_nc_bwd(const BwdProblem &p, const DeviceInfo &dev) {
     const long long part_floats = (long long)(part / sizeof(float));
     NcBwdArgs qa{ws_s, ws_r, (__nv_bfloat16 *)p.dq, nullptr, p.N, nsplit, cps, dev.err_word, part_floats};
     if ((e = set_smem(nc_bwd_query_kernel<D, M>, QCfg<D, M>::SMEM)) != cudaSuccess) return e;
-    e = launch_pdl(nc_bwd_query_kernel<D, M>, grid, block, QCfg<D, M>::SMEM, p.stream, 0u, tq, tg, qa);
+    e = launch_pdl(nc_bwd_query_kernel<D, M>, grid, block, QCfg<D, M>::SMEM, p.stream, 0u, tq, tg, tdq, qa);
     count_launches(1);
     if (e != cudaSuccess) return e;
     NcBwdArgs ka{ws_r, nullptr, (__nv_bfloat16 *)p.dk, (__nv_bfloat16 *)p.dv, p.N, nsplit, cps, dev.err_word,
                  part_floats};
     if ((e = set_smem(nc_bwd_key_kernel<D, M>, KCfg<D, M>::SMEM)) != cudaSuccess) return e;
-    e = launch_pdl(nc_bwd_key_kernel<D, M>, grid, block, KCfg<D, M>::SMEM, p.stream, 0u, tk, tv, ka);
+    e = launch_pdl(nc_bwd_key_kernel<D, M>, grid, block, KCfg<D, M>::SMEM, p.stream, 0u, tk, tv, tdk, tdv, ka);
     count_launches(1);
     return e;
 }

@@ -63,39 +63,6 @@ __device__ __forceinline__ void sum_partials_to_tile(const float *slots, int nsp
         *reinterpret_cast<uint4 *>(wa + sw128_offset(r, c)) = make_uint4(c == 0 ? hl : 0u, c == 0 ? hl : 0u, 0u, 0u);
 }
 
-// One fp32 slot [X (D x M) | w (D)] into the bf16 operand tile
-// [X_hi | w | X_lo], read with coalesced 16-byte loads, all in flight at
-// once: thread t of NT takes float4 t, t + NT, ... of X and entry t of w.
-template <int D, int M, int NT>
-__device__ __forceinline__ void load_sum_tile(const float *slot, uint8_t *tile, int t) {
-    constexpr int NF4 = D * M / 4 / NT;
-    static_assert((D * M / 4) % NT == 0 && D <= NT, "whole float4 rounds");
-    const float4 *src = reinterpret_cast<const float4 *>(slot);
-    float4 a[NF4];
-#pragma unroll
-    for (int i = 0; i < NF4; ++i) a[i] = __ldcg(src + i * NT + t);
-    const float w = t < D ? __ldcg(slot + D * M + t) : 0.f;
-#pragma unroll
-    for (int i = 0; i < NF4; ++i) {
-        const int e = 4 * (i * NT + t);
-        const int row = e / M, col = e % M;
-        const uint32_t off = (uint32_t)(col / 64) * D * 128 + sw128_offset(row, col % 64);
-        const uint32_t h0 = pack_bf16x2(a[i].x, a[i].y), h1 = pack_bf16x2(a[i].z, a[i].w);
-        const uint32_t l0 = pack_bf16x2(a[i].x - bf16lo(h0), a[i].y - bf16hi(h0));
-        const uint32_t l1 = pack_bf16x2(a[i].z - bf16lo(h1), a[i].w - bf16hi(h1));
-        *reinterpret_cast<uint2 *>(tile + off) = make_uint2(h0, h1);
-        *reinterpret_cast<uint2 *>(tile + XwTile<D, M>::LO + off) = make_uint2(l0, l1);
-    }
-    if (t < D) {
-        const float hi = __bfloat162float(__float2bfloat16_rn(w));
-        const uint32_t hl = pack_bf16x2(hi, w - hi);
-        uint8_t *wa = tile + XwTile<D, M>::W_ATOM;
-#pragma unroll
-        for (int c = 0; c < 64; c += 8)
-            *reinterpret_cast<uint4 *>(wa + sw128_offset(t, c)) = make_uint4(c == 0 ? hl : 0u, c == 0 ? hl : 0u, 0u, 0u);
-    }
-}
-
 // Row r of a bf16 result (n columns, fp32 in x) to global memory: 256-bit
 // stores when the row start allows, else 128-bit.
 template <int NCOL>
