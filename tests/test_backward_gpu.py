@@ -127,6 +127,29 @@ def test_causal_backward_with_state(dtype, D, M):
     assert head_rel_err(dz0.cpu(), rz) <= (2e-2 if tc else 1e-4)
 
 
+@pytest.mark.parametrize("B,H,N,D,M", [(16, 4, 2000, 128, 128),    # two segments of eight chunks per head
+                                       (16, 8, 1000, 64, 128)])    # one segment per head
+def test_segmented_backward_with_state_many_heads(B, H, N, D, M):
+    """Carried-in state and final-state gradient on the segmented route with
+    several chunks per segment (the state carried along the segment in TMEM)
+    and with one segment per head (no segment key sums: the scan only copies
+    the carried-in state)."""
+    dtype = torch.bfloat16
+    q, k, v = inputs.qkv(B, H, N, D, M, dtype, 0.125, seed=905)
+    G = _dout(B, H, N, M, dtype, 906)
+    S0, z0 = inputs.state(B, H, D, M, seed=907, scale=0.05)
+    dSN, dzN = inputs.state(B, H, D, M, seed=908, scale=0.001)
+    rq, rk, rv, rS, rz = oracle.causal_backward(q, k, v, G, S0=S0, z0=z0, dSN=dSN, dzN=dzN)
+    dS0 = torch.empty(B, H, D, M, device=DEV)
+    dz0 = torch.empty(B, H, D, device=DEV)
+    qd, kd, vd, Gd, S0d, z0d, dSNd, dzNd = _dev(q, k, v, G, S0, z0, dSN, dzN)
+    got = la.la_backward_causal(qd, kd, vd, Gd, S0=S0d, z0=z0d, dSN=dSNd, dzN=dzNd, dS0=dS0, dz0=dz0)
+    torch.cuda.synchronize()
+    assert la.la_get_last_error() == la.LA_OK
+    _check_grads(got, (rq, rk, rv), dtype, G, "segmented state")
+    assert head_rel_err(dS0.cpu(), rS) <= 2e-2 and head_rel_err(dz0.cpu(), rz) <= 2e-2
+
+
 @pytest.mark.parametrize("dtype,D,M", [(torch.float32, 64, 64), (torch.bfloat16, 64, 64),
                                        (torch.bfloat16, 128, 128)])
 def test_causal_backward_split_chains(dtype, D, M):
