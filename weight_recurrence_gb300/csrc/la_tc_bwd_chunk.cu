@@ -124,7 +124,7 @@ struct SegBwdArgs {
     __nv_bfloat16 *ws_g;     // [BH, N, M]: g (query pass writes it)
     float *ws_e;             // [BH, N]: e
     __nv_bfloat16 *g0, *g1;  // query pass: dQ; key pass: dK, dV
-    int N, nch, nseg, L;     // chunks per head, segments per head, chunks per segment (the last may be shorter)
+    int N, nch, nseg, L;     // rows and chunks per head, segments per head, chunks per segment (the last may be shorter)
     int *err;
 };
 
@@ -154,8 +154,9 @@ struct SegCols {
 };
 
 // Operand tile of a D x M fp32 sum as bf16 [X_hi | X_lo], each part M/64
-// swizzled atoms of D rows; read MN-major ([x] as B of phi x X) and K-major
-// (as B of g X^T).  Also the fp32 staging area of a D x M block.
+// swizzled atoms of D rows; read MN-major (as the B operand of phi X) and
+// K-major (as the B operand of g X^T).  Also the fp32 staging area of a
+// D x M block.
 template <int D, int M>
 struct SnapTile {
     static constexpr int ATOM = D * 128;
@@ -164,7 +165,7 @@ struct SnapTile {
     static_assert(D * M * 4 <= BYTES, "staging area");
 };
 
-// Columns [c_begin, c_begin + 32) of row r of the fp32 state in TMEM at
+// Columns [c0, c0 + 32) of row r of the fp32 state in TMEM at
 // `col`, plus the column sums `cs` not held there, into the bf16 hi and lo
 // parts of the operand tile.
 template <int D, int M>
