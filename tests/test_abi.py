@@ -233,3 +233,26 @@ def test_checked_build_exports_the_same_abi(lib):
     finally:
         la.select_library(False)
     assert not la.la_checked_build()
+
+
+@pytest.mark.parametrize("B,H,N,D,M", [(1, 16, 65536, 128, 128), (16, 8, 3072, 128, 128), (1, 1, 4097, 128, 64),
+                                       (64, 4, 700, 64, 128), (300, 1, 128, 128, 128)])
+def test_segmented_backward_workspace(lib, B, H, N, D, M):
+    """bf16 causal backward at D, M in {64, 128} (not 64/64) takes the segmented
+    route: its workspace holds g (bf16) and e of every token, and two fp32
+    [S | z] slots per segment for the most segments any device picks (up to
+    192 SMs: one CTA per SM, at least one segment per head, at most one per
+    128-row chunk), each part on a 256-byte boundary."""
+    def up(b):
+        return (b + 255) // 256 * 256
+    sh = _shape(B=B, H=H, N=N, D=D, M=M, dt=la.LA_DTYPE_BF16)
+    BH, nch = B * H, (N + 127) // 128
+    nseg = max(1, min(nch, 192 // BH))
+    L = (nch + nseg - 1) // nseg
+    nseg = (nch + L - 1) // L
+    seg = 2 * up(BH * nseg * (D * M + D) * 4) + up(BH * N * M * 2) + BH * N * 4
+    # the CUDA-core route's need is the floor (the two share the call's workspace)
+    assert la.la_workspace_bytes(la.LA_OP_CAUSAL_BWD, sh) >= seg
+    # fp32 at the same sizes runs on CUDA cores: g and e per token, two segment sums
+    fp = la.la_workspace_bytes(la.LA_OP_CAUSAL_BWD, _shape(B=B, H=H, N=N, D=D, M=M))
+    assert fp >= BH * N * (M + 1) * 4
